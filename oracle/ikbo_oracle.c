@@ -1,0 +1,305 @@
+/*
+ * ikbo_oracle.c -- CPU oracle for the In-Kernel Broadcast Optimization (IKBO)
+ * hot path.  TEST INFRASTRUCTURE ONLY: the tests, the smoke check and the
+ * benchmark's CPU-baseline leg call it; no product code path may.
+ *
+ * It computes, plainly and slowly, in double precision, what the IKBO kernels
+ * compute quickly: the MATERIALISED-broadcast definition.  IKBO's claim is that
+ * it reaches the same result without ever building the replicated user tensor;
+ * this file builds it, on purpose, so that nothing here resembles the GPU path.
+ *
+ * Sources (the IKBO write-ups):
+ *   - "IKBO: recsys kernel optimization" (aixai.ru blog), section "Что такое
+ *     broadcast-проблема": user features are the same for all candidates of a
+ *     request and are replicated ~70x to match the candidate batch.
+ *   - same page, "Deep Dive: Linear Compression": LCE is one batched matmul of
+ *     the (replicated) input embeddings with a learned projection W; stage 1
+ *     splits it by linearity into a user part and a candidate part.
+ *   - "Meta Optimizes Inference for Recommendation Systems" (aibriefing), LCE
+ *     deep dive: the split is along the K axis.
+ *   - aixai.ru, "Deep Dive: Flash Attention": IKBO attention is ordinary
+ *     attention whose K/V come from the candidate's user; nothing changes in
+ *     the result, only in how K/V are fetched.
+ *
+ * Readings taken where the pages are silent (each repeated at its function):
+ *   - LCE orientation: X[i] is [K, D] (K embeddings of width D), W is [K, N],
+ *     Y[i] = W^T X[i] is [N, D]; user rows come first along K.
+ *   - LCE bias b[N] is added once per output element, broadcast over D.
+ *   - Attention: scale 1/sqrt(d) unless the caller passes another, no mask,
+ *     heads independent; an empty key range gives output 0.
+ *   - Segments: stable counting sort (ascending candidate index within a
+ *     user); work units ordered by user, then head, then chunk.
+ *
+ * All inputs arrive as bf16 bit patterns (uint16) and are widened to double
+ * exactly; every sum is formed in double in ascending index order.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORACLE_OK 0
+#define ORACLE_BAD_ARG 1
+#define ORACLE_MAP_OUT_OF_RANGE 2
+#define ORACLE_NO_MEMORY 3
+#define ORACLE_WORK_OVERFLOW 4
+
+/* Exact widening of a bf16 bit pattern: its bits are the top half of a float. */
+static double bf16_bits_to_double(uint16_t h)
+{
+    uint32_t bits = ((uint32_t)h) << 16;
+    float f;
+    memcpy(&f, &bits, sizeof f);
+    return (double)f;
+}
+
+static void set_threads(int n_threads)
+{
+#ifdef _OPENMP
+    if (n_threads > 0) omp_set_num_threads(n_threads);
+#else
+    (void)n_threads;
+#endif
+}
+
+int ikbo_oracle_max_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/*
+ * Segments: counts[u] = #{i : map[i] = u}; offsets = exclusive prefix sum of
+ * counts (offsets[n_users] = n_cand); perm lists the candidates grouped by
+ * user, keeping ascending candidate order inside a user.  The attention work
+ * list follows: for each user u, each head h, each run of at most
+ * `cands_per_unit` consecutive entries of u's segment, one unit
+ * (u, h, first position in perm, count).
+ *
+ * Grouping a user's candidates is what lets their K/V be fetched once ("K/V
+ * accesses amortised across candidates sharing one user", aixai.ru, "Deep
+ * Dive: Flash Attention").
+ */
+int ikbo_oracle_segments(const int32_t *map, int n_cand, int n_users, int H, int cands_per_unit,
+                         int32_t *counts, int32_t *offsets, int32_t *perm,
+                         int32_t *work, int64_t max_units, int64_t *n_units)
+{
+    if (n_cand < 0 || n_users < 1 || H < 1 || cands_per_unit < 1) return ORACLE_BAD_ARG;
+    for (int i = 0; i < n_cand; ++i)
+        if (map[i] < 0 || map[i] >= n_users) return ORACLE_MAP_OUT_OF_RANGE;
+
+    for (int u = 0; u < n_users; ++u) counts[u] = 0;
+    for (int i = 0; i < n_cand; ++i) counts[map[i]] += 1;
+
+    offsets[0] = 0;
+    for (int u = 0; u < n_users; ++u) offsets[u + 1] = offsets[u] + counts[u];
+
+    int32_t *next = (int32_t *)malloc(sizeof(int32_t) * (size_t)n_users);
+    if (!next) return ORACLE_NO_MEMORY;
+    for (int u = 0; u < n_users; ++u) next[u] = offsets[u];
+    for (int i = 0; i < n_cand; ++i) {       /* ascending i: stable */
+        int u = map[i];
+        perm[next[u]] = i;
+        next[u] += 1;
+    }
+    free(next);
+
+    int64_t k = 0;
+    for (int u = 0; u < n_users; ++u) {
+        for (int h = 0; h < H; ++h) {
+            for (int c = 0; c < counts[u]; c += cands_per_unit) {
+                if (k >= max_units) return ORACLE_WORK_OVERFLOW;
+                int cnt = counts[u] - c;
+                if (cnt > cands_per_unit) cnt = cands_per_unit;
+                work[4 * k + 0] = u;
+                work[4 * k + 1] = h;
+                work[4 * k + 2] = offsets[u] + c;
+                work[4 * k + 3] = cnt;
+                k += 1;
+            }
+        }
+    }
+    *n_units = k;
+    return ORACLE_OK;
+}
+
+/*
+ * Linear Compression Embedding, materialised form.
+ *
+ * For candidate i with user u = map[i]:
+ *   X[i] = [ U[u] ; C[i] ]              ((K_u + K_c) x D, the replicated input)
+ *   W    = [ W_u  ; W_c  ]              ((K_u + K_c) x N)
+ *   Y[i][n][d] = b[n] + sum_k W[k][n] * X[i][k][d]
+ *
+ * This is the baseline "one batched matmul over all candidates" of aixai.ru,
+ * "Deep Dive: Linear Compression"; the IKBO kernels reach the same Y through
+ * the K-axis split (stage 1), which is exact in exact arithmetic.
+ *
+ * Layouts (row-major): map[n_cand]; U[n_users][K_u][D]; C[n_cand][K_c][D];
+ * Wu[K_u][N]; Wc[K_c][N]; b[N] or NULL; output Y[n_sel][N][D] in double for
+ * the selected candidates cands[0..n_sel) (all candidates, in order, when
+ * cands is NULL and n_sel == n_cand).
+ */
+int ikbo_oracle_lce(const int32_t *map, const uint16_t *U, const uint16_t *C,
+                    const uint16_t *Wu, const uint16_t *Wc, const uint16_t *b,
+                    int n_cand, int n_users, int K_u, int K_c, int D, int N,
+                    const int32_t *cands, int n_sel, double *Y, int n_threads)
+{
+    if (n_cand < 0 || n_users < 1 || K_u < 0 || K_c < 0 || D < 1 || N < 1 || n_sel < 0)
+        return ORACLE_BAD_ARG;
+    if (!cands && n_sel != n_cand) return ORACLE_BAD_ARG;
+    const int K = K_u + K_c;
+
+    for (int s = 0; s < n_sel; ++s) {
+        int i = cands ? cands[s] : s;
+        if (i < 0 || i >= n_cand) return ORACLE_BAD_ARG;
+        if (map[i] < 0 || map[i] >= n_users) return ORACLE_MAP_OUT_OF_RANGE;
+    }
+
+    /* W = concat_rows(W_u, W_c) */
+    double *W = (double *)malloc(sizeof(double) * (size_t)(K > 0 ? K : 1) * (size_t)N);
+    if (!W) return ORACLE_NO_MEMORY;
+    for (int k = 0; k < K_u; ++k)
+        for (int n = 0; n < N; ++n) W[(size_t)k * N + n] = bf16_bits_to_double(Wu[(size_t)k * N + n]);
+    for (int k = 0; k < K_c; ++k)
+        for (int n = 0; n < N; ++n)
+            W[(size_t)(K_u + k) * N + n] = bf16_bits_to_double(Wc[(size_t)k * N + n]);
+
+    int status = ORACLE_OK;
+    set_threads(n_threads);
+#pragma omp parallel
+    {
+        double *X = (double *)malloc(sizeof(double) * (size_t)(K > 0 ? K : 1) * (size_t)D);
+        if (!X) {
+#pragma omp atomic write
+            status = ORACLE_NO_MEMORY;
+        }
+#pragma omp for schedule(dynamic, 1)
+        for (int s = 0; s < n_sel; ++s) {
+            if (!X) continue;
+            int i = cands ? cands[s] : s;
+            int u = map[i];
+            /* the broadcast: copy user u's rows, then candidate i's rows */
+            for (int k = 0; k < K_u; ++k)
+                for (int d = 0; d < D; ++d)
+                    X[(size_t)k * D + d] = bf16_bits_to_double(U[((size_t)u * K_u + k) * D + d]);
+            for (int k = 0; k < K_c; ++k)
+                for (int d = 0; d < D; ++d)
+                    X[(size_t)(K_u + k) * D + d] = bf16_bits_to_double(C[((size_t)i * K_c + k) * D + d]);
+            double *Yi = Y + (size_t)s * N * D;
+            for (int n = 0; n < N; ++n) {
+                double bias = b ? bf16_bits_to_double(b[n]) : 0.0;
+                for (int d = 0; d < D; ++d) {
+                    double acc = 0.0;
+                    for (int k = 0; k < K; ++k) acc += W[(size_t)k * N + n] * X[(size_t)k * D + d];
+                    Yi[(size_t)n * D + d] = bias + acc;
+                }
+            }
+        }
+        free(X);
+    }
+    free(W);
+    return status;
+}
+
+/*
+ * Broadcast attention, ordinary softmax attention per (candidate, head):
+ *   u = map[i];  keys/values are user u's rows j in [0, L_u)
+ *   s_j  = scale * sum_c Q[i,h,q,c] * K[u,h,j,c]
+ *   m    = max_j s_j;   p_j = exp(s_j - m)
+ *   O[i,h,q,:] = sum_j p_j V[u,h,j,:] / sum_j p_j        (0 when L_u = 0)
+ *
+ * aixai.ru, "Deep Dive: Flash Attention": IKBO FA reuses one user's K/V for
+ * all of that user's candidates; the attention itself is unchanged.
+ *
+ * Layouts: Q[n_cand][H][Lq][d].  Dense K/V (kv_offsets NULL):
+ * K[n_users][H][Lkv][d].  Jagged K/V: K[total][H][d], user u owning rows
+ * kv_offsets[u] .. kv_offsets[u+1]-1.  Output O[n_sel][Lq][d] in double for
+ * the selected (i, h) pairs pairs[2s], pairs[2s+1] (all pairs in (i, h) order
+ * when pairs is NULL and n_sel == n_cand*H).
+ */
+int ikbo_oracle_attn(const int32_t *map, const uint16_t *Q, const uint16_t *K, const uint16_t *V,
+                     const int32_t *kv_offsets, int n_cand, int n_users, int H, int Lq, int Lkv,
+                     int d, double scale, const int32_t *pairs, int n_sel, double *O, int n_threads)
+{
+    if (n_cand < 0 || n_users < 1 || H < 1 || Lq < 1 || d < 1 || n_sel < 0) return ORACLE_BAD_ARG;
+    if (!kv_offsets && Lkv < 0) return ORACLE_BAD_ARG;
+    if (!pairs && n_sel != n_cand * H) return ORACLE_BAD_ARG;
+    for (int s = 0; s < n_sel; ++s) {
+        int i = pairs ? pairs[2 * s] : s / H;
+        int h = pairs ? pairs[2 * s + 1] : s % H;
+        if (i < 0 || i >= n_cand || h < 0 || h >= H) return ORACLE_BAD_ARG;
+        if (map[i] < 0 || map[i] >= n_users) return ORACLE_MAP_OUT_OF_RANGE;
+    }
+    int max_len = Lkv;
+    if (kv_offsets) {
+        max_len = 0;
+        for (int u = 0; u < n_users; ++u) {
+            int L = kv_offsets[u + 1] - kv_offsets[u];
+            if (L < 0) return ORACLE_BAD_ARG;
+            if (L > max_len) max_len = L;
+        }
+    }
+
+    int status = ORACLE_OK;
+    set_threads(n_threads);
+#pragma omp parallel
+    {
+        double *sc = (double *)malloc(sizeof(double) * (size_t)(max_len > 0 ? max_len : 1));
+        if (!sc) {
+#pragma omp atomic write
+            status = ORACLE_NO_MEMORY;
+        }
+#pragma omp for schedule(dynamic, 1)
+        for (int s = 0; s < n_sel; ++s) {
+            if (!sc) continue;
+            int i = pairs ? pairs[2 * s] : s / H;
+            int h = pairs ? pairs[2 * s + 1] : s % H;
+            int u = map[i];
+            int L;
+            size_t row0, row_stride; /* element offset of key row 0 and between key rows */
+            if (kv_offsets) {
+                L = kv_offsets[u + 1] - kv_offsets[u];
+                row0 = ((size_t)kv_offsets[u] * H + h) * d;
+                row_stride = (size_t)H * d;
+            } else {
+                L = Lkv;
+                row0 = ((size_t)u * H + h) * (size_t)Lkv * d;
+                row_stride = (size_t)d;
+            }
+            for (int q = 0; q < Lq; ++q) {
+                const uint16_t *qrow = Q + (((size_t)i * H + h) * Lq + q) * d;
+                double *orow = O + ((size_t)s * Lq + q) * d;
+                for (int c = 0; c < d; ++c) orow[c] = 0.0;
+                if (L == 0) continue;
+                double m = -INFINITY;
+                for (int j = 0; j < L; ++j) {
+                    const uint16_t *krow = K + row0 + (size_t)j * row_stride;
+                    double dot = 0.0;
+                    for (int c = 0; c < d; ++c) dot += bf16_bits_to_double(qrow[c]) * bf16_bits_to_double(krow[c]);
+                    sc[j] = scale * dot;
+                    if (sc[j] > m) m = sc[j];
+                }
+                double l = 0.0;
+                for (int j = 0; j < L; ++j) {
+                    sc[j] = exp(sc[j] - m);
+                    l += sc[j];
+                }
+                for (int j = 0; j < L; ++j) {
+                    const uint16_t *vrow = V + row0 + (size_t)j * row_stride;
+                    double w = sc[j];
+                    for (int c = 0; c < d; ++c) orow[c] += w * bf16_bits_to_double(vrow[c]);
+                }
+                for (int c = 0; c < d; ++c) orow[c] /= l;
+            }
+        }
+        free(sc);
+    }
+    return status;
+}

@@ -1,0 +1,294 @@
+"""Pins for the CPU oracle: checks against what the IKBO pages and plain
+mathematics fix, never against the oracle's own formula retyped.
+
+Each ``pin_*`` takes a loaded oracle build and raises AssertionError when the
+oracle disagrees with the pin.  ``test_oracle_*.py`` run them on the real
+oracle; ``test_oracle_mutations.py`` runs them on copies of the oracle with a
+planted mistake and expects at least one pin to fail.
+"""
+from __future__ import annotations
+
+import math
+from fractions import Fraction
+
+import numpy as np
+import torch
+import torch.nn.functional as F
+
+from broadcast_gemm_attention_gb300 import inputs as gen
+
+
+def f64(t: torch.Tensor) -> np.ndarray:
+    return t.to(torch.float64).numpy()
+
+
+# ====================================================================== LCE
+def _small_lce(seed=7, n_cand=9, n_users=3, K_u=5, K_c=7, D=8, N=4, map_kind="permuted", bias=True):
+    return gen.make_lce("pin", seed, n_cand, n_users, K_u, K_c, D, N, map_kind=map_kind, bias=bias,
+                        w_var=0.3)
+
+
+def pin_lce_decomposition(orc):
+    """Type I decomposition (aibriefing, "Type I"; aixai.ru, LCE stage 1): the
+    materialised GEMM equals U[map[i]]-part + C[i]-part + b, each a separate
+    library matmul at its own batch size."""
+    x = _small_lce()
+    Y = orc.lce(x.map, x.U, x.C, x.Wu, x.Wc, x.b)
+    m = x.map.numpy()
+    user = np.einsum("kn,ukd->und", f64(x.Wu), f64(x.U))          # at n_users
+    cand = np.matmul(f64(x.Wc).T[None], f64(x.C))                  # at n_cand
+    ref = user[m] + cand + f64(x.b)[None, :, None]
+    np.testing.assert_allclose(Y, ref, rtol=1e-12, atol=1e-12)
+
+
+def pin_lce_exact_rational(orc):
+    """Brute force in exact rational arithmetic on the tiny workload: bf16
+    inputs are dyadic rationals, so the exact value of every output is known;
+    fp64 accumulation of <= 40 products must land within 1e-13 of it."""
+    x = gen.lce_tiny()
+    Y = orc.lce(x.map, x.U, x.C, x.Wu, x.Wc, x.b)
+    U, C, Wu, Wc, b = (t.to(torch.float64).tolist() for t in (x.U, x.C, x.Wu, x.Wc, x.b))
+    m = x.map.tolist()
+    picks = [(0, 0, 0), (3, 7, 31), (8, 2, 5), (15, 5, 17), (11, 0, 30)]
+    for i, n, d in picks:
+        u = m[i]
+        acc = Fraction(b[n])
+        for k in range(x.K_u):
+            acc += Fraction(Wu[k][n]) * Fraction(U[u][k][d])
+        for k in range(x.K_c):
+            acc += Fraction(Wc[k][n]) * Fraction(C[i][k][d])
+        assert abs(Y[i, n, d] - float(acc)) <= 1e-13 * (1 + abs(float(acc))), (i, n, d)
+
+
+def pin_lce_single_user_no_candidate_part(orc):
+    """n_users = 1 and W_c = 0: every candidate gets W_u^T U[0] + b (one matmul)."""
+    x = _small_lce(n_users=1, map_kind="sorted")
+    Wc0 = torch.zeros_like(x.Wc)
+    Y = orc.lce(x.map, x.U, x.C, x.Wu, Wc0, x.b)
+    ref = np.matmul(f64(x.Wu).T, f64(x.U)[0]) + f64(x.b)[:, None]
+    for i in range(x.n_cand):
+        np.testing.assert_allclose(Y[i], ref, rtol=1e-12, atol=1e-12)
+
+
+def pin_lce_identity_map_is_batched_gemm(orc):
+    """map = identity with no user rows (K_u = 0): a plain batched GEMM."""
+    x = gen.make_lce("pin", 11, 6, 6, 0, 9, 8, 4, explicit_map=list(range(6)), bias=False, w_var=0.3)
+    Y = orc.lce(x.map, x.U, x.C, x.Wu, x.Wc, None)
+    ref = np.matmul(f64(x.Wc).T[None], f64(x.C))
+    np.testing.assert_allclose(Y, ref, rtol=1e-12, atol=1e-12)
+
+
+def pin_lce_one_sided(orc):
+    """U = 0 leaves the candidate GEMM + b; C = 0 leaves the user GEMM + b."""
+    x = _small_lce(seed=9)
+    m = x.map.numpy()
+    Y = orc.lce(x.map, torch.zeros_like(x.U), x.C, x.Wu, x.Wc, x.b)
+    np.testing.assert_allclose(Y, np.matmul(f64(x.Wc).T[None], f64(x.C)) + f64(x.b)[None, :, None],
+                               rtol=1e-12, atol=1e-12)
+    Y = orc.lce(x.map, x.U, torch.zeros_like(x.C), x.Wu, x.Wc, x.b)
+    ref = np.matmul(f64(x.Wu).T[None], f64(x.U)[m]) + f64(x.b)[None, :, None]
+    np.testing.assert_allclose(Y, ref, rtol=1e-12, atol=1e-12)
+
+
+def pin_lce_permutation(orc):
+    """Permuting candidates (map and C together) permutes Y, exactly."""
+    x = _small_lce(seed=13, n_cand=12, n_users=4)
+    Y = orc.lce(x.map, x.U, x.C, x.Wu, x.Wc, x.b)
+    p = torch.from_numpy(np.random.default_rng(5).permutation(x.n_cand))
+    Yp = orc.lce(x.map[p], x.U, x.C[p], x.Wu, x.Wc, x.b)
+    assert np.array_equal(Yp, Y[p.numpy()])
+
+
+def pin_lce_zero_padding(orc):
+    """Zero-padding K (the pages' stage 2 trick, stated mathematically
+    equivalent) leaves Y unchanged."""
+    x = _small_lce(seed=17)
+    Y = orc.lce(x.map, x.U, x.C, x.Wu, x.Wc, x.b)
+    pu, pc = 3, 5
+    U2 = torch.cat([x.U, torch.zeros(x.n_users, pu, x.D, dtype=torch.bfloat16)], 1)
+    Wu2 = torch.cat([x.Wu, torch.zeros(pu, x.N, dtype=torch.bfloat16)], 0)
+    C2 = torch.cat([x.C, torch.zeros(x.n_cand, pc, x.D, dtype=torch.bfloat16)], 1)
+    Wc2 = torch.cat([x.Wc, torch.zeros(pc, x.N, dtype=torch.bfloat16)], 0)
+    Y2 = orc.lce(x.map, U2, C2, Wu2, Wc2, x.b)
+    np.testing.assert_allclose(Y2, Y, rtol=0, atol=1e-15)
+
+
+def pin_lce_selection(orc):
+    """Evaluating a subset of candidates returns exactly those rows."""
+    x = _small_lce(seed=19)
+    Y = orc.lce(x.map, x.U, x.C, x.Wu, x.Wc, x.b)
+    sel = [4, 0, 8, 4]
+    Ys = orc.lce(x.map, x.U, x.C, x.Wu, x.Wc, x.b, cands=sel)
+    assert np.array_equal(Ys, Y[sel])
+
+
+LCE_PINS = [pin_lce_decomposition, pin_lce_exact_rational, pin_lce_single_user_no_candidate_part,
+            pin_lce_identity_map_is_batched_gemm, pin_lce_one_sided, pin_lce_permutation,
+            pin_lce_zero_padding, pin_lce_selection]
+
+
+# ================================================================ attention
+def _sdpa64(q, k, v, scale=None):
+    return F.scaled_dot_product_attention(q.to(torch.float64), k.to(torch.float64),
+                                          v.to(torch.float64), scale=scale).numpy()
+
+
+def pin_attn_identity_map_is_sdpa(orc):
+    """map = identity (one candidate per user) is ordinary batched attention:
+    torch's fp64 scaled_dot_product_attention on the CPU."""
+    x = gen.make_attn("pin", 21, n_cand=5, n_users=5, H=3, Lq=4, d=16, Lkv=11,
+                      explicit_map=list(range(5)))
+    O = orc.attn(x.map, x.Q, x.K, x.V).reshape(5, 3, 4, 16)
+    ref = _sdpa64(x.Q, x.K, x.V)
+    np.testing.assert_allclose(O, ref, rtol=1e-10, atol=1e-12)
+
+
+def pin_attn_single_user_is_mqa(orc):
+    """One user serving every candidate: multi-query attention of all
+    candidates' queries against the one K/V (SDPA on the expanded K/V)."""
+    x = gen.make_attn("pin", 23, n_cand=6, n_users=1, H=2, Lq=3, d=16, Lkv=9, explicit_map=[0] * 6)
+    O = orc.attn(x.map, x.Q, x.K, x.V).reshape(6, 2, 3, 16)
+    ref = _sdpa64(x.Q, x.K.expand(6, -1, -1, -1), x.V.expand(6, -1, -1, -1))
+    np.testing.assert_allclose(O, ref, rtol=1e-10, atol=1e-12)
+
+
+def pin_attn_broadcast_is_sdpa_on_gathered_kv(orc):
+    """General map: equal to SDPA on the materialised K[map], V[map]."""
+    x = gen.make_attn("pin", 25, n_cand=10, n_users=3, H=2, Lq=5, d=16, Lkv=13, map_kind="permuted")
+    O = orc.attn(x.map, x.Q, x.K, x.V).reshape(10, 2, 5, 16)
+    idx = x.map.long()
+    ref = _sdpa64(x.Q, x.K[idx], x.V[idx])
+    np.testing.assert_allclose(O, ref, rtol=1e-10, atol=1e-12)
+
+
+def pin_attn_closed_forms(orc):
+    """Q = 0 gives the mean of the user's V rows; a constant V gives that
+    constant; a single key gives its V row; one dominant score picks its row."""
+    d, L = 16, 7
+    x = gen.make_attn("pin", 27, n_cand=4, n_users=2, H=1, Lq=2, d=d, Lkv=L, explicit_map=[1, 0, 1, 0])
+    O = orc.attn(x.map, torch.zeros_like(x.Q), x.K, x.V).reshape(4, 2, d)
+    for i, u in enumerate(x.map.tolist()):
+        mean = f64(x.V[u, 0]).mean(0)
+        np.testing.assert_allclose(O[i], np.broadcast_to(mean, (2, d)), rtol=1e-12, atol=1e-13)
+    Vc = torch.full_like(x.V, 0.375)
+    O = orc.attn(x.map, x.Q, x.K, Vc)
+    np.testing.assert_allclose(O, 0.375, rtol=0, atol=1e-14)
+    x1 = gen.make_attn("pin", 29, n_cand=3, n_users=2, H=2, Lq=2, d=d, Lkv=1, explicit_map=[1, 1, 0])
+    O = orc.attn(x1.map, x1.Q, x1.K, x1.V).reshape(3, 2, 2, d)
+    for i, u in enumerate(x1.map.tolist()):
+        for h in range(2):
+            np.testing.assert_allclose(O[i, h], np.broadcast_to(f64(x1.V[u, h, 0]), (2, d)), rtol=0, atol=0)
+    # one dominant score: key j* = 3 aligned with the query, the rest orthogonal
+    K = torch.zeros(1, 1, 6, d, dtype=torch.bfloat16)
+    K[0, 0, 3, 0] = 8.0
+    K[0, 0, :, 1] = 1.0
+    Q = torch.zeros(1, 1, 1, d, dtype=torch.bfloat16)
+    Q[0, 0, 0, 0] = 8.0
+    V = gen.make_attn("pin", 31, 1, 1, 1, 1, d, Lkv=6, explicit_map=[0]).V
+    O = orc.attn(torch.tensor([0], dtype=torch.int32), Q, K, V)
+    # score gap 64/sqrt(16) = 16 -> the other 5 rows weigh 5 e^-16 ~ 5.6e-7 in total
+    np.testing.assert_allclose(O[0, 0], f64(V[0, 0, 3]), rtol=0, atol=5e-6)
+
+
+def pin_attn_permutation(orc):
+    """Permuting candidates (map and Q together) permutes O, exactly."""
+    x = gen.make_attn("pin", 33, n_cand=8, n_users=3, H=2, Lq=3, d=16, Lkv=10, map_kind="permuted")
+    O = orc.attn(x.map, x.Q, x.K, x.V).reshape(8, 2, 3, 16)
+    p = torch.from_numpy(np.random.default_rng(3).permutation(8))
+    Op = orc.attn(x.map[p], x.Q[p], x.K, x.V).reshape(8, 2, 3, 16)
+    assert np.array_equal(Op, O[p.numpy()])
+
+
+def pin_attn_jagged(orc):
+    """Jagged K/V [sum L, H, d] with int32 offsets: each candidate attends to
+    exactly its user's slice (SDPA per slice); an empty slice gives 0."""
+    lens = [5, 0, 12, 3]
+    x = gen.make_attn("pin", 35, n_cand=7, n_users=4, H=2, Lq=3, d=16,
+                      explicit_map=[2, 0, 1, 3, 2, 0, 1], explicit_lengths=lens)
+    O = orc.attn(x.map, x.Q, x.K, x.V, kv_offsets=x.kv_offsets).reshape(7, 2, 3, 16)
+    offs = x.kv_offsets.tolist()
+    for i, u in enumerate(x.map.tolist()):
+        a, b = offs[u], offs[u + 1]
+        if b == a:
+            assert np.all(O[i] == 0)
+            continue
+        k = x.K[a:b].permute(1, 0, 2).unsqueeze(0)
+        v = x.V[a:b].permute(1, 0, 2).unsqueeze(0)
+        ref = _sdpa64(x.Q[i:i + 1], k, v)[0]
+        np.testing.assert_allclose(O[i], ref, rtol=1e-10, atol=1e-12)
+
+
+def pin_attn_scale(orc):
+    """An explicit scale is honoured: scale s on Q.K equals default scale on (s*sqrt(d)) Q."""
+    x = gen.make_attn("pin", 37, n_cand=3, n_users=2, H=1, Lq=2, d=16, Lkv=6, explicit_map=[0, 1, 1])
+    O = orc.attn(x.map, x.Q, x.K, x.V, scale=0.5).reshape(3, 1, 2, 16)
+    ref = _sdpa64(x.Q, x.K[x.map.long()], x.V[x.map.long()], scale=0.5)
+    np.testing.assert_allclose(O, ref, rtol=1e-10, atol=1e-12)
+
+
+ATTN_PINS = [pin_attn_identity_map_is_sdpa, pin_attn_single_user_is_mqa,
+             pin_attn_broadcast_is_sdpa_on_gathered_kv, pin_attn_closed_forms,
+             pin_attn_permutation, pin_attn_jagged, pin_attn_scale]
+
+
+# ================================================================ segments
+def _check_segments_against_brute_force(orc, m: np.ndarray, n_users: int, H: int, cpu: int):
+    counts, offsets, perm, work = orc.segments(m, n_users, H, cpu)
+    # brute force with library routines
+    assert np.array_equal(counts, np.bincount(m, minlength=n_users))
+    assert np.array_equal(perm, np.argsort(m, kind="stable"))
+    assert offsets[0] == 0 and offsets[-1] == len(m)
+    assert np.array_equal(np.diff(offsets), counts)
+    # invariants
+    assert sorted(perm.tolist()) == list(range(len(m)))
+    for u in range(n_users):
+        seg = perm[offsets[u]:offsets[u + 1]]
+        assert np.all(m[seg] == u)
+        assert np.all(np.diff(seg) > 0)
+    # work list: units cover every (u, h) segment exactly, in (u, h, start) order
+    covered = {}
+    prev = None
+    for u, h, s, c in work.tolist():
+        assert 1 <= c <= cpu
+        key = (u, h, s)
+        assert prev is None or key > prev
+        prev = key
+        covered.setdefault((u, h), []).append((s, c))
+    for u in range(n_users):
+        for h in range(H):
+            runs = covered.get((u, h), [])
+            if counts[u] == 0:
+                assert runs == []
+                continue
+            pos = offsets[u]
+            for s, c in runs:
+                assert s == pos
+                pos += c
+            assert pos == offsets[u + 1]
+            assert all(c == cpu for _, c in runs[:-1])
+    assert len(work) == H * sum(-(-int(c) // cpu) for c in counts)
+
+
+def pin_segments_brute_force(orc):
+    rng = np.random.default_rng(41)
+    for n, U in [(1, 1), (17, 4), (300, 7), (1024, 15), (513, 600)]:
+        m = rng.integers(0, U, size=n).astype(np.int32)
+        _check_segments_against_brute_force(orc, m, U, 3, 4)
+    m = gen.zipf_permuted_map(np.random.default_rng(2), 4096, 64, 1.1)
+    _check_segments_against_brute_force(orc, m, 64, 8, 16)
+
+
+def pin_segments_special_cases(orc):
+    m = np.repeat(np.arange(5, dtype=np.int32), [3, 0, 4, 1, 2])
+    counts, offsets, perm, work = orc.segments(m, 5, 2, 2)
+    assert np.array_equal(perm, np.arange(len(m)))           # sorted map: identity
+    assert offsets.tolist() == [0, 3, 3, 7, 8, 10]
+    counts, offsets, perm, work = orc.segments(np.zeros(9, np.int32), 1, 1, 4)
+    assert offsets.tolist() == [0, 9] and work.tolist() == [[0, 0, 0, 4], [0, 0, 4, 4], [0, 0, 8, 1]]
+    counts, offsets, perm, work = orc.segments(np.array([2, 0, 2, 0, 1], np.int32), 4, 1, 8)
+    assert perm.tolist() == [1, 3, 4, 0, 2] and counts.tolist() == [2, 1, 2, 0]
+    assert work.tolist() == [[0, 0, 0, 2], [1, 0, 2, 1], [2, 0, 3, 2]]
+
+
+SEG_PINS = [pin_segments_brute_force, pin_segments_special_cases]
+ALL_PINS = LCE_PINS + ATTN_PINS + SEG_PINS

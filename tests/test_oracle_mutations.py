@@ -1,0 +1,50 @@
+"""Plant plausible mistakes in copies of the oracle's C source and check that
+the pins catch every one (a pin that a planted mistake slips past is a pin
+that would not catch that mistake in the real oracle either)."""
+import os
+
+import pytest
+
+import oracle
+from oracle_pins import ATTN_PINS, LCE_PINS, SEG_PINS
+
+MUTATIONS = {
+    # LCE
+    "lce_drop_bias": ("double bias = b ? bf16_bits_to_double(b[n]) : 0.0;", "double bias = 0.0;", LCE_PINS),
+    "lce_user_index_is_candidate": ("int u = map[i];\n            /* the broadcast", "int u = i % n_users;\n            /* the broadcast", LCE_PINS),
+    "lce_drop_last_k": ("for (int k = 0; k < K; ++k) acc +=", "for (int k = 0; k < K - 1; ++k) acc +=", LCE_PINS),
+    "lce_sign_flip": ("acc += W[(size_t)k * N + n] * X", "acc -= W[(size_t)k * N + n] * X", LCE_PINS),
+    "lce_transposed_w": ("W[(size_t)(K_u + k) * N + n] = bf16_bits_to_double(Wc[(size_t)k * N + n]);",
+                         "W[(size_t)(K_u + k) * N + n] = bf16_bits_to_double(Wc[((size_t)k * N + n) % ((size_t)K_c * N) / K_c + ((size_t)k * N + n) % K_c * N]);", LCE_PINS),
+    "lce_user_rows_from_candidate": ("X[(size_t)k * D + d] = bf16_bits_to_double(U[((size_t)u * K_u + k) * D + d]);",
+                                     "X[(size_t)k * D + d] = bf16_bits_to_double(U[((size_t)(u ? 0 : u) * K_u + k) * D + d]);", LCE_PINS),
+    # attention
+    "attn_no_scale": ("sc[j] = scale * dot;", "sc[j] = dot;", ATTN_PINS),
+    "attn_no_normalise": ("for (int c = 0; c < d; ++c) orow[c] /= l;", "", ATTN_PINS),
+    "attn_v_from_k": ("const uint16_t *vrow = V + row0", "const uint16_t *vrow = K + row0", ATTN_PINS),
+    "attn_user_is_candidate": ("int u = map[i];\n            int L;", "int u = i % n_users;\n            int L;", ATTN_PINS),
+    "attn_drop_last_key": ("for (int j = 0; j < L; ++j) {\n                    const uint16_t *vrow", "for (int j = 0; j < L - 1; ++j) {\n                    const uint16_t *vrow", ATTN_PINS),
+    "attn_jagged_stride": ("row_stride = (size_t)H * d;", "row_stride = (size_t)d;", ATTN_PINS),
+    # segments
+    "seg_unstable": ("for (int i = 0; i < n_cand; ++i) {       /* ascending i: stable */", "for (int i = n_cand - 1; i >= 0; --i) {", SEG_PINS),
+    "seg_inclusive_scan": ("for (int u = 0; u < n_users; ++u) next[u] = offsets[u];", "for (int u = 0; u < n_users; ++u) next[u] = offsets[u] + (counts[u] > 1);", SEG_PINS),
+    "seg_chunk_off_by_one": ("if (cnt > cands_per_unit) cnt = cands_per_unit;", "if (cnt >= cands_per_unit) cnt = cands_per_unit - 1 + (cands_per_unit == 1);", SEG_PINS),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_pins_catch_planted_mistake(name, tmp_path):
+    old, new, pins = MUTATIONS[name]
+    src = open(oracle.SOURCE).read()
+    assert src.count(old) == 1, f"mutation anchor for {name} not unique/not found"
+    mutated = tmp_path / "mut.c"
+    mutated.write_text(src.replace(old, new))
+    lib = oracle.compile_source(str(mutated), str(tmp_path / "libmut.so"))
+    orc = oracle.Oracle(lib)
+    caught = []
+    for pin in pins:
+        try:
+            pin(orc)
+        except (AssertionError, oracle.OracleError, ValueError, IndexError):
+            caught.append(pin.__name__)
+    assert caught, f"no pin caught the planted mistake {name}"
