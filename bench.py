@@ -1,0 +1,457 @@
+#!/usr/bin/env python
+"""Benchmark of the IKBO hot path on one 1024-candidate, 15-user request.
+
+One step = one request through the whole hot path:
+  ikbo_plan         segment build from the candidate->user map
+  ikbo_lce_forward  fused LCE  (n_cand 1024, n_users 15, K_u 381, K_c 243, D 256, N 192)
+  ikbo_attn_forward broadcast attention (H 8, Lq 32, Lkv 2048, d 128) on the same map
+Inputs are seeded synthetic tensors resident in HBM; the L2 is flushed
+(256 MiB memset) between steps, outside the per-step CUDA events.
+
+Output: one JSON line (rank 0).  `value` = algorithmic TFLOP/s of the whole
+step over all ranks (weak scaling: each rank runs its own request);
+`roofline` is the attention kernel's tensor-core fraction, `roofline_lce`
+the LCE kernel's HBM fraction; `cpu_baseline` is the fp64 oracle timed on
+this host's cores on a bounded sample of the same request; `e2e` repeats the
+step through the C ABI with host buffers (H2D of every input, D2H of Y and
+O inside the timed region).
+
+    python bench.py [--steps K] [--warmup W] [--impl ikbo|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "LCE & broadcast-attn BF16 TFLOP/s, % of roofline; µs per 1024-cand request"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            j = json.load(f)
+        return {"hbm_gbs": float(j["hbm_gbs"]), "bf16_tflops": float(j["bf16_tflops"]),
+                "bf16_tflops_sustained": float(j.get("bf16_tflops_sustained", j["bf16_tflops"])),
+                "source": "measured (MEASURED_PEAKS.json)"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback (no MEASURED_PEAKS.json)"}
+
+
+def source_hash(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+KERNEL_SOURCES = {
+    "attn": ["broadcast_gemm_attention_gb300/csrc/attn.cu", "broadcast_gemm_attention_gb300/csrc/ptx.cuh",
+             "broadcast_gemm_attention_gb300/csrc/ikbo_internal.h"],
+    "lce": ["broadcast_gemm_attention_gb300/csrc/lce.cu", "broadcast_gemm_attention_gb300/csrc/ptx.cuh",
+            "broadcast_gemm_attention_gb300/csrc/ikbo_internal.h"],
+}
+
+
+def recorded_traffic(kernel):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel
+    source is unchanged since the counters were taken; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            j = json.load(f)[kernel]
+        if j.get("source_hash") == source_hash(KERNEL_SOURCES[kernel]):
+            return float(j["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 100 ms while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.lines = []
+        self.dev = device_index
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            time.sleep(0.3)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.proc:
+            return None
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------------- workload
+def workload():
+    from broadcast_gemm_attention_gb300 import inputs as gen
+    x = gen.lce_70to1()
+    a = gen.attn_70to1()
+    assert x.map.tolist() == a.map.tolist()
+    return x, a
+
+
+def flops_bytes(x, a):
+    from broadcast_gemm_attention_gb300 import accounting as acc
+    lf = acc.lce_flops(x.n_cand, x.n_users, x.K_u, x.K_c, x.D, x.N)
+    lb = acc.lce_bytes(x.n_cand, x.n_users, x.K_u, x.K_c, x.D, x.N)
+    af = acc.attn_flops(a.H, a.Lq, a.d, [a.Lkv] * a.n_cand)
+    ab = acc.attn_bytes(a.n_cand, a.H, a.Lq, a.d, a.n_users * a.Lkv)
+    return lf, lb, af, ab
+
+
+def config_dict(x, a):
+    return {
+        "workload": "request_70to1: plan + LCE + broadcast attention, 1024 candidates / 15 users (sorted "
+                    "multinomial map)",
+        "lce": {"n_cand": x.n_cand, "n_users": x.n_users, "K_u": x.K_u, "K_c": x.K_c, "D": x.D, "N": x.N},
+        "attn": {"n_cand": a.n_cand, "n_users": a.n_users, "H": a.H, "Lq": a.Lq, "Lkv": a.Lkv, "d": a.d},
+        "l2": "256 MiB memset between steps (outside the per-step events); each step also streams ~490 MB",
+    }
+
+
+# ------------------------------------------------------------ CPU oracle
+def cpu_oracle_sample(x, a, n: int, seed: int = 0):
+    """The fp64 oracle on a bounded sample: n candidates' complete share of the
+    request (their LCE rows and their attention over all heads).  Returns
+    (seconds, algorithmic flops credited, description, threads)."""
+    import numpy as np
+    import oracle
+    rng = np.random.default_rng(seed)
+    cands = sorted(rng.choice(x.n_cand, size=n, replace=False).tolist())
+    pairs = [(i, h) for i in cands for h in range(a.H)]
+    per_cand = 2.0 * x.D * x.N * (x.K_c + x.K_u * x.n_users / x.n_cand)   # user GEMM amortised
+    per_cand += a.H * 4.0 * a.Lq * a.Lkv * a.d
+    t0 = time.perf_counter()
+    oracle.lce(x.map, x.U, x.C, x.Wu, x.Wc, x.b, cands=cands)
+    oracle.attn(a.map, a.Q, a.K, a.V, pairs=pairs)
+    dt = time.perf_counter() - t0
+    desc = (f"{n} of the 1024 candidates of the 70:1 request, each with its LCE rows and its attention over "
+            f"all {a.H} heads; credited with the GPU path's algorithmic FLOPs for that share")
+    return dt, n * per_cand, desc, oracle.max_threads()
+
+
+def calibrate_oracle(x, a, seconds: float, lo: int = 1, hi: int = 1024):
+    """Candidates per sample so that one sample takes about `seconds`."""
+    dt, _, _, _ = cpu_oracle_sample(x, a, 2, seed=12345)
+    n = int(round(seconds / max(dt / 2, 1e-6)))
+    return max(lo, min(hi, n))
+
+
+def run_reference(args):
+    """The reference arm: the oracle, as it stands, on the host cores."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    x, a = workload()
+    per_step = max(0.05, min(3.0, args.ref_budget / max(1, args.steps + args.warmup)))
+    n = calibrate_oracle(x, a, per_step)
+    for w in range(args.warmup):
+        cpu_oracle_sample(x, a, n, seed=1000 + w)
+    tot_t, tot_f = 0.0, 0.0
+    desc, thr = "", 0
+    for k in range(args.steps):
+        dt, fl, desc, thr = cpu_oracle_sample(x, a, n, seed=k)
+        tot_t += dt
+        tot_f += fl
+    v = tot_f / tot_t / 1e12
+    out = {"impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOP/s", "n_gpus": args.gpus,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot_t / args.steps,
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+           "data": "synthetic", "config": config_dict(x, a),
+           "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
+                            "sample": f"per step: {desc}"},
+           "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+# ------------------------------------------------------------------ GPU
+def run_gpu(args):
+    import torch
+    import __graft_entry__ as ge
+    from broadcast_gemm_attention_gb300 import binding as B
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    ge.build()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    stream = torch.cuda.current_stream()
+    x, a = workload()
+    lf, lb, af, ab = flops_bytes(x, a)
+    step_flops = lf + af
+
+    d = {k: v.to(dev) for k, v in dict(map=x.map, U=x.U, C=x.C, Wu=x.Wu, Wc=x.Wc, b=x.b, Q=a.Q, K=a.K, V=a.V).items()}
+    Y = torch.empty(x.n_cand, x.N, x.D, dtype=torch.bfloat16, device=dev)
+    O = torch.empty_like(d["Q"])
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    plan = B.Plan(x.n_cand, max(x.n_users, x.n_cand), a.H)
+
+    def step():
+        plan.plan(d["map"], x.n_users, a.H, a.Lq, stream)
+        plan.lce_forward(d["U"], d["C"], d["Wu"], d["Wc"], d["b"], Y, stream)
+        plan.attn_forward(d["Q"], d["K"], d["V"], None, O, None, stream)
+
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        step()
+    st = plan.status()
+    if st != B.IKBO_OK:
+        raise RuntimeError(f"device status after warm-up: {B.ikbo_status_string(st)}")
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    launches0 = plan.launches()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        for k in range(K):
+            flush.zero_()
+            e = ev[k]
+            e[0].record(stream)
+            plan.plan(d["map"], x.n_users, a.H, a.Lq, stream)
+            e[1].record(stream)
+            plan.lce_forward(d["U"], d["C"], d["Wu"], d["Wc"], d["b"], Y, stream)
+            e[2].record(stream)
+            plan.attn_forward(d["Q"], d["K"], d["V"], None, O, None, stream)
+            e[3].record(stream)
+        torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    gpu_launches = plan.launches() - launches0
+    st = plan.status()
+    if st != B.IKBO_OK:
+        raise RuntimeError(f"device status after timing: {B.ikbo_status_string(st)}")
+    plan_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    lce_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    attn_ms = [e[2].elapsed_time(e[3]) for e in ev]
+    step_ms = [e[0].elapsed_time(e[3]) for e in ev]
+    total_ms = sum(step_ms)
+    if dist:
+        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / K
+    value = world * step_flops * K / (total_ms * 1e-3) / 1e12
+
+    pk = peaks()
+    lce_s = statistics.mean(lce_ms) * 1e-3
+    attn_s = statistics.mean(attn_ms) * 1e-3
+    attn_tf = af / attn_s / 1e12
+    lce_tf = lf / lce_s / 1e12
+    lce_gbs = lb / lce_s / 1e9
+    roofline = {"kernel": "attn_fwd_kernel (broadcast attention)", "bound": "tensor", "achieved": attn_tf,
+                "peak": pk["bf16_tflops"], "unit": "TFLOP/s", "frac": attn_tf / pk["bf16_tflops"],
+                "traffic": recorded_traffic("attn"),
+                "peak_source": pk["source"] + ", bf16 burst (kernel timed alone in a short step)",
+                "algorithmic": f"{af:.4g} FLOP per launch = 4*H*Lq*d*sum_i Lkv"}
+    roofline_lce = {"kernel": "lce_fused_kernel", "bound": "hbm", "achieved": lce_gbs, "peak": pk["hbm_gbs"],
+                    "unit": "GB/s", "frac": lce_gbs / pk["hbm_gbs"], "traffic": recorded_traffic("lce"),
+                    "tflops": lce_tf, "algorithmic": f"{lb:.4g} bytes per launch (inputs once, Y once)"}
+
+    # ---------------- end to end through the C ABI with host buffers
+    e2e = None
+    if not args.no_e2e:
+        h_in = {k: v.cpu().pin_memory() for k, v in d.items()}
+        hY = torch.empty(Y.shape, dtype=Y.dtype).pin_memory()
+        hO = torch.empty(O.shape, dtype=O.dtype).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in h_in.values())
+        d2h = hY.numel() * 2 + hO.numel() * 2
+        n_e2e = max(3, min(args.e2e_steps, K))
+        e_s = torch.cuda.Event(enable_timing=True)
+        e_e = torch.cuda.Event(enable_timing=True)
+
+        def e2e_step():
+            for k, t in h_in.items():
+                d[k].copy_(t, non_blocking=True)
+            step()
+            hY.copy_(Y, non_blocking=True)
+            hO.copy_(O, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        e_s.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        e_e.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = e_s.elapsed_time(e_e) / n_e2e
+        if dist:
+            t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        e2e = {"value": world * step_flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "steps": n_e2e,
+               "path": "pinned host -> device copies, ikbo_plan + ikbo_lce_forward + ikbo_attn_forward, "
+                       "device -> pinned host copies of Y and O, one stream"}
+
+    # ---------------- ablation: our kernels fed a materialised broadcast
+    ablation = None
+    if not args.no_ablation:
+        ablation = ablation_run(plan, d, x, a, Y, O, flush, stream, dev)
+
+    plan.close()
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return
+
+    cpu = None
+    if world == 1 or rank == 0:
+        n = calibrate_oracle(x, a, args.cpu_seconds)
+        dt, fl, desc, thr = cpu_oracle_sample(x, a, n)
+        cpu = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": thr, "kind": "oracle", "sample": desc,
+               "seconds": dt}
+
+    out = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic (seeded bf16 N(0,1) activations, fan-in-scaled weights)",
+        "config": config_dict(x, a),
+        "us_per_request": 1e3 * ms_per_step,
+        "us_per_request_forward_only": 1e3 * (statistics.mean(lce_ms) + statistics.mean(attn_ms)),
+        "kernels": {"plan_us": 1e3 * statistics.mean(plan_ms), "lce_us": 1e3 * statistics.mean(lce_ms),
+                    "attn_us": 1e3 * statistics.mean(attn_ms), "lce_tflops": lce_tf, "lce_gbs": lce_gbs,
+                    "attn_tflops": attn_tf, "lce_us_median": 1e3 * statistics.median(lce_ms),
+                    "attn_us_median": 1e3 * statistics.median(attn_ms)},
+        "roofline": roofline, "roofline_lce": roofline_lce,
+        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": gpu_launches,
+        "clocks": clk.summary(), "ablation": ablation,
+    }
+    print(json.dumps(out), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+def ablation_run(plan, d, x, a, Y, O, flush, stream, dev, iters=5):
+    """Same kernels on the replicated tensors (identity map, n_users = n_cand),
+    plus the cost of materialising them (torch index_select)."""
+    import torch
+    from broadcast_gemm_attention_gb300 import binding as B
+    ident = torch.arange(x.n_cand, dtype=torch.int32, device=dev)
+    idx = d["map"].long()
+    res = {}
+
+    def timed(fn):
+        ts = []
+        for _ in range(iters + 1):
+            flush.zero_()
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record(stream)
+            fn()
+            e.record(stream)
+            torch.cuda.synchronize()
+            ts.append(s.elapsed_time(e))
+        return 1e3 * statistics.median(ts[1:])
+
+    U_rep = torch.empty(x.n_cand, x.K_u, x.D, dtype=torch.bfloat16, device=dev)
+    res["lce_materialise_us"] = timed(lambda: torch.index_select(d["U"], 0, idx, out=U_rep))
+    p2 = B.Plan(x.n_cand, x.n_cand, a.H)
+    p2.plan(ident, x.n_cand, a.H, a.Lq, stream)
+    res["lce_on_materialised_us"] = timed(lambda: p2.lce_forward(U_rep, d["C"], d["Wu"], d["Wc"], d["b"], Y, stream))
+    del U_rep
+    K_rep = torch.empty(a.n_cand, a.H, a.Lkv, a.d, dtype=torch.bfloat16, device=dev)
+    V_rep = torch.empty_like(K_rep)
+
+    def mat():
+        torch.index_select(d["K"], 0, idx, out=K_rep)
+        torch.index_select(d["V"], 0, idx, out=V_rep)
+
+    res["attn_materialise_us"] = timed(mat)
+    res["attn_on_materialised_us"] = timed(lambda: p2.attn_forward(d["Q"], K_rep, V_rep, None, O, None, stream))
+    st = p2.status()
+    p2.close()
+    del K_rep, V_rep
+    torch.cuda.empty_cache()
+    res["status"] = B.ikbo_status_string(st)
+    res["note"] = "identity map with n_users = n_cand: the replicated user tensors are real inputs"
+    return res
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ikbo", "reference"], default="ikbo")
+    ap.add_argument("--no-ablation", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target length of the CPU-oracle baseline")
+    ap.add_argument("--ref-budget", type=float, default=120.0, help="reference arm: total seconds of oracle work")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,398 @@
+// api.cu -- the C ABI declared in include/ikbo.h: plan lifetime, argument
+// validation, TMA tensor-map encoding and kernel launches.  No computation
+// of the method happens on the host.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <new>
+
+#include "ikbo.h"
+#include "ikbo_internal.h"
+
+namespace ikbo {
+cudaError_t launch_seg_build(const SegParams& p, cudaStream_t s);
+size_t lce_smem_bytes(const LceParams& p);
+cudaError_t launch_lce(const CUtensorMap& tmU, const CUtensorMap& tmC, const CUtensorMap& tmWu,
+                       const CUtensorMap& tmWc, const LceParams& p, int grid, cudaStream_t s);
+size_t attn_smem_bytes();
+cudaError_t launch_attn(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV, const AttnParams& p,
+                        int grid, cudaStream_t s);
+}  // namespace ikbo
+
+using namespace ikbo;
+
+struct ikbo_plan_s {
+  int device = 0;
+  int num_sms = 0;
+  size_t max_smem = 0;
+  int max_cand = 0, max_users = 0, max_heads = 0;
+  // the bound request
+  bool planned = false;
+  const int32_t* d_map = nullptr;
+  int n_cand = 0, n_users = 0, H = 0, Lq = 0, cands_per_unit = 0;
+  // plan-owned device memory
+  int32_t* d_counts = nullptr;
+  int32_t* d_offsets = nullptr;
+  int32_t* d_perm = nullptr;
+  int32_t* d_work = nullptr;
+  int32_t* d_n_units = nullptr;
+  int64_t max_units = 0;
+  uint32_t* d_status = nullptr;  // [0] status bits, [1] LCE flag-timeout epoch
+  float* d_partial = nullptr;
+  size_t partial_elems = 0;
+  uint32_t* d_flags = nullptr;
+  size_t flags_elems = 0;
+  uint32_t epoch = 0;
+  uint32_t debug = 0;
+  uint64_t timeout_ns = 2000000000ull;
+  std::atomic<uint64_t> launches{0};
+};
+
+namespace {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  });
+  return fn;
+}
+
+// bf16 tensor map with 128-byte swizzle; out-of-bounds elements read as zero.
+bool encode_bf16(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, const uint64_t* strides_bytes,
+                 const uint32_t* box) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t gd[5], gs[4];
+  cuuint32_t bx[5], es[5];
+  for (int i = 0; i < rank; ++i) {
+    gd[i] = dims[i];
+    bx[i] = box[i];
+    es[i] = 1;
+  }
+  for (int i = 0; i < rank - 1; ++i) gs[i] = strides_bytes[i];
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, static_cast<cuuint32_t>(rank), const_cast<void*>(base), gd,
+                  gs, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+template <typename T>
+cudaError_t grow(T** ptr, size_t* have, size_t need) {
+  if (*have >= need && *ptr) return cudaSuccess;
+  if (*ptr) cudaFree(*ptr);
+  *ptr = nullptr;
+  *have = 0;
+  cudaError_t e = cudaMalloc(reinterpret_cast<void**>(ptr), need * sizeof(T));
+  if (e != cudaSuccess) return e;
+  e = cudaMemset(*ptr, 0, need * sizeof(T));
+  if (e != cudaSuccess) return e;
+  *have = need;
+  return cudaSuccess;
+}
+
+void free_plan(ikbo_plan_t p) {
+  if (!p) return;
+  cudaFree(p->d_counts);
+  cudaFree(p->d_offsets);
+  cudaFree(p->d_perm);
+  cudaFree(p->d_work);
+  cudaFree(p->d_n_units);
+  cudaFree(p->d_status);
+  cudaFree(p->d_partial);
+  cudaFree(p->d_flags);
+  delete p;
+}
+
+}  // namespace
+
+extern "C" {
+
+int ikbo_version(void) { return 100; }
+
+const char* ikbo_status_string(ikbo_status_t s) {
+  switch (s) {
+    case IKBO_OK: return "ok";
+    case IKBO_ERR_INVALID_ARG: return "invalid argument";
+    case IKBO_ERR_UNSUPPORTED: return "unsupported shape or layout";
+    case IKBO_ERR_CUDA: return "CUDA error";
+    case IKBO_ERR_MAP_OUT_OF_RANGE: return "map value out of range";
+    case IKBO_ERR_TIMEOUT: return "device wait timed out";
+    case IKBO_ERR_NOT_PLANNED: return "no request planned";
+    case IKBO_ERR_INTERNAL: return "internal error (work list)";
+  }
+  return "unknown status";
+}
+
+ikbo_status_t ikbo_plan_create(ikbo_plan_t* out, int max_cand, int max_users, int max_heads) {
+  if (!out) return IKBO_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (max_cand < 1 || max_users < 1 || max_heads < 1) return IKBO_ERR_INVALID_ARG;
+  if (max_users > SEG_MAX_USERS) return IKBO_ERR_UNSUPPORTED;
+  ikbo_plan_t p = new (std::nothrow) ikbo_plan_s();
+  if (!p) return IKBO_ERR_CUDA;
+  if (cudaGetDevice(&p->device) != cudaSuccess) {
+    delete p;
+    return IKBO_ERR_CUDA;
+  }
+  cudaDeviceProp prop;
+  if (cudaGetDeviceProperties(&prop, p->device) != cudaSuccess) {
+    delete p;
+    return IKBO_ERR_CUDA;
+  }
+  if (prop.major != 10 || prop.minor != 3) {
+    delete p;
+    return IKBO_ERR_UNSUPPORTED;
+  }
+  p->num_sms = prop.multiProcessorCount;
+  p->max_smem = prop.sharedMemPerBlockOptin;
+  p->max_cand = max_cand;
+  p->max_users = max_users;
+  p->max_heads = max_heads;
+  // every candidate run is <= cands_per_unit and each user adds at most one
+  // partial run per head, so H * (n_users + n_cand) bounds the unit count
+  p->max_units = static_cast<int64_t>(max_heads) * (max_users + max_cand);
+  bool ok = cudaMalloc(&p->d_counts, sizeof(int32_t) * max_users) == cudaSuccess &&
+            cudaMalloc(&p->d_offsets, sizeof(int32_t) * (max_users + 1)) == cudaSuccess &&
+            cudaMalloc(&p->d_perm, sizeof(int32_t) * max_cand) == cudaSuccess &&
+            cudaMalloc(&p->d_work, sizeof(int32_t) * 4 * p->max_units) == cudaSuccess &&
+            cudaMalloc(&p->d_n_units, sizeof(int32_t)) == cudaSuccess &&
+            cudaMalloc(&p->d_status, sizeof(uint32_t) * 2) == cudaSuccess &&
+            cudaMemset(p->d_status, 0, sizeof(uint32_t) * 2) == cudaSuccess &&
+            cudaMemset(p->d_n_units, 0, sizeof(int32_t)) == cudaSuccess;
+  if (!ok) {
+    free_plan(p);
+    return IKBO_ERR_CUDA;
+  }
+  *out = p;
+  return IKBO_OK;
+}
+
+void ikbo_plan_destroy(ikbo_plan_t p) {
+  if (!p) return;
+  cudaDeviceSynchronize();
+  free_plan(p);
+}
+
+ikbo_status_t ikbo_plan_set_debug(ikbo_plan_t p, unsigned flags) {
+  if (!p) return IKBO_ERR_INVALID_ARG;
+  p->debug = flags;
+  return IKBO_OK;
+}
+
+ikbo_status_t ikbo_plan_set_timeout_ns(ikbo_plan_t p, uint64_t timeout_ns) {
+  if (!p || timeout_ns == 0) return IKBO_ERR_INVALID_ARG;
+  p->timeout_ns = timeout_ns;
+  return IKBO_OK;
+}
+
+uint64_t ikbo_plan_launch_count(ikbo_plan_t p) { return p ? p->launches.load() : 0; }
+
+ikbo_status_t ikbo_plan(ikbo_plan_t p, const int32_t* d_map, int n_cand, int n_users, int H, int Lq,
+                        cudaStream_t stream) {
+  if (!p || !d_map) return IKBO_ERR_INVALID_ARG;
+  if (n_cand < 1 || n_cand > p->max_cand || n_users < 1 || n_users > p->max_users || H < 1 || H > p->max_heads)
+    return IKBO_ERR_INVALID_ARG;
+  if (Lq < 8 || Lq > ATT_BM || Lq % 8 != 0) return IKBO_ERR_UNSUPPORTED;
+  const int cpt = ATT_BM / Lq;
+  SegParams sp;
+  sp.map = d_map;
+  sp.n_cand = n_cand;
+  sp.n_users = n_users;
+  sp.H = H;
+  sp.cands_per_unit = ATT_TILES * cpt;
+  sp.counts = p->d_counts;
+  sp.offsets = p->d_offsets;
+  sp.perm = p->d_perm;
+  sp.work = p->d_work;
+  sp.n_units = p->d_n_units;
+  sp.max_units = p->max_units;
+  sp.status = p->d_status;
+  if (launch_seg_build(sp, stream) != cudaSuccess) {
+    p->planned = false;
+    return IKBO_ERR_CUDA;
+  }
+  p->launches++;
+  p->planned = true;
+  p->d_map = d_map;
+  p->n_cand = n_cand;
+  p->n_users = n_users;
+  p->H = H;
+  p->Lq = Lq;
+  p->cands_per_unit = sp.cands_per_unit;
+  return IKBO_OK;
+}
+
+ikbo_status_t ikbo_plan_segments(ikbo_plan_t p, const int32_t** d_counts, const int32_t** d_offsets,
+                                 const int32_t** d_perm) {
+  if (!p) return IKBO_ERR_INVALID_ARG;
+  if (!p->planned) return IKBO_ERR_NOT_PLANNED;
+  if (d_counts) *d_counts = p->d_counts;
+  if (d_offsets) *d_offsets = p->d_offsets;
+  if (d_perm) *d_perm = p->d_perm;
+  return IKBO_OK;
+}
+
+ikbo_status_t ikbo_plan_worklist(ikbo_plan_t p, const int32_t** d_work, const int32_t** d_n_units,
+                                 int* cands_per_unit, int* max_units) {
+  if (!p) return IKBO_ERR_INVALID_ARG;
+  if (!p->planned) return IKBO_ERR_NOT_PLANNED;
+  if (d_work) *d_work = p->d_work;
+  if (d_n_units) *d_n_units = p->d_n_units;
+  if (cands_per_unit) *cands_per_unit = p->cands_per_unit;
+  if (max_units) *max_units = static_cast<int>(p->max_units);
+  return IKBO_OK;
+}
+
+ikbo_status_t ikbo_plan_get_status(ikbo_plan_t p, cudaStream_t stream) {
+  if (!p) return IKBO_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return IKBO_ERR_CUDA;
+  uint32_t word = 0;
+  if (cudaMemcpy(&word, p->d_status, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return IKBO_ERR_CUDA;
+  if (word && cudaMemset(p->d_status, 0, sizeof(uint32_t)) != cudaSuccess) return IKBO_ERR_CUDA;
+  if (word & DEV_ERR_MAP_RANGE) return IKBO_ERR_MAP_OUT_OF_RANGE;
+  if (word & (DEV_ERR_FLAG_TIMEOUT | DEV_ERR_PIPE_TIMEOUT)) return IKBO_ERR_TIMEOUT;
+  if (word & DEV_ERR_BAD_WORK) return IKBO_ERR_INTERNAL;
+  return IKBO_OK;
+}
+
+ikbo_status_t ikbo_lce_forward(ikbo_plan_t p, const void* U, const void* C, const void* Wu, const void* Wc,
+                               const void* b, void* Y, int K_u, int K_c, int D, int N, cudaStream_t stream) {
+  if (!p) return IKBO_ERR_INVALID_ARG;
+  if (!p->planned) return IKBO_ERR_NOT_PLANNED;
+  if (!U || !C || !Wu || !Wc || !Y) return IKBO_ERR_INVALID_ARG;
+  if (K_u < 1 || K_c < 1 || D < 1 || N < 1) return IKBO_ERR_UNSUPPORTED;
+  if (!aligned16(U) || !aligned16(C) || !aligned16(Wu) || !aligned16(Wc) || !aligned16(Y) || (b && !aligned16(b)))
+    return IKBO_ERR_INVALID_ARG;
+  if (D % 8 != 0 || N % 8 != 0 || N > 256) return IKBO_ERR_UNSUPPORTED;
+
+  LceParams lp;
+  std::memset(&lp, 0, sizeof(lp));
+  lp.map = p->d_map;
+  lp.bias = static_cast<const uint16_t*>(b);
+  lp.Y = static_cast<uint16_t*>(Y);
+  lp.n_cand = p->n_cand;
+  lp.n_users = p->n_users;
+  lp.K_u = K_u;
+  lp.K_c = K_c;
+  lp.D = D;
+  lp.N = N;
+  lp.N_mma = (N + 15) / 16 * 16;
+  lp.NB = (lp.N_mma + 63) / 64;
+  lp.n_dblk = (D + LCE_BM - 1) / LCE_BM;
+  lp.n_user_units = p->n_users * lp.n_dblk;
+  lp.n_units = (p->n_users + p->n_cand) * lp.n_dblk;
+  lp.kc_u = (K_u + LCE_BK - 1) / LCE_BK;
+  lp.kc_c = (K_c + LCE_BK - 1) / LCE_BK;
+  lp.ks_u = (K_u + 15) / 16;
+  lp.ks_c = (K_c + 15) / 16;
+  const int region_chunks = lp.kc_c < 2 ? 2 : lp.kc_c;
+  if (lp.kc_c * lp.NB > 16) return IKBO_ERR_UNSUPPORTED;
+  lp.w_region_bytes = static_cast<uint32_t>(region_chunks) * lp.NB * 64 * 64 * 2;
+  lp.w_slots = region_chunks < LCE_MAX_W_SLOTS ? region_chunks : LCE_MAX_W_SLOTS;
+  lp.stages = LCE_MAX_STAGES;
+  while (lp.stages > 2 && lce_smem_bytes(lp) > p->max_smem) --lp.stages;
+  if (lce_smem_bytes(lp) > p->max_smem) return IKBO_ERR_UNSUPPORTED;
+
+  const size_t part = static_cast<size_t>(p->n_users) * N * D;
+  const size_t nflags = static_cast<size_t>(p->n_users) * lp.n_dblk;
+  if (grow(&p->d_partial, &p->partial_elems, part) != cudaSuccess) return IKBO_ERR_CUDA;
+  if (grow(&p->d_flags, &p->flags_elems, nflags) != cudaSuccess) return IKBO_ERR_CUDA;
+  lp.partial = p->d_partial;
+  lp.flags = p->d_flags;
+  lp.status = p->d_status;
+  lp.timeout_epoch = p->d_status + 1;
+  lp.epoch = ++p->epoch;
+  if (lp.epoch == 0) lp.epoch = ++p->epoch;  // 0 is the flags' initial value
+  lp.debug = p->debug;
+  lp.timeout_ns = p->timeout_ns;
+
+  CUtensorMap tmU, tmC, tmWu, tmWc;
+  const uint64_t ud[3] = {static_cast<uint64_t>(D), static_cast<uint64_t>(K_u), static_cast<uint64_t>(p->n_users)};
+  const uint64_t us[2] = {static_cast<uint64_t>(D) * 2, static_cast<uint64_t>(K_u) * D * 2};
+  const uint64_t cd[3] = {static_cast<uint64_t>(D), static_cast<uint64_t>(K_c), static_cast<uint64_t>(p->n_cand)};
+  const uint64_t cs[2] = {static_cast<uint64_t>(D) * 2, static_cast<uint64_t>(K_c) * D * 2};
+  const uint32_t abox[3] = {64, LCE_BK, 1};
+  const uint64_t wud[2] = {static_cast<uint64_t>(N), static_cast<uint64_t>(K_u)};
+  const uint64_t wcd[2] = {static_cast<uint64_t>(N), static_cast<uint64_t>(K_c)};
+  const uint64_t ws[1] = {static_cast<uint64_t>(N) * 2};
+  const uint32_t wbox[2] = {64, LCE_BK};
+  if (!encode_bf16(&tmU, U, 3, ud, us, abox) || !encode_bf16(&tmC, C, 3, cd, cs, abox) ||
+      !encode_bf16(&tmWu, Wu, 2, wud, ws, wbox) || !encode_bf16(&tmWc, Wc, 2, wcd, ws, wbox))
+    return IKBO_ERR_CUDA;
+
+  const int grid = lp.n_units < p->num_sms ? lp.n_units : p->num_sms;
+  if (launch_lce(tmU, tmC, tmWu, tmWc, lp, grid, stream) != cudaSuccess) return IKBO_ERR_CUDA;
+  p->launches++;
+  return IKBO_OK;
+}
+
+ikbo_status_t ikbo_attn_forward(ikbo_plan_t p, const void* Q, const void* K, const void* V,
+                                const int32_t* d_kv_offsets, void* O, int Lkv, int d, float scale,
+                                cudaStream_t stream) {
+  if (!p) return IKBO_ERR_INVALID_ARG;
+  if (!p->planned) return IKBO_ERR_NOT_PLANNED;
+  if (!Q || !K || !V || !O) return IKBO_ERR_INVALID_ARG;
+  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O)) return IKBO_ERR_INVALID_ARG;
+  if (d != ATT_D) return IKBO_ERR_UNSUPPORTED;
+  if (Lkv < 1 || !(scale > 0.f) || !std::isfinite(scale)) return IKBO_ERR_INVALID_ARG;
+  if (attn_smem_bytes() > p->max_smem) return IKBO_ERR_UNSUPPORTED;
+
+  AttnParams ap;
+  std::memset(&ap, 0, sizeof(ap));
+  ap.perm = p->d_perm;
+  ap.work = p->d_work;
+  ap.n_units = p->d_n_units;
+  ap.kv_offsets = d_kv_offsets;
+  ap.O = static_cast<uint16_t*>(O);
+  ap.status = p->d_status;
+  ap.n_cand = p->n_cand;
+  ap.n_users = p->n_users;
+  ap.H = p->H;
+  ap.Lq = p->Lq;
+  ap.Lkv = Lkv;
+  ap.cands_per_tile = ATT_BM / p->Lq;
+  ap.scale_log2 = scale * 1.4426950408889634f;
+  ap.timeout_ns = p->timeout_ns;
+
+  const uint64_t H = static_cast<uint64_t>(p->H), Lq = static_cast<uint64_t>(p->Lq);
+  CUtensorMap tmQ, tmK, tmV;
+  const uint64_t qd[4] = {ATT_D, Lq, H, static_cast<uint64_t>(p->n_cand)};
+  const uint64_t qs[3] = {ATT_D * 2, Lq * ATT_D * 2, H * Lq * ATT_D * 2};
+  const uint32_t qbox[4] = {64, static_cast<uint32_t>(p->Lq), 1, 1};
+  if (!encode_bf16(&tmQ, Q, 4, qd, qs, qbox)) return IKBO_ERR_CUDA;
+  if (d_kv_offsets) {
+    const uint64_t kd[3] = {ATT_D, H, static_cast<uint64_t>(Lkv)};
+    const uint64_t ks[2] = {ATT_D * 2, H * ATT_D * 2};
+    const uint32_t kbox[3] = {64, 1, ATT_BN};
+    if (!encode_bf16(&tmK, K, 3, kd, ks, kbox) || !encode_bf16(&tmV, V, 3, kd, ks, kbox)) return IKBO_ERR_CUDA;
+  } else {
+    const uint64_t L = static_cast<uint64_t>(Lkv);
+    const uint64_t kd[4] = {ATT_D, L, H, static_cast<uint64_t>(p->n_users)};
+    const uint64_t ks[3] = {ATT_D * 2, L * ATT_D * 2, H * L * ATT_D * 2};
+    const uint32_t kbox[4] = {64, ATT_BN, 1, 1};
+    if (!encode_bf16(&tmK, K, 4, kd, ks, kbox) || !encode_bf16(&tmV, V, 4, kd, ks, kbox)) return IKBO_ERR_CUDA;
+  }
+  if (launch_attn(tmQ, tmK, tmV, ap, p->num_sms, stream) != cudaSuccess) return IKBO_ERR_CUDA;
+  p->launches++;
+  return IKBO_OK;
+}
+
+}  // extern "C"

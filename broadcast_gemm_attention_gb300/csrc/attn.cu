@@ -1,0 +1,442 @@
+// attn.cu -- broadcast FlashAttention for sm_103a.
+//
+// O[i,h] = softmax(Q[i,h] K[map[i],h]^T * scale) V[map[i],h]
+//
+// IKBO attention (aixai.ru, "Deep Dive: Flash Attention"): candidates that
+// share a user share that user's K/V, so a kernel that keeps a user's K/V
+// tiles on chip and runs all of the user's candidates' queries against them
+// turns the operator from IO-bound into compute-bound.  The pages reorder the
+// launch grid (candidate index before heads) so that CTAs of one user run at
+// the same time; here the grouping is explicit: a work unit is one (user,
+// head) and up to 2 x floor(128 / Lq) of that user's candidates (from the
+// segment builder's perm), i.e. two 128-row query tiles that read every K/V
+// tile once from shared memory.  Units of the same (user, head) are adjacent
+// in the work list, so neighbouring CTAs stream the same K/V through L2.
+//
+// Per CTA (persistent, one per SM):
+//   warp 0      TMA producer: Q tiles (one box per candidate and d-half,
+//               gathered through perm), K/V tiles through a 4-stage ring
+//   warp 1      MMA issuer: S_t = Q_t K^T (SS), O_t += P_t V (TS: P in TMEM)
+//   warp 2      TMEM owner (512 columns: S0 S1 O0 O1, 128 each)
+//   warps 4-7   softmax + epilogue of query tile 0 (one thread per row)
+//   warps 8-11  softmax + epilogue of query tile 1
+// Online softmax in fp32 in the log2 domain (exp2 with scale*log2(e) folded
+// in); the running max is only moved when it grows by more than 2^8, so O is
+// rescaled rarely (the result is the same: O and l share the reference max).
+// P is rounded to bf16 and written over the first 64 columns of S.
+#include <cuda_bf16.h>
+
+#include "ikbo_internal.h"
+#include "ptx.cuh"
+
+namespace ikbo {
+
+namespace {
+
+constexpr uint32_t HALF_TILE = ATT_BM * 64 * 2;  // 128 rows x 64 bf16 = 16 KB
+constexpr float RESCALE_THRESHOLD = 8.0f;          // log2 units
+
+struct AttSmem {
+  uint8_t* q;      // 2 tiles x 32 KB
+  uint8_t* kv;     // ATT_STAGES x 32 KB
+  uint64_t* q_full;
+  uint64_t* q_empty;
+  uint64_t* kv_full;
+  uint64_t* kv_empty;
+  uint64_t* s_full;   // [2]
+  uint64_t* p_full;   // [2]
+  uint64_t* o_full;   // [2]
+  uint64_t* o_empty;  // [2]
+  uint32_t* tmem_slot;
+  uint32_t* abort;
+};
+
+__device__ __forceinline__ AttSmem carve(uint8_t* base) {
+  AttSmem s;
+  s.q = base;
+  s.kv = base + ATT_TILES * ATT_Q_TILE_BYTES;
+  uint64_t* b = reinterpret_cast<uint64_t*>(s.kv + ATT_STAGES * ATT_KV_STAGE_BYTES);
+  s.q_full = b;
+  s.q_empty = b + 1;
+  s.kv_full = b + 2;
+  s.kv_empty = s.kv_full + ATT_STAGES;
+  s.s_full = s.kv_empty + ATT_STAGES;
+  s.p_full = s.s_full + 2;
+  s.o_full = s.p_full + 2;
+  s.o_empty = s.o_full + 2;
+  s.tmem_slot = reinterpret_cast<uint32_t*>(s.o_empty + 2);
+  s.abort = s.tmem_slot + 1;
+  return s;
+}
+
+struct Unit {
+  int u, h, start, cnt;
+  int ntq;     // query tiles in use (0 = skip the unit)
+  int L;       // keys of this user
+  int kv0;     // first packed row (jagged) or 0
+  int ntiles;  // ceil(L / 128)
+};
+
+__device__ __forceinline__ Unit decode(const AttnParams& p, int unit) {
+  const int4 w = reinterpret_cast<const int4*>(p.work)[unit];
+  Unit x;
+  x.u = w.x;
+  x.h = w.y;
+  x.start = w.z;
+  x.cnt = w.w;
+  const int cap = 2 * p.cands_per_tile;
+  const bool ok = x.u >= 0 && x.u < p.n_users && x.h >= 0 && x.h < p.H && x.cnt >= 1 && x.cnt <= cap &&
+                  x.start >= 0 && x.start + x.cnt <= p.n_cand;
+  if (!ok) {
+    x.ntq = 0;
+    x.L = 0;
+    x.kv0 = 0;
+    x.ntiles = 0;
+    return x;
+  }
+  x.ntq = x.cnt > p.cands_per_tile ? 2 : 1;
+  if (p.kv_offsets) {
+    x.kv0 = p.kv_offsets[x.u];
+    x.L = p.kv_offsets[x.u + 1] - x.kv0;
+    if (x.L < 0) x.L = 0;
+  } else {
+    x.kv0 = 0;
+    x.L = p.Lkv;
+  }
+  x.ntiles = (x.L + ATT_BN - 1) / ATT_BN;
+  return x;
+}
+
+// ------------------------------------------------------------ producer
+__device__ void att_producer(const AttnParams& p, const AttSmem& s, const CUtensorMap* tmQ, const CUtensorMap* tmK,
+                             const CUtensorMap* tmV, int n_units) {
+  int stage = 0;
+  uint32_t phase = 0;
+  uint32_t q_uses = 0;
+  const int cpt = p.cands_per_tile;
+  for (int unit = blockIdx.x; unit < n_units; unit += gridDim.x) {
+    const Unit x = decode(p, unit);
+    if (x.ntq == 0) {
+      atomicOr(p.status, DEV_ERR_BAD_WORK);
+      continue;
+    }
+    if (x.ntiles == 0) continue;
+    if (!mbar_wait(s.q_empty, (q_uses & 1u) ^ 1u, s.abort, p.timeout_ns, 1)) return;
+    ++q_uses;
+    mbar_arrive_expect_tx(s.q_full, static_cast<uint32_t>(x.ntq * cpt * p.Lq * ATT_D * 2));
+    for (int t = 0; t < x.ntq; ++t) {
+      for (int j = 0; j < cpt; ++j) {
+        const int slot = t * cpt + j;
+        // empty slots read one past the last candidate: TMA fills them with zeros
+        const int cand = slot < x.cnt ? p.perm[x.start + slot] : p.n_cand;
+        uint8_t* dst = s.q + t * ATT_Q_TILE_BYTES + j * p.Lq * 128;
+        tma_load_4d(dst, tmQ, s.q_full, 0, 0, x.h, cand);
+        tma_load_4d(dst + HALF_TILE, tmQ, s.q_full, 64, 0, x.h, cand);
+      }
+    }
+    for (int jt = 0; jt < x.ntiles; ++jt) {
+      for (int kv = 0; kv < 2; ++kv) {
+        if (!mbar_wait(&s.kv_empty[stage], phase ^ 1u, s.abort, p.timeout_ns, 1)) return;
+        mbar_arrive_expect_tx(&s.kv_full[stage], ATT_KV_STAGE_BYTES);
+        uint8_t* dst = s.kv + stage * ATT_KV_STAGE_BYTES;
+        const CUtensorMap* tm = kv == 0 ? tmK : tmV;
+        if (p.kv_offsets) {
+          tma_load_3d(dst, tm, &s.kv_full[stage], 0, x.h, x.kv0 + jt * ATT_BN);
+          tma_load_3d(dst + HALF_TILE, tm, &s.kv_full[stage], 64, x.h, x.kv0 + jt * ATT_BN);
+        } else {
+          tma_load_4d(dst, tm, &s.kv_full[stage], 0, jt * ATT_BN, x.h, x.u);
+          tma_load_4d(dst + HALF_TILE, tm, &s.kv_full[stage], 64, jt * ATT_BN, x.h, x.u);
+        }
+        if (++stage == ATT_STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+  }
+}
+
+// ----------------------------------------------------------------- MMA
+// S_t = Q_t K^T: A = Q tile (K-major, 128 x 128), B = K tile (K-major).
+// The d = 128 reduction is 8 steps of 16: steps 0-3 in the first 64-wide
+// half (32-byte advances inside the swizzled row), 4-7 in the second.
+__device__ __forceinline__ void issue_qk(uint32_t s_tmem, uint32_t q_base, uint32_t k_base) {
+  constexpr uint32_t idesc = idesc_bf16_f32(ATT_BM, ATT_BN, false, false);
+#pragma unroll
+  for (int ks = 0; ks < 8; ++ks) {
+    const uint32_t off = (ks >> 2) * HALF_TILE + (ks & 3) * 32;
+    mma_bf16_ss(s_tmem, sdesc_sw128(q_base + off, 16, 1024), sdesc_sw128(k_base + off, 16, 1024), idesc,
+                ks > 0 ? 1u : 0u);
+  }
+}
+
+// O_t += P_t V: A = P (TMEM, 128 rows x 128 keys as 64 packed columns), B =
+// V tile (MN-major: d contiguous; 64-wide d halves one HALF_TILE apart, 8 key
+// rows per 1024-byte atom).  16 keys per step = 8 TMEM columns of P.
+__device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint32_t v_base, bool accumulate) {
+  constexpr uint32_t idesc = idesc_bf16_f32(ATT_BM, ATT_D, false, true);
+#pragma unroll
+  for (int ks = 0; ks < 8; ++ks) {
+    mma_bf16_ts(o_tmem, p_tmem + ks * 8, sdesc_sw128(v_base + ks * 2048, HALF_TILE, 1024), idesc,
+                (accumulate || ks > 0) ? 1u : 0u);
+  }
+}
+
+__device__ void att_mma(const AttnParams& p, const AttSmem& s, uint32_t tmem, int n_units) {
+  int stage = 0;
+  uint32_t phase = 0;
+  uint32_t q_uses = 0;
+  uint32_t p_uses[2] = {0, 0};
+  uint32_t o_uses[2] = {0, 0};
+  const uint32_t q_base0 = smem_u32(s.q);
+  for (int unit = blockIdx.x; unit < n_units; unit += gridDim.x) {
+    const Unit x = decode(p, unit);
+    if (x.ntq == 0 || x.ntiles == 0) continue;
+    if (!mbar_wait(s.q_full, q_uses & 1u, s.abort, p.timeout_ns, 1)) return;
+    ++q_uses;
+    // first K tile
+    int k_stage = stage;
+    if (!mbar_wait(&s.kv_full[k_stage], phase, s.abort, p.timeout_ns, 1)) return;
+    if (++stage == ATT_STAGES) {
+      stage = 0;
+      phase ^= 1u;
+    }
+    tc_fence_after();
+    for (int t = 0; t < x.ntq; ++t) {
+      issue_qk(tmem + t * 128, q_base0 + t * ATT_Q_TILE_BYTES, smem_u32(s.kv + k_stage * ATT_KV_STAGE_BYTES));
+      mma_commit(&s.s_full[t]);
+    }
+    mma_commit(&s.kv_empty[k_stage]);
+    for (int jt = 0; jt < x.ntiles; ++jt) {
+      const int v_stage = stage;
+      if (!mbar_wait(&s.kv_full[v_stage], phase, s.abort, p.timeout_ns, 1)) return;
+      if (++stage == ATT_STAGES) {
+        stage = 0;
+        phase ^= 1u;
+      }
+      const bool has_next = jt + 1 < x.ntiles;
+      if (has_next) {
+        k_stage = stage;
+        if (!mbar_wait(&s.kv_full[k_stage], phase, s.abort, p.timeout_ns, 1)) return;
+        if (++stage == ATT_STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      const uint32_t v_base = smem_u32(s.kv + v_stage * ATT_KV_STAGE_BYTES);
+      const uint32_t k_base = smem_u32(s.kv + k_stage * ATT_KV_STAGE_BYTES);
+      for (int t = 0; t < x.ntq; ++t) {
+        if (!mbar_wait(&s.p_full[t], p_uses[t] & 1u, s.abort, p.timeout_ns, 1)) return;
+        ++p_uses[t];
+        if (jt == 0) {
+          // the previous unit's epilogue must be done reading O_t
+          if (!mbar_wait(&s.o_empty[t], (o_uses[t] & 1u) ^ 1u, s.abort, p.timeout_ns, 1)) return;
+        }
+        tc_fence_after();
+        issue_pv(tmem + 256 + t * 128, tmem + t * 128, v_base, jt > 0);
+        if (!has_next) {
+          mma_commit(&s.o_full[t]);
+          ++o_uses[t];
+        } else {
+          issue_qk(tmem + t * 128, q_base0 + t * ATT_Q_TILE_BYTES, k_base);
+          mma_commit(&s.s_full[t]);
+        }
+      }
+      mma_commit(&s.kv_empty[v_stage]);
+      if (has_next) mma_commit(&s.kv_empty[k_stage]);
+    }
+    mma_commit(s.q_empty);
+  }
+}
+
+// ---------------------------------------------------- softmax + epilogue
+__device__ void att_softmax(const AttnParams& p, const AttSmem& s, uint32_t tmem, int n_units) {
+  const int warp = threadIdx.x >> 5;
+  const int wg = (warp - 4) >> 2;                       // query tile 0 or 1
+  const int r = ((warp & 3) << 5) + static_cast<int>(lane_id());  // row = TMEM lane
+  const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+  const uint32_t S = tmem + lane_base + wg * 128;
+  const uint32_t Ot = tmem + lane_base + 256 + wg * 128;
+  const int cpt = p.cands_per_tile;
+  const float sl = p.scale_log2;
+  uint32_t s_uses = 0, o_uses = 0;
+
+  for (int unit = blockIdx.x; unit < n_units; unit += gridDim.x) {
+    const Unit x = decode(p, unit);
+    if (x.ntq <= wg) continue;
+    const int slot = wg * cpt + r / p.Lq;
+    const int q = r % p.Lq;
+    const bool row_valid = r < cpt * p.Lq && slot < x.cnt;
+    __nv_bfloat16* orow = nullptr;
+    if (row_valid) {
+      const int cand = p.perm[x.start + slot];
+      orow = reinterpret_cast<__nv_bfloat16*>(p.O) + ((static_cast<size_t>(cand) * p.H + x.h) * p.Lq + q) * ATT_D;
+    }
+    if (x.ntiles == 0) {  // empty key range: O = 0
+      if (row_valid) {
+        uint4 z = make_uint4(0, 0, 0, 0);
+        for (int c = 0; c < ATT_D / 8; ++c) reinterpret_cast<uint4*>(orow)[c] = z;
+      }
+      continue;
+    }
+    float m = -INFINITY, l = 0.f;
+    for (int jt = 0; jt < x.ntiles; ++jt) {
+      if (!mbar_wait(&s.s_full[wg], s_uses & 1u, s.abort, p.timeout_ns, 1)) return;
+      ++s_uses;
+      tc_fence_after();
+      const int ncols = min(ATT_BN, x.L - jt * ATT_BN);
+      // pass 1: row max of this tile
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t v[32];
+        tmem_ld32(S + c * 32, v);
+        tmem_ld_wait(v);
+        if (ncols >= (c + 1) * 32) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) mx = fmaxf(mx, __uint_as_float(v[j]));
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (c * 32 + j < ncols) mx = fmaxf(mx, __uint_as_float(v[j]));
+        }
+      }
+      const float m_new = fmaxf(m, mx * sl);
+      if (m_new > m + RESCALE_THRESHOLD) {
+        const float alpha = ex2(m - m_new);  // 0 on the first tile
+        l *= alpha;
+        if (jt > 0) {
+          // PV of the previous tile has completed (it was committed before this S)
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t v[32];
+            tmem_ld32(Ot + c * 32, v);
+            tmem_ld_wait(v);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * alpha);
+            tmem_st32(Ot + c * 32, v);
+          }
+          tmem_st_wait();
+        }
+        m = m_new;
+      }
+      // pass 2: p = 2^(s*sl - m), rounded to bf16, packed over S columns [0, 64)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t v[32];
+        tmem_ld32(S + c * 32, v);
+        tmem_ld_wait(v);
+        uint32_t pk[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int col = c * 32 + 2 * j;
+          const float p0 = col < ncols ? ex2(fmaf(__uint_as_float(v[2 * j]), sl, -m)) : 0.f;
+          const float p1 = col + 1 < ncols ? ex2(fmaf(__uint_as_float(v[2 * j + 1]), sl, -m)) : 0.f;
+          l += p0 + p1;
+          pk[j] = pack_bf16x2(p0, p1);
+        }
+        tmem_st16(S + c * 16, pk);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&s.p_full[wg]);
+    }
+    // epilogue: O / l -> bf16 -> O[cand, h, q, :]
+    if (!mbar_wait(&s.o_full[wg], o_uses & 1u, s.abort, p.timeout_ns, 1)) return;
+    ++o_uses;
+    tc_fence_after();
+    const float inv = l > 0.f ? 1.0f / l : 0.f;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      uint32_t v[32];
+      tmem_ld32(Ot + c * 32, v);
+      tmem_ld_wait(v);
+      if (row_valid) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          pk[j] = pack_bf16x2(__uint_as_float(v[2 * j]) * inv, __uint_as_float(v[2 * j + 1]) * inv);
+        uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) dst[k] = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+      }
+    }
+    tc_fence_before();
+    mbar_arrive(&s.o_empty[wg]);
+  }
+}
+
+__global__ void __launch_bounds__(ATT_THREADS, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const AttSmem s = carve(base);
+  const int warp = threadIdx.x >> 5;
+  const int n_units = *p.n_units;
+
+  if (threadIdx.x == 0) {
+    mbar_init(s.q_full, 1);
+    mbar_init(s.q_empty, 1);
+    for (int i = 0; i < ATT_STAGES; ++i) {
+      mbar_init(&s.kv_full[i], 1);
+      mbar_init(&s.kv_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s.s_full[i], 1);
+      mbar_init(&s.p_full[i], 128);
+      mbar_init(&s.o_full[i], 1);
+      mbar_init(&s.o_empty[i], 128);
+    }
+    *s.abort = 0;
+    fence_barrier_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == 0 && lane_id() == 0) {
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+  }
+  if (warp == 2) {
+    tmem_alloc(s.tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *s.tmem_slot;
+
+  if (warp == 0) {
+    if (lane_id() == 0) att_producer(p, s, &tmQ, &tmK, &tmV, n_units);
+  } else if (warp == 1) {
+    if (lane_id() == 0) att_mma(p, s, tmem, n_units);
+  } else if (warp >= 4) {
+    att_softmax(p, s, tmem, n_units);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (*s.abort && threadIdx.x == 0) atomicOr(p.status, DEV_ERR_PIPE_TIMEOUT);
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace
+
+size_t attn_smem_bytes() {
+  return 1024 + ATT_TILES * ATT_Q_TILE_BYTES + ATT_STAGES * ATT_KV_STAGE_BYTES + 256;
+}
+
+cudaError_t launch_attn(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV, const AttnParams& p,
+                        int grid, cudaStream_t s) {
+  const size_t smem = attn_smem_bytes();
+  cudaError_t e =
+      cudaFuncSetAttribute(attn_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  attn_fwd_kernel<<<grid, ATT_THREADS, smem, s>>>(tmQ, tmK, tmV, p);
+  return cudaGetLastError();
+}
+
+}  // namespace ikbo

@@ -1,0 +1,99 @@
+// ikbo_internal.h -- kernel parameter blocks, tile constants and the device
+// status word shared by the kernels (seg.cu, lce.cu, attn.cu) and the host
+// API (api.cu).  Not part of the public ABI (include/ikbo.h is).
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace ikbo {
+
+// ----------------------------------------------------------- status word
+// One uint32 in device memory per plan; kernels OR these bits in, the host
+// reads and clears it in ikbo_plan_get_status.
+enum : uint32_t {
+  DEV_ERR_MAP_RANGE = 1u << 0,     // a map entry outside [0, n_users)
+  DEV_ERR_FLAG_TIMEOUT = 1u << 1,  // an LCE user partial never became ready
+  DEV_ERR_PIPE_TIMEOUT = 1u << 2,  // an mbarrier wait inside a kernel ran out
+  DEV_ERR_BAD_WORK = 1u << 3,      // inconsistent attention work unit
+};
+
+// Debug switches (ikbo_plan_set_debug).
+enum : uint32_t {
+  DEBUG_WITHHOLD_USER_PARTIAL = 1u << 0,  // LCE: never publish user partials
+};
+
+// ------------------------------------------------------------ segments
+constexpr int SEG_THREADS = 1024;
+constexpr int SEG_MAX_USERS = 8192;
+
+struct SegParams {
+  const int32_t* map;
+  int n_cand, n_users, H, cands_per_unit;
+  int32_t* counts;    // [n_users]
+  int32_t* offsets;   // [n_users + 1]
+  int32_t* perm;      // [n_cand]
+  int32_t* work;      // [max_units][4]
+  int32_t* n_units;   // [1]
+  int64_t max_units;
+  uint32_t* status;
+};
+
+// ----------------------------------------------------------------- LCE
+// Tiles: M = 128 rows of D (TMEM lanes), N = N_mma columns (<= 256), K in
+// chunks of 64 (one 128-byte swizzle row per k when MN-major).
+constexpr int LCE_BM = 128;
+constexpr int LCE_BK = 64;
+constexpr int LCE_THREADS = 256;            // warp 0 TMA, 1 MMA, 2 TMEM, 3 idle, 4-7 epilogue
+constexpr int LCE_A_STAGE_BYTES = LCE_BM * LCE_BK * 2;   // 16 KB: two 64(d) x 64(k) boxes
+constexpr int LCE_MAX_STAGES = 8;
+constexpr int LCE_MAX_W_SLOTS = 8;
+
+struct LceParams {
+  const int32_t* map;
+  const uint16_t* bias;   // [N] bf16 or null
+  uint16_t* Y;            // [n_cand][N][D] bf16
+  float* partial;         // [n_users][N][D] fp32 workspace (user GEMM + bias)
+  uint32_t* flags;        // [n_users][n_dblk] readiness epochs
+  uint32_t* status;
+  uint32_t* timeout_epoch;  // set to `epoch` by the first flag wait that times out in a launch
+  int n_cand, n_users, K_u, K_c, D, N;
+  int N_mma;              // N rounded up to 16
+  int NB;                 // 64-wide column blocks of W (ceil(N_mma / 64))
+  int n_dblk;             // ceil(D / 128)
+  int n_user_units;       // n_users * n_dblk
+  int n_units;            // (n_users + n_cand) * n_dblk
+  int kc_u, kc_c;         // 64-wide K chunks (ceil(K / 64))
+  int ks_u, ks_c;         // 16-wide MMA k-steps (ceil(K / 16))
+  int stages;             // A ring depth
+  int w_slots;            // B-chunk slots in the W region used by user tiles (2..8)
+  uint32_t w_region_bytes;
+  uint32_t epoch;         // value written to / awaited in `flags`
+  uint32_t debug;
+  uint64_t timeout_ns;
+};
+
+// ----------------------------------------------------------- attention
+constexpr int ATT_BM = 128;        // query rows per tile (TMEM lanes)
+constexpr int ATT_BN = 128;        // keys per K/V tile
+constexpr int ATT_D = 128;         // head dim (the only one supported)
+constexpr int ATT_TILES = 2;       // query tiles per work unit (share K/V)
+constexpr int ATT_THREADS = 384;   // warp 0 TMA, 1 MMA, 2 TMEM, 3 idle, 4-7 / 8-11 softmax
+constexpr int ATT_KV_STAGE_BYTES = ATT_BN * ATT_D * 2;   // 32 KB
+constexpr int ATT_Q_TILE_BYTES = ATT_BM * ATT_D * 2;     // 32 KB
+constexpr int ATT_STAGES = 4;
+
+struct AttnParams {
+  const int32_t* perm;
+  const int32_t* work;       // [n_units][4]: user, head, perm start, count
+  const int32_t* n_units;    // device scalar written by the segment builder
+  const int32_t* kv_offsets; // [n_users+1] or null (dense)
+  uint16_t* O;               // [n_cand][H][Lq][d]
+  uint32_t* status;
+  int n_cand, n_users, H, Lq, Lkv;  // Lkv: dense length (ignored when jagged)
+  int cands_per_tile;        // floor(128 / Lq)
+  float scale_log2;          // scale * log2(e)
+  uint64_t timeout_ns;
+};
+
+}  // namespace ikbo

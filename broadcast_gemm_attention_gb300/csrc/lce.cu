@@ -1,0 +1,392 @@
+// lce.cu -- fused Linear Compression Embedding with in-kernel broadcast.
+//
+// Y[i][n][d] = sum_k Wc[k][n] C[i][k][d] + P[map[i]][n][d],
+// P[u][n][d] = b[n] + sum_k Wu[k][n] U[u][k][d].
+//
+// This is the four-stage IKBO LCE of aixai.ru, "Deep Dive: Linear
+// Compression" (and "Meta Optimizes Inference for Recommendation Systems",
+// LCE case), rebuilt for sm_103a:
+//   stage 1, split along K: the user GEMM runs at n_users, the candidate GEMM
+//     at n_cand; only the small user result P is broadcast;
+//   stage 2, K padding: K is padded with zeros to the MMA step, but only in
+//     shared memory -- TMA fills the out-of-bounds rows of both operands with
+//     zeros, so no padded copy of any tensor exists;
+//   stage 3, broadcast-add in the candidate GEMM's epilogue: the epilogue
+//     reads P[map[i]] by index and adds it in registers; Y is written once;
+//   stage 4, one persistent warp-specialised launch: user tiles and candidate
+//     tiles share the launch, user tiles first in every CTA's static order,
+//     and a candidate epilogue acquires the release flag of its user tile.
+//
+// Per CTA (one per SM, all co-resident: cooperative launch):
+//   warp 0  TMA producer   (A ring: U[u] or C[i] chunks; W chunks / resident Wc)
+//   warp 1  MMA issuer     (tcgen05.mma, fp32 accumulators in TMEM, 2 buffers)
+//   warp 2  TMEM owner     (alloc / dealloc of 512 columns)
+//   warps 4-7  epilogue    (tcgen05.ld, + P or + b, bf16 or fp32 stores)
+//
+// Tile: 128 rows of D (TMEM lanes) x N_mma columns (N rounded up to 16) of
+// one candidate (or user).  Operands are MN-major (D and N are the contiguous
+// dimensions in memory), staged by TMA with 128-byte swizzle: a box of 64
+// elements along D (or N) by 64 k rows, 8 KB.
+#include <cuda_bf16.h>
+
+#include "ikbo_internal.h"
+#include "ptx.cuh"
+
+namespace ikbo {
+
+namespace {
+
+constexpr uint32_t BOX_BYTES = 64 * 64 * 2;  // one 64 x 64 bf16 box
+
+struct LceSmem {
+  uint8_t* w_region;
+  uint8_t* a_ring;
+  uint64_t* a_full;
+  uint64_t* a_empty;
+  uint64_t* w_full;
+  uint64_t* w_empty;
+  uint64_t* wc_full;
+  uint64_t* acc_full;
+  uint64_t* acc_empty;
+  uint64_t* pub;  // the 128 epilogue threads finished writing a user partial
+  uint32_t* tmem_slot;
+  uint32_t* abort;
+};
+
+__device__ __forceinline__ LceSmem carve(uint8_t* base, const LceParams& p) {
+  LceSmem s;
+  s.w_region = base;
+  s.a_ring = base + p.w_region_bytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(s.a_ring + static_cast<size_t>(p.stages) * LCE_A_STAGE_BYTES);
+  s.a_full = bars;
+  s.a_empty = s.a_full + p.stages;
+  s.w_full = s.a_empty + p.stages;
+  s.w_empty = s.w_full + p.w_slots;
+  s.wc_full = s.w_empty + p.w_slots;
+  s.acc_full = s.wc_full + 1;
+  s.acc_empty = s.acc_full + 2;
+  s.pub = s.acc_empty + 2;
+  s.tmem_slot = reinterpret_cast<uint32_t*>(s.pub + 1);
+  s.abort = s.tmem_slot + 1;
+  return s;
+}
+
+struct UnitInfo {
+  bool is_user;
+  int row;   // user u or candidate i
+  int dblk;  // 128-row block of D
+};
+
+__device__ __forceinline__ UnitInfo unit_info(const LceParams& p, int unit) {
+  UnitInfo x;
+  x.is_user = unit < p.n_user_units;
+  const int idx = x.is_user ? unit : unit - p.n_user_units;
+  x.row = idx / p.n_dblk;
+  x.dblk = idx - x.row * p.n_dblk;
+  return x;
+}
+
+// ------------------------------------------------------------ producer
+__device__ void lce_producer(const LceParams& p, const LceSmem& s, const CUtensorMap* tmU, const CUtensorMap* tmC,
+                             const CUtensorMap* tmWu, const CUtensorMap* tmWc) {
+  int stage = 0;
+  uint32_t a_phase = 0;
+  int wslot = 0;
+  uint32_t w_phase = 0;
+  uint32_t w_uses[LCE_MAX_W_SLOTS] = {0, 0, 0, 0, 0, 0, 0, 0};
+  bool wc_loaded = false;
+  const uint32_t w_chunk_bytes = static_cast<uint32_t>(p.NB) * BOX_BYTES;
+
+  for (int unit = blockIdx.x; unit < p.n_units; unit += gridDim.x) {
+    const UnitInfo x = unit_info(p, unit);
+    const CUtensorMap* tmA = x.is_user ? tmU : tmC;
+    const int kc_n = x.is_user ? p.kc_u : p.kc_c;
+    const int d0 = x.dblk * LCE_BM;
+    if (!x.is_user && !wc_loaded) {
+      // every W slot used by the user phase must be drained before Wc lands
+      for (int w = 0; w < p.w_slots; ++w)
+        if (w_uses[w] > 0 && !mbar_wait(&s.w_empty[w], (w_uses[w] - 1) & 1u, s.abort, p.timeout_ns, 1)) return;
+      mbar_arrive_expect_tx(s.wc_full, static_cast<uint32_t>(p.kc_c) * w_chunk_bytes);
+      for (int kc = 0; kc < p.kc_c; ++kc)
+        for (int nb = 0; nb < p.NB; ++nb)
+          tma_load_2d(s.w_region + (static_cast<size_t>(kc) * p.NB + nb) * BOX_BYTES, tmWc, s.wc_full, nb * 64,
+                      kc * LCE_BK);
+      wc_loaded = true;
+    }
+    for (int kc = 0; kc < kc_n; ++kc) {
+      if (!mbar_wait(&s.a_empty[stage], a_phase ^ 1u, s.abort, p.timeout_ns, 1)) return;
+      uint8_t* dst = s.a_ring + static_cast<size_t>(stage) * LCE_A_STAGE_BYTES;
+      mbar_arrive_expect_tx(&s.a_full[stage], LCE_A_STAGE_BYTES);
+      tma_load_3d(dst, tmA, &s.a_full[stage], d0, kc * LCE_BK, x.row);
+      tma_load_3d(dst + BOX_BYTES, tmA, &s.a_full[stage], d0 + 64, kc * LCE_BK, x.row);
+      if (x.is_user) {
+        if (!mbar_wait(&s.w_empty[wslot], w_phase ^ 1u, s.abort, p.timeout_ns, 1)) return;
+        mbar_arrive_expect_tx(&s.w_full[wslot], w_chunk_bytes);
+        uint8_t* wdst = s.w_region + static_cast<size_t>(wslot) * w_chunk_bytes;
+        for (int nb = 0; nb < p.NB; ++nb)
+          tma_load_2d(wdst + static_cast<size_t>(nb) * BOX_BYTES, tmWu, &s.w_full[wslot], nb * 64, kc * LCE_BK);
+        w_uses[wslot] += 1;
+        if (++wslot == p.w_slots) {
+          wslot = 0;
+          w_phase ^= 1u;
+        }
+      }
+      if (++stage == p.stages) {
+        stage = 0;
+        a_phase ^= 1u;
+      }
+    }
+  }
+}
+
+// ----------------------------------------------------------------- MMA
+__device__ void lce_mma(const LceParams& p, const LceSmem& s, uint32_t tmem) {
+  const uint32_t idesc = idesc_bf16_f32(LCE_BM, static_cast<uint32_t>(p.N_mma), true, true);
+  const uint32_t w_chunk_bytes = static_cast<uint32_t>(p.NB) * BOX_BYTES;
+  int stage = 0;
+  uint32_t a_phase = 0;
+  int wslot = 0;
+  uint32_t w_phase = 0;
+  bool wc_ready = false;
+  int local = 0;
+  for (int unit = blockIdx.x; unit < p.n_units; unit += gridDim.x, ++local) {
+    const UnitInfo x = unit_info(p, unit);
+    const int kc_n = x.is_user ? p.kc_u : p.kc_c;
+    int ks_left = x.is_user ? p.ks_u : p.ks_c;
+    const int buf = local & 1;
+    const uint32_t use = static_cast<uint32_t>(local >> 1);
+    if (!mbar_wait(&s.acc_empty[buf], (use & 1u) ^ 1u, s.abort, p.timeout_ns, 1)) return;
+    if (!x.is_user && !wc_ready) {
+      if (!mbar_wait(s.wc_full, 0, s.abort, p.timeout_ns, 1)) return;
+      wc_ready = true;
+    }
+    tc_fence_after();
+    const uint32_t d_tmem = tmem + static_cast<uint32_t>(buf) * 256u;
+    for (int kc = 0; kc < kc_n; ++kc) {
+      if (!mbar_wait(&s.a_full[stage], a_phase, s.abort, p.timeout_ns, 1)) return;
+      if (x.is_user && !mbar_wait(&s.w_full[wslot], w_phase, s.abort, p.timeout_ns, 1)) return;
+      tc_fence_after();
+      const uint32_t a_base = smem_u32(s.a_ring + static_cast<size_t>(stage) * LCE_A_STAGE_BYTES);
+      const uint32_t b_base =
+          smem_u32(s.w_region + static_cast<size_t>(x.is_user ? wslot : kc) * w_chunk_bytes);
+      const int nsteps = ks_left < 4 ? ks_left : 4;
+      for (int st = 0; st < nsteps; ++st) {
+        // 16 k rows of 128 bytes per MMA step; 64-element blocks along M / N are one box apart
+        const uint64_t adesc = sdesc_sw128(a_base + st * 2048u, BOX_BYTES, 1024u);
+        const uint64_t bdesc = sdesc_sw128(b_base + st * 2048u, BOX_BYTES, 1024u);
+        mma_bf16_ss(d_tmem, adesc, bdesc, idesc, (kc > 0 || st > 0) ? 1u : 0u);
+      }
+      ks_left -= nsteps;
+      mma_commit(&s.a_empty[stage]);
+      if (x.is_user) {
+        mma_commit(&s.w_empty[wslot]);
+        if (++wslot == p.w_slots) {
+          wslot = 0;
+          w_phase ^= 1u;
+        }
+      }
+      if (++stage == p.stages) {
+        stage = 0;
+        a_phase ^= 1u;
+      }
+    }
+    mma_commit(&s.acc_full[buf]);
+  }
+}
+
+// Wait (one lane per warp polls) until flags[idx] == epoch.  Gives up on an
+// earlier flag timeout anywhere in the launch, or after timeout_ns.
+__device__ __forceinline__ bool wait_user_partial(const LceParams& p, int idx) {
+  int ok = 0;
+  if (lane_id() == 0) {
+    const uint32_t* f = p.flags + idx;
+    if (ld_acquire_gpu(f) == p.epoch) {
+      ok = 1;
+    } else {
+      const uint64_t t0 = globaltimer_ns();
+      for (;;) {
+        if (ld_acquire_gpu(f) == p.epoch) {
+          ok = 1;
+          break;
+        }
+        if (ld_volatile_u32(p.timeout_epoch) == p.epoch) break;  // an earlier wait of this launch gave up
+        if (globaltimer_ns() - t0 > p.timeout_ns) {
+          atomicOr(p.status, DEV_ERR_FLAG_TIMEOUT);
+          atomicExch(p.timeout_epoch, p.epoch);
+          break;
+        }
+        __nanosleep(64);
+      }
+    }
+  }
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  if (ok) (void)ld_acquire_gpu(p.flags + idx);  // every lane synchronises with the release
+  return ok != 0;
+}
+
+// ------------------------------------------------------------ epilogue
+__device__ void lce_epilogue(const LceParams& p, const LceSmem& s, uint32_t tmem) {
+  const int warp = threadIdx.x >> 5;
+  const int et = threadIdx.x - 128;  // 0..127: TMEM lane = row of the D block
+  const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+  int local = 0;
+  uint32_t pubs = 0;
+  for (int unit = blockIdx.x; unit < p.n_units; unit += gridDim.x, ++local) {
+    const UnitInfo x = unit_info(p, unit);
+    const int buf = local & 1;
+    const uint32_t use = static_cast<uint32_t>(local >> 1);
+    if (!mbar_wait(&s.acc_full[buf], use & 1u, s.abort, p.timeout_ns, 1)) return;
+    tc_fence_after();
+    const uint32_t t_acc = tmem + lane_base + static_cast<uint32_t>(buf) * 256u;
+    const int d = x.dblk * LCE_BM + et;
+    const bool dok = d < p.D;
+    const size_t ND = static_cast<size_t>(p.N) * p.D;
+    if (x.is_user) {
+      float* P = p.partial + static_cast<size_t>(x.row) * ND + d;
+      for (int c0 = 0; c0 < p.N; c0 += 32) {
+        uint32_t v[32];
+        tmem_ld32(t_acc + c0, v);
+        tmem_ld_wait(v);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const int n = c0 + j;
+          if (n < p.N && dok) {
+            float b = 0.f;
+            if (p.bias) b = __bfloat162float(__ushort_as_bfloat16(p.bias[n]));
+            __stcg(P + static_cast<size_t>(n) * p.D, __uint_as_float(v[j]) + b);
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&s.acc_empty[buf]);
+      // publish: every writer fences its P rows, then thread 0 releases the flag
+      // once all 128 have arrived (bounded wait, so an abort cannot strand it)
+      __threadfence();
+      mbar_arrive(s.pub);
+      if (et == 0) {
+        const bool all = mbar_wait(s.pub, pubs & 1u, s.abort, p.timeout_ns, 1);
+        if (all && !(p.debug & DEBUG_WITHHOLD_USER_PARTIAL)) {
+          __threadfence();
+          st_release_gpu(p.flags + x.row * p.n_dblk + x.dblk, p.epoch);
+        }
+      }
+      ++pubs;
+    } else {
+      const int i = x.row;
+      const int u = p.map[i];
+      const bool uok = u >= 0 && u < p.n_users;
+      if (!uok && et == 0) atomicOr(p.status, DEV_ERR_MAP_RANGE);
+      const bool ready = uok && wait_user_partial(p, u * p.n_dblk + x.dblk);
+      if (ready) {
+        const float* P = p.partial + static_cast<size_t>(u) * ND + d;
+        __nv_bfloat16* Y = reinterpret_cast<__nv_bfloat16*>(p.Y) + static_cast<size_t>(i) * ND + d;
+        for (int c0 = 0; c0 < p.N; c0 += 32) {
+          uint32_t v[32];
+          tmem_ld32(t_acc + c0, v);
+          float pu[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int n = c0 + j;
+            pu[j] = (n < p.N && dok) ? __ldcg(P + static_cast<size_t>(n) * p.D) : 0.f;
+          }
+          tmem_ld_wait(v);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int n = c0 + j;
+            if (n < p.N && dok) Y[static_cast<size_t>(n) * p.D] = __float2bfloat16_rn(__uint_as_float(v[j]) + pu[j]);
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&s.acc_empty[buf]);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(LCE_THREADS, 1)
+    lce_fused_kernel(const __grid_constant__ CUtensorMap tmU, const __grid_constant__ CUtensorMap tmC,
+                     const __grid_constant__ CUtensorMap tmWu, const __grid_constant__ CUtensorMap tmWc,
+                     const LceParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const LceSmem s = carve(base, p);
+  const int warp = threadIdx.x >> 5;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < p.stages; ++i) {
+      mbar_init(&s.a_full[i], 1);
+      mbar_init(&s.a_empty[i], 1);
+    }
+    for (int i = 0; i < p.w_slots; ++i) {
+      mbar_init(&s.w_full[i], 1);
+      mbar_init(&s.w_empty[i], 1);
+    }
+    mbar_init(s.wc_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s.acc_full[i], 1);
+      mbar_init(&s.acc_empty[i], 128);
+    }
+    mbar_init(s.pub, 128);
+    *s.abort = 0;
+    fence_barrier_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == 0 && lane_id() == 0) {
+    tma_prefetch_desc(&tmU);
+    tma_prefetch_desc(&tmC);
+    tma_prefetch_desc(&tmWu);
+    tma_prefetch_desc(&tmWc);
+  }
+  if (warp == 2) {
+    tmem_alloc(s.tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *s.tmem_slot;
+
+  if (warp == 0) {
+    if (lane_id() == 0) lce_producer(p, s, &tmU, &tmC, &tmWu, &tmWc);
+  } else if (warp == 1) {
+    if (lane_id() == 0) lce_mma(p, s, tmem);
+  } else if (warp >= 4) {
+    lce_epilogue(p, s, tmem);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (*s.abort && threadIdx.x == 0) atomicOr(p.status, DEV_ERR_PIPE_TIMEOUT);
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace
+
+size_t lce_smem_bytes(const LceParams& p) {
+  const size_t bars = sizeof(uint64_t) * (2 * p.stages + 2 * p.w_slots + 1 + 4 + 1) + 2 * sizeof(uint32_t);
+  return 1024 + p.w_region_bytes + static_cast<size_t>(p.stages) * LCE_A_STAGE_BYTES + bars;
+}
+
+cudaError_t launch_lce(const CUtensorMap& tmU, const CUtensorMap& tmC, const CUtensorMap& tmWu,
+                       const CUtensorMap& tmWc, const LceParams& p, int grid, cudaStream_t s) {
+  const size_t smem = lce_smem_bytes(p);
+  cudaError_t e = cudaFuncSetAttribute(lce_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(LCE_THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;  // all CTAs co-resident: the flag hand-off needs it
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, lce_fused_kernel, tmU, tmC, tmWu, tmWc, p);
+}
+
+}  // namespace ikbo

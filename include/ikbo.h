@@ -1,0 +1,160 @@
+/*
+ * ikbo.h -- C ABI of the GB300 (sm_103a) In-Kernel Broadcast Optimization
+ * (IKBO) hot path.
+ *
+ * IKBO ("Meta Optimizes Inference for Recommendation Systems", RO/NRO and
+ * Type I / Type II paragraphs; aixai.ru, "Почему broadcast — это проблема
+ * раскладки данных"): an interaction operator takes the request-only (user)
+ * tensors at their own batch n_users, the per-candidate tensors at n_cand,
+ * and a candidate->user map, and never materialises the user tensors
+ * replicated to n_cand -- not in memory, not on the bus, not in cache.
+ *
+ * Two operators are provided:
+ *   - Linear Compression Embedding (LCE, Type I, decomposable):
+ *       Y[i] = W_u^T U[map[i]] + W_c^T C[i] + b
+ *   - broadcast attention (Type II, broadcast inside the kernel):
+ *       O[i,h] = softmax(Q[i,h] K[map[i],h]^T * scale) V[map[i],h]
+ *
+ * Conventions for every entry point:
+ *   - All tensor arguments are DEVICE pointers to row-major, contiguous
+ *     memory owned by the caller; bf16 tensors are passed as `const void*`
+ *     (IEEE bfloat16 bit patterns), integer tensors as int32.  Every tensor
+ *     pointer must be 16-byte aligned (TMA requirement).
+ *   - Every call is asynchronous and ordered on the given CUDA stream; no
+ *     call synchronises except ikbo_plan_get_status and ikbo_plan_destroy.
+ *   - Arguments are validated before any launch; a rejected call launches
+ *     nothing and returns an error code.  No exception crosses the ABI and
+ *     no kernel traps: errors detected on the device (a map value out of
+ *     range, a bounded wait that ran out) are recorded in the plan's status
+ *     word and returned by ikbo_plan_get_status.
+ *   - One plan must not be used by two streams at the same time.
+ *   - Device: one GPU of compute capability 10.3 (sm_103a), the device that
+ *     is current when the plan is created.
+ */
+#ifndef IKBO_H
+#define IKBO_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  IKBO_OK = 0,
+  IKBO_ERR_INVALID_ARG = 1,       /* null pointer, non-positive size, size above the plan's maximum, misalignment */
+  IKBO_ERR_UNSUPPORTED = 2,       /* legal but not implemented: d != 128, D or N not a multiple of 8, ... */
+  IKBO_ERR_CUDA = 3,              /* a CUDA runtime / driver call failed (launch, allocation, tensor map) */
+  IKBO_ERR_MAP_OUT_OF_RANGE = 4,  /* device-detected: some map[i] outside [0, n_users) */
+  IKBO_ERR_TIMEOUT = 5,           /* device-detected: a bounded wait inside a kernel gave up */
+  IKBO_ERR_NOT_PLANNED = 6,       /* forward called before ikbo_plan */
+  IKBO_ERR_INTERNAL = 7           /* device-detected: inconsistent work list */
+} ikbo_status_t;
+
+/* Opaque plan: owns the segment arrays, the attention work list, the fp32
+ * user-partial workspace of LCE, its readiness flags and the status word. */
+typedef struct ikbo_plan_s* ikbo_plan_t;
+
+/* Create a plan for requests of at most max_cand candidates, max_users users
+ * and max_heads attention heads (each >= 1; max_users <= 8192).  Allocates
+ * the plan's device memory on the current device (synchronous allocation).
+ * On success *out receives the plan; on failure *out is set to NULL. */
+ikbo_status_t ikbo_plan_create(ikbo_plan_t* out, int max_cand, int max_users, int max_heads);
+
+/* Bind a request to the plan and build its segments on `stream`
+ * (the runtime "passes a candidate-to-user mapping", aibriefing RO/NRO
+ * paragraph; grouping the candidates of one user is what lets their K/V be
+ * loaded once, aixai.ru "Deep Dive: Flash Attention"):
+ *   d_map     int32 [n_cand], values in [0, n_users); BORROWED: must stay
+ *             valid and unchanged until the last forward call of this request
+ *   n_cand    1..max_cand;  n_users 1..max_users
+ *   H, Lq     attention heads (1..max_heads) and queries per candidate
+ *             (multiple of 8, at most 128); they shape the work list.
+ * Produces, stream-ordered and bit-exact:
+ *   counts[u]  = #{i : map[i] = u}
+ *   offsets[u] = sum_{v<u} counts[v]   (offsets[n_users] = n_cand)
+ *   perm       = candidates grouped by user, ascending i within a user
+ *   work       = for u, for h, for each run of <= cands_per_unit entries of
+ *                u's segment: {u, h, first position in perm, run length}
+ * A map value out of range is skipped and reported by ikbo_plan_get_status. */
+ikbo_status_t ikbo_plan(ikbo_plan_t p, const int32_t* d_map, int n_cand, int n_users, int H, int Lq,
+                        cudaStream_t stream);
+
+/* Borrow the segment arrays of the last ikbo_plan (device pointers, valid
+ * until the next ikbo_plan or ikbo_plan_destroy): counts [n_users], offsets
+ * [n_users+1], perm [n_cand].  Any output pointer may be NULL. */
+ikbo_status_t ikbo_plan_segments(ikbo_plan_t p, const int32_t** d_counts, const int32_t** d_offsets,
+                                 const int32_t** d_perm);
+
+/* Borrow the attention work list: d_work int32 [max_units][4], d_n_units a
+ * device int32 holding the number of units, *cands_per_unit and *max_units
+ * host values.  Any output pointer may be NULL. */
+ikbo_status_t ikbo_plan_worklist(ikbo_plan_t p, const int32_t** d_work, const int32_t** d_n_units,
+                                 int* cands_per_unit, int* max_units);
+
+/* Linear Compression Embedding with in-kernel broadcast (aixai.ru, "Deep
+ * Dive: Linear Compression", stages 1-4; aibriefing, LCE deep dive):
+ *   Y[i][n][d] = b[n] + sum_{k<K_u} Wu[k][n] U[map[i]][k][d]
+ *                     + sum_{k<K_c} Wc[k][n] C[i][k][d]
+ * with the map, n_cand and n_users of the last ikbo_plan.
+ *   U  bf16 [n_users][K_u][D]     C  bf16 [n_cand][K_c][D]
+ *   Wu bf16 [K_u][N]              Wc bf16 [K_c][N]
+ *   b  bf16 [N] or NULL           Y  bf16 [n_cand][N][D] (written)
+ * bf16 inputs, fp32 accumulation, round-to-nearest-even bf16 output.  The
+ * user GEMM runs at n_users into a plan-owned fp32 workspace (grown on the
+ * first call that needs more; that call allocates synchronously) and is
+ * added in the candidate GEMM's epilogue by map lookup.  One launch.
+ * Limits: K_u, K_c >= 1; D, N multiples of 8; N <= 256;
+ * ceil(K_c/64) * ceil(roundup(N,16)/64) <= 16 (Wc stays in shared memory);
+ * else IKBO_ERR_UNSUPPORTED. */
+ikbo_status_t ikbo_lce_forward(ikbo_plan_t p, const void* U, const void* C, const void* Wu, const void* Wc,
+                               const void* b, void* Y, int K_u, int K_c, int D, int N, cudaStream_t stream);
+
+/* Broadcast attention (aixai.ru, "Deep Dive: Flash Attention"; aibriefing,
+ * Flash Attention case): for every candidate i and head h, with u = map[i],
+ *   O[i,h,q,:] = sum_j softmax_j(scale * Q[i,h,q,:].K[u,h,j,:]) V[u,h,j,:]
+ * with the map, n_cand, n_users, H and Lq of the last ikbo_plan.
+ *   Q bf16 [n_cand][H][Lq][d]
+ *   dense  (d_kv_offsets == NULL): K, V bf16 [n_users][H][Lkv][d], Lkv >= 1
+ *   jagged (d_kv_offsets != NULL): K, V bf16 [Lkv][H][d] where Lkv is the
+ *          total packed rows and user u owns rows d_kv_offsets[u] ..
+ *          d_kv_offsets[u+1]-1 (int32 [n_users+1], offsets[0] = 0)
+ *   O bf16 [n_cand][H][Lq][d] (written; rows whose user has no keys get 0)
+ *   scale  > 0 (usually 1/sqrt(d)).  No mask.
+ * Each user's K/V tile is read once per work unit and shared by up to
+ * 2*floor(128/Lq) candidates.  fp32 scores and softmax, P rounded to bf16
+ * for P.V, fp32 accumulation, bf16 output.  Limits: d == 128. */
+ikbo_status_t ikbo_attn_forward(ikbo_plan_t p, const void* Q, const void* K, const void* V,
+                                const int32_t* d_kv_offsets, void* O, int Lkv, int d, float scale,
+                                cudaStream_t stream);
+
+/* Synchronise `stream`, then return (and clear) the first device-detected
+ * error recorded since the last call: IKBO_ERR_MAP_OUT_OF_RANGE,
+ * IKBO_ERR_TIMEOUT, IKBO_ERR_INTERNAL, or IKBO_OK. */
+ikbo_status_t ikbo_plan_get_status(ikbo_plan_t p, cudaStream_t stream);
+
+/* Debug and robustness knobs.  flags: bit 0 = LCE user tiles compute but do
+ * not publish their partials (candidate epilogues then wait, give up after
+ * the timeout, skip their stores and report IKBO_ERR_TIMEOUT).  The timeout
+ * bounds every wait inside the kernels (default 2 s). */
+ikbo_status_t ikbo_plan_set_debug(ikbo_plan_t p, unsigned flags);
+ikbo_status_t ikbo_plan_set_timeout_ns(ikbo_plan_t p, uint64_t timeout_ns);
+
+/* Number of kernel launches the forward calls and ikbo_plan have made
+ * through this plan since it was created. */
+uint64_t ikbo_plan_launch_count(ikbo_plan_t p);
+
+const char* ikbo_status_string(ikbo_status_t s);
+
+/* Synchronise the device and free the plan's memory.  NULL is a no-op. */
+void ikbo_plan_destroy(ikbo_plan_t p);
+
+/* ABI version (major * 100 + minor). */
+int ikbo_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* IKBO_H */
