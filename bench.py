@@ -141,6 +141,23 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def max_over_ranks(value: float, dist=None, device=None) -> float:
+    """Max of a per-rank float over the process group (identity when alone).
+    Uses the group's own backend: a CUDA tensor for NCCL, a CPU one otherwise."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return float(value)
+    import torch
+    dev = device if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(value)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_scaling_value(flops_per_step: float, steps: int, world: int, max_ms: float) -> float:
+    """Whole-job TFLOP/s: every rank ran `steps` requests; time = slowest rank."""
+    return world * flops_per_step * steps / (max_ms * 1e-3) / 1e12
+
+
 # --------------------------------------------------------------- workload
 def workload():
     from broadcast_gemm_attention_gb300 import inputs as gen
@@ -293,13 +310,9 @@ def run_gpu(args):
     lce_ms = [e[1].elapsed_time(e[2]) for e in ev]
     attn_ms = [e[2].elapsed_time(e[3]) for e in ev]
     step_ms = [e[0].elapsed_time(e[3]) for e in ev]
-    total_ms = sum(step_ms)
-    if dist:
-        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(step_ms), dist, dev)
     ms_per_step = total_ms / K
-    value = world * step_flops * K / (total_ms * 1e-3) / 1e12
+    value = weak_scaling_value(step_flops, K, world, total_ms)
 
     pk = peaks()
     lce_s = statistics.mean(lce_ms) * 1e-3
@@ -342,11 +355,7 @@ def run_gpu(args):
             e2e_step()
         e_e.record(stream)
         torch.cuda.synchronize()
-        e2e_ms = e_s.elapsed_time(e_e) / n_e2e
-        if dist:
-            t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
+        e2e_ms = max_over_ranks(e_s.elapsed_time(e_e) / n_e2e, dist, dev)
         e2e = {"value": world * step_flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "steps": n_e2e,
                "path": "pinned host -> device copies, ikbo_plan + ikbo_lce_forward + ikbo_attn_forward, "
@@ -364,7 +373,7 @@ def run_gpu(args):
         return
 
     cpu = None
-    if world == 1 or rank == 0:
+    if (world == 1 or rank == 0) and args.cpu_seconds > 0:
         n = calibrate_oracle(x, a, args.cpu_seconds)
         dt, fl, desc, thr = cpu_oracle_sample(x, a, n)
         cpu = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": thr, "kind": "oracle", "sample": desc,
@@ -444,7 +453,8 @@ def main():
     ap.add_argument("--no-ablation", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
-    ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target length of the CPU-oracle baseline")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0,
+                    help="target length of the CPU-oracle baseline (0 skips it, e.g. under a profiler)")
     ap.add_argument("--ref-budget", type=float, default=120.0, help="reference arm: total seconds of oracle work")
     args = ap.parse_args()
     if args.impl == "reference":

@@ -302,8 +302,10 @@ __device__ void att_softmax(const AttnParams& p, const AttSmem& s, uint32_t tmem
         }
       }
       const float m_new = fmaxf(m, mx * sl);
-      if (m_new > m + RESCALE_THRESHOLD) {
-        const float alpha = ex2(m - m_new);  // 0 on the first tile
+      // tcgen05.ld/st are warp-collective: the rescale decision must be
+      // uniform across the warp, so any row that needs it moves all 32
+      if (__any_sync(0xffffffffu, m_new > m + RESCALE_THRESHOLD)) {
+        const float alpha = ex2(m - m_new);  // 0 on the first tile, 1 for rows whose max did not move
         l *= alpha;
         if (jt > 0) {
           // PV of the previous tile has completed (it was committed before this S)
