@@ -248,7 +248,7 @@ class _DeviceArray:
     """Exposes a borrowed device int32 array through __cuda_array_interface__."""
 
     def __init__(self, ptr: int, count: int):
-        self.__cuda_array_interface__ = {"shape": (count,), "typestr": "<i4", "data": (ptr, True),
+        self.__cuda_array_interface__ = {"shape": (count,), "typestr": "<i4", "data": (ptr, False),
                                          "version": 3, "strides": None}
 
 

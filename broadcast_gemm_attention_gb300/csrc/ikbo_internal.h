@@ -44,7 +44,9 @@ struct SegParams {
 // chunks of 64 (one 128-byte swizzle row per k when MN-major).
 constexpr int LCE_BM = 128;
 constexpr int LCE_BK = 64;
-constexpr int LCE_THREADS = 256;            // warp 0 TMA, 1 MMA, 2 TMEM, 3 idle, 4-7 epilogue
+constexpr int LCE_THREADS = 384;            // warp 0 TMA, 1 MMA, 2 TMEM, 3 idle, 4-11 epilogue
+constexpr int LCE_EPI_WARP0 = 4;
+constexpr int LCE_EPI_THREADS = LCE_THREADS - 32 * LCE_EPI_WARP0;
 constexpr int LCE_A_STAGE_BYTES = LCE_BM * LCE_BK * 2;   // 16 KB: two 64(d) x 64(k) boxes
 constexpr int LCE_MAX_STAGES = 8;
 constexpr int LCE_MAX_W_SLOTS = 8;

@@ -21,7 +21,7 @@
 //   warp 0  TMA producer   (A ring: U[u] or C[i] chunks; W chunks / resident Wc)
 //   warp 1  MMA issuer     (tcgen05.mma, fp32 accumulators in TMEM, 2 buffers)
 //   warp 2  TMEM owner     (alloc / dealloc of 512 columns)
-//   warps 4-7  epilogue    (tcgen05.ld, + P or + b, bf16 or fp32 stores)
+//   warps 4-11 epilogue    (tcgen05.ld, + P or + b, bf16 or fp32 stores)
 //
 // Tile: 128 rows of D (TMEM lanes) x N_mma columns (N rounded up to 16) of
 // one candidate (or user).  Operands are MN-major (D and N are the contiguous
@@ -225,31 +225,41 @@ __device__ __forceinline__ bool wait_user_partial(const LceParams& p, int idx) {
 }
 
 // ------------------------------------------------------------ epilogue
+// Eight warps: warp w reads TMEM lane quarter w % 4 (rows 32*(w%4) .. +31 of
+// the D block) and every other 32-column chunk, starting at (w - 4) / 4.
+// Candidate tiles fetch their P[map[i]] chunks before waiting for the
+// accumulator, so the L2 latency of that gather hides behind the MMA.
+constexpr int EPI_PREFETCH = 3;  // chunks of P held in registers ahead of the accumulator
+
 __device__ void lce_epilogue(const LceParams& p, const LceSmem& s, uint32_t tmem) {
   const int warp = threadIdx.x >> 5;
-  const int et = threadIdx.x - 128;  // 0..127: TMEM lane = row of the D block
-  const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+  const int quarter = warp & 3;
+  const int half = (warp - LCE_EPI_WARP0) >> 2;
+  const int et = quarter * 32 + static_cast<int>(lane_id());  // TMEM lane = row of the D block
+  const bool leader = warp == LCE_EPI_WARP0 && lane_id() == 0;
+  const uint32_t lane_base = static_cast<uint32_t>(32 * quarter) << 16;
+  const int nchunks = (p.N + 31) / 32;
   int local = 0;
   uint32_t pubs = 0;
   for (int unit = blockIdx.x; unit < p.n_units; unit += gridDim.x, ++local) {
     const UnitInfo x = unit_info(p, unit);
     const int buf = local & 1;
     const uint32_t use = static_cast<uint32_t>(local >> 1);
-    if (!mbar_wait(&s.acc_full[buf], use & 1u, s.abort, p.timeout_ns, 1)) return;
-    tc_fence_after();
-    const uint32_t t_acc = tmem + lane_base + static_cast<uint32_t>(buf) * 256u;
     const int d = x.dblk * LCE_BM + et;
     const bool dok = d < p.D;
     const size_t ND = static_cast<size_t>(p.N) * p.D;
+    const uint32_t t_acc = tmem + lane_base + static_cast<uint32_t>(buf) * 256u;
     if (x.is_user) {
+      if (!mbar_wait(&s.acc_full[buf], use & 1u, s.abort, p.timeout_ns, 1)) return;
+      tc_fence_after();
       float* P = p.partial + static_cast<size_t>(x.row) * ND + d;
-      for (int c0 = 0; c0 < p.N; c0 += 32) {
+      for (int c = half; c < nchunks; c += 2) {
         uint32_t v[32];
-        tmem_ld32(t_acc + c0, v);
+        tmem_ld32(t_acc + c * 32, v);
         tmem_ld_wait(v);
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
-          const int n = c0 + j;
+          const int n = c * 32 + j;
           if (n < p.N && dok) {
             float b = 0.f;
             if (p.bias) b = __bfloat162float(__ushort_as_bfloat16(p.bias[n]));
@@ -259,11 +269,11 @@ __device__ void lce_epilogue(const LceParams& p, const LceSmem& s, uint32_t tmem
       }
       tc_fence_before();
       mbar_arrive(&s.acc_empty[buf]);
-      // publish: every writer fences its P rows, then thread 0 releases the flag
-      // once all 128 have arrived (bounded wait, so an abort cannot strand it)
+      // publish: every writer fences its P rows, then one thread releases the
+      // flag once all epilogue threads have arrived (bounded wait)
       __threadfence();
       mbar_arrive(s.pub);
-      if (et == 0) {
+      if (leader) {
         const bool all = mbar_wait(s.pub, pubs & 1u, s.abort, p.timeout_ns, 1);
         if (all && !(p.debug & DEBUG_WITHHOLD_USER_PARTIAL)) {
           __threadfence();
@@ -275,25 +285,53 @@ __device__ void lce_epilogue(const LceParams& p, const LceSmem& s, uint32_t tmem
       const int i = x.row;
       const int u = p.map[i];
       const bool uok = u >= 0 && u < p.n_users;
-      if (!uok && et == 0) atomicOr(p.status, DEV_ERR_MAP_RANGE);
+      if (!uok && leader) atomicOr(p.status, DEV_ERR_MAP_RANGE);
       const bool ready = uok && wait_user_partial(p, u * p.n_dblk + x.dblk);
+      const float* P = p.partial + static_cast<size_t>(uok ? u : 0) * ND + d;
+      float pre[EPI_PREFETCH][32];
       if (ready) {
-        const float* P = p.partial + static_cast<size_t>(u) * ND + d;
-        __nv_bfloat16* Y = reinterpret_cast<__nv_bfloat16*>(p.Y) + static_cast<size_t>(i) * ND + d;
-        for (int c0 = 0; c0 < p.N; c0 += 32) {
-          uint32_t v[32];
-          tmem_ld32(t_acc + c0, v);
-          float pu[32];
+#pragma unroll
+        for (int k = 0; k < EPI_PREFETCH; ++k) {
+          const int c = half + 2 * k;
+          const float* pp = P + static_cast<size_t>(c * 32) * p.D;
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
-            const int n = c0 + j;
-            pu[j] = (n < p.N && dok) ? __ldcg(P + static_cast<size_t>(n) * p.D) : 0.f;
+            pre[k][j] = (c * 32 + j < p.N && dok) ? __ldcg(pp) : 0.f;
+            pp += p.D;
           }
+        }
+      }
+      if (!mbar_wait(&s.acc_full[buf], use & 1u, s.abort, p.timeout_ns, 1)) return;
+      tc_fence_after();
+      if (ready) {
+        __nv_bfloat16* Y = reinterpret_cast<__nv_bfloat16*>(p.Y) + static_cast<size_t>(i) * ND + d;
+#pragma unroll
+        for (int k = 0; k < EPI_PREFETCH; ++k) {
+          const int c = half + 2 * k;
+          if (c >= nchunks) break;
+          uint32_t v[32];
+          tmem_ld32(t_acc + c * 32, v);
           tmem_ld_wait(v);
+          __nv_bfloat16* y = Y + static_cast<size_t>(c * 32) * p.D;
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
-            const int n = c0 + j;
-            if (n < p.N && dok) Y[static_cast<size_t>(n) * p.D] = __float2bfloat16_rn(__uint_as_float(v[j]) + pu[j]);
+            if (c * 32 + j < p.N && dok) *y = __float2bfloat16_rn(__uint_as_float(v[j]) + pre[k][j]);
+            y += p.D;
+          }
+        }
+        for (int c = half + 2 * EPI_PREFETCH; c < nchunks; c += 2) {  // beyond the prefetch (N > 192)
+          uint32_t v[32];
+          tmem_ld32(t_acc + c * 32, v);
+          float pu[32];
+          const float* pp = P + static_cast<size_t>(c * 32) * p.D;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) pu[j] = (c * 32 + j < p.N && dok) ? __ldcg(pp + static_cast<size_t>(j) * p.D) : 0.f;
+          tmem_ld_wait(v);
+          __nv_bfloat16* y = Y + static_cast<size_t>(c * 32) * p.D;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            if (c * 32 + j < p.N && dok) *y = __float2bfloat16_rn(__uint_as_float(v[j]) + pu[j]);
+            y += p.D;
           }
         }
       }
@@ -324,9 +362,9 @@ __global__ void __launch_bounds__(LCE_THREADS, 1)
     mbar_init(s.wc_full, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s.acc_full[i], 1);
-      mbar_init(&s.acc_empty[i], 128);
+      mbar_init(&s.acc_empty[i], LCE_EPI_THREADS);
     }
-    mbar_init(s.pub, 128);
+    mbar_init(s.pub, LCE_EPI_THREADS);
     *s.abort = 0;
     fence_barrier_init();
     fence_proxy_async_smem();
@@ -346,11 +384,18 @@ __global__ void __launch_bounds__(LCE_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *s.tmem_slot;
 
-  if (warp == 0) {
-    if (lane_id() == 0) lce_producer(p, s, &tmU, &tmC, &tmWu, &tmWc);
-  } else if (warp == 1) {
-    if (lane_id() == 0) lce_mma(p, s, tmem);
-  } else if (warp >= 4) {
+  // registers: launched at 168 per thread (384 x 168 = 64512); the control
+  // warpgroup gives back down to 72 and the two epilogue warpgroups take 216
+  // (128 x 72 + 256 x 216 = 64512)
+  if (warp < LCE_EPI_WARP0) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 72;");
+    if (warp == 0) {
+      if (lane_id() == 0) lce_producer(p, s, &tmU, &tmC, &tmWu, &tmWc);
+    } else if (warp == 1) {
+      if (lane_id() == 0) lce_mma(p, s, tmem);
+    }
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 216;");
     lce_epilogue(p, s, tmem);
   }
 
