@@ -50,7 +50,7 @@ def compile_source(src: str, out: str) -> str:
     """gcc -O2 -fopenmp (no fast-math: IEEE double semantics are kept)."""
     os.makedirs(os.path.dirname(out), exist_ok=True)
     tmp = out + f".tmp{os.getpid()}"
-    cmd = ["gcc", "-O2", "-fPIC", "-shared", "-std=c11", "-Wall", "-o", tmp, src, "-lm"]
+    cmd = ["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c11", "-Wall", "-o", tmp, src, "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, out)
     return out

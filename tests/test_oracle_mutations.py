@@ -27,7 +27,8 @@ MUTATIONS = {
     "attn_jagged_stride": ("row_stride = (size_t)H * d;", "row_stride = (size_t)d;", ATTN_PINS),
     # segments
     "seg_unstable": ("for (int i = 0; i < n_cand; ++i) {       /* ascending i: stable */", "for (int i = n_cand - 1; i >= 0; --i) {", SEG_PINS),
-    "seg_inclusive_scan": ("for (int u = 0; u < n_users; ++u) next[u] = offsets[u];", "for (int u = 0; u < n_users; ++u) next[u] = offsets[u] + (counts[u] > 1);", SEG_PINS),
+    # every planted mistake keeps its writes inside the caller's buffers
+    "seg_perm_stores_user": ("perm[next[u]] = i;", "perm[next[u]] = u;", SEG_PINS),
     "seg_chunk_off_by_one": ("if (cnt > cands_per_unit) cnt = cands_per_unit;", "if (cnt >= cands_per_unit) cnt = cands_per_unit - 1 + (cands_per_unit == 1);", SEG_PINS),
 }
 
