@@ -40,6 +40,7 @@ SIGNATURES = {
     "ikbo_plan_worklist": (_i, [_vp, ctypes.POINTER(_vp), ctypes.POINTER(_vp), ctypes.POINTER(_i),
                                 ctypes.POINTER(_i)]),
     "ikbo_lce_forward": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp]),
+    "ikbo_lce_forward_noalloc": (_i, [_vp, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp]),
     "ikbo_attn_forward": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, ctypes.c_float, _vp]),
     "ikbo_plan_get_status": (_i, [_vp, _vp]),
     "ikbo_plan_set_debug": (_i, [_vp, ctypes.c_uint]),
@@ -154,6 +155,31 @@ def ikbo_lce_forward(plan: int, U: torch.Tensor, C: torch.Tensor, Wu: torch.Tens
         bptr = _dev(b, bf, "b")
     _check(load().ikbo_lce_forward(plan, _dev(U, bf, "U"), _dev(C, bf, "C"), _dev(Wu, bf, "Wu"), _dev(Wc, bf, "Wc"),
                                    bptr, _dev(Y, bf, "Y"), K_u, K_c, D, N, _stream(stream)), "ikbo_lce_forward")
+
+
+def ikbo_lce_forward_noalloc(map_: torch.Tensor, n_users: int, U: torch.Tensor, C: torch.Tensor,
+                             Wu: torch.Tensor, Wc: torch.Tensor, b: Optional[torch.Tensor], Y: torch.Tensor,
+                             stream=None) -> None:
+    """The fused LCE without a plan: its scratch lives in the library's own
+    fixed device array, so the call allocates nothing (for callers whose
+    device memory belongs to another allocator).  Calls share that scratch:
+    do not overlap them on the GPU."""
+    bf = torch.bfloat16
+    n_u, K_u, D = U.shape
+    n_cand, K_c, D2 = C.shape
+    N = Wu.shape[1]
+    if n_u != n_users or D2 != D or tuple(Wu.shape) != (K_u, N) or tuple(Wc.shape) != (K_c, N) or \
+            tuple(Y.shape) != (n_cand, N, D) or map_.numel() != n_cand:
+        raise ValueError("inconsistent LCE shapes")
+    bptr = None
+    if b is not None:
+        if tuple(b.shape) != (N,):
+            raise ValueError("b must be [N]")
+        bptr = _dev(b, bf, "b")
+    _check(load().ikbo_lce_forward_noalloc(_dev(map_, torch.int32, "map"), n_cand, n_users, _dev(U, bf, "U"),
+                                           _dev(C, bf, "C"), _dev(Wu, bf, "Wu"), _dev(Wc, bf, "Wc"), bptr,
+                                           _dev(Y, bf, "Y"), K_u, K_c, D, N, _stream(stream)),
+           "ikbo_lce_forward_noalloc")
 
 
 def ikbo_attn_forward(plan: int, Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor,

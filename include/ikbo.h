@@ -111,6 +111,37 @@ ikbo_status_t ikbo_plan_worklist(ikbo_plan_t p, const int32_t** d_work, const in
 ikbo_status_t ikbo_lce_forward(ikbo_plan_t p, const void* U, const void* C, const void* Wu, const void* Wc,
                                const void* b, void* Y, int K_u, int K_c, int D, int N, cudaStream_t stream);
 
+/* The same fused LCE as ikbo_lce_forward, for callers that cannot allocate
+ * device memory.  (The IKBO write-ups have no counterpart to this entry
+ * point: it exists for deployment, not for the method.)
+ *
+ * ikbo_lce_forward keeps its scratch (fp32 user partials, readiness flags)
+ * in a plan that ikbo_plan_create allocates with cudaMalloc.  Callers whose
+ * device memory is owned by another allocator (a framework's memory pool, a
+ * fixed per-process budget), or whose request path may not call cudaMalloc
+ * or cudaFree (both can synchronise the device), use this instead: it takes
+ * the request directly and keeps its scratch in a 16 MiB array that the
+ * library declares in device memory, so it allocates nothing.
+ *   d_map   int32 [n_cand], values in [0, n_users)
+ *   U, C, Wu, Wc, b, Y, K_u, K_c, D, N: exactly as ikbo_lce_forward
+ * Limits: those of ikbo_lce_forward, and
+ *   4 * n_users * N * D + 4 * n_users * ceil(D/128) (rounded up to 256) + 256
+ *   <= 16 MiB, else IKBO_ERR_UNSUPPORTED before any launch.
+ * Notes:
+ *   - every GPU that loads the library holds the 16 MiB until process exit;
+ *   - the first call made with a given device current looks up the array's
+ *     device address (cudaGetSymbolAddress) and the device's limits; make
+ *     that first call before capturing any stream;
+ *   - all calls share the array and it keeps the last call's contents; the
+ *     call clears the words that must start at zero itself (the readiness
+ *     flags are per-call epochs and never need clearing); calls that overlap
+ *     on the GPU (two streams, or two host threads on one device) race;
+ *   - device-detected errors (map values out of range) are not reported:
+ *     those candidates' rows of Y are left untouched. */
+ikbo_status_t ikbo_lce_forward_noalloc(const int32_t* d_map, int n_cand, int n_users, const void* U, const void* C,
+                                       const void* Wu, const void* Wc, const void* b, void* Y, int K_u, int K_c,
+                                       int D, int N, cudaStream_t stream);
+
 /* Broadcast attention (aixai.ru, "Deep Dive: Flash Attention"; aibriefing,
  * Flash Attention case): for every candidate i and head h, with u = map[i],
  *   O[i,h,q,:] = sum_j softmax_j(scale * Q[i,h,q,:].K[u,h,j,:]) V[u,h,j,:]
