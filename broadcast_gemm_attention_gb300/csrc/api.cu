@@ -18,7 +18,7 @@ namespace ikbo {
 cudaError_t launch_seg_build(const SegParams& p, cudaStream_t s);
 size_t lce_smem_bytes(const LceParams& p);
 cudaError_t launch_lce(const CUtensorMap& tmU, const CUtensorMap& tmC, const CUtensorMap& tmWu,
-                       const CUtensorMap& tmWc, const LceParams& p, int grid, cudaStream_t s);
+                       const CUtensorMap& tmWc, const LceParams& p, int num_sms, cudaStream_t s);
 size_t attn_smem_bytes();
 cudaError_t launch_attn(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV, const AttnParams& p,
                         int grid, cudaStream_t s);
@@ -285,34 +285,19 @@ ikbo_status_t ikbo_lce_forward(ikbo_plan_t p, const void* U, const void* C, cons
 
   LceParams lp;
   std::memset(&lp, 0, sizeof(lp));
-  lp.map = p->d_map;
-  lp.bias = static_cast<const uint16_t*>(b);
-  lp.Y = static_cast<uint16_t*>(Y);
   lp.n_cand = p->n_cand;
   lp.n_users = p->n_users;
   lp.K_u = K_u;
   lp.K_c = K_c;
   lp.D = D;
   lp.N = N;
-  lp.N_mma = (N + 15) / 16 * 16;
-  lp.NB = (lp.N_mma + 63) / 64;
-  lp.n_dblk = (D + LCE_BM - 1) / LCE_BM;
-  lp.n_user_units = p->n_users * lp.n_dblk;
-  lp.n_units = (p->n_users + p->n_cand) * lp.n_dblk;
-  lp.kc_u = (K_u + LCE_BK - 1) / LCE_BK;
-  lp.kc_c = (K_c + LCE_BK - 1) / LCE_BK;
-  lp.ks_u = (K_u + 15) / 16;
-  lp.ks_c = (K_c + 15) / 16;
-  const int region_chunks = lp.kc_c < 2 ? 2 : lp.kc_c;
-  if (lp.kc_c * lp.NB > 16) return IKBO_ERR_UNSUPPORTED;
-  lp.w_region_bytes = static_cast<uint32_t>(region_chunks) * lp.NB * 64 * 64 * 2;
-  lp.w_slots = region_chunks < LCE_MAX_W_SLOTS ? region_chunks : LCE_MAX_W_SLOTS;
-  lp.stages = LCE_MAX_STAGES;
-  while (lp.stages > 2 && lce_smem_bytes(lp) > p->max_smem) --lp.stages;
-  if (lce_smem_bytes(lp) > p->max_smem) return IKBO_ERR_UNSUPPORTED;
+  if (!lce_configure(&lp, p->max_smem)) return IKBO_ERR_UNSUPPORTED;
+  lp.map = p->d_map;
+  lp.bias = static_cast<const uint16_t*>(b);
+  lp.Y = static_cast<uint16_t*>(Y);
 
   const size_t part = static_cast<size_t>(p->n_users) * N * D;
-  const size_t nflags = static_cast<size_t>(p->n_users) * lp.n_dblk;
+  const size_t nflags = lce_flag_count(lp);
   if (grow(&p->d_partial, &p->partial_elems, part) != cudaSuccess) return IKBO_ERR_CUDA;
   if (grow(&p->d_flags, &p->flags_elems, nflags) != cudaSuccess) return IKBO_ERR_CUDA;
   lp.partial = p->d_partial;
@@ -338,9 +323,8 @@ ikbo_status_t ikbo_lce_forward(ikbo_plan_t p, const void* U, const void* C, cons
       !encode_bf16(&tmWu, Wu, 2, wud, ws, wbox) || !encode_bf16(&tmWc, Wc, 2, wcd, ws, wbox))
     return IKBO_ERR_CUDA;
 
-  const int grid = lp.n_units < p->num_sms ? lp.n_units : p->num_sms;
-  if (launch_lce(tmU, tmC, tmWu, tmWc, lp, grid, stream) != cudaSuccess) return IKBO_ERR_CUDA;
-  p->launches++;
+  if (launch_lce(tmU, tmC, tmWu, tmWc, lp, p->num_sms, stream) != cudaSuccess) return IKBO_ERR_CUDA;
+  p->launches += 2;  // user tiles, then candidate tiles
   return IKBO_OK;
 }
 

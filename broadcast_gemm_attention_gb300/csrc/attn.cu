@@ -15,10 +15,12 @@
 //
 // Per CTA (persistent, one per SM, 12 warps = 3 warpgroups):
 //   warp 0      TMA producer: Q tiles (one box per candidate and d-half,
-//               gathered through perm), K/V tiles through a 4-stage ring
-//   warp 1      MMA issuer (one lane) and TMEM owner (512 columns: S0 S1 O0
-//               O1, 128 each): S_t = Q_t K^T (SS), O_t += P_t V (TS: P in TMEM)
-//   warps 2-3   idle
+//               gathered through perm), K/V tiles through a 5-stage ring
+//   warp 1      MMA issuer of query tile 0 (one lane) and TMEM owner (512
+//               columns: S0 S1 O0 O1, 128 each): S_t = Q_t K^T (SS),
+//               O_t += P_t V (TS: P in TMEM)
+//   warp 2      MMA issuer of query tile 1
+//   warp 3      idle
 //   warps 4-7   softmax + epilogue of query tile 0 (one thread per row; warp w
 //               reaches TMEM lanes 32*(w%4) .. +31)
 //   warps 8-11  softmax + epilogue of query tile 1
@@ -58,6 +60,7 @@ struct AttSmem {
   uint64_t* p_full;   // [2]
   uint64_t* o_full;   // [2]
   uint64_t* o_empty;  // [2]
+  uint64_t* tok;      // [2] issuer turns
   uint32_t* tmem_slot;
   uint32_t* abort;
 };
@@ -75,7 +78,8 @@ __device__ __forceinline__ AttSmem carve(uint8_t* base) {
   s.p_full = s.s_full + 2;
   s.o_full = s.p_full + 2;
   s.o_empty = s.o_full + 2;
-  s.tmem_slot = reinterpret_cast<uint32_t*>(s.o_empty + 2);
+  s.tok = s.o_empty + 2;
+  s.tmem_slot = reinterpret_cast<uint32_t*>(s.tok + 2);
   s.abort = s.tmem_slot + 1;
   return s;
 }
@@ -219,70 +223,105 @@ __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint3
   }
 }
 
-__device__ void att_mma(const AttnParams& p, const AttSmem& s, uint32_t tmem, int n_units) {
+// One issuer per query tile (warp 1 issues tile 0, warp 2 tile 1), taking
+// turns.  A burst is what one tile issues between two of its softmax steps:
+// S_t(0) at the start of a unit, then P_t V (+ the next S_t) per key tile.
+// The tensor pipe queues only a few instructions, so a lone issuer that
+// stops to check its barriers lets the pipe drain; here each issuer does its
+// checks while the other's burst is in the pipe.  The bursts alternate
+// (tile 0's b-th, tile 1's b-th, tile 0's (b+1)-th, ...) through two token
+// barriers, which keeps the tiles half a period apart, so one tile's softmax
+// always overlaps the other tile's products.
+// Each K/V stage is released once by each issuer (kv_empty counts 2).  When
+// a unit uses only tile 0, the tile-1 issuer still walks the unit burst by
+// burst -- waits for each stage to be loaded, releases it with a plain
+// arrive, takes and passes its turn -- so the stage and token counts of the
+// two issuers never drift apart (the parity waits could not tell the laps
+// apart if one issuer ran a full lap ahead).
+__device__ void att_mma(const AttnParams& p, const AttSmem& s, uint32_t tmem, int n_units, int t) {
   int stage = 0;
   uint32_t phase = 0;
-  uint32_t q_uses[2] = {0, 0};
-  uint32_t p_uses[2] = {0, 0};
-  uint32_t o_uses[2] = {0, 0};
-  const uint32_t q_base0 = smem_u32(s.q);
-  for (int unit = blockIdx.x; unit < n_units; unit += gridDim.x) {
-    const Unit x = decode(p, unit);
-    if (x.ntq == 0 || x.ntiles == 0) continue;
-    // first K tile
-    int k_stage = stage;
-    if (!mbar_wait(&s.kv_full[k_stage], phase, s.abort, p.timeout_ns, 1)) return;
+  uint32_t q_uses = 0, p_uses = 0, o_uses = 0, bursts = 0;
+  const uint32_t q_base = smem_u32(s.q) + t * ATT_Q_TILE_BYTES;
+  const uint32_t s_tmem = tmem + t * 128;
+  const uint32_t o_tmem = tmem + 256 + t * 128;
+  auto advance = [&]() {
     if (++stage == ATT_STAGES) {
       stage = 0;
       phase ^= 1u;
     }
-    for (int t = 0; t < x.ntq; ++t) {
-      if (!mbar_wait(&s.q_full[t], q_uses[t] & 1u, s.abort, p.timeout_ns, 1)) return;
-      ++q_uses[t];
-      tc_fence_after();
-      issue_qk(tmem + t * 128, q_base0 + t * ATT_Q_TILE_BYTES, smem_u32(s.kv + k_stage * ATT_KV_STAGE_BYTES));
-      mma_commit(&s.s_full[t]);
-      if (x.ntiles == 1) mma_commit(&s.q_empty[t]);  // that was the last S_t of the unit
+  };
+  // wait until the other issuer has issued its previous burst
+  auto take_turn = [&]() -> bool {
+    if (t == 0) return bursts == 0 || mbar_wait(&s.tok[1], (bursts - 1) & 1u, s.abort, p.timeout_ns, 1);
+    return mbar_wait(&s.tok[0], bursts & 1u, s.abort, p.timeout_ns, 1);
+  };
+  auto pass_turn = [&]() {
+    mbar_arrive(&s.tok[t]);
+    ++bursts;
+  };
+  // an empty tile's burst: stages go by in order, released without use
+  auto pass_stages = [&](int n) -> bool {
+    for (int i = 0; i < n; ++i) {
+      if (!mbar_wait(&s.kv_full[stage], phase, s.abort, p.timeout_ns, 1)) return false;
+      mbar_arrive(&s.kv_empty[stage]);
+      advance();
     }
+    if (!take_turn()) return false;
+    pass_turn();
+    return true;
+  };
+  for (int unit = blockIdx.x; unit < n_units; unit += gridDim.x) {
+    const Unit x = decode(p, unit);
+    if (x.ntq == 0 || x.ntiles == 0) continue;
+    if (t >= x.ntq) {
+      if (!pass_stages(1)) return;                                             // burst of S(0)
+      for (int jt = 0; jt < x.ntiles; ++jt)
+        if (!pass_stages(jt + 1 < x.ntiles ? 2 : 1)) return;                    // bursts of P.V (+ S)
+      continue;
+    }
+    int k_stage = stage;
+    if (!mbar_wait(&s.kv_full[k_stage], phase, s.abort, p.timeout_ns, 1)) return;
+    advance();
+    if (!mbar_wait(&s.q_full[t], q_uses & 1u, s.abort, p.timeout_ns, 1)) return;
+    ++q_uses;
+    if (!take_turn()) return;
+    tc_fence_after();
+    issue_qk(s_tmem, q_base, smem_u32(s.kv + k_stage * ATT_KV_STAGE_BYTES));
+    mma_commit(&s.s_full[t]);
+    if (x.ntiles == 1) mma_commit(&s.q_empty[t]);  // that was the last S_t of the unit
     mma_commit(&s.kv_empty[k_stage]);
+    pass_turn();
     for (int jt = 0; jt < x.ntiles; ++jt) {
       const int v_stage = stage;
       if (!mbar_wait(&s.kv_full[v_stage], phase, s.abort, p.timeout_ns, 1)) return;
-      if (++stage == ATT_STAGES) {
-        stage = 0;
-        phase ^= 1u;
-      }
+      advance();
       const bool has_next = jt + 1 < x.ntiles;
       if (has_next) {
         k_stage = stage;
         if (!mbar_wait(&s.kv_full[k_stage], phase, s.abort, p.timeout_ns, 1)) return;
-        if (++stage == ATT_STAGES) {
-          stage = 0;
-          phase ^= 1u;
-        }
+        advance();
       }
-      const uint32_t v_base = smem_u32(s.kv + v_stage * ATT_KV_STAGE_BYTES);
-      const uint32_t k_base = smem_u32(s.kv + k_stage * ATT_KV_STAGE_BYTES);
-      for (int t = 0; t < x.ntq; ++t) {
-        if (!mbar_wait(&s.p_full[t], p_uses[t] & 1u, s.abort, p.timeout_ns, 1)) return;
-        ++p_uses[t];
-        if (jt == 0) {
-          // the previous unit's epilogue must be done reading O_t
-          if (!mbar_wait(&s.o_empty[t], (o_uses[t] & 1u) ^ 1u, s.abort, p.timeout_ns, 1)) return;
-        }
-        tc_fence_after();
-        issue_pv(tmem + 256 + t * 128, tmem + t * 128, v_base, jt > 0);
-        if (!has_next) {
-          mma_commit(&s.o_full[t]);
-          ++o_uses[t];
-        } else {
-          issue_qk(tmem + t * 128, q_base0 + t * ATT_Q_TILE_BYTES, k_base);
-          mma_commit(&s.s_full[t]);
-          if (jt + 2 == x.ntiles) mma_commit(&s.q_empty[t]);  // last S_t of the unit
-        }
+      if (!mbar_wait(&s.p_full[t], p_uses & 1u, s.abort, p.timeout_ns, 1)) return;
+      ++p_uses;
+      if (jt == 0) {
+        // the previous unit's epilogue must be done reading O_t
+        if (!mbar_wait(&s.o_empty[t], (o_uses & 1u) ^ 1u, s.abort, p.timeout_ns, 1)) return;
       }
+      if (!take_turn()) return;
+      tc_fence_after();
+      issue_pv(o_tmem, s_tmem, smem_u32(s.kv + v_stage * ATT_KV_STAGE_BYTES), jt > 0);
       mma_commit(&s.kv_empty[v_stage]);
-      if (has_next) mma_commit(&s.kv_empty[k_stage]);
+      if (!has_next) {
+        mma_commit(&s.o_full[t]);
+        ++o_uses;
+      } else {
+        issue_qk(s_tmem, q_base, smem_u32(s.kv + k_stage * ATT_KV_STAGE_BYTES));
+        mma_commit(&s.s_full[t]);
+        if (jt + 2 == x.ntiles) mma_commit(&s.q_empty[t]);  // last S_t of the unit
+        mma_commit(&s.kv_empty[k_stage]);
+      }
+      pass_turn();
     }
   }
 }
@@ -433,10 +472,11 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       mbar_init(&s.p_full[i], 128);
       mbar_init(&s.o_full[i], 1);
       mbar_init(&s.o_empty[i], 128);
+      mbar_init(&s.tok[i], 1);
     }
     for (int i = 0; i < ATT_STAGES; ++i) {
       mbar_init(&s.kv_full[i], 1);
-      mbar_init(&s.kv_empty[i], 1);
+      mbar_init(&s.kv_empty[i], 2);  // one release per query tile
     }
     *s.abort = 0;
     fence_barrier_init();
@@ -460,8 +500,8 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(REGS_CONTROL));
     if (warp == 0) {
       if (lane_id() == 0) att_producer(p, s, &tmQ, &tmK, &tmV, n_units);
-    } else if (warp == 1) {
-      if (lane_id() == 0) att_mma(p, s, tmem, n_units);
+    } else if (warp == 1 || warp == 2) {
+      if (lane_id() == 0) att_mma(p, s, tmem, n_units, warp - 1);
     }
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(REGS_SOFTMAX));

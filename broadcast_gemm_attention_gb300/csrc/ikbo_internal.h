@@ -56,24 +56,31 @@ struct LceParams {
   const uint16_t* bias;   // [N] bf16 or null
   uint16_t* Y;            // [n_cand][N][D] bf16
   float* partial;         // [n_users][N][D] fp32 workspace (user GEMM + bias)
-  uint32_t* flags;        // [n_users][n_dblk] readiness epochs
+  uint32_t* flags;        // [n_users][n_dblk][NB] readiness epochs (one per user tile)
   uint32_t* status;
   uint32_t* timeout_epoch;  // set to `epoch` by the first flag wait that times out in a launch
   int n_cand, n_users, K_u, K_c, D, N;
   int N_mma;              // N rounded up to 16
   int NB;                 // 64-wide column blocks of W (ceil(N_mma / 64))
   int n_dblk;             // ceil(D / 128)
-  int n_user_units;       // n_users * n_dblk
-  int n_units;            // (n_users + n_cand) * n_dblk
+  int n_user_units;       // n_users * n_dblk * NB (user tiles are split along N)
+  int n_units;            // n_user_units + n_cand * n_dblk
   int kc_u, kc_c;         // 64-wide K chunks (ceil(K / 64))
   int ks_u, ks_c;         // 16-wide MMA k-steps (ceil(K / 16))
   int stages;             // A ring depth
-  int w_slots;            // B-chunk slots in the W region used by user tiles (2..8)
+  int w_slots;            // 8 KB W_u slots in the W region used by user tiles (2..8)
   uint32_t w_region_bytes;
   uint32_t epoch;         // value written to / awaited in `flags`
   uint32_t debug;
   uint64_t timeout_ns;
 };
+
+// Fills the derived fields of an LceParams from its sizes (n_cand, n_users,
+// K_u, K_c, D, N); returns false for shapes the kernel does not support.
+// Shared by every LCE entry point so they configure the kernel identically.
+bool lce_configure(LceParams* lp, size_t max_smem);
+size_t lce_flag_count(const LceParams& lp);
+size_t lce_smem_bytes(const LceParams& lp);
 
 // ----------------------------------------------------------- attention
 constexpr int ATT_BM = 128;        // query rows per tile (TMEM lanes)
@@ -83,7 +90,7 @@ constexpr int ATT_TILES = 2;       // query tiles per work unit (share K/V)
 constexpr int ATT_THREADS = 384;   // warp 0 TMA, 1 MMA, 2 TMEM, 3 idle, 4-7 / 8-11 softmax
 constexpr int ATT_KV_STAGE_BYTES = ATT_BN * ATT_D * 2;   // 32 KB
 constexpr int ATT_Q_TILE_BYTES = ATT_BM * ATT_D * 2;     // 32 KB
-constexpr int ATT_STAGES = 4;
+constexpr int ATT_STAGES = 5;            // K/V ring: 2 x 32 KB Q + 5 x 32 KB = 224 KB of 227
 
 struct AttnParams {
   const int32_t* perm;

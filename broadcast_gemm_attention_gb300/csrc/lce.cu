@@ -17,7 +17,8 @@
 //     tiles share the launch, user tiles first in every CTA's static order,
 //     and a candidate epilogue acquires the release flag of its user tile.
 //
-// Per CTA (one per SM, all co-resident: cooperative launch):
+// Two launches of one persistent kernel body (one CTA per SM): the user
+// tiles first, then the candidate tiles.  Per CTA:
 //   warp 0  TMA producer   (A ring: U[u] or C[i] chunks; W chunks / resident Wc)
 //   warp 1  MMA issuer     (tcgen05.mma, fp32 accumulators in TMEM, 2 buffers)
 //   warp 2  TMEM owner     (alloc / dealloc of 512 columns)
@@ -71,24 +72,40 @@ __device__ __forceinline__ LceSmem carve(uint8_t* base, const LceParams& p) {
   return s;
 }
 
+// Units: user tiles (u, D block, 64-wide N block) first, then candidate
+// tiles (i, D block) covering all of N.  User tiles are split along N so that
+// the user phase, which every candidate epilogue waits for, is spread over
+// more SMs and each of its tiles loads and writes a third as much.
 struct UnitInfo {
   bool is_user;
   int row;   // user u or candidate i
   int dblk;  // 128-row block of D
+  int nblk;  // user tiles: 64-wide block of N
 };
 
 __device__ __forceinline__ UnitInfo unit_info(const LceParams& p, int unit) {
   UnitInfo x;
   x.is_user = unit < p.n_user_units;
-  const int idx = x.is_user ? unit : unit - p.n_user_units;
-  x.row = idx / p.n_dblk;
-  x.dblk = idx - x.row * p.n_dblk;
+  if (x.is_user) {
+    x.nblk = unit % p.NB;
+    const int ud = unit / p.NB;
+    x.row = ud / p.n_dblk;
+    x.dblk = ud - x.row * p.n_dblk;
+  } else {
+    const int idx = unit - p.n_user_units;
+    x.row = idx / p.n_dblk;
+    x.dblk = idx - x.row * p.n_dblk;
+    x.nblk = 0;
+  }
   return x;
 }
 
+// columns of a user tile's accumulator (a multiple of 16, at most 64)
+__device__ __forceinline__ int user_tile_n(const LceParams& p, int nblk) { return min(64, p.N_mma - nblk * 64); }
+
 // ------------------------------------------------------------ producer
 __device__ void lce_producer(const LceParams& p, const LceSmem& s, const CUtensorMap* tmU, const CUtensorMap* tmC,
-                             const CUtensorMap* tmWu, const CUtensorMap* tmWc) {
+                             const CUtensorMap* tmWu, const CUtensorMap* tmWc, int u0, int u1) {
   int stage = 0;
   uint32_t a_phase = 0;
   int wslot = 0;
@@ -97,7 +114,7 @@ __device__ void lce_producer(const LceParams& p, const LceSmem& s, const CUtenso
   bool wc_loaded = false;
   const uint32_t w_chunk_bytes = static_cast<uint32_t>(p.NB) * BOX_BYTES;
 
-  for (int unit = blockIdx.x; unit < p.n_units; unit += gridDim.x) {
+  for (int unit = u0 + blockIdx.x; unit < u1; unit += gridDim.x) {
     const UnitInfo x = unit_info(p, unit);
     const CUtensorMap* tmA = x.is_user ? tmU : tmC;
     const int kc_n = x.is_user ? p.kc_u : p.kc_c;
@@ -121,10 +138,9 @@ __device__ void lce_producer(const LceParams& p, const LceSmem& s, const CUtenso
       tma_load_3d(dst + BOX_BYTES, tmA, &s.a_full[stage], d0 + 64, kc * LCE_BK, x.row);
       if (x.is_user) {
         if (!mbar_wait(&s.w_empty[wslot], w_phase ^ 1u, s.abort, p.timeout_ns, 1)) return;
-        mbar_arrive_expect_tx(&s.w_full[wslot], w_chunk_bytes);
-        uint8_t* wdst = s.w_region + static_cast<size_t>(wslot) * w_chunk_bytes;
-        for (int nb = 0; nb < p.NB; ++nb)
-          tma_load_2d(wdst + static_cast<size_t>(nb) * BOX_BYTES, tmWu, &s.w_full[wslot], nb * 64, kc * LCE_BK);
+        mbar_arrive_expect_tx(&s.w_full[wslot], BOX_BYTES);
+        tma_load_2d(s.w_region + static_cast<size_t>(wslot) * BOX_BYTES, tmWu, &s.w_full[wslot], x.nblk * 64,
+                    kc * LCE_BK);
         w_uses[wslot] += 1;
         if (++wslot == p.w_slots) {
           wslot = 0;
@@ -140,8 +156,8 @@ __device__ void lce_producer(const LceParams& p, const LceSmem& s, const CUtenso
 }
 
 // ----------------------------------------------------------------- MMA
-__device__ void lce_mma(const LceParams& p, const LceSmem& s, uint32_t tmem) {
-  const uint32_t idesc = idesc_bf16_f32(LCE_BM, static_cast<uint32_t>(p.N_mma), true, true);
+__device__ void lce_mma(const LceParams& p, const LceSmem& s, uint32_t tmem, int u0, int u1) {
+  const uint32_t idesc_c = idesc_bf16_f32(LCE_BM, static_cast<uint32_t>(p.N_mma), true, true);
   const uint32_t w_chunk_bytes = static_cast<uint32_t>(p.NB) * BOX_BYTES;
   int stage = 0;
   uint32_t a_phase = 0;
@@ -149,7 +165,7 @@ __device__ void lce_mma(const LceParams& p, const LceSmem& s, uint32_t tmem) {
   uint32_t w_phase = 0;
   bool wc_ready = false;
   int local = 0;
-  for (int unit = blockIdx.x; unit < p.n_units; unit += gridDim.x, ++local) {
+  for (int unit = u0 + blockIdx.x; unit < u1; unit += gridDim.x, ++local) {
     const UnitInfo x = unit_info(p, unit);
     const int kc_n = x.is_user ? p.kc_u : p.kc_c;
     int ks_left = x.is_user ? p.ks_u : p.ks_c;
@@ -162,13 +178,15 @@ __device__ void lce_mma(const LceParams& p, const LceSmem& s, uint32_t tmem) {
     }
     tc_fence_after();
     const uint32_t d_tmem = tmem + static_cast<uint32_t>(buf) * 256u;
+    const uint32_t idesc =
+        x.is_user ? idesc_bf16_f32(LCE_BM, static_cast<uint32_t>(user_tile_n(p, x.nblk)), true, true) : idesc_c;
     for (int kc = 0; kc < kc_n; ++kc) {
       if (!mbar_wait(&s.a_full[stage], a_phase, s.abort, p.timeout_ns, 1)) return;
       if (x.is_user && !mbar_wait(&s.w_full[wslot], w_phase, s.abort, p.timeout_ns, 1)) return;
       tc_fence_after();
       const uint32_t a_base = smem_u32(s.a_ring + static_cast<size_t>(stage) * LCE_A_STAGE_BYTES);
-      const uint32_t b_base =
-          smem_u32(s.w_region + static_cast<size_t>(x.is_user ? wslot : kc) * w_chunk_bytes);
+      const uint32_t b_base = smem_u32(s.w_region + (x.is_user ? static_cast<size_t>(wslot) * BOX_BYTES
+                                                                  : static_cast<size_t>(kc) * w_chunk_bytes));
       const int nsteps = ks_left < 4 ? ks_left : 4;
       for (int st = 0; st < nsteps; ++st) {
         // 16 k rows of 128 bytes per MMA step; 64-element blocks along M / N are one box apart
@@ -194,34 +212,34 @@ __device__ void lce_mma(const LceParams& p, const LceSmem& s, uint32_t tmem) {
   }
 }
 
-// Wait (one lane per warp polls) until flags[idx] == epoch.  Gives up on an
-// earlier flag timeout anywhere in the launch, or after timeout_ns.
-__device__ __forceinline__ bool wait_user_partial(const LceParams& p, int idx) {
-  int ok = 0;
-  if (lane_id() == 0) {
-    const uint32_t* f = p.flags + idx;
-    if (ld_acquire_gpu(f) == p.epoch) {
-      ok = 1;
-    } else {
-      const uint64_t t0 = globaltimer_ns();
-      for (;;) {
-        if (ld_acquire_gpu(f) == p.epoch) {
-          ok = 1;
-          break;
-        }
-        if (ld_volatile_u32(p.timeout_epoch) == p.epoch) break;  // an earlier wait of this launch gave up
-        if (globaltimer_ns() - t0 > p.timeout_ns) {
+// Wait until every user tile of this launch has published its partial
+// (flags[k] == epoch for all k).  The lanes of the warp poll the flags in
+// parallel, so when they are already set (the user kernel ran first on the
+// stream) this costs one round trip per warp and launch.  Gives up after
+// timeout_ns, or at once if another wait of this launch already gave up.
+__device__ __forceinline__ bool wait_all_user_partials(const LceParams& p) {
+  const int nflags = p.n_user_units;
+  const uint64_t t0 = globaltimer_ns();
+  for (int base = 0; base < nflags; base += 32) {
+    const int k = base + static_cast<int>(lane_id());
+    for (;;) {
+      const bool mine = k >= nflags || ld_acquire_gpu(p.flags + k) == p.epoch;
+      if (__all_sync(0xffffffffu, mine)) break;
+      int give_up = 0;
+      if (lane_id() == 0) {
+        if (ld_volatile_u32(p.timeout_epoch) == p.epoch) {
+          give_up = 1;
+        } else if (globaltimer_ns() - t0 > p.timeout_ns) {
           atomicOr(p.status, DEV_ERR_FLAG_TIMEOUT);
           atomicExch(p.timeout_epoch, p.epoch);
-          break;
+          give_up = 1;
         }
-        __nanosleep(64);
       }
+      if (__shfl_sync(0xffffffffu, give_up, 0)) return false;
+      __nanosleep(256);
     }
   }
-  ok = __shfl_sync(0xffffffffu, ok, 0);
-  if (ok) (void)ld_acquire_gpu(p.flags + idx);  // every lane synchronises with the release
-  return ok != 0;
+  return true;
 }
 
 // ------------------------------------------------------------ epilogue
@@ -231,7 +249,7 @@ __device__ __forceinline__ bool wait_user_partial(const LceParams& p, int idx) {
 // accumulator, so the L2 latency of that gather hides behind the MMA.
 constexpr int EPI_PREFETCH = 3;  // chunks of P held in registers ahead of the accumulator
 
-__device__ void lce_epilogue(const LceParams& p, const LceSmem& s, uint32_t tmem) {
+__device__ void lce_epilogue(const LceParams& p, const LceSmem& s, uint32_t tmem, int u0, int u1) {
   const int warp = threadIdx.x >> 5;
   const int quarter = warp & 3;
   const int half = (warp - LCE_EPI_WARP0) >> 2;
@@ -241,7 +259,8 @@ __device__ void lce_epilogue(const LceParams& p, const LceSmem& s, uint32_t tmem
   const int nchunks = (p.N + 31) / 32;
   int local = 0;
   uint32_t pubs = 0;
-  for (int unit = blockIdx.x; unit < p.n_units; unit += gridDim.x, ++local) {
+  int users_ready = -1;  // candidate tiles: -1 not checked yet, 1 all user partials seen, 0 gave up
+  for (int unit = u0 + blockIdx.x; unit < u1; unit += gridDim.x, ++local) {
     const UnitInfo x = unit_info(p, unit);
     const int buf = local & 1;
     const uint32_t use = static_cast<uint32_t>(local >> 1);
@@ -250,21 +269,29 @@ __device__ void lce_epilogue(const LceParams& p, const LceSmem& s, uint32_t tmem
     const size_t ND = static_cast<size_t>(p.N) * p.D;
     const uint32_t t_acc = tmem + lane_base + static_cast<uint32_t>(buf) * 256u;
     if (x.is_user) {
+      // this tile holds columns n0 .. n0 + nw - 1 of P
+      const int n0 = x.nblk * 64;
+      const int nw = user_tile_n(p, x.nblk);
       if (!mbar_wait(&s.acc_full[buf], use & 1u, s.abort, p.timeout_ns, 1)) return;
       tc_fence_after();
       float* P = p.partial + static_cast<size_t>(x.row) * ND + d;
-      for (int c = half; c < nchunks; c += 2) {
+      for (int c = half; c * 32 < nw; c += 2) {
+        // the bias of this chunk, loaded before any store (the stores could
+        // otherwise alias it and serialise every load behind them)
+        float bias[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const int n = n0 + c * 32 + j;
+          bias[j] = (p.bias && n < p.N) ? __bfloat162float(__ushort_as_bfloat16(__ldg(p.bias + n))) : 0.f;
+        }
         uint32_t v[32];
         tmem_ld32(t_acc + c * 32, v);
         tmem_ld_wait(v);
+        float* pp = P + static_cast<size_t>(n0 + c * 32) * p.D;
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
-          const int n = c * 32 + j;
-          if (n < p.N && dok) {
-            float b = 0.f;
-            if (p.bias) b = __bfloat162float(__ushort_as_bfloat16(p.bias[n]));
-            __stcg(P + static_cast<size_t>(n) * p.D, __uint_as_float(v[j]) + b);
-          }
+          if (n0 + c * 32 + j < p.N && dok) __stcg(pp, __uint_as_float(v[j]) + bias[j]);
+          pp += p.D;
         }
       }
       tc_fence_before();
@@ -277,7 +304,7 @@ __device__ void lce_epilogue(const LceParams& p, const LceSmem& s, uint32_t tmem
         const bool all = mbar_wait(s.pub, pubs & 1u, s.abort, p.timeout_ns, 1);
         if (all && !(p.debug & DEBUG_WITHHOLD_USER_PARTIAL)) {
           __threadfence();
-          st_release_gpu(p.flags + x.row * p.n_dblk + x.dblk, p.epoch);
+          st_release_gpu(p.flags + (x.row * p.n_dblk + x.dblk) * p.NB + x.nblk, p.epoch);
         }
       }
       ++pubs;
@@ -286,7 +313,8 @@ __device__ void lce_epilogue(const LceParams& p, const LceSmem& s, uint32_t tmem
       const int u = p.map[i];
       const bool uok = u >= 0 && u < p.n_users;
       if (!uok && leader) atomicOr(p.status, DEV_ERR_MAP_RANGE);
-      const bool ready = uok && wait_user_partial(p, u * p.n_dblk + x.dblk);
+      if (users_ready < 0) users_ready = wait_all_user_partials(p) ? 1 : 0;
+      const bool ready = uok && users_ready == 1;
       const float* P = p.partial + static_cast<size_t>(uok ? u : 0) * ND + d;
       float pre[EPI_PREFETCH][32];
       if (ready) {
@@ -341,10 +369,17 @@ __device__ void lce_epilogue(const LceParams& p, const LceSmem& s, uint32_t tmem
   }
 }
 
+// One body, two launches: kUserPhase computes the user tiles (P and their
+// release flags), the other launch the candidate tiles, which acquire the
+// flags and add P in their epilogue.  The user launch runs first on the
+// stream, so the candidate launch finds every flag set at its first check.
+template <bool kUserPhase>
 __global__ void __launch_bounds__(LCE_THREADS, 1)
-    lce_fused_kernel(const __grid_constant__ CUtensorMap tmU, const __grid_constant__ CUtensorMap tmC,
-                     const __grid_constant__ CUtensorMap tmWu, const __grid_constant__ CUtensorMap tmWc,
-                     const LceParams p) {
+    lce_kernel(const __grid_constant__ CUtensorMap tmU, const __grid_constant__ CUtensorMap tmC,
+               const __grid_constant__ CUtensorMap tmWu, const __grid_constant__ CUtensorMap tmWc,
+               const LceParams p) {
+  const int u0 = kUserPhase ? 0 : p.n_user_units;
+  const int u1 = kUserPhase ? p.n_user_units : p.n_units;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const LceSmem s = carve(base, p);
@@ -390,13 +425,13 @@ __global__ void __launch_bounds__(LCE_THREADS, 1)
   if (warp < LCE_EPI_WARP0) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 72;");
     if (warp == 0) {
-      if (lane_id() == 0) lce_producer(p, s, &tmU, &tmC, &tmWu, &tmWc);
+      if (lane_id() == 0) lce_producer(p, s, &tmU, &tmC, &tmWu, &tmWc, u0, u1);
     } else if (warp == 1) {
-      if (lane_id() == 0) lce_mma(p, s, tmem);
+      if (lane_id() == 0) lce_mma(p, s, tmem, u0, u1);
     }
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 216;");
-    lce_epilogue(p, s, tmem);
+    lce_epilogue(p, s, tmem, u0, u1);
   }
 
   tc_fence_before();
@@ -410,28 +445,56 @@ __global__ void __launch_bounds__(LCE_THREADS, 1)
 
 }  // namespace
 
+bool lce_configure(LceParams* lp, size_t max_smem) {
+  if (lp->K_u < 1 || lp->K_c < 1 || lp->D < 1 || lp->N < 1 || lp->n_users < 1 || lp->n_cand < 1) return false;
+  if (lp->D % 8 != 0 || lp->N % 8 != 0 || lp->N > 256) return false;
+  lp->N_mma = (lp->N + 15) / 16 * 16;
+  lp->NB = (lp->N_mma + 63) / 64;
+  lp->n_dblk = (lp->D + LCE_BM - 1) / LCE_BM;
+  lp->n_user_units = lp->n_users * lp->n_dblk * lp->NB;
+  lp->n_units = lp->n_user_units + lp->n_cand * lp->n_dblk;
+  lp->kc_u = (lp->K_u + LCE_BK - 1) / LCE_BK;
+  lp->kc_c = (lp->K_c + LCE_BK - 1) / LCE_BK;
+  lp->ks_u = (lp->K_u + 15) / 16;
+  lp->ks_c = (lp->K_c + 15) / 16;
+  const int wc_boxes = lp->kc_c * lp->NB;  // W_c stays resident: one 8 KB box per (K chunk, N block)
+  if (wc_boxes > 16) return false;
+  const int region_boxes = wc_boxes < 2 ? 2 : wc_boxes;
+  lp->w_region_bytes = static_cast<uint32_t>(region_boxes) * BOX_BYTES;
+  lp->w_slots = region_boxes < LCE_MAX_W_SLOTS ? region_boxes : LCE_MAX_W_SLOTS;
+  lp->stages = LCE_MAX_STAGES;
+  while (lp->stages > 2 && lce_smem_bytes(*lp) > max_smem) --lp->stages;
+  return lce_smem_bytes(*lp) <= max_smem;
+}
+
+size_t lce_flag_count(const LceParams& lp) {
+  return static_cast<size_t>(lp.n_users) * lp.n_dblk * lp.NB;
+}
+
 size_t lce_smem_bytes(const LceParams& p) {
   const size_t bars = sizeof(uint64_t) * (2 * p.stages + 2 * p.w_slots + 1 + 4 + 1) + 2 * sizeof(uint32_t);
   return 1024 + p.w_region_bytes + static_cast<size_t>(p.stages) * LCE_A_STAGE_BYTES + bars;
 }
 
-cudaError_t launch_lce(const CUtensorMap& tmU, const CUtensorMap& tmC, const CUtensorMap& tmWu,
-                       const CUtensorMap& tmWc, const LceParams& p, int grid, cudaStream_t s) {
+template <bool kUserPhase>
+cudaError_t launch_phase(const CUtensorMap& tmU, const CUtensorMap& tmC, const CUtensorMap& tmWu,
+                         const CUtensorMap& tmWc, const LceParams& p, int units, int num_sms, cudaStream_t s) {
+  if (units <= 0) return cudaSuccess;
   const size_t smem = lce_smem_bytes(p);
-  cudaError_t e = cudaFuncSetAttribute(lce_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(lce_kernel<kUserPhase>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(LCE_THREADS);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;  // all CTAs co-resident: the flag hand-off needs it
-  attr[0].val.cooperative = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, lce_fused_kernel, tmU, tmC, tmWu, tmWc, p);
+  const int grid = units < num_sms ? units : num_sms;
+  lce_kernel<kUserPhase><<<grid, LCE_THREADS, smem, s>>>(tmU, tmC, tmWu, tmWc, p);
+  return cudaGetLastError();
+}
+
+// Two launches on one stream: the user tiles, then the candidate tiles.
+cudaError_t launch_lce(const CUtensorMap& tmU, const CUtensorMap& tmC, const CUtensorMap& tmWu,
+                       const CUtensorMap& tmWc, const LceParams& p, int num_sms, cudaStream_t s) {
+  cudaError_t e = launch_phase<true>(tmU, tmC, tmWu, tmWc, p, p.n_user_units, num_sms, s);
+  if (e != cudaSuccess) return e;
+  return launch_phase<false>(tmU, tmC, tmWu, tmWc, p, p.n_units - p.n_user_units, num_sms, s);
 }
 
 }  // namespace ikbo

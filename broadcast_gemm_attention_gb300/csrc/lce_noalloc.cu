@@ -29,9 +29,8 @@
 #include "ikbo_internal.h"
 
 namespace ikbo {
-size_t lce_smem_bytes(const LceParams& p);
 cudaError_t launch_lce(const CUtensorMap& tmU, const CUtensorMap& tmC, const CUtensorMap& tmWu,
-                       const CUtensorMap& tmWc, const LceParams& p, int grid, cudaStream_t s);
+                       const CUtensorMap& tmWc, const LceParams& p, int num_sms, cudaStream_t s);
 }  // namespace ikbo
 
 using namespace ikbo;
@@ -147,22 +146,11 @@ extern "C" ikbo_status_t ikbo_lce_forward_noalloc(const int32_t* d_map, int n_ca
   lp.K_c = K_c;
   lp.D = D;
   lp.N = N;
-  lp.N_mma = (N + 15) / 16 * 16;
-  lp.NB = (lp.N_mma + 63) / 64;
-  lp.n_dblk = (D + LCE_BM - 1) / LCE_BM;
-  lp.n_user_units = n_users * lp.n_dblk;
-  lp.n_units = (n_users + n_cand) * lp.n_dblk;
-  lp.kc_u = (K_u + LCE_BK - 1) / LCE_BK;
-  lp.kc_c = (K_c + LCE_BK - 1) / LCE_BK;
-  lp.ks_u = (K_u + 15) / 16;
-  lp.ks_c = (K_c + 15) / 16;
-  if (lp.kc_c * lp.NB > 16) return IKBO_ERR_UNSUPPORTED;
-  const int region_chunks = lp.kc_c < 2 ? 2 : lp.kc_c;
-  lp.w_region_bytes = static_cast<uint32_t>(region_chunks) * lp.NB * 64 * 64 * 2;
-  lp.w_slots = region_chunks < LCE_MAX_W_SLOTS ? region_chunks : LCE_MAX_W_SLOTS;
+  // shapes only here; the shared-memory limit is checked once the device is known
+  if (!lce_configure(&lp, SIZE_MAX)) return IKBO_ERR_UNSUPPORTED;
 
   // scratch layout: control words | flags [n_users][n_dblk] | partial [n_users][N][D] fp32
-  const size_t flag_bytes = round256(sizeof(uint32_t) * static_cast<size_t>(n_users) * lp.n_dblk);
+  const size_t flag_bytes = round256(sizeof(uint32_t) * lce_flag_count(lp));
   const size_t part_bytes = sizeof(float) * static_cast<size_t>(n_users) * N * D;
   if (kControlBytes + flag_bytes + part_bytes > kNoallocScratchBytes) return IKBO_ERR_UNSUPPORTED;
 
@@ -176,9 +164,7 @@ extern "C" ikbo_status_t ikbo_lce_forward_noalloc(const int32_t* d_map, int n_ca
     epoch = ++slot->epoch;
     if (epoch == 0) epoch = ++slot->epoch;  // flags start at zero; zero is never a live epoch
   }
-  lp.stages = LCE_MAX_STAGES;
-  while (lp.stages > 2 && lce_smem_bytes(lp) > slot->max_smem) --lp.stages;
-  if (lce_smem_bytes(lp) > slot->max_smem) return IKBO_ERR_UNSUPPORTED;
+  if (!lce_configure(&lp, slot->max_smem)) return IKBO_ERR_UNSUPPORTED;
 
   unsigned char* base = slot->scratch;
   lp.map = d_map;
@@ -208,7 +194,6 @@ extern "C" ikbo_status_t ikbo_lce_forward_noalloc(const int32_t* d_map, int n_ca
 
   // the status words must start at zero for this call (the flags do not: see epoch)
   if (cudaMemsetAsync(base, 0, 2 * sizeof(uint32_t), stream) != cudaSuccess) return IKBO_ERR_CUDA;
-  const int grid = lp.n_units < slot->num_sms ? lp.n_units : slot->num_sms;
-  if (launch_lce(tmU, tmC, tmWu, tmWc, lp, grid, stream) != cudaSuccess) return IKBO_ERR_CUDA;
+  if (launch_lce(tmU, tmC, tmWu, tmWc, lp, slot->num_sms, stream) != cudaSuccess) return IKBO_ERR_CUDA;
   return IKBO_OK;
 }
