@@ -86,11 +86,12 @@ size_t lce_smem_bytes(const LceParams& lp);
 constexpr int ATT_BM = 128;        // query rows per tile (TMEM lanes)
 constexpr int ATT_BN = 128;        // keys per K/V tile
 constexpr int ATT_D = 128;         // head dim (the only one supported)
-constexpr int ATT_TILES = 2;       // query tiles per work unit (share K/V)
-constexpr int ATT_THREADS = 384;   // warp 0 TMA, 1 MMA, 2 TMEM, 3 idle, 4-7 / 8-11 softmax
+constexpr int ATT_TILES = 1;       // query tiles per work unit
+constexpr int ATT_THREADS = 256;   // warp 0 TMA, 1 S issuer, 2 P.V issuer, 3 idle, 4-7 softmax
 constexpr int ATT_KV_STAGE_BYTES = ATT_BN * ATT_D * 2;   // 32 KB
 constexpr int ATT_Q_TILE_BYTES = ATT_BM * ATT_D * 2;     // 32 KB
-constexpr int ATT_STAGES = 5;            // K/V ring: 2 x 32 KB Q + 5 x 32 KB = 224 KB of 227
+constexpr int ATT_Q_BUFS = 2;      // Q landing buffers (the next unit's Q loads early)
+constexpr int ATT_STAGES = 5;      // K/V ring: 2 x 32 KB Q + 5 x 32 KB = 224 KB of 227
 
 struct AttnParams {
   const int32_t* perm;

@@ -154,7 +154,7 @@ ikbo_status_t ikbo_lce_forward_noalloc(const int32_t* d_map, int n_cand, int n_u
  *   O bf16 [n_cand][H][Lq][d] (written; rows whose user has no keys get 0)
  *   scale  > 0 (usually 1/sqrt(d)).  No mask.
  * Each user's K/V tile is read once per work unit and shared by up to
- * 2*floor(128/Lq) candidates.  fp32 scores and softmax, P rounded to bf16
+ * floor(128/Lq) candidates.  fp32 scores and softmax, P rounded to bf16
  * for P.V, fp32 accumulation, bf16 output.  Limits: d == 128. */
 ikbo_status_t ikbo_attn_forward(ikbo_plan_t p, const void* Q, const void* K, const void* V,
                                 const int32_t* d_kv_offsets, void* O, int Lkv, int d, float scale,

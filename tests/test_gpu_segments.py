@@ -33,7 +33,7 @@ def test_segments_bit_exact(name, m, n_users, H, Lq):
         assert p.status() == B.IKBO_OK
         counts, offsets, perm = p.segments(n, n_users)
         work, cpu = p.worklist()
-        assert cpu == 2 * (128 // Lq)
+        assert cpu == 128 // Lq
         c, o, pm, w = oracle.segments(m, n_users, H, cpu)
         assert np.array_equal(counts.numpy(), c)
         assert np.array_equal(offsets.numpy(), o)
