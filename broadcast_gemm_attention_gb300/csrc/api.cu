@@ -269,7 +269,7 @@ ikbo_status_t ikbo_plan_get_status(ikbo_plan_t p, cudaStream_t stream) {
   if (word && cudaMemset(p->d_status, 0, sizeof(uint32_t)) != cudaSuccess) return IKBO_ERR_CUDA;
   if (word & DEV_ERR_MAP_RANGE) return IKBO_ERR_MAP_OUT_OF_RANGE;
   if (word & (DEV_ERR_FLAG_TIMEOUT | DEV_ERR_PIPE_TIMEOUT)) return IKBO_ERR_TIMEOUT;
-  if (word & DEV_ERR_BAD_WORK) return IKBO_ERR_INTERNAL;
+  if (word & (DEV_ERR_BAD_WORK | DEV_ERR_SMEM_LAYOUT)) return IKBO_ERR_INTERNAL;
   return IKBO_OK;
 }
 

@@ -14,24 +14,30 @@
 // are adjacent in the work list, so neighbouring CTAs stream the same K/V
 // through L2.
 //
-// Per CTA (persistent, one per SM, 8 warps):
+// Per CTA (persistent, one per SM, 12 warps):
 //   warp 0      TMA producer: the unit's Q tile (one box per candidate and
-//               d-half, gathered through perm) into one of two landing
-//               buffers; K and V tiles of 128 keys through a 5-stage ring
+//               d-half, gathered through perm) into the Q landing buffer;
+//               K and V tiles of 128 keys through a 6-stage ring
 //   warp 1      S issuer and TMEM owner: S = Q K^T into S0 / S1 alternately
 //   warp 2      P.V issuer: O += P V
 //   warp 3      idle
-//   warps 4-7   softmax + epilogue (one thread per query row = TMEM lane)
+//   warps 4-11  softmax + epilogue.  Warps w and w+4 share the 32 TMEM lanes
+//               (query rows) of quarter w % 4 and split the 128 key columns
+//               of a tile (and the 128 d columns of O) into halves; they
+//               exchange their row maxima through shared memory.  Two warps
+//               per scheduler hide the exp2 / convert latency that one warp
+//               alone cannot.
 // TMEM (512 columns): S0 S1 (128 each, fp32), P (64, bf16 pairs), Q (64,
-// bf16 pairs), O (128, fp32).  Both products take A from TMEM, so shared
-// memory only feeds K, V and the TMA writes.
+// bf16 pairs), O (128, fp32).
 //
-// Why two issuers and a separate P: one thread can issue a tcgen05.mma only
-// every ~128 cycles, while an M=128, N=128, K=16 product needs 64 cycles of
-// the tensor pipe, so a lone issuer leaves the pipe half idle.  Here S(j+2)
-// can be issued as soon as the softmax has read S(j) out of its buffer, and
-// P.V(j-1) as soon as P(j-1) is written, so both issuers are busy while the
-// softmax of tile j runs and the softmax itself never waits for a product.
+// Why two issuers and a separate P: one thread issues a tcgen05.mma only
+// every ~80-130 cycles, while an M=128, N=128, K=16 product needs 64 cycles
+// of the tensor pipe, so one chain of products leaves the pipe partly idle.
+// S(j+2) is issued as soon as the softmax has read S(j) out of its buffer
+// and P.V(j-1) as soon as P(j-1) is written, so the two chains overlap.
+// The first two S of a unit take Q from the landing buffer in shared memory
+// (the softmax warps copy it into TMEM meanwhile); later ones read it from
+// TMEM.
 //
 // Online softmax in fp32 in the log2 domain (exp2 with scale*log2(e) folded
 // in); the running max is only moved when it grows by more than 2^8, so O is
@@ -48,47 +54,62 @@ namespace {
 constexpr uint32_t HALF_TILE = ATT_BM * 64 * 2;  // 128 rows x 64 bf16 = 16 KB (Q and K/V tiles alike)
 constexpr float RESCALE_THRESHOLD = 8.0f;          // log2 units
 constexpr int SOFTMAX_WARP0 = 4;                   // first softmax warp
+constexpr int SOFTMAX_THREADS = ATT_THREADS - 32 * SOFTMAX_WARP0;
 constexpr uint32_t TM_S = 0;                       // S_b at TM_S + 128 b
 constexpr uint32_t TM_P = 256;
 constexpr uint32_t TM_Q = 320;
 constexpr uint32_t TM_O = 384;
 
+// dynamic shared memory: [Q landing][K/V ring] (1024-aligned for the
+// 128-byte swizzle), then the barriers, two words, and the row exchange
+constexpr uint32_t TILE_REGION = ATT_Q_BUFS * ATT_Q_TILE_BYTES + ATT_STAGES * ATT_KV_STAGE_BYTES;
+constexpr int NUM_BARS = 11 + 2 * ATT_STAGES + 8;
+constexpr uint32_t XVAL_OFFSET = NUM_BARS * 8 + 8;
+constexpr uint32_t AUX_BYTES = XVAL_OFFSET + 2 * 2 * ATT_BM * 4;
+constexpr uint32_t SMEM_USED = TILE_REGION + AUX_BYTES;
+constexpr uint32_t SMEM_ALLOC = 227 * 1024;
+static_assert(SMEM_USED <= SMEM_ALLOC, "attention tiles do not fit in shared memory");
+
 struct AttSmem {
-  uint8_t* q;          // ATT_Q_BUFS landing buffers x 32 KB
+  uint8_t* q;          // Q landing buffer, 32 KB
   uint8_t* kv;         // ATT_STAGES x 32 KB
-  uint64_t* q_full;    // [2] landing buffer loaded
-  uint64_t* q_empty;   // [2] landing buffer copied into TMEM
+  uint64_t* q_full;    // Q landed
+  uint64_t* q_empty;   // Q copied into TMEM and read by the first S products
   uint64_t* qt_ready;  // Q of the unit is in TMEM
-  uint64_t* kv_full;
-  uint64_t* kv_empty;
   uint64_t* s_full;    // [2] S_b computed
   uint64_t* s_free;    // [2] S_b read by the softmax
   uint64_t* p_full;    // P written
   uint64_t* pv_done;   // a P.V completed (P is free again, O is up to date)
   uint64_t* o_full;    // the unit's last P.V completed
   uint64_t* o_empty;   // the unit's epilogue has read O
+  uint64_t* kv_full;
+  uint64_t* kv_empty;
+  uint64_t* xbar;      // [4 quarters][2] row exchange between the two warps of a quarter
   uint32_t* tmem_slot;
   uint32_t* abort;
+  float* xval;         // [2 buffers][2 halves][128 rows]
 };
 
 __device__ __forceinline__ AttSmem carve(uint8_t* base) {
   AttSmem s;
   s.q = base;
   s.kv = base + ATT_Q_BUFS * ATT_Q_TILE_BYTES;
-  uint64_t* b = reinterpret_cast<uint64_t*>(s.kv + ATT_STAGES * ATT_KV_STAGE_BYTES);
+  uint64_t* b = reinterpret_cast<uint64_t*>(base + TILE_REGION);
   s.q_full = b;
-  s.q_empty = b + 2;
-  s.qt_ready = b + 4;
-  s.kv_full = b + 5;
+  s.q_empty = b + 1;
+  s.qt_ready = b + 2;
+  s.s_full = b + 3;
+  s.s_free = b + 5;
+  s.p_full = b + 7;
+  s.pv_done = b + 8;
+  s.o_full = b + 9;
+  s.o_empty = b + 10;
+  s.kv_full = b + 11;
   s.kv_empty = s.kv_full + ATT_STAGES;
-  s.s_full = s.kv_empty + ATT_STAGES;
-  s.s_free = s.s_full + 2;
-  s.p_full = s.s_free + 2;
-  s.pv_done = s.p_full + 1;
-  s.o_full = s.pv_done + 1;
-  s.o_empty = s.o_full + 1;
-  s.tmem_slot = reinterpret_cast<uint32_t*>(s.o_empty + 1);
+  s.xbar = s.kv_empty + ATT_STAGES;
+  s.tmem_slot = reinterpret_cast<uint32_t*>(base + TILE_REGION + NUM_BARS * 8);
   s.abort = s.tmem_slot + 1;
+  s.xval = reinterpret_cast<float*>(base + TILE_REGION + XVAL_OFFSET);
   return s;
 }
 
@@ -100,8 +121,14 @@ struct Unit {
   int ntiles;  // ceil(L / 128)
 };
 
-__device__ __forceinline__ Unit decode(const AttnParams& p, int unit) {
-  const int4 w = reinterpret_cast<const int4*>(p.work)[unit];
+// The work entry is loaded one unit ahead (the load is issued early and only
+// waited for where the entry is first used) so the dependent reads of the
+// next unit stay off the critical path.
+__device__ __forceinline__ int4 load_work(const AttnParams& p, int unit, int n_units) {
+  return unit < n_units ? __ldg(reinterpret_cast<const int4*>(p.work) + unit) : make_int4(-1, -1, -1, -1);
+}
+
+__device__ __forceinline__ Unit decode(const AttnParams& p, int4 w) {
   Unit x;
   x.u = w.x;
   x.h = w.y;
@@ -166,45 +193,74 @@ __device__ __forceinline__ void tmem_st32p(uint32_t taddr, const uint32_t* r) {
 }
 
 // ------------------------------------------------------------ producer
+// Candidate ids of a unit's Q slots (empty slots read one past the last
+// candidate: TMA fills them with zeros).  At most 16 slots (Lq >= 8).
+struct QSlots {
+  int cand[16];
+};
+
+__device__ __forceinline__ void load_slots(const AttnParams& p, const Unit& x, QSlots& q) {
+#pragma unroll
+  for (int j = 0; j < 16; ++j) q.cand[j] = (x.ok && j < x.cnt) ? __ldg(p.perm + x.start + j) : p.n_cand;
+}
+
 __device__ void att_producer(const AttnParams& p, const AttSmem& s, const CUtensorMap* tmQ, const CUtensorMap* tmK,
                              const CUtensorMap* tmV, int n_units) {
   uint32_t c = 0;   // K/V loads issued
   uint32_t qc = 0;  // Q tiles loaded
   const int cpt = p.cands_per_tile;
-  for (int unit = blockIdx.x; unit < n_units; unit += gridDim.x) {
-    const Unit x = decode(p, unit);
-    if (!x.ok) {
-      atomicOr(p.status, DEV_ERR_BAD_WORK);
-      continue;
-    }
-    if (x.ntiles == 0) continue;
-    const int qb = static_cast<int>(qc & 1u);
-    if (!mbar_wait(&s.q_empty[qb], ((qc >> 1) & 1u) ^ 1u, s.abort, p.timeout_ns, 1)) return;
-    ++qc;
-    mbar_arrive_expect_tx(&s.q_full[qb], static_cast<uint32_t>(cpt * p.Lq * ATT_D * 2));
-    for (int j = 0; j < cpt; ++j) {
-      // empty slots read one past the last candidate: TMA fills them with zeros
-      const int cand = j < x.cnt ? p.perm[x.start + j] : p.n_cand;
-      uint8_t* dst = s.q + qb * ATT_Q_TILE_BYTES + j * p.Lq * 128;
-      tma_load_4d(dst, tmQ, &s.q_full[qb], 0, 0, x.h, cand);
-      tma_load_4d(dst + HALF_TILE, tmQ, &s.q_full[qb], 64, 0, x.h, cand);
-    }
-    for (int jt = 0; jt < x.ntiles; ++jt) {
-      for (int kv = 0; kv < 2; ++kv, ++c) {
-        const int st = ring_stage(c);
-        if (!mbar_wait(&s.kv_empty[st], ring_phase(c) ^ 1u, s.abort, p.timeout_ns, 1)) return;
-        mbar_arrive_expect_tx(&s.kv_full[st], ATT_KV_STAGE_BYTES);
-        uint8_t* dst = s.kv + st * ATT_KV_STAGE_BYTES;
-        const CUtensorMap* tm = kv == 0 ? tmK : tmV;
-        if (p.kv_offsets) {
-          tma_load_3d(dst, tm, &s.kv_full[st], 0, x.h, x.kv0 + jt * ATT_BN);
-          tma_load_3d(dst + HALF_TILE, tm, &s.kv_full[st], 64, x.h, x.kv0 + jt * ATT_BN);
-        } else {
-          tma_load_4d(dst, tm, &s.kv_full[st], 0, jt * ATT_BN, x.h, x.u);
-          tma_load_4d(dst + HALF_TILE, tm, &s.kv_full[st], 64, jt * ATT_BN, x.h, x.u);
+  int unit = blockIdx.x;
+  Unit x = decode(p, load_work(p, unit, n_units));
+  QSlots qs;
+  load_slots(p, x, qs);
+  while (unit < n_units) {
+    const int nunit = unit + static_cast<int>(gridDim.x);
+    const int4 nw = load_work(p, nunit, n_units);
+    Unit nx;
+    QSlots nqs;
+    bool prefetched = false;
+    if (!x.ok) atomicOr(p.status, DEV_ERR_BAD_WORK);
+    if (x.ntiles > 0) {
+      if (!mbar_wait(s.q_empty, (qc & 1u) ^ 1u, s.abort, p.timeout_ns, 1)) return;
+      ++qc;
+      mbar_arrive_expect_tx(s.q_full, static_cast<uint32_t>(cpt * p.Lq * ATT_D * 2));
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        if (j < cpt) {
+          uint8_t* dst = s.q + j * p.Lq * 128;
+          tma_load_4d(dst, tmQ, s.q_full, 0, 0, x.h, qs.cand[j]);
+          tma_load_4d(dst + HALF_TILE, tmQ, s.q_full, 64, 0, x.h, qs.cand[j]);
+        }
+      }
+      for (int jt = 0; jt < x.ntiles; ++jt) {
+        for (int kv = 0; kv < 2; ++kv, ++c) {
+          const int st = ring_stage(c);
+          if (!mbar_wait(&s.kv_empty[st], ring_phase(c) ^ 1u, s.abort, p.timeout_ns, 1)) return;
+          mbar_arrive_expect_tx(&s.kv_full[st], ATT_KV_STAGE_BYTES);
+          uint8_t* dst = s.kv + st * ATT_KV_STAGE_BYTES;
+          const CUtensorMap* tm = kv == 0 ? tmK : tmV;
+          if (p.kv_offsets) {
+            tma_load_3d(dst, tm, &s.kv_full[st], 0, x.h, x.kv0 + jt * ATT_BN);
+            tma_load_3d(dst + HALF_TILE, tm, &s.kv_full[st], 64, x.h, x.kv0 + jt * ATT_BN);
+          } else {
+            tma_load_4d(dst, tm, &s.kv_full[st], 0, jt * ATT_BN, x.h, x.u);
+            tma_load_4d(dst + HALF_TILE, tm, &s.kv_full[st], 64, jt * ATT_BN, x.h, x.u);
+          }
+          if (!prefetched) {  // the next unit's entry has arrived by now
+            prefetched = true;
+            nx = decode(p, nw);
+            load_slots(p, nx, nqs);
+          }
         }
       }
     }
+    if (!prefetched) {
+      nx = decode(p, nw);
+      load_slots(p, nx, nqs);
+    }
+    x = nx;
+    qs = nqs;
+    unit = nunit;
   }
 }
 
@@ -213,9 +269,9 @@ __device__ void att_producer(const AttnParams& p, const AttSmem& s, const CUtens
 // to the start-address field; shared memory is below 256 KB, so the 14-bit
 // field never carries into the next one.
 //
-// S = Q K^T: A = Q (TMEM, 16 d per step = 8 columns), B = K tile (K-major,
-// 128 keys x 128 d as two 64-wide d halves; steps 0-3 advance 32 bytes
-// inside the swizzled rows of the first half, 4-7 in the second).
+// S = Q K^T with K-major operands (128 rows x 128 d as two 64-wide d halves;
+// steps 0-3 advance 32 bytes inside the swizzled rows of the first half,
+// 4-7 in the second).  A = Q from TMEM (16 d per step = 8 columns) ...
 __device__ __forceinline__ void issue_qk(uint32_t s_tmem, uint32_t q_tmem, uint32_t k_base) {
   constexpr uint32_t idesc = idesc_bf16_f32(ATT_BM, ATT_BN, false, false);
   const uint64_t kd = sdesc_sw128(k_base, 16, 1024);
@@ -223,6 +279,18 @@ __device__ __forceinline__ void issue_qk(uint32_t s_tmem, uint32_t q_tmem, uint3
   for (int ks = 0; ks < 8; ++ks) {
     const uint32_t off = ((ks >> 2) * HALF_TILE + (ks & 3) * 32) >> 4;
     mma_bf16_ts(s_tmem, q_tmem + ks * 8, kd + off, idesc, ks > 0 ? 1u : 0u);
+  }
+}
+
+// ... or from the landing buffer in shared memory (same layout as K).
+__device__ __forceinline__ void issue_qk_ss(uint32_t s_tmem, uint32_t q_base, uint32_t k_base) {
+  constexpr uint32_t idesc = idesc_bf16_f32(ATT_BM, ATT_BN, false, false);
+  const uint64_t qd = sdesc_sw128(q_base, 16, 1024);
+  const uint64_t kd = sdesc_sw128(k_base, 16, 1024);
+#pragma unroll
+  for (int ks = 0; ks < 8; ++ks) {
+    const uint32_t off = ((ks >> 2) * HALF_TILE + (ks & 3) * 32) >> 4;
+    mma_bf16_ss(s_tmem, qd + off, kd + off, idesc, ks > 0 ? 1u : 0u);
   }
 }
 
@@ -241,22 +309,40 @@ __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint3
 // S issuer: tile g goes to S_(g&1) once the softmax has read S(g-2) out of it.
 __device__ void att_s_issuer(const AttnParams& p, const AttSmem& s, uint32_t tmem, int n_units) {
   uint32_t g = 0, qu = 0;
-  for (int unit = blockIdx.x; unit < n_units; unit += gridDim.x) {
-    const Unit x = decode(p, unit);
-    if (x.ntiles == 0) continue;
-    if (!mbar_wait(s.qt_ready, qu & 1u, s.abort, p.timeout_ns, 1)) return;
-    ++qu;
-    for (int jt = 0; jt < x.ntiles; ++jt, ++g) {
-      const int b = static_cast<int>(g & 1u);
-      const uint32_t n = g >> 1;
-      const uint32_t kc = 2 * g;
-      if (!mbar_wait(&s.kv_full[ring_stage(kc)], ring_phase(kc), s.abort, p.timeout_ns, 1)) return;
-      if (n > 0 && !mbar_wait(&s.s_free[b], (n - 1) & 1u, s.abort, p.timeout_ns, 1)) return;
-      tc_fence_after();
-      issue_qk(tmem + TM_S + b * 128, tmem + TM_Q, smem_u32(s.kv + ring_stage(kc) * ATT_KV_STAGE_BYTES));
-      mma_commit(&s.s_full[b]);
-      mma_commit(&s.kv_empty[ring_stage(kc)]);
+  int unit = blockIdx.x;
+  int4 w = load_work(p, unit, n_units);
+  while (unit < n_units) {
+    const int nunit = unit + static_cast<int>(gridDim.x);
+    const int4 nw = load_work(p, nunit, n_units);
+    const Unit x = decode(p, w);
+    if (x.ntiles > 0) {
+      const int last_ss = min(1, x.ntiles - 1);
+      for (int jt = 0; jt < x.ntiles; ++jt, ++g) {
+        const int b = static_cast<int>(g & 1u);
+        const uint32_t n = g >> 1;
+        const uint32_t kc = 2 * g;
+        if (!mbar_wait(&s.kv_full[ring_stage(kc)], ring_phase(kc), s.abort, p.timeout_ns, 1)) return;
+        if (n > 0 && !mbar_wait(&s.s_free[b], (n - 1) & 1u, s.abort, p.timeout_ns, 1)) return;
+        const uint32_t k_base = smem_u32(s.kv + ring_stage(kc) * ATT_KV_STAGE_BYTES);
+        if (jt <= last_ss) {
+          if (jt == 0 && !mbar_wait(s.q_full, qu & 1u, s.abort, p.timeout_ns, 1)) return;
+          tc_fence_after();
+          issue_qk_ss(tmem + TM_S + b * 128, smem_u32(s.q), k_base);
+        } else {
+          // skipped for units of at most two tiles: the softmax's next arrival
+          // needs this unit's S, so the barrier never runs two phases ahead
+          if (jt == last_ss + 1 && !mbar_wait(s.qt_ready, qu & 1u, s.abort, p.timeout_ns, 1)) return;
+          tc_fence_after();
+          issue_qk(tmem + TM_S + b * 128, tmem + TM_Q, k_base);
+        }
+        mma_commit(&s.s_full[b]);
+        mma_commit(&s.kv_empty[ring_stage(kc)]);
+        if (jt == last_ss) mma_commit(s.q_empty);  // the landing buffer's last reader
+      }
+      ++qu;
     }
+    w = nw;
+    unit = nunit;
   }
 }
 
@@ -264,9 +350,12 @@ __device__ void att_s_issuer(const AttnParams& p, const AttSmem& s, uint32_t tme
 // for the previous unit's epilogue to have read O.
 __device__ void att_pv_issuer(const AttnParams& p, const AttSmem& s, uint32_t tmem, int n_units) {
   uint32_t g = 0, ou = 0;
-  for (int unit = blockIdx.x; unit < n_units; unit += gridDim.x) {
-    const Unit x = decode(p, unit);
-    if (x.ntiles == 0) continue;
+  int unit = blockIdx.x;
+  int4 w = load_work(p, unit, n_units);
+  while (unit < n_units) {
+    const int nunit = unit + static_cast<int>(gridDim.x);
+    const int4 nw = load_work(p, nunit, n_units);
+    const Unit x = decode(p, w);
     for (int jt = 0; jt < x.ntiles; ++jt, ++g) {
       const uint32_t vc = 2 * g + 1;
       if (!mbar_wait(s.p_full, g & 1u, s.abort, p.timeout_ns, 1)) return;
@@ -281,26 +370,51 @@ __device__ void att_pv_issuer(const AttnParams& p, const AttSmem& s, uint32_t tm
         ++ou;
       }
     }
+    w = nw;
+    unit = nunit;
   }
 }
 
 // ---------------------------------------------------- softmax + epilogue
+struct Lane {
+  int quarter, half, r;
+  uint32_t xc;  // exchanges done with the partner warp
+};
+
+// Hands `mine` to the other warp of the quarter and returns its value for
+// the same row.  Double-buffered by exchange count: a warp refills a buffer
+// only after passing the next exchange, i.e. after its partner has read it.
+__device__ __forceinline__ bool pair_exchange(const AttnParams& p, const AttSmem& s, Lane& ln, float mine,
+                                              float& theirs) {
+  const uint32_t buf = ln.xc & 1u;
+  s.xval[buf * 256 + ln.half * 128 + ln.r] = mine;
+  uint64_t* bar = &s.xbar[ln.quarter * 2 + buf];
+  mbar_arrive(bar);
+  if (!mbar_wait(bar, (ln.xc >> 1) & 1u, s.abort, p.timeout_ns, 1)) return false;
+  theirs = s.xval[buf * 256 + (ln.half ^ 1) * 128 + ln.r];
+  ++ln.xc;
+  return true;
+}
+
 struct RowOut {
   bool pending;  // a finished unit whose O has not been written yet
   bool valid;    // this thread's row belongs to a candidate of that unit
   __nv_bfloat16* row;
-  float l;
+  float l;       // this warp's half of the row sum
 };
 
-// O / l -> bf16 -> the row of O in global memory; then O may be overwritten.
+// O / l -> bf16 -> this warp's half of the row of O; then O may be overwritten.
 __device__ __forceinline__ bool att_epilogue(const AttnParams& p, const AttSmem& s, uint32_t Ot, const RowOut& ro,
-                                             uint32_t& ou) {
+                                             Lane& ln, uint32_t& ou) {
+  float lp;
+  if (!pair_exchange(p, s, ln, ro.l, lp)) return false;
+  const float l = ro.l + lp;
   if (!mbar_wait(s.o_full, ou & 1u, s.abort, p.timeout_ns, 1)) return false;
   ++ou;
   tc_fence_after();
-  const float inv = ro.l > 0.f ? 1.0f / ro.l : 0.f;
+  const float inv = l > 0.f ? 1.0f / l : 0.f;
 #pragma unroll
-  for (int c = 0; c < 4; ++c) {
+  for (int c = 0; c < 2; ++c) {
     uint32_t o[32];
     tmem_ld32(Ot + c * 32, o);
     tmem_ld_wait(o);
@@ -309,7 +423,7 @@ __device__ __forceinline__ bool att_epilogue(const AttnParams& p, const AttSmem&
 #pragma unroll
       for (int j = 0; j < 16; ++j)
         pk[j] = pack_bf16x2(__uint_as_float(o[2 * j]) * inv, __uint_as_float(o[2 * j + 1]) * inv);
-      uint4* dst = reinterpret_cast<uint4*>(ro.row + c * 32);
+      uint4* dst = reinterpret_cast<uint4*>(ro.row + ln.half * 64 + c * 32);
 #pragma unroll
       for (int k = 0; k < 4; ++k) dst[k] = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
     }
@@ -321,171 +435,201 @@ __device__ __forceinline__ bool att_epilogue(const AttnParams& p, const AttSmem&
 
 __device__ void att_softmax(const AttnParams& p, const AttSmem& s, uint32_t tmem, int n_units) {
   const int warp = threadIdx.x >> 5;
-  const int quarter = warp & 3;                                    // TMEM lane quarter of this warp
-  const int r = (quarter << 5) + static_cast<int>(lane_id());     // row = TMEM lane
-  const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-  const uint32_t Pt = tmem + lane_base + TM_P;
-  const uint32_t Qt = tmem + lane_base + TM_Q;
-  const uint32_t Ot = tmem + lane_base + TM_O;
+  Lane ln;
+  ln.quarter = warp & 3;                                     // TMEM lane quarter of this warp
+  ln.half = (warp - SOFTMAX_WARP0) >> 2;                     // column half of this warp
+  ln.r = (ln.quarter << 5) + static_cast<int>(lane_id());    // row = TMEM lane
+  ln.xc = 0;
+  const int half = ln.half;
+  const uint32_t lane_base = static_cast<uint32_t>(ln.quarter * 32) << 16;
+  const uint32_t St = tmem + lane_base + TM_S + half * 64;
+  const uint32_t Pt = tmem + lane_base + TM_P + half * 32;
+  const uint32_t Qt = tmem + lane_base + TM_Q + half * 32;
+  const uint32_t Ot = tmem + lane_base + TM_O + half * 64;
   const float sl = p.scale_log2;
+  const int slot = ln.r / p.Lq;
+  const int qrow = ln.r % p.Lq;
+  const bool row_in_tile = ln.r < p.cands_per_tile * p.Lq;
   uint32_t g = 0, qc = 0, ou = 0;
   RowOut prev = {false, false, nullptr, 0.f};
 
-  for (int unit = blockIdx.x; unit < n_units; unit += gridDim.x) {
-    const Unit x = decode(p, unit);
-    const int slot = r / p.Lq;
-    const int q = r % p.Lq;
-    const bool row_valid = x.ok && r < p.cands_per_tile * p.Lq && slot < x.cnt;
+  int unit = blockIdx.x;
+  Unit x = decode(p, load_work(p, unit, n_units));
+  bool rv = x.ok && row_in_tile && slot < x.cnt;
+  int cand = rv ? __ldg(p.perm + x.start + slot) : 0;
+  while (unit < n_units) {
+    const int nunit = unit + static_cast<int>(gridDim.x);
+    const int4 nw = load_work(p, nunit, n_units);
+    Unit nx;
+    bool nrv = false;
+    int ncand = 0;
+    bool prefetched = false;
     __nv_bfloat16* orow = nullptr;
-    if (row_valid) {
-      const int cand = p.perm[x.start + slot];
-      orow = reinterpret_cast<__nv_bfloat16*>(p.O) + ((static_cast<size_t>(cand) * p.H + x.h) * p.Lq + q) * ATT_D;
-    }
-    if (x.ntiles == 0) {  // empty key range: O = 0
-      if (row_valid) {
-        uint4 z = make_uint4(0, 0, 0, 0);
-        for (int c = 0; c < ATT_D / 8; ++c) reinterpret_cast<uint4*>(orow)[c] = z;
-      }
-      continue;
-    }
-    // Q row: landing buffer (128-byte swizzle: 16-byte chunk c of row r sits
-    // at chunk c ^ (r % 8)) -> TMEM columns of Q as bf16 pairs.  Every S of
-    // the previous unit has been read by this thread already, so Q is free.
-    const int qb = static_cast<int>(qc & 1u);
-    if (!mbar_wait(&s.q_full[qb], (qc >> 1) & 1u, s.abort, p.timeout_ns, 1)) return;
-    ++qc;
-    const uint8_t* qrow = s.q + qb * ATT_Q_TILE_BYTES + r * 128;
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      uint32_t w[32];
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const uint4 v = *reinterpret_cast<const uint4*>(qrow + half * HALF_TILE + ((c ^ (r & 7)) << 4));
-        w[4 * c + 0] = v.x;
-        w[4 * c + 1] = v.y;
-        w[4 * c + 2] = v.z;
-        w[4 * c + 3] = v.w;
-      }
-      tmem_st32(Qt + half * 32, w);
-    }
-    tmem_st_wait();
-    tc_fence_before();
-    mbar_arrive(s.qt_ready);
-    mbar_arrive(&s.q_empty[qb]);
-    // the previous unit's O is written out while this unit's first S are computed
-    if (prev.pending) {
-      if (!att_epilogue(p, s, Ot, prev, ou)) return;
-      prev.pending = false;
-    }
+    if (rv) orow = reinterpret_cast<__nv_bfloat16*>(p.O) + ((static_cast<size_t>(cand) * p.H + x.h) * p.Lq + qrow) * ATT_D;
 
-    float m = -INFINITY, l = 0.f;
-    for (int jt = 0; jt < x.ntiles; ++jt, ++g) {
-      const int b = static_cast<int>(g & 1u);
-      const uint32_t S = tmem + lane_base + TM_S + b * 128;
-      if (!mbar_wait(&s.s_full[b], (g >> 1) & 1u, s.abort, p.timeout_ns, 1)) return;
-      tc_fence_after();
-      const int ncols = min(ATT_BN, x.L - jt * ATT_BN);
-      uint32_t v[128];
-      tmem_ld32p(S + 0, v);
-      tmem_ld32p(S + 32, v + 32);
-      tmem_ld32p(S + 64, v + 64);
-      tmem_ld32p(S + 96, v + 96);
-      tmem_ld_wait();
-      reg_fence32(v);
-      reg_fence32(v + 32);
-      reg_fence32(v + 64);
-      reg_fence32(v + 96);
-      tc_fence_before();
-      mbar_arrive(&s.s_free[b]);  // S_b may take S(g + 2) now
-      if (ncols < ATT_BN) {
+    if (x.ntiles == 0) {  // empty key range: O = 0
+      if (rv) {
+        const uint4 z = make_uint4(0, 0, 0, 0);
 #pragma unroll
-        for (int j = 0; j < ATT_BN; ++j)
-          if (j >= ncols) v[j] = __float_as_uint(-INFINITY);
+        for (int c = 0; c < 8; ++c) reinterpret_cast<uint4*>(orow + half * 64)[c] = z;
       }
-      float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+    } else {
+      // this warp's d half of the Q row: landing buffer (128-byte swizzle:
+      // 16-byte chunk c of row r sits at chunk c ^ (r % 8)) -> TMEM.  Every S
+      // of the previous unit has been read by this thread, so Q is free.
+      if (!mbar_wait(s.q_full, qc & 1u, s.abort, p.timeout_ns, 1)) return;
+      ++qc;
+      {
+        const uint8_t* qsrc = s.q + half * HALF_TILE + ln.r * 128;
+        uint32_t w[32];
 #pragma unroll
-      for (int j = 0; j < ATT_BN; j += 4) {
-        mx0 = fmaxf(mx0, __uint_as_float(v[j]));
-        mx1 = fmaxf(mx1, __uint_as_float(v[j + 1]));
-        mx2 = fmaxf(mx2, __uint_as_float(v[j + 2]));
-        mx3 = fmaxf(mx3, __uint_as_float(v[j + 3]));
-      }
-      const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
-      const float m_new = fmaxf(m, mx * sl);
-      // tcgen05.ld/st are warp-collective: the rescale decision must be
-      // uniform across the warp, so any row that needs it moves all 32
-      const bool rescale = __any_sync(0xffffffffu, m_new > m + RESCALE_THRESHOLD);
-      float alpha = 1.f;
-      if (rescale) {
-        alpha = ex2(m - m_new);  // 0 on the first tile, 1 for rows whose max did not move
-        l *= alpha;
-        m = m_new;
-      }
-      // p = 2^(s*sl - m) (masked columns give 2^-inf = 0) as bf16 pairs
-      float l0 = 0.f, l1 = 0.f;
-      uint32_t pk[64];
-#pragma unroll
-      for (int j = 0; j < 64; ++j) {
-        const float p0 = ex2(fmaf(__uint_as_float(v[2 * j]), sl, -m));
-        const float p1 = ex2(fmaf(__uint_as_float(v[2 * j + 1]), sl, -m));
-        l0 += p0;
-        l1 += p1;
-        pk[j] = pack_bf16x2(p0, p1);
-      }
-      l += l0 + l1;
-      // P and O are free once the previous P.V has completed
-      if (g > 0 && !mbar_wait(s.pv_done, (g - 1) & 1u, s.abort, p.timeout_ns, 1)) return;
-      tc_fence_after();
-      if (rescale && jt > 0) {
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t o[32];
-          tmem_ld32(Ot + c * 32, o);
-          tmem_ld_wait(o);
-#pragma unroll
-          for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
-          tmem_st32(Ot + c * 32, o);
+        for (int c = 0; c < 8; ++c) {
+          const uint4 v = *reinterpret_cast<const uint4*>(qsrc + ((c ^ (ln.r & 7)) << 4));
+          w[4 * c + 0] = v.x;
+          w[4 * c + 1] = v.y;
+          w[4 * c + 2] = v.z;
+          w[4 * c + 3] = v.w;
         }
+        tmem_st32(Qt, w);
       }
-      tmem_st32p(Pt, pk);
-      tmem_st32p(Pt + 32, pk + 32);
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(s.p_full);
+      mbar_arrive(s.qt_ready);
+      mbar_arrive(s.q_empty);
+      // the previous unit's O is written out while this unit's first S are computed
+      if (prev.pending) {
+        if (!att_epilogue(p, s, Ot, prev, ln, ou)) return;
+        prev.pending = false;
+      }
+
+      float m = -INFINITY, l = 0.f;
+      for (int jt = 0; jt < x.ntiles; ++jt, ++g) {
+        const int b = static_cast<int>(g & 1u);
+        if (!mbar_wait(&s.s_full[b], (g >> 1) & 1u, s.abort, p.timeout_ns, 1)) return;
+        tc_fence_after();
+        const int ncols = min(ATT_BN, x.L - jt * ATT_BN) - half * 64;  // valid columns of this half
+        uint32_t v[64];
+        tmem_ld32p(St + b * 128, v);
+        tmem_ld32p(St + b * 128 + 32, v + 32);
+        tmem_ld_wait();
+        reg_fence32(v);
+        reg_fence32(v + 32);
+        tc_fence_before();
+        mbar_arrive(&s.s_free[b]);  // S_b may take S(g + 2) now
+        if (ncols < 64) {
+#pragma unroll
+          for (int j = 0; j < 64; ++j)
+            if (j >= ncols) v[j] = __float_as_uint(-INFINITY);
+        }
+        float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < 64; j += 4) {
+          mx0 = fmaxf(mx0, __uint_as_float(v[j]));
+          mx1 = fmaxf(mx1, __uint_as_float(v[j + 1]));
+          mx2 = fmaxf(mx2, __uint_as_float(v[j + 2]));
+          mx3 = fmaxf(mx3, __uint_as_float(v[j + 3]));
+        }
+        float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
+        float mp;
+        if (!pair_exchange(p, s, ln, mx, mp)) return;
+        mx = fmaxf(mx, mp);
+        const float m_new = fmaxf(m, mx * sl);
+        // tcgen05.ld/st are warp-collective: the rescale decision must be
+        // uniform across the warp, so any row that needs it moves all 32.
+        // Both warps of the quarter see the same maxima, so they agree.
+        const bool rescale = __any_sync(0xffffffffu, m_new > m + RESCALE_THRESHOLD);
+        float alpha = 1.f;
+        if (rescale) {
+          alpha = ex2(m - m_new);  // 0 on the first tile, 1 for rows whose max did not move
+          l *= alpha;
+          m = m_new;
+        }
+        // p = 2^(s*sl - m) (masked columns give 2^-inf = 0) as bf16 pairs
+        float l0 = 0.f, l1 = 0.f;
+        uint32_t pk[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const float p0 = ex2(fmaf(__uint_as_float(v[2 * j]), sl, -m));
+          const float p1 = ex2(fmaf(__uint_as_float(v[2 * j + 1]), sl, -m));
+          l0 += p0;
+          l1 += p1;
+          pk[j] = pack_bf16x2(p0, p1);
+        }
+        l += l0 + l1;
+        // P and O are free once the previous P.V has completed
+        if (g > 0 && !mbar_wait(s.pv_done, (g - 1) & 1u, s.abort, p.timeout_ns, 1)) return;
+        tc_fence_after();
+        if (rescale && jt > 0) {
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            uint32_t o[32];
+            tmem_ld32(Ot + c * 32, o);
+            tmem_ld_wait(o);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
+            tmem_st32(Ot + c * 32, o);
+          }
+        }
+        tmem_st32p(Pt, pk);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(s.p_full);
+        if (!prefetched) {  // the next unit's entry and this row's candidate in it
+          prefetched = true;
+          nx = decode(p, nw);
+          nrv = nx.ok && row_in_tile && slot < nx.cnt;
+          ncand = nrv ? __ldg(p.perm + nx.start + slot) : 0;
+        }
+      }
+      prev.pending = true;
+      prev.valid = rv;
+      prev.row = orow;
+      prev.l = l;
     }
-    prev.pending = true;
-    prev.valid = row_valid;
-    prev.row = orow;
-    prev.l = l;
+    if (!prefetched) {
+      nx = decode(p, nw);
+      nrv = nx.ok && row_in_tile && slot < nx.cnt;
+      ncand = nrv ? __ldg(p.perm + nx.start + slot) : 0;
+    }
+    x = nx;
+    rv = nrv;
+    cand = ncand;
+    unit = nunit;
   }
-  if (prev.pending) att_epilogue(p, s, Ot, prev, ou);
+  if (prev.pending) att_epilogue(p, s, Ot, prev, ln, ou);
 }
 
 __global__ void __launch_bounds__(ATT_THREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const AttSmem s = carve(base);
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t pad = ((raw + 1023u) & ~1023u) - raw;
+  if (pad + SMEM_USED > SMEM_ALLOC) {  // uniform across the CTA, before any barrier exists
+    if (threadIdx.x == 0) atomicOr(p.status, DEV_ERR_SMEM_LAYOUT);
+    return;
+  }
+  const AttSmem s = carve(smem_raw + pad);
   const int warp = threadIdx.x >> 5;
   const int n_units = *p.n_units;
 
   if (threadIdx.x == 0) {
+    mbar_init(s.q_full, 1);
+    mbar_init(s.q_empty, 1 + SOFTMAX_THREADS);
+    mbar_init(s.qt_ready, SOFTMAX_THREADS);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&s.q_full[i], 1);
-      mbar_init(&s.q_empty[i], 128);
       mbar_init(&s.s_full[i], 1);
-      mbar_init(&s.s_free[i], 128);
+      mbar_init(&s.s_free[i], SOFTMAX_THREADS);
     }
-    mbar_init(s.qt_ready, 128);
-    mbar_init(s.p_full, 128);
+    mbar_init(s.p_full, SOFTMAX_THREADS);
     mbar_init(s.pv_done, 1);
     mbar_init(s.o_full, 1);
-    mbar_init(s.o_empty, 128);
+    mbar_init(s.o_empty, SOFTMAX_THREADS);
     for (int i = 0; i < ATT_STAGES; ++i) {
       mbar_init(&s.kv_full[i], 1);
       mbar_init(&s.kv_empty[i], 1);
     }
+    for (int i = 0; i < 8; ++i) mbar_init(&s.xbar[i], 64);
     *s.abort = 0;
     fence_barrier_init();
     fence_proxy_async_smem();
@@ -525,9 +669,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
 
 }  // namespace
 
-size_t attn_smem_bytes() {
-  return 1024 + ATT_Q_BUFS * ATT_Q_TILE_BYTES + ATT_STAGES * ATT_KV_STAGE_BYTES + 512;
-}
+size_t attn_smem_bytes() { return SMEM_ALLOC; }
 
 cudaError_t launch_attn(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV, const AttnParams& p,
                         int grid, cudaStream_t s) {

@@ -16,6 +16,7 @@ enum : uint32_t {
   DEV_ERR_FLAG_TIMEOUT = 1u << 1,  // an LCE user partial never became ready
   DEV_ERR_PIPE_TIMEOUT = 1u << 2,  // an mbarrier wait inside a kernel ran out
   DEV_ERR_BAD_WORK = 1u << 3,      // inconsistent attention work unit
+  DEV_ERR_SMEM_LAYOUT = 1u << 4,   // dynamic shared memory too misaligned for the tile layout
 };
 
 // Debug switches (ikbo_plan_set_debug).
@@ -87,11 +88,11 @@ constexpr int ATT_BM = 128;        // query rows per tile (TMEM lanes)
 constexpr int ATT_BN = 128;        // keys per K/V tile
 constexpr int ATT_D = 128;         // head dim (the only one supported)
 constexpr int ATT_TILES = 1;       // query tiles per work unit
-constexpr int ATT_THREADS = 256;   // warp 0 TMA, 1 S issuer, 2 P.V issuer, 3 idle, 4-7 softmax
+constexpr int ATT_THREADS = 384;   // warp 0 TMA, 1 S issuer, 2 P.V issuer, 3 idle, 4-11 softmax
 constexpr int ATT_KV_STAGE_BYTES = ATT_BN * ATT_D * 2;   // 32 KB
 constexpr int ATT_Q_TILE_BYTES = ATT_BM * ATT_D * 2;     // 32 KB
-constexpr int ATT_Q_BUFS = 2;      // Q landing buffers (the next unit's Q loads early)
-constexpr int ATT_STAGES = 5;      // K/V ring: 2 x 32 KB Q + 5 x 32 KB = 224 KB of 227
+constexpr int ATT_Q_BUFS = 1;      // Q landing buffer
+constexpr int ATT_STAGES = 6;      // K/V ring: 32 KB Q + 6 x 32 KB = 224 KB of 227
 
 struct AttnParams {
   const int32_t* perm;
