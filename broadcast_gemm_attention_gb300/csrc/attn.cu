@@ -15,12 +15,14 @@
 // through L2.
 //
 // Per CTA (persistent, one per SM, 12 warps):
-//   warp 0      TMA producer: the unit's Q tile (one box per candidate and
-//               d-half, gathered through perm) into the Q landing buffer;
-//               K and V tiles of 128 keys through a 6-stage ring
+//   warp 0      TMA producer for Q and K: the unit's Q tile (one box per
+//               candidate and d-half, gathered through perm) into the Q
+//               landing buffer; K tiles of 128 keys through a 3-stage ring
 //   warp 1      S issuer and TMEM owner: S = Q K^T into S0 / S1 alternately
 //   warp 2      P.V issuer: O += P V
-//   warp 3      idle
+//   warp 3      TMA producer for V (3-stage ring).  K and V have rings and
+//               producers of their own so that a K load never queues
+//               behind a V load that waits for a P.V several tiles back.
 //   warps 4-11  softmax + epilogue.  Warps w and w+4 share the 32 TMEM lanes
 //               (query rows) of quarter w % 4 and split the 128 key columns
 //               of a tile (and the 128 d columns of O) into halves; they
@@ -62,8 +64,9 @@ constexpr uint32_t TM_O = 384;
 
 // dynamic shared memory: [Q landing][K/V ring] (1024-aligned for the
 // 128-byte swizzle), then the barriers, two words, and the row exchange
-constexpr uint32_t TILE_REGION = ATT_Q_BUFS * ATT_Q_TILE_BYTES + ATT_STAGES * ATT_KV_STAGE_BYTES;
-constexpr int NUM_BARS = 11 + 2 * ATT_STAGES + 8;
+constexpr uint32_t TILE_REGION =
+    ATT_Q_BUFS * ATT_Q_TILE_BYTES + (ATT_K_STAGES + ATT_V_STAGES) * ATT_KV_STAGE_BYTES;
+constexpr int NUM_BARS = 11 + 2 * (ATT_K_STAGES + ATT_V_STAGES) + 8;
 constexpr uint32_t XVAL_OFFSET = NUM_BARS * 8 + 8;
 constexpr uint32_t AUX_BYTES = XVAL_OFFSET + 2 * 2 * ATT_BM * 4;
 constexpr uint32_t SMEM_USED = TILE_REGION + AUX_BYTES;
@@ -72,7 +75,8 @@ static_assert(SMEM_USED <= SMEM_ALLOC, "attention tiles do not fit in shared mem
 
 struct AttSmem {
   uint8_t* q;          // Q landing buffer, 32 KB
-  uint8_t* kv;         // ATT_STAGES x 32 KB
+  uint8_t* k;          // ATT_K_STAGES x 32 KB
+  uint8_t* v;          // ATT_V_STAGES x 32 KB
   uint64_t* q_full;    // Q landed
   uint64_t* q_empty;   // Q copied into TMEM and read by the first S products
   uint64_t* qt_ready;  // Q of the unit is in TMEM
@@ -82,8 +86,10 @@ struct AttSmem {
   uint64_t* pv_done;   // a P.V completed (P is free again, O is up to date)
   uint64_t* o_full;    // the unit's last P.V completed
   uint64_t* o_empty;   // the unit's epilogue has read O
-  uint64_t* kv_full;
-  uint64_t* kv_empty;
+  uint64_t* k_full;
+  uint64_t* k_empty;
+  uint64_t* v_full;
+  uint64_t* v_empty;
   uint64_t* xbar;      // [4 quarters][2] row exchange between the two warps of a quarter
   uint32_t* tmem_slot;
   uint32_t* abort;
@@ -93,7 +99,8 @@ struct AttSmem {
 __device__ __forceinline__ AttSmem carve(uint8_t* base) {
   AttSmem s;
   s.q = base;
-  s.kv = base + ATT_Q_BUFS * ATT_Q_TILE_BYTES;
+  s.k = base + ATT_Q_BUFS * ATT_Q_TILE_BYTES;
+  s.v = s.k + ATT_K_STAGES * ATT_KV_STAGE_BYTES;
   uint64_t* b = reinterpret_cast<uint64_t*>(base + TILE_REGION);
   s.q_full = b;
   s.q_empty = b + 1;
@@ -104,9 +111,11 @@ __device__ __forceinline__ AttSmem carve(uint8_t* base) {
   s.pv_done = b + 8;
   s.o_full = b + 9;
   s.o_empty = b + 10;
-  s.kv_full = b + 11;
-  s.kv_empty = s.kv_full + ATT_STAGES;
-  s.xbar = s.kv_empty + ATT_STAGES;
+  s.k_full = b + 11;
+  s.k_empty = s.k_full + ATT_K_STAGES;
+  s.v_full = s.k_empty + ATT_K_STAGES;
+  s.v_empty = s.v_full + ATT_V_STAGES;
+  s.xbar = s.v_empty + ATT_V_STAGES;
   s.tmem_slot = reinterpret_cast<uint32_t*>(base + TILE_REGION + NUM_BARS * 8);
   s.abort = s.tmem_slot + 1;
   s.xval = reinterpret_cast<float*>(base + TILE_REGION + XVAL_OFFSET);
@@ -154,9 +163,11 @@ __device__ __forceinline__ Unit decode(const AttnParams& p, int4 w) {
   return x;
 }
 
-// position of K/V load c (K of global tile g is load 2g, its V load 2g+1) in the ring
-__device__ __forceinline__ int ring_stage(uint32_t c) { return static_cast<int>(c % ATT_STAGES); }
-__device__ __forceinline__ uint32_t ring_phase(uint32_t c) { return (c / ATT_STAGES) & 1u; }
+// stage and phase of the tile with global index g (tiles this CTA has run) in a ring
+template <int kStages>
+__device__ __forceinline__ int ring_stage(uint32_t g) { return static_cast<int>(g % kStages); }
+template <int kStages>
+__device__ __forceinline__ uint32_t ring_phase(uint32_t g) { return (g / kStages) & 1u; }
 
 // Keeps the compiler from moving uses of r above a preceding tcgen05.wait.
 __device__ __forceinline__ void reg_fence32(uint32_t* r) {
@@ -204,9 +215,21 @@ __device__ __forceinline__ void load_slots(const AttnParams& p, const Unit& x, Q
   for (int j = 0; j < 16; ++j) q.cand[j] = (x.ok && j < x.cnt) ? __ldg(p.perm + x.start + j) : p.n_cand;
 }
 
-__device__ void att_producer(const AttnParams& p, const AttSmem& s, const CUtensorMap* tmQ, const CUtensorMap* tmK,
-                             const CUtensorMap* tmV, int n_units) {
-  uint32_t c = 0;   // K/V loads issued
+// K or V tile jt of unit x into a ring stage
+__device__ __forceinline__ void load_kv_tile(const AttnParams& p, const CUtensorMap* tm, uint8_t* dst, uint64_t* bar,
+                                             const Unit& x, int jt) {
+  if (p.kv_offsets) {
+    tma_load_3d(dst, tm, bar, 0, x.h, x.kv0 + jt * ATT_BN);
+    tma_load_3d(dst + HALF_TILE, tm, bar, 64, x.h, x.kv0 + jt * ATT_BN);
+  } else {
+    tma_load_4d(dst, tm, bar, 0, jt * ATT_BN, x.h, x.u);
+    tma_load_4d(dst + HALF_TILE, tm, bar, 64, jt * ATT_BN, x.h, x.u);
+  }
+}
+
+__device__ void att_producer_qk(const AttnParams& p, const AttSmem& s, const CUtensorMap* tmQ,
+                                const CUtensorMap* tmK, int n_units) {
+  uint32_t g = 0;   // K tiles loaded
   uint32_t qc = 0;  // Q tiles loaded
   const int cpt = p.cands_per_tile;
   int unit = blockIdx.x;
@@ -232,25 +255,15 @@ __device__ void att_producer(const AttnParams& p, const AttSmem& s, const CUtens
           tma_load_4d(dst + HALF_TILE, tmQ, s.q_full, 64, 0, x.h, qs.cand[j]);
         }
       }
-      for (int jt = 0; jt < x.ntiles; ++jt) {
-        for (int kv = 0; kv < 2; ++kv, ++c) {
-          const int st = ring_stage(c);
-          if (!mbar_wait(&s.kv_empty[st], ring_phase(c) ^ 1u, s.abort, p.timeout_ns, 1)) return;
-          mbar_arrive_expect_tx(&s.kv_full[st], ATT_KV_STAGE_BYTES);
-          uint8_t* dst = s.kv + st * ATT_KV_STAGE_BYTES;
-          const CUtensorMap* tm = kv == 0 ? tmK : tmV;
-          if (p.kv_offsets) {
-            tma_load_3d(dst, tm, &s.kv_full[st], 0, x.h, x.kv0 + jt * ATT_BN);
-            tma_load_3d(dst + HALF_TILE, tm, &s.kv_full[st], 64, x.h, x.kv0 + jt * ATT_BN);
-          } else {
-            tma_load_4d(dst, tm, &s.kv_full[st], 0, jt * ATT_BN, x.h, x.u);
-            tma_load_4d(dst + HALF_TILE, tm, &s.kv_full[st], 64, jt * ATT_BN, x.h, x.u);
-          }
-          if (!prefetched) {  // the next unit's entry has arrived by now
-            prefetched = true;
-            nx = decode(p, nw);
-            load_slots(p, nx, nqs);
-          }
+      for (int jt = 0; jt < x.ntiles; ++jt, ++g) {
+        const int st = ring_stage<ATT_K_STAGES>(g);
+        if (!mbar_wait(&s.k_empty[st], ring_phase<ATT_K_STAGES>(g) ^ 1u, s.abort, p.timeout_ns, 1)) return;
+        mbar_arrive_expect_tx(&s.k_full[st], ATT_KV_STAGE_BYTES);
+        load_kv_tile(p, tmK, s.k + st * ATT_KV_STAGE_BYTES, &s.k_full[st], x, jt);
+        if (!prefetched) {  // the next unit's entry has arrived by now
+          prefetched = true;
+          nx = decode(p, nw);
+          load_slots(p, nx, nqs);
         }
       }
     }
@@ -260,6 +273,25 @@ __device__ void att_producer(const AttnParams& p, const AttSmem& s, const CUtens
     }
     x = nx;
     qs = nqs;
+    unit = nunit;
+  }
+}
+
+__device__ void att_producer_v(const AttnParams& p, const AttSmem& s, const CUtensorMap* tmV, int n_units) {
+  uint32_t g = 0;  // V tiles loaded
+  int unit = blockIdx.x;
+  int4 w = load_work(p, unit, n_units);
+  while (unit < n_units) {
+    const int nunit = unit + static_cast<int>(gridDim.x);
+    const int4 nw = load_work(p, nunit, n_units);
+    const Unit x = decode(p, w);
+    for (int jt = 0; jt < x.ntiles; ++jt, ++g) {
+      const int st = ring_stage<ATT_V_STAGES>(g);
+      if (!mbar_wait(&s.v_empty[st], ring_phase<ATT_V_STAGES>(g) ^ 1u, s.abort, p.timeout_ns, 1)) return;
+      mbar_arrive_expect_tx(&s.v_full[st], ATT_KV_STAGE_BYTES);
+      load_kv_tile(p, tmV, s.v + st * ATT_KV_STAGE_BYTES, &s.v_full[st], x, jt);
+    }
+    w = nw;
     unit = nunit;
   }
 }
@@ -306,7 +338,15 @@ __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint3
   }
 }
 
-// S issuer: tile g goes to S_(g&1) once the softmax has read S(g-2) out of it.
+// A wait taken by a whole warp: every lane polls, and the lanes agree on the
+// outcome so that a timeout never splits the warp.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const AttSmem& s, const AttnParams& p) {
+  const bool ok = mbar_wait(bar, parity, s.abort, p.timeout_ns, 1);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// S issuer (whole warp; one elected lane issues): tile g goes to S_(g&1)
+// once the softmax has read S(g-2) out of it.
 __device__ void att_s_issuer(const AttnParams& p, const AttSmem& s, uint32_t tmem, int n_units) {
   uint32_t g = 0, qu = 0;
   int unit = blockIdx.x;
@@ -320,24 +360,29 @@ __device__ void att_s_issuer(const AttnParams& p, const AttSmem& s, uint32_t tme
       for (int jt = 0; jt < x.ntiles; ++jt, ++g) {
         const int b = static_cast<int>(g & 1u);
         const uint32_t n = g >> 1;
-        const uint32_t kc = 2 * g;
-        if (!mbar_wait(&s.kv_full[ring_stage(kc)], ring_phase(kc), s.abort, p.timeout_ns, 1)) return;
-        if (n > 0 && !mbar_wait(&s.s_free[b], (n - 1) & 1u, s.abort, p.timeout_ns, 1)) return;
-        const uint32_t k_base = smem_u32(s.kv + ring_stage(kc) * ATT_KV_STAGE_BYTES);
-        if (jt <= last_ss) {
-          if (jt == 0 && !mbar_wait(s.q_full, qu & 1u, s.abort, p.timeout_ns, 1)) return;
-          tc_fence_after();
-          issue_qk_ss(tmem + TM_S + b * 128, smem_u32(s.q), k_base);
+        const int kst = ring_stage<ATT_K_STAGES>(g);
+        if (!warp_wait(&s.k_full[kst], ring_phase<ATT_K_STAGES>(g), s, p)) return;
+        if (n > 0 && !warp_wait(&s.s_free[b], (n - 1) & 1u, s, p)) return;
+        const uint32_t k_base = smem_u32(s.k + kst * ATT_KV_STAGE_BYTES);
+        const bool ss = jt <= last_ss;
+        if (ss) {
+          if (jt == 0 && !warp_wait(s.q_full, qu & 1u, s, p)) return;
         } else {
           // skipped for units of at most two tiles: the softmax's next arrival
           // needs this unit's S, so the barrier never runs two phases ahead
-          if (jt == last_ss + 1 && !mbar_wait(s.qt_ready, qu & 1u, s.abort, p.timeout_ns, 1)) return;
-          tc_fence_after();
-          issue_qk(tmem + TM_S + b * 128, tmem + TM_Q, k_base);
+          if (jt == last_ss + 1 && !warp_wait(s.qt_ready, qu & 1u, s, p)) return;
         }
-        mma_commit(&s.s_full[b]);
-        mma_commit(&s.kv_empty[ring_stage(kc)]);
-        if (jt == last_ss) mma_commit(s.q_empty);  // the landing buffer's last reader
+        tc_fence_after();
+        if (elect_one()) {
+          if (ss)
+            issue_qk_ss(tmem + TM_S + b * 128, smem_u32(s.q), k_base);
+          else
+            issue_qk(tmem + TM_S + b * 128, tmem + TM_Q, k_base);
+          mma_commit(&s.s_full[b]);
+          mma_commit(&s.k_empty[kst]);
+          if (jt == last_ss) mma_commit(s.q_empty);  // the landing buffer's last reader
+        }
+        __syncwarp();
       }
       ++qu;
     }
@@ -346,8 +391,9 @@ __device__ void att_s_issuer(const AttnParams& p, const AttSmem& s, uint32_t tme
   }
 }
 
-// P.V issuer: tile g once its P is written; the unit's first one also waits
-// for the previous unit's epilogue to have read O.
+// P.V issuer (whole warp; one elected lane issues): tile g once its P is
+// written; the unit's first one also waits for the previous unit's epilogue
+// to have read O.
 __device__ void att_pv_issuer(const AttnParams& p, const AttSmem& s, uint32_t tmem, int n_units) {
   uint32_t g = 0, ou = 0;
   int unit = blockIdx.x;
@@ -357,18 +403,19 @@ __device__ void att_pv_issuer(const AttnParams& p, const AttSmem& s, uint32_t tm
     const int4 nw = load_work(p, nunit, n_units);
     const Unit x = decode(p, w);
     for (int jt = 0; jt < x.ntiles; ++jt, ++g) {
-      const uint32_t vc = 2 * g + 1;
-      if (!mbar_wait(s.p_full, g & 1u, s.abort, p.timeout_ns, 1)) return;
-      if (!mbar_wait(&s.kv_full[ring_stage(vc)], ring_phase(vc), s.abort, p.timeout_ns, 1)) return;
-      if (jt == 0 && !mbar_wait(s.o_empty, (ou & 1u) ^ 1u, s.abort, p.timeout_ns, 1)) return;
+      const int vst = ring_stage<ATT_V_STAGES>(g);
+      if (!warp_wait(s.p_full, g & 1u, s, p)) return;
+      if (!warp_wait(&s.v_full[vst], ring_phase<ATT_V_STAGES>(g), s, p)) return;
+      if (jt == 0 && !warp_wait(s.o_empty, (ou & 1u) ^ 1u, s, p)) return;
       tc_fence_after();
-      issue_pv(tmem + TM_O, tmem + TM_P, smem_u32(s.kv + ring_stage(vc) * ATT_KV_STAGE_BYTES), jt > 0);
-      mma_commit(s.pv_done);
-      mma_commit(&s.kv_empty[ring_stage(vc)]);
-      if (jt + 1 == x.ntiles) {
-        mma_commit(s.o_full);
-        ++ou;
+      if (elect_one()) {
+        issue_pv(tmem + TM_O, tmem + TM_P, smem_u32(s.v + vst * ATT_KV_STAGE_BYTES), jt > 0);
+        mma_commit(s.pv_done);
+        mma_commit(&s.v_empty[vst]);
+        if (jt + 1 == x.ntiles) mma_commit(s.o_full);
       }
+      __syncwarp();
+      if (jt + 1 == x.ntiles) ++ou;
     }
     w = nw;
     unit = nunit;
@@ -625,9 +672,13 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
     mbar_init(s.pv_done, 1);
     mbar_init(s.o_full, 1);
     mbar_init(s.o_empty, SOFTMAX_THREADS);
-    for (int i = 0; i < ATT_STAGES; ++i) {
-      mbar_init(&s.kv_full[i], 1);
-      mbar_init(&s.kv_empty[i], 1);
+    for (int i = 0; i < ATT_K_STAGES; ++i) {
+      mbar_init(&s.k_full[i], 1);
+      mbar_init(&s.k_empty[i], 1);
+    }
+    for (int i = 0; i < ATT_V_STAGES; ++i) {
+      mbar_init(&s.v_full[i], 1);
+      mbar_init(&s.v_empty[i], 1);
     }
     for (int i = 0; i < 8; ++i) mbar_init(&s.xbar[i], 64);
     *s.abort = 0;
@@ -649,11 +700,13 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
   const uint32_t tmem = *s.tmem_slot;
 
   if (warp == 0) {
-    if (lane_id() == 0) att_producer(p, s, &tmQ, &tmK, &tmV, n_units);
+    if (lane_id() == 0) att_producer_qk(p, s, &tmQ, &tmK, n_units);
+  } else if (warp == 3) {
+    if (lane_id() == 0) att_producer_v(p, s, &tmV, n_units);
   } else if (warp == 1) {
-    if (lane_id() == 0) att_s_issuer(p, s, tmem, n_units);
+    att_s_issuer(p, s, tmem, n_units);
   } else if (warp == 2) {
-    if (lane_id() == 0) att_pv_issuer(p, s, tmem, n_units);
+    att_pv_issuer(p, s, tmem, n_units);
   } else if (warp >= SOFTMAX_WARP0) {
     att_softmax(p, s, tmem, n_units);
   }

@@ -88,11 +88,12 @@ constexpr int ATT_BM = 128;        // query rows per tile (TMEM lanes)
 constexpr int ATT_BN = 128;        // keys per K/V tile
 constexpr int ATT_D = 128;         // head dim (the only one supported)
 constexpr int ATT_TILES = 1;       // query tiles per work unit
-constexpr int ATT_THREADS = 384;   // warp 0 TMA, 1 S issuer, 2 P.V issuer, 3 idle, 4-11 softmax
+constexpr int ATT_THREADS = 384;   // warp 0 TMA Q+K, 1 S issuer, 2 P.V issuer, 3 TMA V, 4-11 softmax
 constexpr int ATT_KV_STAGE_BYTES = ATT_BN * ATT_D * 2;   // 32 KB
 constexpr int ATT_Q_TILE_BYTES = ATT_BM * ATT_D * 2;     // 32 KB
 constexpr int ATT_Q_BUFS = 1;      // Q landing buffer
-constexpr int ATT_STAGES = 6;      // K/V ring: 32 KB Q + 6 x 32 KB = 224 KB of 227
+constexpr int ATT_K_STAGES = 3;    // K ring
+constexpr int ATT_V_STAGES = 3;    // V ring: 32 KB Q + 6 x 32 KB = 224 KB of 227
 
 struct AttnParams {
   const int32_t* perm;
