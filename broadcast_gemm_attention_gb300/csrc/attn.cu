@@ -20,7 +20,7 @@
 //               landing buffer; K tiles of 128 keys through a 3-stage ring
 //   warp 1      S issuer and TMEM owner: S = Q K^T into S0 / S1 alternately
 //   warp 2      P.V issuer: O += P V
-//   warp 3      TMA producer for V (3-stage ring).  K and V have rings and
+//   warp 3      TMA producer for V (2-stage ring).  K and V have rings and
 //               producers of their own so that a K load never queues
 //               behind a V load that waits for a P.V several tiles back.
 //   warps 4-11  softmax + epilogue.  Warps w and w+4 share the 32 TMEM lanes
@@ -30,7 +30,11 @@
 //               per scheduler hide the exp2 / convert latency that one warp
 //               alone cannot.
 // TMEM (512 columns): S0 S1 (128 each, fp32), P (64, bf16 pairs), Q (64,
-// bf16 pairs), O (128, fp32).
+// bf16 pairs), O (128, fp32).  A unit's O leaves through shared memory: a
+// thread owns a query row, so its direct stores would scatter 32 rows per
+// warp instruction; each warp writes its 32 rows x 64 d into its own 4 KB of
+// a staging tile and reads them back 4 rows per instruction, 8 lanes per
+// contiguous 128-byte half row.
 //
 // Why two issuers and a separate P: one thread issues a tcgen05.mma only
 // every ~80-130 cycles, while an M=128, N=128, K=16 product needs 64 cycles
@@ -64,8 +68,8 @@ constexpr uint32_t TM_O = 384;
 
 // dynamic shared memory: [Q landing][K/V ring] (1024-aligned for the
 // 128-byte swizzle), then the barriers, two words, and the row exchange
-constexpr uint32_t TILE_REGION =
-    ATT_Q_BUFS * ATT_Q_TILE_BYTES + (ATT_K_STAGES + ATT_V_STAGES) * ATT_KV_STAGE_BYTES;
+constexpr uint32_t TILE_REGION = ATT_Q_BUFS * ATT_Q_TILE_BYTES +
+                                 (ATT_K_STAGES + ATT_V_STAGES) * ATT_KV_STAGE_BYTES + ATT_O_TILE_BYTES;
 constexpr int NUM_BARS = 11 + 2 * (ATT_K_STAGES + ATT_V_STAGES) + 8;
 constexpr uint32_t XVAL_OFFSET = NUM_BARS * 8 + 8;
 constexpr uint32_t AUX_BYTES = XVAL_OFFSET + 2 * 2 * ATT_BM * 4;
@@ -77,6 +81,7 @@ struct AttSmem {
   uint8_t* q;          // Q landing buffer, 32 KB
   uint8_t* k;          // ATT_K_STAGES x 32 KB
   uint8_t* v;          // ATT_V_STAGES x 32 KB
+  uint8_t* o;          // O staging, 4 KB per softmax warp
   uint64_t* q_full;    // Q landed
   uint64_t* q_empty;   // Q copied into TMEM and read by the first S products
   uint64_t* qt_ready;  // Q of the unit is in TMEM
@@ -101,6 +106,7 @@ __device__ __forceinline__ AttSmem carve(uint8_t* base) {
   s.q = base;
   s.k = base + ATT_Q_BUFS * ATT_Q_TILE_BYTES;
   s.v = s.k + ATT_K_STAGES * ATT_KV_STAGE_BYTES;
+  s.o = s.v + ATT_V_STAGES * ATT_KV_STAGE_BYTES;
   uint64_t* b = reinterpret_cast<uint64_t*>(base + TILE_REGION);
   s.q_full = b;
   s.q_empty = b + 1;
@@ -450,7 +456,9 @@ struct RowOut {
   float l;       // this warp's half of the row sum
 };
 
-// O / l -> bf16 -> this warp's half of the row of O; then O may be overwritten.
+// O / l -> bf16 -> this warp's d half of its 32 rows, through its 4 KB of
+// staging (128-byte rows, 16-byte chunk c of row r at chunk c ^ (r % 8)) to
+// global memory 4 rows per store instruction; then O may be overwritten.
 __device__ __forceinline__ bool att_epilogue(const AttnParams& p, const AttSmem& s, uint32_t Ot, const RowOut& ro,
                                              Lane& ln, uint32_t& ou) {
   float lp;
@@ -460,23 +468,38 @@ __device__ __forceinline__ bool att_epilogue(const AttnParams& p, const AttSmem&
   ++ou;
   tc_fence_after();
   const float inv = l > 0.f ? 1.0f / l : 0.f;
+  const int lane = static_cast<int>(lane_id());
+  uint8_t* stage = s.o + ((ln.quarter * 2 + ln.half) << 12);
 #pragma unroll
   for (int c = 0; c < 2; ++c) {
     uint32_t o[32];
     tmem_ld32(Ot + c * 32, o);
     tmem_ld_wait(o);
-    if (ro.valid) {
-      uint32_t pk[16];
 #pragma unroll
-      for (int j = 0; j < 16; ++j)
-        pk[j] = pack_bf16x2(__uint_as_float(o[2 * j]) * inv, __uint_as_float(o[2 * j + 1]) * inv);
-      uint4* dst = reinterpret_cast<uint4*>(ro.row + ln.half * 64 + c * 32);
-#pragma unroll
-      for (int k = 0; k < 4; ++k) dst[k] = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+    for (int k = 0; k < 4; ++k) {
+      uint4 w;
+      w.x = pack_bf16x2(__uint_as_float(o[8 * k + 0]) * inv, __uint_as_float(o[8 * k + 1]) * inv);
+      w.y = pack_bf16x2(__uint_as_float(o[8 * k + 2]) * inv, __uint_as_float(o[8 * k + 3]) * inv);
+      w.z = pack_bf16x2(__uint_as_float(o[8 * k + 4]) * inv, __uint_as_float(o[8 * k + 5]) * inv);
+      w.w = pack_bf16x2(__uint_as_float(o[8 * k + 6]) * inv, __uint_as_float(o[8 * k + 7]) * inv);
+      *reinterpret_cast<uint4*>(stage + lane * 128 + (((4 * c + k) ^ (lane & 7)) << 4)) = w;
     }
   }
   tc_fence_before();
   mbar_arrive(s.o_empty);
+  __syncwarp();
+  // read back: instruction i covers rows 4i .. 4i+3 of the warp, lane = 8 * (row - 4i) + chunk
+  const int chunk = lane & 7;
+  const uint64_t my_row = reinterpret_cast<uint64_t>(ro.row);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int r = 4 * i + (lane >> 3);
+    const uint64_t dst_row = __shfl_sync(0xffffffffu, my_row, r);
+    const bool valid = __shfl_sync(0xffffffffu, ro.valid, r);
+    const uint4 w = *reinterpret_cast<const uint4*>(stage + r * 128 + ((chunk ^ (r & 7)) << 4));
+    if (valid) reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(dst_row) + ln.half * 64)[chunk] = w;
+  }
+  __syncwarp();  // the staging rows are read before this warp's next epilogue writes them
   return true;
 }
 

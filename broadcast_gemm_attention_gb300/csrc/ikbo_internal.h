@@ -93,7 +93,9 @@ constexpr int ATT_KV_STAGE_BYTES = ATT_BN * ATT_D * 2;   // 32 KB
 constexpr int ATT_Q_TILE_BYTES = ATT_BM * ATT_D * 2;     // 32 KB
 constexpr int ATT_Q_BUFS = 1;      // Q landing buffer
 constexpr int ATT_K_STAGES = 3;    // K ring
-constexpr int ATT_V_STAGES = 3;    // V ring: 32 KB Q + 6 x 32 KB = 224 KB of 227
+constexpr int ATT_V_STAGES = 2;    // V ring
+constexpr int ATT_O_TILE_BYTES = ATT_BM * ATT_D * 2;     // 32 KB O staging (4 KB per softmax warp)
+// shared memory: 32 KB Q + 5 x 32 KB K/V + 32 KB O = 224 KB of 227
 
 struct AttnParams {
   const int32_t* perm;
