@@ -325,7 +325,7 @@ def run_gpu(args):
                 "traffic": recorded_traffic("attn"),
                 "peak_source": pk["source"] + ", bf16 burst (kernel timed alone in a short step)",
                 "algorithmic": f"{af:.4g} FLOP per launch = 4*H*Lq*d*sum_i Lkv"}
-    roofline_lce = {"kernel": "lce_fused_kernel", "bound": "hbm", "achieved": lce_gbs, "peak": pk["hbm_gbs"],
+    roofline_lce = {"kernel": "lce_kernel (user-tile + candidate-tile launches)", "bound": "hbm", "achieved": lce_gbs, "peak": pk["hbm_gbs"],
                     "unit": "GB/s", "frac": lce_gbs / pk["hbm_gbs"], "traffic": recorded_traffic("lce"),
                     "tflops": lce_tf, "algorithmic": f"{lb:.4g} bytes per launch (inputs once, Y once)"}
 
