@@ -6,7 +6,9 @@ One step = one request through the whole hot path:
   ikbo_lce_forward  fused LCE  (n_cand 1024, n_users 15, K_u 381, K_c 243, D 256, N 192)
   ikbo_attn_forward broadcast attention (H 8, Lq 32, Lkv 2048, d 128) on the same map
 Inputs are seeded synthetic tensors resident in HBM; the L2 is flushed
-(256 MiB memset) between steps, outside the per-step CUDA events.
+between steps, outside the per-step CUDA events: a 256 MiB memset (no input
+survives in L2), then a 256 MiB read, which evicts the memset's dirty lines
+so that their write-back does not land inside the next timed step.
 
 Output: one JSON line (rank 0).  `value` = algorithmic TFLOP/s of the whole
 step over all ranks (weak scaling: each rank runs its own request);
@@ -36,6 +38,22 @@ sys.path.insert(0, ROOT)
 
 METRIC = "LCE & broadcast-attn BF16 TFLOP/s, % of roofline; µs per 1024-cand request"
 L2_FLUSH_BYTES = 256 << 20
+
+
+class L2Flush:
+    """Cold and clean L2 between timed steps: write a buffer larger than L2,
+    then read another one (evicting the written lines; their write-back runs
+    here, not in the next step's kernels)."""
+
+    def __init__(self, dev):
+        import torch
+        self.w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        self.r = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+
+    def __call__(self):
+        import torch
+        self.w.zero_()
+        torch.amax(self.r)
 
 
 def peaks():
@@ -182,7 +200,7 @@ def config_dict(x, a):
                     "multinomial map)",
         "lce": {"n_cand": x.n_cand, "n_users": x.n_users, "K_u": x.K_u, "K_c": x.K_c, "D": x.D, "N": x.N},
         "attn": {"n_cand": a.n_cand, "n_users": a.n_users, "H": a.H, "Lq": a.Lq, "Lkv": a.Lkv, "d": a.d},
-        "l2": "256 MiB memset between steps (outside the per-step events); each step also streams ~490 MB",
+        "l2": "flushed between steps, outside the per-step events: 256 MiB memset, then a 256 MiB read that evicts its dirty lines (cold, clean L2); each step also streams ~490 MB",
     }
 
 
@@ -267,7 +285,7 @@ def run_gpu(args):
     d = {k: v.to(dev) for k, v in dict(map=x.map, U=x.U, C=x.C, Wu=x.Wu, Wc=x.Wc, b=x.b, Q=a.Q, K=a.K, V=a.V).items()}
     Y = torch.empty(x.n_cand, x.N, x.D, dtype=torch.bfloat16, device=dev)
     O = torch.empty_like(d["Q"])
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
     plan = B.Plan(x.n_cand, max(x.n_users, x.n_cand), a.H)
 
     def step():
@@ -276,7 +294,7 @@ def run_gpu(args):
         plan.attn_forward(d["Q"], d["K"], d["V"], None, O, None, stream)
 
     for _ in range(max(3, args.warmup)):
-        flush.zero_()
+        flush()
         step()
     st = plan.status()
     if st != B.IKBO_OK:
@@ -290,7 +308,7 @@ def run_gpu(args):
     torch.cuda.synchronize()
     with ClockSampler(torch.cuda.current_device()) as clk:
         for k in range(K):
-            flush.zero_()
+            flush()
             e = ev[k]
             e[0].record(stream)
             plan.plan(d["map"], x.n_users, a.H, a.Lq, stream)
@@ -411,7 +429,7 @@ def ablation_run(plan, d, x, a, Y, O, flush, stream, dev, iters=5):
     def timed(fn):
         ts = []
         for _ in range(iters + 1):
-            flush.zero_()
+            flush()
             s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             s.record(stream)
             fn()

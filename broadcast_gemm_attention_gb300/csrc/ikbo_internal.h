@@ -54,6 +54,8 @@ constexpr int LCE_MAX_W_SLOTS = 8;
 
 struct LceParams {
   const int32_t* map;
+  const int32_t* order;   // candidate order for the candidate tiles (a permutation of 0..n_cand-1, grouped
+                          // by user) or null for 0..n_cand-1
   const uint16_t* bias;   // [N] bf16 or null
   uint16_t* Y;            // [n_cand][N][D] bf16
   float* partial;         // [n_users][N][D] fp32 workspace (user GEMM + bias)

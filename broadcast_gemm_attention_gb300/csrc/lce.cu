@@ -93,11 +93,32 @@ __device__ __forceinline__ UnitInfo unit_info(const LceParams& p, int unit) {
     x.dblk = ud - x.row * p.n_dblk;
   } else {
     const int idx = unit - p.n_user_units;
-    x.row = idx / p.n_dblk;
-    x.dblk = idx - x.row * p.n_dblk;
+    const int pos = idx / p.n_dblk;  // position in the candidate order
+    x.dblk = idx - pos * p.n_dblk;
     x.nblk = 0;
+    const int i = p.order ? __ldg(p.order + pos) : pos;
+    x.row = (i >= 0 && i < p.n_cand) ? i : pos;
   }
   return x;
+}
+
+// The t-th unit of this CTA within [u0, u1), or -1 past its end.  User tiles
+// are dealt round-robin.  Candidate tiles go out as one contiguous run of
+// positions in the candidate order per CTA, D block outermost, so that a
+// CTA's consecutive tiles mostly share (user, D block) and its epilogue keeps
+// that user's partial in registers instead of reading it again from L2.
+__device__ __forceinline__ int cta_unit(const LceParams& p, int u0, int u1, int t) {
+  if (u0 < p.n_user_units) {
+    const int unit = u0 + static_cast<int>(blockIdx.x) + t * static_cast<int>(gridDim.x);
+    return unit < u1 ? unit : -1;
+  }
+  const int c0 = static_cast<int>(static_cast<long long>(blockIdx.x) * p.n_cand / gridDim.x);
+  const int c1 = static_cast<int>(static_cast<long long>(blockIdx.x + 1) * p.n_cand / gridDim.x);
+  const int span = c1 - c0;
+  if (span <= 0 || t >= span * p.n_dblk) return -1;
+  const int dblk = t / span;
+  const int pos = c0 + (t - dblk * span);
+  return p.n_user_units + pos * p.n_dblk + dblk;
 }
 
 // columns of a user tile's accumulator (a multiple of 16, at most 64)
@@ -114,7 +135,9 @@ __device__ void lce_producer(const LceParams& p, const LceSmem& s, const CUtenso
   bool wc_loaded = false;
   const uint32_t w_chunk_bytes = static_cast<uint32_t>(p.NB) * BOX_BYTES;
 
-  for (int unit = u0 + blockIdx.x; unit < u1; unit += gridDim.x) {
+  for (int t = 0;; ++t) {
+    const int unit = cta_unit(p, u0, u1, t);
+    if (unit < 0) break;
     const UnitInfo x = unit_info(p, unit);
     const CUtensorMap* tmA = x.is_user ? tmU : tmC;
     const int kc_n = x.is_user ? p.kc_u : p.kc_c;
@@ -156,6 +179,15 @@ __device__ void lce_producer(const LceParams& p, const LceSmem& s, const CUtenso
 }
 
 // ----------------------------------------------------------------- MMA
+// A wait taken by a whole warp: every lane polls, and the lanes agree on the
+// outcome so that a timeout never splits the warp.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const LceSmem& s, const LceParams& p) {
+  const bool ok = mbar_wait(bar, parity, s.abort, p.timeout_ns, 1);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// MMA issuer: the whole warp runs the loop (its values stay warp-uniform) and
+// one elected lane issues; a lone lane pays far more per tcgen05.mma.
 __device__ void lce_mma(const LceParams& p, const LceSmem& s, uint32_t tmem, int u0, int u1) {
   const uint32_t idesc_c = idesc_bf16_f32(LCE_BM, static_cast<uint32_t>(p.N_mma), true, true);
   const uint32_t w_chunk_bytes = static_cast<uint32_t>(p.NB) * BOX_BYTES;
@@ -165,15 +197,17 @@ __device__ void lce_mma(const LceParams& p, const LceSmem& s, uint32_t tmem, int
   uint32_t w_phase = 0;
   bool wc_ready = false;
   int local = 0;
-  for (int unit = u0 + blockIdx.x; unit < u1; unit += gridDim.x, ++local) {
+  for (int t = 0;; ++t, ++local) {
+    const int unit = cta_unit(p, u0, u1, t);
+    if (unit < 0) break;
     const UnitInfo x = unit_info(p, unit);
     const int kc_n = x.is_user ? p.kc_u : p.kc_c;
     int ks_left = x.is_user ? p.ks_u : p.ks_c;
     const int buf = local & 1;
     const uint32_t use = static_cast<uint32_t>(local >> 1);
-    if (!mbar_wait(&s.acc_empty[buf], (use & 1u) ^ 1u, s.abort, p.timeout_ns, 1)) return;
+    if (!warp_wait(&s.acc_empty[buf], (use & 1u) ^ 1u, s, p)) return;
     if (!x.is_user && !wc_ready) {
-      if (!mbar_wait(s.wc_full, 0, s.abort, p.timeout_ns, 1)) return;
+      if (!warp_wait(s.wc_full, 0, s, p)) return;
       wc_ready = true;
     }
     tc_fence_after();
@@ -181,23 +215,33 @@ __device__ void lce_mma(const LceParams& p, const LceSmem& s, uint32_t tmem, int
     const uint32_t idesc =
         x.is_user ? idesc_bf16_f32(LCE_BM, static_cast<uint32_t>(user_tile_n(p, x.nblk)), true, true) : idesc_c;
     for (int kc = 0; kc < kc_n; ++kc) {
-      if (!mbar_wait(&s.a_full[stage], a_phase, s.abort, p.timeout_ns, 1)) return;
-      if (x.is_user && !mbar_wait(&s.w_full[wslot], w_phase, s.abort, p.timeout_ns, 1)) return;
+      if (!warp_wait(&s.a_full[stage], a_phase, s, p)) return;
+      if (x.is_user && !warp_wait(&s.w_full[wslot], w_phase, s, p)) return;
       tc_fence_after();
       const uint32_t a_base = smem_u32(s.a_ring + static_cast<size_t>(stage) * LCE_A_STAGE_BYTES);
       const uint32_t b_base = smem_u32(s.w_region + (x.is_user ? static_cast<size_t>(wslot) * BOX_BYTES
                                                                   : static_cast<size_t>(kc) * w_chunk_bytes));
       const int nsteps = ks_left < 4 ? ks_left : 4;
-      for (int st = 0; st < nsteps; ++st) {
-        // 16 k rows of 128 bytes per MMA step; 64-element blocks along M / N are one box apart
-        const uint64_t adesc = sdesc_sw128(a_base + st * 2048u, BOX_BYTES, 1024u);
-        const uint64_t bdesc = sdesc_sw128(b_base + st * 2048u, BOX_BYTES, 1024u);
-        mma_bf16_ss(d_tmem, adesc, bdesc, idesc, (kc > 0 || st > 0) ? 1u : 0u);
+      // 16 k rows of 128 bytes per MMA step; 64-element blocks along M / N
+      // are one box apart; steps advance the start address by 2048 bytes
+      const uint64_t adesc = sdesc_sw128(a_base, BOX_BYTES, 1024u);
+      const uint64_t bdesc = sdesc_sw128(b_base, BOX_BYTES, 1024u);
+      const uint32_t acc0 = kc > 0 ? 1u : 0u;
+      if (elect_one()) {
+        if (nsteps == 4) {
+#pragma unroll
+          for (int st = 0; st < 4; ++st)
+            mma_bf16_ss(d_tmem, adesc + st * (2048u >> 4), bdesc + st * (2048u >> 4), idesc, st > 0 ? 1u : acc0);
+        } else {
+          for (int st = 0; st < nsteps; ++st)
+            mma_bf16_ss(d_tmem, adesc + st * (2048u >> 4), bdesc + st * (2048u >> 4), idesc, st > 0 ? 1u : acc0);
+        }
+        mma_commit(&s.a_empty[stage]);
+        if (x.is_user) mma_commit(&s.w_empty[wslot]);
       }
+      __syncwarp();
       ks_left -= nsteps;
-      mma_commit(&s.a_empty[stage]);
       if (x.is_user) {
-        mma_commit(&s.w_empty[wslot]);
         if (++wslot == p.w_slots) {
           wslot = 0;
           w_phase ^= 1u;
@@ -208,7 +252,8 @@ __device__ void lce_mma(const LceParams& p, const LceSmem& s, uint32_t tmem, int
         a_phase ^= 1u;
       }
     }
-    mma_commit(&s.acc_full[buf]);
+    if (elect_one()) mma_commit(&s.acc_full[buf]);
+    __syncwarp();
   }
 }
 
@@ -260,7 +305,12 @@ __device__ void lce_epilogue(const LceParams& p, const LceSmem& s, uint32_t tmem
   int local = 0;
   uint32_t pubs = 0;
   int users_ready = -1;  // candidate tiles: -1 not checked yet, 1 all user partials seen, 0 gave up
-  for (int unit = u0 + blockIdx.x; unit < u1; unit += gridDim.x, ++local) {
+  // the user partial of the current (user, D block), kept across tiles
+  float pre[EPI_PREFETCH][32];
+  int pre_u = -1, pre_dblk = -1;
+  for (int t = 0;; ++t, ++local) {
+    const int unit = cta_unit(p, u0, u1, t);
+    if (unit < 0) break;
     const UnitInfo x = unit_info(p, unit);
     const int buf = local & 1;
     const uint32_t use = static_cast<uint32_t>(local >> 1);
@@ -296,9 +346,9 @@ __device__ void lce_epilogue(const LceParams& p, const LceSmem& s, uint32_t tmem
       }
       tc_fence_before();
       mbar_arrive(&s.acc_empty[buf]);
-      // publish: every writer fences its P rows, then one thread releases the
-      // flag once all epilogue threads have arrived (bounded wait)
-      __threadfence();
+      // publish: the writers arrive on an mbarrier (release at CTA scope), and
+      // the one thread that has seen all of them arrive fences and releases
+      // the flag at GPU scope, which covers their stores (cumulativity)
       mbar_arrive(s.pub);
       if (leader) {
         const bool all = mbar_wait(s.pub, pubs & 1u, s.abort, p.timeout_ns, 1);
@@ -316,8 +366,9 @@ __device__ void lce_epilogue(const LceParams& p, const LceSmem& s, uint32_t tmem
       if (users_ready < 0) users_ready = wait_all_user_partials(p) ? 1 : 0;
       const bool ready = uok && users_ready == 1;
       const float* P = p.partial + static_cast<size_t>(uok ? u : 0) * ND + d;
-      float pre[EPI_PREFETCH][32];
-      if (ready) {
+      if (ready && (u != pre_u || x.dblk != pre_dblk)) {
+        pre_u = u;
+        pre_dblk = x.dblk;
 #pragma unroll
         for (int k = 0; k < EPI_PREFETCH; ++k) {
           const int c = half + 2 * k;
@@ -373,6 +424,8 @@ __device__ void lce_epilogue(const LceParams& p, const LceSmem& s, uint32_t tmem
 // release flags), the other launch the candidate tiles, which acquire the
 // flags and add P in their epilogue.  The user launch runs first on the
 // stream, so the candidate launch finds every flag set at its first check.
+// (One launch with user tiles first in every CTA's list measured slower: its
+// candidate epilogues wait for user tiles still running on other SMs.)
 template <bool kUserPhase>
 __global__ void __launch_bounds__(LCE_THREADS, 1)
     lce_kernel(const __grid_constant__ CUtensorMap tmU, const __grid_constant__ CUtensorMap tmC,
@@ -427,7 +480,7 @@ __global__ void __launch_bounds__(LCE_THREADS, 1)
     if (warp == 0) {
       if (lane_id() == 0) lce_producer(p, s, &tmU, &tmC, &tmWu, &tmWc, u0, u1);
     } else if (warp == 1) {
-      if (lane_id() == 0) lce_mma(p, s, tmem, u0, u1);
+      lce_mma(p, s, tmem, u0, u1);
     }
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 216;");
