@@ -103,21 +103,23 @@ __device__ __forceinline__ UnitInfo unit_info(const LceParams& p, int unit) {
 }
 
 // The t-th unit of this CTA within [u0, u1), or -1 past its end.  User tiles
-// are dealt round-robin.  Candidate tiles go out as one contiguous run of
-// positions in the candidate order per CTA, D block outermost, so that a
-// CTA's consecutive tiles mostly share (user, D block) and its epilogue keeps
-// that user's partial in registers instead of reading it again from L2.
+// are dealt round-robin.  Candidate tiles, numbered D-block-major over the
+// candidate order (q = dblk * n_cand + position), go out as one contiguous
+// range of q per CTA: a CTA stays within one D block (crossing at most one
+// boundary) on consecutive candidates that mostly share a user, so its
+// epilogue loads that user's partial once and keeps it in registers.
 __device__ __forceinline__ int cta_unit(const LceParams& p, int u0, int u1, int t) {
   if (u0 < p.n_user_units) {
     const int unit = u0 + static_cast<int>(blockIdx.x) + t * static_cast<int>(gridDim.x);
     return unit < u1 ? unit : -1;
   }
-  const int c0 = static_cast<int>(static_cast<long long>(blockIdx.x) * p.n_cand / gridDim.x);
-  const int c1 = static_cast<int>(static_cast<long long>(blockIdx.x + 1) * p.n_cand / gridDim.x);
-  const int span = c1 - c0;
-  if (span <= 0 || t >= span * p.n_dblk) return -1;
-  const int dblk = t / span;
-  const int pos = c0 + (t - dblk * span);
+  const long long nq = static_cast<long long>(p.n_cand) * p.n_dblk;
+  const int q0 = static_cast<int>(blockIdx.x * nq / gridDim.x);
+  const int q1 = static_cast<int>((blockIdx.x + 1) * nq / gridDim.x);
+  if (t >= q1 - q0) return -1;
+  const int q = q0 + t;
+  const int dblk = q / p.n_cand;
+  const int pos = q - dblk * p.n_cand;
   return p.n_user_units + pos * p.n_dblk + dblk;
 }
 
