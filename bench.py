@@ -226,9 +226,18 @@ def cpu_oracle_sample(x, a, n: int, seed: int = 0):
 
 
 def calibrate_oracle(x, a, seconds: float, lo: int = 1, hi: int = 1024):
-    """Candidates per sample so that one sample takes about `seconds`."""
-    dt, _, _, _ = cpu_oracle_sample(x, a, 2, seed=12345)
-    n = int(round(seconds / max(dt / 2, 1e-6)))
+    """Candidates per sample so that one sample takes about `seconds`.
+
+    Two probes: a tiny one, then one of about a quarter of the target, whose
+    per-candidate time reflects the thread parallelism the full sample gets
+    (a 2-candidate probe on a many-core host overestimates it several-fold)."""
+    n0 = 16
+    dt, _, _, _ = cpu_oracle_sample(x, a, n0, seed=12345)
+    n1 = max(n0, min(hi, int(round(0.25 * seconds / max(dt / n0, 1e-6)))))
+    if n1 > n0:
+        dt, _, _, _ = cpu_oracle_sample(x, a, n1, seed=12346)
+        n0 = n1
+    n = int(round(seconds / max(dt / n0, 1e-6)))
     return max(lo, min(hi, n))
 
 
