@@ -393,6 +393,11 @@ def run_gpu(args):
     if not args.no_ablation:
         ablation = ablation_run(plan, d, x, a, Y, O, flush, stream, dev)
 
+    # ---------------- self + target attention in one launch vs two
+    self_target = None
+    if not args.no_self_target:
+        self_target = self_target_run(plan, d, x, a, O, flush, stream, dev)
+
     plan.close()
     if rank != 0:
         if dist:
@@ -419,11 +424,52 @@ def run_gpu(args):
                     "attn_us_median": 1e3 * statistics.median(attn_ms)},
         "roofline": roofline, "roofline_lce": roofline_lce,
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": gpu_launches,
-        "clocks": clk.summary(), "ablation": ablation,
+        "clocks": clk.summary(), "ablation": ablation, "self_target": self_target,
     }
     print(json.dumps(out), flush=True)
     if dist:
         dist.destroy_process_group()
+
+
+def self_target_run(plan, d, x, a, O, flush, stream, dev, Lq_u=64, iters=20):
+    """The request's target attention plus each user's own Lq_u queries over
+    the same K/V: one launch (ikbo_attn_self_target_forward) against two
+    (ikbo_attn_forward for the target part, then for the self part through
+    a plan whose map is the identity over users)."""
+    import statistics
+    import torch
+    from broadcast_gemm_attention_gb300 import binding as B
+    from broadcast_gemm_attention_gb300 import inputs as gen
+    Qu = gen.make_user_queries(1093, x.n_users, a.H, Lq_u, a.d).to(dev)
+    Ou = torch.empty_like(Qu)
+    Ou2 = torch.empty_like(Qu)
+    ident = torch.arange(x.n_users, dtype=torch.int32, device=dev)
+    plan_u = B.Plan(x.n_users, x.n_users, a.H)
+    plan_u.plan(ident, x.n_users, a.H, Lq_u, stream)
+
+    def timed(fn):
+        ts = []
+        for k in range(iters + 2):
+            flush()
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record(stream)
+            fn()
+            e.record(stream)
+            torch.cuda.synchronize()
+            if k >= 2:
+                ts.append(s.elapsed_time(e))
+        return 1e3 * statistics.median(ts)
+
+    fused = timed(lambda: plan.attn_self_target_forward(d["Q"], Qu, d["K"], d["V"], None, O, Ou, None, stream))
+    sep = timed(lambda: (plan.attn_forward(d["Q"], d["K"], d["V"], None, O, None, stream),
+                         plan_u.attn_forward(Qu, d["K"], d["V"], None, Ou2, None, stream)))
+    st = plan.status()
+    same = bool(torch.equal(Ou, Ou2))
+    plan_u.close()
+    flops = 4.0 * a.H * a.d * a.Lkv * (x.n_cand * a.Lq + x.n_users * Lq_u)
+    return {"Lq_u": Lq_u, "fused_us": fused, "separate_us": sep, "fused_tflops": flops / (fused * 1e-6) / 1e12,
+            "launches": {"fused": 1, "separate": 2}, "self_rows_identical": same,
+            "status": "ok" if st == B.IKBO_OK else B.ikbo_status_string(st)}
 
 
 def ablation_run(plan, d, x, a, Y, O, flush, stream, dev, iters=5):
@@ -478,6 +524,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ikbo", "reference"], default="ikbo")
     ap.add_argument("--no-ablation", action="store_true")
+    ap.add_argument("--no-self-target", action="store_true", help="skip the self + target attention comparison")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=15.0,

@@ -42,6 +42,7 @@ SIGNATURES = {
     "ikbo_lce_forward": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp]),
     "ikbo_lce_forward_noalloc": (_i, [_vp, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp]),
     "ikbo_attn_forward": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, ctypes.c_float, _vp]),
+    "ikbo_attn_self_target_forward": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, ctypes.c_float, _vp]),
     "ikbo_plan_get_status": (_i, [_vp, _vp]),
     "ikbo_plan_set_debug": (_i, [_vp, ctypes.c_uint]),
     "ikbo_plan_set_timeout_ns": (_i, [_vp, _u64]),
@@ -202,6 +203,29 @@ def ikbo_attn_forward(plan: int, Q: torch.Tensor, K: torch.Tensor, V: torch.Tens
                                     _dev(O, bf, "O"), Lkv, d, float(scale), _stream(stream)), "ikbo_attn_forward")
 
 
+def ikbo_attn_self_target_forward(plan: int, Q: torch.Tensor, Q_user: torch.Tensor, K: torch.Tensor,
+                                  V: torch.Tensor, kv_offsets: Optional[torch.Tensor], O: torch.Tensor,
+                                  O_user: torch.Tensor, scale: Optional[float] = None, stream=None) -> None:
+    """Target attention (as ikbo_attn_forward) and the users' own queries
+    O_user[u,h] = softmax(Q_user[u,h] K[u,h]^T scale) V[u,h], in one launch."""
+    bf = torch.bfloat16
+    d = Q.shape[-1]
+    if kv_offsets is None:
+        Lkv = K.shape[2]
+        optr = None
+    else:
+        Lkv = K.shape[0]
+        optr = _dev(kv_offsets, torch.int32, "kv_offsets")
+    if K.shape != V.shape or O.shape != Q.shape or O_user.shape != Q_user.shape or Q_user.dim() != 4:
+        raise ValueError("shape mismatch among Q/O, Q_user/O_user, K/V")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    _check(load().ikbo_attn_self_target_forward(plan, _dev(Q, bf, "Q"), _dev(Q_user, bf, "Q_user"), _dev(K, bf, "K"),
+                                                _dev(V, bf, "V"), optr, _dev(O, bf, "O"), _dev(O_user, bf, "O_user"),
+                                                Q_user.shape[2], Lkv, d, float(scale), _stream(stream)),
+           "ikbo_attn_self_target_forward")
+
+
 def ikbo_plan_get_status(plan: int, stream=None) -> int:
     """Synchronises the stream; returns the device-detected status code (and clears it)."""
     return int(load().ikbo_plan_get_status(plan, _stream(stream)))
@@ -251,6 +275,9 @@ class Plan:
 
     def attn_forward(self, Q, K, V, kv_offsets, O, scale=None, stream=None):
         ikbo_attn_forward(self.handle, Q, K, V, kv_offsets, O, scale, stream)
+
+    def attn_self_target_forward(self, Q, Q_user, K, V, kv_offsets, O, O_user, scale=None, stream=None):
+        ikbo_attn_self_target_forward(self.handle, Q, Q_user, K, V, kv_offsets, O, O_user, scale, stream)
 
     def status(self, stream=None) -> int:
         return ikbo_plan_get_status(self.handle, stream)

@@ -20,8 +20,8 @@ size_t lce_smem_bytes(const LceParams& p);
 cudaError_t launch_lce(const CUtensorMap& tmU, const CUtensorMap& tmC, const CUtensorMap& tmWu,
                        const CUtensorMap& tmWc, const LceParams& p, int num_sms, cudaStream_t s);
 size_t attn_smem_bytes();
-cudaError_t launch_attn(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV, const AttnParams& p,
-                        int grid, cudaStream_t s);
+cudaError_t launch_attn(const CUtensorMap& tmQ, const CUtensorMap& tmQu, const CUtensorMap& tmK,
+                        const CUtensorMap& tmV, const AttnParams& p, int grid, cudaStream_t s);
 }  // namespace ikbo
 
 using namespace ikbo;
@@ -123,9 +123,83 @@ void free_plan(ikbo_plan_t p) {
 
 }  // namespace
 
+namespace {
+// Both attention entry points: the work list's (target) units, plus, when
+// Q_user is given, n_users * H * ceil(Lq_u / 128) self units in the same launch.
+ikbo_status_t attn_launch(ikbo_plan_t p, const void* Q, const void* Q_user, const void* K, const void* V,
+                          const int32_t* d_kv_offsets, void* O, void* O_user, int Lq_u, int Lkv, int d, float scale,
+                          cudaStream_t stream) {
+  if (!p) return IKBO_ERR_INVALID_ARG;
+  if (!p->planned) return IKBO_ERR_NOT_PLANNED;
+  if (!Q || !K || !V || !O) return IKBO_ERR_INVALID_ARG;
+  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O)) return IKBO_ERR_INVALID_ARG;
+  if (d != ATT_D) return IKBO_ERR_UNSUPPORTED;
+  if (Lkv < 1 || !(scale > 0.f) || !std::isfinite(scale)) return IKBO_ERR_INVALID_ARG;
+  const bool self = Q_user != nullptr;
+  if (self) {
+    if (!O_user || !aligned16(Q_user) || !aligned16(O_user) || Lq_u < 1) return IKBO_ERR_INVALID_ARG;
+    if (Lq_u % 8 != 0) return IKBO_ERR_UNSUPPORTED;
+  }
+  if (attn_smem_bytes() > p->max_smem) return IKBO_ERR_UNSUPPORTED;
+
+  AttnParams ap;
+  std::memset(&ap, 0, sizeof(ap));
+  ap.perm = p->d_perm;
+  ap.work = p->d_work;
+  ap.n_units = p->d_n_units;
+  ap.kv_offsets = d_kv_offsets;
+  ap.O = static_cast<uint16_t*>(O);
+  ap.status = p->d_status;
+  ap.n_cand = p->n_cand;
+  ap.n_users = p->n_users;
+  ap.H = p->H;
+  ap.Lq = p->Lq;
+  ap.Lkv = Lkv;
+  ap.cands_per_tile = ATT_BM / p->Lq;
+  ap.scale_log2 = scale * 1.4426950408889634f;
+  ap.timeout_ns = p->timeout_ns;
+
+  const uint64_t H = static_cast<uint64_t>(p->H), Lq = static_cast<uint64_t>(p->Lq);
+  CUtensorMap tmQ, tmQu, tmK, tmV;
+  const uint64_t qd[4] = {ATT_D, Lq, H, static_cast<uint64_t>(p->n_cand)};
+  const uint64_t qs[3] = {ATT_D * 2, Lq * ATT_D * 2, H * Lq * ATT_D * 2};
+  const uint32_t qbox[4] = {64, static_cast<uint32_t>(p->Lq), 1, 1};
+  if (!encode_bf16(&tmQ, Q, 4, qd, qs, qbox)) return IKBO_ERR_CUDA;
+  if (self) {
+    ap.O_user = static_cast<uint16_t*>(O_user);
+    ap.Lq_u = Lq_u;
+    ap.self_rows = Lq_u < ATT_BM ? Lq_u : ATT_BM;
+    ap.self_tiles = (Lq_u + ap.self_rows - 1) / ap.self_rows;
+    ap.n_self = p->n_users * p->H * ap.self_tiles;
+    const uint64_t Lu = static_cast<uint64_t>(Lq_u);
+    const uint64_t ud[4] = {ATT_D, Lu, H, static_cast<uint64_t>(p->n_users)};
+    const uint64_t us[3] = {ATT_D * 2, Lu * ATT_D * 2, H * Lu * ATT_D * 2};
+    const uint32_t ubox[4] = {64, static_cast<uint32_t>(ap.self_rows), 1, 1};
+    if (!encode_bf16(&tmQu, Q_user, 4, ud, us, ubox)) return IKBO_ERR_CUDA;
+  } else {
+    tmQu = tmQ;  // not read without self units
+  }
+  if (d_kv_offsets) {
+    const uint64_t kd[3] = {ATT_D, H, static_cast<uint64_t>(Lkv)};
+    const uint64_t ks[2] = {ATT_D * 2, H * ATT_D * 2};
+    const uint32_t kbox[3] = {64, 1, ATT_BN};
+    if (!encode_bf16(&tmK, K, 3, kd, ks, kbox) || !encode_bf16(&tmV, V, 3, kd, ks, kbox)) return IKBO_ERR_CUDA;
+  } else {
+    const uint64_t L = static_cast<uint64_t>(Lkv);
+    const uint64_t kd[4] = {ATT_D, L, H, static_cast<uint64_t>(p->n_users)};
+    const uint64_t ks[3] = {ATT_D * 2, L * ATT_D * 2, H * L * ATT_D * 2};
+    const uint32_t kbox[4] = {64, ATT_BN, 1, 1};
+    if (!encode_bf16(&tmK, K, 4, kd, ks, kbox) || !encode_bf16(&tmV, V, 4, kd, ks, kbox)) return IKBO_ERR_CUDA;
+  }
+  if (launch_attn(tmQ, tmQu, tmK, tmV, ap, p->num_sms, stream) != cudaSuccess) return IKBO_ERR_CUDA;
+  p->launches++;
+  return IKBO_OK;
+}
+}  // namespace
+
 extern "C" {
 
-int ikbo_version(void) { return 100; }
+int ikbo_version(void) { return 101; }
 
 const char* ikbo_status_string(ikbo_status_t s) {
   switch (s) {
@@ -329,55 +403,18 @@ ikbo_status_t ikbo_lce_forward(ikbo_plan_t p, const void* U, const void* C, cons
   return IKBO_OK;
 }
 
+
 ikbo_status_t ikbo_attn_forward(ikbo_plan_t p, const void* Q, const void* K, const void* V,
                                 const int32_t* d_kv_offsets, void* O, int Lkv, int d, float scale,
                                 cudaStream_t stream) {
-  if (!p) return IKBO_ERR_INVALID_ARG;
-  if (!p->planned) return IKBO_ERR_NOT_PLANNED;
-  if (!Q || !K || !V || !O) return IKBO_ERR_INVALID_ARG;
-  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O)) return IKBO_ERR_INVALID_ARG;
-  if (d != ATT_D) return IKBO_ERR_UNSUPPORTED;
-  if (Lkv < 1 || !(scale > 0.f) || !std::isfinite(scale)) return IKBO_ERR_INVALID_ARG;
-  if (attn_smem_bytes() > p->max_smem) return IKBO_ERR_UNSUPPORTED;
+  return attn_launch(p, Q, nullptr, K, V, d_kv_offsets, O, nullptr, 0, Lkv, d, scale, stream);
+}
 
-  AttnParams ap;
-  std::memset(&ap, 0, sizeof(ap));
-  ap.perm = p->d_perm;
-  ap.work = p->d_work;
-  ap.n_units = p->d_n_units;
-  ap.kv_offsets = d_kv_offsets;
-  ap.O = static_cast<uint16_t*>(O);
-  ap.status = p->d_status;
-  ap.n_cand = p->n_cand;
-  ap.n_users = p->n_users;
-  ap.H = p->H;
-  ap.Lq = p->Lq;
-  ap.Lkv = Lkv;
-  ap.cands_per_tile = ATT_BM / p->Lq;
-  ap.scale_log2 = scale * 1.4426950408889634f;
-  ap.timeout_ns = p->timeout_ns;
-
-  const uint64_t H = static_cast<uint64_t>(p->H), Lq = static_cast<uint64_t>(p->Lq);
-  CUtensorMap tmQ, tmK, tmV;
-  const uint64_t qd[4] = {ATT_D, Lq, H, static_cast<uint64_t>(p->n_cand)};
-  const uint64_t qs[3] = {ATT_D * 2, Lq * ATT_D * 2, H * Lq * ATT_D * 2};
-  const uint32_t qbox[4] = {64, static_cast<uint32_t>(p->Lq), 1, 1};
-  if (!encode_bf16(&tmQ, Q, 4, qd, qs, qbox)) return IKBO_ERR_CUDA;
-  if (d_kv_offsets) {
-    const uint64_t kd[3] = {ATT_D, H, static_cast<uint64_t>(Lkv)};
-    const uint64_t ks[2] = {ATT_D * 2, H * ATT_D * 2};
-    const uint32_t kbox[3] = {64, 1, ATT_BN};
-    if (!encode_bf16(&tmK, K, 3, kd, ks, kbox) || !encode_bf16(&tmV, V, 3, kd, ks, kbox)) return IKBO_ERR_CUDA;
-  } else {
-    const uint64_t L = static_cast<uint64_t>(Lkv);
-    const uint64_t kd[4] = {ATT_D, L, H, static_cast<uint64_t>(p->n_users)};
-    const uint64_t ks[3] = {ATT_D * 2, L * ATT_D * 2, H * L * ATT_D * 2};
-    const uint32_t kbox[4] = {64, ATT_BN, 1, 1};
-    if (!encode_bf16(&tmK, K, 4, kd, ks, kbox) || !encode_bf16(&tmV, V, 4, kd, ks, kbox)) return IKBO_ERR_CUDA;
-  }
-  if (launch_attn(tmQ, tmK, tmV, ap, p->num_sms, stream) != cudaSuccess) return IKBO_ERR_CUDA;
-  p->launches++;
-  return IKBO_OK;
+ikbo_status_t ikbo_attn_self_target_forward(ikbo_plan_t p, const void* Q, const void* Q_user, const void* K,
+                                            const void* V, const int32_t* d_kv_offsets, void* O, void* O_user,
+                                            int Lq_u, int Lkv, int d, float scale, cudaStream_t stream) {
+  if (!Q_user) return IKBO_ERR_INVALID_ARG;
+  return attn_launch(p, Q, Q_user, K, V, d_kv_offsets, O, O_user, Lq_u, Lkv, d, scale, stream);
 }
 
 }  // extern "C"

@@ -129,28 +129,56 @@ __device__ __forceinline__ AttSmem carve(uint8_t* base) {
 }
 
 struct Unit {
-  int u, h, start, cnt;
+  int u, h, start, cnt;  // self units: start = first query row of Q_user[u][h], cnt = its rows
   bool ok;
+  bool self;             // the user's own queries (Q_user) rather than its candidates'
   int L;       // keys of this user
   int kv0;     // first packed row (jagged) or 0
   int ntiles;  // ceil(L / 128)
 };
 
+// Self units (see ikbo_attn_self_target_forward) follow the work list's
+// units; they are numbered user-major, then head, then query tile, and carry
+// this bit in their user field.
+constexpr int SELF_UNIT = 1 << 30;
+
 // The work entry is loaded one unit ahead (the load is issued early and only
 // waited for where the entry is first used) so the dependent reads of the
 // next unit stay off the critical path.
-__device__ __forceinline__ int4 load_work(const AttnParams& p, int unit, int n_units) {
-  return unit < n_units ? __ldg(reinterpret_cast<const int4*>(p.work) + unit) : make_int4(-1, -1, -1, -1);
+struct UnitCount {
+  int target;  // work-list units (read once per CTA)
+  int total;   // target + self units
+};
+
+template <bool kSelf>
+__device__ __forceinline__ int4 load_work(const AttnParams& p, int unit, const UnitCount& n) {
+  if (unit >= n.total) return make_int4(-1, -1, -1, -1);
+  const int n_target = n.target;
+  if (!kSelf || unit < n_target) return __ldg(reinterpret_cast<const int4*>(p.work) + unit);
+  const int s = unit - n_target;
+  const int per_user = p.H * p.self_tiles;
+  const int u = s / per_user;
+  const int rem = s - u * per_user;
+  const int h = rem / p.self_tiles;
+  return make_int4(u | SELF_UNIT, h, rem - h * p.self_tiles, 0);
 }
 
+template <bool kSelf>
 __device__ __forceinline__ Unit decode(const AttnParams& p, int4 w) {
   Unit x;
-  x.u = w.x;
+  x.self = kSelf && w.x >= 0 && (w.x & SELF_UNIT);
+  x.u = x.self ? (w.x & ~SELF_UNIT) : w.x;
   x.h = w.y;
-  x.start = w.z;
-  x.cnt = w.w;
-  x.ok = x.u >= 0 && x.u < p.n_users && x.h >= 0 && x.h < p.H && x.cnt >= 1 && x.cnt <= p.cands_per_tile &&
-         x.start >= 0 && x.start + x.cnt <= p.n_cand;
+  if (x.self) {
+    x.start = w.z * p.self_rows;
+    x.cnt = min(p.self_rows, p.Lq_u - x.start);
+    x.ok = x.u < p.n_users && x.h >= 0 && x.h < p.H && w.z >= 0 && w.z < p.self_tiles && x.cnt >= 1;
+  } else {
+    x.start = w.z;
+    x.cnt = w.w;
+    x.ok = x.u >= 0 && x.u < p.n_users && x.h >= 0 && x.h < p.H && x.cnt >= 1 && x.cnt <= p.cands_per_tile &&
+           x.start >= 0 && x.start + x.cnt <= p.n_cand;
+  }
   if (!x.ok) {
     x.L = 0;
     x.kv0 = 0;
@@ -218,7 +246,7 @@ struct QSlots {
 
 __device__ __forceinline__ void load_slots(const AttnParams& p, const Unit& x, QSlots& q) {
 #pragma unroll
-  for (int j = 0; j < 16; ++j) q.cand[j] = (x.ok && j < x.cnt) ? __ldg(p.perm + x.start + j) : p.n_cand;
+  for (int j = 0; j < 16; ++j) q.cand[j] = (x.ok && !x.self && j < x.cnt) ? __ldg(p.perm + x.start + j) : p.n_cand;
 }
 
 // K or V tile jt of unit x into a ring stage
@@ -233,18 +261,19 @@ __device__ __forceinline__ void load_kv_tile(const AttnParams& p, const CUtensor
   }
 }
 
+template <bool kSelf>
 __device__ void att_producer_qk(const AttnParams& p, const AttSmem& s, const CUtensorMap* tmQ,
-                                const CUtensorMap* tmK, int n_units) {
+                                const CUtensorMap* tmQu, const CUtensorMap* tmK, const UnitCount& n_units) {
   uint32_t g = 0;   // K tiles loaded
   uint32_t qc = 0;  // Q tiles loaded
   const int cpt = p.cands_per_tile;
   int unit = blockIdx.x;
-  Unit x = decode(p, load_work(p, unit, n_units));
+  Unit x = decode<kSelf>(p, load_work<kSelf>(p, unit, n_units));
   QSlots qs;
   load_slots(p, x, qs);
-  while (unit < n_units) {
+  while (unit < n_units.total) {
     const int nunit = unit + static_cast<int>(gridDim.x);
-    const int4 nw = load_work(p, nunit, n_units);
+    const int4 nw = load_work<kSelf>(p, nunit, n_units);
     Unit nx;
     QSlots nqs;
     bool prefetched = false;
@@ -252,13 +281,19 @@ __device__ void att_producer_qk(const AttnParams& p, const AttSmem& s, const CUt
     if (x.ntiles > 0) {
       if (!mbar_wait(s.q_empty, (qc & 1u) ^ 1u, s.abort, p.timeout_ns, 1)) return;
       ++qc;
-      mbar_arrive_expect_tx(s.q_full, static_cast<uint32_t>(cpt * p.Lq * ATT_D * 2));
+      if (x.self) {  // rows start .. start + self_rows - 1 of Q_user[u][h] (past Lq_u: TMA zero fill)
+        mbar_arrive_expect_tx(s.q_full, static_cast<uint32_t>(p.self_rows * ATT_D * 2));
+        tma_load_4d(s.q, tmQu, s.q_full, 0, x.start, x.h, x.u);
+        tma_load_4d(s.q + HALF_TILE, tmQu, s.q_full, 64, x.start, x.h, x.u);
+      } else {
+        mbar_arrive_expect_tx(s.q_full, static_cast<uint32_t>(cpt * p.Lq * ATT_D * 2));
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        if (j < cpt) {
-          uint8_t* dst = s.q + j * p.Lq * 128;
-          tma_load_4d(dst, tmQ, s.q_full, 0, 0, x.h, qs.cand[j]);
-          tma_load_4d(dst + HALF_TILE, tmQ, s.q_full, 64, 0, x.h, qs.cand[j]);
+        for (int j = 0; j < 16; ++j) {
+          if (j < cpt) {
+            uint8_t* dst = s.q + j * p.Lq * 128;
+            tma_load_4d(dst, tmQ, s.q_full, 0, 0, x.h, qs.cand[j]);
+            tma_load_4d(dst + HALF_TILE, tmQ, s.q_full, 64, 0, x.h, qs.cand[j]);
+          }
         }
       }
       for (int jt = 0; jt < x.ntiles; ++jt, ++g) {
@@ -268,13 +303,13 @@ __device__ void att_producer_qk(const AttnParams& p, const AttSmem& s, const CUt
         load_kv_tile(p, tmK, s.k + st * ATT_KV_STAGE_BYTES, &s.k_full[st], x, jt);
         if (!prefetched) {  // the next unit's entry has arrived by now
           prefetched = true;
-          nx = decode(p, nw);
+          nx = decode<kSelf>(p, nw);
           load_slots(p, nx, nqs);
         }
       }
     }
     if (!prefetched) {
-      nx = decode(p, nw);
+      nx = decode<kSelf>(p, nw);
       load_slots(p, nx, nqs);
     }
     x = nx;
@@ -283,14 +318,15 @@ __device__ void att_producer_qk(const AttnParams& p, const AttSmem& s, const CUt
   }
 }
 
-__device__ void att_producer_v(const AttnParams& p, const AttSmem& s, const CUtensorMap* tmV, int n_units) {
+template <bool kSelf>
+__device__ void att_producer_v(const AttnParams& p, const AttSmem& s, const CUtensorMap* tmV, const UnitCount& n_units) {
   uint32_t g = 0;  // V tiles loaded
   int unit = blockIdx.x;
-  int4 w = load_work(p, unit, n_units);
-  while (unit < n_units) {
+  int4 w = load_work<kSelf>(p, unit, n_units);
+  while (unit < n_units.total) {
     const int nunit = unit + static_cast<int>(gridDim.x);
-    const int4 nw = load_work(p, nunit, n_units);
-    const Unit x = decode(p, w);
+    const int4 nw = load_work<kSelf>(p, nunit, n_units);
+    const Unit x = decode<kSelf>(p, w);
     for (int jt = 0; jt < x.ntiles; ++jt, ++g) {
       const int st = ring_stage<ATT_V_STAGES>(g);
       if (!mbar_wait(&s.v_empty[st], ring_phase<ATT_V_STAGES>(g) ^ 1u, s.abort, p.timeout_ns, 1)) return;
@@ -353,14 +389,15 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
 
 // S issuer (whole warp; one elected lane issues): tile g goes to S_(g&1)
 // once the softmax has read S(g-2) out of it.
-__device__ void att_s_issuer(const AttnParams& p, const AttSmem& s, uint32_t tmem, int n_units) {
+template <bool kSelf>
+__device__ void att_s_issuer(const AttnParams& p, const AttSmem& s, uint32_t tmem, const UnitCount& n_units) {
   uint32_t g = 0, qu = 0;
   int unit = blockIdx.x;
-  int4 w = load_work(p, unit, n_units);
-  while (unit < n_units) {
+  int4 w = load_work<kSelf>(p, unit, n_units);
+  while (unit < n_units.total) {
     const int nunit = unit + static_cast<int>(gridDim.x);
-    const int4 nw = load_work(p, nunit, n_units);
-    const Unit x = decode(p, w);
+    const int4 nw = load_work<kSelf>(p, nunit, n_units);
+    const Unit x = decode<kSelf>(p, w);
     if (x.ntiles > 0) {
       const int last_ss = min(1, x.ntiles - 1);
       for (int jt = 0; jt < x.ntiles; ++jt, ++g) {
@@ -400,14 +437,15 @@ __device__ void att_s_issuer(const AttnParams& p, const AttSmem& s, uint32_t tme
 // P.V issuer (whole warp; one elected lane issues): tile g once its P is
 // written; the unit's first one also waits for the previous unit's epilogue
 // to have read O.
-__device__ void att_pv_issuer(const AttnParams& p, const AttSmem& s, uint32_t tmem, int n_units) {
+template <bool kSelf>
+__device__ void att_pv_issuer(const AttnParams& p, const AttSmem& s, uint32_t tmem, const UnitCount& n_units) {
   uint32_t g = 0, ou = 0;
   int unit = blockIdx.x;
-  int4 w = load_work(p, unit, n_units);
-  while (unit < n_units) {
+  int4 w = load_work<kSelf>(p, unit, n_units);
+  while (unit < n_units.total) {
     const int nunit = unit + static_cast<int>(gridDim.x);
-    const int4 nw = load_work(p, nunit, n_units);
-    const Unit x = decode(p, w);
+    const int4 nw = load_work<kSelf>(p, nunit, n_units);
+    const Unit x = decode<kSelf>(p, w);
     for (int jt = 0; jt < x.ntiles; ++jt, ++g) {
       const int vst = ring_stage<ATT_V_STAGES>(g);
       if (!warp_wait(s.p_full, g & 1u, s, p)) return;
@@ -447,6 +485,12 @@ __device__ __forceinline__ bool pair_exchange(const AttnParams& p, const AttSmem
   theirs = s.xval[buf * 256 + (ln.half ^ 1) * 128 + ln.r];
   ++ln.xc;
   return true;
+}
+
+// Does this thread's row (TMEM lane r) hold a query of unit x: one of the
+// unit's candidates' rows, or for a self unit one of its Q_user rows?
+__device__ __forceinline__ bool row_valid(const Unit& x, int r, int slot, bool row_in_tile) {
+  return x.ok && (x.self ? r < x.cnt : (row_in_tile && slot < x.cnt));
 }
 
 struct RowOut {
@@ -503,7 +547,8 @@ __device__ __forceinline__ bool att_epilogue(const AttnParams& p, const AttSmem&
   return true;
 }
 
-__device__ void att_softmax(const AttnParams& p, const AttSmem& s, uint32_t tmem, int n_units) {
+template <bool kSelf>
+__device__ void att_softmax(const AttnParams& p, const AttSmem& s, uint32_t tmem, const UnitCount& n_units) {
   const int warp = threadIdx.x >> 5;
   Lane ln;
   ln.quarter = warp & 3;                                     // TMEM lane quarter of this warp
@@ -524,18 +569,21 @@ __device__ void att_softmax(const AttnParams& p, const AttSmem& s, uint32_t tmem
   RowOut prev = {false, false, nullptr, 0.f};
 
   int unit = blockIdx.x;
-  Unit x = decode(p, load_work(p, unit, n_units));
-  bool rv = x.ok && row_in_tile && slot < x.cnt;
-  int cand = rv ? __ldg(p.perm + x.start + slot) : 0;
-  while (unit < n_units) {
+  Unit x = decode<kSelf>(p, load_work<kSelf>(p, unit, n_units));
+  bool rv = row_valid(x, ln.r, slot, row_in_tile);
+  int cand = (rv && !x.self) ? __ldg(p.perm + x.start + slot) : 0;
+  while (unit < n_units.total) {
     const int nunit = unit + static_cast<int>(gridDim.x);
-    const int4 nw = load_work(p, nunit, n_units);
+    const int4 nw = load_work<kSelf>(p, nunit, n_units);
     Unit nx;
     bool nrv = false;
     int ncand = 0;
     bool prefetched = false;
     __nv_bfloat16* orow = nullptr;
-    if (rv) orow = reinterpret_cast<__nv_bfloat16*>(p.O) + ((static_cast<size_t>(cand) * p.H + x.h) * p.Lq + qrow) * ATT_D;
+    if (rv)
+      orow = x.self ? reinterpret_cast<__nv_bfloat16*>(p.O_user) +
+                          ((static_cast<size_t>(x.u) * p.H + x.h) * p.Lq_u + x.start + ln.r) * ATT_D
+                    : reinterpret_cast<__nv_bfloat16*>(p.O) + ((static_cast<size_t>(cand) * p.H + x.h) * p.Lq + qrow) * ATT_D;
 
     if (x.ntiles == 0) {  // empty key range: O = 0
       if (rv) {
@@ -646,9 +694,9 @@ __device__ void att_softmax(const AttnParams& p, const AttSmem& s, uint32_t tmem
         mbar_arrive(s.p_full);
         if (!prefetched) {  // the next unit's entry and this row's candidate in it
           prefetched = true;
-          nx = decode(p, nw);
-          nrv = nx.ok && row_in_tile && slot < nx.cnt;
-          ncand = nrv ? __ldg(p.perm + nx.start + slot) : 0;
+          nx = decode<kSelf>(p, nw);
+          nrv = row_valid(nx, ln.r, slot, row_in_tile);
+          ncand = (nrv && !nx.self) ? __ldg(p.perm + nx.start + slot) : 0;
         }
       }
       prev.pending = true;
@@ -657,9 +705,9 @@ __device__ void att_softmax(const AttnParams& p, const AttSmem& s, uint32_t tmem
       prev.l = l;
     }
     if (!prefetched) {
-      nx = decode(p, nw);
-      nrv = nx.ok && row_in_tile && slot < nx.cnt;
-      ncand = nrv ? __ldg(p.perm + nx.start + slot) : 0;
+      nx = decode<kSelf>(p, nw);
+      nrv = row_valid(nx, ln.r, slot, row_in_tile);
+      ncand = (nrv && !nx.self) ? __ldg(p.perm + nx.start + slot) : 0;
     }
     x = nx;
     rv = nrv;
@@ -669,9 +717,13 @@ __device__ void att_softmax(const AttnParams& p, const AttSmem& s, uint32_t tmem
   if (prev.pending) att_epilogue(p, s, Ot, prev, ln, ou);
 }
 
+// kSelf: the launch also runs self units (ikbo_attn_self_target_forward);
+// without them the self branches compile away.
+template <bool kSelf>
 __global__ void __launch_bounds__(ATT_THREADS, 1)
-    attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                    const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmQu,
+                    const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                    const AttnParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t pad = ((raw + 1023u) & ~1023u) - raw;
@@ -681,7 +733,9 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
   }
   const AttSmem s = carve(smem_raw + pad);
   const int warp = threadIdx.x >> 5;
-  const int n_units = *p.n_units;
+  UnitCount n_units;  // work-list units, then self units
+  n_units.target = *p.n_units;
+  n_units.total = n_units.target + (kSelf ? p.n_self : 0);
 
   if (threadIdx.x == 0) {
     mbar_init(s.q_full, 1);
@@ -710,6 +764,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
   }
   if (warp == 0 && lane_id() == 0) {
     tma_prefetch_desc(&tmQ);
+    if (kSelf) tma_prefetch_desc(&tmQu);
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
   }
@@ -723,15 +778,15 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
   const uint32_t tmem = *s.tmem_slot;
 
   if (warp == 0) {
-    if (lane_id() == 0) att_producer_qk(p, s, &tmQ, &tmK, n_units);
+    if (lane_id() == 0) att_producer_qk<kSelf>(p, s, &tmQ, &tmQu, &tmK, n_units);
   } else if (warp == 3) {
-    if (lane_id() == 0) att_producer_v(p, s, &tmV, n_units);
+    if (lane_id() == 0) att_producer_v<kSelf>(p, s, &tmV, n_units);
   } else if (warp == 1) {
-    att_s_issuer(p, s, tmem, n_units);
+    att_s_issuer<kSelf>(p, s, tmem, n_units);
   } else if (warp == 2) {
-    att_pv_issuer(p, s, tmem, n_units);
+    att_pv_issuer<kSelf>(p, s, tmem, n_units);
   } else if (warp >= SOFTMAX_WARP0) {
-    att_softmax(p, s, tmem, n_units);
+    att_softmax<kSelf>(p, s, tmem, n_units);
   }
 
   tc_fence_before();
@@ -747,13 +802,13 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
 
 size_t attn_smem_bytes() { return SMEM_ALLOC; }
 
-cudaError_t launch_attn(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV, const AttnParams& p,
-                        int grid, cudaStream_t s) {
+cudaError_t launch_attn(const CUtensorMap& tmQ, const CUtensorMap& tmQu, const CUtensorMap& tmK,
+                        const CUtensorMap& tmV, const AttnParams& p, int grid, cudaStream_t s) {
   const size_t smem = attn_smem_bytes();
-  cudaError_t e =
-      cudaFuncSetAttribute(attn_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  auto kernel = p.n_self > 0 ? attn_fwd_kernel<true> : attn_fwd_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  attn_fwd_kernel<<<grid, ATT_THREADS, smem, s>>>(tmQ, tmK, tmV, p);
+  kernel<<<grid, ATT_THREADS, smem, s>>>(tmQ, tmQu, tmK, tmV, p);
   return cudaGetLastError();
 }
 

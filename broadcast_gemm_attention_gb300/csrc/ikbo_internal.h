@@ -110,6 +110,10 @@ struct AttnParams {
   int cands_per_tile;        // floor(128 / Lq)
   float scale_log2;          // scale * log2(e)
   uint64_t timeout_ns;
+  // self units (users' own queries against the same K/V), after the work
+  // list's units: n_self = n_users * H * self_tiles, 0 if none
+  uint16_t* O_user;          // [n_users][H][Lq_u][d]
+  int n_self, self_tiles, self_rows, Lq_u;  // self_rows = query rows per self tile (<= 128)
 };
 
 }  // namespace ikbo

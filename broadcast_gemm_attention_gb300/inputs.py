@@ -172,6 +172,13 @@ def make_attn(name: str, seed: int, n_cand: int, n_users: int, H: int, Lq: int, 
     return AttnInputs(name, n_cand, n_users, H, Lq, Lkv_out, d, torch.from_numpy(m), Q, K, V, kv_offsets)
 
 
+def make_user_queries(seed: int, n_users: int, H: int, Lq_u: int, d: int) -> torch.Tensor:
+    """The users' own query set Q_user [n_users, H, Lq_u, d], bf16 N(0, 1), for
+    self + target attention (its own seed, drawn after nothing else)."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    return _normal(rng, (n_users, H, Lq_u, d), 1.0)
+
+
 # --------------------------------------------------------------------------
 # The named workloads.
 # --------------------------------------------------------------------------

@@ -160,6 +160,27 @@ ikbo_status_t ikbo_attn_forward(ikbo_plan_t p, const void* Q, const void* K, con
                                 const int32_t* d_kv_offsets, void* O, int Lkv, int d, float scale,
                                 cudaStream_t stream);
 
+/* Self + target attention in one launch (aixai.ru IKBO blog, section
+ * "Self + Target Attention Fusion"): self-attention and target-attention
+ * read the same per-user K/V and differ only in their queries -- the users'
+ * own query set (self) and their candidates' queries (target) -- so both run
+ * as work units of one launch of the broadcast attention kernel:
+ *   O[i,h]      = softmax(Q[i,h] K[map[i],h]^T * scale) V[map[i],h]   (as ikbo_attn_forward)
+ *   O_user[u,h] = softmax(Q_user[u,h] K[u,h]^T * scale) V[u,h]
+ * The pages give no mask, causality or query length for the self part; it
+ * is read here as the same unmasked attention over the user's whole key
+ * range, with its own query length Lq_u.
+ *   Q_user, O_user bf16 [n_users][H][Lq_u][d], 16-byte aligned; Lq_u >= 8,
+ *   a multiple of 8 (else IKBO_ERR_UNSUPPORTED); users with no keys get
+ *   O_user rows of 0.  Every other argument, limit and error as for
+ *   ikbo_attn_forward (the plan's map, n_users, H and Lq; K/V dense or
+ *   jagged).  The target rows of O are bit-identical to ikbo_attn_forward's.
+ *   The self units (n_users * H * ceil(Lq_u / 128) tiles of up to 128 query
+ *   rows) follow the plan's work list in the persistent launch. */
+ikbo_status_t ikbo_attn_self_target_forward(ikbo_plan_t p, const void* Q, const void* Q_user, const void* K,
+                                            const void* V, const int32_t* d_kv_offsets, void* O, void* O_user,
+                                            int Lq_u, int Lkv, int d, float scale, cudaStream_t stream);
+
 /* Synchronise `stream`, then return (and clear) the first device-detected
  * error recorded since the last call: IKBO_ERR_MAP_OUT_OF_RANGE,
  * IKBO_ERR_TIMEOUT, IKBO_ERR_INTERNAL, or IKBO_OK. */
