@@ -393,6 +393,11 @@ def run_gpu(args):
     if not args.no_ablation:
         ablation = ablation_run(plan, d, x, a, Y, O, flush, stream, dev)
 
+    # ---------------- the pages' LCE stage ladder, rebuilt from our kernel
+    lce_stages = None
+    if not args.no_ablation:
+        lce_stages = lce_stage_run(plan, d, Y, flush, stream)
+
     # ---------------- self + target attention in one launch vs two
     self_target = None
     if not args.no_self_target:
@@ -424,11 +429,36 @@ def run_gpu(args):
                     "attn_us_median": 1e3 * statistics.median(attn_ms)},
         "roofline": roofline, "roofline_lce": roofline_lce,
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": gpu_launches,
-        "clocks": clk.summary(), "ablation": ablation, "self_target": self_target,
+        "clocks": clk.summary(), "ablation": ablation, "lce_stages": lce_stages, "self_target": self_target,
     }
     print(json.dumps(out), flush=True)
     if dist:
         dist.destroy_process_group()
+
+
+def lce_stage_run(plan, d, Y, flush, stream, iters=20):
+    """ikbo_lce_forward_staged at stages 1 (decomposed: user GEMM, candidate
+    GEMM, separate broadcast add), 3 (fused epilogue, one accumulator) and 4
+    (the full kernel), median µs over `iters` flushed runs each."""
+    import statistics
+    import torch
+    res = {}
+    for st in (1, 3, 4):
+        ts = []
+        for k in range(iters + 2):
+            flush()
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record(stream)
+            plan.lce_forward_staged(d["U"], d["C"], d["Wu"], d["Wc"], d["b"], Y, st, stream)
+            e.record(stream)
+            torch.cuda.synchronize()
+            if k >= 2:
+                ts.append(s.elapsed_time(e))
+        res[f"stage{st}_us"] = 1e3 * statistics.median(ts)
+    res["note"] = ("stage 1: 3 launches, Y written then read back for the add; stage 3: add fused, one "
+                   "accumulator; stage 4: = ikbo_lce_forward. The pages' stage 2 (pad K) is TMA's zero fill "
+                   "in every stage")
+    return res
 
 
 def self_target_run(plan, d, x, a, O, flush, stream, dev, Lq_u=64, iters=20):
@@ -458,16 +488,18 @@ def self_target_run(plan, d, x, a, O, flush, stream, dev, Lq_u=64, iters=20):
             torch.cuda.synchronize()
             if k >= 2:
                 ts.append(s.elapsed_time(e))
-        return 1e3 * statistics.median(ts)
+        return 1e3 * statistics.median(ts), 1e3 * statistics.mean(ts)
 
-    fused = timed(lambda: plan.attn_self_target_forward(d["Q"], Qu, d["K"], d["V"], None, O, Ou, None, stream))
-    sep = timed(lambda: (plan.attn_forward(d["Q"], d["K"], d["V"], None, O, None, stream),
-                         plan_u.attn_forward(Qu, d["K"], d["V"], None, Ou2, None, stream)))
+    fused, fused_mean = timed(lambda: plan.attn_self_target_forward(d["Q"], Qu, d["K"], d["V"], None, O, Ou, None,
+                                                                    stream))
+    sep, sep_mean = timed(lambda: (plan.attn_forward(d["Q"], d["K"], d["V"], None, O, None, stream),
+                                   plan_u.attn_forward(Qu, d["K"], d["V"], None, Ou2, None, stream)))
     st = plan.status()
     same = bool(torch.equal(Ou, Ou2))
     plan_u.close()
     flops = 4.0 * a.H * a.d * a.Lkv * (x.n_cand * a.Lq + x.n_users * Lq_u)
-    return {"Lq_u": Lq_u, "fused_us": fused, "separate_us": sep, "fused_tflops": flops / (fused * 1e-6) / 1e12,
+    return {"Lq_u": Lq_u, "fused_us": fused, "separate_us": sep, "fused_mean_us": fused_mean,
+            "separate_mean_us": sep_mean, "fused_tflops": flops / (fused * 1e-6) / 1e12,
             "launches": {"fused": 1, "separate": 2}, "self_rows_identical": same,
             "status": "ok" if st == B.IKBO_OK else B.ikbo_status_string(st)}
 

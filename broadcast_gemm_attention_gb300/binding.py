@@ -40,6 +40,7 @@ SIGNATURES = {
     "ikbo_plan_worklist": (_i, [_vp, ctypes.POINTER(_vp), ctypes.POINTER(_vp), ctypes.POINTER(_i),
                                 ctypes.POINTER(_i)]),
     "ikbo_lce_forward": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp]),
+    "ikbo_lce_forward_staged": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp]),
     "ikbo_lce_forward_noalloc": (_i, [_vp, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp]),
     "ikbo_attn_forward": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, ctypes.c_float, _vp]),
     "ikbo_attn_self_target_forward": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, ctypes.c_float, _vp]),
@@ -158,6 +159,22 @@ def ikbo_lce_forward(plan: int, U: torch.Tensor, C: torch.Tensor, Wu: torch.Tens
                                    bptr, _dev(Y, bf, "Y"), K_u, K_c, D, N, _stream(stream)), "ikbo_lce_forward")
 
 
+def ikbo_lce_forward_staged(plan: int, U: torch.Tensor, C: torch.Tensor, Wu: torch.Tensor, Wc: torch.Tensor,
+                            b: Optional[torch.Tensor], Y: torch.Tensor, stage: int, stream=None) -> None:
+    """The LCE as stage 1 (decomposed, unfused), 3 (fused epilogue, one
+    accumulator) or 4 (the full kernel) of the pages' stage ladder."""
+    bf = torch.bfloat16
+    n_users, K_u, D = U.shape
+    n_cand, K_c, D2 = C.shape
+    N = Wu.shape[1]
+    if D2 != D or tuple(Wu.shape) != (K_u, N) or tuple(Wc.shape) != (K_c, N) or tuple(Y.shape) != (n_cand, N, D):
+        raise ValueError("inconsistent LCE shapes")
+    bptr = None if b is None else _dev(b, bf, "b")
+    _check(load().ikbo_lce_forward_staged(plan, _dev(U, bf, "U"), _dev(C, bf, "C"), _dev(Wu, bf, "Wu"),
+                                          _dev(Wc, bf, "Wc"), bptr, _dev(Y, bf, "Y"), K_u, K_c, D, N, int(stage),
+                                          _stream(stream)), "ikbo_lce_forward_staged")
+
+
 def ikbo_lce_forward_noalloc(map_: torch.Tensor, n_users: int, U: torch.Tensor, C: torch.Tensor,
                              Wu: torch.Tensor, Wc: torch.Tensor, b: Optional[torch.Tensor], Y: torch.Tensor,
                              stream=None) -> None:
@@ -272,6 +289,9 @@ class Plan:
 
     def lce_forward(self, U, C, Wu, Wc, b, Y, stream=None):
         ikbo_lce_forward(self.handle, U, C, Wu, Wc, b, Y, stream)
+
+    def lce_forward_staged(self, U, C, Wu, Wc, b, Y, stage, stream=None):
+        ikbo_lce_forward_staged(self.handle, U, C, Wu, Wc, b, Y, stage, stream)
 
     def attn_forward(self, Q, K, V, kv_offsets, O, scale=None, stream=None):
         ikbo_attn_forward(self.handle, Q, K, V, kv_offsets, O, scale, stream)

@@ -19,6 +19,9 @@ cudaError_t launch_seg_build(const SegParams& p, cudaStream_t s);
 size_t lce_smem_bytes(const LceParams& p);
 cudaError_t launch_lce(const CUtensorMap& tmU, const CUtensorMap& tmC, const CUtensorMap& tmWu,
                        const CUtensorMap& tmWc, const LceParams& p, int num_sms, cudaStream_t s);
+cudaError_t launch_lce_stage(const CUtensorMap& tmU, const CUtensorMap& tmC, const CUtensorMap& tmWu,
+                             const CUtensorMap& tmWc, LceParams p, int stage, int num_sms, cudaStream_t s,
+                             int* launches);
 size_t attn_smem_bytes();
 cudaError_t launch_attn(const CUtensorMap& tmQ, const CUtensorMap& tmQu, const CUtensorMap& tmK,
                         const CUtensorMap& tmV, const AttnParams& p, int grid, cudaStream_t s);
@@ -124,6 +127,66 @@ void free_plan(ikbo_plan_t p) {
 }  // namespace
 
 namespace {
+// Both LCE entry points: stage 4 is the full kernel, 1 and 3 the ablations.
+ikbo_status_t lce_launch(ikbo_plan_t p, const void* U, const void* C, const void* Wu, const void* Wc, const void* b,
+                         void* Y, int K_u, int K_c, int D, int N, int stage, cudaStream_t stream) {
+  if (!p) return IKBO_ERR_INVALID_ARG;
+  if (!p->planned) return IKBO_ERR_NOT_PLANNED;
+  if (!U || !C || !Wu || !Wc || !Y) return IKBO_ERR_INVALID_ARG;
+  if (K_u < 1 || K_c < 1 || D < 1 || N < 1) return IKBO_ERR_UNSUPPORTED;
+  if (!aligned16(U) || !aligned16(C) || !aligned16(Wu) || !aligned16(Wc) || !aligned16(Y) || (b && !aligned16(b)))
+    return IKBO_ERR_INVALID_ARG;
+  if (D % 8 != 0 || N % 8 != 0 || N > 256) return IKBO_ERR_UNSUPPORTED;
+
+  LceParams lp;
+  std::memset(&lp, 0, sizeof(lp));
+  lp.n_cand = p->n_cand;
+  lp.n_users = p->n_users;
+  lp.K_u = K_u;
+  lp.K_c = K_c;
+  lp.D = D;
+  lp.N = N;
+  if (!lce_configure(&lp, p->max_smem)) return IKBO_ERR_UNSUPPORTED;
+  lp.map = p->d_map;
+  lp.order = p->d_perm;  // candidates grouped by user: consecutive tiles of a CTA share the user partial
+  lp.bias = static_cast<const uint16_t*>(b);
+  lp.Y = static_cast<uint16_t*>(Y);
+
+  const size_t part = static_cast<size_t>(p->n_users) * N * D;
+  const size_t nflags = lce_flag_count(lp);
+  if (grow(&p->d_partial, &p->partial_elems, part) != cudaSuccess) return IKBO_ERR_CUDA;
+  if (grow(&p->d_flags, &p->flags_elems, nflags) != cudaSuccess) return IKBO_ERR_CUDA;
+  lp.partial = p->d_partial;
+  lp.flags = p->d_flags;
+  lp.status = p->d_status;
+  lp.timeout_epoch = p->d_status + 1;
+  lp.epoch = ++p->epoch;
+  if (lp.epoch == 0) lp.epoch = ++p->epoch;  // 0 is the flags' initial value
+  lp.debug = p->debug;
+  lp.timeout_ns = p->timeout_ns;
+
+  CUtensorMap tmU, tmC, tmWu, tmWc;
+  const uint64_t ud[3] = {static_cast<uint64_t>(D), static_cast<uint64_t>(K_u), static_cast<uint64_t>(p->n_users)};
+  const uint64_t us[2] = {static_cast<uint64_t>(D) * 2, static_cast<uint64_t>(K_u) * D * 2};
+  const uint64_t cd[3] = {static_cast<uint64_t>(D), static_cast<uint64_t>(K_c), static_cast<uint64_t>(p->n_cand)};
+  const uint64_t cs[2] = {static_cast<uint64_t>(D) * 2, static_cast<uint64_t>(K_c) * D * 2};
+  const uint32_t abox[3] = {64, LCE_BK, 1};
+  const uint64_t wud[2] = {static_cast<uint64_t>(N), static_cast<uint64_t>(K_u)};
+  const uint64_t wcd[2] = {static_cast<uint64_t>(N), static_cast<uint64_t>(K_c)};
+  const uint64_t ws[1] = {static_cast<uint64_t>(N) * 2};
+  const uint32_t wbox[2] = {64, LCE_BK};
+  if (!encode_bf16(&tmU, U, 3, ud, us, abox) || !encode_bf16(&tmC, C, 3, cd, cs, abox) ||
+      !encode_bf16(&tmWu, Wu, 2, wud, ws, wbox) || !encode_bf16(&tmWc, Wc, 2, wcd, ws, wbox))
+    return IKBO_ERR_CUDA;
+
+  int launches = 0;
+  const cudaError_t e = launch_lce_stage(tmU, tmC, tmWu, tmWc, lp, stage, p->num_sms, stream, &launches);
+  p->launches += static_cast<uint64_t>(launches);
+  return e == cudaSuccess ? IKBO_OK : IKBO_ERR_CUDA;
+}
+}  // namespace
+
+namespace {
 // Both attention entry points: the work list's (target) units, plus, when
 // Q_user is given, n_users * H * ceil(Lq_u / 128) self units in the same launch.
 ikbo_status_t attn_launch(ikbo_plan_t p, const void* Q, const void* Q_user, const void* K, const void* V,
@@ -199,7 +262,7 @@ ikbo_status_t attn_launch(ikbo_plan_t p, const void* Q, const void* Q_user, cons
 
 extern "C" {
 
-int ikbo_version(void) { return 101; }
+int ikbo_version(void) { return 102; }
 
 const char* ikbo_status_string(ikbo_status_t s) {
   switch (s) {
@@ -349,58 +412,14 @@ ikbo_status_t ikbo_plan_get_status(ikbo_plan_t p, cudaStream_t stream) {
 
 ikbo_status_t ikbo_lce_forward(ikbo_plan_t p, const void* U, const void* C, const void* Wu, const void* Wc,
                                const void* b, void* Y, int K_u, int K_c, int D, int N, cudaStream_t stream) {
-  if (!p) return IKBO_ERR_INVALID_ARG;
-  if (!p->planned) return IKBO_ERR_NOT_PLANNED;
-  if (!U || !C || !Wu || !Wc || !Y) return IKBO_ERR_INVALID_ARG;
-  if (K_u < 1 || K_c < 1 || D < 1 || N < 1) return IKBO_ERR_UNSUPPORTED;
-  if (!aligned16(U) || !aligned16(C) || !aligned16(Wu) || !aligned16(Wc) || !aligned16(Y) || (b && !aligned16(b)))
-    return IKBO_ERR_INVALID_ARG;
-  if (D % 8 != 0 || N % 8 != 0 || N > 256) return IKBO_ERR_UNSUPPORTED;
+  return lce_launch(p, U, C, Wu, Wc, b, Y, K_u, K_c, D, N, 4, stream);
+}
 
-  LceParams lp;
-  std::memset(&lp, 0, sizeof(lp));
-  lp.n_cand = p->n_cand;
-  lp.n_users = p->n_users;
-  lp.K_u = K_u;
-  lp.K_c = K_c;
-  lp.D = D;
-  lp.N = N;
-  if (!lce_configure(&lp, p->max_smem)) return IKBO_ERR_UNSUPPORTED;
-  lp.map = p->d_map;
-  lp.order = p->d_perm;  // candidates grouped by user: consecutive tiles of a CTA share the user partial
-  lp.bias = static_cast<const uint16_t*>(b);
-  lp.Y = static_cast<uint16_t*>(Y);
-
-  const size_t part = static_cast<size_t>(p->n_users) * N * D;
-  const size_t nflags = lce_flag_count(lp);
-  if (grow(&p->d_partial, &p->partial_elems, part) != cudaSuccess) return IKBO_ERR_CUDA;
-  if (grow(&p->d_flags, &p->flags_elems, nflags) != cudaSuccess) return IKBO_ERR_CUDA;
-  lp.partial = p->d_partial;
-  lp.flags = p->d_flags;
-  lp.status = p->d_status;
-  lp.timeout_epoch = p->d_status + 1;
-  lp.epoch = ++p->epoch;
-  if (lp.epoch == 0) lp.epoch = ++p->epoch;  // 0 is the flags' initial value
-  lp.debug = p->debug;
-  lp.timeout_ns = p->timeout_ns;
-
-  CUtensorMap tmU, tmC, tmWu, tmWc;
-  const uint64_t ud[3] = {static_cast<uint64_t>(D), static_cast<uint64_t>(K_u), static_cast<uint64_t>(p->n_users)};
-  const uint64_t us[2] = {static_cast<uint64_t>(D) * 2, static_cast<uint64_t>(K_u) * D * 2};
-  const uint64_t cd[3] = {static_cast<uint64_t>(D), static_cast<uint64_t>(K_c), static_cast<uint64_t>(p->n_cand)};
-  const uint64_t cs[2] = {static_cast<uint64_t>(D) * 2, static_cast<uint64_t>(K_c) * D * 2};
-  const uint32_t abox[3] = {64, LCE_BK, 1};
-  const uint64_t wud[2] = {static_cast<uint64_t>(N), static_cast<uint64_t>(K_u)};
-  const uint64_t wcd[2] = {static_cast<uint64_t>(N), static_cast<uint64_t>(K_c)};
-  const uint64_t ws[1] = {static_cast<uint64_t>(N) * 2};
-  const uint32_t wbox[2] = {64, LCE_BK};
-  if (!encode_bf16(&tmU, U, 3, ud, us, abox) || !encode_bf16(&tmC, C, 3, cd, cs, abox) ||
-      !encode_bf16(&tmWu, Wu, 2, wud, ws, wbox) || !encode_bf16(&tmWc, Wc, 2, wcd, ws, wbox))
-    return IKBO_ERR_CUDA;
-
-  if (launch_lce(tmU, tmC, tmWu, tmWc, lp, p->num_sms, stream) != cudaSuccess) return IKBO_ERR_CUDA;
-  p->launches += 2;  // user tiles, then candidate tiles
-  return IKBO_OK;
+ikbo_status_t ikbo_lce_forward_staged(ikbo_plan_t p, const void* U, const void* C, const void* Wu, const void* Wc,
+                                      const void* b, void* Y, int K_u, int K_c, int D, int N, int stage,
+                                      cudaStream_t stream) {
+  if (stage != 1 && stage != 3 && stage != 4) return IKBO_ERR_INVALID_ARG;
+  return lce_launch(p, U, C, Wu, Wc, b, Y, K_u, K_c, D, N, stage, stream);
 }
 
 

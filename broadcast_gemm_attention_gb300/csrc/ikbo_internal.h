@@ -75,7 +75,19 @@ struct LceParams {
   uint32_t w_region_bytes;
   uint32_t epoch;         // value written to / awaited in `flags`
   uint32_t debug;
+  uint32_t mode;          // LCE_MODE_* bits: the stage-ladder ablations (0 = the full kernel)
   uint64_t timeout_ns;
+};
+
+// Ablation modes of the LCE kernel (the pages' stage ladder, rebuilt from
+// this kernel): NO_PARTIAL = candidate tiles store bf16(C W_c) without the
+// user partial (a separate broadcast-add launch adds it: the decomposed,
+// unfused stage); ONE_ACC = a single TMEM accumulator, so a tile's epilogue
+// and the next tile's products no longer overlap (fused epilogue without
+// the warp-specialised pipelining across tiles).
+enum : uint32_t {
+  LCE_MODE_NO_PARTIAL = 1u << 0,
+  LCE_MODE_ONE_ACC = 1u << 1,
 };
 
 // Fills the derived fields of an LceParams from its sizes (n_cand, n_users,

@@ -205,8 +205,9 @@ __device__ void lce_mma(const LceParams& p, const LceSmem& s, uint32_t tmem, int
     const UnitInfo x = unit_info(p, unit);
     const int kc_n = x.is_user ? p.kc_u : p.kc_c;
     int ks_left = x.is_user ? p.ks_u : p.ks_c;
-    const int buf = local & 1;
-    const uint32_t use = static_cast<uint32_t>(local >> 1);
+    const bool one_acc = p.mode & LCE_MODE_ONE_ACC;
+    const int buf = one_acc ? 0 : (local & 1);
+    const uint32_t use = static_cast<uint32_t>(one_acc ? local : (local >> 1));
     if (!warp_wait(&s.acc_empty[buf], (use & 1u) ^ 1u, s, p)) return;
     if (!x.is_user && !wc_ready) {
       if (!warp_wait(s.wc_full, 0, s, p)) return;
@@ -314,8 +315,9 @@ __device__ void lce_epilogue(const LceParams& p, const LceSmem& s, uint32_t tmem
     const int unit = cta_unit(p, u0, u1, t);
     if (unit < 0) break;
     const UnitInfo x = unit_info(p, unit);
-    const int buf = local & 1;
-    const uint32_t use = static_cast<uint32_t>(local >> 1);
+    const bool one_acc = p.mode & LCE_MODE_ONE_ACC;
+    const int buf = one_acc ? 0 : (local & 1);
+    const uint32_t use = static_cast<uint32_t>(one_acc ? local : (local >> 1));
     const int d = x.dblk * LCE_BM + et;
     const bool dok = d < p.D;
     const size_t ND = static_cast<size_t>(p.N) * p.D;
@@ -362,13 +364,21 @@ __device__ void lce_epilogue(const LceParams& p, const LceSmem& s, uint32_t tmem
       ++pubs;
     } else {
       const int i = x.row;
-      const int u = p.map[i];
+      const bool add_p = !(p.mode & LCE_MODE_NO_PARTIAL);
+      const int u = add_p ? p.map[i] : 0;
       const bool uok = u >= 0 && u < p.n_users;
       if (!uok && leader) atomicOr(p.status, DEV_ERR_MAP_RANGE);
-      if (users_ready < 0) users_ready = wait_all_user_partials(p) ? 1 : 0;
-      const bool ready = uok && users_ready == 1;
+      if (add_p && users_ready < 0) users_ready = wait_all_user_partials(p) ? 1 : 0;
+      const bool ready = uok && (!add_p || users_ready == 1);
       const float* P = p.partial + static_cast<size_t>(uok ? u : 0) * ND + d;
-      if (ready && (u != pre_u || x.dblk != pre_dblk)) {
+      if (!add_p && pre_u != -2) {  // decomposed stage: no partial here (a later launch adds it)
+        pre_u = -2;
+#pragma unroll
+        for (int k = 0; k < EPI_PREFETCH; ++k)
+#pragma unroll
+          for (int j = 0; j < 32; ++j) pre[k][j] = 0.f;
+      }
+      if (add_p && ready && (u != pre_u || x.dblk != pre_dblk)) {
         pre_u = u;
         pre_dblk = x.dblk;
 #pragma unroll
@@ -406,7 +416,8 @@ __device__ void lce_epilogue(const LceParams& p, const LceSmem& s, uint32_t tmem
           float pu[32];
           const float* pp = P + static_cast<size_t>(c * 32) * p.D;
 #pragma unroll
-          for (int j = 0; j < 32; ++j) pu[j] = (c * 32 + j < p.N && dok) ? __ldcg(pp + static_cast<size_t>(j) * p.D) : 0.f;
+          for (int j = 0; j < 32; ++j)
+            pu[j] = (add_p && c * 32 + j < p.N && dok) ? __ldcg(pp + static_cast<size_t>(j) * p.D) : 0.f;
           tmem_ld_wait(v);
           __nv_bfloat16* y = Y + static_cast<size_t>(c * 32) * p.D;
 #pragma unroll
@@ -550,6 +561,63 @@ cudaError_t launch_lce(const CUtensorMap& tmU, const CUtensorMap& tmC, const CUt
   cudaError_t e = launch_phase<true>(tmU, tmC, tmWu, tmWc, p, p.n_user_units, num_sms, s);
   if (e != cudaSuccess) return e;
   return launch_phase<false>(tmU, tmC, tmWu, tmWc, p, p.n_units - p.n_user_units, num_sms, s);
+}
+
+namespace {
+// The decomposed stage's separate broadcast add: Y[i] = bf16(Y[i] + P[map[i]]),
+// 8 elements (16 bytes of Y, 32 of P) per thread and step; D % 8 == 0.
+__global__ void __launch_bounds__(256) lce_broadcast_add_kernel(const int32_t* map, const float* P, uint16_t* Y,
+                                                               int n_cand, int n_users, int N, int D,
+                                                               uint32_t* status) {
+  const size_t nd8 = static_cast<size_t>(N) * D / 8;
+  const size_t total = static_cast<size_t>(n_cand) * nd8;
+  for (size_t t = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; t < total;
+       t += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const int i = static_cast<int>(t / nd8);
+    const size_t e = t - static_cast<size_t>(i) * nd8;
+    const int u = __ldg(map + i);
+    if (u < 0 || u >= n_users) {
+      if (e == 0) atomicOr(status, DEV_ERR_MAP_RANGE);
+      continue;
+    }
+    uint4* yp = reinterpret_cast<uint4*>(Y) + t;
+    const float4* pp = reinterpret_cast<const float4*>(P + (static_cast<size_t>(u) * nd8 + e) * 8);
+    const uint4 y = *yp;
+    const float4 a = __ldg(pp), b = __ldg(pp + 1);
+    uint4 o;
+    o.x = pack_bf16x2(__uint_as_float(y.x << 16) + a.x, __uint_as_float(y.x & 0xffff0000u) + a.y);
+    o.y = pack_bf16x2(__uint_as_float(y.y << 16) + a.z, __uint_as_float(y.y & 0xffff0000u) + a.w);
+    o.z = pack_bf16x2(__uint_as_float(y.z << 16) + b.x, __uint_as_float(y.z & 0xffff0000u) + b.y);
+    o.w = pack_bf16x2(__uint_as_float(y.w << 16) + b.z, __uint_as_float(y.w & 0xffff0000u) + b.w);
+    *yp = o;
+  }
+}
+}  // namespace
+
+// The pages' LCE stage ladder rebuilt from this kernel (see LCE_MODE_*):
+// stage 1 decomposed and unfused (user tiles; candidate tiles without the
+// partial; broadcast-add launch), stage 3 fused epilogue with one
+// accumulator, stage 4 the full kernel.  Returns the number of launches in
+// *launches.
+cudaError_t launch_lce_stage(const CUtensorMap& tmU, const CUtensorMap& tmC, const CUtensorMap& tmWu,
+                             const CUtensorMap& tmWc, LceParams p, int stage, int num_sms, cudaStream_t s,
+                             int* launches) {
+  *launches = 0;
+  if (stage == 4) {
+    *launches = 2;
+    return launch_lce(tmU, tmC, tmWu, tmWc, p, num_sms, s);
+  }
+  p.mode = stage == 1 ? LCE_MODE_NO_PARTIAL : LCE_MODE_ONE_ACC;
+  cudaError_t e = launch_lce(tmU, tmC, tmWu, tmWc, p, num_sms, s);
+  if (e != cudaSuccess) return e;
+  *launches = 2;
+  if (stage == 1) {
+    lce_broadcast_add_kernel<<<num_sms * 4, 256, 0, s>>>(p.map, p.partial, p.Y, p.n_cand, p.n_users, p.N, p.D,
+                                                          p.status);
+    e = cudaGetLastError();
+    if (e == cudaSuccess) *launches = 3;
+  }
+  return e;
 }
 
 }  // namespace ikbo

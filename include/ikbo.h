@@ -142,6 +142,25 @@ ikbo_status_t ikbo_lce_forward_noalloc(const int32_t* d_map, int n_cand, int n_u
                                        const void* Wu, const void* Wc, const void* b, void* Y, int K_u, int K_c,
                                        int D, int N, cudaStream_t stream);
 
+/* The pages' LCE stage ladder as ablations of this kernel (aixai.ru IKBO
+ * blog, "Deep Dive: Linear Compression": decompose, pad K, fuse the
+ * broadcast add into the epilogue, warp-specialised persistent fusion; the
+ * aibriefing LCE deep dive's per-stage latencies).  Same arguments, result
+ * and errors as ikbo_lce_forward; `stage`:
+ *   1  decomposed and unfused: user tiles -> fp32 partial; candidate tiles
+ *      store bf16(C[i] W_c) without it; a separate broadcast-add launch adds
+ *      P[map[i]] (Y rounded twice; within the LCE tolerance)
+ *   3  broadcast add fused into the candidate epilogue, one TMEM
+ *      accumulator (a tile's epilogue and the next tile's products do not
+ *      overlap)
+ *   4  the full kernel (= ikbo_lce_forward)
+ * The pages' stage 2 (pad K) has no separate variant here: TMA's
+ * out-of-bounds zero fill pads K in every stage.  Other values:
+ * IKBO_ERR_INVALID_ARG. */
+ikbo_status_t ikbo_lce_forward_staged(ikbo_plan_t p, const void* U, const void* C, const void* Wu, const void* Wc,
+                                      const void* b, void* Y, int K_u, int K_c, int D, int N, int stage,
+                                      cudaStream_t stream);
+
 /* Broadcast attention (aixai.ru, "Deep Dive: Flash Attention"; aibriefing,
  * Flash Attention case): for every candidate i and head h, with u = map[i],
  *   O[i,h,q,:] = sum_j softmax_j(scale * Q[i,h,q,:].K[u,h,j,:]) V[u,h,j,:]

@@ -1,0 +1,72 @@
+"""The pages' LCE stage ladder (ikbo_lce_forward_staged) against the fp64
+oracle: stage 1 (decomposed, unfused: separate broadcast-add launch),
+stage 3 (fused epilogue, one accumulator), stage 4 (the full kernel).
+
+Tolerance: |Y_gpu - Y_ref| <= 1e-2 (1 + |Y_ref|) element-wise.  Stages 3
+and 4 do the same arithmetic in another schedule, so they agree bit for bit.
+"""
+import pytest
+import torch
+
+import oracle
+from broadcast_gemm_attention_gb300 import binding as B
+from broadcast_gemm_attention_gb300 import inputs as gen
+from gpu_util import assert_lce_close, sample_candidates, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def run_stages(x, stages=(1, 3, 4)):
+    U, C, Wu, Wc, b, m = to_dev(x.U, x.C, x.Wu, x.Wc, x.b, x.map)
+    out, launches = {}, {}
+    with B.Plan(x.n_cand, x.n_users, 1) as p:
+        p.plan(m, x.n_users)
+        for st in stages:
+            Y = torch.full((x.n_cand, x.N, x.D), float("nan"), dtype=torch.bfloat16, device="cuda")
+            l0 = p.launches()
+            p.lce_forward_staged(U, C, Wu, Wc, b, Y, st)
+            launches[st] = p.launches() - l0
+            assert p.status() == B.IKBO_OK
+            out[st] = Y
+    return out, launches
+
+
+@pytest.mark.parametrize("shape", [
+    dict(n_cand=16, n_users=2, K_u=24, K_c=16, D=32, N=8),
+    dict(n_cand=37, n_users=3, K_u=37, K_c=29, D=136, N=40),
+    dict(n_cand=300, n_users=7, K_u=381, K_c=243, D=384, N=200),
+])
+def test_lce_stages_full(shape):
+    x = gen.make_lce("stages", 81, map_kind="permuted", **shape)
+    out, launches = run_stages(x)
+    assert launches == {1: 3, 3: 2, 4: 2}
+    ref = oracle.lce(x.map, x.U, x.C, x.Wu, x.Wc, x.b)
+    for st, Y in out.items():
+        assert_lce_close(Y, ref, f"stage {st}")
+    assert torch.equal(out[3], out[4])
+
+
+def test_lce_stages_70to1_sampled():
+    x = gen.lce_70to1()
+    out, _ = run_stages(x)
+    sel = sample_candidates(x.map, 24)
+    ref = oracle.lce(x.map, x.U, x.C, x.Wu, x.Wc, x.b, cands=sel)
+    for st, Y in out.items():
+        assert_lce_close(Y[sel], ref, f"70:1 stage {st}")
+    assert torch.equal(out[3], out[4])
+
+
+def test_lce_stage_argument_and_map_errors():
+    x = gen.make_lce("stage_err", 82, 12, 3, 16, 16, 32, 16)
+    U, C, Wu, Wc, b = to_dev(x.U, x.C, x.Wu, x.Wc, x.b)
+    Y = torch.empty((x.n_cand, x.N, x.D), dtype=torch.bfloat16, device="cuda")
+    bad = x.map.clone()
+    bad[5] = 7
+    with B.Plan(x.n_cand, x.n_users, 1) as p:
+        p.plan(bad.cuda(), x.n_users)
+        for st in (0, 2, 5):
+            with pytest.raises(B.IkboError) as e:
+                p.lce_forward_staged(U, C, Wu, Wc, b, Y, st)
+            assert e.value.code == B.IKBO_ERR_INVALID_ARG
+        p.lce_forward_staged(U, C, Wu, Wc, b, Y, 1)
+        assert p.status() == B.IKBO_ERR_MAP_OUT_OF_RANGE
