@@ -436,6 +436,74 @@ def run_gpu(args):
         dist.destroy_process_group()
 
 
+def run_sweep(args):
+    """Shape sweep (not the headline metric): the LCE over n_cand in
+    {256, 1024, 4096} x ratio in {10, 70, 1000, 10000} and the attention ratio
+    sweep (4096 candidates, Lq 16, Lkv 2048), each timed (median of flushed
+    runs) and set against its own roofline.  One JSON line per point."""
+    import statistics
+    import torch
+    import __graft_entry__ as ge
+    from broadcast_gemm_attention_gb300 import accounting as acc
+    from broadcast_gemm_attention_gb300 import binding as B
+    from broadcast_gemm_attention_gb300 import inputs as gen
+    ge.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    flush = L2Flush(dev)
+    pk = peaks()
+
+    def timed(fn, iters=20):
+        ts = []
+        for k in range(iters + 3):
+            flush()
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record(stream)
+            fn()
+            e.record(stream)
+            torch.cuda.synchronize()
+            if k >= 3:
+                ts.append(s.elapsed_time(e))
+        return 1e3 * statistics.median(ts)
+
+    for n, r, seed in gen.lce_sweep_points():
+        x = gen.lce_sweep(n, r, seed)
+        U, C, Wu, Wc, b, m = [t.to(dev) for t in (x.U, x.C, x.Wu, x.Wc, x.b, x.map)]
+        Y = torch.empty(x.n_cand, x.N, x.D, dtype=torch.bfloat16, device=dev)
+        sched = {}
+        with B.Plan(x.n_cand, x.n_users, 1) as p:
+            p.plan(m, x.n_users, 1, 8, stream)
+            for name, code in (("two_launches", 1), ("one_launch", 2), ("auto", 0)):
+                p.set_lce_schedule(code)
+                sched[name] = timed(lambda: p.lce_forward(U, C, Wu, Wc, b, Y, stream))
+            us = sched["auto"]
+            st = p.status()
+        byt = acc.lce_bytes(x.n_cand, x.n_users, x.K_u, x.K_c, x.D, x.N)
+        fl = acc.lce_flops(x.n_cand, x.n_users, x.K_u, x.K_c, x.D, x.N)
+        t_roof = max(byt / (pk["hbm_gbs"] * 1e9), fl / (pk["bf16_tflops"] * 1e12))
+        print(json.dumps({"sweep": "lce", "n_cand": n, "ratio": r, "n_users": x.n_users, "us": us, "schedules_us": sched,
+                          "roofline_us": t_roof * 1e6, "frac": t_roof * 1e6 / us, "gbs": byt / (us * 1e-6) / 1e9,
+                          "status": B.ikbo_status_string(st)}), flush=True)
+        del U, C, Wu, Wc, b, m, Y
+    for n, r, seed in gen.attn_ratio_sweep_points():
+        x = gen.attn_ratio_sweep(n, r, seed)
+        Q, K, V, m = [t.to(dev) for t in (x.Q, x.K, x.V, x.map)]
+        O = torch.empty_like(Q)
+        with B.Plan(x.n_cand, x.n_users, x.H) as p:
+            p.plan(m, x.n_users, x.H, x.Lq, stream)
+            us = timed(lambda: p.attn_forward(Q, K, V, None, O, None, stream))
+            st = p.status()
+        fl = acc.attn_flops(x.H, x.Lq, x.d, [x.Lkv] * x.n_cand)
+        byt = acc.attn_bytes(x.n_cand, x.H, x.Lq, x.d, x.n_users * x.Lkv)
+        t_roof = max(byt / (pk["hbm_gbs"] * 1e9), fl / (pk["bf16_tflops"] * 1e12))
+        print(json.dumps({"sweep": "attn", "n_cand": n, "ratio": r, "n_users": x.n_users, "us": us,
+                          "roofline_us": t_roof * 1e6, "frac": t_roof * 1e6 / us, "tflops": fl / (us * 1e-6) / 1e12,
+                          "bound": "hbm" if byt / (pk["hbm_gbs"] * 1e9) > fl / (pk["bf16_tflops"] * 1e12) else "tensor",
+                          "status": B.ikbo_status_string(st)}), flush=True)
+        del Q, K, V, m, O
+
+
 def lce_stage_run(plan, d, Y, flush, stream, iters=20):
     """ikbo_lce_forward_staged at stages 1 (decomposed: user GEMM, candidate
     GEMM, separate broadcast add), 3 (fused epilogue, one accumulator) and 4
@@ -557,13 +625,16 @@ def main():
     ap.add_argument("--impl", choices=["ikbo", "reference"], default="ikbo")
     ap.add_argument("--no-ablation", action="store_true")
     ap.add_argument("--no-self-target", action="store_true", help="skip the self + target attention comparison")
+    ap.add_argument("--sweep", action="store_true", help="shape sweep (LCE and attention) instead of the benchmark")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target length of the CPU-oracle baseline (0 skips it, e.g. under a profiler)")
     ap.add_argument("--ref-budget", type=float, default=120.0, help="reference arm: total seconds of oracle work")
     args = ap.parse_args()
-    if args.impl == "reference":
+    if args.sweep:
+        run_sweep(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_gpu(args)

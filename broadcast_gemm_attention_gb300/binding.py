@@ -47,6 +47,7 @@ SIGNATURES = {
     "ikbo_plan_get_status": (_i, [_vp, _vp]),
     "ikbo_plan_set_debug": (_i, [_vp, ctypes.c_uint]),
     "ikbo_plan_set_timeout_ns": (_i, [_vp, _u64]),
+    "ikbo_plan_set_lce_schedule": (_i, [_vp, _i]),
     "ikbo_plan_launch_count": (_u64, [_vp]),
     "ikbo_status_string": (ctypes.c_char_p, [_i]),
     "ikbo_plan_destroy": (None, [_vp]),
@@ -252,6 +253,11 @@ def ikbo_plan_set_debug(plan: int, flags: int) -> None:
     _check(load().ikbo_plan_set_debug(plan, flags), "ikbo_plan_set_debug")
 
 
+def ikbo_plan_set_lce_schedule(plan: int, schedule: int) -> None:
+    """0 = chosen from the shape, 1 = two launches, 2 = one launch."""
+    _check(load().ikbo_plan_set_lce_schedule(plan, int(schedule)), "ikbo_plan_set_lce_schedule")
+
+
 def ikbo_plan_set_timeout_ns(plan: int, ns: int) -> None:
     _check(load().ikbo_plan_set_timeout_ns(plan, ns), "ikbo_plan_set_timeout_ns")
 
@@ -301,6 +307,9 @@ class Plan:
 
     def status(self, stream=None) -> int:
         return ikbo_plan_get_status(self.handle, stream)
+
+    def set_lce_schedule(self, schedule: int) -> None:
+        ikbo_plan_set_lce_schedule(self.handle, schedule)
 
     def launches(self) -> int:
         return ikbo_plan_launch_count(self.handle)

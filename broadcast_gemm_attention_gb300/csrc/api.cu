@@ -18,7 +18,7 @@ namespace ikbo {
 cudaError_t launch_seg_build(const SegParams& p, cudaStream_t s);
 size_t lce_smem_bytes(const LceParams& p);
 cudaError_t launch_lce(const CUtensorMap& tmU, const CUtensorMap& tmC, const CUtensorMap& tmWu,
-                       const CUtensorMap& tmWc, const LceParams& p, int num_sms, cudaStream_t s);
+                       const CUtensorMap& tmWc, const LceParams& p, int num_sms, cudaStream_t s, int* launches);
 cudaError_t launch_lce_stage(const CUtensorMap& tmU, const CUtensorMap& tmC, const CUtensorMap& tmWu,
                              const CUtensorMap& tmWc, LceParams p, int stage, int num_sms, cudaStream_t s,
                              int* launches);
@@ -53,6 +53,7 @@ struct ikbo_plan_s {
   uint32_t epoch = 0;
   uint32_t debug = 0;
   uint64_t timeout_ns = 2000000000ull;
+  int lce_schedule = LCE_SCHEDULE_AUTO;
   std::atomic<uint64_t> launches{0};
 };
 
@@ -163,6 +164,7 @@ ikbo_status_t lce_launch(ikbo_plan_t p, const void* U, const void* C, const void
   lp.epoch = ++p->epoch;
   if (lp.epoch == 0) lp.epoch = ++p->epoch;  // 0 is the flags' initial value
   lp.debug = p->debug;
+  lp.schedule = p->lce_schedule;
   lp.timeout_ns = p->timeout_ns;
 
   CUtensorMap tmU, tmC, tmWu, tmWc;
@@ -262,7 +264,7 @@ ikbo_status_t attn_launch(ikbo_plan_t p, const void* Q, const void* Q_user, cons
 
 extern "C" {
 
-int ikbo_version(void) { return 102; }
+int ikbo_version(void) { return 103; }
 
 const char* ikbo_status_string(ikbo_status_t s) {
   switch (s) {
@@ -331,6 +333,12 @@ void ikbo_plan_destroy(ikbo_plan_t p) {
 ikbo_status_t ikbo_plan_set_debug(ikbo_plan_t p, unsigned flags) {
   if (!p) return IKBO_ERR_INVALID_ARG;
   p->debug = flags;
+  return IKBO_OK;
+}
+
+ikbo_status_t ikbo_plan_set_lce_schedule(ikbo_plan_t p, int schedule) {
+  if (!p || schedule < LCE_SCHEDULE_AUTO || schedule > LCE_SCHEDULE_ONE) return IKBO_ERR_INVALID_ARG;
+  p->lce_schedule = schedule;
   return IKBO_OK;
 }
 

@@ -76,6 +76,7 @@ struct LceParams {
   uint32_t epoch;         // value written to / awaited in `flags`
   uint32_t debug;
   uint32_t mode;          // LCE_MODE_* bits: the stage-ladder ablations (0 = the full kernel)
+  int schedule;           // LCE_SCHEDULE_*: one launch or two (plan-time choice by default)
   uint64_t timeout_ns;
 };
 
@@ -89,6 +90,15 @@ enum : uint32_t {
   LCE_MODE_NO_PARTIAL = 1u << 0,
   LCE_MODE_ONE_ACC = 1u << 1,
 };
+
+// Launch schedule of the LCE: chosen from the shape (AUTO), or forced.
+enum : int {
+  LCE_SCHEDULE_AUTO = 0,
+  LCE_SCHEDULE_TWO = 1,  // user tiles, then candidate tiles
+  LCE_SCHEDULE_ONE = 2,  // one launch, user tiles first in every CTA's list
+};
+// AUTO takes one launch below this many candidate tiles per SM.
+constexpr int LCE_ONE_LAUNCH_TILES_PER_SM = 8;
 
 // Fills the derived fields of an LceParams from its sizes (n_cand, n_users,
 // K_u, K_c, D, N); returns false for shapes the kernel does not support.

@@ -108,19 +108,50 @@ __device__ __forceinline__ UnitInfo unit_info(const LceParams& p, int unit) {
 // range of q per CTA: a CTA stays within one D block (crossing at most one
 // boundary) on consecutive candidates that mostly share a user, so its
 // epilogue loads that user's partial once and keeps it in registers.
+//
+// In the one-launch schedule (u0 == 0 and u1 == n_units) every CTA first
+// computes its user tiles (round-robin), then its range of candidate tiles;
+// while each CTA has at most one user tile, the ranges are weighted so that
+// a CTA with one takes two candidate tiles fewer.
+__device__ __forceinline__ long long fused_q_start(const LceParams& p, int b) {
+  const int g = static_cast<int>(gridDim.x);
+  const long long nq = static_cast<long long>(p.n_cand) * p.n_dblk;
+  if (b >= g) return nq;
+  const long long uu = p.n_user_units;
+  long long w = uu <= g ? (2ll << 8) : 0;  // candidate tiles a user tile stands for, in 1/256
+  long long tq = ((nq << 8) + w * uu) / g;
+  if (tq < w) {  // too few candidate tiles to lighten anyone
+    w = 0;
+    tq = (nq << 8) / g;
+  }
+  const long long cum = (b * tq - w * (b < uu ? b : uu) + 128) >> 8;
+  return cum < 0 ? 0 : (cum > nq ? nq : cum);
+}
+
 __device__ __forceinline__ int cta_unit(const LceParams& p, int u0, int u1, int t) {
-  if (u0 < p.n_user_units) {
-    const int unit = u0 + static_cast<int>(blockIdx.x) + t * static_cast<int>(gridDim.x);
+  const int g = static_cast<int>(gridDim.x), b = static_cast<int>(blockIdx.x);
+  const int uu = p.n_user_units;
+  if (u0 == 0 && u1 == uu) {  // user launch
+    const int unit = b + t * g;
     return unit < u1 ? unit : -1;
   }
-  const long long nq = static_cast<long long>(p.n_cand) * p.n_dblk;
-  const int q0 = static_cast<int>(blockIdx.x * nq / gridDim.x);
-  const int q1 = static_cast<int>((blockIdx.x + 1) * nq / gridDim.x);
+  long long q0, q1;
+  if (u0 == 0) {  // one launch: this CTA's user tiles first
+    const int nu = uu > b ? (uu - b + g - 1) / g : 0;
+    if (t < nu) return b + t * g;
+    t -= nu;
+    q0 = fused_q_start(p, b);
+    q1 = fused_q_start(p, b + 1);
+  } else {  // candidate launch
+    const long long nq = static_cast<long long>(p.n_cand) * p.n_dblk;
+    q0 = b * nq / g;
+    q1 = (b + 1) * nq / g;
+  }
   if (t >= q1 - q0) return -1;
-  const int q = q0 + t;
+  const int q = static_cast<int>(q0 + t);
   const int dblk = q / p.n_cand;
   const int pos = q - dblk * p.n_cand;
-  return p.n_user_units + pos * p.n_dblk + dblk;
+  return uu + pos * p.n_dblk + dblk;
 }
 
 // columns of a user tile's accumulator (a multiple of 16, at most 64)
@@ -433,19 +464,20 @@ __device__ void lce_epilogue(const LceParams& p, const LceSmem& s, uint32_t tmem
   }
 }
 
-// One body, two launches: kUserPhase computes the user tiles (P and their
-// release flags), the other launch the candidate tiles, which acquire the
-// flags and add P in their epilogue.  The user launch runs first on the
-// stream, so the candidate launch finds every flag set at its first check.
-// (One launch with user tiles first in every CTA's list measured slower: its
-// candidate epilogues wait for user tiles still running on other SMs.)
-template <bool kUserPhase>
+// One body, launched either as two kernels -- kPhase LCE_PHASE_USER computes
+// the user tiles (P and their release flags), then LCE_PHASE_CAND the
+// candidate tiles, which acquire the flags and add P in their epilogue -- or
+// as one (LCE_PHASE_BOTH: user tiles first in every CTA's list).  The grid
+// never exceeds the SM count and takes one CTA per SM, so every CTA is
+// resident and a flag wait always ends.
+constexpr int LCE_PHASE_CAND = 0, LCE_PHASE_USER = 1, LCE_PHASE_BOTH = 2;
+template <int kPhase>
 __global__ void __launch_bounds__(LCE_THREADS, 1)
     lce_kernel(const __grid_constant__ CUtensorMap tmU, const __grid_constant__ CUtensorMap tmC,
                const __grid_constant__ CUtensorMap tmWu, const __grid_constant__ CUtensorMap tmWc,
                const LceParams p) {
-  const int u0 = kUserPhase ? 0 : p.n_user_units;
-  const int u1 = kUserPhase ? p.n_user_units : p.n_units;
+  const int u0 = kPhase == LCE_PHASE_CAND ? p.n_user_units : 0;
+  const int u1 = kPhase == LCE_PHASE_USER ? p.n_user_units : p.n_units;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const LceSmem s = carve(base, p);
@@ -542,25 +574,42 @@ size_t lce_smem_bytes(const LceParams& p) {
   return 1024 + p.w_region_bytes + static_cast<size_t>(p.stages) * LCE_A_STAGE_BYTES + bars;
 }
 
-template <bool kUserPhase>
+template <int kPhase>
 cudaError_t launch_phase(const CUtensorMap& tmU, const CUtensorMap& tmC, const CUtensorMap& tmWu,
                          const CUtensorMap& tmWc, const LceParams& p, int units, int num_sms, cudaStream_t s) {
   if (units <= 0) return cudaSuccess;
   const size_t smem = lce_smem_bytes(p);
-  cudaError_t e = cudaFuncSetAttribute(lce_kernel<kUserPhase>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(lce_kernel<kPhase>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   const int grid = units < num_sms ? units : num_sms;
-  lce_kernel<kUserPhase><<<grid, LCE_THREADS, smem, s>>>(tmU, tmC, tmWu, tmWc, p);
+  lce_kernel<kPhase><<<grid, LCE_THREADS, smem, s>>>(tmU, tmC, tmWu, tmWc, p);
   return cudaGetLastError();
 }
 
-// Two launches on one stream: the user tiles, then the candidate tiles.
+bool lce_one_launch(const LceParams& p, int num_sms, int schedule) {
+  if (schedule == LCE_SCHEDULE_TWO) return false;
+  if (schedule == LCE_SCHEDULE_ONE) return true;
+  // Plan-time choice (measured over the n_cand x ratio sweep): with few
+  // candidate tiles per SM, one launch hides the user tiles under the
+  // candidate tiles' start-up; with many, two launches keep every
+  // candidate epilogue from waiting on user tiles still running elsewhere.
+  const long long cand_tiles = static_cast<long long>(p.n_cand) * p.n_dblk;
+  return cand_tiles < static_cast<long long>(LCE_ONE_LAUNCH_TILES_PER_SM) * num_sms;
+}
+
+// The user tiles and the candidate tiles: two launches on one stream, or one
+// (see lce_one_launch).  *launches receives the number of launches.
 cudaError_t launch_lce(const CUtensorMap& tmU, const CUtensorMap& tmC, const CUtensorMap& tmWu,
-                       const CUtensorMap& tmWc, const LceParams& p, int num_sms, cudaStream_t s) {
-  cudaError_t e = launch_phase<true>(tmU, tmC, tmWu, tmWc, p, p.n_user_units, num_sms, s);
+                       const CUtensorMap& tmWc, const LceParams& p, int num_sms, cudaStream_t s, int* launches) {
+  if (lce_one_launch(p, num_sms, p.schedule)) {
+    *launches = 1;
+    return launch_phase<LCE_PHASE_BOTH>(tmU, tmC, tmWu, tmWc, p, p.n_units, num_sms, s);
+  }
+  *launches = 2;
+  cudaError_t e = launch_phase<LCE_PHASE_USER>(tmU, tmC, tmWu, tmWc, p, p.n_user_units, num_sms, s);
   if (e != cudaSuccess) return e;
-  return launch_phase<false>(tmU, tmC, tmWu, tmWc, p, p.n_units - p.n_user_units, num_sms, s);
+  return launch_phase<LCE_PHASE_CAND>(tmU, tmC, tmWu, tmWc, p, p.n_units - p.n_user_units, num_sms, s);
 }
 
 namespace {
@@ -603,19 +652,15 @@ cudaError_t launch_lce_stage(const CUtensorMap& tmU, const CUtensorMap& tmC, con
                              const CUtensorMap& tmWc, LceParams p, int stage, int num_sms, cudaStream_t s,
                              int* launches) {
   *launches = 0;
-  if (stage == 4) {
-    *launches = 2;
-    return launch_lce(tmU, tmC, tmWu, tmWc, p, num_sms, s);
-  }
+  if (stage == 4) return launch_lce(tmU, tmC, tmWu, tmWc, p, num_sms, s, launches);
   p.mode = stage == 1 ? LCE_MODE_NO_PARTIAL : LCE_MODE_ONE_ACC;
-  cudaError_t e = launch_lce(tmU, tmC, tmWu, tmWc, p, num_sms, s);
+  cudaError_t e = launch_lce(tmU, tmC, tmWu, tmWc, p, num_sms, s, launches);
   if (e != cudaSuccess) return e;
-  *launches = 2;
   if (stage == 1) {
     lce_broadcast_add_kernel<<<num_sms * 4, 256, 0, s>>>(p.map, p.partial, p.Y, p.n_cand, p.n_users, p.N, p.D,
                                                           p.status);
     e = cudaGetLastError();
-    if (e == cudaSuccess) *launches = 3;
+    if (e == cudaSuccess) *launches += 1;
   }
   return e;
 }

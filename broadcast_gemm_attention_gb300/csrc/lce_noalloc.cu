@@ -30,7 +30,7 @@
 
 namespace ikbo {
 cudaError_t launch_lce(const CUtensorMap& tmU, const CUtensorMap& tmC, const CUtensorMap& tmWu,
-                       const CUtensorMap& tmWc, const LceParams& p, int num_sms, cudaStream_t s);
+                       const CUtensorMap& tmWc, const LceParams& p, int num_sms, cudaStream_t s, int* launches);
 }  // namespace ikbo
 
 using namespace ikbo;
@@ -194,6 +194,7 @@ extern "C" ikbo_status_t ikbo_lce_forward_noalloc(const int32_t* d_map, int n_ca
 
   // the status words must start at zero for this call (the flags do not: see epoch)
   if (cudaMemsetAsync(base, 0, 2 * sizeof(uint32_t), stream) != cudaSuccess) return IKBO_ERR_CUDA;
-  if (launch_lce(tmU, tmC, tmWu, tmWc, lp, slot->num_sms, stream) != cudaSuccess) return IKBO_ERR_CUDA;
+  int launches = 0;
+  if (launch_lce(tmU, tmC, tmWu, tmWc, lp, slot->num_sms, stream, &launches) != cudaSuccess) return IKBO_ERR_CUDA;
   return IKBO_OK;
 }

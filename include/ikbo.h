@@ -212,6 +212,15 @@ ikbo_status_t ikbo_plan_get_status(ikbo_plan_t p, cudaStream_t stream);
 ikbo_status_t ikbo_plan_set_debug(ikbo_plan_t p, unsigned flags);
 ikbo_status_t ikbo_plan_set_timeout_ns(ikbo_plan_t p, uint64_t timeout_ns);
 
+/* Launch schedule of ikbo_lce_forward (plan-time kernel selection over the
+ * shape range, the "compile for a range of shapes" idea of the pages done as
+ * a runtime choice): 0 = chosen from the shape (default: one launch when the
+ * request has fewer than 8 candidate tiles of 128 D-rows per SM, else two),
+ * 1 = two launches (user tiles, then candidate tiles), 2 = one launch (user
+ * tiles first in every CTA's list).  Results are identical; only the time
+ * differs.  Other values: IKBO_ERR_INVALID_ARG. */
+ikbo_status_t ikbo_plan_set_lce_schedule(ikbo_plan_t p, int schedule);
+
 /* Number of kernel launches the forward calls and ikbo_plan have made
  * through this plan since it was created. */
 uint64_t ikbo_plan_launch_count(ikbo_plan_t p);

@@ -16,10 +16,11 @@ from gpu_util import assert_lce_close, sample_candidates, to_dev
 pytestmark = pytest.mark.gpu
 
 
-def run_stages(x, stages=(1, 3, 4)):
+def run_stages(x, stages=(1, 3, 4), schedule=1):
     U, C, Wu, Wc, b, m = to_dev(x.U, x.C, x.Wu, x.Wc, x.b, x.map)
     out, launches = {}, {}
     with B.Plan(x.n_cand, x.n_users, 1) as p:
+        p.set_lce_schedule(schedule)
         p.plan(m, x.n_users)
         for st in stages:
             Y = torch.full((x.n_cand, x.N, x.D), float("nan"), dtype=torch.bfloat16, device="cuda")
@@ -36,10 +37,11 @@ def run_stages(x, stages=(1, 3, 4)):
     dict(n_cand=37, n_users=3, K_u=37, K_c=29, D=136, N=40),
     dict(n_cand=300, n_users=7, K_u=381, K_c=243, D=384, N=200),
 ])
-def test_lce_stages_full(shape):
+@pytest.mark.parametrize("schedule", [1, 2])
+def test_lce_stages_full(shape, schedule):
     x = gen.make_lce("stages", 81, map_kind="permuted", **shape)
-    out, launches = run_stages(x)
-    assert launches == {1: 3, 3: 2, 4: 2}
+    out, launches = run_stages(x, schedule=schedule)
+    assert launches == ({1: 3, 3: 2, 4: 2} if schedule == 1 else {1: 2, 3: 1, 4: 1})
     ref = oracle.lce(x.map, x.U, x.C, x.Wu, x.Wc, x.b)
     for st, Y in out.items():
         assert_lce_close(Y, ref, f"stage {st}")
@@ -70,3 +72,32 @@ def test_lce_stage_argument_and_map_errors():
             assert e.value.code == B.IKBO_ERR_INVALID_ARG
         p.lce_forward_staged(U, C, Wu, Wc, b, Y, 1)
         assert p.status() == B.IKBO_ERR_MAP_OUT_OF_RANGE
+
+
+@pytest.mark.parametrize("shape", [
+    dict(n_cand=256, n_users=26, K_u=381, K_c=243, D=256, N=192),
+    dict(n_cand=1024, n_users=15, K_u=381, K_c=243, D=256, N=192),
+    dict(n_cand=64, n_users=1, K_u=700, K_c=100, D=256, N=192),
+])
+def test_lce_schedules_agree(shape):
+    """One launch and two launches do the same arithmetic per tile: identical Y;
+    the automatic choice is one of them."""
+    x = gen.make_lce("sched", 83, map_kind="permuted", **shape)
+    U, C, Wu, Wc, b, m = to_dev(x.U, x.C, x.Wu, x.Wc, x.b, x.map)
+    ys = {}
+    with B.Plan(x.n_cand, x.n_users, 1) as p:
+        p.plan(m, x.n_users)
+        for sch in (0, 1, 2):
+            p.set_lce_schedule(sch)
+            Y = torch.full((x.n_cand, x.N, x.D), float("nan"), dtype=torch.bfloat16, device="cuda")
+            l0 = p.launches()
+            p.lce_forward(U, C, Wu, Wc, b, Y)
+            assert p.launches() - l0 == (2 if sch == 1 else 1 if sch == 2 else p.launches() - l0)
+            assert p.status() == B.IKBO_OK
+            ys[sch] = Y
+        with pytest.raises(B.IkboError):
+            p.set_lce_schedule(3)
+    assert torch.equal(ys[1], ys[2])
+    assert torch.equal(ys[0], ys[1])
+    sel = sample_candidates(x.map, 12)
+    assert_lce_close(ys[2][sel], oracle.lce(x.map, x.U, x.C, x.Wu, x.Wc, x.b, cands=sel), "one launch")
