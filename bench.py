@@ -296,6 +296,7 @@ def run_gpu(args):
     O = torch.empty_like(d["Q"])
     flush = L2Flush(dev)
     plan = B.Plan(x.n_cand, max(x.n_users, x.n_cand), a.H)
+    plan.set_lce_schedule(args.lce_schedule)
 
     def step():
         plan.plan(d["map"], x.n_users, a.H, a.Lq, stream)
@@ -352,7 +353,12 @@ def run_gpu(args):
                 "traffic": recorded_traffic("attn"),
                 "peak_source": pk["source"] + ", bf16 burst (kernel timed alone in a short step)",
                 "algorithmic": f"{af:.4g} FLOP per launch = 4*H*Lq*d*sum_i Lkv"}
-    roofline_lce = {"kernel": "lce_kernel (user-tile + candidate-tile launches)", "bound": "hbm", "achieved": lce_gbs, "peak": pk["hbm_gbs"],
+    lce_launches = gpu_launches / K - 2  # a step is segment build + LCE + attention
+    lce_kernel = {1: "lce_kernel (one launch)", 2: "lce_kernel (user-tile + candidate-tile launches)"}.get(
+        round(lce_launches), "lce_kernel")
+    if args.lce_schedule in (0, 3) and round(lce_launches) == 1 and x.N <= 192:
+        lce_kernel = "lce_kernel (one launch: local user partials)"
+    roofline_lce = {"kernel": lce_kernel, "bound": "hbm", "achieved": lce_gbs, "peak": pk["hbm_gbs"],
                     "unit": "GB/s", "frac": lce_gbs / pk["hbm_gbs"], "traffic": recorded_traffic("lce"),
                     "tflops": lce_tf, "algorithmic": f"{lb:.4g} bytes per launch (inputs once, Y once)"}
 
@@ -474,7 +480,7 @@ def run_sweep(args):
         sched = {}
         with B.Plan(x.n_cand, x.n_users, 1) as p:
             p.plan(m, x.n_users, 1, 8, stream)
-            for name, code in (("two_launches", 1), ("one_launch", 2), ("auto", 0)):
+            for name, code in (("two_launches", 1), ("one_launch", 2), ("local_partials", 3), ("auto", 0)):
                 p.set_lce_schedule(code)
                 sched[name] = timed(lambda: p.lce_forward(U, C, Wu, Wc, b, Y, stream))
             us = sched["auto"]
@@ -627,6 +633,8 @@ def main():
     ap.add_argument("--no-self-target", action="store_true", help="skip the self + target attention comparison")
     ap.add_argument("--sweep", action="store_true", help="shape sweep (LCE and attention) instead of the benchmark")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--lce-schedule", type=int, default=0, choices=[0, 1, 2, 3],
+                    help="LCE launch schedule: 0 plan-time choice, 1 two launches, 2 one launch, 3 local partials")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target length of the CPU-oracle baseline (0 skips it, e.g. under a profiler)")

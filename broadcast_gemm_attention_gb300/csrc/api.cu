@@ -337,7 +337,7 @@ ikbo_status_t ikbo_plan_set_debug(ikbo_plan_t p, unsigned flags) {
 }
 
 ikbo_status_t ikbo_plan_set_lce_schedule(ikbo_plan_t p, int schedule) {
-  if (!p || schedule < LCE_SCHEDULE_AUTO || schedule > LCE_SCHEDULE_ONE) return IKBO_ERR_INVALID_ARG;
+  if (!p || schedule < LCE_SCHEDULE_AUTO || schedule > LCE_SCHEDULE_LOCAL) return IKBO_ERR_INVALID_ARG;
   p->lce_schedule = schedule;
   return IKBO_OK;
 }

@@ -71,7 +71,9 @@ struct LceParams {
   int kc_u, kc_c;         // 64-wide K chunks (ceil(K / 64))
   int ks_u, ks_c;         // 16-wide MMA k-steps (ceil(K / 16))
   int stages;             // A ring depth
+  int stages_local;       // A ring depth of the local-partial schedule (0: that schedule does not fit)
   int w_slots;            // 8 KB W_u slots in the W region used by user tiles (2..8)
+  int wu_slots;           // full-width W_u chunk slots after the A ring (local-partial schedule only, else 0)
   uint32_t w_region_bytes;
   uint32_t epoch;         // value written to / awaited in `flags`
   uint32_t debug;
@@ -94,16 +96,23 @@ enum : uint32_t {
 // Launch schedule of the LCE: chosen from the shape (AUTO), or forced.
 enum : int {
   LCE_SCHEDULE_AUTO = 0,
-  LCE_SCHEDULE_TWO = 1,  // user tiles, then candidate tiles
-  LCE_SCHEDULE_ONE = 2,  // one launch, user tiles first in every CTA's list
+  LCE_SCHEDULE_TWO = 1,    // user tiles, then candidate tiles
+  LCE_SCHEDULE_ONE = 2,    // one launch, user tiles first in every CTA's list
+  LCE_SCHEDULE_LOCAL = 3,  // one launch of candidate tiles; each CTA computes the user partials its
+                           // own tiles need, into TMEM (N <= 192)
 };
 // AUTO takes one launch below this many candidate tiles per SM.
 constexpr int LCE_ONE_LAUNCH_TILES_PER_SM = 8;
+constexpr int LCE_WU_SLOTS = 2;     // W_u chunk slots of the local-partial schedule
+constexpr int LCE_LOCAL_MAX_N = 192;  // the epilogue keeps a partial of at most 6 x 32 columns per row
 
 // Fills the derived fields of an LceParams from its sizes (n_cand, n_users,
 // K_u, K_c, D, N); returns false for shapes the kernel does not support.
 // Shared by every LCE entry point so they configure the kernel identically.
 bool lce_configure(LceParams* lp, size_t max_smem);
+// The schedule a launch of lp runs: lp->schedule where it applies to the
+// shape and mode, else the plan-time choice.
+int lce_resolve_schedule(const LceParams& lp, int num_sms);
 size_t lce_flag_count(const LceParams& lp);
 size_t lce_smem_bytes(const LceParams& lp);
 

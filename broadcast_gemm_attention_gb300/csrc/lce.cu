@@ -17,8 +17,15 @@
 //     tiles share the launch, user tiles first in every CTA's static order,
 //     and a candidate epilogue acquires the release flag of its user tile.
 //
-// Two launches of one persistent kernel body (one CTA per SM): the user
-// tiles first, then the candidate tiles.  Per CTA:
+// Schedules of one persistent kernel body (one CTA per SM):
+//   two launches: the user tiles, then the candidate tiles;
+//   one launch: user tiles first in every CTA's list, candidate tiles after;
+//   local partials: one launch of candidate tiles only; before the first
+//     candidate tile of each (user, D block) a CTA computes that user's
+//     partial itself, into TMEM, and its epilogue keeps it in registers --
+//     no workspace, no hand-off between CTAs (the user GEMM is repeated by the
+//     few CTAs that share a user: the work is small and U stays in L2).
+// Per CTA:
 //   warp 0  TMA producer   (A ring: U[u] or C[i] chunks; W chunks / resident Wc)
 //   warp 1  MMA issuer     (tcgen05.mma, fp32 accumulators in TMEM, 2 buffers)
 //   warp 2  TMEM owner     (alloc / dealloc of 512 columns)
@@ -46,6 +53,9 @@ struct LceSmem {
   uint64_t* a_empty;
   uint64_t* w_full;
   uint64_t* w_empty;
+  uint8_t* wu_ring;    // local-partial schedule: full-width W_u chunks (NB boxes each)
+  uint64_t* wu_full;
+  uint64_t* wu_empty;
   uint64_t* wc_full;
   uint64_t* acc_full;
   uint64_t* acc_empty;
@@ -58,12 +68,15 @@ __device__ __forceinline__ LceSmem carve(uint8_t* base, const LceParams& p) {
   LceSmem s;
   s.w_region = base;
   s.a_ring = base + p.w_region_bytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(s.a_ring + static_cast<size_t>(p.stages) * LCE_A_STAGE_BYTES);
+  s.wu_ring = s.a_ring + static_cast<size_t>(p.stages) * LCE_A_STAGE_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(s.wu_ring + static_cast<size_t>(p.wu_slots) * p.NB * BOX_BYTES);
   s.a_full = bars;
   s.a_empty = s.a_full + p.stages;
   s.w_full = s.a_empty + p.stages;
   s.w_empty = s.w_full + p.w_slots;
-  s.wc_full = s.w_empty + p.w_slots;
+  s.wu_full = s.w_empty + p.w_slots;
+  s.wu_empty = s.wu_full + p.wu_slots;
+  s.wc_full = s.wu_empty + p.wu_slots;
   s.acc_full = s.wc_full + 1;
   s.acc_empty = s.acc_full + 2;
   s.pub = s.acc_empty + 2;
@@ -78,14 +91,16 @@ __device__ __forceinline__ LceSmem carve(uint8_t* base, const LceParams& p) {
 // more SMs and each of its tiles loads and writes a third as much.
 struct UnitInfo {
   bool is_user;
-  int row;   // user u or candidate i
-  int dblk;  // 128-row block of D
-  int nblk;  // user tiles: 64-wide block of N
+  bool local;  // a user tile of the local-partial schedule: all of N, kept in this CTA
+  int row;     // user u or candidate i
+  int dblk;    // 128-row block of D
+  int nblk;    // user tiles: 64-wide block of N
 };
 
 __device__ __forceinline__ UnitInfo unit_info(const LceParams& p, int unit) {
   UnitInfo x;
   x.is_user = unit < p.n_user_units;
+  x.local = false;
   if (x.is_user) {
     x.nblk = unit % p.NB;
     const int ud = unit / p.NB;
@@ -154,10 +169,91 @@ __device__ __forceinline__ int cta_unit(const LceParams& p, int u0, int u1, int 
   return uu + pos * p.n_dblk + dblk;
 }
 
+constexpr int LCE_PHASE_CAND = 0, LCE_PHASE_USER = 1, LCE_PHASE_BOTH = 2, LCE_PHASE_LOCAL = 3;
+
+// The units a CTA runs, in order: its units of [u0, u1), and in the
+// local-partial schedule, before a candidate tile whose (user, D block)
+// differs from the previous one, a local user tile for that pair.  Every
+// role walks the same sequence, a whole warp at a time: the lanes look up 32
+// units at once (list position -> unit -> candidate -> user) and each step
+// takes its unit from one lane, so the dependent global loads of a lookup --
+// half a microsecond each while HBM streams -- are paid once per 32 units
+// instead of on every tile's critical path.  All lanes must call walk_next.
+struct Walk {
+  int t = 0;      // next index in this CTA's list
+  int t0 = -32;   // list index of lane 0's window entry
+  int w_unit = -1, w_row = 0, w_dblk = 0, w_nblk = 0, w_user = -1;  // this lane's entry
+  int cur_u = -1, cur_dblk = -1;
+  bool held = false;
+  UnitInfo next;
+  int next_user = -1;
+};
+
+template <int kPhase>
+__device__ __forceinline__ bool walk_next(const LceParams& p, int u0, int u1, Walk& w, UnitInfo& x, int& user) {
+  if (kPhase == LCE_PHASE_LOCAL && w.held) {
+    x = w.next;
+    user = w.next_user;
+    w.held = false;
+    return true;
+  }
+  if (w.t - w.t0 >= 32) {
+    w.t0 = w.t;
+    w.w_unit = cta_unit(p, u0, u1, w.t0 + static_cast<int>(lane_id()));
+    if (w.w_unit >= 0) {
+      const UnitInfo y = unit_info(p, w.w_unit);
+      w.w_row = y.row;
+      w.w_dblk = y.dblk;
+      w.w_nblk = y.nblk;
+      w.w_user = y.is_user ? y.row : __ldg(p.map + y.row);
+    }
+  }
+  const int k = w.t - w.t0;
+  const int unit = __shfl_sync(0xffffffffu, w.w_unit, k);
+  if (unit < 0) return false;
+  ++w.t;
+  x.is_user = unit < p.n_user_units;
+  x.local = false;
+  x.row = __shfl_sync(0xffffffffu, w.w_row, k);
+  x.dblk = __shfl_sync(0xffffffffu, w.w_dblk, k);
+  x.nblk = __shfl_sync(0xffffffffu, w.w_nblk, k);
+  user = __shfl_sync(0xffffffffu, w.w_user, k);
+  if (kPhase == LCE_PHASE_LOCAL && user >= 0 && user < p.n_users && (user != w.cur_u || x.dblk != w.cur_dblk)) {
+    w.cur_u = user;
+    w.cur_dblk = x.dblk;
+    w.next = x;
+    w.next_user = user;
+    w.held = true;
+    x.is_user = true;
+    x.local = true;
+    x.row = user;
+    x.nblk = 0;
+  }
+  return true;
+}
+
 // columns of a user tile's accumulator (a multiple of 16, at most 64)
 __device__ __forceinline__ int user_tile_n(const LceParams& p, int nblk) { return min(64, p.N_mma - nblk * 64); }
 
 // ------------------------------------------------------------ producer
+// A wait taken by a whole warp: every lane polls, and the lanes agree on the
+// outcome so that a timeout never splits the warp.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const LceSmem& s, const LceParams& p) {
+  const bool ok = mbar_wait(bar, parity, s.abort, p.timeout_ns, 1);
+  return __all_sync(0xffffffffu, ok);
+}
+
+__device__ __forceinline__ void load_wc(const LceParams& p, const LceSmem& s, const CUtensorMap* tmWc) {
+  mbar_arrive_expect_tx(s.wc_full, static_cast<uint32_t>(p.kc_c * p.NB) * BOX_BYTES);
+  for (int kc = 0; kc < p.kc_c; ++kc)
+    for (int nb = 0; nb < p.NB; ++nb)
+      tma_load_2d(s.w_region + (static_cast<size_t>(kc) * p.NB + nb) * BOX_BYTES, tmWc, s.wc_full, nb * 64,
+                  kc * LCE_BK);
+}
+
+// TMA producer: the whole warp runs the loop and waits; one elected lane
+// issues the copies.
+template <int kPhase>
 __device__ void lce_producer(const LceParams& p, const LceSmem& s, const CUtensorMap* tmU, const CUtensorMap* tmC,
                              const CUtensorMap* tmWu, const CUtensorMap* tmWc, int u0, int u1) {
   int stage = 0;
@@ -165,38 +261,60 @@ __device__ void lce_producer(const LceParams& p, const LceSmem& s, const CUtenso
   int wslot = 0;
   uint32_t w_phase = 0;
   uint32_t w_uses[LCE_MAX_W_SLOTS] = {0, 0, 0, 0, 0, 0, 0, 0};
+  int uslot = 0;
+  uint32_t u_phase = 0;
   bool wc_loaded = false;
   const uint32_t w_chunk_bytes = static_cast<uint32_t>(p.NB) * BOX_BYTES;
+  if (kPhase == LCE_PHASE_LOCAL) {  // no user tile uses the W region: W_c lands at once
+    if (elect_one()) load_wc(p, s, tmWc);
+    __syncwarp();
+    wc_loaded = true;
+  }
 
-  for (int t = 0;; ++t) {
-    const int unit = cta_unit(p, u0, u1, t);
-    if (unit < 0) break;
-    const UnitInfo x = unit_info(p, unit);
+  Walk walk;
+  for (;;) {
+    UnitInfo x;
+    int user;
+    if (!walk_next<kPhase>(p, u0, u1, walk, x, user)) break;
     const CUtensorMap* tmA = x.is_user ? tmU : tmC;
     const int kc_n = x.is_user ? p.kc_u : p.kc_c;
     const int d0 = x.dblk * LCE_BM;
     if (!x.is_user && !wc_loaded) {
       // every W slot used by the user phase must be drained before Wc lands
       for (int w = 0; w < p.w_slots; ++w)
-        if (w_uses[w] > 0 && !mbar_wait(&s.w_empty[w], (w_uses[w] - 1) & 1u, s.abort, p.timeout_ns, 1)) return;
-      mbar_arrive_expect_tx(s.wc_full, static_cast<uint32_t>(p.kc_c) * w_chunk_bytes);
-      for (int kc = 0; kc < p.kc_c; ++kc)
-        for (int nb = 0; nb < p.NB; ++nb)
-          tma_load_2d(s.w_region + (static_cast<size_t>(kc) * p.NB + nb) * BOX_BYTES, tmWc, s.wc_full, nb * 64,
-                      kc * LCE_BK);
+        if (w_uses[w] > 0 && !warp_wait(&s.w_empty[w], (w_uses[w] - 1) & 1u, s, p)) return;
+      if (elect_one()) load_wc(p, s, tmWc);
+      __syncwarp();
       wc_loaded = true;
     }
     for (int kc = 0; kc < kc_n; ++kc) {
-      if (!mbar_wait(&s.a_empty[stage], a_phase ^ 1u, s.abort, p.timeout_ns, 1)) return;
-      uint8_t* dst = s.a_ring + static_cast<size_t>(stage) * LCE_A_STAGE_BYTES;
-      mbar_arrive_expect_tx(&s.a_full[stage], LCE_A_STAGE_BYTES);
-      tma_load_3d(dst, tmA, &s.a_full[stage], d0, kc * LCE_BK, x.row);
-      tma_load_3d(dst + BOX_BYTES, tmA, &s.a_full[stage], d0 + 64, kc * LCE_BK, x.row);
-      if (x.is_user) {
-        if (!mbar_wait(&s.w_empty[wslot], w_phase ^ 1u, s.abort, p.timeout_ns, 1)) return;
-        mbar_arrive_expect_tx(&s.w_full[wslot], BOX_BYTES);
-        tma_load_2d(s.w_region + static_cast<size_t>(wslot) * BOX_BYTES, tmWu, &s.w_full[wslot], x.nblk * 64,
-                    kc * LCE_BK);
+      if (!warp_wait(&s.a_empty[stage], a_phase ^ 1u, s, p)) return;
+      const bool wu_ring = kPhase == LCE_PHASE_LOCAL && x.local;  // all NB boxes of this K chunk of W_u
+      if (wu_ring && !warp_wait(&s.wu_empty[uslot], u_phase ^ 1u, s, p)) return;
+      if (!wu_ring && x.is_user && !warp_wait(&s.w_empty[wslot], w_phase ^ 1u, s, p)) return;
+      if (elect_one()) {
+        uint8_t* dst = s.a_ring + static_cast<size_t>(stage) * LCE_A_STAGE_BYTES;
+        mbar_arrive_expect_tx(&s.a_full[stage], LCE_A_STAGE_BYTES);
+        tma_load_3d(dst, tmA, &s.a_full[stage], d0, kc * LCE_BK, x.row);
+        tma_load_3d(dst + BOX_BYTES, tmA, &s.a_full[stage], d0 + 64, kc * LCE_BK, x.row);
+        if (wu_ring) {
+          uint8_t* wdst = s.wu_ring + static_cast<size_t>(uslot) * w_chunk_bytes;
+          mbar_arrive_expect_tx(&s.wu_full[uslot], w_chunk_bytes);
+          for (int nb = 0; nb < p.NB; ++nb)
+            tma_load_2d(wdst + static_cast<size_t>(nb) * BOX_BYTES, tmWu, &s.wu_full[uslot], nb * 64, kc * LCE_BK);
+        } else if (x.is_user) {
+          mbar_arrive_expect_tx(&s.w_full[wslot], BOX_BYTES);
+          tma_load_2d(s.w_region + static_cast<size_t>(wslot) * BOX_BYTES, tmWu, &s.w_full[wslot], x.nblk * 64,
+                      kc * LCE_BK);
+        }
+      }
+      __syncwarp();
+      if (wu_ring) {
+        if (++uslot == p.wu_slots) {
+          uslot = 0;
+          u_phase ^= 1u;
+        }
+      } else if (x.is_user) {
         w_uses[wslot] += 1;
         if (++wslot == p.w_slots) {
           wslot = 0;
@@ -212,15 +330,9 @@ __device__ void lce_producer(const LceParams& p, const LceSmem& s, const CUtenso
 }
 
 // ----------------------------------------------------------------- MMA
-// A wait taken by a whole warp: every lane polls, and the lanes agree on the
-// outcome so that a timeout never splits the warp.
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const LceSmem& s, const LceParams& p) {
-  const bool ok = mbar_wait(bar, parity, s.abort, p.timeout_ns, 1);
-  return __all_sync(0xffffffffu, ok);
-}
-
 // MMA issuer: the whole warp runs the loop (its values stay warp-uniform) and
 // one elected lane issues; a lone lane pays far more per tcgen05.mma.
+template <int kPhase>
 __device__ void lce_mma(const LceParams& p, const LceSmem& s, uint32_t tmem, int u0, int u1) {
   const uint32_t idesc_c = idesc_bf16_f32(LCE_BM, static_cast<uint32_t>(p.N_mma), true, true);
   const uint32_t w_chunk_bytes = static_cast<uint32_t>(p.NB) * BOX_BYTES;
@@ -228,12 +340,15 @@ __device__ void lce_mma(const LceParams& p, const LceSmem& s, uint32_t tmem, int
   uint32_t a_phase = 0;
   int wslot = 0;
   uint32_t w_phase = 0;
+  int uslot = 0;
+  uint32_t u_phase = 0;
   bool wc_ready = false;
-  int local = 0;
-  for (int t = 0;; ++t, ++local) {
-    const int unit = cta_unit(p, u0, u1, t);
-    if (unit < 0) break;
-    const UnitInfo x = unit_info(p, unit);
+  Walk walk;
+  for (int local = 0;; ++local) {
+    UnitInfo x;
+    int user;
+    if (!walk_next<kPhase>(p, u0, u1, walk, x, user)) break;
+    const bool wu_ring = kPhase == LCE_PHASE_LOCAL && x.local;  // W_u from the full-width ring
     const int kc_n = x.is_user ? p.kc_u : p.kc_c;
     int ks_left = x.is_user ? p.ks_u : p.ks_c;
     const bool one_acc = p.mode & LCE_MODE_ONE_ACC;
@@ -246,15 +361,22 @@ __device__ void lce_mma(const LceParams& p, const LceSmem& s, uint32_t tmem, int
     }
     tc_fence_after();
     const uint32_t d_tmem = tmem + static_cast<uint32_t>(buf) * 256u;
-    const uint32_t idesc =
-        x.is_user ? idesc_bf16_f32(LCE_BM, static_cast<uint32_t>(user_tile_n(p, x.nblk)), true, true) : idesc_c;
+    const uint32_t idesc = (x.is_user && !wu_ring)
+                               ? idesc_bf16_f32(LCE_BM, static_cast<uint32_t>(user_tile_n(p, x.nblk)), true, true)
+                               : idesc_c;
     for (int kc = 0; kc < kc_n; ++kc) {
       if (!warp_wait(&s.a_full[stage], a_phase, s, p)) return;
-      if (x.is_user && !warp_wait(&s.w_full[wslot], w_phase, s, p)) return;
+      if (wu_ring) {
+        if (!warp_wait(&s.wu_full[uslot], u_phase, s, p)) return;
+      } else if (x.is_user && !warp_wait(&s.w_full[wslot], w_phase, s, p)) {
+        return;
+      }
       tc_fence_after();
       const uint32_t a_base = smem_u32(s.a_ring + static_cast<size_t>(stage) * LCE_A_STAGE_BYTES);
-      const uint32_t b_base = smem_u32(s.w_region + (x.is_user ? static_cast<size_t>(wslot) * BOX_BYTES
-                                                                  : static_cast<size_t>(kc) * w_chunk_bytes));
+      const uint32_t b_base =
+          wu_ring ? smem_u32(s.wu_ring + static_cast<size_t>(uslot) * w_chunk_bytes)
+                  : smem_u32(s.w_region + (x.is_user ? static_cast<size_t>(wslot) * BOX_BYTES
+                                                     : static_cast<size_t>(kc) * w_chunk_bytes));
       const int nsteps = ks_left < 4 ? ks_left : 4;
       // 16 k rows of 128 bytes per MMA step; 64-element blocks along M / N
       // are one box apart; steps advance the start address by 2048 bytes
@@ -271,11 +393,19 @@ __device__ void lce_mma(const LceParams& p, const LceSmem& s, uint32_t tmem, int
             mma_bf16_ss(d_tmem, adesc + st * (2048u >> 4), bdesc + st * (2048u >> 4), idesc, st > 0 ? 1u : acc0);
         }
         mma_commit(&s.a_empty[stage]);
-        if (x.is_user) mma_commit(&s.w_empty[wslot]);
+        if (wu_ring)
+          mma_commit(&s.wu_empty[uslot]);
+        else if (x.is_user)
+          mma_commit(&s.w_empty[wslot]);
       }
       __syncwarp();
       ks_left -= nsteps;
-      if (x.is_user) {
+      if (wu_ring) {
+        if (++uslot == p.wu_slots) {
+          uslot = 0;
+          u_phase ^= 1u;
+        }
+      } else if (x.is_user) {
         if (++wslot == p.w_slots) {
           wslot = 0;
           w_phase ^= 1u;
@@ -328,6 +458,7 @@ __device__ __forceinline__ bool wait_all_user_partials(const LceParams& p) {
 // accumulator, so the L2 latency of that gather hides behind the MMA.
 constexpr int EPI_PREFETCH = 3;  // chunks of P held in registers ahead of the accumulator
 
+template <int kPhase>
 __device__ void lce_epilogue(const LceParams& p, const LceSmem& s, uint32_t tmem, int u0, int u1) {
   const int warp = threadIdx.x >> 5;
   const int quarter = warp & 3;
@@ -342,10 +473,11 @@ __device__ void lce_epilogue(const LceParams& p, const LceSmem& s, uint32_t tmem
   // the user partial of the current (user, D block), kept across tiles
   float pre[EPI_PREFETCH][32];
   int pre_u = -1, pre_dblk = -1;
-  for (int t = 0;; ++t, ++local) {
-    const int unit = cta_unit(p, u0, u1, t);
-    if (unit < 0) break;
-    const UnitInfo x = unit_info(p, unit);
+  Walk walk;
+  for (;; ++local) {
+    UnitInfo x;
+    int user;  // candidate tiles: map[i] (the warp's lanes looked it up together)
+    if (!walk_next<kPhase>(p, u0, u1, walk, x, user)) break;
     const bool one_acc = p.mode & LCE_MODE_ONE_ACC;
     const int buf = one_acc ? 0 : (local & 1);
     const uint32_t use = static_cast<uint32_t>(one_acc ? local : (local >> 1));
@@ -353,11 +485,40 @@ __device__ void lce_epilogue(const LceParams& p, const LceSmem& s, uint32_t tmem
     const bool dok = d < p.D;
     const size_t ND = static_cast<size_t>(p.N) * p.D;
     const uint32_t t_acc = tmem + lane_base + static_cast<uint32_t>(buf) * 256u;
-    if (x.is_user) {
+    if (kPhase == LCE_PHASE_LOCAL && x.local) {
+      // this CTA's own partial of (user, D block): accumulator + b -> registers;
+      // b is loaded before the wait, so its latency hides behind the MMA
+#pragma unroll
+      for (int k = 0; k < EPI_PREFETCH; ++k) {
+        const int c = half + 2 * k;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const int n = c * 32 + j;
+          pre[k][j] = (p.bias && n < p.N) ? __bfloat162float(__ushort_as_bfloat16(__ldg(p.bias + n))) : 0.f;
+        }
+      }
+      if (!warp_wait(&s.acc_full[buf], use & 1u, s, p)) return;
+      tc_fence_after();
+#pragma unroll
+      for (int k = 0; k < EPI_PREFETCH; ++k) {
+        const int c = half + 2 * k;
+        if (c < nchunks) {
+          uint32_t v[32];
+          tmem_ld32(t_acc + c * 32, v);
+          tmem_ld_wait(v);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) pre[k][j] += __uint_as_float(v[j]);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&s.acc_empty[buf]);
+      pre_u = x.row;
+      pre_dblk = x.dblk;
+    } else if (x.is_user) {
       // this tile holds columns n0 .. n0 + nw - 1 of P
       const int n0 = x.nblk * 64;
       const int nw = user_tile_n(p, x.nblk);
-      if (!mbar_wait(&s.acc_full[buf], use & 1u, s.abort, p.timeout_ns, 1)) return;
+      if (!warp_wait(&s.acc_full[buf], use & 1u, s, p)) return;
       tc_fence_after();
       float* P = p.partial + static_cast<size_t>(x.row) * ND + d;
       for (int c = half; c * 32 < nw; c += 2) {
@@ -396,11 +557,16 @@ __device__ void lce_epilogue(const LceParams& p, const LceSmem& s, uint32_t tmem
     } else {
       const int i = x.row;
       const bool add_p = !(p.mode & LCE_MODE_NO_PARTIAL);
-      const int u = add_p ? p.map[i] : 0;
+      const int u = add_p ? user : 0;
       const bool uok = u >= 0 && u < p.n_users;
       if (!uok && leader) atomicOr(p.status, DEV_ERR_MAP_RANGE);
-      if (add_p && users_ready < 0) users_ready = wait_all_user_partials(p) ? 1 : 0;
-      const bool ready = uok && (!add_p || users_ready == 1);
+      if (kPhase != LCE_PHASE_LOCAL && add_p && users_ready < 0) users_ready = wait_all_user_partials(p) ? 1 : 0;
+      // local partials: the walk put this (user, D block)'s own tile just before
+      bool ready = uok && (kPhase == LCE_PHASE_LOCAL || !add_p || users_ready == 1);
+      if (kPhase == LCE_PHASE_LOCAL && ready && (pre_u != u || pre_dblk != x.dblk)) {
+        if (leader) atomicOr(p.status, DEV_ERR_BAD_WORK);
+        ready = false;
+      }
       const float* P = p.partial + static_cast<size_t>(uok ? u : 0) * ND + d;
       if (!add_p && pre_u != -2) {  // decomposed stage: no partial here (a later launch adds it)
         pre_u = -2;
@@ -409,7 +575,7 @@ __device__ void lce_epilogue(const LceParams& p, const LceSmem& s, uint32_t tmem
 #pragma unroll
           for (int j = 0; j < 32; ++j) pre[k][j] = 0.f;
       }
-      if (add_p && ready && (u != pre_u || x.dblk != pre_dblk)) {
+      if (kPhase != LCE_PHASE_LOCAL && add_p && ready && (u != pre_u || x.dblk != pre_dblk)) {
         pre_u = u;
         pre_dblk = x.dblk;
 #pragma unroll
@@ -423,7 +589,7 @@ __device__ void lce_epilogue(const LceParams& p, const LceSmem& s, uint32_t tmem
           }
         }
       }
-      if (!mbar_wait(&s.acc_full[buf], use & 1u, s.abort, p.timeout_ns, 1)) return;
+      if (!warp_wait(&s.acc_full[buf], use & 1u, s, p)) return;
       tc_fence_after();
       if (ready) {
         __nv_bfloat16* Y = reinterpret_cast<__nv_bfloat16*>(p.Y) + static_cast<size_t>(i) * ND + d;
@@ -441,7 +607,7 @@ __device__ void lce_epilogue(const LceParams& p, const LceSmem& s, uint32_t tmem
             y += p.D;
           }
         }
-        for (int c = half + 2 * EPI_PREFETCH; c < nchunks; c += 2) {  // beyond the prefetch (N > 192)
+        for (int c = half + 2 * EPI_PREFETCH; kPhase != LCE_PHASE_LOCAL && c < nchunks; c += 2) {  // N > 192
           uint32_t v[32];
           tmem_ld32(t_acc + c * 32, v);
           float pu[32];
@@ -467,16 +633,16 @@ __device__ void lce_epilogue(const LceParams& p, const LceSmem& s, uint32_t tmem
 // One body, launched either as two kernels -- kPhase LCE_PHASE_USER computes
 // the user tiles (P and their release flags), then LCE_PHASE_CAND the
 // candidate tiles, which acquire the flags and add P in their epilogue -- or
-// as one (LCE_PHASE_BOTH: user tiles first in every CTA's list).  The grid
+// as one (LCE_PHASE_BOTH: user tiles first in every CTA's list;
+// LCE_PHASE_LOCAL: candidate tiles with each CTA's own user partials).  The grid
 // never exceeds the SM count and takes one CTA per SM, so every CTA is
 // resident and a flag wait always ends.
-constexpr int LCE_PHASE_CAND = 0, LCE_PHASE_USER = 1, LCE_PHASE_BOTH = 2;
 template <int kPhase>
 __global__ void __launch_bounds__(LCE_THREADS, 1)
     lce_kernel(const __grid_constant__ CUtensorMap tmU, const __grid_constant__ CUtensorMap tmC,
                const __grid_constant__ CUtensorMap tmWu, const __grid_constant__ CUtensorMap tmWc,
                const LceParams p) {
-  const int u0 = kPhase == LCE_PHASE_CAND ? p.n_user_units : 0;
+  const int u0 = (kPhase == LCE_PHASE_CAND || kPhase == LCE_PHASE_LOCAL) ? p.n_user_units : 0;
   const int u1 = kPhase == LCE_PHASE_USER ? p.n_user_units : p.n_units;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -491,6 +657,10 @@ __global__ void __launch_bounds__(LCE_THREADS, 1)
     for (int i = 0; i < p.w_slots; ++i) {
       mbar_init(&s.w_full[i], 1);
       mbar_init(&s.w_empty[i], 1);
+    }
+    for (int i = 0; i < p.wu_slots; ++i) {
+      mbar_init(&s.wu_full[i], 1);
+      mbar_init(&s.wu_empty[i], 1);
     }
     mbar_init(s.wc_full, 1);
     for (int i = 0; i < 2; ++i) {
@@ -523,13 +693,13 @@ __global__ void __launch_bounds__(LCE_THREADS, 1)
   if (warp < LCE_EPI_WARP0) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 72;");
     if (warp == 0) {
-      if (lane_id() == 0) lce_producer(p, s, &tmU, &tmC, &tmWu, &tmWc, u0, u1);
+      lce_producer<kPhase>(p, s, &tmU, &tmC, &tmWu, &tmWc, u0, u1);
     } else if (warp == 1) {
-      lce_mma(p, s, tmem, u0, u1);
+      lce_mma<kPhase>(p, s, tmem, u0, u1);
     }
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 216;");
-    lce_epilogue(p, s, tmem, u0, u1);
+    lce_epilogue<kPhase>(p, s, tmem, u0, u1);
   }
 
   tc_fence_before();
@@ -560,9 +730,21 @@ bool lce_configure(LceParams* lp, size_t max_smem) {
   const int region_boxes = wc_boxes < 2 ? 2 : wc_boxes;
   lp->w_region_bytes = static_cast<uint32_t>(region_boxes) * BOX_BYTES;
   lp->w_slots = region_boxes < LCE_MAX_W_SLOTS ? region_boxes : LCE_MAX_W_SLOTS;
+  lp->wu_slots = 0;
   lp->stages = LCE_MAX_STAGES;
   while (lp->stages > 2 && lce_smem_bytes(*lp) > max_smem) --lp->stages;
-  return lce_smem_bytes(*lp) <= max_smem;
+  if (lce_smem_bytes(*lp) > max_smem) return false;
+  // the local-partial schedule: a W_u ring after the A ring, which gives up
+  // stages for it (the candidate stream runs as fast on 4 stages as on 8)
+  lp->stages_local = 0;
+  if (lp->N <= LCE_LOCAL_MAX_N) {
+    LceParams q = *lp;
+    q.wu_slots = LCE_WU_SLOTS;
+    q.stages = LCE_MAX_STAGES;
+    while (q.stages > 2 && lce_smem_bytes(q) > max_smem) --q.stages;
+    if (lce_smem_bytes(q) <= max_smem) lp->stages_local = q.stages;
+  }
+  return true;
 }
 
 size_t lce_flag_count(const LceParams& lp) {
@@ -570,8 +752,10 @@ size_t lce_flag_count(const LceParams& lp) {
 }
 
 size_t lce_smem_bytes(const LceParams& p) {
-  const size_t bars = sizeof(uint64_t) * (2 * p.stages + 2 * p.w_slots + 1 + 4 + 1) + 2 * sizeof(uint32_t);
-  return 1024 + p.w_region_bytes + static_cast<size_t>(p.stages) * LCE_A_STAGE_BYTES + bars;
+  const size_t bars =
+      sizeof(uint64_t) * (2 * p.stages + 2 * p.w_slots + 2 * p.wu_slots + 1 + 4 + 1) + 2 * sizeof(uint32_t);
+  return 1024 + p.w_region_bytes + static_cast<size_t>(p.stages) * LCE_A_STAGE_BYTES +
+         static_cast<size_t>(p.wu_slots) * p.NB * BOX_BYTES + bars;
 }
 
 template <int kPhase>
@@ -587,22 +771,34 @@ cudaError_t launch_phase(const CUtensorMap& tmU, const CUtensorMap& tmC, const C
   return cudaGetLastError();
 }
 
-bool lce_one_launch(const LceParams& p, int num_sms, int schedule) {
-  if (schedule == LCE_SCHEDULE_TWO) return false;
-  if (schedule == LCE_SCHEDULE_ONE) return true;
+int lce_resolve_schedule(const LceParams& p, int num_sms) {
+  // local partials need the candidates grouped by user (the plan's order):
+  // in map order a CTA's range could change user at every tile
+  const bool local_ok = p.stages_local >= 2 && p.mode == 0 && p.order != nullptr;
+  if (p.schedule == LCE_SCHEDULE_TWO || p.schedule == LCE_SCHEDULE_ONE) return p.schedule;
+  if (local_ok) return LCE_SCHEDULE_LOCAL;
   // Plan-time choice (measured over the n_cand x ratio sweep): with few
   // candidate tiles per SM, one launch hides the user tiles under the
   // candidate tiles' start-up; with many, two launches keep every
   // candidate epilogue from waiting on user tiles still running elsewhere.
   const long long cand_tiles = static_cast<long long>(p.n_cand) * p.n_dblk;
-  return cand_tiles < static_cast<long long>(LCE_ONE_LAUNCH_TILES_PER_SM) * num_sms;
+  return cand_tiles < static_cast<long long>(LCE_ONE_LAUNCH_TILES_PER_SM) * num_sms ? LCE_SCHEDULE_ONE
+                                                                                    : LCE_SCHEDULE_TWO;
 }
 
 // The user tiles and the candidate tiles: two launches on one stream, or one
-// (see lce_one_launch).  *launches receives the number of launches.
+// (see lce_resolve_schedule).  *launches receives the number of launches.
 cudaError_t launch_lce(const CUtensorMap& tmU, const CUtensorMap& tmC, const CUtensorMap& tmWu,
                        const CUtensorMap& tmWc, const LceParams& p, int num_sms, cudaStream_t s, int* launches) {
-  if (lce_one_launch(p, num_sms, p.schedule)) {
+  const int schedule = lce_resolve_schedule(p, num_sms);
+  if (schedule == LCE_SCHEDULE_LOCAL) {
+    LceParams q = p;
+    q.stages = p.stages_local;
+    q.wu_slots = LCE_WU_SLOTS;
+    *launches = 1;
+    return launch_phase<LCE_PHASE_LOCAL>(tmU, tmC, tmWu, tmWc, q, p.n_units - p.n_user_units, num_sms, s);
+  }
+  if (schedule == LCE_SCHEDULE_ONE) {
     *launches = 1;
     return launch_phase<LCE_PHASE_BOTH>(tmU, tmC, tmWu, tmWc, p, p.n_units, num_sms, s);
   }

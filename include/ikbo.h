@@ -214,11 +214,19 @@ ikbo_status_t ikbo_plan_set_timeout_ns(ikbo_plan_t p, uint64_t timeout_ns);
 
 /* Launch schedule of ikbo_lce_forward (plan-time kernel selection over the
  * shape range, the "compile for a range of shapes" idea of the pages done as
- * a runtime choice): 0 = chosen from the shape (default: one launch when the
- * request has fewer than 8 candidate tiles of 128 D-rows per SM, else two),
- * 1 = two launches (user tiles, then candidate tiles), 2 = one launch (user
- * tiles first in every CTA's list).  Results are identical; only the time
- * differs.  Other values: IKBO_ERR_INVALID_ARG. */
+ * a runtime choice):
+ *   0  chosen from the shape (default): 3 where it applies, else 2 when the
+ *      request has fewer than 8 candidate tiles of 128 D-rows per SM, else 1
+ *   1  two launches: user tiles (fp32 partials in the plan's workspace, with
+ *      release flags), then candidate tiles
+ *   2  one launch: user tiles first in every CTA's list
+ *   3  local partials, one launch: each CTA computes, into TMEM, the partial
+ *      of every (user, 128-row D block) its candidate tiles need and keeps it
+ *      in registers; no workspace and no hand-off between CTAs.  Applies when
+ *      N <= 192 and shared memory holds W_c plus two full-width W_u chunks;
+ *      elsewhere a request for 3 runs as 0.
+ * Results are identical; only the time differs.  Other values:
+ * IKBO_ERR_INVALID_ARG. */
 ikbo_status_t ikbo_plan_set_lce_schedule(ikbo_plan_t p, int schedule);
 
 /* Number of kernel launches the forward calls and ikbo_plan have made

@@ -125,6 +125,7 @@ def test_forced_flag_timeout_returns_error_and_context_survives():
     and the next normal call on the same context is correct."""
     x = gen.make_lce("to", 31, 64, 4, 40, 30, 128, 32, map_kind="permuted")
     with B.Plan(64, 4, 1) as p:
+        p.set_lce_schedule(1)  # the schedule that hands partials between CTAs
         B.ikbo_plan_set_timeout_ns(p.handle, 20_000_000)  # 20 ms
         B.ikbo_plan_set_debug(p.handle, B.DEBUG_WITHHOLD_USER_PARTIAL)
         Y, st = run_lce(x, p)

@@ -78,26 +78,58 @@ def test_lce_stage_argument_and_map_errors():
     dict(n_cand=256, n_users=26, K_u=381, K_c=243, D=256, N=192),
     dict(n_cand=1024, n_users=15, K_u=381, K_c=243, D=256, N=192),
     dict(n_cand=64, n_users=1, K_u=700, K_c=100, D=256, N=192),
+    dict(n_cand=200, n_users=9, K_u=100, K_c=60, D=200, N=104),
+    dict(n_cand=120, n_users=5, K_u=381, K_c=243, D=256, N=200),  # N > 192: no local partials
 ])
 def test_lce_schedules_agree(shape):
-    """One launch and two launches do the same arithmetic per tile: identical Y;
-    the automatic choice is one of them."""
+    """Two launches, one launch and local partials do the same arithmetic per
+    element: identical Y; the automatic choice is one of them.  A request
+    for local partials where they do not apply runs as the automatic one."""
     x = gen.make_lce("sched", 83, map_kind="permuted", **shape)
     U, C, Wu, Wc, b, m = to_dev(x.U, x.C, x.Wu, x.Wc, x.b, x.map)
-    ys = {}
+    ys, launched = {}, {}
     with B.Plan(x.n_cand, x.n_users, 1) as p:
         p.plan(m, x.n_users)
-        for sch in (0, 1, 2):
+        for sch in (0, 1, 2, 3):
             p.set_lce_schedule(sch)
             Y = torch.full((x.n_cand, x.N, x.D), float("nan"), dtype=torch.bfloat16, device="cuda")
             l0 = p.launches()
             p.lce_forward(U, C, Wu, Wc, b, Y)
-            assert p.launches() - l0 == (2 if sch == 1 else 1 if sch == 2 else p.launches() - l0)
+            launched[sch] = p.launches() - l0
             assert p.status() == B.IKBO_OK
             ys[sch] = Y
-        with pytest.raises(B.IkboError):
-            p.set_lce_schedule(3)
+        for bad in (-1, 4):
+            with pytest.raises(B.IkboError):
+                p.set_lce_schedule(bad)
+    assert launched[1] == 2 and launched[2] == 1 and launched[3] in (1, launched[0])
     assert torch.equal(ys[1], ys[2])
+    assert torch.equal(ys[3], ys[1])
     assert torch.equal(ys[0], ys[1])
     sel = sample_candidates(x.map, 12)
-    assert_lce_close(ys[2][sel], oracle.lce(x.map, x.U, x.C, x.Wu, x.Wc, x.b, cands=sel), "one launch")
+    assert_lce_close(ys[3][sel], oracle.lce(x.map, x.U, x.C, x.Wu, x.Wc, x.b, cands=sel), "local partials")
+
+
+@pytest.mark.parametrize("schedule", [1, 2, 3])
+def test_lce_schedules_map_out_of_range(schedule):
+    """A map value out of range: that candidate's rows stay untouched, the
+    status says so, and the candidates around it (same user before and after)
+    are still right -- in the local-partial schedule the bad candidate must
+    not disturb the partial its neighbours share."""
+    x = gen.make_lce("sched_oor", 84, 300, 4, 381, 243, 256, 192)
+    bad = x.map.clone()
+    order = torch.argsort(x.map, stable=True)
+    hits = [int(order[k]) for k in (0, 37, 150, 299)]
+    for i in hits:
+        bad[i] = 4 if i % 2 else -3
+    U, C, Wu, Wc, b, m = to_dev(x.U, x.C, x.Wu, x.Wc, x.b, bad)
+    Y = torch.full((x.n_cand, x.N, x.D), float("nan"), dtype=torch.bfloat16, device="cuda")
+    with B.Plan(x.n_cand, x.n_users, 1) as p:
+        p.set_lce_schedule(schedule)
+        p.plan(m, x.n_users)
+        p.lce_forward(U, C, Wu, Wc, b, Y)
+        assert p.status() == B.IKBO_ERR_MAP_OUT_OF_RANGE
+    for i in hits:
+        assert torch.isnan(Y[i].float()).all()
+    good = [i for i in range(x.n_cand) if i not in hits]
+    sel = sorted(set(good[:8] + good[-8:] + [int(order[k]) for k in (1, 36, 38, 149, 151, 298)]))
+    assert_lce_close(Y[sel], oracle.lce(x.map, x.U, x.C, x.Wu, x.Wc, x.b, cands=sel), f"schedule {schedule}")
