@@ -246,3 +246,11 @@ def attn_ratio_sweep(n_cand: int, ratio: int, seed: int) -> AttnInputs:
     return make_attn(f"attn_sweep_{n_cand}_{ratio}", seed, n_cand=n_cand,
                      n_users=sweep_users(n_cand, ratio), H=8, Lq=16, d=128, Lkv=2048,
                      map_kind="permuted")
+
+
+def make_lce_grad(seed: int, n_cand: int, N: int, D: int) -> torch.Tensor:
+    """Upstream gradient dY = dL/dY for the LCE backward: bf16 [n_cand, N, D]
+    ~ N(0, 1), from its own PCG64 stream (seed + 500, so it never repeats the
+    forward inputs' draws)."""
+    rng = np.random.Generator(np.random.PCG64(seed + 500))
+    return _normal(rng, (n_cand, N, D), 1.0)

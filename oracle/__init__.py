@@ -14,6 +14,10 @@ Parity status per function (the pins are in ``tests/test_oracle_*.py``):
   * ``lce``       -- pinned: the K-axis decomposition identity, exact
     rational brute force on tiny inputs, special cases that reduce to a
     library matmul, permutation and zero-padding invariance;
+  * ``lce_backward`` -- pinned: the adjoint identity <dY, Y(x + dx) - Y(x)>
+    = <grad, dx> against the (separately pinned) forward for each input,
+    torch fp64 autograd on small cases, closed forms (dY = 0, dY = 1, one
+    user), and invariance under candidate permutation;
   * ``attn``      -- pinned: identity map equals torch fp64 SDPA, one user
     equals multi-query SDPA, closed forms (Q=0, constant V, one key, one
     dominant score, empty key range), permutation invariance, jagged slices
@@ -88,9 +92,11 @@ class Oracle:
         lib.ikbo_oracle_segments.argtypes = [p, i, i, i, i, p, p, p, p, ctypes.c_int64, p]
         lib.ikbo_oracle_lce.argtypes = [p, p, p, p, p, p, i, i, i, i, i, i, p, i, p, i]
         lib.ikbo_oracle_attn.argtypes = [p, p, p, p, p, i, i, i, i, i, i, ctypes.c_double, p, i, p, i]
+        lib.ikbo_oracle_lce_backward.argtypes = [p, p, p, p, p, p, i, i, i, i, i, i, p, i, p, i, i,
+                                                 p, p, p, p, p, i]
         lib.ikbo_oracle_max_threads.argtypes = []
         for f in (lib.ikbo_oracle_segments, lib.ikbo_oracle_lce, lib.ikbo_oracle_attn,
-                  lib.ikbo_oracle_max_threads):
+                  lib.ikbo_oracle_lce_backward, lib.ikbo_oracle_max_threads):
             f.restype = ctypes.c_int
         self.lib = lib
         self.path = lib_path
@@ -143,6 +149,36 @@ class Oracle:
                                       n_threads)
         self._check(rc, "lce")
         return Y
+
+    def lce_backward(self, map_, U, C, Wu, Wc, dY, cands: Optional[Sequence[int]] = None,
+                     users: Optional[Sequence[int]] = None, weights: bool = True, n_threads: int = 0) -> dict:
+        """Gradients of the materialised LCE in fp64 for upstream gradient dY [n_cand, N, D]:
+        dC [n_csel, K_c, D] for ``cands`` (all when None), dU [n_usel, K_u, D] for
+        ``users`` (all when None), and, when ``weights``, dWu [K_u, N], dWc [K_c, N],
+        db [N].  Returns a dict of float64 arrays.
+        """
+        m = _i32(map_)
+        n_users, K_u, D = U.shape
+        n_cand, K_c, D2 = C.shape
+        N = Wu.shape[1]
+        assert D2 == D and tuple(Wc.shape) == (K_c, N) and tuple(Wu.shape) == (K_u, N)
+        assert tuple(dY.shape) == (n_cand, N, D)
+        csel = None if cands is None else _i32(cands)
+        usel = None if users is None else _i32(users)
+        n_csel = n_cand if csel is None else csel.shape[0]
+        n_usel = n_users if usel is None else usel.shape[0]
+        out = {"dC": np.zeros((n_csel, K_c, D), np.float64), "dU": np.zeros((n_usel, K_u, D), np.float64),
+               "dWu": np.zeros((K_u, N), np.float64), "dWc": np.zeros((K_c, N), np.float64),
+               "db": np.zeros((N,), np.float64)}
+        rc = self.lib.ikbo_oracle_lce_backward(
+            _ptr(m), _ptr(_bits(U)), _ptr(_bits(C)), _ptr(_bits(Wu)), _ptr(_bits(Wc)), _ptr(_bits(dY)),
+            n_cand, n_users, K_u, K_c, D, N, _ptr(csel), n_csel, _ptr(usel), n_usel, 1 if weights else 0,
+            _ptr(out["dC"]), _ptr(out["dU"]), _ptr(out["dWu"]), _ptr(out["dWc"]), _ptr(out["db"]), n_threads)
+        self._check(rc, "lce_backward")
+        if not weights:
+            for k in ("dWu", "dWc", "db"):
+                out.pop(k)
+        return out
 
     def attn(self, map_, Q, K, V, kv_offsets=None, n_users: Optional[int] = None,
              scale: Optional[float] = None, pairs: Optional[Sequence] = None,
@@ -200,6 +236,10 @@ def lce(*a, **k):
 
 def attn(*a, **k):
     return default().attn(*a, **k)
+
+
+def lce_backward(*a, **k):
+    return default().lce_backward(*a, **k)
 
 
 def max_threads() -> int:

@@ -303,3 +303,109 @@ int ikbo_oracle_attn(const int32_t *map, const uint16_t *Q, const uint16_t *K, c
     }
     return status;
 }
+
+/*
+ * LCE backward (training), from the materialised definition.  The pages say
+ * the IKBO kernels serve training as they are when the candidate:user ratio
+ * exceeds 1 ("Meta Optimizes Inference for Recommendation Systems",
+ * aibriefing, the paragraph on kernels, compilation and runtime); they give
+ * no backward formulas, so this is the chain rule of the forward above:
+ *
+ *   X[i] = [U[map[i]]; C[i]]  (the replicated input, K = K_u + K_c rows)
+ *   Y[i] = W^T X[i] + b,  W = [W_u; W_c]
+ *   given dY[i] = dL/dY[i]:
+ *     dX[i][k][d] = sum_n W[k][n] dY[i][n][d]
+ *     dW[k][n]    = sum_i sum_d X[i][k][d] dY[i][n][d]
+ *     db[n]       = sum_i sum_d dY[i][n][d]
+ *   and the broadcast's own rule: every copy of U[u] passes its gradient back,
+ *     dU[u] = sum_{i : map[i] = u} dX[i][0 .. K_u)
+ *     dC[i] = dX[i][K_u .. K)
+ *   dW_u = dW[0 .. K_u), dW_c = dW[K_u .. K).
+ *
+ * Selections keep the cost bounded: dC for candidates csel[0..n_csel) (all,
+ * in order, when csel is NULL and n_csel == n_cand), dU for users
+ * usel[0..n_usel) (all when usel is NULL and n_usel == n_users), and dW_u,
+ * dW_c, db only when want_w != 0.  Outputs in double: dC[n_csel][K_c][D],
+ * dU[n_usel][K_u][D], dWu[K_u][N], dWc[K_c][N], db[N].  Every sum runs over
+ * candidates in ascending order, then n (or d) ascending.
+ */
+int ikbo_oracle_lce_backward(const int32_t *map, const uint16_t *U, const uint16_t *C,
+                             const uint16_t *Wu, const uint16_t *Wc, const uint16_t *dY,
+                             int n_cand, int n_users, int K_u, int K_c, int D, int N,
+                             const int32_t *csel, int n_csel, const int32_t *usel, int n_usel,
+                             int want_w, double *dC, double *dU, double *dWu, double *dWc,
+                             double *db, int n_threads)
+{
+    if (n_cand < 0 || n_users < 1 || K_u < 0 || K_c < 0 || D < 1 || N < 1 || n_csel < 0 || n_usel < 0)
+        return ORACLE_BAD_ARG;
+    if (!csel && n_csel != n_cand) return ORACLE_BAD_ARG;
+    if (!usel && n_usel != n_users) return ORACLE_BAD_ARG;
+    for (int i = 0; i < n_cand; ++i)
+        if (map[i] < 0 || map[i] >= n_users) return ORACLE_MAP_OUT_OF_RANGE;
+    for (int s = 0; s < n_csel; ++s)
+        if ((csel ? csel[s] : s) < 0 || (csel ? csel[s] : s) >= n_cand) return ORACLE_BAD_ARG;
+    for (int s = 0; s < n_usel; ++s)
+        if ((usel ? usel[s] : s) < 0 || (usel ? usel[s] : s) >= n_users) return ORACLE_BAD_ARG;
+    const int K = K_u + K_c;
+    set_threads(n_threads);
+
+    /* dX[i][K_u + k] for the selected candidates: their dC */
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int s = 0; s < n_csel; ++s) {
+        const int i = csel ? csel[s] : s;
+        for (int k = 0; k < K_c; ++k)
+            for (int d = 0; d < D; ++d) {
+                double acc = 0.0;
+                for (int n = 0; n < N; ++n)
+                    acc += bf16_bits_to_double(Wc[(size_t)k * N + n]) *
+                           bf16_bits_to_double(dY[((size_t)i * N + n) * D + d]);
+                dC[((size_t)s * K_c + k) * D + d] = acc;
+            }
+    }
+
+    /* dU[u]: the user rows of dX[i], summed over every copy of U[u] */
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int s = 0; s < n_usel; ++s) {
+        const int u = usel ? usel[s] : s;
+        double *out = dU + (size_t)s * K_u * D;
+        for (size_t e = 0; e < (size_t)K_u * D; ++e) out[e] = 0.0;
+        for (int i = 0; i < n_cand; ++i) {
+            if (map[i] != u) continue;
+            for (int k = 0; k < K_u; ++k)
+                for (int d = 0; d < D; ++d) {
+                    double acc = 0.0;
+                    for (int n = 0; n < N; ++n)
+                        acc += bf16_bits_to_double(Wu[(size_t)k * N + n]) *
+                               bf16_bits_to_double(dY[((size_t)i * N + n) * D + d]);
+                    out[(size_t)k * D + d] += acc;
+                }
+        }
+    }
+
+    if (!want_w) return ORACLE_OK;
+
+    /* dW[k][n] = sum_i sum_d X[i][k][d] dY[i][n][d], X[i] the replicated input */
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int k = 0; k < K; ++k) {
+        for (int n = 0; n < N; ++n) {
+            double acc = 0.0;
+            for (int i = 0; i < n_cand; ++i) {
+                const uint16_t *xrow = k < K_u ? U + ((size_t)map[i] * K_u + k) * D
+                                               : C + ((size_t)i * K_c + (k - K_u)) * D;
+                const uint16_t *grow = dY + ((size_t)i * N + n) * D;
+                for (int d = 0; d < D; ++d) acc += bf16_bits_to_double(xrow[d]) * bf16_bits_to_double(grow[d]);
+            }
+            if (k < K_u)
+                dWu[(size_t)k * N + n] = acc;
+            else
+                dWc[(size_t)(k - K_u) * N + n] = acc;
+        }
+    }
+    for (int n = 0; n < N; ++n) {
+        double acc = 0.0;
+        for (int i = 0; i < n_cand; ++i)
+            for (int d = 0; d < D; ++d) acc += bf16_bits_to_double(dY[((size_t)i * N + n) * D + d]);
+        db[n] = acc;
+    }
+    return ORACLE_OK;
+}

@@ -127,6 +127,103 @@ LCE_PINS = [pin_lce_decomposition, pin_lce_exact_rational, pin_lce_single_user_n
             pin_lce_zero_padding, pin_lce_selection]
 
 
+# ============================================================ LCE backward
+def _dot(a, b) -> float:
+    return float(np.sum(np.asarray(a, np.float64) * np.asarray(b, np.float64)))
+
+
+def _bwd_case(seed=23, **kw):
+    x = _small_lce(seed=seed, **kw)
+    return x, gen.make_lce_grad(seed, x.n_cand, x.N, x.D)
+
+
+def pin_lce_bwd_adjoint(orc):
+    """The adjoint identity of a linear map: for each input t, with the others
+    fixed, Y is affine in t, so <dY, Y(t = dt) - Y(t = 0)> = <dL/dt, dt>.  The
+    right-hand side uses the backward; the left-hand side only the forward
+    (pinned on its own), evaluated with every other contribution zeroed."""
+    x, dY = _bwd_case()
+    g = orc.lce_backward(x.map, x.U, x.C, x.Wu, x.Wc, dY)
+    rng = np.random.default_rng(3)
+    bf = lambda shape: torch.from_numpy(rng.standard_normal(shape).astype(np.float32)).to(torch.bfloat16)
+    zU, zC = torch.zeros_like(x.U), torch.zeros_like(x.C)
+    dU, dC, dWu, dWc, db = bf(tuple(x.U.shape)), bf(tuple(x.C.shape)), bf(tuple(x.Wu.shape)), bf(tuple(x.Wc.shape)), bf((x.N,))
+    lhs = {
+        "dU": _dot(f64(dY), orc.lce(x.map, dU, zC, x.Wu, x.Wc, None)),
+        "dC": _dot(f64(dY), orc.lce(x.map, zU, dC, x.Wu, x.Wc, None)),
+        "dWu": _dot(f64(dY), orc.lce(x.map, x.U, zC, dWu, x.Wc, None)),
+        "dWc": _dot(f64(dY), orc.lce(x.map, zU, x.C, x.Wu, dWc, None)),
+        "db": _dot(f64(dY), orc.lce(x.map, zU, zC, x.Wu, x.Wc, db)),
+    }
+    rhs = {"dU": _dot(g["dU"], f64(dU)), "dC": _dot(g["dC"], f64(dC)), "dWu": _dot(g["dWu"], f64(dWu)),
+           "dWc": _dot(g["dWc"], f64(dWc)), "db": _dot(g["db"], f64(db))}
+    for k in lhs:
+        assert abs(lhs[k] - rhs[k]) <= 1e-10 * (1 + abs(lhs[k])), (k, lhs[k], rhs[k])
+
+
+def pin_lce_bwd_autograd(orc):
+    """torch fp64 autograd through the materialised forward (U[map] gathered,
+    concatenated with C, one batched matmul, + b) gives every gradient."""
+    x, dY = _bwd_case(seed=29, n_cand=11, n_users=4)
+    g = orc.lce_backward(x.map, x.U, x.C, x.Wu, x.Wc, dY)
+    t = {k: torch.tensor(f64(v), requires_grad=True) for k, v in
+         dict(U=x.U, C=x.C, Wu=x.Wu, Wc=x.Wc, b=x.b).items()}
+    Xrep = torch.cat([t["U"][x.map.long()], t["C"]], dim=1)
+    W = torch.cat([t["Wu"], t["Wc"]], dim=0)
+    Y = torch.matmul(W.t().unsqueeze(0), Xrep) + t["b"][None, :, None]
+    (Y * torch.tensor(f64(dY))).sum().backward()
+    for mine, ref in (("dU", "U"), ("dC", "C"), ("dWu", "Wu"), ("dWc", "Wc"), ("db", "b")):
+        np.testing.assert_allclose(g[mine], t[ref].grad.numpy(), rtol=1e-11, atol=1e-11, err_msg=mine)
+
+
+def pin_lce_bwd_closed_forms(orc):
+    """dY = 0 gives zero gradients.  dY = 1 gives db[n] = n_cand * D,
+    dWc[k][n] = sum_{i,d} C[i][k][d] (the same for every n),
+    dU[u][k][d] = count_u * sum_n Wu[k][n] (0 for a user with no candidates),
+    dC[i][k][d] = sum_n Wc[k][n]."""
+    x = gen.make_lce("pin", 31, 7, 4, 3, 5, 6, 4, explicit_map=[0, 2, 2, 0, 2, 0, 0], w_var=0.3)
+    z = orc.lce_backward(x.map, x.U, x.C, x.Wu, x.Wc, torch.zeros(x.n_cand, x.N, x.D, dtype=torch.bfloat16))
+    for k, v in z.items():
+        assert not np.any(v), k
+    g = orc.lce_backward(x.map, x.U, x.C, x.Wu, x.Wc, torch.ones(x.n_cand, x.N, x.D, dtype=torch.bfloat16))
+    np.testing.assert_allclose(g["db"], np.full(x.N, x.n_cand * x.D, np.float64), rtol=0, atol=0)
+    csum = f64(x.C).sum(axis=(0, 2))
+    np.testing.assert_allclose(g["dWc"], np.repeat(csum[:, None], x.N, 1), rtol=1e-13, atol=1e-13)
+    counts = np.bincount(x.map.numpy(), minlength=x.n_users)
+    wsum = f64(x.Wu).sum(axis=1)
+    for u in range(x.n_users):
+        np.testing.assert_allclose(g["dU"][u], counts[u] * np.repeat(wsum[:, None], x.D, 1), rtol=1e-13, atol=1e-13)
+    wcs = f64(x.Wc).sum(axis=1)
+    for i in range(x.n_cand):
+        np.testing.assert_allclose(g["dC"][i], np.repeat(wcs[:, None], x.D, 1), rtol=1e-13, atol=1e-13)
+
+
+def pin_lce_bwd_permutation(orc):
+    """Permuting candidates (map, C and dY together) permutes dC and leaves
+    dU, dWu, dWc and db unchanged."""
+    x, dY = _bwd_case(seed=37, n_cand=12, n_users=4)
+    g = orc.lce_backward(x.map, x.U, x.C, x.Wu, x.Wc, dY)
+    p = torch.from_numpy(np.random.default_rng(8).permutation(x.n_cand))
+    gp = orc.lce_backward(x.map[p], x.U, x.C[p], x.Wu, x.Wc, dY[p])
+    assert np.array_equal(gp["dC"], g["dC"][p.numpy()])
+    for k in ("dU", "dWu", "dWc", "db"):
+        np.testing.assert_allclose(gp[k], g[k], rtol=1e-12, atol=1e-12, err_msg=k)
+
+
+def pin_lce_bwd_selection(orc):
+    """Selected candidates and users return exactly those rows."""
+    x, dY = _bwd_case(seed=41)
+    g = orc.lce_backward(x.map, x.U, x.C, x.Wu, x.Wc, dY)
+    s = orc.lce_backward(x.map, x.U, x.C, x.Wu, x.Wc, dY, cands=[5, 0, 5], users=[2, 0], weights=False)
+    assert np.array_equal(s["dC"], g["dC"][[5, 0, 5]])
+    assert np.array_equal(s["dU"], g["dU"][[2, 0]])
+    assert set(s) == {"dC", "dU"}
+
+
+LCE_BWD_PINS = [pin_lce_bwd_adjoint, pin_lce_bwd_autograd, pin_lce_bwd_closed_forms, pin_lce_bwd_permutation,
+                pin_lce_bwd_selection]
+
+
 # ================================================================ attention
 def _sdpa64(q, k, v, scale=None):
     return F.scaled_dot_product_attention(q.to(torch.float64), k.to(torch.float64),

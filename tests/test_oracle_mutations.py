@@ -6,7 +6,7 @@ import os
 import pytest
 
 import oracle
-from oracle_pins import ATTN_PINS, LCE_PINS, SEG_PINS
+from oracle_pins import ATTN_PINS, LCE_BWD_PINS, LCE_PINS, SEG_PINS
 
 MUTATIONS = {
     # LCE
@@ -18,6 +18,17 @@ MUTATIONS = {
                          "W[(size_t)(K_u + k) * N + n] = bf16_bits_to_double(Wc[((size_t)k * N + n) % ((size_t)K_c * N) / K_c + ((size_t)k * N + n) % K_c * N]);", LCE_PINS),
     "lce_user_rows_from_candidate": ("X[(size_t)k * D + d] = bf16_bits_to_double(U[((size_t)u * K_u + k) * D + d]);",
                                      "X[(size_t)k * D + d] = bf16_bits_to_double(U[((size_t)(u ? 0 : u) * K_u + k) * D + d]);", LCE_PINS),
+    # LCE backward
+    "bwd_dc_uses_wu": ("acc += bf16_bits_to_double(Wc[(size_t)k * N + n]) *\n                           bf16_bits_to_double(dY[((size_t)i * N + n) * D + d]);\n                dC",
+                       "acc += bf16_bits_to_double(Wu[(size_t)k * N + n]) *\n                           bf16_bits_to_double(dY[((size_t)i * N + n) * D + d]);\n                dC", LCE_BWD_PINS),
+    "bwd_du_every_candidate": ("if (map[i] != u) continue;", "if (map[i] < 0) continue;", LCE_BWD_PINS),
+    "bwd_dw_user_rows_not_broadcast": ("const uint16_t *xrow = k < K_u ? U + ((size_t)map[i] * K_u + k) * D",
+                                       "const uint16_t *xrow = k < K_u ? U + ((size_t)(i % n_users) * K_u + k) * D", LCE_BWD_PINS),
+    "bwd_db_drop_last_d": ("for (int d = 0; d < D; ++d) acc += bf16_bits_to_double(dY[((size_t)i * N + n) * D + d]);",
+                           "for (int d = 0; d < D - 1; ++d) acc += bf16_bits_to_double(dY[((size_t)i * N + n) * D + d]);", LCE_BWD_PINS),
+    "bwd_dwc_sign": ("dWc[(size_t)(k - K_u) * N + n] = acc;", "dWc[(size_t)(k - K_u) * N + n] = -acc;", LCE_BWD_PINS),
+    "bwd_dc_drop_last_n": ("for (int n = 0; n < N; ++n)\n                    acc += bf16_bits_to_double(Wc",
+                           "for (int n = 0; n < N - 1; ++n)\n                    acc += bf16_bits_to_double(Wc", LCE_BWD_PINS),
     # attention
     "attn_no_scale": ("sc[j] = scale * dot;", "sc[j] = dot;", ATTN_PINS),
     "attn_no_normalise": ("for (int c = 0; c < d; ++c) orow[c] /= l;", "", ATTN_PINS),

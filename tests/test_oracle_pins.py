@@ -4,12 +4,17 @@ import pytest
 import torch
 
 import oracle
-from oracle_pins import ATTN_PINS, LCE_PINS, SEG_PINS
+from oracle_pins import ATTN_PINS, LCE_BWD_PINS, LCE_PINS, SEG_PINS
 from broadcast_gemm_attention_gb300 import inputs as gen
 
 
 @pytest.mark.parametrize("pin", LCE_PINS, ids=lambda f: f.__name__)
 def test_lce_pin(orc, pin):
+    pin(orc)
+
+
+@pytest.mark.parametrize("pin", LCE_BWD_PINS, ids=lambda f: f.__name__)
+def test_lce_backward_pin(orc, pin):
     pin(orc)
 
 
