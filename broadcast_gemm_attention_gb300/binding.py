@@ -42,6 +42,7 @@ SIGNATURES = {
     "ikbo_lce_forward": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp]),
     "ikbo_lce_forward_staged": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp]),
     "ikbo_lce_forward_noalloc": (_i, [_vp, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp]),
+    "ikbo_lce_backward": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp]),
     "ikbo_attn_forward": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, ctypes.c_float, _vp]),
     "ikbo_attn_self_target_forward": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, ctypes.c_float, _vp]),
     "ikbo_plan_get_status": (_i, [_vp, _vp]),
@@ -158,6 +159,33 @@ def ikbo_lce_forward(plan: int, U: torch.Tensor, C: torch.Tensor, Wu: torch.Tens
         bptr = _dev(b, bf, "b")
     _check(load().ikbo_lce_forward(plan, _dev(U, bf, "U"), _dev(C, bf, "C"), _dev(Wu, bf, "Wu"), _dev(Wc, bf, "Wc"),
                                    bptr, _dev(Y, bf, "Y"), K_u, K_c, D, N, _stream(stream)), "ikbo_lce_forward")
+
+
+def ikbo_lce_backward(plan: int, U: torch.Tensor, C: torch.Tensor, Wu: torch.Tensor, Wc: torch.Tensor,
+                      dY: torch.Tensor, dU: Optional[torch.Tensor], dC: Optional[torch.Tensor],
+                      dWu: Optional[torch.Tensor], dWc: Optional[torch.Tensor], db: Optional[torch.Tensor],
+                      stream=None) -> None:
+    """Gradients of the LCE for upstream dY (any output may be None to skip it):
+    dU/dC bf16, dWu/dWc/db fp32, all overwritten."""
+    bf, f32 = torch.bfloat16, torch.float32
+    n_users, K_u, D = U.shape
+    n_cand, K_c, D2 = C.shape
+    N = Wu.shape[1]
+    if D2 != D or tuple(Wu.shape) != (K_u, N) or tuple(Wc.shape) != (K_c, N) or tuple(dY.shape) != (n_cand, N, D):
+        raise ValueError("inconsistent LCE shapes")
+    want = {"dU": (dU, (n_users, K_u, D), bf), "dC": (dC, (n_cand, K_c, D), bf), "dWu": (dWu, (K_u, N), f32),
+            "dWc": (dWc, (K_c, N), f32), "db": (db, (N,), f32)}
+    ptrs = {}
+    for name, (t, shape, dt) in want.items():
+        if t is None:
+            ptrs[name] = None
+            continue
+        if tuple(t.shape) != shape:
+            raise ValueError(f"{name} must be {list(shape)}")
+        ptrs[name] = _dev(t, dt, name)
+    _check(load().ikbo_lce_backward(plan, _dev(U, bf, "U"), _dev(C, bf, "C"), _dev(Wu, bf, "Wu"), _dev(Wc, bf, "Wc"),
+                                    _dev(dY, bf, "dY"), ptrs["dU"], ptrs["dC"], ptrs["dWu"], ptrs["dWc"], ptrs["db"],
+                                    K_u, K_c, D, N, _stream(stream)), "ikbo_lce_backward")
 
 
 def ikbo_lce_forward_staged(plan: int, U: torch.Tensor, C: torch.Tensor, Wu: torch.Tensor, Wc: torch.Tensor,
@@ -295,6 +323,9 @@ class Plan:
 
     def lce_forward(self, U, C, Wu, Wc, b, Y, stream=None):
         ikbo_lce_forward(self.handle, U, C, Wu, Wc, b, Y, stream)
+
+    def lce_backward(self, U, C, Wu, Wc, dY, dU=None, dC=None, dWu=None, dWc=None, db=None, stream=None):
+        ikbo_lce_backward(self.handle, U, C, Wu, Wc, dY, dU, dC, dWu, dWc, db, stream)
 
     def lce_forward_staged(self, U, C, Wu, Wc, b, Y, stage, stream=None):
         ikbo_lce_forward_staged(self.handle, U, C, Wu, Wc, b, Y, stage, stream)

@@ -25,6 +25,16 @@ cudaError_t launch_lce_stage(const CUtensorMap& tmU, const CUtensorMap& tmC, con
 size_t attn_smem_bytes();
 cudaError_t launch_attn(const CUtensorMap& tmQ, const CUtensorMap& tmQu, const CUtensorMap& tmK,
                         const CUtensorMap& tmV, const AttnParams& p, int grid, cudaStream_t s);
+int bwd_segsum_chunks(int n_cand, int n_users, int ND, int num_sms);
+cudaError_t launch_bwd_segsum(const SegSumParams& p, cudaStream_t s, int* launches);
+cudaError_t launch_bwd_db(const float* S, float* db, int n_users, int N, int D, cudaStream_t s);
+bool bwd_act_configure(ActParams* p, size_t max_smem, bool pair);
+cudaError_t launch_bwd_act(const CUtensorMap& tmX, const CUtensorMap& tmW, const ActParams& p, int num_sms,
+                           cudaStream_t s);
+bool bwd_wgrad_configure(WgradParams* p, int num_sms, size_t max_smem);
+size_t bwd_wgrad_part_elems(const WgradParams& p);
+cudaError_t launch_bwd_wgrad(const CUtensorMap& tmA, const CUtensorMap& tmG, const WgradParams& p, float* dW,
+                             int num_sms, cudaStream_t s, int* launches);
 }  // namespace ikbo
 
 using namespace ikbo;
@@ -50,6 +60,15 @@ struct ikbo_plan_s {
   size_t partial_elems = 0;
   uint32_t* d_flags = nullptr;
   size_t flags_elems = 0;
+  // LCE backward workspaces (grown on first use)
+  float* d_bwd_S = nullptr;
+  size_t bwd_S_elems = 0;
+  uint16_t* d_bwd_Sb = nullptr;
+  size_t bwd_Sb_elems = 0;
+  float* d_bwd_seg = nullptr;
+  size_t bwd_seg_elems = 0;
+  float* d_bwd_wpart = nullptr;
+  size_t bwd_wpart_elems = 0;
   uint32_t epoch = 0;
   uint32_t debug = 0;
   uint64_t timeout_ns = 2000000000ull;
@@ -122,6 +141,10 @@ void free_plan(ikbo_plan_t p) {
   cudaFree(p->d_status);
   cudaFree(p->d_partial);
   cudaFree(p->d_flags);
+  cudaFree(p->d_bwd_S);
+  cudaFree(p->d_bwd_Sb);
+  cudaFree(p->d_bwd_seg);
+  cudaFree(p->d_bwd_wpart);
   delete p;
 }
 
@@ -264,7 +287,7 @@ ikbo_status_t attn_launch(ikbo_plan_t p, const void* Q, const void* Q_user, cons
 
 extern "C" {
 
-int ikbo_version(void) { return 103; }
+int ikbo_version(void) { return 104; }
 
 const char* ikbo_status_string(ikbo_status_t s) {
   switch (s) {
@@ -430,6 +453,142 @@ ikbo_status_t ikbo_lce_forward_staged(ikbo_plan_t p, const void* U, const void* 
   return lce_launch(p, U, C, Wu, Wc, b, Y, K_u, K_c, D, N, stage, stream);
 }
 
+
+ikbo_status_t ikbo_lce_backward(ikbo_plan_t p, const void* U, const void* C, const void* Wu, const void* Wc,
+                                const void* dY, void* dU, void* dC, float* dWu, float* dWc, float* db, int K_u,
+                                int K_c, int D, int N, cudaStream_t stream) {
+  if (!p) return IKBO_ERR_INVALID_ARG;
+  if (!p->planned) return IKBO_ERR_NOT_PLANNED;
+  if (!dY || (dU && !Wu) || (dC && !Wc) || (dWu && !U) || (dWc && !C)) return IKBO_ERR_INVALID_ARG;
+  const void* ptrs[] = {U, C, Wu, Wc, dY, dU, dC, dWu, dWc, db};
+  for (const void* q : ptrs)
+    if (q && !aligned16(q)) return IKBO_ERR_INVALID_ARG;
+  if (K_u < 1 || K_c < 1 || D < 1 || N < 1) return IKBO_ERR_UNSUPPORTED;
+  if (D % 8 != 0 || N % 8 != 0 || N > 256) return IKBO_ERR_UNSUPPORTED;
+  const int n_cand = p->n_cand, n_users = p->n_users;
+
+  // configure every product that is asked for before launching anything
+  ActParams ac{}, au{};
+  WgradParams wc{}, wu{};
+  ac.B = n_cand, ac.M = K_c, ac.D = D, ac.N = N;
+  au.B = n_users, au.M = K_u, au.D = D, au.N = N;
+  wc.B = n_cand, wc.M = K_c, wc.D = D, wc.N = N;
+  wu.M = K_u, wu.D = D, wu.N = N;
+  wu.B = 2 * n_users;  // G = the hi/lo pair of S per user; A = U[b >> 1]
+  wu.a_shift = 1;
+  if ((dC && !bwd_act_configure(&ac, p->max_smem, false)) || (dU && !bwd_act_configure(&au, p->max_smem, true)) ||
+      (dWc && !bwd_wgrad_configure(&wc, p->num_sms, p->max_smem)) ||
+      (dWu && !bwd_wgrad_configure(&wu, p->num_sms, p->max_smem)))
+    return IKBO_ERR_UNSUPPORTED;
+
+  const bool need_S = dU || dWu || db;
+  const int ND = N * D;
+  const int NP = (N + 63) / 64 * 64;  // rows per half of the hi/lo pair
+  SegSumParams sp{};
+  if (need_S) {
+    sp.nch = bwd_segsum_chunks(n_cand, n_users, ND, p->num_sms);
+    sp.slices = (ND + BWD_SEG_SLICE - 1) / BWD_SEG_SLICE;
+    sp.NPD = NP * D;
+    const size_t nS = static_cast<size_t>(n_users) * ND;
+    if (grow(&p->d_bwd_S, &p->bwd_S_elems, nS) != cudaSuccess ||
+        grow(&p->d_bwd_Sb, &p->bwd_Sb_elems, static_cast<size_t>(n_users) * 2 * NP * D) != cudaSuccess)
+      return IKBO_ERR_CUDA;
+    if (sp.nch > 1 && grow(&p->d_bwd_seg, &p->bwd_seg_elems, nS * sp.nch) != cudaSuccess) return IKBO_ERR_CUDA;
+  }
+  size_t wpart = 0;
+  if (dWc) wpart = bwd_wgrad_part_elems(wc);
+  if (dWu && bwd_wgrad_part_elems(wu) > wpart) wpart = bwd_wgrad_part_elems(wu);
+  if (wpart && grow(&p->d_bwd_wpart, &p->bwd_wpart_elems, wpart) != cudaSuccess) return IKBO_ERR_CUDA;
+
+  // tensor maps: [B][rows][D] operands with 64-wide boxes along D (rows 64 or
+  // 128 high), and the weights as [M][N] with 64-wide boxes along N
+  const uint64_t dyd[3] = {static_cast<uint64_t>(D), static_cast<uint64_t>(N), static_cast<uint64_t>(n_cand)};
+  const uint64_t dys[2] = {static_cast<uint64_t>(D) * 2, static_cast<uint64_t>(N) * D * 2};
+  // S2 [n_users][2][NP][D]: as X of dU, 2 * NP rows per user; as G of dWu,
+  // NP rows per (user, half)
+  const uint64_t s2x[3] = {static_cast<uint64_t>(D), static_cast<uint64_t>(2 * NP), static_cast<uint64_t>(n_users)};
+  const uint64_t s2xs[2] = {static_cast<uint64_t>(D) * 2, static_cast<uint64_t>(2 * NP) * D * 2};
+  const uint64_t s2g[3] = {static_cast<uint64_t>(D), static_cast<uint64_t>(NP), static_cast<uint64_t>(2 * n_users)};
+  const uint64_t s2gs[2] = {static_cast<uint64_t>(D) * 2, static_cast<uint64_t>(NP) * D * 2};
+  const uint32_t box64[3] = {64, 64, 1};
+  const uint32_t box128[3] = {64, 128, 1};
+  const uint32_t wbox[2] = {64, 128};
+  CUtensorMap tmDY, tmSX, tmSG, tmWc, tmWu, tmC, tmU;
+  if (!encode_bf16(&tmDY, dY, 3, dyd, dys, box64)) return IKBO_ERR_CUDA;
+  if (need_S && (!encode_bf16(&tmSX, p->d_bwd_Sb, 3, s2x, s2xs, box64) ||
+                 !encode_bf16(&tmSG, p->d_bwd_Sb, 3, s2g, s2gs, box64)))
+    return IKBO_ERR_CUDA;
+  if (dC) {
+    const uint64_t wd[2] = {static_cast<uint64_t>(N), static_cast<uint64_t>(K_c)};
+    const uint64_t ws[1] = {static_cast<uint64_t>(N) * 2};
+    if (!encode_bf16(&tmWc, Wc, 2, wd, ws, wbox)) return IKBO_ERR_CUDA;
+  }
+  if (dU) {
+    const uint64_t wd[2] = {static_cast<uint64_t>(N), static_cast<uint64_t>(K_u)};
+    const uint64_t ws[1] = {static_cast<uint64_t>(N) * 2};
+    if (!encode_bf16(&tmWu, Wu, 2, wd, ws, wbox)) return IKBO_ERR_CUDA;
+  }
+  if (dWc) {
+    const uint64_t cd[3] = {static_cast<uint64_t>(D), static_cast<uint64_t>(K_c), static_cast<uint64_t>(n_cand)};
+    const uint64_t cs[2] = {static_cast<uint64_t>(D) * 2, static_cast<uint64_t>(K_c) * D * 2};
+    if (!encode_bf16(&tmC, C, 3, cd, cs, box128)) return IKBO_ERR_CUDA;
+  }
+  if (dWu) {
+    const uint64_t ud[3] = {static_cast<uint64_t>(D), static_cast<uint64_t>(K_u), static_cast<uint64_t>(n_users)};
+    const uint64_t us[2] = {static_cast<uint64_t>(D) * 2, static_cast<uint64_t>(K_u) * D * 2};
+    if (!encode_bf16(&tmU, U, 3, ud, us, box128)) return IKBO_ERR_CUDA;
+  }
+
+  int launches = 0;
+  cudaError_t e = cudaSuccess;
+  if (need_S) {
+    sp.dY = static_cast<const uint16_t*>(dY);
+    sp.offsets = p->d_offsets;
+    sp.perm = p->d_perm;
+    sp.S = p->d_bwd_S;
+    sp.S2 = p->d_bwd_Sb;
+    // rows N .. NP-1 of each half must read as zeros
+    if (NP != N)
+      e = cudaMemsetAsync(p->d_bwd_Sb, 0, sizeof(uint16_t) * static_cast<size_t>(n_users) * 2 * NP * D, stream);
+    sp.part = p->d_bwd_seg;
+    sp.n_cand = n_cand;
+    sp.n_users = n_users;
+    sp.ND = ND;
+    if (e == cudaSuccess) e = launch_bwd_segsum(sp, stream, &launches);
+  }
+  if (e == cudaSuccess && db) {
+    e = launch_bwd_db(p->d_bwd_S, db, n_users, N, D, stream);
+    if (e == cudaSuccess) ++launches;
+  }
+  if (e == cudaSuccess && dC) {
+    ac.out = static_cast<uint16_t*>(dC);
+    ac.status = p->d_status;
+    ac.timeout_ns = p->timeout_ns;
+    e = launch_bwd_act(tmDY, tmWc, ac, p->num_sms, stream);
+    if (e == cudaSuccess) ++launches;
+  }
+  if (e == cudaSuccess && dWc) {
+    wc.part = p->d_bwd_wpart;
+    wc.status = p->d_status;
+    wc.timeout_ns = p->timeout_ns;
+    e = launch_bwd_wgrad(tmC, tmDY, wc, dWc, p->num_sms, stream, &launches);
+  }
+  if (e == cudaSuccess && dU) {
+    au.out = static_cast<uint16_t*>(dU);
+    au.status = p->d_status;
+    au.timeout_ns = p->timeout_ns;
+    e = launch_bwd_act(tmSX, tmWu, au, p->num_sms, stream);
+    if (e == cudaSuccess) ++launches;
+  }
+  if (e == cudaSuccess && dWu) {
+    wu.part = p->d_bwd_wpart;
+    wu.status = p->d_status;
+    wu.timeout_ns = p->timeout_ns;
+    e = launch_bwd_wgrad(tmU, tmSG, wu, dWu, p->num_sms, stream, &launches);
+  }
+  p->launches += static_cast<uint64_t>(launches);
+  return e == cudaSuccess ? IKBO_OK : IKBO_ERR_CUDA;
+}
 
 ikbo_status_t ikbo_attn_forward(ikbo_plan_t p, const void* Q, const void* K, const void* V,
                                 const int32_t* d_kv_offsets, void* O, int Lkv, int d, float scale,

@@ -116,6 +116,68 @@ int lce_resolve_schedule(const LceParams& lp, int num_sms);
 size_t lce_flag_count(const LceParams& lp);
 size_t lce_smem_bytes(const LceParams& lp);
 
+// -------------------------------------------------------- LCE backward
+// S[u] = sum of dY over user u's candidates (the broadcast's transpose).
+// 128 threads x 8 elements per CTA slice; a user's segment may be split
+// into nch chunks whose fp32 partial sums a second pass adds in order.  For
+// the tensor-core products S is kept as a bf16 pair, hi = bf16(S) and
+// lo = bf16(S - hi) (16 significant bits), in S2[u][hi, lo][NP][D] with
+// NP = ceil(N / 64) * 64 rows per half (rows N .. NP-1 are zero).
+constexpr int BWD_SEG_THREADS = 128;
+constexpr int BWD_SEG_SLICE = BWD_SEG_THREADS * 8;
+
+struct SegSumParams {
+  const uint16_t* dY;        // [n_cand][N][D] bf16
+  const int32_t* offsets;    // [n_users + 1] (the plan's)
+  const int32_t* perm;       // [n_cand] candidates grouped by user (the plan's)
+  float* S;                  // [n_users][N][D] fp32
+  uint16_t* S2;              // [n_users][2][NP][D] bf16: hi, lo
+  float* part;               // [n_users * nch][N][D] fp32 when nch > 1
+  int n_cand, n_users, ND, NPD, nch, slices;   // NPD = NP * D
+};
+
+// Activation-gradient GEMM: out[b][m][d] = sum_n W[m][n] X[b][n][d] (dC from
+// dY and W_c, dU from S and W_u).  Tile = (b, 128-row block of D) over all m:
+// M = 128 d rows on TMEM lanes, N = m in ranges of <= 256 columns, K = n.
+// X chunks stream (MN-major, as the forward's C); W stays resident (K-major).
+// X may hold kcx = 2 * kc chunks per b (the hi and lo halves of S2): X chunk
+// j multiplies W chunk j % kc.
+constexpr int BWD_THREADS = 384;       // warp 0 TMA, 1 MMA, 2 TMEM, 3 idle, 4-11 epilogue
+constexpr int BWD_ACT_MAX_STAGES = 4;  // X ring depth: 4, or fewer (>= 2) when W leaves less room
+
+struct ActParams {
+  uint16_t* out;             // [B][M][D] bf16
+  uint32_t* status;
+  int B, M, D, N;
+  int n_dblk;                // ceil(D / 128)
+  int kc;                    // ceil(N / 64): resident W chunks
+  int kcx;                   // X chunks per b (kc, or 2 * kc for a hi/lo pair)
+  int m_pad;                 // roundup(M, 16): accumulator columns
+  int m_rows;                // roundup(M, 128): resident W rows per K chunk
+  int bufs;                  // accumulator buffers (2 when m_pad <= 256)
+  int stages;                // X ring depth
+  uint64_t timeout_ns;
+};
+
+// Weight-gradient GEMM, split along K = (b, d): unit (m block, b range)
+// accumulates A[b][m][d] G[b][n][d] over its b range into TMEM (M = 128 m
+// rows, N = n, both operands K-major) and writes an fp32 partial; a reduce
+// pass adds the partials of each m block in order.
+constexpr int BWD_WG_STAGES = 4;
+
+struct WgradParams {
+  float* part;               // [n_units][128][N] fp32
+  uint32_t* status;
+  int B, M, D, N;            // B = batches of G; A's batch is b >> a_shift
+  int a_shift;               // 1 when G holds a hi/lo pair per batch of A
+  int n_mblk;                // ceil(M / 128)
+  int R;                     // b ranges per m block (n_units = n_mblk * R)
+  int dc;                    // ceil(D / 64)
+  int n_mma;                 // roundup(N, 16)
+  int nb;                    // ceil(n_mma / 64): 64-row boxes of G per chunk
+  uint64_t timeout_ns;
+};
+
 // ----------------------------------------------------------- attention
 constexpr int ATT_BM = 128;        // query rows per tile (TMEM lanes)
 constexpr int ATT_BN = 128;        // keys per K/V tile

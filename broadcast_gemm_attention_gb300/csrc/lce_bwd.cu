@@ -1,0 +1,644 @@
+// lce_bwd.cu -- LCE backward (training) with the broadcast kept implicit.
+//
+// The IKBO write-ups state that the same kernels serve training when the
+// candidate:user ratio exceeds 1 ("Meta Optimizes Inference for
+// Recommendation Systems", the paragraph on kernels, compilation and
+// runtime).  The backward of Y[i] = W_u^T U[map[i]] + W_c^T C[i] + b is the
+// forward's Type I split run in reverse: the transpose of "broadcast U[u] to
+// every candidate of u" is "sum the gradients of u's candidates", so the user
+// side never sees n_cand either:
+//   S[u]  = sum_{i : map[i] = u} dY[i]          segment sum (fp32), n_users rows
+//   db[n] = sum_u sum_d S[u][n][d]
+//   dU[u] = W_u S[u]        dW_u = sum_u U[u] S[u]^T     (at n_users)
+//   dC[i] = W_c dY[i]       dW_c = sum_i C[i] dY[i]^T    (at n_cand)
+// S is rounded to bf16 for the two tensor-core products that read it.
+//
+// Kernels:
+//   bwd_segsum_kernel / bwd_segsum_finish_kernel  S (HBM-bound reduction)
+//   bwd_db_kernel                                 db from S
+//   bwd_act_kernel     out[b][m][d] = sum_n W[m][n] X[b][n][d]   (dC, dU)
+//   bwd_wgrad_kernel   split-K partials of sum_b sum_d A[b][m][d] G[b][n][d]
+//   bwd_wgrad_reduce_kernel                       (dW_c, dW_u)
+// The two GEMM kernels are persistent, one CTA per SM, warp-specialised like
+// the forward: warp 0 TMA (elected lane issues), warp 1 tcgen05.mma (elected
+// lane), warp 2 TMEM owner, warps 4-11 epilogue.  Every wait is bounded.
+#include <cuda_bf16.h>
+
+#include "ikbo_internal.h"
+#include "ptx.cuh"
+
+namespace ikbo {
+
+namespace {
+
+constexpr uint32_t BOX = 64 * 64 * 2;  // one 64 x 64 bf16 box, 8 KB
+
+// ------------------------------------------------------------ segment sum
+// S2[u][0][.] = bf16(S), S2[u][1][.] = bf16(S - bf16(S)) for 8 elements at e.
+__device__ __forceinline__ void store_pair(const SegSumParams& p, int u, int e, const float (&acc)[8]) {
+  uint32_t hi[4], lo[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    hi[j] = pack_bf16x2(acc[2 * j], acc[2 * j + 1]);
+    lo[j] = pack_bf16x2(acc[2 * j] - __uint_as_float(hi[j] << 16),
+                        acc[2 * j + 1] - __uint_as_float(hi[j] & 0xffff0000u));
+  }
+  uint16_t* base = p.S2 + static_cast<size_t>(u) * 2 * p.NPD + e;
+  *reinterpret_cast<uint4*>(base) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+  *reinterpret_cast<uint4*>(base + p.NPD) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+}
+
+// Task = (user u, chunk c of u's segment, slice s of the N*D elements); each
+// thread sums 8 consecutive elements (one 16-byte load per candidate) over
+// the chunk's candidates in ascending perm order, four loads in flight.
+__global__ void __launch_bounds__(BWD_SEG_THREADS) bwd_segsum_kernel(const SegSumParams p) {
+  const int task = blockIdx.x;
+  const int s = task % p.slices;
+  const int uc = task / p.slices;
+  const int c = uc % p.nch;
+  const int u = uc / p.nch;
+  const int e = s * BWD_SEG_SLICE + static_cast<int>(threadIdx.x) * 8;
+  if (u >= p.n_users || e >= p.ND) return;
+  const int p0 = __ldg(p.offsets + u), cnt = __ldg(p.offsets + u + 1) - p0;
+  const int q0 = p0 + static_cast<int>(static_cast<long long>(cnt) * c / p.nch);
+  const int q1 = p0 + static_cast<int>(static_cast<long long>(cnt) * (c + 1) / p.nch);
+  float acc[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) acc[j] = 0.f;
+  auto add = [&](const uint4& v) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      acc[2 * j] += __uint_as_float(w[j] << 16);
+      acc[2 * j + 1] += __uint_as_float(w[j] & 0xffff0000u);
+    }
+  };
+  auto row = [&](int q) -> const uint4* {
+    int i = __ldg(p.perm + q);
+    i = (i >= 0 && i < p.n_cand) ? i : -1;
+    return i < 0 ? nullptr : reinterpret_cast<const uint4*>(p.dY + static_cast<size_t>(i) * p.ND + e);
+  };
+  const uint4 zero = make_uint4(0, 0, 0, 0);
+  int q = q0;
+  for (; q + 4 <= q1; q += 4) {
+    const uint4* r0 = row(q);
+    const uint4* r1 = row(q + 1);
+    const uint4* r2 = row(q + 2);
+    const uint4* r3 = row(q + 3);
+    const uint4 v0 = r0 ? __ldcs(r0) : zero, v1 = r1 ? __ldcs(r1) : zero;
+    const uint4 v2 = r2 ? __ldcs(r2) : zero, v3 = r3 ? __ldcs(r3) : zero;
+    add(v0);
+    add(v1);
+    add(v2);
+    add(v3);
+  }
+  for (; q < q1; ++q) {
+    const uint4* r = row(q);
+    add(r ? __ldcs(r) : zero);
+  }
+  if (p.nch == 1) {
+    float4* S = reinterpret_cast<float4*>(p.S + static_cast<size_t>(u) * p.ND + e);
+    S[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    S[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    store_pair(p, u, e, acc);
+  } else {
+    float4* P = reinterpret_cast<float4*>(p.part + static_cast<size_t>(u * p.nch + c) * p.ND + e);
+    P[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    P[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+  }
+}
+
+// S[u] = sum over u's chunks, in chunk order.
+__global__ void __launch_bounds__(BWD_SEG_THREADS) bwd_segsum_finish_kernel(const SegSumParams p) {
+  const int s = blockIdx.x % p.slices;
+  const int u = blockIdx.x / p.slices;
+  const int e = s * BWD_SEG_SLICE + static_cast<int>(threadIdx.x) * 8;
+  if (u >= p.n_users || e >= p.ND) return;
+  float acc[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) acc[j] = 0.f;
+  for (int c = 0; c < p.nch; ++c) {
+    const float4* P = reinterpret_cast<const float4*>(p.part + static_cast<size_t>(u * p.nch + c) * p.ND + e);
+    const float4 a = P[0], b = P[1];
+    acc[0] += a.x;
+    acc[1] += a.y;
+    acc[2] += a.z;
+    acc[3] += a.w;
+    acc[4] += b.x;
+    acc[5] += b.y;
+    acc[6] += b.z;
+    acc[7] += b.w;
+  }
+  float4* S = reinterpret_cast<float4*>(p.S + static_cast<size_t>(u) * p.ND + e);
+  S[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+  S[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+  store_pair(p, u, e, acc);
+}
+
+// db[n] = sum_u sum_d S[u][n][d]: one CTA per n, a fixed reduction tree.
+constexpr int BWD_DB_THREADS = 256;
+__global__ void __launch_bounds__(BWD_DB_THREADS) bwd_db_kernel(const float* S, float* db, int n_users, int N,
+                                                                int D) {
+  __shared__ float red[BWD_DB_THREADS];
+  const int n = blockIdx.x;
+  float acc = 0.f;
+  const int total = n_users * D;
+  for (int t = threadIdx.x; t < total; t += BWD_DB_THREADS) {
+    const int u = t / D, d = t - u * D;
+    acc += S[(static_cast<size_t>(u) * N + n) * D + d];
+  }
+  red[threadIdx.x] = acc;
+  __syncthreads();
+  for (int w = BWD_DB_THREADS / 2; w > 0; w >>= 1) {
+    if (static_cast<int>(threadIdx.x) < w) red[threadIdx.x] += red[threadIdx.x + w];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) db[n] = red[0];
+}
+
+// ------------------------------------------------------------------------
+// Shared pieces of the two GEMM kernels.
+
+// A wait taken by a whole warp; the lanes agree on the outcome.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint32_t* abort, uint64_t timeout_ns) {
+  const bool ok = mbar_wait(bar, parity, abort, timeout_ns, 1);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// ------------------------------------------------- activation-gradient GEMM
+// Shared memory: W resident (kc chunks x m_rows rows x 128 B, K-major: row m
+// holds 64 n of one chunk, 128-byte swizzle), then the X ring (stages of two
+// 64 d x 64 n boxes, MN-major), then the barriers.
+struct ActSmem {
+  uint8_t* w;
+  uint8_t* ring;
+  uint64_t* a_full;
+  uint64_t* a_empty;
+  uint64_t* w_full;
+  uint64_t* acc_full;   // [2]
+  uint64_t* acc_empty;  // [2]
+  uint32_t* tmem_slot;
+  uint32_t* abort;
+};
+
+__host__ __device__ constexpr uint32_t act_w_bytes(int kc, int m_rows) {
+  return static_cast<uint32_t>(kc) * static_cast<uint32_t>(m_rows) * 128u;
+}
+
+__device__ __forceinline__ ActSmem act_carve(uint8_t* base, const ActParams& p) {
+  ActSmem s;
+  s.w = base;
+  s.ring = base + act_w_bytes(p.kc, p.m_rows);
+  uint64_t* b = reinterpret_cast<uint64_t*>(s.ring + static_cast<size_t>(p.stages) * 2 * BOX);
+  s.a_full = b;
+  s.a_empty = b + p.stages;
+  s.w_full = b + 2 * p.stages;
+  s.acc_full = s.w_full + 1;
+  s.acc_empty = s.acc_full + 2;
+  s.tmem_slot = reinterpret_cast<uint32_t*>(s.acc_empty + 2);
+  s.abort = s.tmem_slot + 1;
+  return s;
+}
+
+// Tiles q = dblk * B + b (D-block-major); each CTA takes one contiguous range.
+__device__ __forceinline__ void act_range(const ActParams& p, int& q0, int& q1) {
+  const long long nq = static_cast<long long>(p.B) * p.n_dblk;
+  q0 = static_cast<int>(blockIdx.x * nq / gridDim.x);
+  q1 = static_cast<int>((blockIdx.x + 1) * nq / gridDim.x);
+}
+
+__global__ void __launch_bounds__(BWD_THREADS, 1)
+    bwd_act_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
+                   const ActParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const ActSmem s = act_carve(base, p);
+  const int warp = threadIdx.x >> 5;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < p.stages; ++i) {
+      mbar_init(&s.a_full[i], 1);
+      mbar_init(&s.a_empty[i], 1);
+    }
+    mbar_init(s.w_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s.acc_full[i], 1);
+      mbar_init(&s.acc_empty[i], BWD_THREADS - 128);
+    }
+    *s.abort = 0;
+    fence_barrier_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == 0 && lane_id() == 0) {
+    tma_prefetch_desc(&tmX);
+    tma_prefetch_desc(&tmW);
+  }
+  if (warp == 2) {
+    tmem_alloc(s.tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *s.tmem_slot;
+  int q0, q1;
+  act_range(p, q0, q1);
+
+  if (warp == 0) {
+    // ---- TMA producer: W once, then the X chunks of every tile
+    if (elect_one()) {
+      mbar_arrive_expect_tx(s.w_full, act_w_bytes(p.kc, p.m_rows));
+      for (int kc = 0; kc < p.kc; ++kc)
+        for (int r = 0; r < p.m_rows; r += 128)
+          tma_load_2d(s.w + (static_cast<size_t>(kc) * p.m_rows + r) * 128, &tmW, s.w_full, kc * 64, r);
+    }
+    __syncwarp();
+    int stage = 0;
+    uint32_t phase = 0;
+    for (int q = q0; q < q1; ++q) {
+      const int dblk = q / p.B, b = q - dblk * p.B;
+      for (int kc = 0; kc < p.kcx; ++kc) {
+        if (!warp_wait(&s.a_empty[stage], phase ^ 1u, s.abort, p.timeout_ns)) goto done;
+        if (elect_one()) {
+          uint8_t* dst = s.ring + static_cast<size_t>(stage) * 2 * BOX;
+          mbar_arrive_expect_tx(&s.a_full[stage], 2 * BOX);
+          tma_load_3d(dst, &tmX, &s.a_full[stage], dblk * 128, kc * 64, b);
+          tma_load_3d(dst + BOX, &tmX, &s.a_full[stage], dblk * 128 + 64, kc * 64, b);
+        }
+        __syncwarp();
+        if (++stage == p.stages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ---- MMA issuer: per chunk, every m range of the tile
+    if (!warp_wait(s.w_full, 0, s.abort, p.timeout_ns)) goto done;
+    int stage = 0;
+    uint32_t phase = 0;
+    for (int q = q0, t = 0; q < q1; ++q, ++t) {
+      const int buf = p.bufs == 2 ? (t & 1) : 0;
+      const uint32_t use = static_cast<uint32_t>(p.bufs == 2 ? (t >> 1) : t);
+      if (!warp_wait(&s.acc_empty[buf], (use & 1u) ^ 1u, s.abort, p.timeout_ns)) goto done;
+      tc_fence_after();
+      for (int kc = 0; kc < p.kcx; ++kc) {
+        if (!warp_wait(&s.a_full[stage], phase, s.abort, p.timeout_ns)) goto done;
+        tc_fence_after();
+        const int wkc = kc % p.kc;  // K rows past N read as zeros on both sides
+        if (elect_one()) {
+          const uint32_t a_base = smem_u32(s.ring + static_cast<size_t>(stage) * 2 * BOX);
+          // X chunk, MN-major: the two 64-d boxes one BOX apart, 16 n rows per step
+          const uint64_t adesc = sdesc_sw128(a_base, BOX, 1024u);
+          for (int r = 0; r * 256 < p.m_pad; ++r) {
+            const int nr = min(256, p.m_pad - r * 256);
+            const uint32_t idesc = idesc_bf16_f32(128, static_cast<uint32_t>(nr), true, false);
+            // W, K-major: rows m of 128 bytes, 8-row atoms; a 16-n step is 32 bytes
+            const uint64_t bdesc =
+                sdesc_sw128(smem_u32(s.w + (static_cast<size_t>(wkc) * p.m_rows + r * 256) * 128), 16, 1024u);
+            const uint32_t d_tmem = tmem + static_cast<uint32_t>(buf * 256 + r * 256);
+#pragma unroll
+            for (int st = 0; st < 4; ++st)
+              mma_bf16_ss(d_tmem, adesc + st * (2048u >> 4), bdesc + st * (32u >> 4), idesc,
+                          (kc > 0 || st > 0) ? 1u : 0u);
+          }
+          mma_commit(&s.a_empty[stage]);
+        }
+        __syncwarp();
+        if (++stage == p.stages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (elect_one()) mma_commit(&s.acc_full[buf]);
+      __syncwarp();
+    }
+  } else if (warp >= 4) {
+    // ---- epilogue: TMEM lane = row d of the D block, columns = m
+    const int quarter = warp & 3, half = (warp - 4) >> 2;
+    const uint32_t lane_base = static_cast<uint32_t>(32 * quarter) << 16;
+    const int nchunks = (p.M + 31) / 32;
+    for (int q = q0, t = 0; q < q1; ++q, ++t) {
+      const int dblk = q / p.B, b = q - dblk * p.B;
+      const int buf = p.bufs == 2 ? (t & 1) : 0;
+      const uint32_t use = static_cast<uint32_t>(p.bufs == 2 ? (t >> 1) : t);
+      if (!warp_wait(&s.acc_full[buf], use & 1u, s.abort, p.timeout_ns)) goto done;
+      tc_fence_after();
+      const int d = dblk * 128 + quarter * 32 + static_cast<int>(lane_id());
+      const bool dok = d < p.D;
+      __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out) + static_cast<size_t>(b) * p.M * p.D + d;
+      for (int c = half; c < nchunks; c += 2) {
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_base + static_cast<uint32_t>(buf * 256 + c * 32), v);
+        tmem_ld_wait(v);
+        __nv_bfloat16* o = out + static_cast<size_t>(c * 32) * p.D;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          if (c * 32 + j < p.M && dok) *o = __float2bfloat16_rn(__uint_as_float(v[j]));
+          o += p.D;
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&s.acc_empty[buf]);
+    }
+  }
+done:
+  tc_fence_before();
+  __syncthreads();
+  if (*s.abort && threadIdx.x == 0) atomicOr(p.status, DEV_ERR_PIPE_TIMEOUT);
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ---------------------------------------------------- weight-gradient GEMM
+// Stage = one 64 d x 128 m box of A (16 KB) + nb boxes of 64 d x 64 n of G
+// (8 KB each), both K-major (d contiguous) with 128-byte swizzle.
+__host__ __device__ constexpr uint32_t wg_stage_bytes(int nb) { return 2 * BOX + static_cast<uint32_t>(nb) * BOX; }
+
+struct WgSmem {
+  uint8_t* ring;
+  uint64_t* full;
+  uint64_t* empty;
+  uint64_t* acc_full;
+  uint64_t* acc_empty;
+  uint32_t* tmem_slot;
+  uint32_t* abort;
+};
+
+__device__ __forceinline__ WgSmem wg_carve(uint8_t* base, const WgradParams& p) {
+  WgSmem s;
+  s.ring = base;
+  uint64_t* b = reinterpret_cast<uint64_t*>(base + BWD_WG_STAGES * wg_stage_bytes(p.nb));
+  s.full = b;
+  s.empty = b + BWD_WG_STAGES;
+  s.acc_full = b + 2 * BWD_WG_STAGES;
+  s.acc_empty = s.acc_full + 1;
+  s.tmem_slot = reinterpret_cast<uint32_t*>(s.acc_empty + 1);
+  s.abort = s.tmem_slot + 1;
+  return s;
+}
+
+// Unit u = (m block u / R, b range u % R); b range r = [r*B/R, (r+1)*B/R),
+// never empty because R <= B.
+__device__ __forceinline__ void wg_unit(const WgradParams& p, int u, int& mblk, int& b0, int& b1) {
+  mblk = u / p.R;
+  const int r = u - mblk * p.R;
+  b0 = static_cast<int>(static_cast<long long>(r) * p.B / p.R);
+  b1 = static_cast<int>(static_cast<long long>(r + 1) * p.B / p.R);
+}
+
+__global__ void __launch_bounds__(BWD_THREADS, 1)
+    bwd_wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmG,
+                     const WgradParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const WgSmem s = wg_carve(base, p);
+  const int warp = threadIdx.x >> 5;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < BWD_WG_STAGES; ++i) {
+      mbar_init(&s.full[i], 1);
+      mbar_init(&s.empty[i], 1);
+    }
+    mbar_init(s.acc_full, 1);
+    mbar_init(s.acc_empty, BWD_THREADS - 128);
+    *s.abort = 0;
+    fence_barrier_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == 0 && lane_id() == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmG);
+  }
+  if (warp == 2) {
+    tmem_alloc(s.tmem_slot, 256);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *s.tmem_slot;
+  const int n_units = p.n_mblk * p.R;
+  const uint32_t sbytes = wg_stage_bytes(p.nb);
+
+  if (warp == 0) {
+    // ---- TMA producer
+    int stage = 0;
+    uint32_t phase = 0;
+    for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+      int mblk, b0, b1;
+      wg_unit(p, u, mblk, b0, b1);
+      for (int b = b0; b < b1; ++b)
+        for (int dc = 0; dc < p.dc; ++dc) {
+          if (!warp_wait(&s.empty[stage], phase ^ 1u, s.abort, p.timeout_ns)) goto done;
+          if (elect_one()) {
+            uint8_t* dst = s.ring + static_cast<size_t>(stage) * sbytes;
+            mbar_arrive_expect_tx(&s.full[stage], sbytes);
+            tma_load_3d(dst, &tmA, &s.full[stage], dc * 64, mblk * 128, b >> p.a_shift);
+            for (int j = 0; j < p.nb; ++j)
+              tma_load_3d(dst + 2 * BOX + static_cast<size_t>(j) * BOX, &tmG, &s.full[stage], dc * 64, j * 64, b);
+          }
+          __syncwarp();
+          if (++stage == BWD_WG_STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+    }
+  } else if (warp == 1) {
+    // ---- MMA issuer: D[m][n] += A[m][d-chunk] G[n][d-chunk]^T, 4 steps of 16 d
+    const uint32_t idesc = idesc_bf16_f32(128, static_cast<uint32_t>(p.n_mma), false, false);
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t use = 0;
+    for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++use) {
+      int mblk, b0, b1;
+      wg_unit(p, u, mblk, b0, b1);
+      if (!warp_wait(s.acc_empty, (use & 1u) ^ 1u, s.abort, p.timeout_ns)) goto done;
+      tc_fence_after();
+      bool first = true;
+      for (int b = b0; b < b1; ++b)
+        for (int dc = 0; dc < p.dc; ++dc) {
+          if (!warp_wait(&s.full[stage], phase, s.abort, p.timeout_ns)) goto done;
+          tc_fence_after();
+          if (elect_one()) {
+            const uint32_t a_base = smem_u32(s.ring + static_cast<size_t>(stage) * sbytes);
+            const uint64_t adesc = sdesc_sw128(a_base, 16, 1024u);
+            const uint64_t bdesc = sdesc_sw128(a_base + 2 * BOX, 16, 1024u);
+#pragma unroll
+            for (int st = 0; st < 4; ++st)
+              mma_bf16_ss(tmem, adesc + st * (32u >> 4), bdesc + st * (32u >> 4), idesc,
+                          (first && st == 0) ? 0u : 1u);
+            mma_commit(&s.empty[stage]);
+          }
+          __syncwarp();
+          first = false;
+          if (++stage == BWD_WG_STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      if (elect_one()) mma_commit(s.acc_full);
+      __syncwarp();
+    }
+  } else if (warp >= 4) {
+    // ---- epilogue: TMEM lane = row m of the block, columns = n -> fp32 partial
+    const int quarter = warp & 3, half = (warp - 4) >> 2;
+    const uint32_t lane_base = static_cast<uint32_t>(32 * quarter) << 16;
+    const int row = quarter * 32 + static_cast<int>(lane_id());
+    const int nchunks = (p.N + 31) / 32;
+    uint32_t use = 0;
+    for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++use) {
+      if (!warp_wait(s.acc_full, use & 1u, s.abort, p.timeout_ns)) goto done;
+      tc_fence_after();
+      float* out = p.part + (static_cast<size_t>(u) * 128 + row) * p.N;
+      for (int c = half; c < nchunks; c += 2) {
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_base + static_cast<uint32_t>(c * 32), v);
+        tmem_ld_wait(v);
+        if (c * 32 + 32 <= p.N) {
+          float4* o4 = reinterpret_cast<float4*>(out + c * 32);
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            o4[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (c * 32 + j < p.N) out[c * 32 + j] = __uint_as_float(v[j]);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(s.acc_empty);
+    }
+  }
+done:
+  tc_fence_before();
+  __syncthreads();
+  if (*s.abort && threadIdx.x == 0) atomicOr(p.status, DEV_ERR_PIPE_TIMEOUT);
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 256);
+  }
+}
+
+// dW[m][n] = sum over the b ranges of m's block, in range order.
+__global__ void __launch_bounds__(256) bwd_wgrad_reduce_kernel(const float* part, float* dW, int M, int N, int R) {
+  const int idx = blockIdx.x * 256 + threadIdx.x;
+  if (idx >= M * N) return;
+  const int m = idx / N, n = idx - m * N;
+  const int mblk = m >> 7, row = m & 127;
+  float acc = 0.f;
+  for (int r = 0; r < R; ++r) acc += part[(static_cast<size_t>(mblk * R + r) * 128 + row) * N + n];
+  dW[idx] = acc;
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------- host
+namespace {
+constexpr size_t SMEM_ALIGN_PAD = 1024;
+}
+
+int bwd_segsum_chunks(int n_cand, int n_users, int ND, int num_sms) {
+  const int slices = (ND + BWD_SEG_SLICE - 1) / BWD_SEG_SLICE;
+  const long long tasks = static_cast<long long>(n_users) * slices;
+  const long long target = 2ll * num_sms;
+  int nch = tasks >= target ? 1 : static_cast<int>((target + tasks - 1) / tasks);
+  const int cap = n_cand / (16 * n_users);  // at least ~16 candidates per chunk
+  if (nch > cap) nch = cap;
+  return nch < 1 ? 1 : nch;
+}
+
+cudaError_t launch_bwd_segsum(const SegSumParams& p, cudaStream_t s, int* launches) {
+  bwd_segsum_kernel<<<p.n_users * p.nch * p.slices, BWD_SEG_THREADS, 0, s>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  *launches += 1;
+  if (p.nch > 1) {
+    bwd_segsum_finish_kernel<<<p.n_users * p.slices, BWD_SEG_THREADS, 0, s>>>(p);
+    e = cudaGetLastError();
+    if (e == cudaSuccess) *launches += 1;
+  }
+  return e;
+}
+
+cudaError_t launch_bwd_db(const float* S, float* db, int n_users, int N, int D, cudaStream_t s) {
+  bwd_db_kernel<<<N, BWD_DB_THREADS, 0, s>>>(S, db, n_users, N, D);
+  return cudaGetLastError();
+}
+
+size_t bwd_act_smem(const ActParams& p) {
+  return SMEM_ALIGN_PAD + act_w_bytes(p.kc, p.m_rows) + static_cast<size_t>(p.stages) * 2 * BOX +
+         sizeof(uint64_t) * (2 * p.stages + 1 + 4) + 2 * sizeof(uint32_t);
+}
+
+// Fills the derived fields from B, M, D, N; `pair`: X holds a hi/lo pair
+// (2 * kc chunks per b).  False for shapes it cannot run.
+bool bwd_act_configure(ActParams* p, size_t max_smem, bool pair) {
+  if (p->B < 1 || p->M < 1 || p->D < 1 || p->N < 1) return false;
+  p->n_dblk = (p->D + 127) / 128;
+  p->kc = (p->N + 63) / 64;
+  p->m_pad = (p->M + 15) / 16 * 16;
+  p->m_rows = (p->M + 127) / 128 * 128;
+  p->bufs = p->m_pad <= 256 ? 2 : 1;
+  p->kcx = pair ? 2 * p->kc : p->kc;
+  if (p->m_pad > 512) return false;
+  p->stages = BWD_ACT_MAX_STAGES;
+  while (p->stages > 2 && bwd_act_smem(*p) > max_smem) --p->stages;
+  return bwd_act_smem(*p) <= max_smem;
+}
+
+cudaError_t launch_bwd_act(const CUtensorMap& tmX, const CUtensorMap& tmW, const ActParams& p, int num_sms,
+                           cudaStream_t s) {
+  const size_t smem = bwd_act_smem(p);
+  cudaError_t e =
+      cudaFuncSetAttribute(bwd_act_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  const long long tiles = static_cast<long long>(p.B) * p.n_dblk;
+  const int grid = static_cast<int>(tiles < num_sms ? tiles : num_sms);
+  bwd_act_kernel<<<grid, BWD_THREADS, smem, s>>>(tmX, tmW, p);
+  return cudaGetLastError();
+}
+
+size_t bwd_wgrad_smem(const WgradParams& p) {
+  return SMEM_ALIGN_PAD + static_cast<size_t>(BWD_WG_STAGES) * wg_stage_bytes(p.nb) +
+         sizeof(uint64_t) * (2 * BWD_WG_STAGES + 2) + 2 * sizeof(uint32_t);
+}
+
+bool bwd_wgrad_configure(WgradParams* p, int num_sms, size_t max_smem) {
+  if (p->B < 1 || p->M < 1 || p->D < 1 || p->N < 1 || p->N > 256) return false;
+  p->n_mblk = (p->M + 127) / 128;
+  int R = num_sms / p->n_mblk;
+  if (R < 1) R = 1;
+  if (R > p->B) R = p->B;
+  p->R = R;
+  p->dc = (p->D + 63) / 64;
+  p->n_mma = (p->N + 15) / 16 * 16;
+  p->nb = (p->n_mma + 63) / 64;
+  return bwd_wgrad_smem(*p) <= max_smem;
+}
+
+size_t bwd_wgrad_part_elems(const WgradParams& p) {
+  return static_cast<size_t>(p.n_mblk) * p.R * 128 * p.N;
+}
+
+// The split-K kernel (partials into p.part) and the in-order reduce into dW.
+cudaError_t launch_bwd_wgrad(const CUtensorMap& tmA, const CUtensorMap& tmG, const WgradParams& p, float* dW,
+                             int num_sms, cudaStream_t s, int* launches) {
+  const size_t smem = bwd_wgrad_smem(p);
+  cudaError_t e =
+      cudaFuncSetAttribute(bwd_wgrad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  const int units = p.n_mblk * p.R;
+  bwd_wgrad_kernel<<<units < num_sms ? units : num_sms, BWD_THREADS, smem, s>>>(tmA, tmG, p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int total = p.M * p.N;
+  bwd_wgrad_reduce_kernel<<<(total + 255) / 256, 256, 0, s>>>(p.part, dW, p.M, p.N, p.R);
+  e = cudaGetLastError();
+  if (e == cudaSuccess) *launches += 2;
+  return e;
+}
+
+}  // namespace ikbo

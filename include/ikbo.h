@@ -161,6 +161,36 @@ ikbo_status_t ikbo_lce_forward_staged(ikbo_plan_t p, const void* U, const void* 
                                       const void* b, void* Y, int K_u, int K_c, int D, int N, int stage,
                                       cudaStream_t stream);
 
+/* LCE backward for training (aibriefing, "Meta Optimizes Inference for
+ * Recommendation Systems": the IKBO kernels serve training when the
+ * candidate:user ratio exceeds 1; the pages give no backward formulas, so
+ * these are the chain rule of ikbo_lce_forward's definition).  Given the
+ * upstream gradient dY = dL/dY and the map of the last ikbo_plan:
+ *   S[u]       = sum_{i : map[i] = u} dY[i]          (fp32 segment sum; the
+ *                transpose of the broadcast, so the user side stays at n_users)
+ *   dU[u][k][d] = sum_n Wu[k][n] S[u][n][d]            bf16 [n_users][K_u][D]
+ *   dWu[k][n]   = sum_u sum_d U[u][k][d] S[u][n][d]    fp32 [K_u][N]
+ *   dC[i][k][d] = sum_n Wc[k][n] dY[i][n][d]           bf16 [n_cand][K_c][D]
+ *   dWc[k][n]   = sum_i sum_d C[i][k][d] dY[i][n][d]   fp32 [K_c][N]
+ *   db[n]       = sum_u sum_d S[u][n][d]               fp32 [N]
+ *   U, C, Wu, Wc: as ikbo_lce_forward; dY bf16 [n_cand][N][D].
+ * Every output pointer may be NULL to skip that gradient; an input is only
+ * required by the gradients that read it (Wu for dU, Wc for dC, U for dWu,
+ * C for dWc), else IKBO_ERR_INVALID_ARG.  Outputs are overwritten, not
+ * accumulated into.  bf16 operands, fp32 accumulation; S is rounded to bf16
+ * for the two products that read it (dU, dWu).  The weight gradients are
+ * summed over split-K partials in a fixed order, so results repeat bit for
+ * bit.  Candidates whose map value is out of range are left out of S (so of
+ * dU, dWu and db) and reported by the plan's status; they still enter dC and
+ * dWc.  Workspaces (S, partial sums) are plan-owned and grown on first use
+ * (that call allocates synchronously).  Limits: D, N multiples of 8,
+ * N <= 256; for dC / dU, K <= 512 and the weight, roundup(K, 128) *
+ * ceil(N / 64) * 128 bytes, fits in shared memory beside two 16 KB stages
+ * (about 190 KB); else IKBO_ERR_UNSUPPORTED. */
+ikbo_status_t ikbo_lce_backward(ikbo_plan_t p, const void* U, const void* C, const void* Wu, const void* Wc,
+                                const void* dY, void* dU, void* dC, float* dWu, float* dWc, float* db, int K_u,
+                                int K_c, int D, int N, cudaStream_t stream);
+
 /* Broadcast attention (aixai.ru, "Deep Dive: Flash Attention"; aibriefing,
  * Flash Attention case): for every candidate i and head h, with u = map[i],
  *   O[i,h,q,:] = sum_j softmax_j(scale * Q[i,h,q,:].K[u,h,j,:]) V[u,h,j,:]
