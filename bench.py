@@ -408,6 +408,9 @@ def run_gpu(args):
     self_target = None
     if not args.no_self_target:
         self_target = self_target_run(plan, d, x, a, O, flush, stream, dev)
+    lce_backward = None
+    if not args.no_backward:
+        lce_backward = lce_backward_run(plan, d, x, flush, stream, dev, peaks())
 
     plan.close()
     if rank != 0:
@@ -436,6 +439,7 @@ def run_gpu(args):
         "roofline": roofline, "roofline_lce": roofline_lce,
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": gpu_launches,
         "clocks": clk.summary(), "ablation": ablation, "lce_stages": lce_stages, "self_target": self_target,
+        "lce_backward": lce_backward,
     }
     print(json.dumps(out), flush=True)
     if dist:
@@ -535,6 +539,45 @@ def lce_stage_run(plan, d, Y, flush, stream, iters=20):
     return res
 
 
+def lce_backward_run(plan, d, x, flush, stream, dev, pk, iters=20):
+    """ikbo_lce_backward at the request shape (every gradient: dU, dC, dW_u,
+    dW_c, db) for a seeded upstream gradient dY, median and mean µs over
+    `iters` flushed runs, against its HBM roofline."""
+    import statistics
+    import torch
+    from broadcast_gemm_attention_gb300 import accounting as acc
+    from broadcast_gemm_attention_gb300 import inputs as gen
+    dY = gen.make_lce_grad(1001, x.n_cand, x.N, x.D).to(dev)
+    out = dict(dU=torch.empty(x.n_users, x.K_u, x.D, dtype=torch.bfloat16, device=dev),
+               dC=torch.empty(x.n_cand, x.K_c, x.D, dtype=torch.bfloat16, device=dev),
+               dWu=torch.empty(x.K_u, x.N, dtype=torch.float32, device=dev),
+               dWc=torch.empty(x.K_c, x.N, dtype=torch.float32, device=dev),
+               db=torch.empty(x.N, dtype=torch.float32, device=dev))
+    ts = []
+    l0 = plan.launches()
+    for k in range(iters + 3):
+        flush()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        plan.lce_backward(d["U"], d["C"], d["Wu"], d["Wc"], dY, stream=stream, **out)
+        e.record(stream)
+        torch.cuda.synchronize()
+        if k >= 3:
+            ts.append(s.elapsed_time(e))
+    launches = (plan.launches() - l0) / (iters + 3)
+    us = 1e3 * statistics.median(ts)
+    byt = acc.lce_backward_bytes(x.n_cand, x.n_users, x.K_u, x.K_c, x.D, x.N)
+    fl = acc.lce_backward_flops(x.n_cand, x.n_users, x.K_u, x.K_c, x.D, x.N)
+    gbs = byt / (us * 1e-6) / 1e9
+    return {"us_median": us, "us_mean": 1e3 * statistics.mean(ts), "launches_per_call": launches,
+            "tflops": fl / (us * 1e-6) / 1e12,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                         "frac": gbs / pk["hbm_gbs"],
+                         "algorithmic": f"{byt:.4g} bytes per call (dY, U, C, W read once; dU, dC, dW, db written once)"},
+            "note": "S = segment sum of dY (fp32; bf16 hi/lo pair for dU and dW_u); dC = W_c dY, dW_c = sum C dY^T; "
+                    "dU = W_u S, dW_u = sum U S^T, db from S; one stream, L2 flushed before each call"}
+
+
 def self_target_run(plan, d, x, a, O, flush, stream, dev, Lq_u=64, iters=20):
     """The request's target attention plus each user's own Lq_u queries over
     the same K/V: one launch (ikbo_attn_self_target_forward) against two
@@ -631,6 +674,7 @@ def main():
     ap.add_argument("--impl", choices=["ikbo", "reference"], default="ikbo")
     ap.add_argument("--no-ablation", action="store_true")
     ap.add_argument("--no-self-target", action="store_true", help="skip the self + target attention comparison")
+    ap.add_argument("--no-backward", action="store_true", help="skip the LCE backward measurement")
     ap.add_argument("--sweep", action="store_true", help="shape sweep (LCE and attention) instead of the benchmark")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--lce-schedule", type=int, default=0, choices=[0, 1, 2, 3],

@@ -30,6 +30,21 @@ def lce_bytes(n_cand: int, n_users: int, K_u: int, K_c: int, D: int, N: int, bia
     return float(rd + wr)
 
 
+def lce_backward_flops(n_cand: int, n_users: int, K_u: int, K_c: int, D: int, N: int) -> float:
+    """The four products of the LCE backward, each at its own batch: dU and dW_u
+    at n_users, dC and dW_c at n_cand (2*D*N*K per batch row each); the segment
+    sum's additions are not counted."""
+    return 2.0 * lce_flops(n_cand, n_users, K_u, K_c, D, N)
+
+
+def lce_backward_bytes(n_cand: int, n_users: int, K_u: int, K_c: int, D: int, N: int) -> float:
+    """dY, U, C, W_u, W_c and map read once; dU, dC (bf16) and dW_u, dW_c, db
+    (fp32) written once."""
+    rd = BF16 * (n_cand * N * D + n_users * K_u * D + n_cand * K_c * D + K_u * N + K_c * N) + I32 * n_cand
+    wr = BF16 * (n_users * K_u * D + n_cand * K_c * D) + 4 * (K_u * N + K_c * N + N)
+    return float(rd + wr)
+
+
 def lce_materialised_flops(n_cand: int, K_u: int, K_c: int, D: int, N: int) -> float:
     """The replicated baseline: one GEMM over K_u + K_c for every candidate."""
     return 2.0 * D * N * n_cand * (K_u + K_c)

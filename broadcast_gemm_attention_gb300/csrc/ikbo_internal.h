@@ -159,11 +159,11 @@ struct ActParams {
   uint64_t timeout_ns;
 };
 
-// Weight-gradient GEMM, split along K = (b, d): unit (m block, b range)
-// accumulates A[b][m][d] G[b][n][d] over its b range into TMEM (M = 128 m
-// rows, N = n, both operands K-major) and writes an fp32 partial; a reduce
-// pass adds the partials of each m block in order.
-constexpr int BWD_WG_STAGES = 4;
+// Weight-gradient GEMM, split along K = (b, d): unit (group of <= 2 m
+// blocks, b range) accumulates A[b][m][d] G[b][n][d] over its b range into
+// TMEM (M = 128 m rows per block, N = n, both operands K-major) and writes
+// fp32 partials; a reduce pass adds the partials of each m block in order.
+constexpr int BWD_WG_MAX_STAGES = 4;
 
 struct WgradParams {
   float* part;               // [n_units][128][N] fp32
@@ -171,7 +171,10 @@ struct WgradParams {
   int B, M, D, N;            // B = batches of G; A's batch is b >> a_shift
   int a_shift;               // 1 when G holds a hi/lo pair per batch of A
   int n_mblk;                // ceil(M / 128)
-  int R;                     // b ranges per m block (n_units = n_mblk * R)
+  int mg;                    // m blocks per unit (1 or 2)
+  int n_mgrp;                // ceil(n_mblk / mg)
+  int R;                     // b ranges per m group (n_units = n_mgrp * R)
+  int stages;                // ring depth
   int dc;                    // ceil(D / 64)
   int n_mma;                 // roundup(N, 16)
   int nb;                    // ceil(n_mma / 64): 64-row boxes of G per chunk

@@ -50,15 +50,18 @@ __device__ __forceinline__ void store_pair(const SegSumParams& p, int u, int e, 
 
 // Task = (user u, chunk c of u's segment, slice s of the N*D elements); each
 // thread sums 8 consecutive elements (one 16-byte load per candidate) over
-// the chunk's candidates in ascending perm order, four loads in flight.
+// the chunk's candidates in ascending perm order.  The CTA stages 128 perm
+// entries at a time in shared memory, so the dY loads do not wait on a
+// dependent perm load, and each thread keeps 8 loads in flight.
 __global__ void __launch_bounds__(BWD_SEG_THREADS) bwd_segsum_kernel(const SegSumParams p) {
+  __shared__ int rows[BWD_SEG_THREADS];
   const int task = blockIdx.x;
   const int s = task % p.slices;
   const int uc = task / p.slices;
   const int c = uc % p.nch;
   const int u = uc / p.nch;
   const int e = s * BWD_SEG_SLICE + static_cast<int>(threadIdx.x) * 8;
-  if (u >= p.n_users || e >= p.ND) return;
+  const bool active = e < p.ND;
   const int p0 = __ldg(p.offsets + u), cnt = __ldg(p.offsets + u + 1) - p0;
   const int q0 = p0 + static_cast<int>(static_cast<long long>(cnt) * c / p.nch);
   const int q1 = p0 + static_cast<int>(static_cast<long long>(cnt) * (c + 1) / p.nch);
@@ -73,29 +76,30 @@ __global__ void __launch_bounds__(BWD_SEG_THREADS) bwd_segsum_kernel(const SegSu
       acc[2 * j + 1] += __uint_as_float(w[j] & 0xffff0000u);
     }
   };
-  auto row = [&](int q) -> const uint4* {
-    int i = __ldg(p.perm + q);
-    i = (i >= 0 && i < p.n_cand) ? i : -1;
-    return i < 0 ? nullptr : reinterpret_cast<const uint4*>(p.dY + static_cast<size_t>(i) * p.ND + e);
-  };
   const uint4 zero = make_uint4(0, 0, 0, 0);
-  int q = q0;
-  for (; q + 4 <= q1; q += 4) {
-    const uint4* r0 = row(q);
-    const uint4* r1 = row(q + 1);
-    const uint4* r2 = row(q + 2);
-    const uint4* r3 = row(q + 3);
-    const uint4 v0 = r0 ? __ldcs(r0) : zero, v1 = r1 ? __ldcs(r1) : zero;
-    const uint4 v2 = r2 ? __ldcs(r2) : zero, v3 = r3 ? __ldcs(r3) : zero;
-    add(v0);
-    add(v1);
-    add(v2);
-    add(v3);
+  auto load = [&](int r) -> uint4 {
+    return r < 0 ? zero : __ldcs(reinterpret_cast<const uint4*>(p.dY + static_cast<size_t>(r) * p.ND + e));
+  };
+  for (int base = q0; base < q1; base += BWD_SEG_THREADS) {
+    const int n = min(BWD_SEG_THREADS, q1 - base);
+    __syncthreads();
+    if (static_cast<int>(threadIdx.x) < n) {
+      const int i = __ldg(p.perm + base + threadIdx.x);
+      rows[threadIdx.x] = (i >= 0 && i < p.n_cand) ? i : -1;
+    }
+    __syncthreads();
+    if (!active) continue;
+    int j = 0;
+    for (; j + 8 <= n; j += 8) {
+      uint4 v[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) v[k] = load(rows[j + k]);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) add(v[k]);
+    }
+    for (; j < n; ++j) add(load(rows[j]));
   }
-  for (; q < q1; ++q) {
-    const uint4* r = row(q);
-    add(r ? __ldcs(r) : zero);
-  }
+  if (!active) return;
   if (p.nch == 1) {
     float4* S = reinterpret_cast<float4*>(p.S + static_cast<size_t>(u) * p.ND + e);
     S[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
@@ -143,6 +147,7 @@ __global__ void __launch_bounds__(BWD_DB_THREADS) bwd_db_kernel(const float* S, 
   const int n = blockIdx.x;
   float acc = 0.f;
   const int total = n_users * D;
+#pragma unroll 8
   for (int t = threadIdx.x; t < total; t += BWD_DB_THREADS) {
     const int u = t / D, d = t - u * D;
     acc += S[(static_cast<size_t>(u) * N + n) * D + d];
@@ -352,9 +357,14 @@ done:
 }
 
 // ---------------------------------------------------- weight-gradient GEMM
-// Stage = one 64 d x 128 m box of A (16 KB) + nb boxes of 64 d x 64 n of G
-// (8 KB each), both K-major (d contiguous) with 128-byte swizzle.
-__host__ __device__ constexpr uint32_t wg_stage_bytes(int nb) { return 2 * BOX + static_cast<uint32_t>(nb) * BOX; }
+// A unit covers a group of up to two 128-row m blocks (accumulators at TMEM
+// columns 0 and 256) over one b range, so the G tiles it loads serve both
+// blocks.  Stage = one 64 d x 128 m box of A per block of the group (16 KB
+// each) + nb boxes of 64 d x 64 n of G (8 KB each), all K-major (d
+// contiguous), 128-byte swizzle.
+__host__ __device__ constexpr uint32_t wg_stage_bytes(int mg, int nb) {
+  return static_cast<uint32_t>(mg) * 2 * BOX + static_cast<uint32_t>(nb) * BOX;
+}
 
 struct WgSmem {
   uint8_t* ring;
@@ -369,21 +379,24 @@ struct WgSmem {
 __device__ __forceinline__ WgSmem wg_carve(uint8_t* base, const WgradParams& p) {
   WgSmem s;
   s.ring = base;
-  uint64_t* b = reinterpret_cast<uint64_t*>(base + BWD_WG_STAGES * wg_stage_bytes(p.nb));
+  uint64_t* b = reinterpret_cast<uint64_t*>(base + static_cast<size_t>(p.stages) * wg_stage_bytes(p.mg, p.nb));
   s.full = b;
-  s.empty = b + BWD_WG_STAGES;
-  s.acc_full = b + 2 * BWD_WG_STAGES;
+  s.empty = b + p.stages;
+  s.acc_full = b + 2 * p.stages;
   s.acc_empty = s.acc_full + 1;
   s.tmem_slot = reinterpret_cast<uint32_t*>(s.acc_empty + 1);
   s.abort = s.tmem_slot + 1;
   return s;
 }
 
-// Unit u = (m block u / R, b range u % R); b range r = [r*B/R, (r+1)*B/R),
-// never empty because R <= B.
-__device__ __forceinline__ void wg_unit(const WgradParams& p, int u, int& mblk, int& b0, int& b1) {
-  mblk = u / p.R;
-  const int r = u - mblk * p.R;
+// Unit u = (m group u / R, b range u % R); b range r = [r*B/R, (r+1)*B/R),
+// never empty because R <= B.  nblk = the group's m blocks inside M.
+__device__ __forceinline__ void wg_unit(const WgradParams& p, int u, int& mblk0, int& nblk, int& r, int& b0,
+                                        int& b1) {
+  const int g = u / p.R;
+  r = u - g * p.R;
+  mblk0 = g * p.mg;
+  nblk = min(p.mg, p.n_mblk - mblk0);
   b0 = static_cast<int>(static_cast<long long>(r) * p.B / p.R);
   b1 = static_cast<int>(static_cast<long long>(r + 1) * p.B / p.R);
 }
@@ -396,7 +409,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
   const WgSmem s = wg_carve(base, p);
   const int warp = threadIdx.x >> 5;
   if (threadIdx.x == 0) {
-    for (int i = 0; i < BWD_WG_STAGES; ++i) {
+    for (int i = 0; i < p.stages; ++i) {
       mbar_init(&s.full[i], 1);
       mbar_init(&s.empty[i], 1);
     }
@@ -411,49 +424,53 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     tma_prefetch_desc(&tmG);
   }
   if (warp == 2) {
-    tmem_alloc(s.tmem_slot, 256);
+    tmem_alloc(s.tmem_slot, 512);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *s.tmem_slot;
-  const int n_units = p.n_mblk * p.R;
-  const uint32_t sbytes = wg_stage_bytes(p.nb);
+  const int n_units = p.n_mgrp * p.R;
+  const uint32_t sbytes = wg_stage_bytes(p.mg, p.nb);
+  const uint32_t g_off = static_cast<uint32_t>(p.mg) * 2 * BOX;  // G boxes after the A boxes
 
   if (warp == 0) {
     // ---- TMA producer
     int stage = 0;
     uint32_t phase = 0;
     for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
-      int mblk, b0, b1;
-      wg_unit(p, u, mblk, b0, b1);
+      int mblk0, nblk, r, b0, b1;
+      wg_unit(p, u, mblk0, nblk, r, b0, b1);
+      const uint32_t bytes = static_cast<uint32_t>(nblk) * 2 * BOX + static_cast<uint32_t>(p.nb) * BOX;
       for (int b = b0; b < b1; ++b)
         for (int dc = 0; dc < p.dc; ++dc) {
           if (!warp_wait(&s.empty[stage], phase ^ 1u, s.abort, p.timeout_ns)) goto done;
           if (elect_one()) {
             uint8_t* dst = s.ring + static_cast<size_t>(stage) * sbytes;
-            mbar_arrive_expect_tx(&s.full[stage], sbytes);
-            tma_load_3d(dst, &tmA, &s.full[stage], dc * 64, mblk * 128, b >> p.a_shift);
+            mbar_arrive_expect_tx(&s.full[stage], bytes);
+            for (int j = 0; j < nblk; ++j)
+              tma_load_3d(dst + static_cast<size_t>(j) * 2 * BOX, &tmA, &s.full[stage], dc * 64, (mblk0 + j) * 128,
+                          b >> p.a_shift);
             for (int j = 0; j < p.nb; ++j)
-              tma_load_3d(dst + 2 * BOX + static_cast<size_t>(j) * BOX, &tmG, &s.full[stage], dc * 64, j * 64, b);
+              tma_load_3d(dst + g_off + static_cast<size_t>(j) * BOX, &tmG, &s.full[stage], dc * 64, j * 64, b);
           }
           __syncwarp();
-          if (++stage == BWD_WG_STAGES) {
+          if (++stage == p.stages) {
             stage = 0;
             phase ^= 1u;
           }
         }
     }
   } else if (warp == 1) {
-    // ---- MMA issuer: D[m][n] += A[m][d-chunk] G[n][d-chunk]^T, 4 steps of 16 d
+    // ---- MMA issuer: D_j[m][n] += A_j[m][d-chunk] G[n][d-chunk]^T, 4 steps of 16 d
     const uint32_t idesc = idesc_bf16_f32(128, static_cast<uint32_t>(p.n_mma), false, false);
     int stage = 0;
     uint32_t phase = 0;
     uint32_t use = 0;
     for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++use) {
-      int mblk, b0, b1;
-      wg_unit(p, u, mblk, b0, b1);
+      int mblk0, nblk, r, b0, b1;
+      wg_unit(p, u, mblk0, nblk, r, b0, b1);
       if (!warp_wait(s.acc_empty, (use & 1u) ^ 1u, s.abort, p.timeout_ns)) goto done;
       tc_fence_after();
       bool first = true;
@@ -462,18 +479,20 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
           if (!warp_wait(&s.full[stage], phase, s.abort, p.timeout_ns)) goto done;
           tc_fence_after();
           if (elect_one()) {
-            const uint32_t a_base = smem_u32(s.ring + static_cast<size_t>(stage) * sbytes);
-            const uint64_t adesc = sdesc_sw128(a_base, 16, 1024u);
-            const uint64_t bdesc = sdesc_sw128(a_base + 2 * BOX, 16, 1024u);
+            const uint32_t st_base = smem_u32(s.ring + static_cast<size_t>(stage) * sbytes);
+            const uint64_t bdesc = sdesc_sw128(st_base + g_off, 16, 1024u);
+            for (int j = 0; j < nblk; ++j) {
+              const uint64_t adesc = sdesc_sw128(st_base + static_cast<uint32_t>(j) * 2 * BOX, 16, 1024u);
 #pragma unroll
-            for (int st = 0; st < 4; ++st)
-              mma_bf16_ss(tmem, adesc + st * (32u >> 4), bdesc + st * (32u >> 4), idesc,
-                          (first && st == 0) ? 0u : 1u);
+              for (int st = 0; st < 4; ++st)
+                mma_bf16_ss(tmem + static_cast<uint32_t>(j * 256), adesc + st * (32u >> 4), bdesc + st * (32u >> 4),
+                            idesc, (first && st == 0) ? 0u : 1u);
+            }
             mma_commit(&s.empty[stage]);
           }
           __syncwarp();
           first = false;
-          if (++stage == BWD_WG_STAGES) {
+          if (++stage == p.stages) {
             stage = 0;
             phase ^= 1u;
           }
@@ -482,30 +501,35 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       __syncwarp();
     }
   } else if (warp >= 4) {
-    // ---- epilogue: TMEM lane = row m of the block, columns = n -> fp32 partial
+    // ---- epilogue: TMEM lane = row m of a block, columns = n -> fp32 partial
+    // part[(m block * R + r) * 128 + row][n]
     const int quarter = warp & 3, half = (warp - 4) >> 2;
     const uint32_t lane_base = static_cast<uint32_t>(32 * quarter) << 16;
     const int row = quarter * 32 + static_cast<int>(lane_id());
     const int nchunks = (p.N + 31) / 32;
     uint32_t use = 0;
     for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++use) {
+      int mblk0, nblk, r, b0, b1;
+      wg_unit(p, u, mblk0, nblk, r, b0, b1);
       if (!warp_wait(s.acc_full, use & 1u, s.abort, p.timeout_ns)) goto done;
       tc_fence_after();
-      float* out = p.part + (static_cast<size_t>(u) * 128 + row) * p.N;
-      for (int c = half; c < nchunks; c += 2) {
-        uint32_t v[32];
-        tmem_ld32(tmem + lane_base + static_cast<uint32_t>(c * 32), v);
-        tmem_ld_wait(v);
-        if (c * 32 + 32 <= p.N) {
-          float4* o4 = reinterpret_cast<float4*>(out + c * 32);
+      for (int j = 0; j < nblk; ++j) {
+        float* out = p.part + (static_cast<size_t>((mblk0 + j) * p.R + r) * 128 + row) * p.N;
+        for (int c = half; c < nchunks; c += 2) {
+          uint32_t v[32];
+          tmem_ld32(tmem + lane_base + static_cast<uint32_t>(j * 256 + c * 32), v);
+          tmem_ld_wait(v);
+          if (c * 32 + 32 <= p.N) {
+            float4* o4 = reinterpret_cast<float4*>(out + c * 32);
 #pragma unroll
-          for (int j = 0; j < 8; ++j)
-            o4[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
-                                __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
-        } else {
+            for (int k = 0; k < 8; ++k)
+              o4[k] = make_float4(__uint_as_float(v[4 * k]), __uint_as_float(v[4 * k + 1]),
+                                  __uint_as_float(v[4 * k + 2]), __uint_as_float(v[4 * k + 3]));
+          } else {
 #pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (c * 32 + j < p.N) out[c * 32 + j] = __uint_as_float(v[j]);
+            for (int k = 0; k < 32; ++k)
+              if (c * 32 + k < p.N) out[c * 32 + k] = __uint_as_float(v[k]);
+          }
         }
       }
       tc_fence_before();
@@ -518,19 +542,35 @@ done:
   if (*s.abort && threadIdx.x == 0) atomicOr(p.status, DEV_ERR_PIPE_TIMEOUT);
   if (warp == 2) {
     tc_fence_after();
-    tmem_dealloc(tmem, 256);
+    tmem_dealloc(tmem, 512);
   }
 }
 
-// dW[m][n] = sum over the b ranges of m's block, in range order.
-__global__ void __launch_bounds__(256) bwd_wgrad_reduce_kernel(const float* part, float* dW, int M, int N, int R) {
-  const int idx = blockIdx.x * 256 + threadIdx.x;
-  if (idx >= M * N) return;
-  const int m = idx / N, n = idx - m * N;
-  const int mblk = m >> 7, row = m & 127;
+// dW[m][n] = sum over the b ranges of m's block.  32 outputs per CTA, 8
+// threads per output each summing every 8th range, then the 8 sums in order:
+// a fixed order, so the result repeats bit for bit.
+constexpr int WG_RED_OUT = 32, WG_RED_SPLIT = 8;
+__global__ void __launch_bounds__(WG_RED_OUT* WG_RED_SPLIT)
+    bwd_wgrad_reduce_kernel(const float* part, float* dW, int M, int N, int R) {
+  __shared__ float red[WG_RED_SPLIT][WG_RED_OUT + 1];
+  const int o = blockIdx.x * WG_RED_OUT + threadIdx.x;
+  const bool ok = o < M * N;
   float acc = 0.f;
-  for (int r = 0; r < R; ++r) acc += part[(static_cast<size_t>(mblk * R + r) * 128 + row) * N + n];
-  dW[idx] = acc;
+  if (ok) {
+    const int m = o / N, n = o - m * N;
+    const int mblk = m >> 7, row = m & 127;
+#pragma unroll 4
+    for (int r = threadIdx.y; r < R; r += WG_RED_SPLIT)
+      acc += part[(static_cast<size_t>(mblk * R + r) * 128 + row) * N + n];
+  }
+  red[threadIdx.y][threadIdx.x] = acc;
+  __syncthreads();
+  if (threadIdx.y == 0 && ok) {
+    float t = 0.f;
+#pragma unroll
+    for (int k = 0; k < WG_RED_SPLIT; ++k) t += red[k][threadIdx.x];
+    dW[o] = t;
+  }
 }
 
 }  // namespace
@@ -543,7 +583,7 @@ constexpr size_t SMEM_ALIGN_PAD = 1024;
 int bwd_segsum_chunks(int n_cand, int n_users, int ND, int num_sms) {
   const int slices = (ND + BWD_SEG_SLICE - 1) / BWD_SEG_SLICE;
   const long long tasks = static_cast<long long>(n_users) * slices;
-  const long long target = 2ll * num_sms;
+  const long long target = 8ll * num_sms;  // enough threads per SM to keep HBM busy
   int nch = tasks >= target ? 1 : static_cast<int>((target + tasks - 1) / tasks);
   const int cap = n_cand / (16 * n_users);  // at least ~16 candidates per chunk
   if (nch > cap) nch = cap;
@@ -602,20 +642,27 @@ cudaError_t launch_bwd_act(const CUtensorMap& tmX, const CUtensorMap& tmW, const
 }
 
 size_t bwd_wgrad_smem(const WgradParams& p) {
-  return SMEM_ALIGN_PAD + static_cast<size_t>(BWD_WG_STAGES) * wg_stage_bytes(p.nb) +
-         sizeof(uint64_t) * (2 * BWD_WG_STAGES + 2) + 2 * sizeof(uint32_t);
+  return SMEM_ALIGN_PAD + static_cast<size_t>(p.stages) * wg_stage_bytes(p.mg, p.nb) +
+         sizeof(uint64_t) * (2 * p.stages + 2) + 2 * sizeof(uint32_t);
 }
 
 bool bwd_wgrad_configure(WgradParams* p, int num_sms, size_t max_smem) {
   if (p->B < 1 || p->M < 1 || p->D < 1 || p->N < 1 || p->N > 256) return false;
   p->n_mblk = (p->M + 127) / 128;
-  int R = num_sms / p->n_mblk;
+  // One m block per unit: grouping two blocks per unit (one G load serving
+  // both) doubles the b ranges and so the fp32 partials, and measured slower
+  // at the 70:1 shape (dW_c: the second read of dY mostly hits L2 anyway).
+  p->mg = 1;
+  p->n_mgrp = (p->n_mblk + p->mg - 1) / p->mg;
+  int R = num_sms / p->n_mgrp;
   if (R < 1) R = 1;
   if (R > p->B) R = p->B;
   p->R = R;
   p->dc = (p->D + 63) / 64;
   p->n_mma = (p->N + 15) / 16 * 16;
   p->nb = (p->n_mma + 63) / 64;
+  p->stages = BWD_WG_MAX_STAGES;
+  while (p->stages > 2 && bwd_wgrad_smem(*p) > max_smem) --p->stages;
   return bwd_wgrad_smem(*p) <= max_smem;
 }
 
@@ -630,12 +677,13 @@ cudaError_t launch_bwd_wgrad(const CUtensorMap& tmA, const CUtensorMap& tmG, con
   cudaError_t e =
       cudaFuncSetAttribute(bwd_wgrad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  const int units = p.n_mblk * p.R;
+  const int units = p.n_mgrp * p.R;
   bwd_wgrad_kernel<<<units < num_sms ? units : num_sms, BWD_THREADS, smem, s>>>(tmA, tmG, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int total = p.M * p.N;
-  bwd_wgrad_reduce_kernel<<<(total + 255) / 256, 256, 0, s>>>(p.part, dW, p.M, p.N, p.R);
+  bwd_wgrad_reduce_kernel<<<(total + WG_RED_OUT - 1) / WG_RED_OUT, dim3(WG_RED_OUT, WG_RED_SPLIT), 0, s>>>(
+      p.part, dW, p.M, p.N, p.R);
   e = cudaGetLastError();
   if (e == cudaSuccess) *launches += 2;
   return e;

@@ -56,3 +56,15 @@ def test_attention_counts_at_70to1():
     assert abs(f - 4 * 1024 * 8 * 32 * 2048 * 128) < 1
     b = acc.attn_bytes(c["n_cand"], c["H"], c["Lq"], c["d"], c["n_users"] * c["Lkv"])
     assert abs(b / 1e6 - 260.05) < 0.1
+
+
+def test_lce_backward_counts_at_70to1():
+    """The backward's products: twice the forward's FLOPs (each forward GEMM has
+    a data-gradient and a weight-gradient product); bytes counted by hand."""
+    fl = acc.lce_backward_flops(1024, 15, 381, 243, 256, 192)
+    assert fl == 2 * acc.lce_flops(1024, 15, 381, 243, 256, 192)
+    assert abs(fl - 50.046e9) < 0.01e9
+    dY = 1024 * 192 * 256 * 2
+    inputs = (15 * 381 * 256 + 1024 * 243 * 256 + 381 * 192 + 243 * 192) * 2 + 1024 * 4
+    outputs = (15 * 381 * 256 + 1024 * 243 * 256) * 2 + (381 * 192 + 243 * 192 + 192) * 4
+    assert acc.lce_backward_bytes(1024, 15, 381, 243, 256, 192) == dY + inputs + outputs
