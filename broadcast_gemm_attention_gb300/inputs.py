@@ -254,3 +254,10 @@ def make_lce_grad(seed: int, n_cand: int, N: int, D: int) -> torch.Tensor:
     forward inputs' draws)."""
     rng = np.random.Generator(np.random.PCG64(seed + 500))
     return _normal(rng, (n_cand, N, D), 1.0)
+
+
+def make_attn_grad(seed: int, shape) -> torch.Tensor:
+    """Upstream gradient dO = dL/dO for the attention backward: bf16 of the
+    given shape ~ N(0, 1), from its own PCG64 stream (seed + 700)."""
+    rng = np.random.Generator(np.random.PCG64(seed + 700))
+    return _normal(rng, tuple(shape), 1.0)

@@ -18,6 +18,10 @@ Parity status per function (the pins are in ``tests/test_oracle_*.py``):
     = <grad, dx> against the (separately pinned) forward for each input,
     torch fp64 autograd on small cases, closed forms (dY = 0, dY = 1, one
     user), and invariance under candidate permutation;
+  * ``attn_backward`` -- pinned: torch fp64 autograd through softmax
+    attention on K/V gathered by the map (the gather's own backward sums
+    over each user's candidates), closed forms (dO = 0; one key; constant V;
+    sum over keys of dV), candidate permutation, selections, jagged slices;
   * ``attn``      -- pinned: identity map equals torch fp64 SDPA, one user
     equals multi-query SDPA, closed forms (Q=0, constant V, one key, one
     dominant score, empty key range), permutation invariance, jagged slices
@@ -94,9 +98,11 @@ class Oracle:
         lib.ikbo_oracle_attn.argtypes = [p, p, p, p, p, i, i, i, i, i, i, ctypes.c_double, p, i, p, i]
         lib.ikbo_oracle_lce_backward.argtypes = [p, p, p, p, p, p, i, i, i, i, i, i, p, i, p, i, i,
                                                  p, p, p, p, p, i]
+        lib.ikbo_oracle_attn_backward.argtypes = [p, p, p, p, p, p, i, i, i, i, i, i, ctypes.c_double, p, i, p, i,
+                                                  p, p, p, i]
         lib.ikbo_oracle_max_threads.argtypes = []
         for f in (lib.ikbo_oracle_segments, lib.ikbo_oracle_lce, lib.ikbo_oracle_attn,
-                  lib.ikbo_oracle_lce_backward, lib.ikbo_oracle_max_threads):
+                  lib.ikbo_oracle_lce_backward, lib.ikbo_oracle_attn_backward, lib.ikbo_oracle_max_threads):
             f.restype = ctypes.c_int
         self.lib = lib
         self.path = lib_path
@@ -180,6 +186,44 @@ class Oracle:
                 out.pop(k)
         return out
 
+    def attn_backward(self, map_, Q, K, V, dO, kv_offsets=None, n_users: Optional[int] = None,
+                      scale: Optional[float] = None, qpairs: Optional[Sequence] = None,
+                      kvpairs: Optional[Sequence] = None, n_threads: int = 0) -> dict:
+        """Gradients of broadcast attention in fp64 for upstream dO [n_cand, H, Lq, d]:
+        dQ [n_qsel, Lq, d] for the (i, h) ``qpairs`` (all when None); dK, dV
+        [n_kvsel, max_len, d] for the (u, h) ``kvpairs`` (all when None), summed
+        over every candidate of u; rows past a user's key count are 0."""
+        m = _i32(map_)
+        n_cand, H, Lq, d = Q.shape
+        assert tuple(dO.shape) == tuple(Q.shape)
+        if kv_offsets is None:
+            n_users_k, H2, Lkv, d2 = K.shape
+            if n_users is None:
+                n_users = n_users_k
+            offs = None
+            max_len = Lkv
+        else:
+            offs = _i32(kv_offsets)
+            Lkv, H2, d2 = K.shape
+            if n_users is None:
+                n_users = offs.shape[0] - 1
+            max_len = int(np.max(np.diff(offs))) if n_users > 0 else 0
+        assert H2 == H and d2 == d and V.shape == K.shape
+        if scale is None:
+            scale = 1.0 / math.sqrt(d)
+        qs = None if qpairs is None else _i32(qpairs).reshape(-1, 2)
+        ks = None if kvpairs is None else _i32(kvpairs).reshape(-1, 2)
+        n_q = n_cand * H if qs is None else qs.shape[0]
+        n_kv = n_users * H if ks is None else ks.shape[0]
+        out = {"dQ": np.zeros((n_q, Lq, d), np.float64), "dK": np.zeros((n_kv, max(max_len, 0), d), np.float64),
+               "dV": np.zeros((n_kv, max(max_len, 0), d), np.float64)}
+        rc = self.lib.ikbo_oracle_attn_backward(
+            _ptr(m), _ptr(_bits(Q)), _ptr(_bits(K)), _ptr(_bits(V)), _ptr(_bits(dO)), _ptr(offs), n_cand, n_users,
+            H, Lq, Lkv, d, float(scale), _ptr(qs), n_q, _ptr(ks), n_kv, _ptr(out["dQ"]), _ptr(out["dK"]),
+            _ptr(out["dV"]), n_threads)
+        self._check(rc, "attn_backward")
+        return out
+
     def attn(self, map_, Q, K, V, kv_offsets=None, n_users: Optional[int] = None,
              scale: Optional[float] = None, pairs: Optional[Sequence] = None,
              n_threads: int = 0) -> np.ndarray:
@@ -240,6 +284,10 @@ def attn(*a, **k):
 
 def lce_backward(*a, **k):
     return default().lce_backward(*a, **k)
+
+
+def attn_backward(*a, **k):
+    return default().attn_backward(*a, **k)
 
 
 def max_threads() -> int:

@@ -409,3 +409,160 @@ int ikbo_oracle_lce_backward(const int32_t *map, const uint16_t *U, const uint16
     }
     return ORACLE_OK;
 }
+
+/* One query row: p_j = softmax_j(scale * q.k_j) and dS_j = p_j (dP_j - D)
+ * with dP_j = g.v_j and D = sum_j p_j dP_j (= g.o), for the L keys starting
+ * at element row0, row_stride elements apart (scale is applied by callers). */
+static void attn_row(const uint16_t *qr, const uint16_t *gr, const uint16_t *K, const uint16_t *V, size_t row0,
+                     size_t row_stride, int L, int d, double scale, double *p, double *ds)
+{
+    double m = -INFINITY;
+    for (int j = 0; j < L; ++j) {
+        const uint16_t *kr = K + row0 + (size_t)j * row_stride;
+        double dot = 0.0;
+        for (int c = 0; c < d; ++c) dot += bf16_bits_to_double(qr[c]) * bf16_bits_to_double(kr[c]);
+        p[j] = scale * dot;
+        if (p[j] > m) m = p[j];
+    }
+    double l = 0.0;
+    for (int j = 0; j < L; ++j) {
+        p[j] = exp(p[j] - m);
+        l += p[j];
+    }
+    for (int j = 0; j < L; ++j) p[j] /= l;
+    double D = 0.0;
+    for (int j = 0; j < L; ++j) {
+        const uint16_t *vr = V + row0 + (size_t)j * row_stride;
+        double dp = 0.0;
+        for (int c = 0; c < d; ++c) dp += bf16_bits_to_double(gr[c]) * bf16_bits_to_double(vr[c]);
+        ds[j] = dp;
+        D += p[j] * dp;
+    }
+    for (int j = 0; j < L; ++j) ds[j] = p[j] * (ds[j] - D);
+}
+
+/*
+ * Broadcast attention backward (training), from the definition above (the
+ * pages give no backward; the aibriefing paragraph on kernels, compilation
+ * and runtime says the kernels serve training when candidates outnumber
+ * users).  For every candidate i, head h, query q, with u = map[i] and keys
+ * j of user u:
+ *   s_j = scale * Q[i,h,q,:].K[u,h,j,:],  p = softmax(s),  o = sum_j p_j V[u,h,j,:]
+ *   dP_j = dO[i,h,q,:].V[u,h,j,:],  D = dO[i,h,q,:].o,  dS_j = p_j (dP_j - D)
+ *   dQ[i,h,q,:]  = scale * sum_j dS_j K[u,h,j,:]
+ *   dK[u,h,j,:] += scale * dS_j Q[i,h,q,:]      (every candidate of u adds in:
+ *   dV[u,h,j,:] += p_j dO[i,h,q,:]               the broadcast's transpose)
+ * Selections: dQ for (i, h) pairs qpairs[2s], qpairs[2s+1] (all in (i, h)
+ * order when qpairs is NULL and n_qsel == n_cand*H); dK, dV for (u, h) pairs
+ * kvpairs (all in (u, h) order when NULL and n_kvsel == n_users*H).  Outputs
+ * in double: dQ[n_qsel][Lq][d]; dK, dV[n_kvsel][max_len][d], rows past the
+ * user's key count left 0 (max_len = Lkv dense, the longest user jagged).
+ * Candidates and queries are summed in ascending order.
+ */
+int ikbo_oracle_attn_backward(const int32_t *map, const uint16_t *Q, const uint16_t *K, const uint16_t *V,
+                              const uint16_t *dO, const int32_t *kv_offsets, int n_cand, int n_users, int H,
+                              int Lq, int Lkv, int d, double scale, const int32_t *qpairs, int n_qsel,
+                              const int32_t *kvpairs, int n_kvsel, double *dQ, double *dK, double *dV,
+                              int n_threads)
+{
+    if (n_cand < 0 || n_users < 1 || H < 1 || Lq < 1 || d < 1 || n_qsel < 0 || n_kvsel < 0) return ORACLE_BAD_ARG;
+    if (!kv_offsets && Lkv < 0) return ORACLE_BAD_ARG;
+    if (!qpairs && n_qsel != n_cand * H) return ORACLE_BAD_ARG;
+    if (!kvpairs && n_kvsel != n_users * H) return ORACLE_BAD_ARG;
+    for (int i = 0; i < n_cand; ++i)
+        if (map[i] < 0 || map[i] >= n_users) return ORACLE_MAP_OUT_OF_RANGE;
+    int max_len = Lkv;
+    if (kv_offsets) {
+        max_len = 0;
+        for (int u = 0; u < n_users; ++u) {
+            int L = kv_offsets[u + 1] - kv_offsets[u];
+            if (L < 0) return ORACLE_BAD_ARG;
+            if (L > max_len) max_len = L;
+        }
+    }
+    for (int s = 0; s < n_qsel; ++s) {
+        int i = qpairs ? qpairs[2 * s] : s / H, h = qpairs ? qpairs[2 * s + 1] : s % H;
+        if (i < 0 || i >= n_cand || h < 0 || h >= H) return ORACLE_BAD_ARG;
+    }
+    for (int s = 0; s < n_kvsel; ++s) {
+        int u = kvpairs ? kvpairs[2 * s] : s / H, h = kvpairs ? kvpairs[2 * s + 1] : s % H;
+        if (u < 0 || u >= n_users || h < 0 || h >= H) return ORACLE_BAD_ARG;
+    }
+    set_threads(n_threads);
+    int status = ORACLE_OK;
+
+#pragma omp parallel
+    {
+        double *p = (double *)malloc(sizeof(double) * (size_t)(max_len > 0 ? max_len : 1));
+        double *ds = (double *)malloc(sizeof(double) * (size_t)(max_len > 0 ? max_len : 1));
+        if (!p || !ds) {
+#pragma omp atomic write
+            status = ORACLE_NO_MEMORY;
+        }
+        /* dQ */
+#pragma omp for schedule(dynamic, 1)
+        for (int s = 0; s < n_qsel; ++s) {
+            if (!p || !ds) continue;
+            const int i = qpairs ? qpairs[2 * s] : s / H, h = qpairs ? qpairs[2 * s + 1] : s % H;
+            const int u = map[i];
+            int L;
+            size_t row0, row_stride;
+            if (kv_offsets) {
+                L = kv_offsets[u + 1] - kv_offsets[u];
+                row0 = ((size_t)kv_offsets[u] * H + h) * d;
+                row_stride = (size_t)H * d;
+            } else {
+                L = Lkv;
+                row0 = ((size_t)u * H + h) * (size_t)Lkv * d;
+                row_stride = (size_t)d;
+            }
+            for (int q = 0; q < Lq; ++q) {
+                double *out = dQ + ((size_t)s * Lq + q) * d;
+                for (int c = 0; c < d; ++c) out[c] = 0.0;
+                if (L == 0) continue;
+                attn_row(Q + (((size_t)i * H + h) * Lq + q) * d, dO + (((size_t)i * H + h) * Lq + q) * d, K, V, row0,
+                         row_stride, L, d, scale, p, ds);
+                for (int j = 0; j < L; ++j) {
+                    const uint16_t *kr = K + row0 + (size_t)j * row_stride;
+                    for (int c = 0; c < d; ++c) out[c] += scale * ds[j] * bf16_bits_to_double(kr[c]);
+                }
+            }
+        }
+        /* dK, dV: every query of every candidate of u */
+#pragma omp for schedule(dynamic, 1)
+        for (int s = 0; s < n_kvsel; ++s) {
+            if (!p || !ds) continue;
+            const int u = kvpairs ? kvpairs[2 * s] : s / H, h = kvpairs ? kvpairs[2 * s + 1] : s % H;
+            int L;
+            size_t row0, row_stride;
+            if (kv_offsets) {
+                L = kv_offsets[u + 1] - kv_offsets[u];
+                row0 = ((size_t)kv_offsets[u] * H + h) * d;
+                row_stride = (size_t)H * d;
+            } else {
+                L = Lkv;
+                row0 = ((size_t)u * H + h) * (size_t)Lkv * d;
+                row_stride = (size_t)d;
+            }
+            double *gk = dK + (size_t)s * max_len * d, *gv = dV + (size_t)s * max_len * d;
+            for (size_t e = 0; e < (size_t)max_len * d; ++e) gk[e] = gv[e] = 0.0;
+            for (int i = 0; i < n_cand; ++i) {
+                if (map[i] != u || L == 0) continue;
+                for (int q = 0; q < Lq; ++q) {
+                    attn_row(Q + (((size_t)i * H + h) * Lq + q) * d, dO + (((size_t)i * H + h) * Lq + q) * d, K, V,
+                             row0, row_stride, L, d, scale, p, ds);
+                    const uint16_t *qr = Q + (((size_t)i * H + h) * Lq + q) * d;
+                    const uint16_t *gr = dO + (((size_t)i * H + h) * Lq + q) * d;
+                    for (int j = 0; j < L; ++j)
+                        for (int c = 0; c < d; ++c) {
+                            gk[(size_t)j * d + c] += scale * ds[j] * bf16_bits_to_double(qr[c]);
+                            gv[(size_t)j * d + c] += p[j] * bf16_bits_to_double(gr[c]);
+                        }
+                }
+            }
+        }
+        free(p);
+        free(ds);
+    }
+    return status;
+}

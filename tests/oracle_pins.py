@@ -389,3 +389,101 @@ def pin_segments_special_cases(orc):
 
 SEG_PINS = [pin_segments_brute_force, pin_segments_special_cases]
 ALL_PINS = LCE_PINS + ATTN_PINS + SEG_PINS
+
+
+# ===================================================== attention backward
+def _attn_autograd(Q, K, V, dO, m, scale):
+    """torch fp64 autograd through softmax(scale Q K[m]^T) V[m]: the gather's
+    own backward sums the K/V gradients over each user's candidates."""
+    q, k, v = (torch.tensor(f64(t), requires_grad=True) for t in (Q, K, V))
+    idx = m.long()
+    kg, vg = k[idx], v[idx]                       # [n_cand, H, L, d]
+    p = torch.softmax(scale * torch.matmul(q, kg.transpose(-1, -2)), dim=-1)
+    o = torch.matmul(p, vg)
+    (o * torch.tensor(f64(dO))).sum().backward()
+    return q.grad.numpy(), k.grad.numpy(), v.grad.numpy()
+
+
+def pin_attn_bwd_autograd(orc):
+    """Dense K/V, permuted map with a user that has no candidates (its dK, dV
+    must be 0): every gradient equals torch fp64 autograd."""
+    x = gen.make_attn("pin", 41, n_cand=9, n_users=4, H=2, Lq=3, d=16, Lkv=7,
+                      explicit_map=[2, 0, 2, 1, 0, 2, 1, 0, 2])
+    dO = gen.make_attn_grad(41, x.Q.shape)
+    g = orc.attn_backward(x.map, x.Q, x.K, x.V, dO)
+    dq, dk, dv = _attn_autograd(x.Q, x.K, x.V, dO, x.map, 1.0 / math.sqrt(16))
+    np.testing.assert_allclose(g["dQ"].reshape(dq.shape), dq, rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(g["dK"].reshape(dk.shape), dk, rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(g["dV"].reshape(dv.shape), dv, rtol=1e-10, atol=1e-12)
+    assert not np.any(g["dK"].reshape(dk.shape)[3]) and not np.any(g["dV"].reshape(dv.shape)[3])
+
+
+def pin_attn_bwd_closed_forms(orc):
+    """dO = 0: zero gradients.  One key: p = 1, so dQ = dK = 0 and dV[u] = sum
+    of dO over u's candidates and queries.  Constant V rows: dP is constant
+    along keys, dS = 0, so dQ = dK = 0.  Always: sum_j dV[u,h,j] = sum of dO
+    over u's candidates and queries (each row of P sums to 1)."""
+    x = gen.make_attn("pin", 43, n_cand=6, n_users=2, H=2, Lq=4, d=8, Lkv=5, explicit_map=[0, 1, 1, 0, 1, 1])
+    dO = gen.make_attn_grad(43, x.Q.shape)
+    z = orc.attn_backward(x.map, x.Q, x.K, x.V, torch.zeros_like(dO))
+    for k, v in z.items():
+        assert not np.any(v), k
+    g = orc.attn_backward(x.map, x.Q, x.K, x.V, dO)
+    m = x.map.numpy()
+    dOs = np.stack([f64(dO)[m == u].sum(axis=(0, 2)) for u in range(2)])       # [u, H, d]
+    np.testing.assert_allclose(g["dV"].reshape(2, 2, 5, 8).sum(axis=2), dOs, rtol=1e-12, atol=1e-12)
+    one = orc.attn_backward(x.map, x.Q, x.K[:, :, :1].contiguous(), x.V[:, :, :1].contiguous(), dO)
+    assert np.allclose(one["dQ"], 0, atol=1e-13) and np.allclose(one["dK"], 0, atol=1e-13)
+    np.testing.assert_allclose(one["dV"].reshape(2, 2, 8), dOs, rtol=1e-12, atol=1e-12)
+    Vc = x.V[:, :, :1].expand(-1, -1, 5, -1).contiguous()
+    c = orc.attn_backward(x.map, x.Q, x.K, Vc, dO)
+    assert np.allclose(c["dQ"], 0, atol=1e-12) and np.allclose(c["dK"], 0, atol=1e-12)
+
+
+def pin_attn_bwd_permutation(orc):
+    """Permuting candidates (map, Q and dO together) permutes dQ and leaves dK
+    and dV unchanged."""
+    x = gen.make_attn("pin", 47, n_cand=8, n_users=3, H=2, Lq=2, d=8, Lkv=6, map_kind="permuted")
+    dO = gen.make_attn_grad(47, x.Q.shape)
+    g = orc.attn_backward(x.map, x.Q, x.K, x.V, dO)
+    p = torch.from_numpy(np.random.default_rng(4).permutation(8))
+    gp = orc.attn_backward(x.map[p], x.Q[p], x.K, x.V, dO[p])
+    np.testing.assert_array_equal(gp["dQ"].reshape(8, 2, 2, 8), g["dQ"].reshape(8, 2, 2, 8)[p.numpy()])
+    for k in ("dK", "dV"):
+        np.testing.assert_allclose(gp[k], g[k], rtol=1e-12, atol=1e-13, err_msg=k)
+
+
+def pin_attn_bwd_jagged_and_selection(orc):
+    """Jagged K/V: each user's dK/dV slice equals a dense single-user case
+    (its candidates only); selections return exactly those rows."""
+    lens = [4, 0, 7]
+    x = gen.make_attn("pin", 53, n_cand=6, n_users=3, H=2, Lq=2, d=8, explicit_map=[2, 0, 1, 2, 0, 2],
+                      explicit_lengths=lens)
+    dO = gen.make_attn_grad(53, x.Q.shape)
+    g = orc.attn_backward(x.map, x.Q, x.K, x.V, dO, kv_offsets=x.kv_offsets)
+    offs = x.kv_offsets.tolist()
+    m = x.map.numpy()
+    for u in range(3):
+        a, b = offs[u], offs[u + 1]
+        sel = np.nonzero(m == u)[0]
+        gk = g["dK"].reshape(3, 2, 7, 8)[u]
+        gv = g["dV"].reshape(3, 2, 7, 8)[u]
+        if b == a or len(sel) == 0:
+            assert not np.any(gk) and not np.any(gv)
+            continue
+        Kd = x.K[a:b].permute(1, 0, 2).unsqueeze(0).contiguous()
+        Vd = x.V[a:b].permute(1, 0, 2).unsqueeze(0).contiguous()
+        s = orc.attn_backward(torch.zeros(len(sel), dtype=torch.int32), x.Q[sel], Kd, Vd, dO[sel])
+        np.testing.assert_allclose(gk[:, :b - a], s["dK"].reshape(2, b - a, 8), rtol=1e-12, atol=1e-13)
+        np.testing.assert_allclose(gv[:, :b - a], s["dV"].reshape(2, b - a, 8), rtol=1e-12, atol=1e-13)
+        np.testing.assert_allclose(g["dQ"].reshape(6, 2, 2, 8)[sel], s["dQ"].reshape(len(sel), 2, 2, 8),
+                                   rtol=1e-12, atol=1e-13)
+        assert not np.any(gk[:, b - a:]) and not np.any(gv[:, b - a:])
+    part = orc.attn_backward(x.map, x.Q, x.K, x.V, dO, kv_offsets=x.kv_offsets, qpairs=[[4, 1], [0, 0]],
+                             kvpairs=[[2, 1]])
+    assert np.array_equal(part["dQ"], g["dQ"][[4 * 2 + 1, 0]])
+    assert np.array_equal(part["dK"][0], g["dK"][2 * 2 + 1])
+
+
+ATTN_BWD_PINS = [pin_attn_bwd_autograd, pin_attn_bwd_closed_forms, pin_attn_bwd_permutation,
+                 pin_attn_bwd_jagged_and_selection]

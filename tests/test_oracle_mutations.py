@@ -6,7 +6,7 @@ import os
 import pytest
 
 import oracle
-from oracle_pins import ATTN_PINS, LCE_BWD_PINS, LCE_PINS, SEG_PINS
+from oracle_pins import ATTN_BWD_PINS, ATTN_PINS, LCE_BWD_PINS, LCE_PINS, SEG_PINS
 
 MUTATIONS = {
     # LCE
@@ -29,13 +29,26 @@ MUTATIONS = {
     "bwd_dwc_sign": ("dWc[(size_t)(k - K_u) * N + n] = acc;", "dWc[(size_t)(k - K_u) * N + n] = -acc;", LCE_BWD_PINS),
     "bwd_dc_drop_last_n": ("for (int n = 0; n < N; ++n)\n                    acc += bf16_bits_to_double(Wc",
                            "for (int n = 0; n < N - 1; ++n)\n                    acc += bf16_bits_to_double(Wc", LCE_BWD_PINS),
+    # attention backward
+    "abwd_no_D": ("for (int j = 0; j < L; ++j) ds[j] = p[j] * (ds[j] - D);", "for (int j = 0; j < L; ++j) ds[j] = p[j] * ds[j];", ATTN_BWD_PINS),
+    "abwd_dq_no_scale": ("for (int c = 0; c < d; ++c) out[c] += scale * ds[j] * bf16_bits_to_double(kr[c]);",
+                         "for (int c = 0; c < d; ++c) out[c] += ds[j] * bf16_bits_to_double(kr[c]);", ATTN_BWD_PINS),
+    "abwd_dk_from_dO": ("gk[(size_t)j * d + c] += scale * ds[j] * bf16_bits_to_double(qr[c]);",
+                        "gk[(size_t)j * d + c] += scale * ds[j] * bf16_bits_to_double(gr[c]);", ATTN_BWD_PINS),
+    "abwd_dv_uses_ds": ("gv[(size_t)j * d + c] += p[j] * bf16_bits_to_double(gr[c]);",
+                        "gv[(size_t)j * d + c] += ds[j] * bf16_bits_to_double(gr[c]);", ATTN_BWD_PINS),
+    "abwd_dkdv_every_candidate": ("if (map[i] != u || L == 0) continue;", "if (L == 0) continue;", ATTN_BWD_PINS),
+    "abwd_dp_from_k": ("const uint16_t *vr = V + row0 + (size_t)j * row_stride;\n        double dp",
+                       "const uint16_t *vr = K + row0 + (size_t)j * row_stride;\n        double dp", ATTN_BWD_PINS),
     # attention
     "attn_no_scale": ("sc[j] = scale * dot;", "sc[j] = dot;", ATTN_PINS),
     "attn_no_normalise": ("for (int c = 0; c < d; ++c) orow[c] /= l;", "", ATTN_PINS),
     "attn_v_from_k": ("const uint16_t *vrow = V + row0", "const uint16_t *vrow = K + row0", ATTN_PINS),
-    "attn_user_is_candidate": ("int u = map[i];\n            int L;", "int u = i % n_users;\n            int L;", ATTN_PINS),
+    "attn_user_is_candidate": ("int h = pairs ? pairs[2 * s + 1] : s % H;\n            int u = map[i];\n            int L;",
+                               "int h = pairs ? pairs[2 * s + 1] : s % H;\n            int u = i % n_users;\n            int L;", ATTN_PINS),
     "attn_drop_last_key": ("for (int j = 0; j < L; ++j) {\n                    const uint16_t *vrow", "for (int j = 0; j < L - 1; ++j) {\n                    const uint16_t *vrow", ATTN_PINS),
-    "attn_jagged_stride": ("row_stride = (size_t)H * d;", "row_stride = (size_t)d;", ATTN_PINS),
+    "attn_jagged_stride": ("row_stride = (size_t)H * d;\n            } else {\n                L = Lkv;\n                row0 = ((size_t)u * H + h) * (size_t)Lkv * d;\n                row_stride = (size_t)d;\n            }\n            for (int q = 0; q < Lq; ++q) {\n                const uint16_t *qrow",
+                           "row_stride = (size_t)d;\n            } else {\n                L = Lkv;\n                row0 = ((size_t)u * H + h) * (size_t)Lkv * d;\n                row_stride = (size_t)d;\n            }\n            for (int q = 0; q < Lq; ++q) {\n                const uint16_t *qrow", ATTN_PINS),
     # segments
     "seg_unstable": ("for (int i = 0; i < n_cand; ++i) {       /* ascending i: stable */", "for (int i = n_cand - 1; i >= 0; --i) {", SEG_PINS),
     # every planted mistake keeps its writes inside the caller's buffers

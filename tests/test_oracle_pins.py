@@ -4,7 +4,7 @@ import pytest
 import torch
 
 import oracle
-from oracle_pins import ATTN_PINS, LCE_BWD_PINS, LCE_PINS, SEG_PINS
+from oracle_pins import ATTN_BWD_PINS, ATTN_PINS, LCE_BWD_PINS, LCE_PINS, SEG_PINS
 from broadcast_gemm_attention_gb300 import inputs as gen
 
 
@@ -15,6 +15,11 @@ def test_lce_pin(orc, pin):
 
 @pytest.mark.parametrize("pin", LCE_BWD_PINS, ids=lambda f: f.__name__)
 def test_lce_backward_pin(orc, pin):
+    pin(orc)
+
+
+@pytest.mark.parametrize("pin", ATTN_BWD_PINS, ids=lambda f: f.__name__)
+def test_attn_backward_pin(orc, pin):
     pin(orc)
 
 
