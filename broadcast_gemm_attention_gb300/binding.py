@@ -44,6 +44,7 @@ SIGNATURES = {
     "ikbo_lce_forward_noalloc": (_i, [_vp, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp]),
     "ikbo_lce_backward": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp]),
     "ikbo_attn_forward": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, ctypes.c_float, _vp]),
+    "ikbo_attn_backward": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, ctypes.c_float, _vp]),
     "ikbo_attn_self_target_forward": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, ctypes.c_float, _vp]),
     "ikbo_plan_get_status": (_i, [_vp, _vp]),
     "ikbo_plan_set_debug": (_i, [_vp, ctypes.c_uint]),
@@ -249,6 +250,30 @@ def ikbo_attn_forward(plan: int, Q: torch.Tensor, K: torch.Tensor, V: torch.Tens
                                     _dev(O, bf, "O"), Lkv, d, float(scale), _stream(stream)), "ikbo_attn_forward")
 
 
+def ikbo_attn_backward(plan: int, Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, O: torch.Tensor,
+                       dO: torch.Tensor, kv_offsets: Optional[torch.Tensor], dQ: torch.Tensor, dK: torch.Tensor,
+                       dV: torch.Tensor, scale: Optional[float] = None, stream=None) -> None:
+    """Gradients of broadcast attention for upstream dO: dQ (Q's layout), and dK,
+    dV (K's layout) summed over each user's candidates; all bf16, overwritten."""
+    bf = torch.bfloat16
+    d = Q.shape[-1]
+    if kv_offsets is None:
+        Lkv = K.shape[2]
+        optr = None
+    else:
+        Lkv = K.shape[0]
+        optr = _dev(kv_offsets, torch.int32, "kv_offsets")
+    if K.shape != V.shape or O.shape != Q.shape or dO.shape != Q.shape or dQ.shape != Q.shape or \
+            dK.shape != K.shape or dV.shape != V.shape:
+        raise ValueError("inconsistent attention shapes")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    _check(load().ikbo_attn_backward(plan, _dev(Q, bf, "Q"), _dev(K, bf, "K"), _dev(V, bf, "V"), _dev(O, bf, "O"),
+                                     _dev(dO, bf, "dO"), optr, _dev(dQ, bf, "dQ"), _dev(dK, bf, "dK"),
+                                     _dev(dV, bf, "dV"), Lkv, d, float(scale), _stream(stream)),
+           "ikbo_attn_backward")
+
+
 def ikbo_attn_self_target_forward(plan: int, Q: torch.Tensor, Q_user: torch.Tensor, K: torch.Tensor,
                                   V: torch.Tensor, kv_offsets: Optional[torch.Tensor], O: torch.Tensor,
                                   O_user: torch.Tensor, scale: Optional[float] = None, stream=None) -> None:
@@ -332,6 +357,9 @@ class Plan:
 
     def attn_forward(self, Q, K, V, kv_offsets, O, scale=None, stream=None):
         ikbo_attn_forward(self.handle, Q, K, V, kv_offsets, O, scale, stream)
+
+    def attn_backward(self, Q, K, V, O, dO, kv_offsets, dQ, dK, dV, scale=None, stream=None):
+        ikbo_attn_backward(self.handle, Q, K, V, O, dO, kv_offsets, dQ, dK, dV, scale, stream)
 
     def attn_self_target_forward(self, Q, Q_user, K, V, kv_offsets, O, O_user, scale=None, stream=None):
         ikbo_attn_self_target_forward(self.handle, Q, Q_user, K, V, kv_offsets, O, O_user, scale, stream)

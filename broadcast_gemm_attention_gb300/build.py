@@ -22,7 +22,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libikbo.so")
-SOURCES = ["seg.cu", "lce.cu", "lce_noalloc.cu", "lce_bwd.cu", "attn.cu", "api.cu"]
+SOURCES = ["seg.cu", "lce.cu", "lce_noalloc.cu", "lce_bwd.cu", "attn.cu", "attn_bwd.cu", "api.cu"]
 HEADERS = ["ptx.cuh", "ikbo_internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -35,6 +35,10 @@ bool bwd_wgrad_configure(WgradParams* p, int num_sms, size_t max_smem);
 size_t bwd_wgrad_part_elems(const WgradParams& p);
 cudaError_t launch_bwd_wgrad(const CUtensorMap& tmA, const CUtensorMap& tmG, const WgradParams& p, float* dW,
                              int num_sms, cudaStream_t s, int* launches);
+size_t attn_bwd_smem_bytes();
+cudaError_t launch_attn_backward(const CUtensorMap& tmQ, const CUtensorMap& tmDO, const CUtensorMap& tmK,
+                                 const CUtensorMap& tmV, const AttnBwdParams& p, int grid, cudaStream_t s,
+                                 int* launches);
 }  // namespace ikbo
 
 using namespace ikbo;
@@ -69,6 +73,13 @@ struct ikbo_plan_s {
   size_t bwd_seg_elems = 0;
   float* d_bwd_wpart = nullptr;
   size_t bwd_wpart_elems = 0;
+  // attention backward workspaces
+  float* d_abwd_lse = nullptr;
+  size_t abwd_lse_elems = 0;
+  float* d_abwd_drow = nullptr;
+  size_t abwd_drow_elems = 0;
+  int32_t* d_abwd_blk = nullptr;
+  size_t abwd_blk_elems = 0;
   uint32_t epoch = 0;
   uint32_t debug = 0;
   uint64_t timeout_ns = 2000000000ull;
@@ -145,6 +156,9 @@ void free_plan(ikbo_plan_t p) {
   cudaFree(p->d_bwd_Sb);
   cudaFree(p->d_bwd_seg);
   cudaFree(p->d_bwd_wpart);
+  cudaFree(p->d_abwd_lse);
+  cudaFree(p->d_abwd_drow);
+  cudaFree(p->d_abwd_blk);
   delete p;
 }
 
@@ -285,9 +299,86 @@ ikbo_status_t attn_launch(ikbo_plan_t p, const void* Q, const void* Q_user, cons
 }
 }  // namespace
 
+namespace {
+ikbo_status_t attn_backward_launch(ikbo_plan_t p, const void* Q, const void* K, const void* V, const void* O,
+                                   const void* dO, const int32_t* d_kv_offsets, void* dQ, void* dK, void* dV, int Lkv,
+                                   int d, float scale, cudaStream_t stream) {
+  if (!p) return IKBO_ERR_INVALID_ARG;
+  if (!p->planned) return IKBO_ERR_NOT_PLANNED;
+  const void* ptrs[] = {Q, K, V, O, dO, dQ, dK, dV};
+  for (const void* q : ptrs)
+    if (!q || !aligned16(q)) return IKBO_ERR_INVALID_ARG;
+  if (d != ATT_D) return IKBO_ERR_UNSUPPORTED;
+  if (Lkv < 1 || !(scale > 0.f) || !std::isfinite(scale)) return IKBO_ERR_INVALID_ARG;
+  if (attn_bwd_smem_bytes() > p->max_smem) return IKBO_ERR_UNSUPPORTED;
+  const size_t rows = static_cast<size_t>(p->n_cand) * p->H * p->Lq;
+  if (grow(&p->d_abwd_lse, &p->abwd_lse_elems, rows) != cudaSuccess ||
+      grow(&p->d_abwd_drow, &p->abwd_drow_elems, rows) != cudaSuccess ||
+      grow(&p->d_abwd_blk, &p->abwd_blk_elems, static_cast<size_t>(p->n_users) + 1) != cudaSuccess)
+    return IKBO_ERR_CUDA;
+
+  AttnBwdParams bp;
+  std::memset(&bp, 0, sizeof(bp));
+  bp.perm = p->d_perm;
+  bp.work = p->d_work;
+  bp.n_units = p->d_n_units;
+  bp.offsets = p->d_offsets;
+  bp.kv_offsets = d_kv_offsets;
+  bp.blk_prefix = p->d_abwd_blk;
+  bp.O = static_cast<const uint16_t*>(O);
+  bp.dO = static_cast<const uint16_t*>(dO);
+  bp.dQ = static_cast<uint16_t*>(dQ);
+  bp.dK = static_cast<uint16_t*>(dK);
+  bp.dV = static_cast<uint16_t*>(dV);
+  bp.lse = p->d_abwd_lse;
+  bp.Drow = p->d_abwd_drow;
+  bp.status = p->d_status;
+  bp.n_cand = p->n_cand;
+  bp.n_users = p->n_users;
+  bp.H = p->H;
+  bp.Lq = p->Lq;
+  bp.Lkv = Lkv;
+  bp.cands_per_tile = ATT_BM / p->Lq;
+  bp.scale = scale;
+  bp.scale_log2 = scale * 1.4426950408889634f;
+  bp.timeout_ns = p->timeout_ns;
+
+  // the forward's layouts: Q, dO [n_cand][H][Lq][d] one box per candidate;
+  // K, V dense [n_users][H][Lkv][d] or jagged [Lkv][H][d], 128-row boxes
+  const uint64_t H = static_cast<uint64_t>(p->H), Lq = static_cast<uint64_t>(p->Lq);
+  CUtensorMap tmQ, tmDO, tmK, tmV;
+  const uint64_t qd[4] = {ATT_D, Lq, H, static_cast<uint64_t>(p->n_cand)};
+  const uint64_t qs[3] = {ATT_D * 2, Lq * ATT_D * 2, H * Lq * ATT_D * 2};
+  const uint32_t qbox[4] = {64, static_cast<uint32_t>(p->Lq), 1, 1};
+  if (!encode_bf16(&tmQ, Q, 4, qd, qs, qbox) || !encode_bf16(&tmDO, dO, 4, qd, qs, qbox)) return IKBO_ERR_CUDA;
+  if (d_kv_offsets) {
+    const uint64_t kd[3] = {ATT_D, H, static_cast<uint64_t>(Lkv)};
+    const uint64_t ks[2] = {ATT_D * 2, H * ATT_D * 2};
+    const uint32_t kbox[3] = {64, 1, ATT_BN};
+    if (!encode_bf16(&tmK, K, 3, kd, ks, kbox) || !encode_bf16(&tmV, V, 3, kd, ks, kbox)) return IKBO_ERR_CUDA;
+  } else {
+    const uint64_t L = static_cast<uint64_t>(Lkv);
+    const uint64_t kd[4] = {ATT_D, L, H, static_cast<uint64_t>(p->n_users)};
+    const uint64_t ks[3] = {ATT_D * 2, L * ATT_D * 2, H * L * ATT_D * 2};
+    const uint32_t kbox[4] = {64, ATT_BN, 1, 1};
+    if (!encode_bf16(&tmK, K, 4, kd, ks, kbox) || !encode_bf16(&tmV, V, 4, kd, ks, kbox)) return IKBO_ERR_CUDA;
+  }
+  int launches = 0;
+  const cudaError_t e = launch_attn_backward(tmQ, tmDO, tmK, tmV, bp, p->num_sms, stream, &launches);
+  p->launches += static_cast<uint64_t>(launches);
+  return e == cudaSuccess ? IKBO_OK : IKBO_ERR_CUDA;
+}
+}  // namespace
+
 extern "C" {
 
-int ikbo_version(void) { return 104; }
+int ikbo_version(void) { return 105; }
+
+ikbo_status_t ikbo_attn_backward(ikbo_plan_t p, const void* Q, const void* K, const void* V, const void* O,
+                                 const void* dO, const int32_t* d_kv_offsets, void* dQ, void* dK, void* dV, int Lkv,
+                                 int d, float scale, cudaStream_t stream) {
+  return attn_backward_launch(p, Q, K, V, O, dO, d_kv_offsets, dQ, dK, dV, Lkv, d, scale, stream);
+}
 
 const char* ikbo_status_string(ikbo_status_t s) {
   switch (s) {

@@ -212,4 +212,34 @@ struct AttnParams {
   int n_self, self_tiles, self_rows, Lq_u;  // self_rows = query rows per self tile (<= 128)
 };
 
+// ------------------------------------------------- attention backward
+// dQ kernel (per work-list unit = one 128-row query tile): pass 1 over the
+// user's key tiles forms each row's log-sum-exp; pass 2 recomputes S, forms
+// dP = dO V^T, dS = P (dP - D) scale into TMEM and accumulates dQ += dS K.
+// It also stores LSE and D = rowsum(dO * O) for the dK/dV kernel.
+// dK/dV kernel (per (user, head, 128-key block)): over every query tile of
+// the user's candidates, S^T = K Q^T and dP^T = V dO^T with keys on TMEM
+// lanes, then dV += P^T dO and dK += dS^T Q accumulate in TMEM.
+constexpr int ABWD_THREADS = 256;  // warp 0 TMA, 1 MMA + TMEM, 2-3 idle, 4-7 softmax / epilogue
+
+struct AttnBwdParams {
+  const int32_t* perm;
+  const int32_t* work;       // the plan's work list [n_units][4]
+  const int32_t* n_units;
+  const int32_t* offsets;    // the plan's user segment offsets [n_users + 1]
+  const int32_t* kv_offsets; // jagged K/V or null (dense)
+  const int32_t* blk_prefix; // dK/dV kernel: [n_users + 1] prefix of ceil(L_u / 128)
+  const uint16_t* O;         // forward output [n_cand][H][Lq][d]
+  const uint16_t* dO;        // [n_cand][H][Lq][d]
+  uint16_t* dQ;              // [n_cand][H][Lq][d]
+  uint16_t* dK;              // like K
+  uint16_t* dV;              // like V
+  float* lse;                // [n_cand][H][Lq], log2 domain of scale * log2(e) * q.k
+  float* Drow;               // [n_cand][H][Lq]
+  uint32_t* status;
+  int n_cand, n_users, H, Lq, Lkv, cands_per_tile;
+  float scale, scale_log2;
+  uint64_t timeout_ns;
+};
+
 }  // namespace ikbo

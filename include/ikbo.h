@@ -230,6 +230,32 @@ ikbo_status_t ikbo_attn_self_target_forward(ikbo_plan_t p, const void* Q, const 
                                             const void* V, const int32_t* d_kv_offsets, void* O, void* O_user,
                                             int Lq_u, int Lkv, int d, float scale, cudaStream_t stream);
 
+/* Broadcast attention backward for training (aibriefing, "Meta Optimizes
+ * Inference for Recommendation Systems": the kernels serve training when
+ * candidates outnumber users; the pages give no backward, so this is the
+ * chain rule of ikbo_attn_forward's definition).  Given the forward's
+ * inputs, its output O and the upstream gradient dO = dL/dO, with the plan's
+ * map, H and Lq, for every candidate i, head h, query q (u = map[i]):
+ *   p = softmax(scale Q K[u]^T), dP = dO V[u]^T, D = rowsum(dO * O),
+ *   dS = p (dP - D)
+ *   dQ[i,h]  = scale dS K[u,h]                          bf16, Q's layout
+ *   dK[u,h]  = scale sum_{i : map[i] = u} dS_i^T Q[i,h]   bf16, K's layout
+ *   dV[u,h]  = sum_{i : map[i] = u} p_i^T dO[i,h]         bf16, V's layout
+ * so the K/V gradients sum over every candidate of a user, the transpose of
+ * the forward's broadcast; keys of a user with no candidates get 0, queries
+ * of a user with no keys get dQ = 0.
+ *   Q, O, dO bf16 [n_cand][H][Lq][d]; K, V (and dK, dV) dense or jagged
+ *   exactly as in ikbo_attn_forward; all 16-byte aligned, none NULL.
+ * P and dS are rounded to bf16 for the tensor cores (as P is in the
+ * forward); accumulation is fp32.  Gradients are overwritten.  Three
+ * launches; the plan keeps per-row LSE and D (grown on first use, which
+ * allocates synchronously).  Limits: d == 128 (else IKBO_ERR_UNSUPPORTED);
+ * the plan's map values must be in range (a candidate outside is skipped by
+ * the segments, so its dQ is left untouched). */
+ikbo_status_t ikbo_attn_backward(ikbo_plan_t p, const void* Q, const void* K, const void* V, const void* O,
+                                 const void* dO, const int32_t* d_kv_offsets, void* dQ, void* dK, void* dV, int Lkv,
+                                 int d, float scale, cudaStream_t stream);
+
 /* Synchronise `stream`, then return (and clear) the first device-detected
  * error recorded since the last call: IKBO_ERR_MAP_OUT_OF_RANGE,
  * IKBO_ERR_TIMEOUT, IKBO_ERR_INTERNAL, or IKBO_OK. */
