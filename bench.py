@@ -411,6 +411,9 @@ def run_gpu(args):
     lce_backward = None
     if not args.no_backward:
         lce_backward = lce_backward_run(plan, d, x, flush, stream, dev, peaks())
+    attn_backward = None
+    if not args.no_backward:
+        attn_backward = attn_backward_run(plan, d, x, a, O, flush, stream, dev, peaks())
 
     plan.close()
     if rank != 0:
@@ -439,7 +442,7 @@ def run_gpu(args):
         "roofline": roofline, "roofline_lce": roofline_lce,
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": gpu_launches,
         "clocks": clk.summary(), "ablation": ablation, "lce_stages": lce_stages, "self_target": self_target,
-        "lce_backward": lce_backward,
+        "lce_backward": lce_backward, "attn_backward": attn_backward,
     }
     print(json.dumps(out), flush=True)
     if dist:
@@ -578,6 +581,51 @@ def lce_backward_run(plan, d, x, flush, stream, dev, pk, iters=20):
                     "dU = W_u S, dW_u = sum U S^T, db from S; one stream, L2 flushed before each call"}
 
 
+def attn_backward_run(plan, d, x, a, O, flush, stream, dev, pk, iters=20):
+    """ikbo_attn_backward at the request's attention shape (dQ for every
+    candidate, dK / dV summed over each user's candidates) for a seeded
+    upstream gradient dO, after one forward that provides O; median and mean
+    µs over `iters` flushed runs, against the tensor roofline of the five
+    products the backward needs."""
+    import statistics
+    import torch
+    from broadcast_gemm_attention_gb300 import accounting as acc
+    from broadcast_gemm_attention_gb300 import inputs as gen
+    dO = gen.make_attn_grad(1003, tuple(a.Q.shape)).to(dev)
+    dQ = torch.empty_like(d["Q"])
+    dK = torch.empty_like(d["K"])
+    dV = torch.empty_like(d["V"])
+    plan.plan(d["map"], x.n_users, a.H, a.Lq, stream)
+    plan.attn_forward(d["Q"], d["K"], d["V"], None, O, None, stream)
+    ts = []
+    l0 = plan.launches()
+    for k in range(iters + 3):
+        flush()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        plan.attn_backward(d["Q"], d["K"], d["V"], O, dO, None, dQ, dK, dV, None, stream)
+        e.record(stream)
+        torch.cuda.synchronize()
+        if k >= 3:
+            ts.append(s.elapsed_time(e))
+    launches = (plan.launches() - l0) / (iters + 3)
+    st = plan.status()
+    us = 1e3 * statistics.median(ts)
+    lens = [a.Lkv] * a.n_cand
+    fl = acc.attn_backward_flops(a.H, a.Lq, a.d, lens)
+    byt = acc.attn_backward_bytes(a.n_cand, a.H, a.Lq, a.d, a.n_users * a.Lkv)
+    tf = fl / (us * 1e-6) / 1e12
+    return {"us_median": us, "us_mean": 1e3 * statistics.mean(ts), "launches_per_call": launches,
+            "tflops": tf, "gbs": byt / (us * 1e-6) / 1e9,
+            "roofline": {"bound": "tensor", "achieved": tf, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                         "frac": tf / pk["bf16_tflops"],
+                         "algorithmic": f"{fl:.4g} FLOP per call = 10*H*Lq*d*sum_i Lkv (S, dP, dV, dK, dQ)"},
+            "status": "ok" if st == 0 else f"error {st}",
+            "note": "dQ kernel per forward work unit (LSE pass, then dS and dQ += dS K); dK/dV kernel per "
+                    "(user, head, 128-key block) over all of the user's candidates; one stream, L2 flushed "
+                    "before each call"}
+
+
 def self_target_run(plan, d, x, a, O, flush, stream, dev, Lq_u=64, iters=20):
     """The request's target attention plus each user's own Lq_u queries over
     the same K/V: one launch (ikbo_attn_self_target_forward) against two
@@ -674,7 +722,7 @@ def main():
     ap.add_argument("--impl", choices=["ikbo", "reference"], default="ikbo")
     ap.add_argument("--no-ablation", action="store_true")
     ap.add_argument("--no-self-target", action="store_true", help="skip the self + target attention comparison")
-    ap.add_argument("--no-backward", action="store_true", help="skip the LCE backward measurement")
+    ap.add_argument("--no-backward", action="store_true", help="skip the LCE and attention backward measurements")
     ap.add_argument("--sweep", action="store_true", help="shape sweep (LCE and attention) instead of the benchmark")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--lce-schedule", type=int, default=0, choices=[0, 1, 2, 3],

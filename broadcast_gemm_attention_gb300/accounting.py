@@ -71,6 +71,21 @@ def attn_bytes(n_cand: int, H: int, Lq: int, d: int, kv_rows_total: int) -> floa
     return float(BF16 * (2 * n_cand * H * Lq * d + 2 * kv_rows_total * H * d) + I32 * n_cand)
 
 
+def attn_backward_flops(H: int, Lq: int, d: int, kv_len_per_cand) -> float:
+    """The five products of the attention backward per (candidate, head): S
+    recomputed, dP = dO V^T, dV += P^T dO, dK += dS^T Q, dQ = dS K, each
+    2*Lq*L*d multiply-adds -> 10*H*Lq*d*sum_i L_{map[i]} (2.5x the forward).
+    The softmax's element-wise work is not counted."""
+    return 2.5 * attn_flops(H, Lq, d, kv_len_per_cand)
+
+
+def attn_backward_bytes(n_cand: int, H: int, Lq: int, d: int, kv_rows_total: int) -> float:
+    """Q, O, dO read and dQ written once per candidate (bf16); K, V read and
+    dK, dV written once per user; the map read once.  The per-row softmax
+    statistics the kernels keep between passes are not counted."""
+    return float(BF16 * (4 * n_cand * H * Lq * d + 4 * kv_rows_total * H * d) + I32 * n_cand)
+
+
 def attn_intensity_standard(Lq: int, Lkv: int) -> float:
     """FLOP/B of attention on materialised K/V, per (candidate, head).
 

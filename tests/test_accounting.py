@@ -68,3 +68,16 @@ def test_lce_backward_counts_at_70to1():
     inputs = (15 * 381 * 256 + 1024 * 243 * 256 + 381 * 192 + 243 * 192) * 2 + 1024 * 4
     outputs = (15 * 381 * 256 + 1024 * 243 * 256) * 2 + (381 * 192 + 243 * 192 + 192) * 4
     assert acc.lce_backward_bytes(1024, 15, 381, 243, 256, 192) == dY + inputs + outputs
+
+
+def test_attention_backward_counts():
+    """Five products of 2*Lq*L*d multiply-adds each (S, dP, dV, dK, dQ) per
+    (candidate, head), and every tensor of the backward moved once."""
+    H, Lq, d, L = 8, 32, 128, 2048
+    lens = [L] * 70
+    assert acc.attn_backward_flops(H, Lq, d, lens) == 5 * 2 * 2 * Lq * L * d * H * 70 / 2
+    assert acc.attn_backward_flops(H, Lq, d, lens) == 2.5 * acc.attn_flops(H, Lq, d, lens)
+    # Q, O, dO in and dQ out per candidate; K, V in and dK, dV out per user
+    by = acc.attn_backward_bytes(70, H, Lq, d, L)
+    assert by == 2 * (4 * 70 * H * Lq * d + 4 * L * H * d) + 4 * 70
+    assert by - 4 * 70 == 2 * (acc.attn_bytes(70, H, Lq, d, L) - 4 * 70)
