@@ -100,9 +100,11 @@ class Oracle:
                                                  p, p, p, p, p, i]
         lib.ikbo_oracle_attn_backward.argtypes = [p, p, p, p, p, p, i, i, i, i, i, i, ctypes.c_double, p, i, p, i,
                                                   p, p, p, i]
+        lib.ikbo_oracle_attn_lse.argtypes = [p, p, p, p, i, i, i, i, i, i, ctypes.c_double, p, i, p, i]
         lib.ikbo_oracle_max_threads.argtypes = []
         for f in (lib.ikbo_oracle_segments, lib.ikbo_oracle_lce, lib.ikbo_oracle_attn,
-                  lib.ikbo_oracle_lce_backward, lib.ikbo_oracle_attn_backward, lib.ikbo_oracle_max_threads):
+                  lib.ikbo_oracle_lce_backward, lib.ikbo_oracle_attn_backward, lib.ikbo_oracle_attn_lse,
+                  lib.ikbo_oracle_max_threads):
             f.restype = ctypes.c_int
         self.lib = lib
         self.path = lib_path
@@ -257,6 +259,35 @@ class Oracle:
         self._check(rc, "attn")
         return O
 
+    def attn_lse(self, map_, Q, K, kv_offsets=None, n_users: Optional[int] = None,
+                 scale: Optional[float] = None, pairs: Optional[Sequence] = None,
+                 n_threads: int = 0) -> np.ndarray:
+        """Natural-log log-sum-exp of each query row's scores against its user's
+        keys, float64 [n_sel, Lq] for the (i, h) pairs (all when None); -inf
+        for an empty key range."""
+        m = _i32(map_)
+        n_cand, H, Lq, d = Q.shape
+        if kv_offsets is None:
+            n_users_k, H2, Lkv, d2 = K.shape
+            if n_users is None:
+                n_users = n_users_k
+            offs = None
+        else:
+            offs = _i32(kv_offsets)
+            Lkv, H2, d2 = K.shape
+            if n_users is None:
+                n_users = offs.shape[0] - 1
+        assert H2 == H and d2 == d
+        if scale is None:
+            scale = 1.0 / math.sqrt(d)
+        sel = None if pairs is None else _i32(pairs).reshape(-1, 2)
+        n_sel = n_cand * H if sel is None else sel.shape[0]
+        out = np.zeros((n_sel, Lq), np.float64)
+        rc = self.lib.ikbo_oracle_attn_lse(_ptr(m), _ptr(_bits(Q)), _ptr(_bits(K)), _ptr(offs), n_cand, n_users,
+                                           H, Lq, Lkv, d, float(scale), _ptr(sel), n_sel, _ptr(out), n_threads)
+        self._check(rc, "attn_lse")
+        return out
+
 
 _default: Optional[Oracle] = None
 _lock = threading.Lock()
@@ -288,6 +319,10 @@ def lce_backward(*a, **k):
 
 def attn_backward(*a, **k):
     return default().attn_backward(*a, **k)
+
+
+def attn_lse(*a, **k):
+    return default().attn_lse(*a, **k)
 
 
 def max_threads() -> int:

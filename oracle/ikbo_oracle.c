@@ -305,6 +305,65 @@ int ikbo_oracle_attn(const int32_t *map, const uint16_t *Q, const uint16_t *K, c
 }
 
 /*
+ * Log-sum-exp of each query row's scores, the normaliser of the softmax in
+ * ikbo_oracle_attn (aixai.ru, "Deep Dive: Flash Attention": IKBO attention is
+ * ordinary attention whose K/V come from the candidate's user):
+ *   LSE[i,h,q] = log( sum_{j in keys of map[i]} exp(scale * Q[i,h,q] . K[map[i],h,j]) )
+ * in natural log, formed as m + log(sum exp(s_j - m)) with m the row maximum.
+ * An empty key range gives -inf (the sum is empty).  Output double
+ * [n_sel][Lq] for the (i, h) pairs (all, in (i, h) order, when pairs is NULL
+ * and n_sel == n_cand * H).  This is the statistic a training forward keeps
+ * so that its backward can recover every softmax probability as
+ * exp(s_j - LSE) without a second pass over the keys.
+ */
+int ikbo_oracle_attn_lse(const int32_t *map, const uint16_t *Q, const uint16_t *K, const int32_t *kv_offsets,
+                         int n_cand, int n_users, int H, int Lq, int Lkv, int d, double scale,
+                         const int32_t *pairs, int n_sel, double *lse, int n_threads)
+{
+    if (n_cand < 0 || n_users < 1 || H < 1 || Lq < 1 || d < 1 || n_sel < 0) return ORACLE_BAD_ARG;
+    if (!kv_offsets && Lkv < 0) return ORACLE_BAD_ARG;
+    if (!pairs && n_sel != n_cand * H) return ORACLE_BAD_ARG;
+    for (int s = 0; s < n_sel; ++s) {
+        int i = pairs ? pairs[2 * s] : s / H;
+        int h = pairs ? pairs[2 * s + 1] : s % H;
+        if (i < 0 || i >= n_cand || h < 0 || h >= H) return ORACLE_BAD_ARG;
+        if (map[i] < 0 || map[i] >= n_users) return ORACLE_MAP_OUT_OF_RANGE;
+    }
+    if (kv_offsets)
+        for (int u = 0; u < n_users; ++u)
+            if (kv_offsets[u + 1] < kv_offsets[u]) return ORACLE_BAD_ARG;
+    set_threads(n_threads);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int s = 0; s < n_sel; ++s) {
+        int i = pairs ? pairs[2 * s] : s / H;
+        int h = pairs ? pairs[2 * s + 1] : s % H;
+        int u = map[i];
+        int L = kv_offsets ? kv_offsets[u + 1] - kv_offsets[u] : Lkv;
+        for (int q = 0; q < Lq; ++q) {
+            const uint16_t *qrow = Q + (((size_t)i * H + h) * Lq + q) * d;
+            double m = -INFINITY, sum = 0.0;
+            /* two sweeps over the keys: the maximum, then the shifted sum */
+            for (int pass = 0; pass < 2; ++pass) {
+                for (int j = 0; j < L; ++j) {
+                    const uint16_t *krow = kv_offsets ? K + ((size_t)(kv_offsets[u] + j) * H + h) * d
+                                                      : K + (((size_t)u * H + h) * (size_t)Lkv + j) * d;
+                    double dot = 0.0;
+                    for (int c = 0; c < d; ++c) dot += bf16_bits_to_double(qrow[c]) * bf16_bits_to_double(krow[c]);
+                    double sj = scale * dot;
+                    if (pass == 0) {
+                        if (sj > m) m = sj;
+                    } else {
+                        sum += exp(sj - m);
+                    }
+                }
+            }
+            lse[(size_t)s * Lq + q] = L > 0 ? m + log(sum) : -INFINITY;
+        }
+    }
+    return ORACLE_OK;
+}
+
+/*
  * LCE backward (training), from the materialised definition.  The pages say
  * the IKBO kernels serve training as they are when the candidate:user ratio
  * exceeds 1 ("Meta Optimizes Inference for Recommendation Systems",

@@ -327,6 +327,50 @@ ATTN_PINS = [pin_attn_identity_map_is_sdpa, pin_attn_single_user_is_mqa,
              pin_attn_broadcast_is_sdpa_on_gathered_kv, pin_attn_closed_forms,
              pin_attn_permutation, pin_attn_jagged, pin_attn_scale]
 
+# ------------------------------------------------------- softmax log-sum-exp
+def pin_attn_lse_is_logsumexp(orc):
+    """General map and an explicit scale: torch's fp64 logsumexp of the scores
+    against the gathered K[map] (a library routine on a separately formed
+    score matrix)."""
+    x = gen.make_attn("pin", 41, n_cand=9, n_users=3, H=2, Lq=3, d=16, Lkv=14, map_kind="permuted")
+    for scale in (None, 0.3):
+        got = orc.attn_lse(x.map, x.Q, x.K, scale=scale).reshape(9, 2, 3)
+        sc = 0.25 if scale is None else scale
+        s = torch.einsum("ihqc,ihjc->ihqj", x.Q.to(torch.float64), x.K[x.map.long()].to(torch.float64)) * sc
+        np.testing.assert_allclose(got, torch.logsumexp(s, -1).numpy(), rtol=1e-12, atol=1e-12)
+
+
+def pin_attn_lse_closed_forms(orc):
+    """Q = 0: every score is 0, LSE = log L; one key: LSE is its score; an
+    empty jagged slice: -inf; and the forward's output is the softmax that
+    this normaliser defines: O = sum_j exp(s_j - LSE) V_j."""
+    x = gen.make_attn("pin", 43, n_cand=4, n_users=2, H=1, Lq=2, d=16, Lkv=7, explicit_map=[1, 0, 1, 0])
+    got = orc.attn_lse(x.map, torch.zeros_like(x.Q), x.K)
+    np.testing.assert_allclose(got, np.log(7.0), rtol=0, atol=1e-15)
+    x1 = gen.make_attn("pin", 45, n_cand=3, n_users=2, H=2, Lq=2, d=16, Lkv=1, explicit_map=[1, 1, 0])
+    got = orc.attn_lse(x1.map, x1.Q, x1.K).reshape(3, 2, 2)
+    for i, u in enumerate(x1.map.tolist()):
+        for h in range(2):
+            np.testing.assert_allclose(got[i, h], f64(x1.Q[i, h]) @ f64(x1.K[u, h, 0]) * 0.25, rtol=1e-14, atol=1e-14)
+    lens = [5, 0, 9]
+    xj = gen.make_attn("pin", 47, n_cand=5, n_users=3, H=2, Lq=2, d=16,
+                       explicit_map=[2, 1, 0, 1, 2], explicit_lengths=lens)
+    got = orc.attn_lse(xj.map, xj.Q, xj.K, kv_offsets=xj.kv_offsets).reshape(5, 2, 2)
+    assert np.all(np.isneginf(got[1])) and np.all(np.isneginf(got[3]))
+    assert np.all(np.isfinite(got[[0, 2, 4]]))
+    x2 = gen.make_attn("pin", 49, n_cand=5, n_users=2, H=2, Lq=3, d=16, Lkv=10, map_kind="permuted")
+    lse = orc.attn_lse(x2.map, x2.Q, x2.K).reshape(5, 2, 3)
+    O = orc.attn(x2.map, x2.Q, x2.K, x2.V).reshape(5, 2, 3, 16)
+    for i, u in enumerate(x2.map.tolist()):
+        for h in range(2):
+            s = f64(x2.Q[i, h]) @ f64(x2.K[u, h]).T * 0.25
+            w = np.exp(s - lse[i, h][:, None])
+            np.testing.assert_allclose(w.sum(1), 1.0, rtol=1e-13)
+            np.testing.assert_allclose(O[i, h], w @ f64(x2.V[u, h]), rtol=1e-11, atol=1e-12)
+
+
+ATTN_LSE_PINS = [pin_attn_lse_is_logsumexp, pin_attn_lse_closed_forms]
+
 
 # ================================================================ segments
 def _check_segments_against_brute_force(orc, m: np.ndarray, n_users: int, H: int, cpu: int):

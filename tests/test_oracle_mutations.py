@@ -6,7 +6,7 @@ import os
 import pytest
 
 import oracle
-from oracle_pins import ATTN_BWD_PINS, ATTN_PINS, LCE_BWD_PINS, LCE_PINS, SEG_PINS
+from oracle_pins import ATTN_BWD_PINS, ATTN_LSE_PINS, ATTN_PINS, LCE_BWD_PINS, LCE_PINS, SEG_PINS
 
 MUTATIONS = {
     # LCE
@@ -53,6 +53,12 @@ MUTATIONS = {
     "seg_unstable": ("for (int i = 0; i < n_cand; ++i) {       /* ascending i: stable */", "for (int i = n_cand - 1; i >= 0; --i) {", SEG_PINS),
     # every planted mistake keeps its writes inside the caller's buffers
     "seg_perm_stores_user": ("perm[next[u]] = i;", "perm[next[u]] = u;", SEG_PINS),
+    "lse_drop_max": ("lse[(size_t)s * Lq + q] = L > 0 ? m + log(sum) : -INFINITY;",
+                     "lse[(size_t)s * Lq + q] = L > 0 ? log(sum) : -INFINITY;", ATTN_LSE_PINS),
+    "lse_no_scale": ("double sj = scale * dot;", "double sj = dot;", ATTN_LSE_PINS),
+    "lse_drop_last_key": ("for (int j = 0; j < L; ++j) {\n                    const uint16_t *krow = kv_offsets ? K",
+                          "for (int j = 0; j < L - (pass == 1); ++j) {\n                    const uint16_t *krow = kv_offsets ? K",
+                          ATTN_LSE_PINS),
     "seg_chunk_off_by_one": ("if (cnt > cands_per_unit) cnt = cands_per_unit;", "if (cnt >= cands_per_unit) cnt = cands_per_unit - 1 + (cands_per_unit == 1);", SEG_PINS),
 }
 

@@ -4,7 +4,7 @@ import pytest
 import torch
 
 import oracle
-from oracle_pins import ATTN_BWD_PINS, ATTN_PINS, LCE_BWD_PINS, LCE_PINS, SEG_PINS
+from oracle_pins import ATTN_BWD_PINS, ATTN_LSE_PINS, ATTN_PINS, LCE_BWD_PINS, LCE_PINS, SEG_PINS
 from broadcast_gemm_attention_gb300 import inputs as gen
 
 
@@ -25,6 +25,11 @@ def test_attn_backward_pin(orc, pin):
 
 @pytest.mark.parametrize("pin", ATTN_PINS, ids=lambda f: f.__name__)
 def test_attn_pin(orc, pin):
+    pin(orc)
+
+
+@pytest.mark.parametrize("pin", ATTN_LSE_PINS, ids=lambda f: f.__name__)
+def test_attn_lse_pin(orc, pin):
     pin(orc)
 
 
