@@ -595,20 +595,27 @@ def attn_backward_run(plan, d, x, a, O, flush, stream, dev, pk, iters=20):
     dQ = torch.empty_like(d["Q"])
     dK = torch.empty_like(d["K"])
     dV = torch.empty_like(d["V"])
+    lse = torch.empty(tuple(a.Q.shape[:3]), dtype=torch.float32, device=dev)
     plan.plan(d["map"], x.n_users, a.H, a.Lq, stream)
-    plan.attn_forward(d["Q"], d["K"], d["V"], None, O, None, stream)
-    ts = []
-    l0 = plan.launches()
-    for k in range(iters + 3):
-        flush()
-        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        s.record(stream)
-        plan.attn_backward(d["Q"], d["K"], d["V"], O, dO, None, dQ, dK, dV, None, stream)
-        e.record(stream)
-        torch.cuda.synchronize()
-        if k >= 3:
-            ts.append(s.elapsed_time(e))
-    launches = (plan.launches() - l0) / (iters + 3)
+    plan.attn_forward_lse(d["Q"], d["K"], d["V"], None, O, lse, None, stream)
+
+    def timed(with_lse):
+        ts = []
+        l0 = plan.launches()
+        for k in range(iters + 3):
+            flush()
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record(stream)
+            plan.attn_backward(d["Q"], d["K"], d["V"], O, dO, None, dQ, dK, dV, None, stream,
+                               lse=lse if with_lse else None)
+            e.record(stream)
+            torch.cuda.synchronize()
+            if k >= 3:
+                ts.append(s.elapsed_time(e))
+        return ts, (plan.launches() - l0) / (iters + 3)
+
+    ts_re, _ = timed(False)
+    ts, launches = timed(True)
     st = plan.status()
     us = 1e3 * statistics.median(ts)
     lens = [a.Lkv] * a.n_cand
@@ -616,14 +623,16 @@ def attn_backward_run(plan, d, x, a, O, flush, stream, dev, pk, iters=20):
     byt = acc.attn_backward_bytes(a.n_cand, a.H, a.Lq, a.d, a.n_users * a.Lkv)
     tf = fl / (us * 1e-6) / 1e12
     return {"us_median": us, "us_mean": 1e3 * statistics.mean(ts), "launches_per_call": launches,
+            "us_median_recomputed_lse": 1e3 * statistics.median(ts_re),
             "tflops": tf, "gbs": byt / (us * 1e-6) / 1e9,
             "roofline": {"bound": "tensor", "achieved": tf, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
                          "frac": tf / pk["bf16_tflops"],
                          "algorithmic": f"{fl:.4g} FLOP per call = 10*H*Lq*d*sum_i Lkv (S, dP, dV, dK, dQ)"},
             "status": "ok" if st == 0 else f"error {st}",
-            "note": "dQ kernel per forward work unit (LSE pass, then dS and dQ += dS K); dK/dV kernel per "
-                    "(user, head, 128-key block) over all of the user's candidates; one stream, L2 flushed "
-                    "before each call"}
+            "note": "given the forward's log-sum-exp (ikbo_attn_forward_lse): dQ kernel per forward work unit "
+                    "(dS and dQ += dS K), dK/dV kernel per (user, head, 128-key block) over all of the user's "
+                    "candidates; us_median_recomputed_lse: without it (one more pass over the keys); one "
+                    "stream, L2 flushed before each call"}
 
 
 def self_target_run(plan, d, x, a, O, flush, stream, dev, Lq_u=64, iters=20):

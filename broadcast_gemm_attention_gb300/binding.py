@@ -44,7 +44,9 @@ SIGNATURES = {
     "ikbo_lce_forward_noalloc": (_i, [_vp, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp]),
     "ikbo_lce_backward": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp]),
     "ikbo_attn_forward": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, ctypes.c_float, _vp]),
-    "ikbo_attn_backward": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, ctypes.c_float, _vp]),
+    "ikbo_attn_forward_lse": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, ctypes.c_float, _vp]),
+    "ikbo_attn_backward": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, ctypes.c_float,
+                                _vp]),
     "ikbo_attn_self_target_forward": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, ctypes.c_float, _vp]),
     "ikbo_plan_get_status": (_i, [_vp, _vp]),
     "ikbo_plan_set_debug": (_i, [_vp, ctypes.c_uint]),
@@ -250,11 +252,35 @@ def ikbo_attn_forward(plan: int, Q: torch.Tensor, K: torch.Tensor, V: torch.Tens
                                     _dev(O, bf, "O"), Lkv, d, float(scale), _stream(stream)), "ikbo_attn_forward")
 
 
+def ikbo_attn_forward_lse(plan: int, Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor,
+                          kv_offsets: Optional[torch.Tensor], O: torch.Tensor, lse: torch.Tensor,
+                          scale: Optional[float] = None, stream=None) -> None:
+    """ikbo_attn_forward that also writes each query row's natural-log
+    log-sum-exp into lse (fp32 [n_cand, H, Lq])."""
+    bf = torch.bfloat16
+    d = Q.shape[-1]
+    if kv_offsets is None:
+        Lkv = K.shape[2]
+        optr = None
+    else:
+        Lkv = K.shape[0]
+        optr = _dev(kv_offsets, torch.int32, "kv_offsets")
+    if K.shape != V.shape or O.shape != Q.shape or tuple(lse.shape) != tuple(Q.shape[:3]):
+        raise ValueError("inconsistent attention shapes")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    _check(load().ikbo_attn_forward_lse(plan, _dev(Q, bf, "Q"), _dev(K, bf, "K"), _dev(V, bf, "V"), optr,
+                                        _dev(O, bf, "O"), _dev(lse, torch.float32, "lse"), Lkv, d, float(scale),
+                                        _stream(stream)), "ikbo_attn_forward_lse")
+
+
 def ikbo_attn_backward(plan: int, Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, O: torch.Tensor,
                        dO: torch.Tensor, kv_offsets: Optional[torch.Tensor], dQ: torch.Tensor, dK: torch.Tensor,
-                       dV: torch.Tensor, scale: Optional[float] = None, stream=None) -> None:
+                       dV: torch.Tensor, scale: Optional[float] = None, stream=None,
+                       lse: Optional[torch.Tensor] = None) -> None:
     """Gradients of broadcast attention for upstream dO: dQ (Q's layout), and dK,
-    dV (K's layout) summed over each user's candidates; all bf16, overwritten."""
+    dV (K's layout) summed over each user's candidates; all bf16, overwritten.
+    lse: the forward's log-sum-exp (ikbo_attn_forward_lse), or None."""
     bf = torch.bfloat16
     d = Q.shape[-1]
     if kv_offsets is None:
@@ -268,8 +294,13 @@ def ikbo_attn_backward(plan: int, Q: torch.Tensor, K: torch.Tensor, V: torch.Ten
         raise ValueError("inconsistent attention shapes")
     if scale is None:
         scale = 1.0 / math.sqrt(d)
+    lptr = None
+    if lse is not None:
+        if tuple(lse.shape) != tuple(Q.shape[:3]):
+            raise ValueError("inconsistent lse shape")
+        lptr = _dev(lse, torch.float32, "lse")
     _check(load().ikbo_attn_backward(plan, _dev(Q, bf, "Q"), _dev(K, bf, "K"), _dev(V, bf, "V"), _dev(O, bf, "O"),
-                                     _dev(dO, bf, "dO"), optr, _dev(dQ, bf, "dQ"), _dev(dK, bf, "dK"),
+                                     _dev(dO, bf, "dO"), lptr, optr, _dev(dQ, bf, "dQ"), _dev(dK, bf, "dK"),
                                      _dev(dV, bf, "dV"), Lkv, d, float(scale), _stream(stream)),
            "ikbo_attn_backward")
 
@@ -358,8 +389,11 @@ class Plan:
     def attn_forward(self, Q, K, V, kv_offsets, O, scale=None, stream=None):
         ikbo_attn_forward(self.handle, Q, K, V, kv_offsets, O, scale, stream)
 
-    def attn_backward(self, Q, K, V, O, dO, kv_offsets, dQ, dK, dV, scale=None, stream=None):
-        ikbo_attn_backward(self.handle, Q, K, V, O, dO, kv_offsets, dQ, dK, dV, scale, stream)
+    def attn_forward_lse(self, Q, K, V, kv_offsets, O, lse, scale=None, stream=None):
+        ikbo_attn_forward_lse(self.handle, Q, K, V, kv_offsets, O, lse, scale, stream)
+
+    def attn_backward(self, Q, K, V, O, dO, kv_offsets, dQ, dK, dV, scale=None, stream=None, lse=None):
+        ikbo_attn_backward(self.handle, Q, K, V, O, dO, kv_offsets, dQ, dK, dV, scale, stream, lse)
 
     def attn_self_target_forward(self, Q, Q_user, K, V, kv_offsets, O, O_user, scale=None, stream=None):
         ikbo_attn_self_target_forward(self.handle, Q, Q_user, K, V, kv_offsets, O, O_user, scale, stream)

@@ -229,8 +229,8 @@ namespace {
 // Both attention entry points: the work list's (target) units, plus, when
 // Q_user is given, n_users * H * ceil(Lq_u / 128) self units in the same launch.
 ikbo_status_t attn_launch(ikbo_plan_t p, const void* Q, const void* Q_user, const void* K, const void* V,
-                          const int32_t* d_kv_offsets, void* O, void* O_user, int Lq_u, int Lkv, int d, float scale,
-                          cudaStream_t stream) {
+                          const int32_t* d_kv_offsets, void* O, void* O_user, float* lse, int Lq_u, int Lkv, int d,
+                          float scale, cudaStream_t stream) {
   if (!p) return IKBO_ERR_INVALID_ARG;
   if (!p->planned) return IKBO_ERR_NOT_PLANNED;
   if (!Q || !K || !V || !O) return IKBO_ERR_INVALID_ARG;
@@ -251,6 +251,7 @@ ikbo_status_t attn_launch(ikbo_plan_t p, const void* Q, const void* Q_user, cons
   ap.n_units = p->d_n_units;
   ap.kv_offsets = d_kv_offsets;
   ap.O = static_cast<uint16_t*>(O);
+  ap.lse = lse;
   ap.status = p->d_status;
   ap.n_cand = p->n_cand;
   ap.n_users = p->n_users;
@@ -301,13 +302,14 @@ ikbo_status_t attn_launch(ikbo_plan_t p, const void* Q, const void* Q_user, cons
 
 namespace {
 ikbo_status_t attn_backward_launch(ikbo_plan_t p, const void* Q, const void* K, const void* V, const void* O,
-                                   const void* dO, const int32_t* d_kv_offsets, void* dQ, void* dK, void* dV, int Lkv,
-                                   int d, float scale, cudaStream_t stream) {
+                                   const void* dO, const float* lse, const int32_t* d_kv_offsets, void* dQ, void* dK,
+                                   void* dV, int Lkv, int d, float scale, cudaStream_t stream) {
   if (!p) return IKBO_ERR_INVALID_ARG;
   if (!p->planned) return IKBO_ERR_NOT_PLANNED;
   const void* ptrs[] = {Q, K, V, O, dO, dQ, dK, dV};
   for (const void* q : ptrs)
     if (!q || !aligned16(q)) return IKBO_ERR_INVALID_ARG;
+  if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return IKBO_ERR_INVALID_ARG;
   if (d != ATT_D) return IKBO_ERR_UNSUPPORTED;
   if (Lkv < 1 || !(scale > 0.f) || !std::isfinite(scale)) return IKBO_ERR_INVALID_ARG;
   if (attn_bwd_smem_bytes() > p->max_smem) return IKBO_ERR_UNSUPPORTED;
@@ -332,6 +334,7 @@ ikbo_status_t attn_backward_launch(ikbo_plan_t p, const void* Q, const void* K, 
   bp.dV = static_cast<uint16_t*>(dV);
   bp.lse = p->d_abwd_lse;
   bp.Drow = p->d_abwd_drow;
+  bp.lse_in = lse;
   bp.status = p->d_status;
   bp.n_cand = p->n_cand;
   bp.n_users = p->n_users;
@@ -372,12 +375,12 @@ ikbo_status_t attn_backward_launch(ikbo_plan_t p, const void* Q, const void* K, 
 
 extern "C" {
 
-int ikbo_version(void) { return 105; }
+int ikbo_version(void) { return 106; }
 
 ikbo_status_t ikbo_attn_backward(ikbo_plan_t p, const void* Q, const void* K, const void* V, const void* O,
-                                 const void* dO, const int32_t* d_kv_offsets, void* dQ, void* dK, void* dV, int Lkv,
-                                 int d, float scale, cudaStream_t stream) {
-  return attn_backward_launch(p, Q, K, V, O, dO, d_kv_offsets, dQ, dK, dV, Lkv, d, scale, stream);
+                                 const void* dO, const float* lse, const int32_t* d_kv_offsets, void* dQ, void* dK,
+                                 void* dV, int Lkv, int d, float scale, cudaStream_t stream) {
+  return attn_backward_launch(p, Q, K, V, O, dO, lse, d_kv_offsets, dQ, dK, dV, Lkv, d, scale, stream);
 }
 
 const char* ikbo_status_string(ikbo_status_t s) {
@@ -684,14 +687,21 @@ ikbo_status_t ikbo_lce_backward(ikbo_plan_t p, const void* U, const void* C, con
 ikbo_status_t ikbo_attn_forward(ikbo_plan_t p, const void* Q, const void* K, const void* V,
                                 const int32_t* d_kv_offsets, void* O, int Lkv, int d, float scale,
                                 cudaStream_t stream) {
-  return attn_launch(p, Q, nullptr, K, V, d_kv_offsets, O, nullptr, 0, Lkv, d, scale, stream);
+  return attn_launch(p, Q, nullptr, K, V, d_kv_offsets, O, nullptr, nullptr, 0, Lkv, d, scale, stream);
+}
+
+ikbo_status_t ikbo_attn_forward_lse(ikbo_plan_t p, const void* Q, const void* K, const void* V,
+                                    const int32_t* d_kv_offsets, void* O, float* lse, int Lkv, int d, float scale,
+                                    cudaStream_t stream) {
+  if (!lse || (reinterpret_cast<uintptr_t>(lse) & 3u)) return IKBO_ERR_INVALID_ARG;
+  return attn_launch(p, Q, nullptr, K, V, d_kv_offsets, O, nullptr, lse, 0, Lkv, d, scale, stream);
 }
 
 ikbo_status_t ikbo_attn_self_target_forward(ikbo_plan_t p, const void* Q, const void* Q_user, const void* K,
                                             const void* V, const int32_t* d_kv_offsets, void* O, void* O_user,
                                             int Lq_u, int Lkv, int d, float scale, cudaStream_t stream) {
   if (!Q_user) return IKBO_ERR_INVALID_ARG;
-  return attn_launch(p, Q, Q_user, K, V, d_kv_offsets, O, O_user, Lq_u, Lkv, d, scale, stream);
+  return attn_launch(p, Q, Q_user, K, V, d_kv_offsets, O, O_user, nullptr, Lq_u, Lkv, d, scale, stream);
 }
 
 }  // extern "C"

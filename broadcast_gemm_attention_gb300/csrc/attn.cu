@@ -498,16 +498,26 @@ struct RowOut {
   bool valid;    // this thread's row belongs to a candidate of that unit
   __nv_bfloat16* row;
   float l;       // this warp's half of the row sum
+  float m;       // the row's reference maximum (log2 domain) that l is relative to
 };
+
+// The row's natural-log log-sum-exp, m + log2(l) in the log2 domain, into
+// the caller's lse array (the row's index is its O row's).
+__device__ __forceinline__ void store_lse(const AttnParams& p, const __nv_bfloat16* orow, float lse2) {
+  const size_t idx = static_cast<size_t>(reinterpret_cast<const uint16_t*>(orow) - p.O) / ATT_D;
+  p.lse[idx] = lse2 * 0.69314718055994531f;
+}
 
 // O / l -> bf16 -> this warp's d half of its 32 rows, through its 4 KB of
 // staging (128-byte rows, 16-byte chunk c of row r at chunk c ^ (r % 8)) to
 // global memory 4 rows per store instruction; then O may be overwritten.
+template <bool kLse>
 __device__ __forceinline__ bool att_epilogue(const AttnParams& p, const AttSmem& s, uint32_t Ot, const RowOut& ro,
                                              Lane& ln, uint32_t& ou) {
   float lp;
   if (!pair_exchange(p, s, ln, ro.l, lp)) return false;
   const float l = ro.l + lp;
+  if (kLse && ro.valid && ln.half == 0) store_lse(p, ro.row, l > 0.f ? ro.m + __log2f(l) : -INFINITY);
   if (!mbar_wait(s.o_full, ou & 1u, s.abort, p.timeout_ns, 1)) return false;
   ++ou;
   tc_fence_after();
@@ -547,7 +557,8 @@ __device__ __forceinline__ bool att_epilogue(const AttnParams& p, const AttSmem&
   return true;
 }
 
-template <bool kSelf>
+// kLse: also write each row's log-sum-exp (target units only).
+template <bool kSelf, bool kLse>
 __device__ void att_softmax(const AttnParams& p, const AttSmem& s, uint32_t tmem, const UnitCount& n_units) {
   const int warp = threadIdx.x >> 5;
   Lane ln;
@@ -566,7 +577,7 @@ __device__ void att_softmax(const AttnParams& p, const AttSmem& s, uint32_t tmem
   const int qrow = ln.r % p.Lq;
   const bool row_in_tile = ln.r < p.cands_per_tile * p.Lq;
   uint32_t g = 0, qc = 0, ou = 0;
-  RowOut prev = {false, false, nullptr, 0.f};
+  RowOut prev = {false, false, nullptr, 0.f, 0.f};
 
   int unit = blockIdx.x;
   Unit x = decode<kSelf>(p, load_work<kSelf>(p, unit, n_units));
@@ -585,11 +596,12 @@ __device__ void att_softmax(const AttnParams& p, const AttSmem& s, uint32_t tmem
                           ((static_cast<size_t>(x.u) * p.H + x.h) * p.Lq_u + x.start + ln.r) * ATT_D
                     : reinterpret_cast<__nv_bfloat16*>(p.O) + ((static_cast<size_t>(cand) * p.H + x.h) * p.Lq + qrow) * ATT_D;
 
-    if (x.ntiles == 0) {  // empty key range: O = 0
+    if (x.ntiles == 0) {  // empty key range: O = 0 (and LSE = -inf)
       if (rv) {
         const uint4 z = make_uint4(0, 0, 0, 0);
 #pragma unroll
         for (int c = 0; c < 8; ++c) reinterpret_cast<uint4*>(orow + half * 64)[c] = z;
+        if (kLse && half == 0) store_lse(p, orow, -INFINITY);
       }
     } else {
       // this warp's d half of the Q row: landing buffer (128-byte swizzle:
@@ -616,7 +628,7 @@ __device__ void att_softmax(const AttnParams& p, const AttSmem& s, uint32_t tmem
       mbar_arrive(s.q_empty);
       // the previous unit's O is written out while this unit's first S are computed
       if (prev.pending) {
-        if (!att_epilogue(p, s, Ot, prev, ln, ou)) return;
+        if (!att_epilogue<kLse>(p, s, Ot, prev, ln, ou)) return;
         prev.pending = false;
       }
 
@@ -703,6 +715,7 @@ __device__ void att_softmax(const AttnParams& p, const AttSmem& s, uint32_t tmem
       prev.valid = rv;
       prev.row = orow;
       prev.l = l;
+      prev.m = m;
     }
     if (!prefetched) {
       nx = decode<kSelf>(p, nw);
@@ -714,12 +727,13 @@ __device__ void att_softmax(const AttnParams& p, const AttSmem& s, uint32_t tmem
     cand = ncand;
     unit = nunit;
   }
-  if (prev.pending) att_epilogue(p, s, Ot, prev, ln, ou);
+  if (prev.pending) att_epilogue<kLse>(p, s, Ot, prev, ln, ou);
 }
 
 // kSelf: the launch also runs self units (ikbo_attn_self_target_forward);
-// without them the self branches compile away.
-template <bool kSelf>
+// without them the self branches compile away.  kLse: the softmax warps also
+// write each row's log-sum-exp (ikbo_attn_forward_lse; never with kSelf).
+template <bool kSelf, bool kLse>
 __global__ void __launch_bounds__(ATT_THREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmQu,
                     const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -786,7 +800,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
   } else if (warp == 2) {
     att_pv_issuer<kSelf>(p, s, tmem, n_units);
   } else if (warp >= SOFTMAX_WARP0) {
-    att_softmax<kSelf>(p, s, tmem, n_units);
+    att_softmax<kSelf, kLse>(p, s, tmem, n_units);
   }
 
   tc_fence_before();
@@ -805,7 +819,9 @@ size_t attn_smem_bytes() { return SMEM_ALLOC; }
 cudaError_t launch_attn(const CUtensorMap& tmQ, const CUtensorMap& tmQu, const CUtensorMap& tmK,
                         const CUtensorMap& tmV, const AttnParams& p, int grid, cudaStream_t s) {
   const size_t smem = attn_smem_bytes();
-  auto kernel = p.n_self > 0 ? attn_fwd_kernel<true> : attn_fwd_kernel<false>;
+  if (p.n_self > 0 && p.lse) return cudaErrorInvalidValue;
+  auto kernel = p.n_self > 0 ? attn_fwd_kernel<true, false>
+                             : (p.lse ? attn_fwd_kernel<false, true> : attn_fwd_kernel<false, false>);
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   kernel<<<grid, ATT_THREADS, smem, s>>>(tmQ, tmQu, tmK, tmV, p);

@@ -9,17 +9,27 @@
 // K/V gradients of user u sum over every candidate of u:
 //   dK[u,h] = scale sum_{i in seg u} dS_i^T Q_i,   dV[u,h] = sum_i P_i^T dO_i.
 //
-// Two persistent kernels, one CTA per SM, 8 warps: warp 0 TMA (elected lane
-// issues), warp 1 tcgen05.mma (elected lane) and TMEM owner, warps 4-7 the
-// element-wise work (thread = TMEM lane = one row, 128 columns each).
+// Two persistent kernels, one CTA per SM, 12 warps: warp 0 TMA (elected lane
+// issues), warp 1 tcgen05.mma (elected lane) and TMEM owner, warp 2 a second
+// MMA issuer in the dK/dV kernel, warps 4-11 the element-wise work: warps w and w+4 share the 32 TMEM lanes of quarter w % 4
+// and split the 128 columns of every tile in halves.
 //   attn_bwd_dq_kernel    per work-list unit (a 128-row tile of up to
 //                         floor(128/Lq) candidates' queries, as the forward):
-//                         pass 1 forms LSE over the user's key tiles, pass 2
+//                         pass 1 forms LSE over the user's key tiles (S
+//                         double-buffered in TMEM), pass 2 recomputes S, forms
+//                         dP and dS (written over S in TMEM) and accumulates
 //                         dQ += dS K.  Stores LSE and D for the next kernel.
-//   attn_bwd_dkdv_kernel  per (user, head, 128-key block): loops over the
-//                         query tiles of all of the user's candidates.
-// P and dS are rounded to bf16 for the tensor cores (as P is in the
-// forward); every accumulation is fp32.  Every wait is bounded.
+//   attn_bwd_dkdv_kernel  per (user, head, 128-key block), keys on TMEM lanes:
+//                         for every query tile of the user's candidates
+//                         S^T = K Q^T, dP^T = V dO^T, then P^T and dS^T are
+//                         written over them in TMEM and dV += P^T dO,
+//                         dK += dS^T Q accumulate in TMEM -- the sum over a
+//                         user's candidates never leaves the chip.
+// Products that read a bf16 operand written over an fp32 one in TMEM are
+// waited for (commit) before anything writes those columns again; the issue
+// order puts that wait behind an independent product, so the tensor pipe
+// stays fed.  P and dS are rounded to bf16 for the tensor cores (as P is in
+// the forward); every accumulation is fp32.  Every wait is bounded.
 #include <cuda_bf16.h>
 #include <math.h>
 
@@ -32,6 +42,8 @@ namespace {
 
 constexpr uint32_t TILE = 128 * 128 * 2;  // a 128-row x 128-d bf16 tile: two 64-d halves
 constexpr uint32_t HALF = 128 * 64 * 2;   // 16 KB
+constexpr int EW_WARP0 = 4;
+constexpr int EW_THREADS = ABWD_THREADS - 32 * EW_WARP0;  // 256
 
 // A wait taken by a whole warp; the lanes agree on the outcome.
 __device__ __forceinline__ bool wwait(uint64_t* bar, uint32_t parity, uint32_t* abort, uint64_t timeout_ns) {
@@ -91,14 +103,23 @@ __device__ __forceinline__ void mma_rows_dot(uint32_t d_tmem, uint32_t a_base, u
   }
 }
 
-// D += A B with A from TMEM (bf16 pairs, 128 rows x 128 k = 64 columns) and B
-// a [k rows][128 d] tile read MN-major (d contiguous), 8 steps of 16 k.
-__device__ __forceinline__ void mma_tmem_by_tile(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_base, bool accumulate) {
+// Where the bf16 pairs of a 128-column fp32 TMEM tile, converted in place,
+// sit: each column half (64 fp32 columns, one element-wise warp's share)
+// keeps its 32 pairs at its own start, so a warp only overwrites columns it
+// has already read.  k step ks (16 of the 128 elements) -> column offset.
+__device__ __forceinline__ uint32_t inplace_col(int ks) { return static_cast<uint32_t>((ks >> 2) * 64 + (ks & 3) * 8); }
+
+// D (+)= A B with A the bf16 pairs written in place over a 128-column TMEM
+// tile (128 rows x 128 k) and B a [k rows][128 d] tile read MN-major (d
+// contiguous), 8 steps of 16 k.
+__device__ __forceinline__ void mma_inplace_by_tile(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_base,
+                                                    bool accumulate) {
   constexpr uint32_t idesc = idesc_bf16_f32(128, 128, false, true);
   const uint64_t bd = sdesc_sw128(b_base, HALF, 1024);
 #pragma unroll
   for (int ks = 0; ks < 8; ++ks)
-    mma_bf16_ts(d_tmem, a_tmem + ks * 8, bd + ((ks * 2048u) >> 4), idesc, (accumulate || ks > 0) ? 1u : 0u);
+    mma_bf16_ts(d_tmem, a_tmem + inplace_col(ks), bd + ((ks * 2048u) >> 4), idesc,
+                (accumulate || ks > 0) ? 1u : 0u);
 }
 
 // Zero rows [r0, 128) of a 32 KB tile (both halves; the swizzle only moves
@@ -111,32 +132,53 @@ __device__ __forceinline__ void zero_rows(uint8_t* tile, int r0, int tid, int nt
   }
 }
 
+// 32 fp32 values -> 64 bytes of bf16 at dst (16-byte aligned).
+__device__ __forceinline__ void store_bf16x32(uint16_t* dst, const uint32_t (&v)[32]) {
+  uint4* o = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+    o[k] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * k]), __uint_as_float(v[8 * k + 1])),
+                      pack_bf16x2(__uint_as_float(v[8 * k + 2]), __uint_as_float(v[8 * k + 3])),
+                      pack_bf16x2(__uint_as_float(v[8 * k + 4]), __uint_as_float(v[8 * k + 5])),
+                      pack_bf16x2(__uint_as_float(v[8 * k + 6]), __uint_as_float(v[8 * k + 7])));
+}
+
 // ================================================================ dQ kernel
-// TMEM columns: S [0,128), dP [128,256), dS (bf16 pairs) [256,320), dQ [320,448).
-constexpr uint32_t TQ_S = 0, TQ_DP = 128, TQ_DS = 256, TQ_DQ = 320;
-constexpr int DQ_K_STAGES = 2, DQ_V_STAGES = 2;
+// TMEM columns: S0 [0,128), S1 [128,256) (dS written over S in pass 2),
+// dP [256,384), dQ [384,512).
+constexpr uint32_t TQ_S = 0, TQ_DP = 256, TQ_DQ = 384;
+constexpr int DQ_K_STAGES = 3, DQ_V_STAGES = 2;
 
 struct DqSmem {
-  uint8_t* q;   // 32 KB
-  uint8_t* go;  // dO tile, 32 KB
-  uint8_t* k;   // DQ_K_STAGES x 32 KB
-  uint8_t* v;   // DQ_V_STAGES x 32 KB
+  uint8_t* q;    // 32 KB
+  uint8_t* go;   // dO tile, 32 KB
+  uint8_t* k;    // DQ_K_STAGES x 32 KB
+  uint8_t* v;    // DQ_V_STAGES x 32 KB
+  float2* xch;   // [2][128] per column half: the row's running (max, sum) after pass 1
   uint64_t* q_full;
   uint64_t* q_empty;
+  uint64_t* do_full;
+  uint64_t* do_empty;
   uint64_t* k_full;
   uint64_t* k_empty;
   uint64_t* v_full;
   uint64_t* v_empty;
-  uint64_t* s_full;   // S (pass 1) or S and dP (pass 2) computed
-  uint64_t* s_free;   // ... and read by the element-wise warps
-  uint64_t* ds_full;  // dS written to TMEM
-  uint64_t* dq_done;  // a dQ += dS K completed (dS may be overwritten)
-  uint64_t* dq_free;  // the unit's dQ was read out
+  uint64_t* s_full;    // [2] S computed into buffer b
+  uint64_t* s_read;    // [2] pass 1: the element-wise warps have read buffer b
+  uint64_t* s_free;    // [2] pass 2: the dQ product reading dS from buffer b completed
+  uint64_t* dp_full;   // dP computed
+  uint64_t* ds_ready;  // dS written (and dP read)
+  uint64_t* dq_full;   // the unit's dQ is complete
+  uint64_t* dq_free;   // ... and has been read out
+  uint64_t* xch_full;  // every element-wise thread posted its (max, sum)
   uint32_t* tmem_slot;
   uint32_t* abort;
 };
 constexpr uint32_t DQ_TILES = (2 + DQ_K_STAGES + DQ_V_STAGES) * TILE;
-constexpr uint32_t DQ_SMEM = 1024 + DQ_TILES + 8 * (2 + 2 * DQ_K_STAGES + 2 * DQ_V_STAGES + 5) + 8;
+constexpr uint32_t DQ_XCH = 2 * 128 * 8;
+constexpr uint32_t DQ_BARS = 4 + 2 * DQ_K_STAGES + 2 * DQ_V_STAGES + 6 + 5;
+constexpr uint32_t DQ_SMEM_USED = DQ_TILES + DQ_XCH + 8 * DQ_BARS + 8;
+constexpr uint32_t DQ_SMEM = DQ_SMEM_USED;  // no alignment slack: the base must be 1024-aligned (checked)
 
 __device__ __forceinline__ DqSmem dq_carve(uint8_t* base) {
   DqSmem s;
@@ -144,19 +186,32 @@ __device__ __forceinline__ DqSmem dq_carve(uint8_t* base) {
   s.go = base + TILE;
   s.k = base + 2 * TILE;
   s.v = s.k + DQ_K_STAGES * TILE;
-  uint64_t* b = reinterpret_cast<uint64_t*>(base + DQ_TILES);
-  s.q_full = b;
-  s.q_empty = b + 1;
-  s.k_full = b + 2;
-  s.k_empty = s.k_full + DQ_K_STAGES;
-  s.v_full = s.k_empty + DQ_K_STAGES;
-  s.v_empty = s.v_full + DQ_V_STAGES;
-  s.s_full = s.v_empty + DQ_V_STAGES;
-  s.s_free = s.s_full + 1;
-  s.ds_full = s.s_free + 1;
-  s.dq_done = s.ds_full + 1;
-  s.dq_free = s.dq_done + 1;
-  s.tmem_slot = reinterpret_cast<uint32_t*>(s.dq_free + 1);
+  s.xch = reinterpret_cast<float2*>(base + DQ_TILES);
+  uint64_t* b = reinterpret_cast<uint64_t*>(base + DQ_TILES + DQ_XCH);
+  s.q_full = b++;
+  s.q_empty = b++;
+  s.do_full = b++;
+  s.do_empty = b++;
+  s.k_full = b;
+  b += DQ_K_STAGES;
+  s.k_empty = b;
+  b += DQ_K_STAGES;
+  s.v_full = b;
+  b += DQ_V_STAGES;
+  s.v_empty = b;
+  b += DQ_V_STAGES;
+  s.s_full = b;
+  b += 2;
+  s.s_read = b;
+  b += 2;
+  s.s_free = b;
+  b += 2;
+  s.dp_full = b++;
+  s.ds_ready = b++;
+  s.dq_full = b++;
+  s.dq_free = b++;
+  s.xch_full = b++;
+  s.tmem_slot = reinterpret_cast<uint32_t*>(b);
   s.abort = s.tmem_slot + 1;
   return s;
 }
@@ -181,13 +236,23 @@ __device__ __forceinline__ QUnit dq_unit(const AttnBwdParams& p, int unit) {
   return x;
 }
 
+// Ring position: slot and the parity of its current use.
+struct Ring {
+  uint32_t n = 0;
+  __device__ __forceinline__ int slot(int stages) const { return static_cast<int>(n % stages); }
+  __device__ __forceinline__ uint32_t parity(int stages) const { return (n / stages) & 1u; }
+};
+
 __global__ void __launch_bounds__(ABWD_THREADS, 1)
     attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
                        const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                        const AttnBwdParams p) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const DqSmem s = dq_carve(base);
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  if (smem_u32(smem_raw) & 1023u) {  // uniform across the CTA, before any barrier exists
+    if (threadIdx.x == 0) atomicOr(p.status, DEV_ERR_SMEM_LAYOUT);
+    return;
+  }
+  const DqSmem s = dq_carve(smem_raw);
   const int warp = threadIdx.x >> 5;
   const int n_units = *p.n_units;
   const int rows = p.cands_per_tile * p.Lq;
@@ -198,6 +263,8 @@ __global__ void __launch_bounds__(ABWD_THREADS, 1)
   if (threadIdx.x == 0) {
     mbar_init(s.q_full, 1);
     mbar_init(s.q_empty, 1);
+    mbar_init(s.do_full, 1);
+    mbar_init(s.do_empty, 1);
     for (int i = 0; i < DQ_K_STAGES; ++i) {
       mbar_init(&s.k_full[i], 1);
       mbar_init(&s.k_empty[i], 1);
@@ -206,11 +273,16 @@ __global__ void __launch_bounds__(ABWD_THREADS, 1)
       mbar_init(&s.v_full[i], 1);
       mbar_init(&s.v_empty[i], 1);
     }
-    mbar_init(s.s_full, 1);
-    mbar_init(s.s_free, 128);
-    mbar_init(s.ds_full, 128);
-    mbar_init(s.dq_done, 1);
-    mbar_init(s.dq_free, 128);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&s.s_full[b], 1);
+      mbar_init(&s.s_read[b], EW_THREADS);
+      mbar_init(&s.s_free[b], 1);
+    }
+    mbar_init(s.dp_full, 1);
+    mbar_init(s.ds_ready, EW_THREADS);
+    mbar_init(s.dq_full, 1);
+    mbar_init(s.dq_free, EW_THREADS);
+    mbar_init(s.xch_full, EW_THREADS);
     *s.abort = 0;
     fence_barrier_init();
   }
@@ -230,8 +302,9 @@ __global__ void __launch_bounds__(ABWD_THREADS, 1)
   const uint32_t tmem = *s.tmem_slot;
 
   if (warp == 0) {
-    // ---- TMA: Q and dO tiles per unit; K tiles (pass 1), K and V tiles (pass 2)
-    uint32_t qc = 0, kc = 0, vc = 0;
+    // ---- TMA: per unit Q, the K tiles of pass 1, dO, then K and V of pass 2
+    uint32_t nq = 0;
+    Ring kr, vr;
     for (int unit = blockIdx.x; unit < n_units; unit += gridDim.x) {
       const QUnit x = dq_unit(p, unit);
       if (!x.ok) {
@@ -242,98 +315,150 @@ __global__ void __launch_bounds__(ABWD_THREADS, 1)
       int cand[16];
 #pragma unroll
       for (int j = 0; j < 16; ++j) cand[j] = j < x.cnt ? __ldg(p.perm + x.start + j) : p.n_cand;
-      if (!wwait(s.q_empty, (qc & 1u) ^ 1u, s.abort, p.timeout_ns)) goto done;
-      ++qc;
+      if (!wwait(s.q_empty, (nq & 1u) ^ 1u, s.abort, p.timeout_ns)) goto done;
       if (elect_one()) {
-        mbar_arrive_expect_tx(s.q_full, 2u * static_cast<uint32_t>(rows) * 256u);
+        mbar_arrive_expect_tx(s.q_full, static_cast<uint32_t>(rows) * 256u);
         load_qtile(p, &tmQ, s.q, s.q_full, x.h, cand);
-        load_qtile(p, &tmDO, s.go, s.q_full, x.h, cand);
       }
       __syncwarp();
-      for (int pass = 0; pass < 2; ++pass)
+      for (int pass = p.lse_in ? 1 : 0; pass < 2; ++pass) {  // pass 1 only without the forward's LSE
+        if (pass == 1) {
+          if (!wwait(s.do_empty, (nq & 1u) ^ 1u, s.abort, p.timeout_ns)) goto done;
+          if (elect_one()) {
+            mbar_arrive_expect_tx(s.do_full, static_cast<uint32_t>(rows) * 256u);
+            load_qtile(p, &tmDO, s.go, s.do_full, x.h, cand);
+          }
+          __syncwarp();
+        }
         for (int jt = 0; jt < x.ntiles; ++jt) {
-          const int ks = static_cast<int>(kc % DQ_K_STAGES);
-          if (!wwait(&s.k_empty[ks], ((kc / DQ_K_STAGES) & 1u) ^ 1u, s.abort, p.timeout_ns)) goto done;
+          const int ks = kr.slot(DQ_K_STAGES);
+          if (!wwait(&s.k_empty[ks], kr.parity(DQ_K_STAGES) ^ 1u, s.abort, p.timeout_ns)) goto done;
           if (elect_one()) {
             mbar_arrive_expect_tx(&s.k_full[ks], TILE);
             load_kv(p, &tmK, s.k + ks * TILE, &s.k_full[ks], x.u, x.h, x.k.kv0, jt * 128);
           }
           __syncwarp();
-          ++kc;
+          ++kr.n;
           if (pass == 1) {
-            const int vs = static_cast<int>(vc % DQ_V_STAGES);
-            if (!wwait(&s.v_empty[vs], ((vc / DQ_V_STAGES) & 1u) ^ 1u, s.abort, p.timeout_ns)) goto done;
+            const int vs = vr.slot(DQ_V_STAGES);
+            if (!wwait(&s.v_empty[vs], vr.parity(DQ_V_STAGES) ^ 1u, s.abort, p.timeout_ns)) goto done;
             if (elect_one()) {
               mbar_arrive_expect_tx(&s.v_full[vs], TILE);
               load_kv(p, &tmV, s.v + vs * TILE, &s.v_full[vs], x.u, x.h, x.k.kv0, jt * 128);
             }
             __syncwarp();
-            ++vc;
+            ++vr.n;
           }
         }
+      }
+      ++nq;
     }
   } else if (warp == 1) {
-    // ---- MMA issuer
-    uint32_t qc = 0, kc = 0, vc = 0, ns = 0, nds = 0, nu = 0;
+    // ---- MMA issuer.  S buffers alternate over every S of the kernel; a
+    // buffer is reused once its last reader let it go: the element-wise warps
+    // (pass 1) or the dQ product that read dS from it (pass 2).
+    uint32_t nq = 0, sc = 0, nds = 0, nu = 0;
+    // per buffer: kind of its last use (0 none, 1 pass 1, 2 pass 2) and the
+    // completions of s_read / s_free waited so far (scalars: no local memory)
+    uint32_t used0 = 0, used1 = 0, reads0 = 0, reads1 = 0, frees0 = 0, frees1 = 0;
+    Ring kr, vr;
     const uint32_t q_base = smem_u32(s.q), go_base = smem_u32(s.go);
+    // S = Q K^T into the next buffer; kind 1 (pass 1) or 2 (pass 2)
+    auto issue_s = [&](int kslot, uint32_t kind) -> bool {
+      const int b = static_cast<int>(sc & 1u);
+      const uint32_t last = b ? used1 : used0;
+      if (last == 1) {
+        if (!wwait(&s.s_read[b], (b ? reads1 : reads0) & 1u, s.abort, p.timeout_ns)) return false;
+        if (b) ++reads1; else ++reads0;
+      } else if (last == 2) {
+        if (!wwait(&s.s_free[b], (b ? frees1 : frees0) & 1u, s.abort, p.timeout_ns)) return false;
+        if (b) ++frees1; else ++frees0;
+      }
+      if (b) used1 = kind; else used0 = kind;
+      tc_fence_after();
+      if (elect_one()) {
+        mma_rows_dot(tmem + TQ_S + 128u * b, q_base, smem_u32(s.k + kslot * TILE));
+        mma_commit(&s.s_full[b]);
+        if (kind == 1) mma_commit(&s.k_empty[kslot]);
+      }
+      __syncwarp();
+      ++sc;
+      return true;
+    };
+    auto issue_dp = [&](bool last) -> bool {
+      const int vs = vr.slot(DQ_V_STAGES);
+      if (!wwait(&s.v_full[vs], vr.parity(DQ_V_STAGES), s.abort, p.timeout_ns)) return false;
+      tc_fence_after();
+      if (elect_one()) {
+        mma_rows_dot(tmem + TQ_DP, go_base, smem_u32(s.v + vs * TILE));
+        mma_commit(s.dp_full);
+        mma_commit(&s.v_empty[vs]);
+        if (last) mma_commit(s.do_empty);  // last reader of dO
+      }
+      __syncwarp();
+      ++vr.n;
+      return true;
+    };
     for (int unit = blockIdx.x; unit < n_units; unit += gridDim.x) {
       const QUnit x = dq_unit(p, unit);
       if (!x.ok || x.ntiles == 0) continue;
-      if (!wwait(s.q_full, qc & 1u, s.abort, p.timeout_ns)) goto done;
-      ++qc;
-      for (int jt = 0; jt < x.ntiles; ++jt) {  // pass 1: S only
-        const int ks = static_cast<int>(kc % DQ_K_STAGES);
-        if (!wwait(&s.k_full[ks], (kc / DQ_K_STAGES) & 1u, s.abort, p.timeout_ns)) goto done;
-        if (ns > 0 && !wwait(s.s_free, (ns - 1) & 1u, s.abort, p.timeout_ns)) goto done;
-        tc_fence_after();
-        if (elect_one()) {
-          mma_rows_dot(tmem + TQ_S, q_base, smem_u32(s.k + ks * TILE));
-          mma_commit(s.s_full);
-          mma_commit(&s.k_empty[ks]);
-        }
-        __syncwarp();
-        ++ns;
-        ++kc;
+      const int n = x.ntiles;
+      if (!wwait(s.q_full, nq & 1u, s.abort, p.timeout_ns)) goto done;
+      for (int jt = 0; jt < (p.lse_in ? 0 : n); ++jt) {  // pass 1: S only
+        const int ks = kr.slot(DQ_K_STAGES);
+        if (!wwait(&s.k_full[ks], kr.parity(DQ_K_STAGES), s.abort, p.timeout_ns)) goto done;
+        if (!issue_s(ks, 1)) goto done;
+        ++kr.n;
       }
-      for (int jt = 0; jt < x.ntiles; ++jt) {  // pass 2: S, dP, then dQ += dS K
-        const int ks = static_cast<int>(kc % DQ_K_STAGES);
-        const int vs = static_cast<int>(vc % DQ_V_STAGES);
-        const uint32_t k_base = smem_u32(s.k + ks * TILE);
-        if (!wwait(&s.k_full[ks], (kc / DQ_K_STAGES) & 1u, s.abort, p.timeout_ns)) goto done;
-        if (!wwait(&s.v_full[vs], (vc / DQ_V_STAGES) & 1u, s.abort, p.timeout_ns)) goto done;
-        if (!wwait(s.s_free, (ns - 1) & 1u, s.abort, p.timeout_ns)) goto done;
-        tc_fence_after();
-        if (elect_one()) {
-          mma_rows_dot(tmem + TQ_S, q_base, k_base);
-          mma_rows_dot(tmem + TQ_DP, go_base, smem_u32(s.v + vs * TILE));
-          mma_commit(s.s_full);
-          mma_commit(&s.v_empty[vs]);
-          if (jt + 1 == x.ntiles) mma_commit(s.q_empty);  // last reader of Q and dO
+      // pass 2: S(0), dP(0); then per tile S(j+1), dQ += dS(j) K(j), dP(j+1)
+      if (!wwait(s.do_full, nq & 1u, s.abort, p.timeout_ns)) goto done;
+      int kslot = kr.slot(DQ_K_STAGES);
+      if (!wwait(&s.k_full[kslot], kr.parity(DQ_K_STAGES), s.abort, p.timeout_ns)) goto done;
+      uint32_t b_cur = sc & 1u;
+      if (!issue_s(kslot, 2)) goto done;
+      ++kr.n;
+      if (n == 1 && elect_one()) mma_commit(s.q_empty);
+      __syncwarp();
+      if (!issue_dp(n == 1)) goto done;
+      for (int jt = 0; jt < n; ++jt) {
+        int knext = -1;
+        uint32_t b_next = 0;
+        if (jt + 1 < n) {
+          knext = kr.slot(DQ_K_STAGES);
+          if (!wwait(&s.k_full[knext], kr.parity(DQ_K_STAGES), s.abort, p.timeout_ns)) goto done;
+          b_next = sc & 1u;
+          if (!issue_s(knext, 2)) goto done;
+          ++kr.n;
+          if (jt + 2 == n && elect_one()) mma_commit(s.q_empty);  // last reader of Q
+          __syncwarp();
         }
-        __syncwarp();
-        ++ns;
-        ++vc;
-        if (!wwait(s.ds_full, nds & 1u, s.abort, p.timeout_ns)) goto done;
+        if (!wwait(s.ds_ready, nds & 1u, s.abort, p.timeout_ns)) goto done;
         ++nds;
         if (jt == 0 && nu > 0 && !wwait(s.dq_free, (nu - 1) & 1u, s.abort, p.timeout_ns)) goto done;
         tc_fence_after();
         if (elect_one()) {
-          mma_tmem_by_tile(tmem + TQ_DQ, tmem + TQ_DS, k_base, jt > 0);
-          mma_commit(s.dq_done);
-          mma_commit(&s.k_empty[ks]);
+          mma_inplace_by_tile(tmem + TQ_DQ, tmem + TQ_S + 128u * b_cur, smem_u32(s.k + kslot * TILE), jt > 0);
+          mma_commit(&s.s_free[b_cur]);
+          mma_commit(&s.k_empty[kslot]);
+          if (jt + 1 == n) mma_commit(s.dq_full);
         }
         __syncwarp();
-        ++kc;
+        if (jt + 1 < n && !issue_dp(jt + 2 == n)) goto done;
+        kslot = knext;
+        b_cur = b_next;
       }
+      ++nq;
       ++nu;
     }
-  } else if (warp >= 4) {
-    // ---- element-wise warps: thread = TMEM lane = query row r of the tile
-    const int quarter = warp - 4;
+  } else if (warp >= EW_WARP0) {
+    // ---- element-wise warps: lane = query row r of the tile; grp picks the
+    // half of the tile's 128 key columns (and of dQ's d columns)
+    const int ew = warp - EW_WARP0, quarter = ew & 3, grp = ew >> 2;
     const int r = quarter * 32 + static_cast<int>(lane_id());
     const uint32_t lane_base = static_cast<uint32_t>(32 * quarter) << 16;
+    const uint32_t col0 = 64u * grp;
     const float sl = p.scale_log2;
-    uint32_t ns = 0, ndq = 0;
+    uint32_t sc = 0, ndp = 0, ndq = 0, nx = 0;
     for (int unit = blockIdx.x; unit < n_units; unit += gridDim.x) {
       const QUnit x = dq_unit(p, unit);
       if (!x.ok) continue;
@@ -341,17 +466,19 @@ __global__ void __launch_bounds__(ABWD_THREADS, 1)
       const bool valid = r < rows && slot < x.cnt;
       const int cand = valid ? __ldg(p.perm + x.start + slot) : 0;
       const size_t row = (static_cast<size_t>(cand) * p.H + x.h) * p.Lq + q;
-      uint4* dq_row = reinterpret_cast<uint4*>(p.dQ + row * 128);
       if (x.ntiles == 0) {  // no keys: dQ = 0; no row of this user reaches the dK/dV kernel
         if (valid) {
+          uint4* dq_row = reinterpret_cast<uint4*>(p.dQ + row * 128 + col0);
 #pragma unroll
-          for (int c = 0; c < 16; ++c) dq_row[c] = make_uint4(0, 0, 0, 0);
-          p.lse[row] = INFINITY;
-          p.Drow[row] = 0.f;
+          for (int c = 0; c < 8; ++c) dq_row[c] = make_uint4(0, 0, 0, 0);
+          if (grp == 0) {
+            p.lse[row] = INFINITY;
+            p.Drow[row] = 0.f;
+          }
         }
         continue;
       }
-      // D = rowsum(dO * O)
+      // D = rowsum(dO * O) over all of d (both halves compute it: no exchange)
       float D = 0.f;
       if (valid) {
         const uint4* orow = reinterpret_cast<const uint4*>(p.O + row * 128);
@@ -367,88 +494,109 @@ __global__ void __launch_bounds__(ABWD_THREADS, 1)
           }
         }
       }
-      // pass 1: m, l over the user's keys (log2 domain)
-      float m = -INFINITY, l = 0.f;
-      for (int jt = 0; jt < x.ntiles; ++jt) {
-        if (!wwait(s.s_full, ns & 1u, s.abort, p.timeout_ns)) goto done;
-        ++ns;
-        tc_fence_after();
-        const int ncols = min(128, x.k.L - jt * 128);
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          uint32_t v[32];
-          tmem_ld32(tmem + lane_base + TQ_S + c * 32, v);
-          tmem_ld_wait(v);
+      float lse2;
+      if (p.lse_in) {  // the forward's natural-log LSE -> log2 domain; rows without a query: any finite value
+        lse2 = valid ? p.lse_in[row] * 1.4426950408889634f : 0.f;
+      } else {
+        // pass 1: running max and sum over this half's key columns (log2 domain)
+        float m = -INFINITY, l = 0.f;
+        for (int jt = 0; jt < x.ntiles; ++jt) {
+          const uint32_t b = sc & 1u;
+          if (!wwait(&s.s_full[b], (sc >> 1) & 1u, s.abort, p.timeout_ns)) goto done;
+          ++sc;
+          tc_fence_after();
+          const int kcol = jt * 128 + static_cast<int>(col0);
+          uint32_t v[2][32];
+          tmem_ld32(tmem + lane_base + TQ_S + 128u * b + col0, v[0]);
+          tmem_ld32(tmem + lane_base + TQ_S + 128u * b + col0 + 32, v[1]);
+          tmem_ld_wait(v[0]);
+          tmem_ld_wait(v[1]);
+          tc_fence_before();
+          mbar_arrive(&s.s_read[b]);
           float mx = -INFINITY;
 #pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (c * 32 + j < ncols) mx = fmaxf(mx, __uint_as_float(v[j]) * sl);
+          for (int c = 0; c < 2; ++c)
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (kcol + c * 32 + j < x.k.L) mx = fmaxf(mx, __uint_as_float(v[c][j]) * sl);
           const float m_new = fmaxf(m, mx);
           if (m_new == -INFINITY) continue;
           float add = 0.f;
 #pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (c * 32 + j < ncols) add += ex2(fmaf(__uint_as_float(v[j]), sl, -m_new));
+          for (int c = 0; c < 2; ++c)
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (kcol + c * 32 + j < x.k.L) add += ex2(fmaf(__uint_as_float(v[c][j]), sl, -m_new));
           l = l * ex2(m - m_new) + add;
           m = m_new;
         }
-        tc_fence_before();
-        mbar_arrive(s.s_free);
+        // combine the two halves' (max, sum): post, then read the partner's
+        s.xch[grp * 128 + r] = make_float2(m, l);
+        mbar_arrive(s.xch_full);
+        if (!wwait(s.xch_full, nx & 1u, s.abort, p.timeout_ns)) goto done;
+        ++nx;
+        {
+          const float2 o = s.xch[(grp ^ 1) * 128 + r];
+          const float mm = fmaxf(m, o.x);
+          const float ll = (mm == -INFINITY) ? 0.f : l * ex2(m - mm) + o.y * ex2(o.x - mm);
+          m = mm;
+          l = ll;
+        }
+        lse2 = l > 0.f ? m + __log2f(l) : INFINITY;
       }
-      const float lse2 = (valid && l > 0.f) ? m + __log2f(l) : INFINITY;
-      if (valid) {
+      if (valid && grp == 0) {
         p.lse[row] = lse2;
         p.Drow[row] = D;
       }
-      // pass 2: dS = P (dP - D) scale -> TMEM (bf16 pairs)
+      // pass 2: P = 2^(s sl - lse), dS = P (dP - D) scale written over S
       for (int jt = 0; jt < x.ntiles; ++jt) {
-        if (!wwait(s.s_full, ns & 1u, s.abort, p.timeout_ns)) goto done;
-        ++ns;
-        if (jt > 0) {  // the previous dQ MMA has read dS
-          if (!wwait(s.dq_done, ndq & 1u, s.abort, p.timeout_ns)) goto done;
-          ++ndq;
-        }
+        const uint32_t b = sc & 1u;
+        if (!wwait(&s.s_full[b], (sc >> 1) & 1u, s.abort, p.timeout_ns)) goto done;
+        ++sc;
         tc_fence_after();
-        const int ncols = min(128, x.k.L - jt * 128);
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          uint32_t sv[32], dv[32], pk[16];
-          tmem_ld32(tmem + lane_base + TQ_S + c * 32, sv);
-          tmem_ld_wait(sv);
-          tmem_ld32(tmem + lane_base + TQ_DP + c * 32, dv);
+        const int kcol = jt * 128 + static_cast<int>(col0);
+        float pf[64];
+        {
+          uint32_t v[2][32];
+          tmem_ld32(tmem + lane_base + TQ_S + 128u * b + col0, v[0]);
+          tmem_ld32(tmem + lane_base + TQ_S + 128u * b + col0 + 32, v[1]);
+          tmem_ld_wait(v[0]);
+          tmem_ld_wait(v[1]);
+#pragma unroll
+          for (int c = 0; c < 2; ++c)
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              pf[c * 32 + j] =
+                  kcol + c * 32 + j < x.k.L ? ex2(fmaf(__uint_as_float(v[c][j]), sl, -lse2)) : 0.f;
+        }
+        if (!wwait(s.dp_full, ndp & 1u, s.abort, p.timeout_ns)) goto done;
+        ++ndp;
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint32_t dv[32], pk[16];
+          tmem_ld32(tmem + lane_base + TQ_DP + col0 + 32 * c, dv);
           tmem_ld_wait(dv);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int c0 = c * 32 + 2 * j;
-            const float p0 = c0 < ncols ? ex2(fmaf(__uint_as_float(sv[2 * j]), sl, -lse2)) : 0.f;
-            const float p1 = c0 + 1 < ncols ? ex2(fmaf(__uint_as_float(sv[2 * j + 1]), sl, -lse2)) : 0.f;
-            pk[j] = pack_bf16x2(p0 * (__uint_as_float(dv[2 * j]) - D) * p.scale,
-                                p1 * (__uint_as_float(dv[2 * j + 1]) - D) * p.scale);
-          }
-          tmem_st16(tmem + lane_base + TQ_DS + c * 16, pk);
+          for (int j = 0; j < 16; ++j)
+            pk[j] = pack_bf16x2(pf[c * 32 + 2 * j] * (__uint_as_float(dv[2 * j]) - D) * p.scale,
+                                pf[c * 32 + 2 * j + 1] * (__uint_as_float(dv[2 * j + 1]) - D) * p.scale);
+          tmem_st16(tmem + lane_base + TQ_S + 128u * b + col0 + 16 * c, pk);
         }
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(s.s_free);
-        mbar_arrive(s.ds_full);
+        mbar_arrive(s.ds_ready);
       }
-      // epilogue: dQ (fp32 TMEM) -> bf16 row
-      if (!wwait(s.dq_done, ndq & 1u, s.abort, p.timeout_ns)) goto done;
+      // epilogue: this half's 64 d columns of dQ (fp32 TMEM) -> bf16
+      if (!wwait(s.dq_full, ndq & 1u, s.abort, p.timeout_ns)) goto done;
       ++ndq;
       tc_fence_after();
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t v[32];
-        tmem_ld32(tmem + lane_base + TQ_DQ + c * 32, v);
-        tmem_ld_wait(v);
-        if (valid) {
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            dq_row[c * 4 + k] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * k]), __uint_as_float(v[8 * k + 1])),
-                                           pack_bf16x2(__uint_as_float(v[8 * k + 2]), __uint_as_float(v[8 * k + 3])),
-                                           pack_bf16x2(__uint_as_float(v[8 * k + 4]), __uint_as_float(v[8 * k + 5])),
-                                           pack_bf16x2(__uint_as_float(v[8 * k + 6]), __uint_as_float(v[8 * k + 7])));
-        }
+      for (int c = 0; c < 2; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_base + TQ_DQ + col0 + 32 * c, v);
+        tmem_ld_wait(v);
+        if (valid) store_bf16x32(p.dQ + row * 128 + col0 + 32 * c, v);
       }
       tc_fence_before();
       mbar_arrive(s.dq_free);
@@ -465,9 +613,8 @@ done:
 }
 
 // ============================================================= dK/dV kernel
-// TMEM columns: S^T [0,128) (then P^T as bf16 pairs in [0,64)), dP^T [128,256)
-// (then dS^T in [128,192)), dV [256,384), dK [384,512).  Each P^T / dS^T
-// chunk is written over columns its own chunk of S^T / dP^T has been read from.
+// TMEM columns: S^T [0,128) (P^T written over it), dP^T [128,256) (dS^T
+// written over it), dV [256,384), dK [384,512).
 constexpr uint32_t TK_ST = 0, TK_DPT = 128, TK_DV = 256, TK_DK = 384;
 
 struct KvSmem {
@@ -479,17 +626,23 @@ struct KvSmem {
   float* drow;     // [2][128]
   uint64_t* kv_full;
   uint64_t* kv_empty;
-  uint64_t* q_full;   // [2]
-  uint64_t* q_empty;  // [2]
-  uint64_t* st_full;  // S^T and dP^T computed
-  uint64_t* pds_full; // P^T and dS^T written
-  uint64_t* pv_done;  // dV, dK products of a tile completed
-  uint64_t* acc_free; // the block's dV, dK read out
+  uint64_t* q_full;    // [2]
+  uint64_t* q_empty;   // [2]
+  uint64_t* s_full;    // S^T computed
+  uint64_t* dp_full;   // dP^T computed
+  uint64_t* p_ready;   // P^T written (S^T read)
+  uint64_t* ds_ready;  // dS^T written (dP^T read)
+  uint64_t* dv_done;   // dV += P^T dO completed (P^T read)
+  uint64_t* dk_done;   // dK += dS^T Q completed (dS^T read)
+  uint64_t* acc_full;  // the block's dV, dK complete
+  uint64_t* acc_free;  // ... and read out
   uint32_t* tmem_slot;
   uint32_t* abort;
 };
 constexpr uint32_t KV_TILES = 6 * TILE;
-constexpr uint32_t KV_SMEM = 1024 + KV_TILES + 4 * 2 * 128 * 4 + 8 * 10 + 8;
+constexpr uint32_t KV_BARS = 14;
+constexpr uint32_t KV_SMEM_USED = KV_TILES + 4 * 2 * 128 * 4 + 8 * KV_BARS + 8;
+constexpr uint32_t KV_SMEM = KV_SMEM_USED + 1024;
 
 __device__ __forceinline__ KvSmem kv_carve(uint8_t* base) {
   KvSmem s;
@@ -500,15 +653,21 @@ __device__ __forceinline__ KvSmem kv_carve(uint8_t* base) {
   s.lse = reinterpret_cast<float*>(base + KV_TILES);
   s.drow = s.lse + 2 * 128;
   uint64_t* b = reinterpret_cast<uint64_t*>(s.drow + 2 * 128);
-  s.kv_full = b;
-  s.kv_empty = b + 1;
-  s.q_full = b + 2;
-  s.q_empty = b + 4;
-  s.st_full = b + 6;
-  s.pds_full = b + 7;
-  s.pv_done = b + 8;
-  s.acc_free = b + 9;
-  s.tmem_slot = reinterpret_cast<uint32_t*>(b + 10);
+  s.kv_full = b++;
+  s.kv_empty = b++;
+  s.q_full = b;
+  b += 2;
+  s.q_empty = b;
+  b += 2;
+  s.s_full = b++;
+  s.dp_full = b++;
+  s.p_ready = b++;
+  s.ds_ready = b++;
+  s.dv_done = b++;
+  s.dk_done = b++;
+  s.acc_full = b++;
+  s.acc_free = b++;
+  s.tmem_slot = reinterpret_cast<uint32_t*>(b);
   s.abort = s.tmem_slot + 1;
   return s;
 }
@@ -542,9 +701,14 @@ __global__ void __launch_bounds__(ABWD_THREADS, 1)
     attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
                          const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                          const AttnBwdParams p) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const KvSmem s = kv_carve(base);
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t pad = ((raw + 1023u) & ~1023u) - raw;
+  if (pad + KV_SMEM_USED > KV_SMEM) {  // uniform across the CTA, before any barrier exists
+    if (threadIdx.x == 0) atomicOr(p.status, DEV_ERR_SMEM_LAYOUT);
+    return;
+  }
+  const KvSmem s = kv_carve(smem_raw + pad);
   const int warp = threadIdx.x >> 5;
   const int n_items = __ldg(p.blk_prefix + p.n_users) * p.H;
   const int cpt = p.cands_per_tile, rows = cpt * p.Lq;
@@ -555,15 +719,19 @@ __global__ void __launch_bounds__(ABWD_THREADS, 1)
   fence_proxy_async_smem();
   if (threadIdx.x == 0) {
     mbar_init(s.kv_full, 1);
-    mbar_init(s.kv_empty, 1);
+    mbar_init(s.kv_empty, 2);  // both issuers
     for (int b = 0; b < 2; ++b) {
       mbar_init(&s.q_full[b], 1);
-      mbar_init(&s.q_empty[b], 1);
+      mbar_init(&s.q_empty[b], 2);
     }
-    mbar_init(s.st_full, 1);
-    mbar_init(s.pds_full, 128);
-    mbar_init(s.pv_done, 1);
-    mbar_init(s.acc_free, 128);
+    mbar_init(s.s_full, 1);
+    mbar_init(s.dp_full, 1);
+    mbar_init(s.p_ready, EW_THREADS);
+    mbar_init(s.ds_ready, EW_THREADS);
+    mbar_init(s.dv_done, 1);
+    mbar_init(s.dk_done, 1);
+    mbar_init(s.acc_full, 2);
+    mbar_init(s.acc_free, EW_THREADS);
     *s.abort = 0;
     fence_barrier_init();
   }
@@ -600,34 +768,53 @@ __global__ void __launch_bounds__(ABWD_THREADS, 1)
       for (int t = 0; t < x.ntq; ++t, ++tq) {
         const int b = static_cast<int>(tq & 1u);
         if (!wwait(&s.q_empty[b], ((tq >> 1) & 1u) ^ 1u, s.abort, p.timeout_ns)) goto done;
+        // lane j < n holds the tile's j-th candidate; the copies go out first,
+        // the rows' LSE and D (independent loads, 4 rows per lane) after them
         const int first = t * cpt, n = min(cpt, x.count - first);
+        const int lane = static_cast<int>(lane_id());
+        const int mine = lane < n ? __ldg(p.perm + x.seg0 + first + lane) : p.n_cand;
         int cand[16];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) cand[j] = j < n ? __ldg(p.perm + x.seg0 + first + j) : p.n_cand;
-        for (int r = static_cast<int>(lane_id()); r < 128; r += 32) {
-          const int slot = r / p.Lq, q = r - slot * p.Lq;
-          float lse = INFINITY, dr = 0.f;  // rows without a query: P = 0
-          if (r < rows && slot < n) {
-            const size_t row = (static_cast<size_t>(__ldg(p.perm + x.seg0 + first + slot)) * p.H + x.h) * p.Lq + q;
-            lse = p.lse[row];
-            dr = p.Drow[row];
-          }
-          s.lse[b * 128 + r] = lse;
-          s.drow[b * 128 + r] = dr;
-        }
-        __syncwarp();
+        for (int j = 0; j < 16; ++j) cand[j] = __shfl_sync(0xffffffffu, mine, j);
         if (elect_one()) {
-          mbar_arrive_expect_tx(&s.q_full[b], 2u * static_cast<uint32_t>(rows) * 256u);
+          mbar_expect_tx(&s.q_full[b], 2u * static_cast<uint32_t>(rows) * 256u);
           load_qtile(p, &tmQ, s.q + b * TILE, &s.q_full[b], x.h, cand);
           load_qtile(p, &tmDO, s.go + b * TILE, &s.q_full[b], x.h, cand);
         }
         __syncwarp();
+        float lv[4], dr[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int r = lane + 32 * k, slot = r / p.Lq, q = r - slot * p.Lq;
+          const int c = __shfl_sync(0xffffffffu, mine, slot & 31);
+          lv[k] = INFINITY;  // rows without a query: P = 0
+          dr[k] = 0.f;
+          if (r < rows && slot < n) {
+            const size_t row = (static_cast<size_t>(c) * p.H + x.h) * p.Lq + q;
+            lv[k] = p.lse[row];
+            dr[k] = p.Drow[row];
+          }
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          s.lse[b * 128 + lane + 32 * k] = lv[k];
+          s.drow[b * 128 + lane + 32 * k] = dr[k];
+        }
+        __syncwarp();
+        if (elect_one()) mbar_arrive(&s.q_full[b]);
+        __syncwarp();
       }
     }
-  } else if (warp == 1) {
-    // ---- MMA issuer
+  } else if (warp == 1 || warp == 2) {
+    // ---- MMA issuers, one per accumulator: warp 1 S^T and dV += P^T dO,
+    // warp 2 dP^T and dK += dS^T Q.  S^T(t) waits only for dV(t-1) (the
+    // reader of the P^T written over S^T(t-1)), dP^T(t) only for dK(t-1).
+    const bool a_side = warp == 1;
     uint32_t ni = 0, tq = 0;
-    const uint32_t k_base = smem_u32(s.k), v_base = smem_u32(s.v);
+    const uint32_t a_base = smem_u32(a_side ? s.k : s.v);
+    uint64_t* done_bar = a_side ? s.dv_done : s.dk_done;
+    uint64_t* ready_bar = a_side ? s.p_ready : s.ds_ready;
+    const uint32_t t_in = a_side ? TK_ST : TK_DPT, t_acc = a_side ? TK_DV : TK_DK;
     for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
       const KvItem x = kv_item(p, item);
       if (x.ntq == 0) continue;
@@ -636,48 +823,49 @@ __global__ void __launch_bounds__(ABWD_THREADS, 1)
         const int b = static_cast<int>(tq & 1u);
         const uint32_t q_base = smem_u32(s.q + b * TILE), go_base = smem_u32(s.go + b * TILE);
         if (!wwait(&s.q_full[b], (tq >> 1) & 1u, s.abort, p.timeout_ns)) goto done;
-        // S^T and dP^T overwrite the previous tile's P^T and dS^T: wait for their readers
-        if (tq > 0 && !wwait(s.pv_done, (tq - 1) & 1u, s.abort, p.timeout_ns)) goto done;
+        if (tq > 0 && !wwait(done_bar, (tq - 1) & 1u, s.abort, p.timeout_ns)) goto done;
         tc_fence_after();
-        if (elect_one()) {
-          mma_rows_dot(tmem + TK_ST, k_base, q_base);
-          mma_rows_dot(tmem + TK_DPT, v_base, go_base);
-          mma_commit(s.st_full);
-          if (t + 1 == x.ntq) mma_commit(s.kv_empty);  // last reader of K and V
+        if (elect_one()) {  // S^T = K Q^T  or  dP^T = V dO^T
+          mma_rows_dot(tmem + t_in, a_base, a_side ? q_base : go_base);
+          mma_commit(a_side ? s.s_full : s.dp_full);
+          if (t + 1 == x.ntq) mma_commit(s.kv_empty);  // last reader of K (V)
         }
         __syncwarp();
-        if (!wwait(s.pds_full, tq & 1u, s.abort, p.timeout_ns)) goto done;
+        if (!wwait(ready_bar, tq & 1u, s.abort, p.timeout_ns)) goto done;
         if (t == 0 && ni > 0 && !wwait(s.acc_free, (ni - 1) & 1u, s.abort, p.timeout_ns)) goto done;
         tc_fence_after();
-        if (elect_one()) {
-          mma_tmem_by_tile(tmem + TK_DV, tmem + TK_ST, go_base, t > 0);  // dV += P^T dO
-          mma_tmem_by_tile(tmem + TK_DK, tmem + TK_DPT, q_base, t > 0);  // dK += dS^T Q
-          mma_commit(s.pv_done);
+        if (elect_one()) {  // dV += P^T dO  or  dK += dS^T Q
+          mma_inplace_by_tile(tmem + t_acc, tmem + t_in, a_side ? go_base : q_base, t > 0);
+          mma_commit(done_bar);
           mma_commit(&s.q_empty[b]);
+          if (t + 1 == x.ntq) mma_commit(s.acc_full);
         }
         __syncwarp();
       }
       ++ni;
     }
-  } else if (warp >= 4) {
-    // ---- element-wise warps: thread = TMEM lane = key row of the block
-    const int quarter = warp - 4;
+  } else if (warp >= EW_WARP0) {
+    // ---- element-wise warps: lane = key row of the block; grp picks the
+    // half of the tile's 128 query columns (and of dK/dV's d columns)
+    const int ew = warp - EW_WARP0, quarter = ew & 3, grp = ew >> 2;
     const int rk = quarter * 32 + static_cast<int>(lane_id());
     const uint32_t lane_base = static_cast<uint32_t>(32 * quarter) << 16;
+    const uint32_t col0 = 64u * grp;
     const float sl = p.scale_log2;
-    uint32_t tq = 0;
+    uint32_t tq = 0, ni = 0;
     for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
       const KvItem x = kv_item(p, item);
       const int key = x.kb * 128 + rk;
       const bool kvalid = key < x.k.L;
       const size_t krow = p.kv_offsets ? (static_cast<size_t>(x.k.kv0 + key) * p.H + x.h)
                                        : ((static_cast<size_t>(x.u) * p.H + x.h) * p.Lkv + key);
-      uint4* dk_row = reinterpret_cast<uint4*>(p.dK + krow * 128);
-      uint4* dv_row = reinterpret_cast<uint4*>(p.dV + krow * 128);
+      uint16_t* dk_row = p.dK + krow * 128 + col0;
+      uint16_t* dv_row = p.dV + krow * 128 + col0;
       if (x.ntq == 0) {  // no candidate reads these keys: zero gradients
         if (kvalid) {
 #pragma unroll
-          for (int c = 0; c < 16; ++c) dk_row[c] = dv_row[c] = make_uint4(0, 0, 0, 0);
+          for (int c = 0; c < 8; ++c)
+            reinterpret_cast<uint4*>(dk_row)[c] = reinterpret_cast<uint4*>(dv_row)[c] = make_uint4(0, 0, 0, 0);
         }
         continue;
       }
@@ -685,52 +873,84 @@ __global__ void __launch_bounds__(ABWD_THREADS, 1)
         const int b = static_cast<int>(tq & 1u);
         // the producer's lanes stored this tile's LSE and D before arriving on q_full[b]
         if (!wwait(&s.q_full[b], (tq >> 1) & 1u, s.abort, p.timeout_ns)) goto done;
-        if (!wwait(s.st_full, tq & 1u, s.abort, p.timeout_ns)) goto done;
+        if (!wwait(s.s_full, tq & 1u, s.abort, p.timeout_ns)) goto done;
         tc_fence_after();
-        const float* lse = s.lse + b * 128;
-        const float* drow = s.drow + b * 128;
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          uint32_t sv[32], dv[32], pp[16], pd[16];
-          tmem_ld32(tmem + lane_base + TK_ST + c * 32, sv);
-          tmem_ld_wait(sv);
-          tmem_ld32(tmem + lane_base + TK_DPT + c * 32, dv);
-          tmem_ld_wait(dv);
+        const float* lse = s.lse + b * 128 + col0;
+        const float* drow = s.drow + b * 128 + col0;
+        // P^T = 2^(s sl - lse[q]), written over S^T (pairs at this half's start)
+        float pf[64];
+        {
+          uint32_t v[2][32];
+          tmem_ld32(tmem + lane_base + TK_ST + col0, v[0]);
+          tmem_ld32(tmem + lane_base + TK_ST + col0 + 32, v[1]);
+          tmem_ld_wait(v[0]);
+          tmem_ld_wait(v[1]);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int q0 = c * 32 + 2 * j;
-            const float p0 = kvalid ? ex2(fmaf(__uint_as_float(sv[2 * j]), sl, -lse[q0])) : 0.f;
-            const float p1 = kvalid ? ex2(fmaf(__uint_as_float(sv[2 * j + 1]), sl, -lse[q0 + 1])) : 0.f;
-            pp[j] = pack_bf16x2(p0, p1);
-            pd[j] = pack_bf16x2(p0 * (__uint_as_float(dv[2 * j]) - drow[q0]) * p.scale,
-                                p1 * (__uint_as_float(dv[2 * j + 1]) - drow[q0 + 1]) * p.scale);
+          for (int c = 0; c < 2; ++c) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int j4 = 0; j4 < 8; ++j4) {
+              const float4 l4 = *reinterpret_cast<const float4*>(lse + c * 32 + 4 * j4);
+              const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int j = 4 * j4 + e;
+                pf[c * 32 + j] = kvalid ? ex2(fmaf(__uint_as_float(v[c][j]), sl, -lv[e])) : 0.f;
+              }
+            }
+#pragma unroll
+            for (int j = 0; j < 16; ++j) pk[j] = pack_bf16x2(pf[c * 32 + 2 * j], pf[c * 32 + 2 * j + 1]);
+            tmem_st16(tmem + lane_base + TK_ST + col0 + 16 * c, pk);
           }
-          tmem_st16(tmem + lane_base + TK_ST + c * 16, pp);
-          tmem_st16(tmem + lane_base + TK_DPT + c * 16, pd);
         }
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(s.pds_full);
+        mbar_arrive(s.p_ready);
+        // dS^T = P^T (dP^T - D[q]) scale, written over dP^T
+        if (!wwait(s.dp_full, tq & 1u, s.abort, p.timeout_ns)) goto done;
+        tc_fence_after();
+        {
+          uint32_t v[2][32];
+          tmem_ld32(tmem + lane_base + TK_DPT + col0, v[0]);
+          tmem_ld32(tmem + lane_base + TK_DPT + col0 + 32, v[1]);
+          tmem_ld_wait(v[0]);
+          tmem_ld_wait(v[1]);
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int j4 = 0; j4 < 4; ++j4) {
+              const float4 d4 = *reinterpret_cast<const float4*>(drow + c * 32 + 8 * j4);
+              const float4 e4 = *reinterpret_cast<const float4*>(drow + c * 32 + 8 * j4 + 4);
+              const float dv8[8] = {d4.x, d4.y, d4.z, d4.w, e4.x, e4.y, e4.z, e4.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int j = 8 * j4 + 2 * e;
+                pk[4 * j4 + e] = pack_bf16x2(pf[c * 32 + j] * (__uint_as_float(v[c][j]) - dv8[2 * e]) * p.scale,
+                                             pf[c * 32 + j + 1] * (__uint_as_float(v[c][j + 1]) - dv8[2 * e + 1]) *
+                                                 p.scale);
+              }
+            }
+            tmem_st16(tmem + lane_base + TK_DPT + col0 + 16 * c, pk);
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(s.ds_ready);
       }
-      // epilogue: the block's dV and dK rows
-      if (!wwait(s.pv_done, (tq - 1) & 1u, s.abort, p.timeout_ns)) goto done;
+      // epilogue: this half's 64 d columns of the block's dV and dK rows
+      if (!wwait(s.acc_full, ni & 1u, s.abort, p.timeout_ns)) goto done;
+      ++ni;
       tc_fence_after();
 #pragma unroll 1
       for (int g = 0; g < 2; ++g) {
-        uint4* out = g == 0 ? dv_row : dk_row;
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          uint32_t v[32];
-          tmem_ld32(tmem + lane_base + (g == 0 ? TK_DV : TK_DK) + c * 32, v);
-          tmem_ld_wait(v);
-          if (kvalid) {
+        uint16_t* out = g == 0 ? dv_row : dk_row;
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-              out[c * 4 + k] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * k]), __uint_as_float(v[8 * k + 1])),
-                                          pack_bf16x2(__uint_as_float(v[8 * k + 2]), __uint_as_float(v[8 * k + 3])),
-                                          pack_bf16x2(__uint_as_float(v[8 * k + 4]), __uint_as_float(v[8 * k + 5])),
-                                          pack_bf16x2(__uint_as_float(v[8 * k + 6]), __uint_as_float(v[8 * k + 7])));
-          }
+        for (int c = 0; c < 2; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tmem + lane_base + (g == 0 ? TK_DV : TK_DK) + col0 + 32 * c, v);
+          tmem_ld_wait(v);
+          if (kvalid) store_bf16x32(out + 32 * c, v);
         }
       }
       tc_fence_before();

@@ -201,6 +201,7 @@ struct AttnParams {
   const int32_t* n_units;    // device scalar written by the segment builder
   const int32_t* kv_offsets; // [n_users+1] or null (dense)
   uint16_t* O;               // [n_cand][H][Lq][d]
+  float* lse;                // [n_cand][H][Lq] natural-log row log-sum-exp, or null (not written)
   uint32_t* status;
   int n_cand, n_users, H, Lq, Lkv;  // Lkv: dense length (ignored when jagged)
   int cands_per_tile;        // floor(128 / Lq)
@@ -220,7 +221,7 @@ struct AttnParams {
 // dK/dV kernel (per (user, head, 128-key block)): over every query tile of
 // the user's candidates, S^T = K Q^T and dP^T = V dO^T with keys on TMEM
 // lanes, then dV += P^T dO and dK += dS^T Q accumulate in TMEM.
-constexpr int ABWD_THREADS = 256;  // warp 0 TMA, 1 MMA + TMEM, 2-3 idle, 4-7 softmax / epilogue
+constexpr int ABWD_THREADS = 384;  // warp 0 TMA, 1 MMA + TMEM, 2 MMA (dK/dV), 3 idle, 4-11 element-wise
 
 struct AttnBwdParams {
   const int32_t* perm;
@@ -236,6 +237,7 @@ struct AttnBwdParams {
   uint16_t* dV;              // like V
   float* lse;                // [n_cand][H][Lq], log2 domain of scale * log2(e) * q.k
   float* Drow;               // [n_cand][H][Lq]
+  const float* lse_in;       // the forward's natural-log LSE [n_cand][H][Lq], or null (recomputed)
   uint32_t* status;
   int n_cand, n_users, H, Lq, Lkv, cands_per_tile;
   float scale, scale_log2;

@@ -230,6 +230,19 @@ ikbo_status_t ikbo_attn_self_target_forward(ikbo_plan_t p, const void* Q, const 
                                             const void* V, const int32_t* d_kv_offsets, void* O, void* O_user,
                                             int Lq_u, int Lkv, int d, float scale, cudaStream_t stream);
 
+/* ikbo_attn_forward for training: the same O (bit-identical), and also each
+ * query row's softmax log-sum-exp, the statistic the backward needs to
+ * recover every probability without a second pass over the keys:
+ *   lse[i,h,q] = log( sum_j exp(scale Q[i,h,q] . K[map[i],h,j]) )   (natural log)
+ * fp32 [n_cand][H][Lq], caller-owned, 4-byte aligned, overwritten; -inf for
+ * the rows of a user with no keys.  Same inputs, limits and errors as
+ * ikbo_attn_forward (lse NULL: IKBO_ERR_INVALID_ARG).  The definition is the
+ * normaliser of the attention in aixai.ru, "Deep Dive: Flash Attention"
+ * (ordinary attention with K/V from the candidate's user). */
+ikbo_status_t ikbo_attn_forward_lse(ikbo_plan_t p, const void* Q, const void* K, const void* V,
+                                    const int32_t* d_kv_offsets, void* O, float* lse, int Lkv, int d, float scale,
+                                    cudaStream_t stream);
+
 /* Broadcast attention backward for training (aibriefing, "Meta Optimizes
  * Inference for Recommendation Systems": the kernels serve training when
  * candidates outnumber users; the pages give no backward, so this is the
@@ -246,6 +259,9 @@ ikbo_status_t ikbo_attn_self_target_forward(ikbo_plan_t p, const void* Q, const 
  * of a user with no keys get dQ = 0.
  *   Q, O, dO bf16 [n_cand][H][Lq][d]; K, V (and dK, dV) dense or jagged
  *   exactly as in ikbo_attn_forward; all 16-byte aligned, none NULL.
+ *   lse: the forward's log-sum-exp (ikbo_attn_forward_lse on the same
+ *   inputs), fp32 [n_cand][H][Lq], 4-byte aligned; or NULL, and the
+ *   backward recomputes it with one more pass over each user's keys.
  * P and dS are rounded to bf16 for the tensor cores (as P is in the
  * forward); accumulation is fp32.  Gradients are overwritten.  Three
  * launches; the plan keeps per-row LSE and D (grown on first use, which
@@ -253,8 +269,8 @@ ikbo_status_t ikbo_attn_self_target_forward(ikbo_plan_t p, const void* Q, const 
  * the plan's map values must be in range (a candidate outside is skipped by
  * the segments, so its dQ is left untouched). */
 ikbo_status_t ikbo_attn_backward(ikbo_plan_t p, const void* Q, const void* K, const void* V, const void* O,
-                                 const void* dO, const int32_t* d_kv_offsets, void* dQ, void* dK, void* dV, int Lkv,
-                                 int d, float scale, cudaStream_t stream);
+                                 const void* dO, const float* lse, const int32_t* d_kv_offsets, void* dQ, void* dK,
+                                 void* dV, int Lkv, int d, float scale, cudaStream_t stream);
 
 /* Synchronise `stream`, then return (and clear) the first device-detected
  * error recorded since the last call: IKBO_ERR_MAP_OUT_OF_RANGE,

@@ -43,7 +43,7 @@ def test_binding_covers_every_declared_symbol():
 
 def test_status_strings_and_version_need_no_gpu(lib):
     binding.load(build.LIB)
-    assert binding.ikbo_version() == 105
+    assert binding.ikbo_version() == 106
     assert binding.ikbo_status_string(0) == "ok"
     assert "range" in binding.ikbo_status_string(4)
     assert binding.ikbo_status_string(99) == "unknown status"
