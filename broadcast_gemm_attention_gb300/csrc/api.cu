@@ -313,10 +313,12 @@ ikbo_status_t attn_backward_launch(ikbo_plan_t p, const void* Q, const void* K, 
   if (d != ATT_D) return IKBO_ERR_UNSUPPORTED;
   if (Lkv < 1 || !(scale > 0.f) || !std::isfinite(scale)) return IKBO_ERR_INVALID_ARG;
   if (attn_bwd_smem_bytes() > p->max_smem) return IKBO_ERR_UNSUPPORTED;
-  const size_t rows = static_cast<size_t>(p->n_cand) * p->H * p->Lq;
+  // per work unit, its 128 tile rows' LSE and D (the work list holds at most
+  // max_units units); the two user prefixes (key blocks, query tiles)
+  const size_t rows = static_cast<size_t>(p->max_units) * ATT_BM;
   if (grow(&p->d_abwd_lse, &p->abwd_lse_elems, rows) != cudaSuccess ||
       grow(&p->d_abwd_drow, &p->abwd_drow_elems, rows) != cudaSuccess ||
-      grow(&p->d_abwd_blk, &p->abwd_blk_elems, static_cast<size_t>(p->n_users) + 1) != cudaSuccess)
+      grow(&p->d_abwd_blk, &p->abwd_blk_elems, 2 * (static_cast<size_t>(p->n_users) + 1)) != cudaSuccess)
     return IKBO_ERR_CUDA;
 
   AttnBwdParams bp;
@@ -327,6 +329,7 @@ ikbo_status_t attn_backward_launch(ikbo_plan_t p, const void* Q, const void* K, 
   bp.offsets = p->d_offsets;
   bp.kv_offsets = d_kv_offsets;
   bp.blk_prefix = p->d_abwd_blk;
+  bp.tile_prefix = p->d_abwd_blk + p->n_users + 1;
   bp.O = static_cast<const uint16_t*>(O);
   bp.dO = static_cast<const uint16_t*>(dO);
   bp.dQ = static_cast<uint16_t*>(dQ);

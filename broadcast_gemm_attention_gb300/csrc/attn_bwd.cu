@@ -10,8 +10,8 @@
 //   dK[u,h] = scale sum_{i in seg u} dS_i^T Q_i,   dV[u,h] = sum_i P_i^T dO_i.
 //
 // Two persistent kernels, one CTA per SM, 12 warps: warp 0 TMA (elected lane
-// issues), warp 1 tcgen05.mma (elected lane) and TMEM owner, warp 2 a second
-// MMA issuer in the dK/dV kernel, warps 4-11 the element-wise work: warps w and w+4 share the 32 TMEM lanes of quarter w % 4
+// issues), warps 1-3 tcgen05.mma issuers (elected lane; one product chain
+// each, warp 1 also owns TMEM), warps 4-11 the element-wise work: warps w and w+4 share the 32 TMEM lanes of quarter w % 4
 // and split the 128 columns of every tile in halves.
 //   attn_bwd_dq_kernel    per work-list unit (a 128-row tile of up to
 //                         floor(128/Lq) candidates' queries, as the forward):
@@ -167,7 +167,8 @@ struct DqSmem {
   uint64_t* s_read;    // [2] pass 1: the element-wise warps have read buffer b
   uint64_t* s_free;    // [2] pass 2: the dQ product reading dS from buffer b completed
   uint64_t* dp_full;   // dP computed
-  uint64_t* ds_ready;  // dS written (and dP read)
+  uint64_t* dp_read;   // dP read by the element-wise warps (the next dP may overwrite it)
+  uint64_t* ds_ready;  // dS written
   uint64_t* dq_full;   // the unit's dQ is complete
   uint64_t* dq_free;   // ... and has been read out
   uint64_t* xch_full;  // every element-wise thread posted its (max, sum)
@@ -176,7 +177,7 @@ struct DqSmem {
 };
 constexpr uint32_t DQ_TILES = (2 + DQ_K_STAGES + DQ_V_STAGES) * TILE;
 constexpr uint32_t DQ_XCH = 2 * 128 * 8;
-constexpr uint32_t DQ_BARS = 4 + 2 * DQ_K_STAGES + 2 * DQ_V_STAGES + 6 + 5;
+constexpr uint32_t DQ_BARS = 4 + 2 * DQ_K_STAGES + 2 * DQ_V_STAGES + 6 + 6;
 constexpr uint32_t DQ_SMEM_USED = DQ_TILES + DQ_XCH + 8 * DQ_BARS + 8;
 constexpr uint32_t DQ_SMEM = DQ_SMEM_USED;  // no alignment slack: the base must be 1024-aligned (checked)
 
@@ -207,6 +208,7 @@ __device__ __forceinline__ DqSmem dq_carve(uint8_t* base) {
   s.s_free = b;
   b += 2;
   s.dp_full = b++;
+  s.dp_read = b++;
   s.ds_ready = b++;
   s.dq_full = b++;
   s.dq_free = b++;
@@ -279,6 +281,7 @@ __global__ void __launch_bounds__(ABWD_THREADS, 1)
       mbar_init(&s.s_free[b], 1);
     }
     mbar_init(s.dp_full, 1);
+    mbar_init(s.dp_read, EW_THREADS);
     mbar_init(s.ds_ready, EW_THREADS);
     mbar_init(s.dq_full, 1);
     mbar_init(s.dq_free, EW_THREADS);
@@ -353,19 +356,20 @@ __global__ void __launch_bounds__(ABWD_THREADS, 1)
       }
       ++nq;
     }
-  } else if (warp == 1) {
-    // ---- MMA issuer.  S buffers alternate over every S of the kernel; a
-    // buffer is reused once its last reader let it go: the element-wise warps
-    // (pass 1) or the dQ product that read dS from it (pass 2).
-    uint32_t nq = 0, sc = 0, nds = 0, nu = 0;
-    // per buffer: kind of its last use (0 none, 1 pass 1, 2 pass 2) and the
-    // completions of s_read / s_free waited so far (scalars: no local memory)
+  } else if (warp >= 1 && warp <= 3) {
+    // ---- MMA issuers, one per product so that no thread's issue rate bounds
+    // a tile: warp 1 S = Q K^T (and TMEM owner), warp 2 dP = dO V^T, warp 3
+    // dQ += dS K.  Pass 2 per tile j: S(j) once its buffer is free (S runs
+    // ahead by the two buffers), dP(j) once dP(j-1) has been read, dQ(j) once
+    // dS(j) is written.  K(j) stays until dQ(j).  Every role walks the same
+    // unit sequence and counts K tiles and S products the same way.
+    uint32_t nq = 0, kn = 0, sn = 0, vn = 0, nds = 0, nu = 0;
+    // warp 1: per S buffer, the kind of its last use (0 none, 1 pass 1, 2
+    // pass 2) and the completions of s_read / s_free waited so far
     uint32_t used0 = 0, used1 = 0, reads0 = 0, reads1 = 0, frees0 = 0, frees1 = 0;
-    Ring kr, vr;
     const uint32_t q_base = smem_u32(s.q), go_base = smem_u32(s.go);
-    // S = Q K^T into the next buffer; kind 1 (pass 1) or 2 (pass 2)
-    auto issue_s = [&](int kslot, uint32_t kind) -> bool {
-      const int b = static_cast<int>(sc & 1u);
+    auto issue_s = [&](int kslot, uint32_t kind, bool last_q) -> bool {
+      const int b = static_cast<int>(sn & 1u);
       const uint32_t last = b ? used1 : used0;
       if (last == 1) {
         if (!wwait(&s.s_read[b], (b ? reads1 : reads0) & 1u, s.abort, p.timeout_ns)) return false;
@@ -380,72 +384,60 @@ __global__ void __launch_bounds__(ABWD_THREADS, 1)
         mma_rows_dot(tmem + TQ_S + 128u * b, q_base, smem_u32(s.k + kslot * TILE));
         mma_commit(&s.s_full[b]);
         if (kind == 1) mma_commit(&s.k_empty[kslot]);
+        if (last_q) mma_commit(s.q_empty);  // last reader of Q
       }
       __syncwarp();
-      ++sc;
-      return true;
-    };
-    auto issue_dp = [&](bool last) -> bool {
-      const int vs = vr.slot(DQ_V_STAGES);
-      if (!wwait(&s.v_full[vs], vr.parity(DQ_V_STAGES), s.abort, p.timeout_ns)) return false;
-      tc_fence_after();
-      if (elect_one()) {
-        mma_rows_dot(tmem + TQ_DP, go_base, smem_u32(s.v + vs * TILE));
-        mma_commit(s.dp_full);
-        mma_commit(&s.v_empty[vs]);
-        if (last) mma_commit(s.do_empty);  // last reader of dO
-      }
-      __syncwarp();
-      ++vr.n;
+      ++sn;
       return true;
     };
     for (int unit = blockIdx.x; unit < n_units; unit += gridDim.x) {
       const QUnit x = dq_unit(p, unit);
       if (!x.ok || x.ntiles == 0) continue;
       const int n = x.ntiles;
-      if (!wwait(s.q_full, nq & 1u, s.abort, p.timeout_ns)) goto done;
-      for (int jt = 0; jt < (p.lse_in ? 0 : n); ++jt) {  // pass 1: S only
-        const int ks = kr.slot(DQ_K_STAGES);
-        if (!wwait(&s.k_full[ks], kr.parity(DQ_K_STAGES), s.abort, p.timeout_ns)) goto done;
-        if (!issue_s(ks, 1)) goto done;
-        ++kr.n;
-      }
-      // pass 2: S(0), dP(0); then per tile S(j+1), dQ += dS(j) K(j), dP(j+1)
-      if (!wwait(s.do_full, nq & 1u, s.abort, p.timeout_ns)) goto done;
-      int kslot = kr.slot(DQ_K_STAGES);
-      if (!wwait(&s.k_full[kslot], kr.parity(DQ_K_STAGES), s.abort, p.timeout_ns)) goto done;
-      uint32_t b_cur = sc & 1u;
-      if (!issue_s(kslot, 2)) goto done;
-      ++kr.n;
-      if (n == 1 && elect_one()) mma_commit(s.q_empty);
-      __syncwarp();
-      if (!issue_dp(n == 1)) goto done;
-      for (int jt = 0; jt < n; ++jt) {
-        int knext = -1;
-        uint32_t b_next = 0;
-        if (jt + 1 < n) {
-          knext = kr.slot(DQ_K_STAGES);
-          if (!wwait(&s.k_full[knext], kr.parity(DQ_K_STAGES), s.abort, p.timeout_ns)) goto done;
-          b_next = sc & 1u;
-          if (!issue_s(knext, 2)) goto done;
-          ++kr.n;
-          if (jt + 2 == n && elect_one()) mma_commit(s.q_empty);  // last reader of Q
+      const int n1 = p.lse_in ? 0 : n;  // pass-1 tiles
+      if (warp == 1) {
+        if (!wwait(s.q_full, nq & 1u, s.abort, p.timeout_ns)) goto done;
+        for (int j = 0; j < n1 + n; ++j) {  // pass 1 (S only), then pass 2
+          const int ks = static_cast<int>(kn % DQ_K_STAGES);
+          if (!wwait(&s.k_full[ks], (kn / DQ_K_STAGES) & 1u, s.abort, p.timeout_ns)) goto done;
+          if (!issue_s(ks, j < n1 ? 1u : 2u, j + 1 == n1 + n)) goto done;
+          ++kn;
+        }
+      } else if (warp == 2) {
+        if (!wwait(s.do_full, nq & 1u, s.abort, p.timeout_ns)) goto done;
+        for (int j = 0; j < n; ++j) {
+          const int vs = static_cast<int>(vn % DQ_V_STAGES);
+          if (!wwait(&s.v_full[vs], (vn / DQ_V_STAGES) & 1u, s.abort, p.timeout_ns)) goto done;
+          if (vn > 0 && !wwait(s.dp_read, (vn - 1) & 1u, s.abort, p.timeout_ns)) goto done;
+          tc_fence_after();
+          if (elect_one()) {
+            mma_rows_dot(tmem + TQ_DP, go_base, smem_u32(s.v + vs * TILE));
+            mma_commit(s.dp_full);
+            mma_commit(&s.v_empty[vs]);
+            if (j + 1 == n) mma_commit(s.do_empty);  // last reader of dO
+          }
+          __syncwarp();
+          ++vn;
+        }
+      } else {
+        const uint32_t k0 = kn + n1, s0 = sn + n1;  // this unit's pass-2 K tiles and S products
+        for (int j = 0; j < n; ++j) {
+          if (!wwait(s.ds_ready, nds & 1u, s.abort, p.timeout_ns)) goto done;
+          ++nds;
+          if (j == 0 && nu > 0 && !wwait(s.dq_free, (nu - 1) & 1u, s.abort, p.timeout_ns)) goto done;
+          const uint32_t b = (s0 + j) & 1u;
+          const int ks = static_cast<int>((k0 + j) % DQ_K_STAGES);
+          tc_fence_after();
+          if (elect_one()) {
+            mma_inplace_by_tile(tmem + TQ_DQ, tmem + TQ_S + 128u * b, smem_u32(s.k + ks * TILE), j > 0);
+            mma_commit(&s.s_free[b]);
+            mma_commit(&s.k_empty[ks]);
+            if (j + 1 == n) mma_commit(s.dq_full);
+          }
           __syncwarp();
         }
-        if (!wwait(s.ds_ready, nds & 1u, s.abort, p.timeout_ns)) goto done;
-        ++nds;
-        if (jt == 0 && nu > 0 && !wwait(s.dq_free, (nu - 1) & 1u, s.abort, p.timeout_ns)) goto done;
-        tc_fence_after();
-        if (elect_one()) {
-          mma_inplace_by_tile(tmem + TQ_DQ, tmem + TQ_S + 128u * b_cur, smem_u32(s.k + kslot * TILE), jt > 0);
-          mma_commit(&s.s_free[b_cur]);
-          mma_commit(&s.k_empty[kslot]);
-          if (jt + 1 == n) mma_commit(s.dq_full);
-        }
-        __syncwarp();
-        if (jt + 1 < n && !issue_dp(jt + 2 == n)) goto done;
-        kslot = knext;
-        b_cur = b_next;
+        kn += n1 + n;
+        sn += n1 + n;
       }
       ++nq;
       ++nu;
@@ -471,10 +463,6 @@ __global__ void __launch_bounds__(ABWD_THREADS, 1)
           uint4* dq_row = reinterpret_cast<uint4*>(p.dQ + row * 128 + col0);
 #pragma unroll
           for (int c = 0; c < 8; ++c) dq_row[c] = make_uint4(0, 0, 0, 0);
-          if (grp == 0) {
-            p.lse[row] = INFINITY;
-            p.Drow[row] = 0.f;
-          }
         }
         continue;
       }
@@ -544,9 +532,9 @@ __global__ void __launch_bounds__(ABWD_THREADS, 1)
         }
         lse2 = l > 0.f ? m + __log2f(l) : INFINITY;
       }
-      if (valid && grp == 0) {
-        p.lse[row] = lse2;
-        p.Drow[row] = D;
+      if (grp == 0) {  // the unit's 128 tile rows, in tile order, for the dK/dV kernel
+        p.lse[static_cast<size_t>(unit) * 128 + r] = valid ? lse2 : INFINITY;
+        p.Drow[static_cast<size_t>(unit) * 128 + r] = valid ? D : 0.f;
       }
       // pass 2: P = 2^(s sl - lse), dS = P (dP - D) scale written over S
       for (int jt = 0; jt < x.ntiles; ++jt) {
@@ -572,16 +560,23 @@ __global__ void __launch_bounds__(ABWD_THREADS, 1)
         if (!wwait(s.dp_full, ndp & 1u, s.abort, p.timeout_ns)) goto done;
         ++ndp;
         tc_fence_after();
+        {
+          uint32_t dv[2][32];
+          tmem_ld32(tmem + lane_base + TQ_DP + col0, dv[0]);
+          tmem_ld32(tmem + lane_base + TQ_DP + col0 + 32, dv[1]);
+          tmem_ld_wait(dv[0]);
+          tmem_ld_wait(dv[1]);
+          tc_fence_before();
+          mbar_arrive(s.dp_read);  // the next dP may land
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          uint32_t dv[32], pk[16];
-          tmem_ld32(tmem + lane_base + TQ_DP + col0 + 32 * c, dv);
-          tmem_ld_wait(dv);
+          for (int c = 0; c < 2; ++c) {
+            uint32_t pk[16];
 #pragma unroll
-          for (int j = 0; j < 16; ++j)
-            pk[j] = pack_bf16x2(pf[c * 32 + 2 * j] * (__uint_as_float(dv[2 * j]) - D) * p.scale,
-                                pf[c * 32 + 2 * j + 1] * (__uint_as_float(dv[2 * j + 1]) - D) * p.scale);
-          tmem_st16(tmem + lane_base + TQ_S + 128u * b + col0 + 16 * c, pk);
+            for (int j = 0; j < 16; ++j)
+              pk[j] = pack_bf16x2(pf[c * 32 + 2 * j] * (__uint_as_float(dv[c][2 * j]) - D) * p.scale,
+                                  pf[c * 32 + 2 * j + 1] * (__uint_as_float(dv[c][2 * j + 1]) - D) * p.scale);
+            tmem_st16(tmem + lane_base + TQ_S + 128u * b + col0 + 16 * c, pk);
+          }
         }
         tmem_st_wait();
         tc_fence_before();
@@ -614,7 +609,10 @@ done:
 
 // ============================================================= dK/dV kernel
 // TMEM columns: S^T [0,128) (P^T written over it), dP^T [128,256) (dS^T
-// written over it), dV [256,384), dK [384,512).
+// written over it), dV [256,384), dK [384,512).  Shared memory holds K, V
+// and two query-tile stages; P^T stays in TMEM (a P^T tile in shared memory
+// leaves room for only two stages, and the copy latency of the next tiles
+// then bounds every tile: measured slower).
 constexpr uint32_t TK_ST = 0, TK_DPT = 128, TK_DV = 256, TK_DK = 384;
 
 struct KvSmem {
@@ -641,7 +639,7 @@ struct KvSmem {
 };
 constexpr uint32_t KV_TILES = 6 * TILE;
 constexpr uint32_t KV_BARS = 14;
-constexpr uint32_t KV_SMEM_USED = KV_TILES + 4 * 2 * 128 * 4 + 8 * KV_BARS + 8;
+constexpr uint32_t KV_SMEM_USED = KV_TILES + 2 * 2 * 128 * 4 + 8 * KV_BARS + 8;
 constexpr uint32_t KV_SMEM = KV_SMEM_USED + 1024;
 
 __device__ __forceinline__ KvSmem kv_carve(uint8_t* base) {
@@ -752,7 +750,7 @@ __global__ void __launch_bounds__(ABWD_THREADS, 1)
 
   if (warp == 0) {
     // ---- TMA: the key block's K and V, then per query tile Q, dO (TMA) and
-    // the rows' LSE and D (plain loads by the warp's lanes)
+    // the rows' LSE and D (two bulk copies)
     uint32_t ni = 0, tq = 0;
     for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
       const KvItem x = kv_item(p, item);
@@ -765,44 +763,30 @@ __global__ void __launch_bounds__(ABWD_THREADS, 1)
         load_kv(p, &tmV, s.v, s.kv_full, x.u, x.h, x.k.kv0, x.kb * 128);
       }
       __syncwarp();
+      // the user's query tiles are work units ubase .. ubase + ntq - 1 of the
+      // work list (user-major, then head, then chunk): the dQ kernel left
+      // their rows' LSE and D there, 128 per unit, in tile order
+      const size_t ubase =
+          static_cast<size_t>(p.H) * __ldg(p.tile_prefix + x.u) + static_cast<size_t>(x.h) * x.ntq;
+      const int lane = static_cast<int>(lane_id());
+      // lane j < n holds the tile's j-th candidate, loaded one tile ahead
+      int mine = lane < min(cpt, x.count) ? __ldg(p.perm + x.seg0 + lane) : p.n_cand;
       for (int t = 0; t < x.ntq; ++t, ++tq) {
         const int b = static_cast<int>(tq & 1u);
-        if (!wwait(&s.q_empty[b], ((tq >> 1) & 1u) ^ 1u, s.abort, p.timeout_ns)) goto done;
-        // lane j < n holds the tile's j-th candidate; the copies go out first,
-        // the rows' LSE and D (independent loads, 4 rows per lane) after them
-        const int first = t * cpt, n = min(cpt, x.count - first);
-        const int lane = static_cast<int>(lane_id());
-        const int mine = lane < n ? __ldg(p.perm + x.seg0 + first + lane) : p.n_cand;
         int cand[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) cand[j] = __shfl_sync(0xffffffffu, mine, j);
+        if (!wwait(&s.q_empty[b], ((tq >> 1) & 1u) ^ 1u, s.abort, p.timeout_ns)) goto done;
         if (elect_one()) {
-          mbar_expect_tx(&s.q_full[b], 2u * static_cast<uint32_t>(rows) * 256u);
+          mbar_arrive_expect_tx(&s.q_full[b], 2u * static_cast<uint32_t>(rows) * 256u + 2u * 512u);
           load_qtile(p, &tmQ, s.q + b * TILE, &s.q_full[b], x.h, cand);
           load_qtile(p, &tmDO, s.go + b * TILE, &s.q_full[b], x.h, cand);
+          bulk_load(s.lse + b * 128, p.lse + (ubase + t) * 128, 512u, &s.q_full[b]);
+          bulk_load(s.drow + b * 128, p.Drow + (ubase + t) * 128, 512u, &s.q_full[b]);
         }
         __syncwarp();
-        float lv[4], dr[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int r = lane + 32 * k, slot = r / p.Lq, q = r - slot * p.Lq;
-          const int c = __shfl_sync(0xffffffffu, mine, slot & 31);
-          lv[k] = INFINITY;  // rows without a query: P = 0
-          dr[k] = 0.f;
-          if (r < rows && slot < n) {
-            const size_t row = (static_cast<size_t>(c) * p.H + x.h) * p.Lq + q;
-            lv[k] = p.lse[row];
-            dr[k] = p.Drow[row];
-          }
-        }
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          s.lse[b * 128 + lane + 32 * k] = lv[k];
-          s.drow[b * 128 + lane + 32 * k] = dr[k];
-        }
-        __syncwarp();
-        if (elect_one()) mbar_arrive(&s.q_full[b]);
-        __syncwarp();
+        const int nf = (t + 1) * cpt, nn = min(cpt, x.count - nf);
+        mine = (t + 1 < x.ntq && lane < nn) ? __ldg(p.perm + x.seg0 + nf + lane) : p.n_cand;
       }
     }
   } else if (warp == 1 || warp == 2) {
@@ -871,7 +855,7 @@ __global__ void __launch_bounds__(ABWD_THREADS, 1)
       }
       for (int t = 0; t < x.ntq; ++t, ++tq) {
         const int b = static_cast<int>(tq & 1u);
-        // the producer's lanes stored this tile's LSE and D before arriving on q_full[b]
+        // q_full[b] also covers this tile's LSE and D (bulk copies)
         if (!wwait(&s.q_full[b], (tq >> 1) & 1u, s.abort, p.timeout_ns)) goto done;
         if (!wwait(s.s_full, tq & 1u, s.abort, p.timeout_ns)) goto done;
         tc_fence_after();
@@ -967,33 +951,51 @@ done:
   }
 }
 
-// blk_prefix[u] = sum over users v < u of ceil(L_v / 128); one CTA, a scan
-// over chunks of users.
-__global__ void __launch_bounds__(1024) attn_bwd_blocks_kernel(const int32_t* kv_offsets, int n_users, int Lkv,
-                                                               int32_t* blk_prefix) {
-  __shared__ int32_t part[1024];
+// blk_prefix[u] = sum over users v < u of ceil(L_v / 128) (key blocks) and
+// tile_prefix[u] = sum over v < u of ceil(count_v / cpt) (query tiles); one
+// CTA, a scan over chunks of users.
+__device__ __forceinline__ int user_blocks(const int32_t* kv_offsets, int Lkv, int u) {
+  const int L = kv_offsets ? max(0, kv_offsets[u + 1] - kv_offsets[u]) : Lkv;
+  return (L + 127) / 128;
+}
+__device__ __forceinline__ int user_tiles(const int32_t* offsets, int cpt, int u) {
+  return (max(0, offsets[u + 1] - offsets[u]) + cpt - 1) / cpt;
+}
+
+__global__ void __launch_bounds__(1024) attn_bwd_blocks_kernel(const int32_t* kv_offsets, const int32_t* offsets,
+                                                               int n_users, int Lkv, int cpt, int32_t* blk_prefix,
+                                                               int32_t* tile_prefix) {
+  __shared__ int32_t part[2][1024];
   const int per = (n_users + 1023) / 1024;
   const int u0 = threadIdx.x * per;
-  int32_t sum = 0;
+  int32_t sb = 0, st = 0;
   for (int u = u0; u < min(u0 + per, n_users); ++u) {
-    const int L = kv_offsets ? max(0, kv_offsets[u + 1] - kv_offsets[u]) : Lkv;
-    sum += (L + 127) / 128;
+    sb += user_blocks(kv_offsets, Lkv, u);
+    st += user_tiles(offsets, cpt, u);
   }
-  part[threadIdx.x] = sum;
+  part[0][threadIdx.x] = sb;
+  part[1][threadIdx.x] = st;
   __syncthreads();
-  for (int w = 1; w < 1024; w <<= 1) {  // inclusive scan of the chunk sums
-    const int32_t v = threadIdx.x >= w ? part[threadIdx.x - w] : 0;
+  for (int w = 1; w < 1024; w <<= 1) {  // inclusive scans of the chunk sums
+    const int32_t vb = threadIdx.x >= w ? part[0][threadIdx.x - w] : 0;
+    const int32_t vt = threadIdx.x >= w ? part[1][threadIdx.x - w] : 0;
     __syncthreads();
-    part[threadIdx.x] += v;
+    part[0][threadIdx.x] += vb;
+    part[1][threadIdx.x] += vt;
     __syncthreads();
   }
-  int32_t run = threadIdx.x > 0 ? part[threadIdx.x - 1] : 0;
+  int32_t rb = threadIdx.x > 0 ? part[0][threadIdx.x - 1] : 0;
+  int32_t rt = threadIdx.x > 0 ? part[1][threadIdx.x - 1] : 0;
   for (int u = u0; u < min(u0 + per, n_users); ++u) {
-    blk_prefix[u] = run;
-    const int L = kv_offsets ? max(0, kv_offsets[u + 1] - kv_offsets[u]) : Lkv;
-    run += (L + 127) / 128;
+    blk_prefix[u] = rb;
+    tile_prefix[u] = rt;
+    rb += user_blocks(kv_offsets, Lkv, u);
+    rt += user_tiles(offsets, cpt, u);
   }
-  if (threadIdx.x == 1023) blk_prefix[n_users] = part[1023];
+  if (threadIdx.x == 1023) {
+    blk_prefix[n_users] = part[0][1023];
+    tile_prefix[n_users] = part[1][1023];
+  }
 }
 
 }  // namespace
@@ -1005,7 +1007,8 @@ cudaError_t launch_attn_backward(const CUtensorMap& tmQ, const CUtensorMap& tmDO
                                  const CUtensorMap& tmV, const AttnBwdParams& p, int grid, cudaStream_t s,
                                  int* launches) {
   *launches = 0;
-  attn_bwd_blocks_kernel<<<1, 1024, 0, s>>>(p.kv_offsets, p.n_users, p.Lkv, const_cast<int32_t*>(p.blk_prefix));
+  attn_bwd_blocks_kernel<<<1, 1024, 0, s>>>(p.kv_offsets, p.offsets, p.n_users, p.Lkv, p.cands_per_tile,
+                                            const_cast<int32_t*>(p.blk_prefix), const_cast<int32_t*>(p.tile_prefix));
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   ++*launches;

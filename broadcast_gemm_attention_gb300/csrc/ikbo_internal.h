@@ -230,13 +230,14 @@ struct AttnBwdParams {
   const int32_t* offsets;    // the plan's user segment offsets [n_users + 1]
   const int32_t* kv_offsets; // jagged K/V or null (dense)
   const int32_t* blk_prefix; // dK/dV kernel: [n_users + 1] prefix of ceil(L_u / 128)
+  const int32_t* tile_prefix;// [n_users + 1] prefix of the users' query tiles, ceil(count_u / cands_per_tile)
   const uint16_t* O;         // forward output [n_cand][H][Lq][d]
   const uint16_t* dO;        // [n_cand][H][Lq][d]
   uint16_t* dQ;              // [n_cand][H][Lq][d]
   uint16_t* dK;              // like K
   uint16_t* dV;              // like V
-  float* lse;                // [n_cand][H][Lq], log2 domain of scale * log2(e) * q.k
-  float* Drow;               // [n_cand][H][Lq]
+  float* lse;                // [work unit][128 tile rows]: log2-domain LSE (+inf for rows without a query)
+  float* Drow;               // [work unit][128 tile rows]: D = rowsum(dO * O) (0 for rows without a query)
   const float* lse_in;       // the forward's natural-log LSE [n_cand][H][Lq], or null (recomputed)
   uint32_t* status;
   int n_cand, n_users, H, Lq, Lkv, cands_per_tile;
