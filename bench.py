@@ -492,11 +492,25 @@ def run_sweep(args):
                 sched[name] = timed(lambda: p.lce_forward(U, C, Wu, Wc, b, Y, stream))
             us = sched["auto"]
             st = p.status()
+        # ablation: the same kernel fed the materialised broadcast U[map]
+        # (identity map, n_users = n_cand), and the cost of building it
+        idx = m.long()
+        U_rep = torch.empty(x.n_cand, x.K_u, x.D, dtype=torch.bfloat16, device=dev)
+        ident = torch.arange(x.n_cand, dtype=torch.int32, device=dev)
+        mat_us = timed(lambda: torch.index_select(U, 0, idx, out=U_rep))
+        with B.Plan(x.n_cand, x.n_cand, 1) as p2:
+            p2.plan(ident, x.n_cand, 1, 8, stream)
+            on_mat_us = timed(lambda: p2.lce_forward(U_rep, C, Wu, Wc, b, Y, stream))
+            st2 = p2.status()
+        del U_rep
         byt = acc.lce_bytes(x.n_cand, x.n_users, x.K_u, x.K_c, x.D, x.N)
         fl = acc.lce_flops(x.n_cand, x.n_users, x.K_u, x.K_c, x.D, x.N)
         t_roof = max(byt / (pk["hbm_gbs"] * 1e9), fl / (pk["bf16_tflops"] * 1e12))
         print(json.dumps({"sweep": "lce", "n_cand": n, "ratio": r, "n_users": x.n_users, "us": us, "schedules_us": sched,
                           "roofline_us": t_roof * 1e6, "frac": t_roof * 1e6 / us, "gbs": byt / (us * 1e-6) / 1e9,
+                          "materialised": {"build_us": mat_us, "lce_us": on_mat_us, "total_us": mat_us + on_mat_us,
+                                           "ikbo_speedup": (mat_us + on_mat_us) / us,
+                                           "status": B.ikbo_status_string(st2)},
                           "status": B.ikbo_status_string(st)}), flush=True)
         del U, C, Wu, Wc, b, m, Y
     for n, r, seed in gen.attn_ratio_sweep_points():
@@ -515,6 +529,23 @@ def run_sweep(args):
                           "bound": "hbm" if byt / (pk["hbm_gbs"] * 1e9) > fl / (pk["bf16_tflops"] * 1e12) else "tensor",
                           "status": B.ikbo_status_string(st)}), flush=True)
         del Q, K, V, m, O
+    # the stress request: Zipf(1.1) candidates per user, permuted map, jagged
+    # per-user histories packed with int32 offsets
+    x = gen.attn_stress()
+    Q, K, V, m, offs = [t.to(dev) for t in (x.Q, x.K, x.V, x.map, x.kv_offsets)]
+    O = torch.empty_like(Q)
+    with B.Plan(x.n_cand, x.n_users, x.H) as p:
+        p.plan(m, x.n_users, x.H, x.Lq, stream)
+        us = timed(lambda: p.attn_forward(Q, K, V, offs, O, None, stream))
+        st = p.status()
+    lens = (x.kv_offsets[1:] - x.kv_offsets[:-1]).long()
+    fl = acc.attn_flops(x.H, x.Lq, x.d, lens[x.map.long()].tolist())
+    byt = acc.attn_bytes(x.n_cand, x.H, x.Lq, x.d, int(x.kv_offsets[-1]))
+    t_roof = max(byt / (pk["hbm_gbs"] * 1e9), fl / (pk["bf16_tflops"] * 1e12))
+    print(json.dumps({"sweep": "attn_stress", "n_cand": x.n_cand, "n_users": x.n_users, "Lq": x.Lq,
+                      "kv_rows": int(x.kv_offsets[-1]), "us": us, "roofline_us": t_roof * 1e6,
+                      "frac": t_roof * 1e6 / us, "tflops": fl / (us * 1e-6) / 1e12,
+                      "status": B.ikbo_status_string(st)}), flush=True)
 
 
 def lce_stage_run(plan, d, Y, flush, stream, iters=20):
