@@ -57,6 +57,7 @@ __global__ void __launch_bounds__(SEG_THREADS, 1) seg_build_kernel(SegParams p) 
   int32_t* cursor = sm + p.n_users;        // [n_users]
   int32_t* ubase = sm + 2 * p.n_users;     // [n_users + 1]
   __shared__ int warp_sums[33];
+  __shared__ int wcount[SEG_THREADS / 32][SEG_FAST_USERS];  // per warp, per user (few-user scatter)
 
   const int tid = threadIdx.x;
   const int lane = tid & 31, warp = tid >> 5;
@@ -65,11 +66,15 @@ __global__ void __launch_bounds__(SEG_THREADS, 1) seg_build_kernel(SegParams p) 
   for (int u = tid; u < nu; u += SEG_THREADS) cnt[u] = 0;
   __syncthreads();
 
+  // histogram: the lanes of a warp that share a user add their count once
   bool bad = false;
-  for (int i = tid; i < p.n_cand; i += SEG_THREADS) {
-    int u = p.map[i];
-    if (u < 0 || u >= nu) bad = true;
-    else atomicAdd(&cnt[u], 1);
+  for (int base = 0; base < p.n_cand; base += SEG_THREADS) {
+    const int i = base + tid;
+    int u = i < p.n_cand ? p.map[i] : -1;
+    if (i < p.n_cand && (u < 0 || u >= nu)) bad = true;
+    if (u < 0 || u >= nu) u = -1;
+    const uint32_t peers = __match_any_sync(0xffffffffu, u);
+    if (u >= 0 && lane == __ffs(peers) - 1) atomicAdd(&cnt[u], __popc(peers));
   }
   if (bad) atomicOr(p.status, DEV_ERR_MAP_RANGE);
   __syncthreads();
@@ -104,24 +109,57 @@ __global__ void __launch_bounds__(SEG_THREADS, 1) seg_build_kernel(SegParams p) 
 
   // stable scatter into perm
   const uint32_t lt_mask = (1u << lane) - 1u;
-  for (int base = 0; base < p.n_cand; base += SEG_THREADS) {
-    const int i = base + tid;
-    int u = (i < p.n_cand) ? p.map[i] : -1;
-    if (u < 0 || u >= nu) u = -1;
-    const uint32_t peers = __match_any_sync(0xffffffffu, u);
-    const int rank = __popc(peers & lt_mask);
-    const int leader = __ffs(peers) - 1;
-    for (int w = 0; w < SEG_THREADS / 32; ++w) {
-      if (warp == w) {
-        int pos = 0;
-        if (u >= 0 && lane == leader) {
-          pos = cursor[u];
-          cursor[u] = pos + __popc(peers);
+  if (nu <= SEG_FAST_USERS) {
+    // few users: each candidate's place among the block's earlier candidates
+    // of its user = (its user's count in the earlier warps) + (its rank in
+    // its warp); the per-warp counts [warp][user] are scanned over the warps
+    // by one warp per user, so no warp waits for another
+    for (int base = 0; base < p.n_cand; base += SEG_THREADS) {
+      const int i = base + tid;
+      int u = (i < p.n_cand) ? p.map[i] : -1;
+      if (u < 0 || u >= nu) u = -1;
+      const uint32_t peers = __match_any_sync(0xffffffffu, u);
+      const int rank = __popc(peers & lt_mask);
+      wcount[warp][lane] = 0;
+      __syncwarp();
+      if (u >= 0 && lane == __ffs(peers) - 1) wcount[warp][u] = __popc(peers);
+      __syncthreads();
+      if (warp < nu) {  // warp w scans user w's counts over the 32 warps (lane = warp index)
+        const int c = wcount[lane][warp];
+        int incl = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
         }
-        pos = __shfl_sync(0xffffffffu, pos, leader);
-        if (u >= 0) p.perm[pos + rank] = i;
+        wcount[lane][warp] = cursor[warp] + incl - c;  // where this warp's run of the user starts
+        __syncwarp();
+        if (lane == 31) cursor[warp] += incl;
       }
       __syncthreads();
+      if (u >= 0) p.perm[wcount[warp][u] + rank] = i;
+      __syncthreads();  // wcount is rewritten by the next block of candidates
+    }
+  } else {
+    for (int base = 0; base < p.n_cand; base += SEG_THREADS) {
+      const int i = base + tid;
+      int u = (i < p.n_cand) ? p.map[i] : -1;
+      if (u < 0 || u >= nu) u = -1;
+      const uint32_t peers = __match_any_sync(0xffffffffu, u);
+      const int rank = __popc(peers & lt_mask);
+      const int leader = __ffs(peers) - 1;
+      for (int w = 0; w < SEG_THREADS / 32; ++w) {
+        if (warp == w) {
+          int pos = 0;
+          if (u >= 0 && lane == leader) {
+            pos = cursor[u];
+            cursor[u] = pos + __popc(peers);
+          }
+          pos = __shfl_sync(0xffffffffu, pos, leader);
+          if (u >= 0) p.perm[pos + rank] = i;
+        }
+        __syncthreads();
+      }
     }
   }
 

@@ -21,6 +21,9 @@ def _maps():
     yield "one_candidate", np.array([3], np.int32), 4
     yield "identity_4096", np.arange(4096, dtype=np.int32), 4096
     yield "many_users", rng.integers(0, 5000, size=2049).astype(np.int32), 5000
+    # the few-user scatter's limit (32 users, several blocks of 1024) and one past it
+    yield "users_32_blocks", gen.permuted_multinomial_map(rng, 3000, 32), 32
+    yield "users_33_blocks", gen.permuted_multinomial_map(rng, 3000, 33), 33
 
 
 @pytest.mark.parametrize("name,m,n_users", list(_maps()), ids=[x[0] for x in _maps()])
