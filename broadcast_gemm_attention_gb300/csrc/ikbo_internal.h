@@ -27,7 +27,6 @@ enum : uint32_t {
 // ------------------------------------------------------------ segments
 constexpr int SEG_THREADS = 1024;
 constexpr int SEG_MAX_USERS = 8192;
-constexpr int SEG_FAST_USERS = 32;  // up to this many users the stable scatter runs all warps at once
 
 struct SegParams {
   const int32_t* map;

@@ -21,6 +21,8 @@
 
 namespace ikbo {
 
+constexpr int SEG_FAST_USERS = 32;  // up to this many users the stable scatter runs all warps at once
+
 // Exclusive scan over the 1024 threads of the block; returns the prefix and
 // writes the block total to *total.
 __device__ int block_exclusive_scan(int v, int* warp_sums, int* total) {
