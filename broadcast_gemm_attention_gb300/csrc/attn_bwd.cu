@@ -501,20 +501,25 @@ __global__ void __launch_bounds__(ABWD_THREADS, 1)
           tmem_ld_wait(v[1]);
           tc_fence_before();
           mbar_arrive(&s.s_read[b]);
+          if (kcol + 64 > x.k.L) {  // a partial tile: columns past the keys take no part
+#pragma unroll
+            for (int c = 0; c < 2; ++c)
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                if (kcol + c * 32 + j >= x.k.L) v[c][j] = __float_as_uint(-INFINITY);
+          }
           float mx = -INFINITY;
 #pragma unroll
           for (int c = 0; c < 2; ++c)
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (kcol + c * 32 + j < x.k.L) mx = fmaxf(mx, __uint_as_float(v[c][j]) * sl);
+            for (int j = 0; j < 32; ++j) mx = fmaxf(mx, __uint_as_float(v[c][j]) * sl);
           const float m_new = fmaxf(m, mx);
           if (m_new == -INFINITY) continue;
           float add = 0.f;
 #pragma unroll
           for (int c = 0; c < 2; ++c)
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (kcol + c * 32 + j < x.k.L) add += ex2(fmaf(__uint_as_float(v[c][j]), sl, -m_new));
+            for (int j = 0; j < 32; ++j) add += ex2(fmaf(__uint_as_float(v[c][j]), sl, -m_new));
           l = l * ex2(m - m_new) + add;
           m = m_new;
         }
@@ -550,12 +555,19 @@ __global__ void __launch_bounds__(ABWD_THREADS, 1)
           tmem_ld32(tmem + lane_base + TQ_S + 128u * b + col0 + 32, v[1]);
           tmem_ld_wait(v[0]);
           tmem_ld_wait(v[1]);
+          if (kcol + 64 <= x.k.L) {  // every column of this half is a key (the common case)
 #pragma unroll
-          for (int c = 0; c < 2; ++c)
+            for (int c = 0; c < 2; ++c)
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
-              pf[c * 32 + j] =
-                  kcol + c * 32 + j < x.k.L ? ex2(fmaf(__uint_as_float(v[c][j]), sl, -lse2)) : 0.f;
+              for (int j = 0; j < 32; ++j) pf[c * 32 + j] = ex2(fmaf(__uint_as_float(v[c][j]), sl, -lse2));
+          } else {
+#pragma unroll
+            for (int c = 0; c < 2; ++c)
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                pf[c * 32 + j] =
+                    kcol + c * 32 + j < x.k.L ? ex2(fmaf(__uint_as_float(v[c][j]), sl, -lse2)) : 0.f;
+          }
         }
         if (!wwait(s.dp_full, ndp & 1u, s.abort, p.timeout_ns)) goto done;
         ++ndp;
@@ -869,6 +881,9 @@ __global__ void __launch_bounds__(ABWD_THREADS, 1)
           tmem_ld32(tmem + lane_base + TK_ST + col0 + 32, v[1]);
           tmem_ld_wait(v[0]);
           tmem_ld_wait(v[1]);
+          // every row of the warp a key (all but a user's last, partial block):
+          // no per-element select
+          const bool all_keys = __all_sync(0xffffffffu, kvalid);
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
             uint32_t pk[16];
@@ -877,10 +892,11 @@ __global__ void __launch_bounds__(ABWD_THREADS, 1)
               const float4 l4 = *reinterpret_cast<const float4*>(lse + c * 32 + 4 * j4);
               const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const int j = 4 * j4 + e;
-                pf[c * 32 + j] = kvalid ? ex2(fmaf(__uint_as_float(v[c][j]), sl, -lv[e])) : 0.f;
-              }
+              for (int e = 0; e < 4; ++e) pf[c * 32 + 4 * j4 + e] = ex2(fmaf(__uint_as_float(v[c][4 * j4 + e]), sl, -lv[e]));
+            }
+            if (!all_keys && !kvalid) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) pf[c * 32 + j] = 0.f;
             }
 #pragma unroll
             for (int j = 0; j < 16; ++j) pk[j] = pack_bf16x2(pf[c * 32 + 2 * j], pf[c * 32 + 2 * j + 1]);
