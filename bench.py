@@ -365,34 +365,7 @@ def run_gpu(args):
     # ---------------- end to end through the C ABI with host buffers
     e2e = None
     if not args.no_e2e:
-        h_in = {k: v.cpu().pin_memory() for k, v in d.items()}
-        hY = torch.empty(Y.shape, dtype=Y.dtype).pin_memory()
-        hO = torch.empty(O.shape, dtype=O.dtype).pin_memory()
-        h2d = sum(t.numel() * t.element_size() for t in h_in.values())
-        d2h = hY.numel() * 2 + hO.numel() * 2
-        n_e2e = max(3, min(args.e2e_steps, K))
-        e_s = torch.cuda.Event(enable_timing=True)
-        e_e = torch.cuda.Event(enable_timing=True)
-
-        def e2e_step():
-            for k, t in h_in.items():
-                d[k].copy_(t, non_blocking=True)
-            step()
-            hY.copy_(Y, non_blocking=True)
-            hO.copy_(O, non_blocking=True)
-
-        e2e_step()
-        torch.cuda.synchronize()
-        e_s.record(stream)
-        for _ in range(n_e2e):
-            e2e_step()
-        e_e.record(stream)
-        torch.cuda.synchronize()
-        e2e_ms = max_over_ranks(e_s.elapsed_time(e_e) / n_e2e, dist, dev)
-        e2e = {"value": world * step_flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "steps": n_e2e,
-               "path": "pinned host -> device copies, ikbo_plan + ikbo_lce_forward + ikbo_attn_forward, "
-                       "device -> pinned host copies of Y and O, one stream"}
+        e2e = e2e_run(plan, d, Y, O, x, a, step_flops, args, K, world, dist, dev)
 
     # ---------------- ablation: our kernels fed a materialised broadcast
     ablation = None
@@ -546,6 +519,69 @@ def run_sweep(args):
                       "kv_rows": int(x.kv_offsets[-1]), "us": us, "roofline_us": t_roof * 1e6,
                       "frac": t_roof * 1e6 / us, "tflops": fl / (us * 1e-6) / 1e12,
                       "status": B.ikbo_status_string(st)}), flush=True)
+
+
+def e2e_run(plan, d, Y, O, x, a, step_flops, args, K, world, dist, dev):
+    """End to end through the C ABI from pinned host memory, the way a server
+    would run consecutive requests: request k's inputs go host -> device on a
+    copy stream while request k-1 computes and request k-2's Y and O come back
+    device -> host on a third stream (two device buffer sets; events order
+    each request's copy-in, compute and copy-out).  Every request's copies
+    are inside the timed region; ms per request = total time / requests."""
+    import torch
+    h_in = {k: v.cpu().pin_memory() for k, v in d.items()}
+    h2d = sum(t.numel() * t.element_size() for t in h_in.values())
+    d2h = Y.numel() * 2 + O.numel() * 2
+    dbuf = [d, {k: torch.empty_like(v) for k, v in d.items()}]
+    ybuf, obuf = [Y, torch.empty_like(Y)], [O, torch.empty_like(O)]
+    hy = [torch.empty(Y.shape, dtype=Y.dtype).pin_memory() for _ in range(2)]
+    ho = [torch.empty(O.shape, dtype=O.dtype).pin_memory() for _ in range(2)]
+    s_in, s_comp, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev = lambda: torch.cuda.Event()  # noqa: E731
+    in_done, comp_done, out_done = [ev(), ev()], [ev(), ev()], [ev(), ev()]
+    n_e2e = max(3, min(args.e2e_steps, K))
+
+    def request(k):
+        b = k % 2
+        di, yb, ob = dbuf[b], ybuf[b], obuf[b]
+        if k >= 2:
+            s_in.wait_event(comp_done[b])  # request k-2 has finished reading this buffer set
+        for name, t in h_in.items():
+            with torch.cuda.stream(s_in):
+                di[name].copy_(t, non_blocking=True)
+        in_done[b].record(s_in)
+        s_comp.wait_event(in_done[b])
+        if k >= 2:
+            s_comp.wait_event(out_done[b])  # request k-2's Y and O have left this buffer set
+        plan.plan(di["map"], x.n_users, a.H, a.Lq, s_comp)
+        plan.lce_forward(di["U"], di["C"], di["Wu"], di["Wc"], di["b"], yb, s_comp)
+        plan.attn_forward(di["Q"], di["K"], di["V"], None, ob, None, s_comp)
+        comp_done[b].record(s_comp)
+        s_out.wait_event(comp_done[b])
+        with torch.cuda.stream(s_out):
+            hy[b].copy_(yb, non_blocking=True)
+            ho[b].copy_(ob, non_blocking=True)
+        out_done[b].record(s_out)
+
+    for k in range(2):  # warm-up: both buffer sets once
+        request(k)
+    torch.cuda.synchronize()
+    e_s, e_e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e_s.record(s_in)
+    for st in (s_comp, s_out):
+        st.wait_event(e_s)
+    for k in range(n_e2e):
+        request(k)
+    s_in.wait_stream(s_out)
+    e_e.record(s_in)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e_s.elapsed_time(e_e) / n_e2e, dist, dev)
+    st = plan.status()
+    return {"value": world * step_flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "steps": n_e2e, "status": "ok" if st == 0 else st,
+            "path": "pinned host -> device copies of every input, ikbo_plan + ikbo_lce_forward + ikbo_attn_forward, "
+                    "device -> pinned host copies of Y and O; copy-in, compute and copy-out of consecutive requests "
+                    "overlap on three streams (two device buffer sets)"}
 
 
 def lce_stage_run(plan, d, Y, flush, stream, iters=20):
