@@ -20,7 +20,8 @@
 //                         dP and dS (written over S in TMEM) and accumulates
 //                         dQ += dS K.  Stores LSE and D for the next kernel.
 //   attn_bwd_dkdv_kernel  per (user, head, 128-key block), keys on TMEM lanes:
-//                         for every query tile of the user's candidates
+//                         for every query tile of the user's candidates, in
+//                         two 64-query halves on alternating TMEM buffers,
 //                         S^T = K Q^T, dP^T = V dO^T, then P^T and dS^T are
 //                         written over them in TMEM and dV += P^T dO,
 //                         dK += dS^T Q accumulate in TMEM -- the sum over a
@@ -620,12 +621,14 @@ done:
 }
 
 // ============================================================= dK/dV kernel
-// TMEM columns: S^T [0,128) (P^T written over it), dP^T [128,256) (dS^T
-// written over it), dV [256,384), dK [384,512).  Shared memory holds K, V
-// and two query-tile stages; P^T stays in TMEM (a P^T tile in shared memory
-// leaves room for only two stages, and the copy latency of the next tiles
-// then bounds every tile: measured slower).
-constexpr uint32_t TK_ST = 0, TK_DPT = 128, TK_DV = 256, TK_DK = 384;
+// Each 128-query tile is processed as two 64-query halves.  TMEM columns:
+// two half-tile buffers X0 [0,128), X1 [128,256), each S^T [X, X+64) and dP^T
+// [X+64, X+128) of one half (P^T and dS^T written over them as bf16 pairs),
+// then dV [256,384), dK [384,512).  Halves alternate between the buffers, so
+// S^T of half g+2 waits for dV of half g instead of dV of the half just
+// before it, and the products, the element-wise work and the next halves'
+// loads overlap.  Shared memory holds K, V and two query-tile stages.
+constexpr uint32_t TK_X = 0, TK_DV = 256, TK_DK = 384;
 
 struct KvSmem {
   uint8_t* k;      // 32 KB, the key block
@@ -636,21 +639,21 @@ struct KvSmem {
   float* drow;     // [2][128]
   uint64_t* kv_full;
   uint64_t* kv_empty;
-  uint64_t* q_full;    // [2]
+  uint64_t* q_full;    // [2] per query-tile stage
   uint64_t* q_empty;   // [2]
-  uint64_t* s_full;    // S^T computed
-  uint64_t* dp_full;   // dP^T computed
-  uint64_t* p_ready;   // P^T written (S^T read)
-  uint64_t* ds_ready;  // dS^T written (dP^T read)
-  uint64_t* dv_done;   // dV += P^T dO completed (P^T read)
-  uint64_t* dk_done;   // dK += dS^T Q completed (dS^T read)
+  uint64_t* s_full;    // [2] per half-tile buffer: S^T computed
+  uint64_t* dp_full;   // [2] dP^T computed
+  uint64_t* p_ready;   // [2] P^T written (S^T read)
+  uint64_t* ds_ready;  // [2] dS^T written (dP^T read)
+  uint64_t* xa_free;   // [2] dV has read the buffer's P^T (S^T may land)
+  uint64_t* xb_free;   // [2] dK has read the buffer's dS^T (dP^T may land)
   uint64_t* acc_full;  // the block's dV, dK complete
   uint64_t* acc_free;  // ... and read out
   uint32_t* tmem_slot;
   uint32_t* abort;
 };
 constexpr uint32_t KV_TILES = 6 * TILE;
-constexpr uint32_t KV_BARS = 14;
+constexpr uint32_t KV_BARS = 20;
 constexpr uint32_t KV_SMEM_USED = KV_TILES + 2 * 2 * 128 * 4 + 8 * KV_BARS + 8;
 constexpr uint32_t KV_SMEM = KV_SMEM_USED + 1024;
 
@@ -669,17 +672,54 @@ __device__ __forceinline__ KvSmem kv_carve(uint8_t* base) {
   b += 2;
   s.q_empty = b;
   b += 2;
-  s.s_full = b++;
-  s.dp_full = b++;
-  s.p_ready = b++;
-  s.ds_ready = b++;
-  s.dv_done = b++;
-  s.dk_done = b++;
+  s.s_full = b;
+  b += 2;
+  s.dp_full = b;
+  b += 2;
+  s.p_ready = b;
+  b += 2;
+  s.ds_ready = b;
+  b += 2;
+  s.xa_free = b;
+  b += 2;
+  s.xb_free = b;
+  b += 2;
   s.acc_full = b++;
   s.acc_free = b++;
   s.tmem_slot = reinterpret_cast<uint32_t*>(b);
   s.abort = s.tmem_slot + 1;
   return s;
+}
+
+// S^T or dP^T of one half: D[128 keys][64 queries] = A B^T over d = 128, A a
+// [128 keys][d] tile, B rows [q0, q0 + 64) of a [128 queries][d] tile (both
+// K-major), 8 steps of 16 d.
+__device__ __forceinline__ void mma_half_rows_dot(uint32_t d_tmem, uint32_t a_base, uint32_t b_base, int q0) {
+  constexpr uint32_t idesc = idesc_bf16_f32(128, 64, false, false);
+  const uint64_t ad = sdesc_sw128(a_base, 16, 1024);
+  const uint64_t bd = sdesc_sw128(b_base + static_cast<uint32_t>(q0) * 128u, 16, 1024);
+#pragma unroll
+  for (int ks = 0; ks < 8; ++ks) {
+    const uint32_t off = ((ks >> 2) * HALF + (ks & 3) * 32) >> 4;
+    mma_bf16_ss(d_tmem, ad + off, bd + off, idesc, ks > 0 ? 1u : 0u);
+  }
+}
+
+// Where half-tile element pairs sit after the in-place conversion: each of
+// the two element-wise warp groups keeps its 16 pairs (32 queries) at the
+// start of its own 32 fp32 columns.  k step ks (16 queries) -> column offset.
+__device__ __forceinline__ uint32_t half_col(int ks) { return static_cast<uint32_t>((ks >> 1) * 32 + (ks & 1) * 8); }
+
+// D (+)= A B with A the bf16 pairs of one half written in place (128 keys x
+// 64 queries) and B rows [q0, q0 + 64) of a [128 queries][128 d] tile read
+// MN-major, 4 steps of 16 queries.
+__device__ __forceinline__ void mma_half_by_tile(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_base, int q0,
+                                                 bool accumulate) {
+  constexpr uint32_t idesc = idesc_bf16_f32(128, 128, false, true);
+  const uint64_t bd = sdesc_sw128(b_base + static_cast<uint32_t>(q0) * 128u, HALF, 1024);
+#pragma unroll
+  for (int ks = 0; ks < 4; ++ks)
+    mma_bf16_ts(d_tmem, a_tmem + half_col(ks), bd + ((ks * 2048u) >> 4), idesc, (accumulate || ks > 0) ? 1u : 0u);
 }
 
 // Item = (global key block gb, head h), gb over the users' key blocks in
@@ -729,18 +769,18 @@ __global__ void __launch_bounds__(ABWD_THREADS, 1)
   fence_proxy_async_smem();
   if (threadIdx.x == 0) {
     mbar_init(s.kv_full, 1);
-    mbar_init(s.kv_empty, 2);  // both issuers
+    mbar_init(s.kv_empty, 2);  // the S^T and dP^T issuers
     for (int b = 0; b < 2; ++b) {
       mbar_init(&s.q_full[b], 1);
-      mbar_init(&s.q_empty[b], 2);
+      mbar_init(&s.q_empty[b], 1);
+      mbar_init(&s.s_full[b], 1);
+      mbar_init(&s.dp_full[b], 1);
+      mbar_init(&s.p_ready[b], EW_THREADS);
+      mbar_init(&s.ds_ready[b], EW_THREADS);
+      mbar_init(&s.xa_free[b], 1);
+      mbar_init(&s.xb_free[b], 1);
     }
-    mbar_init(s.s_full, 1);
-    mbar_init(s.dp_full, 1);
-    mbar_init(s.p_ready, EW_THREADS);
-    mbar_init(s.ds_ready, EW_THREADS);
-    mbar_init(s.dv_done, 1);
-    mbar_init(s.dk_done, 1);
-    mbar_init(s.acc_full, 2);
+    mbar_init(s.acc_full, 1);
     mbar_init(s.acc_free, EW_THREADS);
     *s.abort = 0;
     fence_barrier_init();
@@ -802,53 +842,82 @@ __global__ void __launch_bounds__(ABWD_THREADS, 1)
       }
     }
   } else if (warp == 1 || warp == 2) {
-    // ---- MMA issuers, one per accumulator: warp 1 S^T and dV += P^T dO,
-    // warp 2 dP^T and dK += dS^T Q.  S^T(t) waits only for dV(t-1) (the
-    // reader of the P^T written over S^T(t-1)), dP^T(t) only for dK(t-1).
-    const bool a_side = warp == 1;
-    uint32_t ni = 0, tq = 0;
-    const uint32_t a_base = smem_u32(a_side ? s.k : s.v);
-    uint64_t* done_bar = a_side ? s.dv_done : s.dk_done;
-    uint64_t* ready_bar = a_side ? s.p_ready : s.ds_ready;
-    const uint32_t t_in = a_side ? TK_ST : TK_DPT, t_acc = a_side ? TK_DV : TK_DK;
+    // ---- S^T (warp 1) and dP^T (warp 2) issuers: half g into buffer
+    // X_{g&1} once dV (dK) of half g-2 has read that buffer's P^T (dS^T)
+    const bool s_side = warp == 1;
+    uint32_t ni = 0, tq = 0, g = 0;
+    const uint32_t a_base = smem_u32(s_side ? s.k : s.v);
+    uint64_t* full = s_side ? s.s_full : s.dp_full;
+    uint64_t* xfree = s_side ? s.xa_free : s.xb_free;
+    const uint32_t col = s_side ? 0u : 64u;
     for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
       const KvItem x = kv_item(p, item);
       if (x.ntq == 0) continue;
       if (!wwait(s.kv_full, ni & 1u, s.abort, p.timeout_ns)) goto done;
       for (int t = 0; t < x.ntq; ++t, ++tq) {
         const int b = static_cast<int>(tq & 1u);
+        const uint32_t b_base = smem_u32((s_side ? s.q : s.go) + b * TILE);
+        if (!wwait(&s.q_full[b], (tq >> 1) & 1u, s.abort, p.timeout_ns)) goto done;
+        for (int h = 0; h < 2; ++h, ++g) {
+          const int xb = static_cast<int>(g & 1u);
+          if (g >= 2 && !wwait(&xfree[xb], ((g >> 1) - 1) & 1u, s.abort, p.timeout_ns)) goto done;
+          tc_fence_after();
+          if (elect_one()) {  // S^T = K Q_h^T  or  dP^T = V dO_h^T
+            mma_half_rows_dot(tmem + TK_X + 128u * xb + col, a_base, b_base, 64 * h);
+            mma_commit(&full[xb]);
+            if (t + 1 == x.ntq && h == 1) mma_commit(s.kv_empty);  // last reader of K (V)
+          }
+          __syncwarp();
+        }
+      }
+      ++ni;
+    }
+  } else if (warp == 3) {
+    // ---- dV / dK issuer: dV += P^T dO_h once P^T of half g is written,
+    // dK += dS^T Q_h once its dS^T is
+    uint32_t ni = 0, tq = 0, g = 0;
+    for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+      const KvItem x = kv_item(p, item);
+      if (x.ntq == 0) continue;
+      for (int t = 0; t < x.ntq; ++t, ++tq) {
+        const int b = static_cast<int>(tq & 1u);
         const uint32_t q_base = smem_u32(s.q + b * TILE), go_base = smem_u32(s.go + b * TILE);
         if (!wwait(&s.q_full[b], (tq >> 1) & 1u, s.abort, p.timeout_ns)) goto done;
-        if (tq > 0 && !wwait(done_bar, (tq - 1) & 1u, s.abort, p.timeout_ns)) goto done;
-        tc_fence_after();
-        if (elect_one()) {  // S^T = K Q^T  or  dP^T = V dO^T
-          mma_rows_dot(tmem + t_in, a_base, a_side ? q_base : go_base);
-          mma_commit(a_side ? s.s_full : s.dp_full);
-          if (t + 1 == x.ntq) mma_commit(s.kv_empty);  // last reader of K (V)
+        for (int h = 0; h < 2; ++h, ++g) {
+          const int xb = static_cast<int>(g & 1u);
+          const uint32_t k = g >> 1;
+          const bool first = t == 0 && h == 0;
+          if (!wwait(&s.p_ready[xb], k & 1u, s.abort, p.timeout_ns)) goto done;
+          if (first && ni > 0 && !wwait(s.acc_free, (ni - 1) & 1u, s.abort, p.timeout_ns)) goto done;
+          tc_fence_after();
+          if (elect_one()) {
+            mma_half_by_tile(tmem + TK_DV, tmem + TK_X + 128u * xb, go_base, 64 * h, !first);
+            mma_commit(&s.xa_free[xb]);
+          }
+          __syncwarp();
+          if (!wwait(&s.ds_ready[xb], k & 1u, s.abort, p.timeout_ns)) goto done;
+          tc_fence_after();
+          if (elect_one()) {
+            mma_half_by_tile(tmem + TK_DK, tmem + TK_X + 128u * xb + 64u, q_base, 64 * h, !first);
+            mma_commit(&s.xb_free[xb]);
+            if (h == 1) mma_commit(&s.q_empty[b]);  // last readers of the query tile
+            if (t + 1 == x.ntq && h == 1) mma_commit(s.acc_full);
+          }
+          __syncwarp();
         }
-        __syncwarp();
-        if (!wwait(ready_bar, tq & 1u, s.abort, p.timeout_ns)) goto done;
-        if (t == 0 && ni > 0 && !wwait(s.acc_free, (ni - 1) & 1u, s.abort, p.timeout_ns)) goto done;
-        tc_fence_after();
-        if (elect_one()) {  // dV += P^T dO  or  dK += dS^T Q
-          mma_inplace_by_tile(tmem + t_acc, tmem + t_in, a_side ? go_base : q_base, t > 0);
-          mma_commit(done_bar);
-          mma_commit(&s.q_empty[b]);
-          if (t + 1 == x.ntq) mma_commit(s.acc_full);
-        }
-        __syncwarp();
       }
       ++ni;
     }
   } else if (warp >= EW_WARP0) {
-    // ---- element-wise warps: lane = key row of the block; grp picks the
-    // half of the tile's 128 query columns (and of dK/dV's d columns)
+    // ---- element-wise warps: lane = key row of the block; grp picks 32 of
+    // each half's 64 query columns (and half of dK/dV's d columns)
     const int ew = warp - EW_WARP0, quarter = ew & 3, grp = ew >> 2;
     const int rk = quarter * 32 + static_cast<int>(lane_id());
     const uint32_t lane_base = static_cast<uint32_t>(32 * quarter) << 16;
-    const uint32_t col0 = 64u * grp;
+    const uint32_t col0 = 64u * grp;   // dK/dV columns in the epilogue
+    const uint32_t qc = 32u * grp;     // query columns within a half
     const float sl = p.scale_log2;
-    uint32_t tq = 0, ni = 0;
+    uint32_t tq = 0, ni = 0, g = 0;
     for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
       const KvItem x = kv_item(p, item);
       const int key = x.kb * 128 + rk;
@@ -865,90 +934,82 @@ __global__ void __launch_bounds__(ABWD_THREADS, 1)
         }
         continue;
       }
+      // every row of the warp a key (all but a user's last, partial block):
+      // no per-element select
+      const bool all_keys = __all_sync(0xffffffffu, kvalid);
       for (int t = 0; t < x.ntq; ++t, ++tq) {
         const int b = static_cast<int>(tq & 1u);
         // q_full[b] also covers this tile's LSE and D (bulk copies)
         if (!wwait(&s.q_full[b], (tq >> 1) & 1u, s.abort, p.timeout_ns)) goto done;
-        if (!wwait(s.s_full, tq & 1u, s.abort, p.timeout_ns)) goto done;
-        tc_fence_after();
-        const float* lse = s.lse + b * 128 + col0;
-        const float* drow = s.drow + b * 128 + col0;
-        // P^T = 2^(s sl - lse[q]), written over S^T (pairs at this half's start)
-        float pf[64];
-        {
-          uint32_t v[2][32];
-          tmem_ld32(tmem + lane_base + TK_ST + col0, v[0]);
-          tmem_ld32(tmem + lane_base + TK_ST + col0 + 32, v[1]);
-          tmem_ld_wait(v[0]);
-          tmem_ld_wait(v[1]);
-          // every row of the warp a key (all but a user's last, partial block):
-          // no per-element select
-          const bool all_keys = __all_sync(0xffffffffu, kvalid);
-#pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            uint32_t pk[16];
+        for (int h = 0; h < 2; ++h, ++g) {
+          const int xb = static_cast<int>(g & 1u);
+          const uint32_t k = g >> 1;
+          const uint32_t X = TK_X + 128u * xb;
+          const float* lse = s.lse + b * 128 + 64 * h + qc;
+          const float* drow = s.drow + b * 128 + 64 * h + qc;
+          // P^T = 2^(s sl - lse[q]), written over S^T (pairs at this group's start)
+          if (!wwait(&s.s_full[xb], k & 1u, s.abort, p.timeout_ns)) goto done;
+          tc_fence_after();
+          float pf[32];
+          {
+            uint32_t v[32], pk[16];
+            tmem_ld32(tmem + lane_base + X + qc, v);
+            tmem_ld_wait(v);
 #pragma unroll
             for (int j4 = 0; j4 < 8; ++j4) {
-              const float4 l4 = *reinterpret_cast<const float4*>(lse + c * 32 + 4 * j4);
+              const float4 l4 = *reinterpret_cast<const float4*>(lse + 4 * j4);
               const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
-              for (int e = 0; e < 4; ++e) pf[c * 32 + 4 * j4 + e] = ex2(fmaf(__uint_as_float(v[c][4 * j4 + e]), sl, -lv[e]));
+              for (int e = 0; e < 4; ++e) pf[4 * j4 + e] = ex2(fmaf(__uint_as_float(v[4 * j4 + e]), sl, -lv[e]));
             }
             if (!all_keys && !kvalid) {
 #pragma unroll
-              for (int j = 0; j < 32; ++j) pf[c * 32 + j] = 0.f;
+              for (int j = 0; j < 32; ++j) pf[j] = 0.f;
             }
 #pragma unroll
-            for (int j = 0; j < 16; ++j) pk[j] = pack_bf16x2(pf[c * 32 + 2 * j], pf[c * 32 + 2 * j + 1]);
-            tmem_st16(tmem + lane_base + TK_ST + col0 + 16 * c, pk);
+            for (int j = 0; j < 16; ++j) pk[j] = pack_bf16x2(pf[2 * j], pf[2 * j + 1]);
+            tmem_st16(tmem + lane_base + X + qc, pk);
           }
-        }
-        tmem_st_wait();
-        tc_fence_before();
-        mbar_arrive(s.p_ready);
-        // dS^T = P^T (dP^T - D[q]) scale, written over dP^T
-        if (!wwait(s.dp_full, tq & 1u, s.abort, p.timeout_ns)) goto done;
-        tc_fence_after();
-        {
-          uint32_t v[2][32];
-          tmem_ld32(tmem + lane_base + TK_DPT + col0, v[0]);
-          tmem_ld32(tmem + lane_base + TK_DPT + col0 + 32, v[1]);
-          tmem_ld_wait(v[0]);
-          tmem_ld_wait(v[1]);
-#pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            uint32_t pk[16];
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(&s.p_ready[xb]);
+          // dS^T = P^T (dP^T - D[q]) scale, written over dP^T
+          if (!wwait(&s.dp_full[xb], k & 1u, s.abort, p.timeout_ns)) goto done;
+          tc_fence_after();
+          {
+            uint32_t v[32], pk[16];
+            tmem_ld32(tmem + lane_base + X + 64u + qc, v);
+            tmem_ld_wait(v);
 #pragma unroll
             for (int j4 = 0; j4 < 4; ++j4) {
-              const float4 d4 = *reinterpret_cast<const float4*>(drow + c * 32 + 8 * j4);
-              const float4 e4 = *reinterpret_cast<const float4*>(drow + c * 32 + 8 * j4 + 4);
+              const float4 d4 = *reinterpret_cast<const float4*>(drow + 8 * j4);
+              const float4 e4 = *reinterpret_cast<const float4*>(drow + 8 * j4 + 4);
               const float dv8[8] = {d4.x, d4.y, d4.z, d4.w, e4.x, e4.y, e4.z, e4.w};
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
                 const int j = 8 * j4 + 2 * e;
-                pk[4 * j4 + e] = pack_bf16x2(pf[c * 32 + j] * (__uint_as_float(v[c][j]) - dv8[2 * e]) * p.scale,
-                                             pf[c * 32 + j + 1] * (__uint_as_float(v[c][j + 1]) - dv8[2 * e + 1]) *
-                                                 p.scale);
+                pk[4 * j4 + e] = pack_bf16x2(pf[j] * (__uint_as_float(v[j]) - dv8[2 * e]) * p.scale,
+                                             pf[j + 1] * (__uint_as_float(v[j + 1]) - dv8[2 * e + 1]) * p.scale);
               }
             }
-            tmem_st16(tmem + lane_base + TK_DPT + col0 + 16 * c, pk);
+            tmem_st16(tmem + lane_base + X + 64u + qc, pk);
           }
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(&s.ds_ready[xb]);
         }
-        tmem_st_wait();
-        tc_fence_before();
-        mbar_arrive(s.ds_ready);
       }
       // epilogue: this half's 64 d columns of the block's dV and dK rows
       if (!wwait(s.acc_full, ni & 1u, s.abort, p.timeout_ns)) goto done;
       ++ni;
       tc_fence_after();
 #pragma unroll 1
-      for (int g = 0; g < 2; ++g) {
-        uint16_t* out = g == 0 ? dv_row : dk_row;
+      for (int a = 0; a < 2; ++a) {  // dV, then dK
+        uint16_t* out = a == 0 ? dv_row : dk_row;
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           uint32_t v[32];
-          tmem_ld32(tmem + lane_base + (g == 0 ? TK_DV : TK_DK) + col0 + 32 * c, v);
+          tmem_ld32(tmem + lane_base + (a == 0 ? TK_DV : TK_DK) + col0 + 32 * c, v);
           tmem_ld_wait(v);
           if (kvalid) store_bf16x32(out + 32 * c, v);
         }
