@@ -91,6 +91,9 @@ def check(x, dO, dQ, dK, dV, qpairs=None, kvpairs=None, what=""):
     dict(n_cand=7, n_users=3, H=2, Lq=32, d=128, Lkv=200),      # two key tiles, ragged 72
     dict(n_cand=40, n_users=4, H=1, Lq=8, d=128, Lkv=130),      # 16 candidates per tile
     dict(n_cand=9, n_users=2, H=2, Lq=48, d=128, Lkv=64),       # 96 of 128 tile rows used
+    dict(n_cand=13, n_users=2, H=1, Lq=24, d=128, Lkv=140),     # 5 candidates per tile: halves of 2, 2, 1
+    dict(n_cand=5, n_users=2, H=2, Lq=72, d=128, Lkv=150),      # one candidate split over two halves
+    dict(n_cand=3, n_users=2, H=1, Lq=128, d=128, Lkv=129),     # a full 128-row candidate
 ])
 @pytest.mark.parametrize("use_lse", [False, True], ids=["recompute_lse", "forward_lse"])
 def test_attn_backward_dense(case, use_lse):
