@@ -187,6 +187,7 @@ ikbo_status_t lce_launch(ikbo_plan_t p, const void* U, const void* C, const void
   if (!lce_configure(&lp, p->max_smem)) return IKBO_ERR_UNSUPPORTED;
   lp.map = p->d_map;
   lp.order = p->d_perm;  // candidates grouped by user: consecutive tiles of a CTA share the user partial
+  lp.seg_offsets = p->d_offsets;
   lp.bias = static_cast<const uint16_t*>(b);
   lp.Y = static_cast<uint16_t*>(Y);
 

@@ -56,6 +56,7 @@ struct LceParams {
   const int32_t* map;
   const int32_t* order;   // candidate order for the candidate tiles (a permutation of 0..n_cand-1, grouped
                           // by user) or null for 0..n_cand-1
+  const int32_t* seg_offsets;  // [n_users + 1] where each user's run starts in order, or null
   const uint16_t* bias;   // [N] bf16 or null
   uint16_t* Y;            // [n_cand][N][D] bf16
   float* partial;         // [n_users][N][D] fp32 workspace (user GEMM + bias)

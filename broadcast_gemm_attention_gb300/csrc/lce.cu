@@ -143,7 +143,60 @@ __device__ __forceinline__ long long fused_q_start(const LceParams& p, int b) {
   return cum < 0 ? 0 : (cum > nq ? nq : cum);
 }
 
-__device__ __forceinline__ int cta_unit(const LceParams& p, int u0, int u1, int t) {
+// The local-partial schedule weights its ranges: a CTA pays for one local user
+// tile per (user, D block) its range touches, and with equal numbers of
+// candidate tiles the CTAs whose range crosses a user boundary end last.  So
+// the range boundaries split V(q) = c*q + h*(user runs starting before q)
+// evenly, q counting candidate tiles D-block-major over the candidate order.
+// c and h are the bytes a candidate tile streams from HBM (C in, Y out) and
+// 0.8 x the bytes of a user tile (U and W_u, mostly L2 hits).  One warp-wide
+// load of the run offsets serves up to 32 users; with more the split stays
+// even.  Every CTA evaluates the same function, so the ranges tile [0, nq).
+// All lanes must call it.
+__device__ __forceinline__ long long local_q_start(int b, int g, long long nq, int n_cand, long long c, long long h,
+                                                   long long vrow, long long vtot, int lo, int hi, bool nz, int rank) {
+  const long long T = b * vtot / g;
+  if (T <= 0) return 0;
+  if (T >= vtot) return nq;
+  const long long dblk = (T - 1) / vrow;  // dblk * vrow < T <= (dblk + 1) * vrow
+  const long long R = T - dblk * vrow;
+  // within a D block, a position in (lo, hi] of a user's run has rank + 1
+  // run starts before it: the first such position with V >= R
+  const long long need = R - h * (rank + 1);
+  long long pos = need <= 0 ? 1 : (need + c - 1) / c;
+  if (pos < lo + 1) pos = lo + 1;
+  const uint32_t ok = __ballot_sync(0xffffffffu, nz && pos <= hi);
+  const int l = ok ? __ffs(ok) - 1 : 31;
+  pos = __shfl_sync(0xffffffffu, ok ? pos : n_cand, l);
+  return dblk * n_cand + (pos < n_cand ? pos : n_cand);
+}
+
+__device__ __forceinline__ void local_range(const LceParams& p, long long& q0, long long& q1) {
+  const int g = static_cast<int>(gridDim.x), b = static_cast<int>(blockIdx.x);
+  const long long nq = static_cast<long long>(p.n_cand) * p.n_dblk;
+  if (p.seg_offsets == nullptr || p.n_users > 32) {
+    q0 = b * nq / g;
+    q1 = (b + 1) * nq / g;
+    return;
+  }
+  const int j = static_cast<int>(lane_id());
+  const bool in = j < p.n_users;
+  const int lo = in ? __ldg(p.seg_offsets + j) : p.n_cand;
+  // the last user's run ends at n_cand even if invalid map entries left
+  // candidates out of the offsets (the plan flags those)
+  const int hi = !in ? p.n_cand : (j == p.n_users - 1 ? p.n_cand : __ldg(p.seg_offsets + j + 1));
+  const bool nz = in && hi > lo;
+  const uint32_t runs = __ballot_sync(0xffffffffu, nz);
+  const int rank = __popc(runs & ((1u << j) - 1u));
+  const long long c = 5ll * LCE_BM * (p.K_c + p.N);
+  const long long h = 4ll * p.K_u * (LCE_BM + p.N);
+  const long long vrow = c * p.n_cand + h * __popc(runs);
+  const long long vtot = vrow * p.n_dblk;
+  q0 = local_q_start(b, g, nq, p.n_cand, c, h, vrow, vtot, lo, hi, nz, rank);
+  q1 = local_q_start(b + 1, g, nq, p.n_cand, c, h, vrow, vtot, lo, hi, nz, rank);
+}
+
+__device__ __forceinline__ int cta_unit(const LceParams& p, int u0, int u1, int t, long long lq0, long long lq1) {
   const int g = static_cast<int>(gridDim.x), b = static_cast<int>(blockIdx.x);
   const int uu = p.n_user_units;
   if (u0 == 0 && u1 == uu) {  // user launch
@@ -157,6 +210,9 @@ __device__ __forceinline__ int cta_unit(const LceParams& p, int u0, int u1, int 
     t -= nu;
     q0 = fused_q_start(p, b);
     q1 = fused_q_start(p, b + 1);
+  } else if (lq0 >= 0) {  // local partials: the weighted range
+    q0 = lq0;
+    q1 = lq1;
   } else {  // candidate launch
     const long long nq = static_cast<long long>(p.n_cand) * p.n_dblk;
     q0 = b * nq / g;
@@ -187,6 +243,7 @@ struct Walk {
   bool held = false;
   UnitInfo next;
   int next_user = -1;
+  long long q0 = -1, q1 = -1;  // the local schedule's range of candidate tiles
 };
 
 template <int kPhase>
@@ -198,8 +255,9 @@ __device__ __forceinline__ bool walk_next(const LceParams& p, int u0, int u1, Wa
     return true;
   }
   if (w.t - w.t0 >= 32) {
+    if (kPhase == LCE_PHASE_LOCAL && w.q0 < 0) local_range(p, w.q0, w.q1);
     w.t0 = w.t;
-    w.w_unit = cta_unit(p, u0, u1, w.t0 + static_cast<int>(lane_id()));
+    w.w_unit = cta_unit(p, u0, u1, w.t0 + static_cast<int>(lane_id()), w.q0, w.q1);
     if (w.w_unit >= 0) {
       const UnitInfo y = unit_info(p, w.w_unit);
       w.w_row = y.row;
