@@ -55,6 +55,7 @@ struct ikbo_plan_s {
   // plan-owned device memory
   int32_t* d_counts = nullptr;
   int32_t* d_offsets = nullptr;
+  int32_t* d_runs = nullptr;
   int32_t* d_perm = nullptr;
   int32_t* d_work = nullptr;
   int32_t* d_n_units = nullptr;
@@ -146,6 +147,7 @@ void free_plan(ikbo_plan_t p) {
   if (!p) return;
   cudaFree(p->d_counts);
   cudaFree(p->d_offsets);
+  cudaFree(p->d_runs);
   cudaFree(p->d_perm);
   cudaFree(p->d_work);
   cudaFree(p->d_n_units);
@@ -188,6 +190,7 @@ ikbo_status_t lce_launch(ikbo_plan_t p, const void* U, const void* C, const void
   lp.map = p->d_map;
   lp.order = p->d_perm;  // candidates grouped by user: consecutive tiles of a CTA share the user partial
   lp.seg_offsets = p->d_offsets;
+  lp.seg_runs = p->d_runs;
   lp.bias = static_cast<const uint16_t*>(b);
   lp.Y = static_cast<uint16_t*>(Y);
 
@@ -431,6 +434,7 @@ ikbo_status_t ikbo_plan_create(ikbo_plan_t* out, int max_cand, int max_users, in
   p->max_units = static_cast<int64_t>(max_heads) * (max_users + max_cand);
   bool ok = cudaMalloc(&p->d_counts, sizeof(int32_t) * max_users) == cudaSuccess &&
             cudaMalloc(&p->d_offsets, sizeof(int32_t) * (max_users + 1)) == cudaSuccess &&
+            cudaMalloc(&p->d_runs, sizeof(int32_t) * (max_users + 1)) == cudaSuccess &&
             cudaMalloc(&p->d_perm, sizeof(int32_t) * max_cand) == cudaSuccess &&
             cudaMalloc(&p->d_work, sizeof(int32_t) * 4 * p->max_units) == cudaSuccess &&
             cudaMalloc(&p->d_n_units, sizeof(int32_t)) == cudaSuccess &&
@@ -486,6 +490,7 @@ ikbo_status_t ikbo_plan(ikbo_plan_t p, const int32_t* d_map, int n_cand, int n_u
   sp.cands_per_unit = ATT_TILES * cpt;
   sp.counts = p->d_counts;
   sp.offsets = p->d_offsets;
+  sp.runs = p->d_runs;
   sp.perm = p->d_perm;
   sp.work = p->d_work;
   sp.n_units = p->d_n_units;

@@ -33,6 +33,7 @@ struct SegParams {
   int n_cand, n_users, H, cands_per_unit;
   int32_t* counts;    // [n_users]
   int32_t* offsets;   // [n_users + 1]
+  int32_t* runs;      // [n_users + 1] users before u with at least one candidate; [n_users] = all such
   int32_t* perm;      // [n_cand]
   int32_t* work;      // [max_units][4]
   int32_t* n_units;   // [1]
@@ -57,6 +58,7 @@ struct LceParams {
   const int32_t* order;   // candidate order for the candidate tiles (a permutation of 0..n_cand-1, grouped
                           // by user) or null for 0..n_cand-1
   const int32_t* seg_offsets;  // [n_users + 1] where each user's run starts in order, or null
+  const int32_t* seg_runs;     // [n_users + 1] non-empty runs before each user (and in all), or null
   const uint16_t* bias;   // [N] bf16 or null
   uint16_t* Y;            // [n_cand][N][D] bf16
   float* partial;         // [n_users][N][D] fp32 workspace (user GEMM + bias)

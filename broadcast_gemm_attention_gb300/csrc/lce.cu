@@ -62,6 +62,7 @@ struct LceSmem {
   uint64_t* pub;  // the 128 epilogue threads finished writing a user partial
   uint32_t* tmem_slot;
   uint32_t* abort;
+  long long* range;  // local-partial schedule: this CTA's [q0, q1) of candidate tiles
 };
 
 __device__ __forceinline__ LceSmem carve(uint8_t* base, const LceParams& p) {
@@ -82,6 +83,7 @@ __device__ __forceinline__ LceSmem carve(uint8_t* base, const LceParams& p) {
   s.pub = s.acc_empty + 2;
   s.tmem_slot = reinterpret_cast<uint32_t*>(s.pub + 1);
   s.abort = s.tmem_slot + 1;
+  s.range = reinterpret_cast<long long*>(s.abort + 1);
   return s;
 }
 
@@ -149,51 +151,74 @@ __device__ __forceinline__ long long fused_q_start(const LceParams& p, int b) {
 // the range boundaries split V(q) = c*q + h*(user runs starting before q)
 // evenly, q counting candidate tiles D-block-major over the candidate order.
 // c and h are the bytes a candidate tile streams from HBM (C in, Y out) and
-// 0.8 x the bytes of a user tile (U and W_u, mostly L2 hits).  One warp-wide
-// load of the run offsets serves up to 32 users; with more the split stays
-// even.  Every CTA evaluates the same function, so the ranges tile [0, nq).
-// All lanes must call it.
-__device__ __forceinline__ long long local_q_start(int b, int g, long long nq, int n_cand, long long c, long long h,
-                                                   long long vrow, long long vtot, int lo, int hi, bool nz, int rank) {
-  const long long T = b * vtot / g;
+// 0.8 x the bytes of a user tile (U and W_u, mostly L2 hits).  Within a D
+// block, a position in (offsets[u], offsets[u + 1]] of a non-empty user u
+// has runs[u + 1] run starts before it; warp 3 of every CTA evaluates the
+// same function, so the ranges tile [0, nq).  The boundary search probes 32
+// users per warp-wide load (one load for up to 32 users).  All lanes must
+// call these.
+struct RunProbe {
+  int stride;          // users per lane in this round
+  long long end, beg;  // the end (and, in the last round, the start) of the lane's user's run
+  long long nr;        // non-empty runs up to and including that user
+};
+
+__device__ __forceinline__ RunProbe run_probe(const LceParams& p, int lo, int hi) {
+  RunProbe r;
+  r.stride = (hi - lo + 32) >> 5;
+  const int u = min(lo + (static_cast<int>(lane_id()) + 1) * r.stride - 1, hi);
+  // the last user's run ends at n_cand even if invalid map entries left
+  // candidates out of the offsets (the plan flags those)
+  r.end = u == p.n_users - 1 ? p.n_cand : __ldg(p.seg_offsets + u + 1);
+  r.beg = r.stride == 1 ? __ldg(p.seg_offsets + u) : 0;
+  r.nr = __ldg(p.seg_runs + u + 1);
+  return r;
+}
+
+// the first q with V(q) >= T; r is the first round's probe (lo 0, hi n_users - 1)
+__device__ __forceinline__ long long local_q_start(const LceParams& p, long long T, long long c, long long h,
+                                                   long long vrow, long long vtot, long long nq, RunProbe r) {
   if (T <= 0) return 0;
   if (T >= vtot) return nq;
   const long long dblk = (T - 1) / vrow;  // dblk * vrow < T <= (dblk + 1) * vrow
   const long long R = T - dblk * vrow;
-  // within a D block, a position in (lo, hi] of a user's run has rank + 1
-  // run starts before it: the first such position with V >= R
-  const long long need = R - h * (rank + 1);
-  long long pos = need <= 0 ? 1 : (need + c - 1) / c;
-  if (pos < lo + 1) pos = lo + 1;
-  const uint32_t ok = __ballot_sync(0xffffffffu, nz && pos <= hi);
-  const int l = ok ? __ffs(ok) - 1 : 31;
-  pos = __shfl_sync(0xffffffffu, ok ? pos : n_cand, l);
-  return dblk * n_cand + (pos < n_cand ? pos : n_cand);
+  // the first user whose run ends at V >= R (V at the last run's end is vrow)
+  int lo = 0, hi = p.n_users - 1;
+  for (;;) {
+    const uint32_t ok = __ballot_sync(0xffffffffu, c * r.end + h * r.nr >= R);
+    const int l = ok ? __ffs(ok) - 1 : 31;
+    if (r.stride == 1) {
+      const long long beg = __shfl_sync(0xffffffffu, r.beg, l);
+      const long long nr = __shfl_sync(0xffffffffu, r.nr, l);
+      const long long need = R - h * nr;
+      long long pos = need <= 0 ? 1 : (need + c - 1) / c;
+      if (pos < beg + 1) pos = beg + 1;
+      return dblk * p.n_cand + (pos < p.n_cand ? pos : p.n_cand);
+    }
+    const int nlo = lo + l * r.stride;
+    hi = min(nlo + r.stride - 1, hi);
+    lo = nlo;
+    r = run_probe(p, lo, hi);
+  }
 }
 
 __device__ __forceinline__ void local_range(const LceParams& p, long long& q0, long long& q1) {
   const int g = static_cast<int>(gridDim.x), b = static_cast<int>(blockIdx.x);
   const long long nq = static_cast<long long>(p.n_cand) * p.n_dblk;
-  if (p.seg_offsets == nullptr || p.n_users > 32) {
+  // with one user the even split already cuts at the D-block boundary
+  if (p.seg_offsets == nullptr || p.seg_runs == nullptr || p.n_users < 2) {
     q0 = b * nq / g;
     q1 = (b + 1) * nq / g;
     return;
   }
-  const int j = static_cast<int>(lane_id());
-  const bool in = j < p.n_users;
-  const int lo = in ? __ldg(p.seg_offsets + j) : p.n_cand;
-  // the last user's run ends at n_cand even if invalid map entries left
-  // candidates out of the offsets (the plan flags those)
-  const int hi = !in ? p.n_cand : (j == p.n_users - 1 ? p.n_cand : __ldg(p.seg_offsets + j + 1));
-  const bool nz = in && hi > lo;
-  const uint32_t runs = __ballot_sync(0xffffffffu, nz);
-  const int rank = __popc(runs & ((1u << j) - 1u));
+  const RunProbe r = run_probe(p, 0, p.n_users - 1);
+  const long long runs = __ldg(p.seg_runs + p.n_users);
   const long long c = 5ll * LCE_BM * (p.K_c + p.N);
   const long long h = 4ll * p.K_u * (LCE_BM + p.N);
-  const long long vrow = c * p.n_cand + h * __popc(runs);
+  const long long vrow = c * p.n_cand + h * runs;
   const long long vtot = vrow * p.n_dblk;
-  q0 = local_q_start(b, g, nq, p.n_cand, c, h, vrow, vtot, lo, hi, nz, rank);
-  q1 = local_q_start(b + 1, g, nq, p.n_cand, c, h, vrow, vtot, lo, hi, nz, rank);
+  q0 = local_q_start(p, b * vtot / g, c, h, vrow, vtot, nq, r);
+  q1 = local_q_start(p, (b + 1) * vtot / g, c, h, vrow, vtot, nq, r);
 }
 
 __device__ __forceinline__ int cta_unit(const LceParams& p, int u0, int u1, int t, long long lq0, long long lq1) {
@@ -244,7 +269,12 @@ struct Walk {
   UnitInfo next;
   int next_user = -1;
   long long q0 = -1, q1 = -1;  // the local schedule's range of candidate tiles
+  const long long* range = nullptr;  // where warp 3 posts it (shared memory)
 };
+
+// The local schedule's range is computed once per CTA by warp 3 while the
+// other warps start; the 11 warps that walk or post it meet on named barrier 1.
+constexpr int LCE_RANGE_BAR = 1, LCE_RANGE_THREADS = 32 * 11;
 
 template <int kPhase>
 __device__ __forceinline__ bool walk_next(const LceParams& p, int u0, int u1, Walk& w, UnitInfo& x, int& user) {
@@ -255,7 +285,11 @@ __device__ __forceinline__ bool walk_next(const LceParams& p, int u0, int u1, Wa
     return true;
   }
   if (w.t - w.t0 >= 32) {
-    if (kPhase == LCE_PHASE_LOCAL && w.q0 < 0) local_range(p, w.q0, w.q1);
+    if (kPhase == LCE_PHASE_LOCAL && w.q0 < 0) {
+      named_barrier_sync(LCE_RANGE_BAR, LCE_RANGE_THREADS);
+      w.q0 = w.range[0];
+      w.q1 = w.range[1];
+    }
     w.t0 = w.t;
     w.w_unit = cta_unit(p, u0, u1, w.t0 + static_cast<int>(lane_id()), w.q0, w.q1);
     if (w.w_unit >= 0) {
@@ -330,6 +364,7 @@ __device__ void lce_producer(const LceParams& p, const LceSmem& s, const CUtenso
   }
 
   Walk walk;
+  walk.range = s.range;
   for (;;) {
     UnitInfo x;
     int user;
@@ -402,6 +437,7 @@ __device__ void lce_mma(const LceParams& p, const LceSmem& s, uint32_t tmem, int
   uint32_t u_phase = 0;
   bool wc_ready = false;
   Walk walk;
+  walk.range = s.range;
   for (int local = 0;; ++local) {
     UnitInfo x;
     int user;
@@ -532,6 +568,7 @@ __device__ void lce_epilogue(const LceParams& p, const LceSmem& s, uint32_t tmem
   float pre[EPI_PREFETCH][32];
   int pre_u = -1, pre_dblk = -1;
   Walk walk;
+  walk.range = s.range;
   for (;; ++local) {
     UnitInfo x;
     int user;  // candidate tiles: map[i] (the warp's lanes looked it up together)
@@ -754,6 +791,14 @@ __global__ void __launch_bounds__(LCE_THREADS, 1)
       lce_producer<kPhase>(p, s, &tmU, &tmC, &tmWu, &tmWc, u0, u1);
     } else if (warp == 1) {
       lce_mma<kPhase>(p, s, tmem, u0, u1);
+    } else if (warp == 3 && kPhase == LCE_PHASE_LOCAL) {
+      long long q0, q1;
+      local_range(p, q0, q1);
+      if (lane_id() == 0) {
+        s.range[0] = q0;
+        s.range[1] = q1;
+      }
+      named_barrier_arrive(LCE_RANGE_BAR, LCE_RANGE_THREADS);
     }
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 216;");
@@ -811,7 +856,8 @@ size_t lce_flag_count(const LceParams& lp) {
 
 size_t lce_smem_bytes(const LceParams& p) {
   const size_t bars =
-      sizeof(uint64_t) * (2 * p.stages + 2 * p.w_slots + 2 * p.wu_slots + 1 + 4 + 1) + 2 * sizeof(uint32_t);
+      sizeof(uint64_t) * (2 * p.stages + 2 * p.w_slots + 2 * p.wu_slots + 1 + 4 + 1) + 2 * sizeof(uint32_t) +
+      2 * sizeof(long long);
   return 1024 + p.w_region_bytes + static_cast<size_t>(p.stages) * LCE_A_STAGE_BYTES +
          static_cast<size_t>(p.wu_slots) * p.NB * BOX_BYTES + bars;
 }

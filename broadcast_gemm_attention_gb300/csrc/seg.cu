@@ -96,6 +96,17 @@ __global__ void __launch_bounds__(SEG_THREADS, 1) seg_build_kernel(SegParams p) 
   }
   if (tid == 0) p.offsets[nu] = total;
 
+  // non-empty runs before each user (the LCE weights its ranges by them)
+  int local_runs = 0;
+  for (int u = lo; u < hi; ++u) local_runs += cnt[u] > 0;
+  int total_runs;
+  int rrun = block_exclusive_scan(local_runs, warp_sums, &total_runs);
+  for (int u = lo; u < hi; ++u) {
+    p.runs[u] = rrun;
+    rrun += cnt[u] > 0;
+  }
+  if (tid == 0) p.runs[nu] = total_runs;
+
   // work units per user: H * ceil(count / cands_per_unit)
   const int cpu = p.cands_per_unit;
   int local_units = 0;
