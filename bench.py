@@ -577,6 +577,11 @@ def e2e_run(plan, d, Y, O, x, a, step_flops, args, K, world, dist, dev):
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e_s.elapsed_time(e_e) / n_e2e, dist, dev)
     st = plan.status()
+    # the plan borrows its map: bind it to the resident one again before
+    # this function's second buffer set is freed (the later measurements
+    # reuse the plan)
+    plan.plan(d["map"], x.n_users, a.H, a.Lq, torch.cuda.current_stream(dev))
+    torch.cuda.synchronize()
     return {"value": world * step_flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "steps": n_e2e, "status": "ok" if st == 0 else st,
             "path": "pinned host -> device copies of every input, ikbo_plan + ikbo_lce_forward + ikbo_attn_forward, "
