@@ -71,6 +71,33 @@ def test_lce_70to1_sampled():
     assert torch.isfinite(Y.float()).all()
 
 
+def test_lce_many_empty_users():
+    """3 000 users of which ~20 have candidates (runs of very different
+    lengths, most users empty): the candidate-tile ranges are weighted by the
+    non-empty runs, found by a search over all users in several rounds."""
+    rng = np.random.default_rng(31)
+    active = np.sort(rng.choice(3000, size=20, replace=False))
+    counts = rng.multinomial(700, rng.dirichlet(np.full(20, 0.5)))
+    m = np.repeat(active, counts)
+    rng.shuffle(m)
+    x = gen.make_lce("empties", 32, 700, 3000, 40, 30, 136, 40, explicit_map=m.tolist())
+    Y, st = run_lce(x)
+    assert st == B.IKBO_OK
+    ref = oracle.lce(x.map, x.U, x.C, x.Wu, x.Wc, x.b)
+    assert_lce_close(Y, ref, "many empty users")
+
+
+def test_lce_users_past_1024():
+    """1 500 users with one candidate each: every candidate tile starts a
+    run, and the range search takes two rounds of 32 probes."""
+    m = np.random.default_rng(33).permutation(1500)
+    x = gen.make_lce("runs", 34, 1500, 1500, 24, 40, 128, 32, explicit_map=m.tolist())
+    Y, st = run_lce(x)
+    assert st == B.IKBO_OK
+    ref = oracle.lce(x.map, x.U, x.C, x.Wu, x.Wc, x.b)
+    assert_lce_close(Y, ref, "users past 1024")
+
+
 @pytest.mark.parametrize("n_cand,ratio", [(256, 10), (4096, 70), (1024, 1000), (4096, 10000)])
 def test_lce_sweep_points_sampled(n_cand, ratio):
     pts = {(n, r): s for n, r, s in gen.lce_sweep_points()}
