@@ -880,7 +880,12 @@ int lce_resolve_schedule(const LceParams& p, int num_sms) {
   // in map order a CTA's range could change user at every tile
   const bool local_ok = p.stages_local >= 2 && p.mode == 0 && p.order != nullptr;
   if (p.schedule == LCE_SCHEDULE_TWO || p.schedule == LCE_SCHEDULE_ONE) return p.schedule;
-  if (local_ok) return LCE_SCHEDULE_LOCAL;
+  if (p.schedule == LCE_SCHEDULE_LOCAL && local_ok) return LCE_SCHEDULE_LOCAL;
+  // with a single user every CTA of the local schedule would repeat the same
+  // user tiles; one launch computes them once (measured faster than local
+  // partials and than two launches at 256, 1024 and 4096 candidates)
+  if (local_ok && p.n_users > 1) return LCE_SCHEDULE_LOCAL;
+  if (p.n_users == 1) return LCE_SCHEDULE_ONE;
   // Plan-time choice (measured over the n_cand x ratio sweep): with few
   // candidate tiles per SM, one launch hides the user tiles under the
   // candidate tiles' start-up; with many, two launches keep every
