@@ -287,7 +287,8 @@ ikbo_status_t ikbo_plan_set_timeout_ns(ikbo_plan_t p, uint64_t timeout_ns);
 /* Launch schedule of ikbo_lce_forward (plan-time kernel selection over the
  * shape range, the "compile for a range of shapes" idea of the pages done as
  * a runtime choice):
- *   0  chosen from the shape (default): 3 where it applies, else 2 when the
+ *   0  chosen from the shape (default): 3 where it applies and the request
+ *      has at least two users; 2 for a single user; otherwise 2 when the
  *      request has fewer than 8 candidate tiles of 128 D-rows per SM, else 1
  *   1  two launches: user tiles (fp32 partials in the plan's workspace, with
  *      release flags), then candidate tiles
