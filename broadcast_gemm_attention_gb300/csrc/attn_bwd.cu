@@ -219,6 +219,11 @@ __device__ __forceinline__ DqSmem dq_carve(uint8_t* base) {
   return s;
 }
 
+// Hint: bring the 128-byte line holding `ptr` into L2.
+__device__ __forceinline__ void prefetch_l2(const void* ptr) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));
+}
+
 // A work-list unit: user, head, its candidates perm[start .. start+cnt).
 struct QUnit {
   int u, h, start, cnt, ntiles;
@@ -472,7 +477,7 @@ __global__ void __launch_bounds__(ABWD_THREADS, 1)
       if (valid) {
         const uint4* orow = reinterpret_cast<const uint4*>(p.O + row * 128);
         const uint4* grow = reinterpret_cast<const uint4*>(p.dO + row * 128);
-#pragma unroll 4
+#pragma unroll 8
         for (int c = 0; c < 16; ++c) {
           const uint4 a = __ldg(orow + c), g = __ldg(grow + c);
           const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, gw[4] = {g.x, g.y, g.z, g.w};
@@ -542,8 +547,26 @@ __global__ void __launch_bounds__(ABWD_THREADS, 1)
         p.lse[static_cast<size_t>(unit) * 128 + r] = valid ? lse2 : INFINITY;
         p.Drow[static_cast<size_t>(unit) * 128 + r] = valid ? D : 0.f;
       }
-      // pass 2: P = 2^(s sl - lse), dS = P (dP - D) scale written over S
+      // pass 2: P = 2^(s sl - lse), dS = P (dP - D) scale written over S.
+      // Over its first three tiles this thread also brings its row of the
+      // next unit's O and dO into L2 (each load has a tile's time to arrive
+      // before its value is used), so the next unit's D starts on L2 hits.
+      const int nunit = unit + static_cast<int>(gridDim.x);
+      int4 nw = make_int4(-1, 0, 0, 0);
+      int ncand = -1;
       for (int jt = 0; jt < x.ntiles; ++jt) {
+        if (jt == 0 && nunit < n_units) {
+          nw = __ldg(reinterpret_cast<const int4*>(p.work) + nunit);
+        } else if (jt == 1) {
+          if (nw.x >= 0 && nw.z >= 0 && slot < nw.w && nw.z + nw.w <= p.n_cand && r < rows)
+            ncand = __ldg(p.perm + nw.z + slot);
+        } else if (jt == 2 && ncand >= 0 && ncand < p.n_cand && nw.y >= 0 && nw.y < p.H) {
+          const size_t nrow = (static_cast<size_t>(ncand) * p.H + nw.y) * p.Lq + q;
+          prefetch_l2(p.O + nrow * 128);
+          prefetch_l2(p.O + nrow * 128 + 64);
+          prefetch_l2(p.dO + nrow * 128);
+          prefetch_l2(p.dO + nrow * 128 + 64);
+        }
         const uint32_t b = sc & 1u;
         if (!wwait(&s.s_full[b], (sc >> 1) & 1u, s.abort, p.timeout_ns)) goto done;
         ++sc;
