@@ -472,6 +472,8 @@ __global__ void __launch_bounds__(ABWD_THREADS, 1)
         }
         continue;
       }
+      // the forward's LSE for this row, loaded beside O and dO
+      const float lse_in = (p.lse_in && valid) ? p.lse_in[row] : 0.f;
       // D = rowsum(dO * O) over all of d (both halves compute it: no exchange)
       float D = 0.f;
       if (valid) {
@@ -490,7 +492,7 @@ __global__ void __launch_bounds__(ABWD_THREADS, 1)
       }
       float lse2;
       if (p.lse_in) {  // the forward's natural-log LSE -> log2 domain; rows without a query: any finite value
-        lse2 = valid ? p.lse_in[row] * 1.4426950408889634f : 0.f;
+        lse2 = lse_in * 1.4426950408889634f;
       } else {
         // pass 1: running max and sum over this half's key columns (log2 domain)
         float m = -INFINITY, l = 0.f;
@@ -566,6 +568,7 @@ __global__ void __launch_bounds__(ABWD_THREADS, 1)
           prefetch_l2(p.O + nrow * 128 + 64);
           prefetch_l2(p.dO + nrow * 128);
           prefetch_l2(p.dO + nrow * 128 + 64);
+          if (p.lse_in) prefetch_l2(p.lse_in + nrow);
         }
         const uint32_t b = sc & 1u;
         if (!wwait(&s.s_full[b], (sc >> 1) & 1u, s.abort, p.timeout_ns)) goto done;
