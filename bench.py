@@ -241,6 +241,107 @@ def calibrate_oracle(x, a, seconds: float, lo: int = 1, hi: int = 1024):
     return max(lo, min(hi, n))
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the machine type)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.machine()
+
+
+def oracle_time(run, total: int, unit: str, seconds: float = 2.0, probe: int = 32) -> dict:
+    """Wall time of the fp64 oracle on a calibrated sample of `total` units
+    (candidates, (candidate, head) pairs, ...): run(n) does n of them.  A
+    probe of `probe` units (enough to keep every host thread busy) sizes the
+    sample to about `seconds`; the full time is that sample's time scaled by
+    total / n.  Returns the estimate, the sample and the host it ran on."""
+    import oracle
+    n0 = max(1, min(total, probe))
+    t0 = time.perf_counter()
+    run(n0)
+    dt = time.perf_counter() - t0
+    n = max(1, min(total, int(round(n0 * seconds / max(dt, 1e-6)))))
+    if n > n0:
+        t0 = time.perf_counter()
+        run(n)
+        dt = time.perf_counter() - t0
+    else:
+        n = n0
+    return {"seconds_full_est": dt * total / n, "seconds_sample": dt, "sample": f"{n} of {total} {unit}",
+            "full": n == total, "cores": oracle.max_threads(), "cpu_model": cpu_model(), "kind": "oracle"}
+
+
+def oracle_lce_time(x, seconds=2.0, seed=0) -> dict:
+    import numpy as np
+    import oracle
+    order = np.random.default_rng(seed).permutation(x.n_cand).tolist()
+    return oracle_time(lambda n: oracle.lce(x.map, x.U, x.C, x.Wu, x.Wc, x.b, cands=sorted(order[:n])),
+                       x.n_cand, "candidates (all their LCE rows)", seconds)
+
+
+def oracle_attn_time(x, seconds=2.0, seed=0) -> dict:
+    import numpy as np
+    import oracle
+    pairs = [(i, h) for i in range(x.n_cand) for h in range(x.H)]
+    order = np.random.default_rng(seed).permutation(len(pairs)).tolist()
+    offs = x.kv_offsets if x.jagged else None
+    return oracle_time(lambda n: oracle.attn(x.map, x.Q, x.K, x.V, kv_offsets=offs, n_users=x.n_users,
+                                             pairs=[pairs[k] for k in sorted(order[:n])]),
+                       len(pairs), "(candidate, head) pairs", seconds)
+
+
+def oracle_lce_backward_time(x, dY) -> dict:
+    """The oracle's LCE backward, every gradient, once in full."""
+    import oracle
+    t0 = time.perf_counter()
+    oracle.lce_backward(x.map, x.U, x.C, x.Wu, x.Wc, dY)
+    dt = time.perf_counter() - t0
+    return {"seconds_full_est": dt, "seconds_sample": dt, "sample": "the whole call (dU, dC, dWu, dWc, db)",
+            "full": True, "cores": oracle.max_threads(), "cpu_model": cpu_model(), "kind": "oracle"}
+
+
+def oracle_attn_backward_time(a, dO, seconds=2.0) -> dict:
+    """The oracle's attention backward on two samples, dQ rows of (candidate,
+    head) pairs and dK/dV of (user, head) pairs, each scaled to the full call."""
+    q = oracle_time(lambda n: oracle_attn_bwd(a, dO, qpairs=[(i % a.n_cand, (i // a.n_cand) % a.H)
+                                                              for i in range(0, n * 7, 7)], kvpairs=[]),
+                    a.n_cand * a.H, "dQ (candidate, head) pairs", seconds / 2)
+    kv = oracle_time(lambda n: oracle_attn_bwd(a, dO, qpairs=[], kvpairs=[(u % a.n_users, (u // a.n_users) % a.H)
+                                                                          for u in range(n)]),
+                     a.n_users * a.H, "dK/dV (user, head) pairs", seconds / 2, probe=16)
+    return {"seconds_full_est": q["seconds_full_est"] + kv["seconds_full_est"],
+            "seconds_sample": q["seconds_sample"] + kv["seconds_sample"],
+            "sample": f"{q['sample']}; {kv['sample']}", "full": False, "cores": q["cores"],
+            "cpu_model": q["cpu_model"], "kind": "oracle"}
+
+
+def gen_grad_lce(x):
+    from broadcast_gemm_attention_gb300 import inputs as gen
+    return gen.make_lce_grad(1001, x.n_cand, x.N, x.D)
+
+
+def gen_grad_attn(a):
+    from broadcast_gemm_attention_gb300 import inputs as gen
+    return gen.make_attn_grad(1003, tuple(a.Q.shape))
+
+
+def oracle_attn_bwd(a, dO, qpairs, kvpairs):
+    import oracle
+    return oracle.attn_backward(a.map, a.Q, a.K, a.V, dO, qpairs=qpairs, kvpairs=kvpairs)
+
+
 def run_reference(args):
     """The reference arm: the oracle, as it stands, on the host cores."""
     rank = int(os.environ.get("RANK", "0"))
@@ -398,8 +499,13 @@ def run_gpu(args):
     if (world == 1 or rank == 0) and args.cpu_seconds > 0:
         n = calibrate_oracle(x, a, args.cpu_seconds)
         dt, fl, desc, thr = cpu_oracle_sample(x, a, n)
-        cpu = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": thr, "kind": "oracle", "sample": desc,
-               "seconds": dt}
+        cpu = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": thr, "cpu_model": cpu_model(), "kind": "oracle",
+               "sample": desc, "seconds": dt, "seconds_full_est": dt * x.n_cand / n}
+        # the oracle's time for the backward passes of the same request
+        if lce_backward is not None:
+            lce_backward["cpu_oracle"] = oracle_lce_backward_time(x, gen_grad_lce(x))
+        if attn_backward is not None:
+            attn_backward["cpu_oracle"] = oracle_attn_backward_time(a, gen_grad_attn(a))
 
     out = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
@@ -479,7 +585,9 @@ def run_sweep(args):
         byt = acc.lce_bytes(x.n_cand, x.n_users, x.K_u, x.K_c, x.D, x.N)
         fl = acc.lce_flops(x.n_cand, x.n_users, x.K_u, x.K_c, x.D, x.N)
         t_roof = max(byt / (pk["hbm_gbs"] * 1e9), fl / (pk["bf16_tflops"] * 1e12))
+        cpu = oracle_lce_time(x) if args.cpu_seconds > 0 else None
         print(json.dumps({"sweep": "lce", "n_cand": n, "ratio": r, "n_users": x.n_users, "us": us, "schedules_us": sched,
+                          "cpu_oracle": cpu,
                           "roofline_us": t_roof * 1e6, "frac": t_roof * 1e6 / us, "gbs": byt / (us * 1e-6) / 1e9,
                           "materialised": {"build_us": mat_us, "lce_us": on_mat_us, "total_us": mat_us + on_mat_us,
                                            "ikbo_speedup": (mat_us + on_mat_us) / us,
@@ -497,10 +605,27 @@ def run_sweep(args):
         fl = acc.attn_flops(x.H, x.Lq, x.d, [x.Lkv] * x.n_cand)
         byt = acc.attn_bytes(x.n_cand, x.H, x.Lq, x.d, x.n_users * x.Lkv)
         t_roof = max(byt / (pk["hbm_gbs"] * 1e9), fl / (pk["bf16_tflops"] * 1e12))
-        print(json.dumps({"sweep": "attn", "n_cand": n, "ratio": r, "n_users": x.n_users, "us": us,
+        cpu = oracle_attn_time(x) if args.cpu_seconds > 0 else None
+        print(json.dumps({"sweep": "attn", "n_cand": n, "ratio": r, "n_users": x.n_users, "us": us, "cpu_oracle": cpu,
                           "roofline_us": t_roof * 1e6, "frac": t_roof * 1e6 / us, "tflops": fl / (us * 1e-6) / 1e12,
                           "bound": "hbm" if byt / (pk["hbm_gbs"] * 1e9) > fl / (pk["bf16_tflops"] * 1e12) else "tensor",
                           "status": B.ikbo_status_string(st)}), flush=True)
+        del Q, K, V, m, O
+    # self + target attention: one launch against two, where the users' own
+    # queries are a real share of the work (Lq_u up to 512 rows per user and
+    # head) and at 4096 candidates of 59 users
+    for x in (gen.attn_70to1(), gen.make_attn("attn_4096_59", 1044, n_cand=4096, n_users=59, H=8, Lq=16, d=128,
+                                               Lkv=2048, map_kind="permuted")):
+        Q, K, V, m = [t.to(dev) for t in (x.Q, x.K, x.V, x.map)]
+        O = torch.empty_like(Q)
+        with B.Plan(x.n_cand, x.n_users, x.H) as p:
+            p.plan(m, x.n_users, x.H, x.Lq, stream)
+            d = {"Q": Q, "K": K, "V": V}
+            for Lq_u in (64, 128, 256, 512):
+                res = self_target_run(p, d, x, x, O, flush, stream, dev, Lq_u=Lq_u)
+                res.update({"sweep": "self_target", "n_cand": x.n_cand, "n_users": x.n_users, "Lq": x.Lq,
+                            "Lkv": x.Lkv, "fused_over_separate": res["fused_us"] / res["separate_us"]})
+                print(json.dumps(res), flush=True)
         del Q, K, V, m, O
     # the stress request: Zipf(1.1) candidates per user, permuted map, jagged
     # per-user histories packed with int32 offsets
@@ -515,7 +640,8 @@ def run_sweep(args):
     fl = acc.attn_flops(x.H, x.Lq, x.d, lens[x.map.long()].tolist())
     byt = acc.attn_bytes(x.n_cand, x.H, x.Lq, x.d, int(x.kv_offsets[-1]))
     t_roof = max(byt / (pk["hbm_gbs"] * 1e9), fl / (pk["bf16_tflops"] * 1e12))
-    print(json.dumps({"sweep": "attn_stress", "n_cand": x.n_cand, "n_users": x.n_users, "Lq": x.Lq,
+    cpu = oracle_attn_time(x) if args.cpu_seconds > 0 else None
+    print(json.dumps({"sweep": "attn_stress", "n_cand": x.n_cand, "n_users": x.n_users, "Lq": x.Lq, "cpu_oracle": cpu,
                       "kv_rows": int(x.kv_offsets[-1]), "us": us, "roofline_us": t_roof * 1e6,
                       "frac": t_roof * 1e6 / us, "tflops": fl / (us * 1e-6) / 1e12,
                       "status": B.ikbo_status_string(st)}), flush=True)
@@ -710,8 +836,8 @@ def attn_backward_run(plan, d, x, a, O, flush, stream, dev, pk, iters=20):
 def self_target_run(plan, d, x, a, O, flush, stream, dev, Lq_u=64, iters=20):
     """The request's target attention plus each user's own Lq_u queries over
     the same K/V: one launch (ikbo_attn_self_target_forward) against two
-    (ikbo_attn_forward for the target part, then for the self part through
-    a plan whose map is the identity over users)."""
+    (ikbo_attn_forward for the target part, then the self part alone:
+    ikbo_attn_self_target_forward without Q and O)."""
     import statistics
     import torch
     from broadcast_gemm_attention_gb300 import binding as B
@@ -719,9 +845,6 @@ def self_target_run(plan, d, x, a, O, flush, stream, dev, Lq_u=64, iters=20):
     Qu = gen.make_user_queries(1093, x.n_users, a.H, Lq_u, a.d).to(dev)
     Ou = torch.empty_like(Qu)
     Ou2 = torch.empty_like(Qu)
-    ident = torch.arange(x.n_users, dtype=torch.int32, device=dev)
-    plan_u = B.Plan(x.n_users, x.n_users, a.H)
-    plan_u.plan(ident, x.n_users, a.H, Lq_u, stream)
 
     def timed(fn):
         ts = []
@@ -739,10 +862,10 @@ def self_target_run(plan, d, x, a, O, flush, stream, dev, Lq_u=64, iters=20):
     fused, fused_mean = timed(lambda: plan.attn_self_target_forward(d["Q"], Qu, d["K"], d["V"], None, O, Ou, None,
                                                                     stream))
     sep, sep_mean = timed(lambda: (plan.attn_forward(d["Q"], d["K"], d["V"], None, O, None, stream),
-                                   plan_u.attn_forward(Qu, d["K"], d["V"], None, Ou2, None, stream)))
+                                   plan.attn_self_target_forward(None, Qu, d["K"], d["V"], None, None, Ou2, None,
+                                                                 stream)))
     st = plan.status()
     same = bool(torch.equal(Ou, Ou2))
-    plan_u.close()
     flops = 4.0 * a.H * a.d * a.Lkv * (x.n_cand * a.Lq + x.n_users * Lq_u)
     return {"Lq_u": Lq_u, "fused_us": fused, "separate_us": sep, "fused_mean_us": fused_mean,
             "separate_mean_us": sep_mean, "fused_tflops": flops / (fused * 1e-6) / 1e12,

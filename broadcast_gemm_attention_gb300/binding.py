@@ -309,21 +309,27 @@ def ikbo_attn_self_target_forward(plan: int, Q: torch.Tensor, Q_user: torch.Tens
                                   V: torch.Tensor, kv_offsets: Optional[torch.Tensor], O: torch.Tensor,
                                   O_user: torch.Tensor, scale: Optional[float] = None, stream=None) -> None:
     """Target attention (as ikbo_attn_forward) and the users' own queries
-    O_user[u,h] = softmax(Q_user[u,h] K[u,h]^T scale) V[u,h], in one launch."""
+    O_user[u,h] = softmax(Q_user[u,h] K[u,h]^T scale) V[u,h], in one launch.
+    Q and O both None: the self part alone."""
     bf = torch.bfloat16
-    d = Q.shape[-1]
+    d = Q_user.shape[-1]
     if kv_offsets is None:
         Lkv = K.shape[2]
         optr = None
     else:
         Lkv = K.shape[0]
         optr = _dev(kv_offsets, torch.int32, "kv_offsets")
-    if K.shape != V.shape or O.shape != Q.shape or O_user.shape != Q_user.shape or Q_user.dim() != 4:
+    if (Q is None) != (O is None):
+        raise ValueError("Q and O are given together or not at all")
+    if K.shape != V.shape or (Q is not None and O.shape != Q.shape) or O_user.shape != Q_user.shape \
+            or Q_user.dim() != 4:
         raise ValueError("shape mismatch among Q/O, Q_user/O_user, K/V")
     if scale is None:
         scale = 1.0 / math.sqrt(d)
-    _check(load().ikbo_attn_self_target_forward(plan, _dev(Q, bf, "Q"), _dev(Q_user, bf, "Q_user"), _dev(K, bf, "K"),
-                                                _dev(V, bf, "V"), optr, _dev(O, bf, "O"), _dev(O_user, bf, "O_user"),
+    qp = None if Q is None else _dev(Q, bf, "Q")
+    op = None if O is None else _dev(O, bf, "O")
+    _check(load().ikbo_attn_self_target_forward(plan, qp, _dev(Q_user, bf, "Q_user"), _dev(K, bf, "K"),
+                                                _dev(V, bf, "V"), optr, op, _dev(O_user, bf, "O_user"),
                                                 Q_user.shape[2], Lkv, d, float(scale), _stream(stream)),
            "ikbo_attn_self_target_forward")
 

@@ -60,7 +60,7 @@ struct ikbo_plan_s {
   int32_t* d_work = nullptr;
   int32_t* d_n_units = nullptr;
   int64_t max_units = 0;
-  uint32_t* d_status = nullptr;  // [0] status bits, [1] LCE flag-timeout epoch
+  uint32_t* d_status = nullptr;  // [0] status bits, [1] LCE flag-timeout word, [2] LCE finished-CTA count
   float* d_partial = nullptr;
   size_t partial_elems = 0;
   uint32_t* d_flags = nullptr;
@@ -81,7 +81,7 @@ struct ikbo_plan_s {
   size_t abwd_drow_elems = 0;
   int32_t* d_abwd_blk = nullptr;
   size_t abwd_blk_elems = 0;
-  uint32_t epoch = 0;
+  bool lce_flags_dirty = false;  // an LCE launch failed: its flags may still be set
   uint32_t debug = 0;
   uint64_t timeout_ns = 2000000000ull;
   int lce_schedule = LCE_SCHEDULE_AUTO;
@@ -129,15 +129,18 @@ bool encode_bf16(CUtensorMap* m, const void* base, int rank, const uint64_t* dim
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Grows a plan workspace to `need` elements.  New memory is zeroed on
+// `stream`, the stream of the call that will use it, so the clear is ordered
+// before that call's kernels.
 template <typename T>
-cudaError_t grow(T** ptr, size_t* have, size_t need) {
+cudaError_t grow(T** ptr, size_t* have, size_t need, cudaStream_t stream) {
   if (*have >= need && *ptr) return cudaSuccess;
   if (*ptr) cudaFree(*ptr);
   *ptr = nullptr;
   *have = 0;
   cudaError_t e = cudaMalloc(reinterpret_cast<void**>(ptr), need * sizeof(T));
   if (e != cudaSuccess) return e;
-  e = cudaMemset(*ptr, 0, need * sizeof(T));
+  e = cudaMemsetAsync(*ptr, 0, need * sizeof(T), stream);
   if (e != cudaSuccess) return e;
   *have = need;
   return cudaSuccess;
@@ -196,14 +199,22 @@ ikbo_status_t lce_launch(ikbo_plan_t p, const void* U, const void* C, const void
 
   const size_t part = static_cast<size_t>(p->n_users) * N * D;
   const size_t nflags = lce_flag_count(lp);
-  if (grow(&p->d_partial, &p->partial_elems, part) != cudaSuccess) return IKBO_ERR_CUDA;
-  if (grow(&p->d_flags, &p->flags_elems, nflags) != cudaSuccess) return IKBO_ERR_CUDA;
+  if (grow(&p->d_partial, &p->partial_elems, part, stream) != cudaSuccess) return IKBO_ERR_CUDA;
+  if (grow(&p->d_flags, &p->flags_elems, nflags, stream) != cudaSuccess) return IKBO_ERR_CUDA;
+  if (p->lce_flags_dirty) {  // a failed launch may have left flags set: clear them, the timeout word and the count
+    if (cudaMemsetAsync(p->d_flags, 0, sizeof(uint32_t) * p->flags_elems, stream) != cudaSuccess ||
+        cudaMemsetAsync(p->d_status + 1, 0, 2 * sizeof(uint32_t), stream) != cudaSuccess)
+      return IKBO_ERR_CUDA;
+    p->lce_flags_dirty = false;
+  }
+  lp.U = static_cast<const uint16_t*>(U);
+  lp.Wu = static_cast<const uint16_t*>(Wu);
   lp.partial = p->d_partial;
   lp.flags = p->d_flags;
   lp.status = p->d_status;
   lp.timeout_epoch = p->d_status + 1;
-  lp.epoch = ++p->epoch;
-  if (lp.epoch == 0) lp.epoch = ++p->epoch;  // 0 is the flags' initial value
+  lp.done = p->d_status + 2;
+  lp.epoch = LCE_FLAG_READY;  // the flags are back at zero after every call
   lp.debug = p->debug;
   lp.schedule = p->lce_schedule;
   lp.timeout_ns = p->timeout_ns;
@@ -225,6 +236,7 @@ ikbo_status_t lce_launch(ikbo_plan_t p, const void* U, const void* C, const void
   int launches = 0;
   const cudaError_t e = launch_lce_stage(tmU, tmC, tmWu, tmWc, lp, stage, p->num_sms, stream, &launches);
   p->launches += static_cast<uint64_t>(launches);
+  if (e != cudaSuccess) p->lce_flags_dirty = true;
   return e == cudaSuccess ? IKBO_OK : IKBO_ERR_CUDA;
 }
 }  // namespace
@@ -237,11 +249,13 @@ ikbo_status_t attn_launch(ikbo_plan_t p, const void* Q, const void* Q_user, cons
                           float scale, cudaStream_t stream) {
   if (!p) return IKBO_ERR_INVALID_ARG;
   if (!p->planned) return IKBO_ERR_NOT_PLANNED;
-  if (!Q || !K || !V || !O) return IKBO_ERR_INVALID_ARG;
-  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O)) return IKBO_ERR_INVALID_ARG;
+  const bool self = Q_user != nullptr;
+  const bool self_only = self && !Q && !O && !lse;  // the users' own queries alone
+  if (!K || !V || (!self_only && (!Q || !O))) return IKBO_ERR_INVALID_ARG;
+  if (!aligned16(K) || !aligned16(V) || (!self_only && (!aligned16(Q) || !aligned16(O))))
+    return IKBO_ERR_INVALID_ARG;
   if (d != ATT_D) return IKBO_ERR_UNSUPPORTED;
   if (Lkv < 1 || !(scale > 0.f) || !std::isfinite(scale)) return IKBO_ERR_INVALID_ARG;
-  const bool self = Q_user != nullptr;
   if (self) {
     if (!O_user || !aligned16(Q_user) || !aligned16(O_user) || Lq_u < 1) return IKBO_ERR_INVALID_ARG;
     if (Lq_u % 8 != 0) return IKBO_ERR_UNSUPPORTED;
@@ -271,7 +285,8 @@ ikbo_status_t attn_launch(ikbo_plan_t p, const void* Q, const void* Q_user, cons
   const uint64_t qd[4] = {ATT_D, Lq, H, static_cast<uint64_t>(p->n_cand)};
   const uint64_t qs[3] = {ATT_D * 2, Lq * ATT_D * 2, H * Lq * ATT_D * 2};
   const uint32_t qbox[4] = {64, static_cast<uint32_t>(p->Lq), 1, 1};
-  if (!encode_bf16(&tmQ, Q, 4, qd, qs, qbox)) return IKBO_ERR_CUDA;
+  ap.self_only = self_only ? 1 : 0;
+  if (!self_only && !encode_bf16(&tmQ, Q, 4, qd, qs, qbox)) return IKBO_ERR_CUDA;
   if (self) {
     ap.O_user = static_cast<uint16_t*>(O_user);
     ap.Lq_u = Lq_u;
@@ -283,6 +298,7 @@ ikbo_status_t attn_launch(ikbo_plan_t p, const void* Q, const void* Q_user, cons
     const uint64_t us[3] = {ATT_D * 2, Lu * ATT_D * 2, H * Lu * ATT_D * 2};
     const uint32_t ubox[4] = {64, static_cast<uint32_t>(ap.self_rows), 1, 1};
     if (!encode_bf16(&tmQu, Q_user, 4, ud, us, ubox)) return IKBO_ERR_CUDA;
+    if (self_only) tmQ = tmQu;  // no target units read it
   } else {
     tmQu = tmQ;  // not read without self units
   }
@@ -320,9 +336,9 @@ ikbo_status_t attn_backward_launch(ikbo_plan_t p, const void* Q, const void* K, 
   // per work unit, its 128 tile rows' LSE and D (the work list holds at most
   // max_units units); the two user prefixes (key blocks, query tiles)
   const size_t rows = static_cast<size_t>(p->max_units) * ATT_BM;
-  if (grow(&p->d_abwd_lse, &p->abwd_lse_elems, rows) != cudaSuccess ||
-      grow(&p->d_abwd_drow, &p->abwd_drow_elems, rows) != cudaSuccess ||
-      grow(&p->d_abwd_blk, &p->abwd_blk_elems, 2 * (static_cast<size_t>(p->n_users) + 1)) != cudaSuccess)
+  if (grow(&p->d_abwd_lse, &p->abwd_lse_elems, rows, stream) != cudaSuccess ||
+      grow(&p->d_abwd_drow, &p->abwd_drow_elems, rows, stream) != cudaSuccess ||
+      grow(&p->d_abwd_blk, &p->abwd_blk_elems, 2 * (static_cast<size_t>(p->n_users) + 1), stream) != cudaSuccess)
     return IKBO_ERR_CUDA;
 
   AttnBwdParams bp;
@@ -438,8 +454,8 @@ ikbo_status_t ikbo_plan_create(ikbo_plan_t* out, int max_cand, int max_users, in
             cudaMalloc(&p->d_perm, sizeof(int32_t) * max_cand) == cudaSuccess &&
             cudaMalloc(&p->d_work, sizeof(int32_t) * 4 * p->max_units) == cudaSuccess &&
             cudaMalloc(&p->d_n_units, sizeof(int32_t)) == cudaSuccess &&
-            cudaMalloc(&p->d_status, sizeof(uint32_t) * 2) == cudaSuccess &&
-            cudaMemset(p->d_status, 0, sizeof(uint32_t) * 2) == cudaSuccess &&
+            cudaMalloc(&p->d_status, sizeof(uint32_t) * 3) == cudaSuccess &&
+            cudaMemset(p->d_status, 0, sizeof(uint32_t) * 3) == cudaSuccess &&
             cudaMemset(p->d_n_units, 0, sizeof(int32_t)) == cudaSuccess;
   if (!ok) {
     free_plan(p);
@@ -593,15 +609,15 @@ ikbo_status_t ikbo_lce_backward(ikbo_plan_t p, const void* U, const void* C, con
     sp.slices = (ND + BWD_SEG_SLICE - 1) / BWD_SEG_SLICE;
     sp.NPD = NP * D;
     const size_t nS = static_cast<size_t>(n_users) * ND;
-    if (grow(&p->d_bwd_S, &p->bwd_S_elems, nS) != cudaSuccess ||
-        grow(&p->d_bwd_Sb, &p->bwd_Sb_elems, static_cast<size_t>(n_users) * 2 * NP * D) != cudaSuccess)
+    if (grow(&p->d_bwd_S, &p->bwd_S_elems, nS, stream) != cudaSuccess ||
+        grow(&p->d_bwd_Sb, &p->bwd_Sb_elems, static_cast<size_t>(n_users) * 2 * NP * D, stream) != cudaSuccess)
       return IKBO_ERR_CUDA;
-    if (sp.nch > 1 && grow(&p->d_bwd_seg, &p->bwd_seg_elems, nS * sp.nch) != cudaSuccess) return IKBO_ERR_CUDA;
+    if (sp.nch > 1 && grow(&p->d_bwd_seg, &p->bwd_seg_elems, nS * sp.nch, stream) != cudaSuccess) return IKBO_ERR_CUDA;
   }
   size_t wpart = 0;
   if (dWc) wpart = bwd_wgrad_part_elems(wc);
   if (dWu && bwd_wgrad_part_elems(wu) > wpart) wpart = bwd_wgrad_part_elems(wu);
-  if (wpart && grow(&p->d_bwd_wpart, &p->bwd_wpart_elems, wpart) != cudaSuccess) return IKBO_ERR_CUDA;
+  if (wpart && grow(&p->d_bwd_wpart, &p->bwd_wpart_elems, wpart, stream) != cudaSuccess) return IKBO_ERR_CUDA;
 
   // tensor maps: [B][rows][D] operands with 64-wide boxes along D (rows 64 or
   // 128 high), and the weights as [M][N] with 64-wide boxes along N

@@ -748,7 +748,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
   const AttSmem s = carve(smem_raw + pad);
   const int warp = threadIdx.x >> 5;
   UnitCount n_units;  // work-list units, then self units
-  n_units.target = *p.n_units;
+  n_units.target = (kSelf && p.self_only) ? 0 : *p.n_units;
   n_units.total = n_units.target + (kSelf ? p.n_self : 0);
 
   if (threadIdx.x == 0) {

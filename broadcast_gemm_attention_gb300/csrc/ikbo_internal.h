@@ -60,11 +60,16 @@ struct LceParams {
   const int32_t* seg_offsets;  // [n_users + 1] where each user's run starts in order, or null
   const int32_t* seg_runs;     // [n_users + 1] non-empty runs before each user (and in all), or null
   const uint16_t* bias;   // [N] bf16 or null
+  const uint16_t* U;      // [n_users][K_u][D] bf16 (read through tmU; raw for the CUDA-core fallback)
+  const uint16_t* Wu;     // [K_u][N] bf16 (likewise)
   uint16_t* Y;            // [n_cand][N][D] bf16
   float* partial;         // [n_users][N][D] fp32 workspace (user GEMM + bias)
-  uint32_t* flags;        // [n_users][n_dblk][NB] readiness epochs (one per user tile)
+  uint32_t* flags;        // [n_users][n_dblk][NB] readiness (one per user tile): `epoch` once published,
+                          // 0 between calls (the launch that reads them clears them as it ends)
   uint32_t* status;
-  uint32_t* timeout_epoch;  // set to `epoch` by the first flag wait that times out in a launch
+  uint32_t* timeout_epoch;  // set to `epoch` by the first flag wait that times out in a launch (cleared
+                            // with the flags)
+  uint32_t* done;         // CTAs of the flag-reading launch that have finished (0 between calls)
   int n_cand, n_users, K_u, K_c, D, N;
   int N_mma;              // N rounded up to 16
   int NB;                 // 64-wide column blocks of W (ceil(N_mma / 64))
@@ -78,7 +83,7 @@ struct LceParams {
   int w_slots;            // 8 KB W_u slots in the W region used by user tiles (2..8)
   int wu_slots;           // full-width W_u chunk slots after the A ring (local-partial schedule only, else 0)
   uint32_t w_region_bytes;
-  uint32_t epoch;         // value written to / awaited in `flags`
+  uint32_t epoch;         // value written to / awaited in `flags` (LCE_FLAG_READY)
   uint32_t debug;
   uint32_t mode;          // LCE_MODE_* bits: the stage-ladder ablations (0 = the full kernel)
   int schedule;           // LCE_SCHEDULE_*: one launch or two (plan-time choice by default)
@@ -104,6 +109,10 @@ enum : int {
   LCE_SCHEDULE_LOCAL = 3,  // one launch of candidate tiles; each CTA computes the user partials its
                            // own tiles need, into TMEM (N <= 192)
 };
+// Value of a published readiness flag.  Flags are zero before every call
+// (cleared by the last CTA of the launch that reads them), so a fixed value
+// serves every call.
+constexpr uint32_t LCE_FLAG_READY = 1;
 // AUTO takes one launch below this many candidate tiles per SM.
 constexpr int LCE_ONE_LAUNCH_TILES_PER_SM = 8;
 constexpr int LCE_WU_SLOTS = 2;     // W_u chunk slots of the local-partial schedule
@@ -214,6 +223,7 @@ struct AttnParams {
   // list's units: n_self = n_users * H * self_tiles, 0 if none
   uint16_t* O_user;          // [n_users][H][Lq_u][d]
   int n_self, self_tiles, self_rows, Lq_u;  // self_rows = query rows per self tile (<= 128)
+  int self_only;             // 1: skip the work list's units (the self part alone)
 };
 
 // ------------------------------------------------- attention backward

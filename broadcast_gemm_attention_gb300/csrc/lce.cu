@@ -545,6 +545,29 @@ __device__ __forceinline__ bool wait_all_user_partials(const LceParams& p) {
   return true;
 }
 
+// The user partial P[u][n][d] = b[n] + sum_k Wu[k][n] U[u][k][d] for the 32
+// columns n0 .. n0+31 of row d, on the CUDA cores (fp32, ascending k).  Only
+// for candidate tiles whose user tiles never published within the wait
+// bound: the tile then still writes its Y, from this slower copy of the
+// partial (another summation order than the tensor cores', same inputs).
+__device__ __noinline__ void user_partial_cuda_cores(const LceParams& p, int u, int d, int n0, float* out) {
+#pragma unroll 1
+  for (int j = 0; j < 32; ++j) {
+    const int n = n0 + j;
+    out[j] = (p.bias && n < p.N) ? __bfloat162float(__ushort_as_bfloat16(__ldg(p.bias + n))) : 0.f;
+  }
+  if (d >= p.D) return;
+  const uint16_t* ur = p.U + static_cast<size_t>(u) * p.K_u * p.D + d;
+#pragma unroll 1
+  for (int k = 0; k < p.K_u; ++k) {
+    const float a = __bfloat162float(__ushort_as_bfloat16(__ldg(ur + static_cast<size_t>(k) * p.D)));
+    const uint16_t* w = p.Wu + static_cast<size_t>(k) * p.N + n0;
+#pragma unroll 4
+    for (int j = 0; j < 32; ++j)
+      if (n0 + j < p.N) out[j] = fmaf(__bfloat162float(__ushort_as_bfloat16(__ldg(w + j))), a, out[j]);
+  }
+}
+
 // ------------------------------------------------------------ epilogue
 // Eight warps: warp w reads TMEM lane quarter w % 4 (rows 32*(w%4) .. +31 of
 // the D block) and every other 32-column chunk, starting at (w - 4) / 4.
@@ -656,8 +679,10 @@ __device__ void lce_epilogue(const LceParams& p, const LceSmem& s, uint32_t tmem
       const bool uok = u >= 0 && u < p.n_users;
       if (!uok && leader) atomicOr(p.status, DEV_ERR_MAP_RANGE);
       if (kPhase != LCE_PHASE_LOCAL && add_p && users_ready < 0) users_ready = wait_all_user_partials(p) ? 1 : 0;
+      // the partials never came (the wait ran out): this CTA forms them itself
+      const bool fallback = kPhase != LCE_PHASE_LOCAL && add_p && users_ready == 0;
       // local partials: the walk put this (user, D block)'s own tile just before
-      bool ready = uok && (kPhase == LCE_PHASE_LOCAL || !add_p || users_ready == 1);
+      bool ready = uok && (kPhase == LCE_PHASE_LOCAL || !add_p || users_ready == 1 || fallback);
       if (kPhase == LCE_PHASE_LOCAL && ready && (pre_u != u || pre_dblk != x.dblk)) {
         if (leader) atomicOr(p.status, DEV_ERR_BAD_WORK);
         ready = false;
@@ -676,6 +701,13 @@ __device__ void lce_epilogue(const LceParams& p, const LceSmem& s, uint32_t tmem
 #pragma unroll
         for (int k = 0; k < EPI_PREFETCH; ++k) {
           const int c = half + 2 * k;
+          if (fallback) {
+            float t[32];
+            if (c < nchunks) user_partial_cuda_cores(p, u, d, c * 32, t);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) pre[k][j] = (c * 32 + j < p.N && dok) ? t[j] : 0.f;
+            continue;
+          }
           const float* pp = P + static_cast<size_t>(c * 32) * p.D;
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
@@ -707,9 +739,16 @@ __device__ void lce_epilogue(const LceParams& p, const LceSmem& s, uint32_t tmem
           tmem_ld32(t_acc + c * 32, v);
           float pu[32];
           const float* pp = P + static_cast<size_t>(c * 32) * p.D;
+          if (fallback) {
+            float t[32];
+            user_partial_cuda_cores(p, u, d, c * 32, t);
 #pragma unroll
-          for (int j = 0; j < 32; ++j)
-            pu[j] = (add_p && c * 32 + j < p.N && dok) ? __ldcg(pp + static_cast<size_t>(j) * p.D) : 0.f;
+            for (int j = 0; j < 32; ++j) pu[j] = t[j];
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              pu[j] = (add_p && c * 32 + j < p.N && dok) ? __ldcg(pp + static_cast<size_t>(j) * p.D) : 0.f;
+          }
           tmem_ld_wait(v);
           __nv_bfloat16* y = Y + static_cast<size_t>(c * 32) * p.D;
 #pragma unroll
@@ -730,8 +769,12 @@ __device__ void lce_epilogue(const LceParams& p, const LceSmem& s, uint32_t tmem
 // candidate tiles, which acquire the flags and add P in their epilogue -- or
 // as one (LCE_PHASE_BOTH: user tiles first in every CTA's list;
 // LCE_PHASE_LOCAL: candidate tiles with each CTA's own user partials).  The grid
-// never exceeds the SM count and takes one CTA per SM, so every CTA is
-// resident and a flag wait always ends.
+// never exceeds the SM count and takes one CTA per SM.  LCE_PHASE_BOTH is
+// launched cooperatively, so its CTAs are resident together and a flag wait
+// ends once the user tiles are done; LCE_PHASE_CAND waits only for flags of
+// the launch before it.  A wait that still runs out (the debug switch that
+// withholds the partials) is reported, and the waiting tiles form the
+// partial on the CUDA cores instead.
 template <int kPhase>
 __global__ void __launch_bounds__(LCE_THREADS, 1)
     lce_kernel(const __grid_constant__ CUtensorMap tmU, const __grid_constant__ CUtensorMap tmC,
@@ -812,6 +855,26 @@ __global__ void __launch_bounds__(LCE_THREADS, 1)
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
+  // The launch that reads the readiness flags returns them (and the timeout
+  // word) to zero for the next call: the last of its CTAs to finish, after
+  // every other CTA has stopped reading them, clears them.
+  if (kPhase == LCE_PHASE_CAND || kPhase == LCE_PHASE_BOTH) {
+    __shared__ uint32_t last_cta;
+    if (threadIdx.x == 0) {
+      __threadfence();
+      last_cta = atomicAdd(p.done, 1u) == gridDim.x - 1 ? 1u : 0u;
+    }
+    __syncthreads();
+    if (last_cta) {
+      __threadfence();
+      for (int k = static_cast<int>(threadIdx.x); k < p.n_user_units; k += static_cast<int>(blockDim.x))
+        p.flags[k] = 0;
+      if (threadIdx.x == 0) {
+        *p.timeout_epoch = 0;
+        *p.done = 0;
+      }
+    }
+  }
 }
 
 }  // namespace
@@ -862,17 +925,35 @@ size_t lce_smem_bytes(const LceParams& p) {
          static_cast<size_t>(p.wu_slots) * p.NB * BOX_BYTES + bars;
 }
 
+// `cooperative`: launched so that all CTAs are resident at once, or not at
+// all (cudaErrorCooperativeLaunchTooLarge, e.g. when fewer SMs are available
+// to this context than the device has): required by the one-launch
+// schedule, whose candidate tiles wait for user tiles of other CTAs.
 template <int kPhase>
 cudaError_t launch_phase(const CUtensorMap& tmU, const CUtensorMap& tmC, const CUtensorMap& tmWu,
-                         const CUtensorMap& tmWc, const LceParams& p, int units, int num_sms, cudaStream_t s) {
+                         const CUtensorMap& tmWc, const LceParams& p, int units, int num_sms, cudaStream_t s,
+                         bool cooperative = false) {
   if (units <= 0) return cudaSuccess;
   const size_t smem = lce_smem_bytes(p);
   cudaError_t e = cudaFuncSetAttribute(lce_kernel<kPhase>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   const int grid = units < num_sms ? units : num_sms;
-  lce_kernel<kPhase><<<grid, LCE_THREADS, smem, s>>>(tmU, tmC, tmWu, tmWc, p);
-  return cudaGetLastError();
+  if (!cooperative) {
+    lce_kernel<kPhase><<<grid, LCE_THREADS, smem, s>>>(tmU, tmC, tmWu, tmWc, p);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(LCE_THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, lce_kernel<kPhase>, tmU, tmC, tmWu, tmWc, p);
 }
 
 int lce_resolve_schedule(const LceParams& p, int num_sms) {
@@ -909,7 +990,9 @@ cudaError_t launch_lce(const CUtensorMap& tmU, const CUtensorMap& tmC, const CUt
   }
   if (schedule == LCE_SCHEDULE_ONE) {
     *launches = 1;
-    return launch_phase<LCE_PHASE_BOTH>(tmU, tmC, tmWu, tmWc, p, p.n_units, num_sms, s);
+    const cudaError_t e = launch_phase<LCE_PHASE_BOTH>(tmU, tmC, tmWu, tmWc, p, p.n_units, num_sms, s, true);
+    if (e != cudaErrorCooperativeLaunchTooLarge) return e;
+    (void)cudaGetLastError();  // not all CTAs could be resident: two launches need no co-residency
   }
   *launches = 2;
   cudaError_t e = launch_phase<LCE_PHASE_USER>(tmU, tmC, tmWu, tmWc, p, p.n_user_units, num_sms, s);

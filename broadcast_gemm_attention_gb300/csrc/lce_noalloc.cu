@@ -15,9 +15,10 @@
 // host-side name is only a stand-in, so the device address is fetched with
 // cudaGetSymbolAddress, once per device, on the first call made while that
 // device is current; make that first call before capturing any stream.
-// All calls share the array and it keeps the last call's contents; calls
-// that overlap on the GPU (two streams, or two host threads on one device)
-// race on it.
+// All calls share the array and it keeps the last call's contents: each call
+// first clears, on its stream, the words that must start at zero (status,
+// readiness flags).  Calls that overlap on the GPU (two streams, or two host
+// threads on one device) race on it.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -40,7 +41,7 @@ namespace {
 // 16 MiB: room for the user partials of n_users * N * D <= ~4.19 M fp32
 // values (for example 80 users at N = 192, D = 256) plus their flags.
 constexpr size_t kNoallocScratchBytes = size_t(16) << 20;
-constexpr size_t kControlBytes = 256;  // [0] status bits, [1] flag-timeout epoch
+constexpr size_t kControlBytes = 256;  // [0] status bits, [1] flag-timeout word, [2] finished-CTA count
 constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_lce_scratch[kNoallocScratchBytes];
@@ -50,7 +51,6 @@ struct DeviceSlot {
   unsigned char* scratch = nullptr;  // device address of g_lce_scratch on this device
   int num_sms = 0;
   size_t max_smem = 0;
-  uint32_t epoch = 0;  // last readiness-flag value handed out on this device
 };
 
 std::mutex g_mu;
@@ -149,32 +149,32 @@ extern "C" ikbo_status_t ikbo_lce_forward_noalloc(const int32_t* d_map, int n_ca
   // shapes only here; the shared-memory limit is checked once the device is known
   if (!lce_configure(&lp, SIZE_MAX)) return IKBO_ERR_UNSUPPORTED;
 
-  // scratch layout: control words | flags [n_users][n_dblk] | partial [n_users][N][D] fp32
+  // scratch layout: control words | flags [n_users][n_dblk][NB] | partial [n_users][N][D] fp32
   const size_t flag_bytes = round256(sizeof(uint32_t) * lce_flag_count(lp));
   const size_t part_bytes = sizeof(float) * static_cast<size_t>(n_users) * N * D;
   if (kControlBytes + flag_bytes + part_bytes > kNoallocScratchBytes) return IKBO_ERR_UNSUPPORTED;
 
-  uint32_t epoch = 0;
   DeviceSlot* slot = nullptr;
   {
     std::lock_guard<std::mutex> g(g_mu);
     cudaError_t e;
     slot = device_slot(&e);
     if (!slot) return IKBO_ERR_CUDA;
-    epoch = ++slot->epoch;
-    if (epoch == 0) epoch = ++slot->epoch;  // flags start at zero; zero is never a live epoch
   }
   if (!lce_configure(&lp, slot->max_smem)) return IKBO_ERR_UNSUPPORTED;
 
   unsigned char* base = slot->scratch;
   lp.map = d_map;
   lp.bias = static_cast<const uint16_t*>(b);
+  lp.U = static_cast<const uint16_t*>(U);
+  lp.Wu = static_cast<const uint16_t*>(Wu);
   lp.Y = static_cast<uint16_t*>(Y);
   lp.status = reinterpret_cast<uint32_t*>(base);
   lp.timeout_epoch = reinterpret_cast<uint32_t*>(base) + 1;
+  lp.done = reinterpret_cast<uint32_t*>(base) + 2;
   lp.flags = reinterpret_cast<uint32_t*>(base + kControlBytes);
   lp.partial = reinterpret_cast<float*>(base + kControlBytes + flag_bytes);
-  lp.epoch = epoch;  // flags from earlier calls hold older epochs, so they need no clearing
+  lp.epoch = LCE_FLAG_READY;
   lp.debug = 0;
   lp.timeout_ns = 2000000000ull;
 
@@ -192,8 +192,9 @@ extern "C" ikbo_status_t ikbo_lce_forward_noalloc(const int32_t* d_map, int n_ca
       !tensor_map(&tmWu, Wu, 2, wud, ws, wbox) || !tensor_map(&tmWc, Wc, 2, wcd, ws, wbox))
     return IKBO_ERR_CUDA;
 
-  // the status words must start at zero for this call (the flags do not: see epoch)
-  if (cudaMemsetAsync(base, 0, 2 * sizeof(uint32_t), stream) != cudaSuccess) return IKBO_ERR_CUDA;
+  // the control words and the readiness flags start at zero on every call
+  // (an earlier call that did not finish cleanly may have left them set)
+  if (cudaMemsetAsync(base, 0, kControlBytes + flag_bytes, stream) != cudaSuccess) return IKBO_ERR_CUDA;
   int launches = 0;
   if (launch_lce(tmU, tmC, tmWu, tmWc, lp, slot->num_sms, stream, &launches) != cudaSuccess) return IKBO_ERR_CUDA;
   return IKBO_OK;

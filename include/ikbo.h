@@ -125,19 +125,22 @@ ikbo_status_t ikbo_lce_forward(ikbo_plan_t p, const void* U, const void* C, cons
  *   d_map   int32 [n_cand], values in [0, n_users)
  *   U, C, Wu, Wc, b, Y, K_u, K_c, D, N: exactly as ikbo_lce_forward
  * Limits: those of ikbo_lce_forward, and
- *   4 * n_users * N * D + 4 * n_users * ceil(D/128) (rounded up to 256) + 256
- *   <= 16 MiB, else IKBO_ERR_UNSUPPORTED before any launch.
+ *   4 * n_users * N * D
+ *   + 4 * n_users * ceil(D/128) * ceil(roundup(N,16)/64) (rounded up to 256)
+ *   + 256  <=  16 MiB, else IKBO_ERR_UNSUPPORTED before any launch.
  * Notes:
  *   - every GPU that loads the library holds the 16 MiB until process exit;
  *   - the first call made with a given device current looks up the array's
  *     device address (cudaGetSymbolAddress) and the device's limits; make
  *     that first call before capturing any stream;
- *   - all calls share the array and it keeps the last call's contents; the
- *     call clears the words that must start at zero itself (the readiness
- *     flags are per-call epochs and never need clearing); calls that overlap
- *     on the GPU (two streams, or two host threads on one device) race;
- *   - device-detected errors (map values out of range) are not reported:
- *     those candidates' rows of Y are left untouched. */
+ *   - all calls share the array and it keeps the last call's contents; each
+ *     call first clears, on its stream, the words that must start at zero
+ *     (status and readiness flags); calls that overlap on the GPU (two
+ *     streams, or two host threads on one device) race;
+ *   - device-detected errors are not reported: a candidate whose map value
+ *     is out of range keeps its rows of Y untouched, and a bounded wait that
+ *     runs out (which makes the waiting tiles form the user partial on the
+ *     CUDA cores, so Y stays right) goes unnoticed. */
 ikbo_status_t ikbo_lce_forward_noalloc(const int32_t* d_map, int n_cand, int n_users, const void* U, const void* C,
                                        const void* Wu, const void* Wc, const void* b, void* Y, int K_u, int K_c,
                                        int D, int N, cudaStream_t stream);
@@ -225,7 +228,9 @@ ikbo_status_t ikbo_attn_forward(ikbo_plan_t p, const void* Q, const void* K, con
  *   ikbo_attn_forward (the plan's map, n_users, H and Lq; K/V dense or
  *   jagged).  The target rows of O are bit-identical to ikbo_attn_forward's.
  *   The self units (n_users * H * ceil(Lq_u / 128) tiles of up to 128 query
- *   rows) follow the plan's work list in the persistent launch. */
+ *   rows) follow the plan's work list in the persistent launch.  Q and O both
+ *   NULL: the self part alone (the plan's map is then not read by the launch,
+ *   but n_users and H still come from the last ikbo_plan). */
 ikbo_status_t ikbo_attn_self_target_forward(ikbo_plan_t p, const void* Q, const void* Q_user, const void* K,
                                             const void* V, const int32_t* d_kv_offsets, void* O, void* O_user,
                                             int Lq_u, int Lkv, int d, float scale, cudaStream_t stream);
@@ -279,8 +284,9 @@ ikbo_status_t ikbo_plan_get_status(ikbo_plan_t p, cudaStream_t stream);
 
 /* Debug and robustness knobs.  flags: bit 0 = LCE user tiles compute but do
  * not publish their partials (candidate epilogues then wait, give up after
- * the timeout, skip their stores and report IKBO_ERR_TIMEOUT).  The timeout
- * bounds every wait inside the kernels (default 2 s). */
+ * the timeout, form the partial themselves on the CUDA cores, still write a
+ * correct Y, and the call reports IKBO_ERR_TIMEOUT).  The timeout bounds
+ * every wait inside the kernels (default 2 s). */
 ikbo_status_t ikbo_plan_set_debug(ikbo_plan_t p, unsigned flags);
 ikbo_status_t ikbo_plan_set_timeout_ns(ikbo_plan_t p, uint64_t timeout_ns);
 
@@ -292,7 +298,11 @@ ikbo_status_t ikbo_plan_set_timeout_ns(ikbo_plan_t p, uint64_t timeout_ns);
  *      request has fewer than 8 candidate tiles of 128 D-rows per SM, else 1
  *   1  two launches: user tiles (fp32 partials in the plan's workspace, with
  *      release flags), then candidate tiles
- *   2  one launch: user tiles first in every CTA's list
+ *   2  one launch: user tiles first in every CTA's list.  Its candidate
+ *      tiles wait for user tiles of other CTAs, so it is a cooperative
+ *      launch (all CTAs resident at once); where the context cannot hold
+ *      one CTA per SM of the device (fewer SMs available to it) it runs
+ *      as 1
  *   3  local partials, one launch: each CTA computes, into TMEM, the partial
  *      of every (user, 128-row D block) its candidate tiles need and keeps it
  *      in registers; no workspace and no hand-off between CTAs.  Applies when

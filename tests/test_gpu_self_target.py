@@ -6,14 +6,13 @@ path per unit); the users' own rows are ordinary attention of Q_user[u]
 against K[u], V[u], i.e. the oracle with the identity map over users.
 Tolerance: |O_gpu - O_ref| <= 2e-2 element-wise.
 """
-import numpy as np
 import pytest
 import torch
 
 import oracle
 from broadcast_gemm_attention_gb300 import binding as B
 from broadcast_gemm_attention_gb300 import inputs as gen
-from gpu_util import assert_attn_close, to_dev
+from gpu_util import assert_attn_close, check_attn_all, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -24,13 +23,16 @@ def run_both(x, Q_user, scale=None):
     O_sep = torch.full_like(Q, float("nan"))
     O = torch.full_like(Q, float("nan"))
     O_user = torch.full_like(Qu, float("nan"))
+    O_user_alone = torch.full_like(Qu, float("nan"))
     with B.Plan(x.n_cand, x.n_users, x.H) as p:
         p.plan(m, x.n_users, x.H, x.Lq)
         p.attn_forward(Q, K, V, offs, O_sep, scale)
         l0 = p.launches()
         p.attn_self_target_forward(Q, Qu, K, V, offs, O, O_user, scale)
         launched = p.launches() - l0
+        p.attn_self_target_forward(None, Qu, K, V, offs, None, O_user_alone, scale)  # the self part alone
         st = p.status()
+    assert torch.equal(O_user, O_user_alone), "self rows differ between the fused and the self-only launch"
     return O, O_user, O_sep, st, launched
 
 
@@ -62,17 +64,14 @@ def test_self_target_jagged_with_empty_user():
     check(x, 48, 91, scale=0.3)
 
 
-def test_self_target_70to1_sampled():
-    """The 70:1 request plus 64 user queries per (user, head); sampled rows."""
+def test_self_target_70to1_full():
+    """The 70:1 request plus 64 user queries per (user, head); every row."""
     x = gen.attn_70to1()
     Q_user = gen.make_user_queries(92, x.n_users, x.H, 64, x.d)
     O, O_user, O_sep, st, launched = run_both(x, Q_user)
     assert st == B.IKBO_OK and launched == 1
     assert torch.equal(O, O_sep)
-    rng = np.random.default_rng(11)
-    pairs = [(int(i), int(h)) for i, h in zip(rng.integers(0, x.n_cand, 16), rng.integers(0, x.H, 16))]
-    ref = oracle.attn(x.map, x.Q, x.K, x.V, pairs=pairs)
-    assert_attn_close(torch.stack([O[i, h] for i, h in pairs]), ref, "70:1 target")
+    check_attn_all(O, x, what="70:1 target", cache_key="attn_70to1")
     ident = torch.arange(x.n_users, dtype=torch.int32)
     ref_u = oracle.attn(ident, Q_user, x.K, x.V).reshape(O_user.shape)
     assert_attn_close(O_user, ref_u, "70:1 self")
@@ -90,5 +89,14 @@ def test_self_target_argument_validation():
         assert e.value.code == B.IKBO_ERR_UNSUPPORTED
         rc = B.load().ikbo_attn_self_target_forward(p.handle, Q.data_ptr(), None, K.data_ptr(), V.data_ptr(), None,
                                                     O.data_ptr(), None, 16, 64, 128, 0.1, None)
+        assert rc == B.IKBO_ERR_INVALID_ARG
+        Qu = torch.zeros(2, 1, 16, 128, dtype=torch.bfloat16, device="cuda")
+        Ou = torch.empty_like(Qu)
+        # Q without O (or O without Q) is an error; neither is the self part alone
+        rc = B.load().ikbo_attn_self_target_forward(p.handle, Q.data_ptr(), Qu.data_ptr(), K.data_ptr(), V.data_ptr(),
+                                                    None, None, Ou.data_ptr(), 16, 64, 128, 0.1, None)
+        assert rc == B.IKBO_ERR_INVALID_ARG
+        rc = B.load().ikbo_attn_self_target_forward(p.handle, None, Qu.data_ptr(), K.data_ptr(), V.data_ptr(),
+                                                    None, O.data_ptr(), Ou.data_ptr(), 16, 64, 128, 0.1, None)
         assert rc == B.IKBO_ERR_INVALID_ARG
         assert p.status() == B.IKBO_OK

@@ -5,9 +5,10 @@ It keeps its scratch in a fixed array inside the library.
 
 Checked through the C ABI against ikbo_lce_forward (the plan-based entry
 point) on two calls in a row, with the LCE tolerance used everywhere else:
-|Y_noalloc - Y_plan| <= 1e-2 (1 + |Y_plan|).  The file is named so that
-pytest collects it last; it also passes on its own in a fresh process (its
-first call then performs the per-device set-up).
+|Y_noalloc - Y_plan| <= 1e-2 (1 + |Y_plan|); and both calls against the
+fp64 oracle, every element.  The file is named so that pytest collects it
+last; it also passes on its own in a fresh process (its first call then
+performs the per-device set-up).
 """
 import numpy as np
 import pytest
@@ -15,6 +16,7 @@ import torch
 
 from broadcast_gemm_attention_gb300 import binding as B
 from broadcast_gemm_attention_gb300 import inputs as gen
+from gpu_util import check_lce_all
 
 pytestmark = pytest.mark.gpu
 
@@ -56,10 +58,12 @@ def test_noalloc_matches_plan_path_on_two_calls_in_a_row():
     b = gen.make_lce("noalloc_b", 4242, n_cand=300, n_users=7, K_u=101, K_c=77, D=136, N=40,
                      map_kind="permuted")                                    # ragged shapes, other map
     ref_a, ref_b = _plan_path(a), _plan_path(b)
-    y_a = _noalloc_path(a)   # first call (per-device set-up when run alone)
-    y_b = _noalloc_path(b)   # second call reuses the scratch left by the first
+    y_a = _noalloc_path(a)   # first call (per-device set-up when run alone); two launches
+    y_b = _noalloc_path(b)   # second call reuses the scratch left by the first; one launch
     _close(y_a, ref_a, "first call")
     _close(y_b, ref_b, "second call")
+    check_lce_all(y_a, a, what="no-alloc 70:1", cache_key="lce_70to1")
+    check_lce_all(y_b, b, what="no-alloc ragged")
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch():
