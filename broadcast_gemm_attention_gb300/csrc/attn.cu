@@ -23,31 +23,38 @@
 //   warp 3      TMA producer for V (2-stage ring).  K and V have rings and
 //               producers of their own so that a K load never queues
 //               behind a V load that waits for a P.V several tiles back.
-//   warps 4-11  softmax + epilogue.  Warps w and w+4 share the 32 TMEM lanes
-//               (query rows) of quarter w % 4 and split the 128 key columns
-//               of a tile (and the 128 d columns of O) into halves; they
-//               exchange their row maxima through shared memory.  Two warps
-//               per scheduler hide the exp2 / convert latency that one warp
-//               alone cannot.
-// TMEM (512 columns): S0 S1 (128 each, fp32), P (64, bf16 pairs), Q (64,
-// bf16 pairs), O (128, fp32).  A unit's O leaves through shared memory: a
-// thread owns a query row, so its direct stores would scatter 32 rows per
-// warp instruction; each warp writes its 32 rows x 64 d into its own 4 KB of
-// a staging tile and reads them back 4 rows per instruction, 8 lanes per
-// contiguous 128-byte half row.
+//   warps 4-11  softmax + epilogue, as two groups that ping-pong over the
+//               key tiles: group 0 (warps 4-7) takes the even tiles of the
+//               CTA's sequence (buffer S0), group 1 (warps 8-11) the odd
+//               ones (S1).  A warp owns the 32 TMEM lanes (query rows) of
+//               quarter w % 4 and all 128 columns of its tiles, so while one
+//               group waits on its tile's loads and handshakes the other
+//               group's exponentials keep the SFU busy on the same
+//               scheduler.  Both groups accumulate into one O: the row's
+//               reference maximum is a chain through the tiles, each tile's
+//               group reading the one before from the other group (one
+//               release / acquire word per row in shared memory).
+// TMEM (512 columns): S0 S1 (128 each, fp32), P0 P1 (64 each, bf16 pairs),
+// O (128, fp32).  Q stays in shared memory for all of a unit's S products
+// (two Q tiles: the next unit's lands while this one's are read), so S(j+2)
+// may be issued as soon as the softmax has read S(j), and P(j) only waits
+// for P.V(j-2) to have read P_b.  A unit's O leaves through shared memory,
+// in the finished unit's Q tile: a thread owns a query row, so its direct
+// stores would scatter 32 rows per warp instruction; each warp writes its 32
+// rows x 64 d into its own 4 KB of the staging tile and reads them back 4
+// rows per instruction, 8 lanes per contiguous 128-byte half row.
 //
-// Why two issuers and a separate P: one thread issues a tcgen05.mma only
-// every ~80-130 cycles, while an M=128, N=128, K=16 product needs 64 cycles
-// of the tensor pipe, so one chain of products leaves the pipe partly idle.
-// S(j+2) is issued as soon as the softmax has read S(j) out of its buffer
-// and P.V(j-1) as soon as P(j-1) is written, so the two chains overlap.
-// The first two S of a unit take Q from the landing buffer in shared memory
-// (the softmax warps copy it into TMEM meanwhile); later ones read it from
-// TMEM.
+// Why two issuers: one thread issues a tcgen05.mma only every ~80-130
+// cycles, while an M=128, N=128, K=16 product needs 64 cycles of the tensor
+// pipe, so one chain of products leaves the pipe partly idle.  S(j+2) is
+// issued as soon as the softmax has read S(j), and P.V(j) once P(j) is
+// written, so the two chains overlap each other and both softmax groups.
 //
 // Online softmax in fp32 in the log2 domain (exp2 with scale*log2(e) folded
-// in); the running max is only moved when it grows by more than 2^8, so O is
-// rescaled rarely (the result is the same: O and l share the reference max).
+// in); the running reference maximum is only moved when a tile's maximum
+// exceeds it by more than 2^8, so O is rescaled rarely (the result is the
+// same: O and l share the reference).  Each group keeps l over its own
+// tiles; the two are brought to the last reference and added at the end.
 #include <cuda_bf16.h>
 
 #include "ikbo_internal.h"
@@ -61,34 +68,37 @@ constexpr uint32_t HALF_TILE = ATT_BM * 64 * 2;  // 128 rows x 64 bf16 = 16 KB (
 constexpr float RESCALE_THRESHOLD = 8.0f;          // log2 units
 constexpr int SOFTMAX_WARP0 = 4;                   // first softmax warp
 constexpr int SOFTMAX_THREADS = ATT_THREADS - 32 * SOFTMAX_WARP0;
+constexpr int GROUP_THREADS = SOFTMAX_THREADS / 2;  // one softmax group (4 warps)
+constexpr int CTRL_REGS = 72;                       // per thread, warps 0-3 (after setmaxnreg)
+constexpr int SOFTMAX_REGS = 216;                   // per thread, warps 4-11
+static_assert(32 * SOFTMAX_WARP0 * CTRL_REGS + SOFTMAX_THREADS * SOFTMAX_REGS <= ATT_THREADS * 168,
+              "register split exceeds the launch's registers");
 constexpr uint32_t TM_S = 0;                       // S_b at TM_S + 128 b
-constexpr uint32_t TM_P = 256;
-constexpr uint32_t TM_Q = 320;
+constexpr uint32_t TM_P = 256;                     // P_b at TM_P + 64 b
 constexpr uint32_t TM_O = 384;
 
-// dynamic shared memory: [Q landing][K/V ring] (1024-aligned for the
-// 128-byte swizzle), then the barriers, two words, and the row exchange
-constexpr uint32_t TILE_REGION = ATT_Q_BUFS * ATT_Q_TILE_BYTES +
-                                 (ATT_K_STAGES + ATT_V_STAGES) * ATT_KV_STAGE_BYTES + ATT_O_TILE_BYTES;
-constexpr int NUM_BARS = 11 + 2 * (ATT_K_STAGES + ATT_V_STAGES) + 8;
+// dynamic shared memory: [Q tiles][K ring][V ring] (1024-aligned for the
+// 128-byte swizzle), then the barriers, two words, the row exchange and the
+// reference chain
+constexpr uint32_t TILE_REGION = ATT_Q_BUFS * ATT_Q_TILE_BYTES + (ATT_K_STAGES + ATT_V_STAGES) * ATT_KV_STAGE_BYTES;
+constexpr int NUM_BARS = 14 + 2 * (ATT_K_STAGES + ATT_V_STAGES) + 8;
 constexpr uint32_t XVAL_OFFSET = NUM_BARS * 8 + 8;
-constexpr uint32_t AUX_BYTES = XVAL_OFFSET + 2 * 2 * ATT_BM * 4;
+constexpr uint32_t CHAIN_OFFSET = XVAL_OFFSET + 2 * 2 * ATT_BM * 4;
+constexpr uint32_t AUX_BYTES = CHAIN_OFFSET + ATT_BM * 4;
 constexpr uint32_t SMEM_USED = TILE_REGION + AUX_BYTES;
 constexpr uint32_t SMEM_ALLOC = 227 * 1024;
 static_assert(SMEM_USED <= SMEM_ALLOC, "attention tiles do not fit in shared memory");
 
 struct AttSmem {
-  uint8_t* q;          // Q landing buffer, 32 KB
+  uint8_t* q;          // ATT_Q_BUFS x 32 KB: Q tiles (and the O staging of a finished unit)
   uint8_t* k;          // ATT_K_STAGES x 32 KB
   uint8_t* v;          // ATT_V_STAGES x 32 KB
-  uint8_t* o;          // O staging, 4 KB per softmax warp
-  uint64_t* q_full;    // Q landed
-  uint64_t* q_empty;   // Q copied into TMEM and read by the first S products
-  uint64_t* qt_ready;  // Q of the unit is in TMEM
+  uint64_t* q_full;    // [2] Q tile landed
+  uint64_t* q_empty;   // [2] the tile's unit: last S done and its O staged out
   uint64_t* s_full;    // [2] S_b computed
-  uint64_t* s_free;    // [2] S_b read by the softmax
-  uint64_t* p_full;    // P written
-  uint64_t* pv_done;   // a P.V completed (P is free again, O is up to date)
+  uint64_t* s_free;    // [2] S_b read by group b
+  uint64_t* p_full;    // [2] P_b written by group b
+  uint64_t* pv_done;   // [2] the P.V of a buffer-b tile completed (P_b is free again, O is up to date)
   uint64_t* o_full;    // the unit's last P.V completed
   uint64_t* o_empty;   // the unit's epilogue has read O
   uint64_t* k_full;
@@ -99,6 +109,7 @@ struct AttSmem {
   uint32_t* tmem_slot;
   uint32_t* abort;
   float* xval;         // [2 buffers][2 halves][128 rows]
+  uint32_t* chain;     // [128 rows] reference maximum of the last tile (high 24 bits) | its tag (low 8)
 };
 
 __device__ __forceinline__ AttSmem carve(uint8_t* base) {
@@ -106,18 +117,16 @@ __device__ __forceinline__ AttSmem carve(uint8_t* base) {
   s.q = base;
   s.k = base + ATT_Q_BUFS * ATT_Q_TILE_BYTES;
   s.v = s.k + ATT_K_STAGES * ATT_KV_STAGE_BYTES;
-  s.o = s.v + ATT_V_STAGES * ATT_KV_STAGE_BYTES;
   uint64_t* b = reinterpret_cast<uint64_t*>(base + TILE_REGION);
   s.q_full = b;
-  s.q_empty = b + 1;
-  s.qt_ready = b + 2;
-  s.s_full = b + 3;
-  s.s_free = b + 5;
-  s.p_full = b + 7;
-  s.pv_done = b + 8;
-  s.o_full = b + 9;
-  s.o_empty = b + 10;
-  s.k_full = b + 11;
+  s.q_empty = b + 2;
+  s.s_full = b + 4;
+  s.s_free = b + 6;
+  s.p_full = b + 8;
+  s.pv_done = b + 10;
+  s.o_full = b + 12;
+  s.o_empty = b + 13;
+  s.k_full = b + 14;
   s.k_empty = s.k_full + ATT_K_STAGES;
   s.v_full = s.k_empty + ATT_K_STAGES;
   s.v_empty = s.v_full + ATT_V_STAGES;
@@ -125,6 +134,7 @@ __device__ __forceinline__ AttSmem carve(uint8_t* base) {
   s.tmem_slot = reinterpret_cast<uint32_t*>(base + TILE_REGION + NUM_BARS * 8);
   s.abort = s.tmem_slot + 1;
   s.xval = reinterpret_cast<float*>(base + TILE_REGION + XVAL_OFFSET);
+  s.chain = reinterpret_cast<uint32_t*>(base + TILE_REGION + CHAIN_OFFSET);
   return s;
 }
 
@@ -279,20 +289,23 @@ __device__ void att_producer_qk(const AttnParams& p, const AttSmem& s, const CUt
     bool prefetched = false;
     if (!x.ok) atomicOr(p.status, DEV_ERR_BAD_WORK);
     if (x.ntiles > 0) {
-      if (!mbar_wait(s.q_empty, (qc & 1u) ^ 1u, s.abort, p.timeout_ns, 1)) return;
+      const int qb = static_cast<int>(qc & 1u);
+      uint8_t* q = s.q + qb * ATT_Q_TILE_BYTES;
+      uint64_t* qf = &s.q_full[qb];
+      if (!mbar_wait(&s.q_empty[qb], ((qc >> 1) & 1u) ^ 1u, s.abort, p.timeout_ns, 1)) return;
       ++qc;
       if (x.self) {  // rows start .. start + self_rows - 1 of Q_user[u][h] (past Lq_u: TMA zero fill)
-        mbar_arrive_expect_tx(s.q_full, static_cast<uint32_t>(p.self_rows * ATT_D * 2));
-        tma_load_4d(s.q, tmQu, s.q_full, 0, x.start, x.h, x.u);
-        tma_load_4d(s.q + HALF_TILE, tmQu, s.q_full, 64, x.start, x.h, x.u);
+        mbar_arrive_expect_tx(qf, static_cast<uint32_t>(p.self_rows * ATT_D * 2));
+        tma_load_4d(q, tmQu, qf, 0, x.start, x.h, x.u);
+        tma_load_4d(q + HALF_TILE, tmQu, qf, 64, x.start, x.h, x.u);
       } else {
-        mbar_arrive_expect_tx(s.q_full, static_cast<uint32_t>(cpt * p.Lq * ATT_D * 2));
+        mbar_arrive_expect_tx(qf, static_cast<uint32_t>(cpt * p.Lq * ATT_D * 2));
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
           if (j < cpt) {
-            uint8_t* dst = s.q + j * p.Lq * 128;
-            tma_load_4d(dst, tmQ, s.q_full, 0, 0, x.h, qs.cand[j]);
-            tma_load_4d(dst + HALF_TILE, tmQ, s.q_full, 64, 0, x.h, qs.cand[j]);
+            uint8_t* dst = q + j * p.Lq * 128;
+            tma_load_4d(dst, tmQ, qf, 0, 0, x.h, qs.cand[j]);
+            tma_load_4d(dst + HALF_TILE, tmQ, qf, 64, 0, x.h, qs.cand[j]);
           }
         }
       }
@@ -343,20 +356,9 @@ __device__ void att_producer_v(const AttnParams& p, const AttSmem& s, const CUte
 // to the start-address field; shared memory is below 256 KB, so the 14-bit
 // field never carries into the next one.
 //
-// S = Q K^T with K-major operands (128 rows x 128 d as two 64-wide d halves;
-// steps 0-3 advance 32 bytes inside the swizzled rows of the first half,
-// 4-7 in the second).  A = Q from TMEM (16 d per step = 8 columns) ...
-__device__ __forceinline__ void issue_qk(uint32_t s_tmem, uint32_t q_tmem, uint32_t k_base) {
-  constexpr uint32_t idesc = idesc_bf16_f32(ATT_BM, ATT_BN, false, false);
-  const uint64_t kd = sdesc_sw128(k_base, 16, 1024);
-#pragma unroll
-  for (int ks = 0; ks < 8; ++ks) {
-    const uint32_t off = ((ks >> 2) * HALF_TILE + (ks & 3) * 32) >> 4;
-    mma_bf16_ts(s_tmem, q_tmem + ks * 8, kd + off, idesc, ks > 0 ? 1u : 0u);
-  }
-}
-
-// ... or from the landing buffer in shared memory (same layout as K).
+// S = Q K^T with K-major operands, both in shared memory (128 rows x 128 d
+// as two 64-wide d halves; steps 0-3 advance 32 bytes inside the swizzled
+// rows of the first half, 4-7 in the second).
 __device__ __forceinline__ void issue_qk_ss(uint32_t s_tmem, uint32_t q_base, uint32_t k_base) {
   constexpr uint32_t idesc = idesc_bf16_f32(ATT_BM, ATT_BN, false, false);
   const uint64_t qd = sdesc_sw128(q_base, 16, 1024);
@@ -388,7 +390,8 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
 }
 
 // S issuer (whole warp; one elected lane issues): tile g goes to S_(g&1)
-// once the softmax has read S(g-2) out of it.
+// once group g&1 has read S(g-2) out of it; the unit's Q tile is released
+// (for the unit after next) by the unit's last S.
 template <bool kSelf>
 __device__ void att_s_issuer(const AttnParams& p, const AttSmem& s, uint32_t tmem, const UnitCount& n_units) {
   uint32_t g = 0, qu = 0;
@@ -399,31 +402,21 @@ __device__ void att_s_issuer(const AttnParams& p, const AttSmem& s, uint32_t tme
     const int4 nw = load_work<kSelf>(p, nunit, n_units);
     const Unit x = decode<kSelf>(p, w);
     if (x.ntiles > 0) {
-      const int last_ss = min(1, x.ntiles - 1);
+      const int qb = static_cast<int>(qu & 1u);
+      const uint32_t q_base = smem_u32(s.q + qb * ATT_Q_TILE_BYTES);
       for (int jt = 0; jt < x.ntiles; ++jt, ++g) {
         const int b = static_cast<int>(g & 1u);
         const uint32_t n = g >> 1;
         const int kst = ring_stage<ATT_K_STAGES>(g);
         if (!warp_wait(&s.k_full[kst], ring_phase<ATT_K_STAGES>(g), s, p)) return;
         if (n > 0 && !warp_wait(&s.s_free[b], (n - 1) & 1u, s, p)) return;
-        const uint32_t k_base = smem_u32(s.k + kst * ATT_KV_STAGE_BYTES);
-        const bool ss = jt <= last_ss;
-        if (ss) {
-          if (jt == 0 && !warp_wait(s.q_full, qu & 1u, s, p)) return;
-        } else {
-          // skipped for units of at most two tiles: the softmax's next arrival
-          // needs this unit's S, so the barrier never runs two phases ahead
-          if (jt == last_ss + 1 && !warp_wait(s.qt_ready, qu & 1u, s, p)) return;
-        }
+        if (jt == 0 && !warp_wait(&s.q_full[qb], (qu >> 1) & 1u, s, p)) return;
         tc_fence_after();
         if (elect_one()) {
-          if (ss)
-            issue_qk_ss(tmem + TM_S + b * 128, smem_u32(s.q), k_base);
-          else
-            issue_qk(tmem + TM_S + b * 128, tmem + TM_Q, k_base);
+          issue_qk_ss(tmem + TM_S + b * 128, q_base, smem_u32(s.k + kst * ATT_KV_STAGE_BYTES));
           mma_commit(&s.s_full[b]);
           mma_commit(&s.k_empty[kst]);
-          if (jt == last_ss) mma_commit(s.q_empty);  // the landing buffer's last reader
+          if (jt + 1 == x.ntiles) mma_commit(&s.q_empty[qb]);  // the tile's last reader
         }
         __syncwarp();
       }
@@ -434,9 +427,9 @@ __device__ void att_s_issuer(const AttnParams& p, const AttSmem& s, uint32_t tme
   }
 }
 
-// P.V issuer (whole warp; one elected lane issues): tile g once its P is
-// written; the unit's first one also waits for the previous unit's epilogue
-// to have read O.
+// P.V issuer (whole warp; one elected lane issues): tile g once group g&1
+// has written its P; the unit's first one also waits for the previous
+// unit's epilogue to have read O.
 template <bool kSelf>
 __device__ void att_pv_issuer(const AttnParams& p, const AttSmem& s, uint32_t tmem, const UnitCount& n_units) {
   uint32_t g = 0, ou = 0;
@@ -448,13 +441,14 @@ __device__ void att_pv_issuer(const AttnParams& p, const AttSmem& s, uint32_t tm
     const Unit x = decode<kSelf>(p, w);
     for (int jt = 0; jt < x.ntiles; ++jt, ++g) {
       const int vst = ring_stage<ATT_V_STAGES>(g);
-      if (!warp_wait(s.p_full, g & 1u, s, p)) return;
+      const int b = static_cast<int>(g & 1u);
+      if (!warp_wait(&s.p_full[b], (g >> 1) & 1u, s, p)) return;
       if (!warp_wait(&s.v_full[vst], ring_phase<ATT_V_STAGES>(g), s, p)) return;
       if (jt == 0 && !warp_wait(s.o_empty, (ou & 1u) ^ 1u, s, p)) return;
       tc_fence_after();
       if (elect_one()) {
-        issue_pv(tmem + TM_O, tmem + TM_P, smem_u32(s.v + vst * ATT_KV_STAGE_BYTES), jt > 0);
-        mma_commit(s.pv_done);
+        issue_pv(tmem + TM_O, tmem + TM_P + b * 64, smem_u32(s.v + vst * ATT_KV_STAGE_BYTES), jt > 0);
+        mma_commit(&s.pv_done[b]);
         mma_commit(&s.v_empty[vst]);
         if (jt + 1 == x.ntiles) mma_commit(s.o_full);
       }
@@ -468,8 +462,8 @@ __device__ void att_pv_issuer(const AttnParams& p, const AttSmem& s, uint32_t tm
 
 // ---------------------------------------------------- softmax + epilogue
 struct Lane {
-  int quarter, half, r;
-  uint32_t xc;  // exchanges done with the partner warp
+  int quarter, half, r;  // half: the warp's group (its key tiles) and its d half of Q and O
+  uint32_t xc;           // exchanges done with the partner warp
 };
 
 // Hands `mine` to the other warp of the quarter and returns its value for
@@ -487,6 +481,58 @@ __device__ __forceinline__ bool pair_exchange(const AttnParams& p, const AttSmem
   return true;
 }
 
+// The reference-maximum chain.  Tile g's group posts the row's reference
+// after that tile (tag (g + 1) mod 256 in the low byte of the same 32-bit
+// word, so one store publishes both and no fence is needed); tile g + 1,
+// the other group's, polls the word.  The word
+// is rewritten at every tile, so the word a reader finds is either the one
+// it waits for or the one its own group posted a tile earlier (tag one
+// less): an 8-bit tag cannot be mistaken.  The other group cannot post past
+// it either: within a unit its next tile waits for this reader's post, and
+// the first tile of the next unit comes only after the unit's last P.V
+// (o_full), which needs this reader's P.  The reference keeps the high 24
+// bits of the fp32 value (both groups use exactly that value, so the
+// dropped bits only move the reference by < 2^-15 relative).
+__device__ __forceinline__ float chain_value(float m) { return __uint_as_float(__float_as_uint(m) & 0xFFFFFF00u); }
+
+__device__ __forceinline__ void chain_post(const AttSmem& s, int r, uint32_t tag, float m) {
+  const uint32_t w = (__float_as_uint(m) & 0xFFFFFF00u) | (tag & 0xFFu);
+  asm volatile("st.volatile.shared.b32 [%0], %1;" ::"r"(smem_u32(s.chain + r)), "r"(w) : "memory");
+}
+
+__device__ __forceinline__ uint32_t chain_load(const AttSmem& s, int r) {
+  uint32_t w;
+  asm volatile("ld.volatile.shared.b32 %0, [%1];" : "=r"(w) : "r"(smem_u32(s.chain + r)) : "memory");
+  return w;
+}
+
+// Bounded like every wait here; the warp's lanes agree on the outcome.
+__device__ __forceinline__ bool chain_wait(const AttnParams& p, const AttSmem& s, int r, uint32_t tag, float& m) {
+  tag &= 0xFFu;
+  uint32_t w = chain_load(s, r);
+  bool ok = true;
+  if ((w & 0xFFu) != tag) {
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t it = 1;; ++it) {
+      w = chain_load(s, r);
+      if ((w & 0xFFu) == tag) break;
+      if ((it & 63u) == 0) {
+        if (*s.abort) {
+          ok = false;
+          break;
+        }
+        if (globaltimer_ns() - t0 > p.timeout_ns) {
+          *s.abort = 1;
+          ok = false;
+          break;
+        }
+      }
+    }
+  }
+  m = __uint_as_float(w & 0xFFFFFF00u);
+  return __all_sync(0xffffffffu, ok);
+}
+
 // Does this thread's row (TMEM lane r) hold a query of unit x: one of the
 // unit's candidates' rows, or for a self unit one of its Q_user rows?
 __device__ __forceinline__ bool row_valid(const Unit& x, int r, int slot, bool row_in_tile) {
@@ -497,8 +543,9 @@ struct RowOut {
   bool pending;  // a finished unit whose O has not been written yet
   bool valid;    // this thread's row belongs to a candidate of that unit
   __nv_bfloat16* row;
-  float l;       // this warp's half of the row sum
-  float m;       // the row's reference maximum (log2 domain) that l is relative to
+  float l;       // the row sum over this warp's group's tiles, relative to m
+  float m;       // the reference of this group's last tile of the unit (-inf if it had none)
+  int qb;        // the unit's Q tile (its O is staged there)
 };
 
 // The row's natural-log log-sum-exp, m + log2(l) in the log2 domain, into
@@ -508,22 +555,31 @@ __device__ __forceinline__ void store_lse(const AttnParams& p, const __nv_bfloat
   p.lse[idx] = lse2 * 0.69314718055994531f;
 }
 
-// O / l -> bf16 -> this warp's d half of its 32 rows, through its 4 KB of
-// staging (128-byte rows, 16-byte chunk c of row r at chunk c ^ (r % 8)) to
-// global memory 4 rows per store instruction; then O may be overwritten.
+// The two groups' row sums are brought to the unit's last reference and
+// added; then O / l -> bf16 -> this warp's d half of its 32 rows, through its
+// 4 KB of the unit's (finished) Q tile (128-byte rows, 16-byte chunk c of
+// row r at chunk c ^ (r % 8)) to global memory 4 rows per store
+// instruction; O may be overwritten once it is read, the Q tile refilled
+// once the staging is read back.  `o_ready`: the caller has already waited
+// for the unit's last P.V.
 template <bool kLse>
 __device__ __forceinline__ bool att_epilogue(const AttnParams& p, const AttSmem& s, uint32_t Ot, const RowOut& ro,
-                                             Lane& ln, uint32_t& ou) {
-  float lp;
-  if (!pair_exchange(p, s, ln, ro.l, lp)) return false;
-  const float l = ro.l + lp;
-  if (kLse && ro.valid && ln.half == 0) store_lse(p, ro.row, l > 0.f ? ro.m + __log2f(l) : -INFINITY);
-  if (!mbar_wait(s.o_full, ou & 1u, s.abort, p.timeout_ns, 1)) return false;
-  ++ou;
+                                             Lane& ln, uint32_t& ou, bool o_ready) {
+  float mp, lp;
+  if (!pair_exchange(p, s, ln, ro.m, mp)) return false;
+  const float mf = fmaxf(ro.m, mp);
+  const float lm = ro.l > 0.f ? ro.l * ex2(ro.m - mf) : 0.f;
+  if (!pair_exchange(p, s, ln, lm, lp)) return false;
+  const float l = lm + lp;
+  if (kLse && ro.valid && ln.half == 0) store_lse(p, ro.row, l > 0.f ? mf + __log2f(l) : -INFINITY);
+  if (!o_ready) {
+    if (!mbar_wait(s.o_full, ou & 1u, s.abort, p.timeout_ns, 1)) return false;
+    ++ou;
+  }
   tc_fence_after();
   const float inv = l > 0.f ? 1.0f / l : 0.f;
   const int lane = static_cast<int>(lane_id());
-  uint8_t* stage = s.o + ((ln.quarter * 2 + ln.half) << 12);
+  uint8_t* stage = s.q + ro.qb * ATT_Q_TILE_BYTES + ((ln.quarter * 2 + ln.half) << 12);
 #pragma unroll
   for (int c = 0; c < 2; ++c) {
     uint32_t o[32];
@@ -553,31 +609,34 @@ __device__ __forceinline__ bool att_epilogue(const AttnParams& p, const AttSmem&
     const uint4 w = *reinterpret_cast<const uint4*>(stage + r * 128 + ((chunk ^ (r & 7)) << 4));
     if (valid) reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(dst_row) + ln.half * 64)[chunk] = w;
   }
-  __syncwarp();  // the staging rows are read before this warp's next epilogue writes them
+  mbar_arrive(&s.q_empty[ro.qb]);  // the staging rows are read: the tile may take the next Q
   return true;
 }
 
+// One softmax warp: the key tiles g of its group (g % 2 == group) of every
+// unit, all 128 columns of its 32 rows; at each unit's start the previous
+// unit's epilogue (its d half of O).
 // kLse: also write each row's log-sum-exp (target units only).
 template <bool kSelf, bool kLse>
 __device__ void att_softmax(const AttnParams& p, const AttSmem& s, uint32_t tmem, const UnitCount& n_units) {
   const int warp = threadIdx.x >> 5;
   Lane ln;
   ln.quarter = warp & 3;                                     // TMEM lane quarter of this warp
-  ln.half = (warp - SOFTMAX_WARP0) >> 2;                     // column half of this warp
+  ln.half = (warp - SOFTMAX_WARP0) >> 2;                     // group = d half of O
   ln.r = (ln.quarter << 5) + static_cast<int>(lane_id());    // row = TMEM lane
   ln.xc = 0;
-  const int half = ln.half;
+  const int grp = ln.half;
   const uint32_t lane_base = static_cast<uint32_t>(ln.quarter * 32) << 16;
-  const uint32_t St = tmem + lane_base + TM_S + half * 64;
-  const uint32_t Pt = tmem + lane_base + TM_P + half * 32;
-  const uint32_t Qt = tmem + lane_base + TM_Q + half * 32;
-  const uint32_t Ot = tmem + lane_base + TM_O + half * 64;
+  const uint32_t St = tmem + lane_base + TM_S + grp * 128;  // this group's S
+  const uint32_t Pt = tmem + lane_base + TM_P + grp * 64;   // and its P
+  const uint32_t Oall = tmem + lane_base + TM_O;
+  const uint32_t Ot = Oall + grp * 64;
   const float sl = p.scale_log2;
   const int slot = ln.r / p.Lq;
   const int qrow = ln.r % p.Lq;
   const bool row_in_tile = ln.r < p.cands_per_tile * p.Lq;
   uint32_t g = 0, qc = 0, ou = 0;
-  RowOut prev = {false, false, nullptr, 0.f, 0.f};
+  RowOut prev = {false, false, nullptr, 0.f, -INFINITY, 0};
 
   int unit = blockIdx.x;
   Unit x = decode<kSelf>(p, load_work<kSelf>(p, unit, n_units));
@@ -600,110 +659,102 @@ __device__ void att_softmax(const AttnParams& p, const AttSmem& s, uint32_t tmem
       if (rv) {
         const uint4 z = make_uint4(0, 0, 0, 0);
 #pragma unroll
-        for (int c = 0; c < 8; ++c) reinterpret_cast<uint4*>(orow + half * 64)[c] = z;
-        if (kLse && half == 0) store_lse(p, orow, -INFINITY);
+        for (int c = 0; c < 8; ++c) reinterpret_cast<uint4*>(orow + grp * 64)[c] = z;
+        if (kLse && grp == 0) store_lse(p, orow, -INFINITY);
       }
     } else {
-      // this warp's d half of the Q row: landing buffer (128-byte swizzle:
-      // 16-byte chunk c of row r sits at chunk c ^ (r % 8)) -> TMEM.  Every S
-      // of the previous unit has been read by this thread, so Q is free.
-      if (!mbar_wait(s.q_full, qc & 1u, s.abort, p.timeout_ns, 1)) return;
-      ++qc;
-      {
-        const uint8_t* qsrc = s.q + half * HALF_TILE + ln.r * 128;
-        uint32_t w[32];
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const uint4 v = *reinterpret_cast<const uint4*>(qsrc + ((c ^ (ln.r & 7)) << 4));
-          w[4 * c + 0] = v.x;
-          w[4 * c + 1] = v.y;
-          w[4 * c + 2] = v.z;
-          w[4 * c + 3] = v.w;
-        }
-        tmem_st32(Qt, w);
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(s.qt_ready);
-      mbar_arrive(s.q_empty);
       // the previous unit's O is written out while this unit's first S are computed
       if (prev.pending) {
-        if (!att_epilogue<kLse>(p, s, Ot, prev, ln, ou)) return;
+        if (!att_epilogue<kLse>(p, s, Ot, prev, ln, ou, false)) return;
         prev.pending = false;
       }
+      const int qb = static_cast<int>(qc & 1u);
+      ++qc;
 
-      float m = -INFINITY, l = 0.f;
+      float mref = -INFINITY, l = 0.f;  // this group's reference and row sum
       for (int jt = 0; jt < x.ntiles; ++jt, ++g) {
-        const int b = static_cast<int>(g & 1u);
-        if (!mbar_wait(&s.s_full[b], (g >> 1) & 1u, s.abort, p.timeout_ns, 1)) return;
+        if (static_cast<int>(g & 1u) != grp) continue;  // the other group's tile
+        if (!mbar_wait(&s.s_full[grp], (g >> 1) & 1u, s.abort, p.timeout_ns, 1)) return;
         tc_fence_after();
-        const int ncols = min(ATT_BN, x.L - jt * ATT_BN) - half * 64;  // valid columns of this half
-        uint32_t v[64];
-        tmem_ld32p(St + b * 128, v);
-        tmem_ld32p(St + b * 128 + 32, v + 32);
+        const int ncols = min(ATT_BN, x.L - jt * ATT_BN);  // valid key columns of this tile
+        uint32_t v[128];
+        tmem_ld32p(St, v);
+        tmem_ld32p(St + 32, v + 32);
+        tmem_ld32p(St + 64, v + 64);
+        tmem_ld32p(St + 96, v + 96);
         tmem_ld_wait();
         reg_fence32(v);
         reg_fence32(v + 32);
+        reg_fence32(v + 64);
+        reg_fence32(v + 96);
         tc_fence_before();
-        mbar_arrive(&s.s_free[b]);  // S_b may take S(g + 2) now
-        if (ncols < 64) {
+        mbar_arrive(&s.s_free[grp]);  // S_b may take S(g + 2) now
+        if (ncols < ATT_BN) {
 #pragma unroll
-          for (int j = 0; j < 64; ++j)
+          for (int j = 0; j < ATT_BN; ++j)
             if (j >= ncols) v[j] = __float_as_uint(-INFINITY);
         }
         float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
-        for (int j = 0; j < 64; j += 4) {
+        for (int j = 0; j < ATT_BN; j += 4) {
           mx0 = fmaxf(mx0, __uint_as_float(v[j]));
           mx1 = fmaxf(mx1, __uint_as_float(v[j + 1]));
           mx2 = fmaxf(mx2, __uint_as_float(v[j + 2]));
           mx3 = fmaxf(mx3, __uint_as_float(v[j + 3]));
         }
-        float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
-        float mp;
-        if (!pair_exchange(p, s, ln, mx, mp)) return;
-        mx = fmaxf(mx, mp);
-        const float m_new = fmaxf(m, mx * sl);
+        const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl;
+        // the reference after the tile before (the other group's), none on the first
+        float mprev = -INFINITY;
+        if (jt > 0 && !chain_wait(p, s, ln.r, g, mprev)) return;
         // tcgen05.ld/st are warp-collective: the rescale decision must be
-        // uniform across the warp, so any row that needs it moves all 32.
-        // Both warps of the quarter see the same maxima, so they agree.
-        const bool rescale = __any_sync(0xffffffffu, m_new > m + RESCALE_THRESHOLD);
-        float alpha = 1.f;
-        if (rescale) {
-          alpha = ex2(m - m_new);  // 0 on the first tile, 1 for rows whose max did not move
-          l *= alpha;
-          m = m_new;
+        // uniform across the warp, so any row that needs it moves all 32
+        const bool rescale = __any_sync(0xffffffffu, mx > mprev + RESCALE_THRESHOLD);
+        const float mj = rescale ? chain_value(fmaxf(mprev, mx)) : mprev;
+        chain_post(s, ln.r, g + 1, mj);
+        if (mj != mref) {  // this group's sum follows the reference (l = 0 on its first tile)
+          l *= ex2(mref - mj);
+          mref = mj;
         }
-        // p = 2^(s*sl - m) (masked columns give 2^-inf = 0) as bf16 pairs
+        // P_b is free once P.V(g - 2) has read it
+        if (g >= 2 && !mbar_wait(&s.pv_done[grp], ((g >> 1) - 1) & 1u, s.abort, p.timeout_ns, 1)) return;
+        tc_fence_after();
+        // p = 2^(s*sl - mj) (masked columns give 2^-inf = 0) as bf16 pairs
+        // into P_b, 32 columns at a time; P.V may read them after p_full
         float l0 = 0.f, l1 = 0.f;
-        uint32_t pk[32];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const float p0 = ex2(fmaf(__uint_as_float(v[2 * j]), sl, -m));
-          const float p1 = ex2(fmaf(__uint_as_float(v[2 * j + 1]), sl, -m));
-          l0 += p0;
-          l1 += p1;
-          pk[j] = pack_bf16x2(p0, p1);
+        for (int h = 0; h < 2; ++h) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const float p0 = ex2(fmaf(__uint_as_float(v[64 * h + 2 * j]), sl, -mj));
+            const float p1 = ex2(fmaf(__uint_as_float(v[64 * h + 2 * j + 1]), sl, -mj));
+            l0 += p0;
+            l1 += p1;
+            pk[j] = pack_bf16x2(p0, p1);
+          }
+          tmem_st32p(Pt + 32 * h, pk);
         }
         l += l0 + l1;
-        // P and O are free once the previous P.V has completed
-        if (g > 0 && !mbar_wait(s.pv_done, (g - 1) & 1u, s.abort, p.timeout_ns, 1)) return;
-        tc_fence_after();
         if (rescale && jt > 0) {
-#pragma unroll
-          for (int c = 0; c < 2; ++c) {
+          // O holds P.V of tiles 0 .. jt-1 relative to mprev: once the last of
+          // them is done, scale all of O's columns of these rows to mj
+          const uint32_t gp = g - 1;
+          if (!mbar_wait(&s.pv_done[gp & 1u], (gp >> 1) & 1u, s.abort, p.timeout_ns, 1)) return;
+          tc_fence_after();
+          const float alpha = ex2(mprev - mj);
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
             uint32_t o[32];
-            tmem_ld32(Ot + c * 32, o);
+            tmem_ld32(Oall + c * 32, o);
             tmem_ld_wait(o);
 #pragma unroll
             for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
-            tmem_st32(Ot + c * 32, o);
+            tmem_st32(Oall + c * 32, o);
           }
         }
-        tmem_st32p(Pt, pk);
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(s.p_full);
+        mbar_arrive(&s.p_full[grp]);
         if (!prefetched) {  // the next unit's entry and this row's candidate in it
           prefetched = true;
           nx = decode<kSelf>(p, nw);
@@ -715,7 +766,8 @@ __device__ void att_softmax(const AttnParams& p, const AttSmem& s, uint32_t tmem
       prev.valid = rv;
       prev.row = orow;
       prev.l = l;
-      prev.m = m;
+      prev.m = mref;
+      prev.qb = qb;
     }
     if (!prefetched) {
       nx = decode<kSelf>(p, nw);
@@ -727,7 +779,7 @@ __device__ void att_softmax(const AttnParams& p, const AttSmem& s, uint32_t tmem
     cand = ncand;
     unit = nunit;
   }
-  if (prev.pending) att_epilogue<kLse>(p, s, Ot, prev, ln, ou);
+  if (prev.pending) att_epilogue<kLse>(p, s, Ot, prev, ln, ou, false);
 }
 
 // kSelf: the launch also runs self units (ikbo_attn_self_target_forward);
@@ -752,15 +804,14 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
   n_units.total = n_units.target + (kSelf ? p.n_self : 0);
 
   if (threadIdx.x == 0) {
-    mbar_init(s.q_full, 1);
-    mbar_init(s.q_empty, 1 + SOFTMAX_THREADS);
-    mbar_init(s.qt_ready, SOFTMAX_THREADS);
     for (int i = 0; i < 2; ++i) {
+      mbar_init(&s.q_full[i], 1);
+      mbar_init(&s.q_empty[i], 1 + SOFTMAX_THREADS);  // the unit's last S, then its epilogue's staging
       mbar_init(&s.s_full[i], 1);
-      mbar_init(&s.s_free[i], SOFTMAX_THREADS);
+      mbar_init(&s.s_free[i], GROUP_THREADS);
+      mbar_init(&s.p_full[i], GROUP_THREADS);
+      mbar_init(&s.pv_done[i], 1);
     }
-    mbar_init(s.p_full, SOFTMAX_THREADS);
-    mbar_init(s.pv_done, 1);
     mbar_init(s.o_full, 1);
     mbar_init(s.o_empty, SOFTMAX_THREADS);
     for (int i = 0; i < ATT_K_STAGES; ++i) {
@@ -772,6 +823,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       mbar_init(&s.v_empty[i], 1);
     }
     for (int i = 0; i < 8; ++i) mbar_init(&s.xbar[i], 64);
+    for (int r = 0; r < ATT_BM; ++r) s.chain[r] = 0;  // tag 0: no tile has posted (tags start at 1)
     *s.abort = 0;
     fence_barrier_init();
     fence_proxy_async_smem();
@@ -791,15 +843,23 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *s.tmem_slot;
 
-  if (warp == 0) {
-    if (lane_id() == 0) att_producer_qk<kSelf>(p, s, &tmQ, &tmQu, &tmK, n_units);
-  } else if (warp == 3) {
-    if (lane_id() == 0) att_producer_v<kSelf>(p, s, &tmV, n_units);
-  } else if (warp == 1) {
-    att_s_issuer<kSelf>(p, s, tmem, n_units);
-  } else if (warp == 2) {
-    att_pv_issuer<kSelf>(p, s, tmem, n_units);
-  } else if (warp >= SOFTMAX_WARP0) {
+  // registers: launched at 168 per thread (384 x 168 = 64512); the four
+  // control warps give back down to CTRL_REGS and the softmax warps, which
+  // hold a whole 128-column tile row each, take SOFTMAX_REGS
+  // (128 x CTRL_REGS + 256 x SOFTMAX_REGS = 64512)
+  if (warp < SOFTMAX_WARP0) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(CTRL_REGS));
+    if (warp == 0) {
+      if (lane_id() == 0) att_producer_qk<kSelf>(p, s, &tmQ, &tmQu, &tmK, n_units);
+    } else if (warp == 3) {
+      if (lane_id() == 0) att_producer_v<kSelf>(p, s, &tmV, n_units);
+    } else if (warp == 1) {
+      att_s_issuer<kSelf>(p, s, tmem, n_units);
+    } else {
+      att_pv_issuer<kSelf>(p, s, tmem, n_units);
+    }
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(SOFTMAX_REGS));
     att_softmax<kSelf, kLse>(p, s, tmem, n_units);
   }
 

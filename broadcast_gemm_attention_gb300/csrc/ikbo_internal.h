@@ -201,11 +201,11 @@ constexpr int ATT_TILES = 1;       // query tiles per work unit
 constexpr int ATT_THREADS = 384;   // warp 0 TMA Q+K, 1 S issuer, 2 P.V issuer, 3 TMA V, 4-11 softmax
 constexpr int ATT_KV_STAGE_BYTES = ATT_BN * ATT_D * 2;   // 32 KB
 constexpr int ATT_Q_TILE_BYTES = ATT_BM * ATT_D * 2;     // 32 KB
-constexpr int ATT_Q_BUFS = 1;      // Q landing buffer
+constexpr int ATT_Q_BUFS = 2;      // Q tiles (a unit's Q stays in shared memory for all of its S products;
+                                   // a finished unit's buffer stages its O on the way out)
 constexpr int ATT_K_STAGES = 3;    // K ring
 constexpr int ATT_V_STAGES = 2;    // V ring
-constexpr int ATT_O_TILE_BYTES = ATT_BM * ATT_D * 2;     // 32 KB O staging (4 KB per softmax warp)
-// shared memory: 32 KB Q + 5 x 32 KB K/V + 32 KB O = 224 KB of 227
+// shared memory: 2 x 32 KB Q + 5 x 32 KB K/V = 224 KB of 227
 
 struct AttnParams {
   const int32_t* perm;
