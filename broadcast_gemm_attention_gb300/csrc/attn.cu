@@ -223,6 +223,36 @@ __device__ __forceinline__ void reg_fence32(uint32_t* r) {
                  "+r"(r[29]), "+r"(r[30]), "+r"(r[31]));
 }
 
+// max of three (one instruction)
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// (r0, r1) = (a0, a1) * b + c: one paired fp32 FMA
+__device__ __forceinline__ void fma2(float& r0, float& r1, float a0, float a1, float b, float c) {
+  asm("{.reg .b64 x, y, z, w;\n\t"
+      "mov.b64 x, {%2, %3};\n\t"
+      "mov.b64 y, {%4, %4};\n\t"
+      "mov.b64 z, {%5, %5};\n\t"
+      "fma.rn.f32x2 w, x, y, z;\n\t"
+      "mov.b64 {%0, %1}, w;}"
+      : "=f"(r0), "=f"(r1)
+      : "f"(a0), "f"(a1), "f"(b), "f"(c));
+}
+
+// (s0, s1) += (a0, a1): one paired fp32 add
+__device__ __forceinline__ void add2(float& s0, float& s1, float a0, float a1) {
+  asm("{.reg .b64 x, y, w;\n\t"
+      "mov.b64 x, {%0, %1};\n\t"
+      "mov.b64 y, {%2, %3};\n\t"
+      "add.rn.f32x2 w, x, y;\n\t"
+      "mov.b64 {%0, %1}, w;}"
+      : "+f"(s0), "+f"(s1)
+      : "f"(a0), "f"(a1));
+}
+
 __device__ __forceinline__ void tmem_ld32p(uint32_t taddr, uint32_t* r) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
@@ -487,10 +517,10 @@ __device__ __forceinline__ bool pair_exchange(const AttnParams& p, const AttSmem
 // the other group's, polls the word.  The word
 // is rewritten at every tile, so the word a reader finds is either the one
 // it waits for or the one its own group posted a tile earlier (tag one
-// less): an 8-bit tag cannot be mistaken.  The other group cannot post past
-// it either: within a unit its next tile waits for this reader's post, and
-// the first tile of the next unit comes only after the unit's last P.V
-// (o_full), which needs this reader's P.  The reference keeps the high 24
+// less): an 8-bit tag cannot be mistaken.  Every tile, the first of a unit
+// included (which ignores the value), waits for the post of the tile before
+// it before posting its own, so the posts form one sequence through all of
+// the CTA's tiles and none overwrites a word before it has been read.  The reference keeps the high 24
 // bits of the fp32 value (both groups use exactly that value, so the
 // dropped bits only move the reference by < 2^-15 relative).
 __device__ __forceinline__ float chain_value(float m) { return __uint_as_float(__float_as_uint(m) & 0xFFFFFF00u); }
@@ -555,16 +585,15 @@ __device__ __forceinline__ void store_lse(const AttnParams& p, const __nv_bfloat
   p.lse[idx] = lse2 * 0.69314718055994531f;
 }
 
-// The two groups' row sums are brought to the unit's last reference and
-// added; then O / l -> bf16 -> this warp's d half of its 32 rows, through its
-// 4 KB of the unit's (finished) Q tile (128-byte rows, 16-byte chunk c of
-// row r at chunk c ^ (r % 8)) to global memory 4 rows per store
-// instruction; O may be overwritten once it is read, the Q tile refilled
-// once the staging is read back.  `o_ready`: the caller has already waited
-// for the unit's last P.V.
+// The unit's epilogue, in two parts so that each group can run a tile of
+// the next unit in between.  Part 1: the two groups' row sums are brought
+// to the unit's last reference and added; once the unit's last P.V is done,
+// O / l -> bf16 -> this warp's d half of its 32 rows into its 4 KB of the
+// unit's (finished) Q tile (128-byte rows, 16-byte chunk c of row r at
+// chunk c ^ (r % 8)); then O may be overwritten.
 template <bool kLse>
-__device__ __forceinline__ bool att_epilogue(const AttnParams& p, const AttSmem& s, uint32_t Ot, const RowOut& ro,
-                                             Lane& ln, uint32_t& ou, bool o_ready) {
+__device__ __forceinline__ bool att_epilogue_read(const AttnParams& p, const AttSmem& s, uint32_t Ot,
+                                                  const RowOut& ro, Lane& ln, uint32_t& ou) {
   float mp, lp;
   if (!pair_exchange(p, s, ln, ro.m, mp)) return false;
   const float mf = fmaxf(ro.m, mp);
@@ -572,10 +601,8 @@ __device__ __forceinline__ bool att_epilogue(const AttnParams& p, const AttSmem&
   if (!pair_exchange(p, s, ln, lm, lp)) return false;
   const float l = lm + lp;
   if (kLse && ro.valid && ln.half == 0) store_lse(p, ro.row, l > 0.f ? mf + __log2f(l) : -INFINITY);
-  if (!o_ready) {
-    if (!mbar_wait(s.o_full, ou & 1u, s.abort, p.timeout_ns, 1)) return false;
-    ++ou;
-  }
+  if (!mbar_wait(s.o_full, ou & 1u, s.abort, p.timeout_ns, 1)) return false;
+  ++ou;
   tc_fence_after();
   const float inv = l > 0.f ? 1.0f / l : 0.f;
   const int lane = static_cast<int>(lane_id());
@@ -597,8 +624,15 @@ __device__ __forceinline__ bool att_epilogue(const AttnParams& p, const AttSmem&
   }
   tc_fence_before();
   mbar_arrive(s.o_empty);
-  __syncwarp();
-  // read back: instruction i covers rows 4i .. 4i+3 of the warp, lane = 8 * (row - 4i) + chunk
+  return true;
+}
+
+// Part 2: the staged rows to global memory, 4 rows per store instruction (8
+// lanes per contiguous 128-byte half row); then the Q tile may be refilled.
+__device__ __forceinline__ void att_epilogue_store(const AttSmem& s, const RowOut& ro, const Lane& ln) {
+  __syncwarp();  // every lane's staging writes are visible to the warp
+  const int lane = static_cast<int>(lane_id());
+  const uint8_t* stage = s.q + ro.qb * ATT_Q_TILE_BYTES + ((ln.quarter * 2 + ln.half) << 12);
   const int chunk = lane & 7;
   const uint64_t my_row = reinterpret_cast<uint64_t>(ro.row);
 #pragma unroll
@@ -610,12 +644,13 @@ __device__ __forceinline__ bool att_epilogue(const AttnParams& p, const AttSmem&
     if (valid) reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(dst_row) + ln.half * 64)[chunk] = w;
   }
   mbar_arrive(&s.q_empty[ro.qb]);  // the staging rows are read: the tile may take the next Q
-  return true;
 }
 
 // One softmax warp: the key tiles g of its group (g % 2 == group) of every
-// unit, all 128 columns of its 32 rows; at each unit's start the previous
-// unit's epilogue (its d half of O).
+// unit, all 128 columns of its 32 rows; the previous unit's epilogue (its d
+// half of O) is interleaved with the group's first tiles of the next unit:
+// its O is read out after the group's first tile (so that tile overlaps the
+// previous unit's last P.V) and stored after the second.
 // kLse: also write each row's log-sum-exp (target units only).
 template <bool kSelf, bool kLse>
 __device__ void att_softmax(const AttnParams& p, const AttSmem& s, uint32_t tmem, const UnitCount& n_units) {
@@ -663,14 +698,10 @@ __device__ void att_softmax(const AttnParams& p, const AttSmem& s, uint32_t tmem
         if (kLse && grp == 0) store_lse(p, orow, -INFINITY);
       }
     } else {
-      // the previous unit's O is written out while this unit's first S are computed
-      if (prev.pending) {
-        if (!att_epilogue<kLse>(p, s, Ot, prev, ln, ou, false)) return;
-        prev.pending = false;
-      }
       const int qb = static_cast<int>(qc & 1u);
       ++qc;
-
+      int epi = prev.pending ? 1 : 0;  // the previous unit's epilogue: 1 read O next, 2 store it next
+      int mine = 0;                     // this group's tiles of the unit so far
       float mref = -INFINITY, l = 0.f;  // this group's reference and row sum
       for (int jt = 0; jt < x.ntiles; ++jt, ++g) {
         if (static_cast<int>(g & 1u) != grp) continue;  // the other group's tile
@@ -696,16 +727,19 @@ __device__ void att_softmax(const AttnParams& p, const AttSmem& s, uint32_t tmem
         }
         float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
-        for (int j = 0; j < ATT_BN; j += 4) {
-          mx0 = fmaxf(mx0, __uint_as_float(v[j]));
-          mx1 = fmaxf(mx1, __uint_as_float(v[j + 1]));
-          mx2 = fmaxf(mx2, __uint_as_float(v[j + 2]));
-          mx3 = fmaxf(mx3, __uint_as_float(v[j + 3]));
+        for (int j = 0; j < ATT_BN; j += 8) {
+          mx0 = fmax3(mx0, __uint_as_float(v[j]), __uint_as_float(v[j + 1]));
+          mx1 = fmax3(mx1, __uint_as_float(v[j + 2]), __uint_as_float(v[j + 3]));
+          mx2 = fmax3(mx2, __uint_as_float(v[j + 4]), __uint_as_float(v[j + 5]));
+          mx3 = fmax3(mx3, __uint_as_float(v[j + 6]), __uint_as_float(v[j + 7]));
         }
-        const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl;
-        // the reference after the tile before (the other group's), none on the first
+        const float mx = fmax3(mx0, mx1, fmaxf(mx2, mx3)) * sl;
+        // the reference after the tile before (posted by the other group, or
+        // by either at the end of the previous unit; the first tile of a unit
+        // only waits for it and starts afresh)
         float mprev = -INFINITY;
-        if (jt > 0 && !chain_wait(p, s, ln.r, g, mprev)) return;
+        if (!chain_wait(p, s, ln.r, g, mprev)) return;
+        if (jt == 0) mprev = -INFINITY;
         // tcgen05.ld/st are warp-collective: the rescale decision must be
         // uniform across the warp, so any row that needs it moves all 32
         const bool rescale = __any_sync(0xffffffffu, mx > mprev + RESCALE_THRESHOLD);
@@ -715,27 +749,35 @@ __device__ void att_softmax(const AttnParams& p, const AttSmem& s, uint32_t tmem
           l *= ex2(mref - mj);
           mref = mj;
         }
-        // P_b is free once P.V(g - 2) has read it
-        if (g >= 2 && !mbar_wait(&s.pv_done[grp], ((g >> 1) - 1) & 1u, s.abort, p.timeout_ns, 1)) return;
-        tc_fence_after();
         // p = 2^(s*sl - mj) (masked columns give 2^-inf = 0) as bf16 pairs
-        // into P_b, 32 columns at a time; P.V may read them after p_full
+        // into P_b, 32 columns at a time (P_b is free once P.V(g - 2) has
+        // read it); P.V may read them after p_full
         float l0 = 0.f, l1 = 0.f;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           uint32_t pk[32];
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
-            const float p0 = ex2(fmaf(__uint_as_float(v[64 * h + 2 * j]), sl, -mj));
-            const float p1 = ex2(fmaf(__uint_as_float(v[64 * h + 2 * j + 1]), sl, -mj));
-            l0 += p0;
-            l1 += p1;
+            float t0, t1;
+            fma2(t0, t1, __uint_as_float(v[64 * h + 2 * j]), __uint_as_float(v[64 * h + 2 * j + 1]), sl, -mj);
+            const float p0 = ex2(t0);
+            const float p1 = ex2(t1);
+            add2(l0, l1, p0, p1);
             pk[j] = pack_bf16x2(p0, p1);
+          }
+          if (h == 0) {
+            if (g >= 2 && !mbar_wait(&s.pv_done[grp], ((g >> 1) - 1) & 1u, s.abort, p.timeout_ns, 1)) return;
+            tc_fence_after();
           }
           tmem_st32p(Pt + 32 * h, pk);
         }
         l += l0 + l1;
         if (rescale && jt > 0) {
+          // O must hold only this unit's P.V: the previous unit's O is read out first
+          if (epi == 1) {
+            if (!att_epilogue_read<kLse>(p, s, Ot, prev, ln, ou)) return;
+            epi = 2;
+          }
           // O holds P.V of tiles 0 .. jt-1 relative to mprev: once the last of
           // them is done, scale all of O's columns of these rows to mj
           const uint32_t gp = g - 1;
@@ -755,6 +797,14 @@ __device__ void att_softmax(const AttnParams& p, const AttSmem& s, uint32_t tmem
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&s.p_full[grp]);
+        ++mine;
+        if (epi == 1) {  // after the group's first tile: read out the previous unit's O
+          if (!att_epilogue_read<kLse>(p, s, Ot, prev, ln, ou)) return;
+          epi = 2;
+        } else if (epi == 2 && mine >= 2) {  // after its second: store it
+          att_epilogue_store(s, prev, ln);
+          epi = 0;
+        }
         if (!prefetched) {  // the next unit's entry and this row's candidate in it
           prefetched = true;
           nx = decode<kSelf>(p, nw);
@@ -762,6 +812,8 @@ __device__ void att_softmax(const AttnParams& p, const AttSmem& s, uint32_t tmem
           ncand = (nrv && !nx.self) ? __ldg(p.perm + nx.start + slot) : 0;
         }
       }
+      if (epi == 1 && !att_epilogue_read<kLse>(p, s, Ot, prev, ln, ou)) return;
+      if (epi >= 1) att_epilogue_store(s, prev, ln);
       prev.pending = true;
       prev.valid = rv;
       prev.row = orow;
@@ -779,7 +831,7 @@ __device__ void att_softmax(const AttnParams& p, const AttSmem& s, uint32_t tmem
     cand = ncand;
     unit = nunit;
   }
-  if (prev.pending) att_epilogue<kLse>(p, s, Ot, prev, ln, ou, false);
+  if (prev.pending && att_epilogue_read<kLse>(p, s, Ot, prev, ln, ou)) att_epilogue_store(s, prev, ln);
 }
 
 // kSelf: the launch also runs self units (ikbo_attn_self_target_forward);
