@@ -725,6 +725,7 @@ __device__ void att_softmax(const AttnParams& p, const AttSmem& s, uint32_t tmem
           for (int j = 0; j < ATT_BN; ++j)
             if (j >= ncols) v[j] = __float_as_uint(-INFINITY);
         }
+        const uint32_t cw = chain_load(s, ln.r);  // usually posted long ago: read it early
         float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
         for (int j = 0; j < ATT_BN; j += 8) {
@@ -737,8 +738,8 @@ __device__ void att_softmax(const AttnParams& p, const AttSmem& s, uint32_t tmem
         // the reference after the tile before (posted by the other group, or
         // by either at the end of the previous unit; the first tile of a unit
         // only waits for it and starts afresh)
-        float mprev = -INFINITY;
-        if (!chain_wait(p, s, ln.r, g, mprev)) return;
+        float mprev = __uint_as_float(cw & 0xFFFFFF00u);
+        if (!__all_sync(0xffffffffu, (cw & 0xFFu) == (g & 0xFFu)) && !chain_wait(p, s, ln.r, g, mprev)) return;
         if (jt == 0) mprev = -INFINITY;
         // tcgen05.ld/st are warp-collective: the rescale decision must be
         // uniform across the warp, so any row that needs it moves all 32
