@@ -9,16 +9,22 @@
 // K/V gradients of user u sum over every candidate of u:
 //   dK[u,h] = scale sum_{i in seg u} dS_i^T Q_i,   dV[u,h] = sum_i P_i^T dO_i.
 //
-// Two persistent kernels, one CTA per SM, 12 warps: warp 0 TMA (elected lane
-// issues), warps 1-3 tcgen05.mma issuers (elected lane; one product chain
-// each, warp 1 also owns TMEM), warps 4-11 the element-wise work: warps w and w+4 share the 32 TMEM lanes of quarter w % 4
-// and split the 128 columns of every tile in halves.
+// A streaming pre-pass, then two persistent kernels, one CTA per SM, 12
+// warps: warp 0 TMA (elected lane issues), warps 1-3 tcgen05.mma issuers
+// (elected lane; one product chain each, warp 1 also owns TMEM), warps 4-11
+// the element-wise work: warps w and w+4 share the 32 TMEM lanes of quarter
+// w % 4 and split the 128 columns of every tile in halves.
+//   attn_bwd_rows_kernel  D = rowsum(dO * O) of every row of every work unit
+//                         (and the forward's LSE in the log2 domain), stored
+//                         in tile order for both kernels; its first block
+//                         also scans the users' key blocks and query tiles.
 //   attn_bwd_dq_kernel    per work-list unit (a 128-row tile of up to
 //                         floor(128/Lq) candidates' queries, as the forward):
-//                         pass 1 forms LSE over the user's key tiles (S
-//                         double-buffered in TMEM), pass 2 recomputes S, forms
-//                         dP and dS (written over S in TMEM) and accumulates
-//                         dQ += dS K.  Stores LSE and D for the next kernel.
+//                         without the forward's LSE, pass 1 forms it over the
+//                         user's key tiles (S double-buffered in TMEM) and
+//                         stores it for the next kernel; pass 2 recomputes S,
+//                         forms dP and dS (written over S in TMEM) and
+//                         accumulates dQ += dS K.
 //   attn_bwd_dkdv_kernel  per (user, head, 128-key block), keys on TMEM lanes:
 //                         for every query tile of the user's candidates, in
 //                         two 64-query halves on alternating TMEM buffers,
@@ -217,11 +223,6 @@ __device__ __forceinline__ DqSmem dq_carve(uint8_t* base) {
   s.tmem_slot = reinterpret_cast<uint32_t*>(b);
   s.abort = s.tmem_slot + 1;
   return s;
-}
-
-// Hint: bring the 128-byte line holding `ptr` into L2.
-__device__ __forceinline__ void prefetch_l2(const void* ptr) {
-  asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));
 }
 
 // A work-list unit: user, head, its candidates perm[start .. start+cnt).
@@ -472,27 +473,12 @@ __global__ void __launch_bounds__(ABWD_THREADS, 1)
         }
         continue;
       }
-      // the forward's LSE for this row, loaded beside O and dO
-      const float lse_in = (p.lse_in && valid) ? p.lse_in[row] : 0.f;
-      // D = rowsum(dO * O) over all of d (both halves compute it: no exchange)
-      float D = 0.f;
-      if (valid) {
-        const uint4* orow = reinterpret_cast<const uint4*>(p.O + row * 128);
-        const uint4* grow = reinterpret_cast<const uint4*>(p.dO + row * 128);
-#pragma unroll 8
-        for (int c = 0; c < 16; ++c) {
-          const uint4 a = __ldg(orow + c), g = __ldg(grow + c);
-          const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, gw[4] = {g.x, g.y, g.z, g.w};
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            D = fmaf(__uint_as_float(aw[k] << 16), __uint_as_float(gw[k] << 16), D);
-            D = fmaf(__uint_as_float(aw[k] & 0xffff0000u), __uint_as_float(gw[k] & 0xffff0000u), D);
-          }
-        }
-      }
+      // the row's D (and the forward's LSE), formed by the pre-pass in tile order
+      const float D = p.Drow[static_cast<size_t>(unit) * 128 + r];
+      const float lse_tile = p.lse_in ? p.lse[static_cast<size_t>(unit) * 128 + r] : 0.f;
       float lse2;
-      if (p.lse_in) {  // the forward's natural-log LSE -> log2 domain; rows without a query: any finite value
-        lse2 = lse_in * 1.4426950408889634f;
+      if (p.lse_in) {  // the forward's LSE (log2 domain; +inf for rows without a query: P = 0)
+        lse2 = lse_tile;
       } else {
         // pass 1: running max and sum over this half's key columns (log2 domain)
         float m = -INFINITY, l = 0.f;
@@ -545,31 +531,10 @@ __global__ void __launch_bounds__(ABWD_THREADS, 1)
         }
         lse2 = l > 0.f ? m + __log2f(l) : INFINITY;
       }
-      if (grp == 0) {  // the unit's 128 tile rows, in tile order, for the dK/dV kernel
+      if (!p.lse_in && grp == 0)  // the unit's 128 tile rows, in tile order, for the dK/dV kernel
         p.lse[static_cast<size_t>(unit) * 128 + r] = valid ? lse2 : INFINITY;
-        p.Drow[static_cast<size_t>(unit) * 128 + r] = valid ? D : 0.f;
-      }
       // pass 2: P = 2^(s sl - lse), dS = P (dP - D) scale written over S.
-      // Over its first three tiles this thread also brings its row of the
-      // next unit's O and dO into L2 (each load has a tile's time to arrive
-      // before its value is used), so the next unit's D starts on L2 hits.
-      const int nunit = unit + static_cast<int>(gridDim.x);
-      int4 nw = make_int4(-1, 0, 0, 0);
-      int ncand = -1;
       for (int jt = 0; jt < x.ntiles; ++jt) {
-        if (jt == 0 && nunit < n_units) {
-          nw = __ldg(reinterpret_cast<const int4*>(p.work) + nunit);
-        } else if (jt == 1) {
-          if (nw.x >= 0 && nw.z >= 0 && slot < nw.w && nw.z + nw.w <= p.n_cand && r < rows)
-            ncand = __ldg(p.perm + nw.z + slot);
-        } else if (jt == 2 && ncand >= 0 && ncand < p.n_cand && nw.y >= 0 && nw.y < p.H) {
-          const size_t nrow = (static_cast<size_t>(ncand) * p.H + nw.y) * p.Lq + q;
-          prefetch_l2(p.O + nrow * 128);
-          prefetch_l2(p.O + nrow * 128 + 64);
-          prefetch_l2(p.dO + nrow * 128);
-          prefetch_l2(p.dO + nrow * 128 + 64);
-          if (p.lse_in) prefetch_l2(p.lse_in + nrow);
-        }
         const uint32_t b = sc & 1u;
         if (!wwait(&s.s_full[b], (sc >> 1) & 1u, s.abort, p.timeout_ns)) goto done;
         ++sc;
@@ -1065,23 +1030,24 @@ __device__ __forceinline__ int user_tiles(const int32_t* offsets, int cpt, int u
   return (max(0, offsets[u + 1] - offsets[u]) + cpt - 1) / cpt;
 }
 
-__global__ void __launch_bounds__(1024) attn_bwd_blocks_kernel(const int32_t* kv_offsets, const int32_t* offsets,
-                                                               int n_users, int Lkv, int cpt, int32_t* blk_prefix,
-                                                               int32_t* tile_prefix) {
-  __shared__ int32_t part[2][1024];
-  const int per = (n_users + 1023) / 1024;
-  const int u0 = threadIdx.x * per;
+// Prefix sums over the users of their key blocks and query tiles (for the
+// dK/dV kernel's work numbering), by one block of ROWS_THREADS threads.
+constexpr int ROWS_THREADS = 256;
+__device__ void user_prefixes(const AttnBwdParams& p) {
+  __shared__ int32_t part[2][ROWS_THREADS];
+  const int per = (p.n_users + ROWS_THREADS - 1) / ROWS_THREADS;
+  const int u0 = static_cast<int>(threadIdx.x) * per;
   int32_t sb = 0, st = 0;
-  for (int u = u0; u < min(u0 + per, n_users); ++u) {
-    sb += user_blocks(kv_offsets, Lkv, u);
-    st += user_tiles(offsets, cpt, u);
+  for (int u = u0; u < min(u0 + per, p.n_users); ++u) {
+    sb += user_blocks(p.kv_offsets, p.Lkv, u);
+    st += user_tiles(p.offsets, p.cands_per_tile, u);
   }
   part[0][threadIdx.x] = sb;
   part[1][threadIdx.x] = st;
   __syncthreads();
-  for (int w = 1; w < 1024; w <<= 1) {  // inclusive scans of the chunk sums
-    const int32_t vb = threadIdx.x >= w ? part[0][threadIdx.x - w] : 0;
-    const int32_t vt = threadIdx.x >= w ? part[1][threadIdx.x - w] : 0;
+  for (int w = 1; w < ROWS_THREADS; w <<= 1) {  // inclusive scans of the chunk sums
+    const int32_t vb = static_cast<int>(threadIdx.x) >= w ? part[0][threadIdx.x - w] : 0;
+    const int32_t vt = static_cast<int>(threadIdx.x) >= w ? part[1][threadIdx.x - w] : 0;
     __syncthreads();
     part[0][threadIdx.x] += vb;
     part[1][threadIdx.x] += vt;
@@ -1089,15 +1055,63 @@ __global__ void __launch_bounds__(1024) attn_bwd_blocks_kernel(const int32_t* kv
   }
   int32_t rb = threadIdx.x > 0 ? part[0][threadIdx.x - 1] : 0;
   int32_t rt = threadIdx.x > 0 ? part[1][threadIdx.x - 1] : 0;
-  for (int u = u0; u < min(u0 + per, n_users); ++u) {
+  int32_t* blk_prefix = const_cast<int32_t*>(p.blk_prefix);
+  int32_t* tile_prefix = const_cast<int32_t*>(p.tile_prefix);
+  for (int u = u0; u < min(u0 + per, p.n_users); ++u) {
     blk_prefix[u] = rb;
     tile_prefix[u] = rt;
-    rb += user_blocks(kv_offsets, Lkv, u);
-    rt += user_tiles(offsets, cpt, u);
+    rb += user_blocks(p.kv_offsets, p.Lkv, u);
+    rt += user_tiles(p.offsets, p.cands_per_tile, u);
   }
-  if (threadIdx.x == 1023) {
-    blk_prefix[n_users] = part[0][1023];
-    tile_prefix[n_users] = part[1][1023];
+  if (threadIdx.x == ROWS_THREADS - 1) {
+    blk_prefix[p.n_users] = part[0][ROWS_THREADS - 1];
+    tile_prefix[p.n_users] = part[1][ROWS_THREADS - 1];
+  }
+}
+
+// Row statistics in tile order: for tile row r of work unit w (candidate
+// perm[start + r / Lq], query r % Lq), Drow[w][r] = sum_d dO[row][d] O[row][d]
+// and, given the forward's natural-log LSE, lse[w][r] = LSE[row] log2(e);
+// rows without a query get D = 0 and lse = +inf.  Half a warp per row, 16
+// bytes of O and of dO per lane; blocks stride over the units' rows.  Block 0
+// computes the user prefixes instead.
+__global__ void __launch_bounds__(ROWS_THREADS) attn_bwd_rows_kernel(const AttnBwdParams p) {
+  if (blockIdx.x == 0) {
+    user_prefixes(p);
+    return;
+  }
+  const int n_units = *p.n_units;
+  const int rows = p.cands_per_tile * p.Lq;
+  const int sub = static_cast<int>(threadIdx.x & 15u);                               // lane within the row
+  const long long nrows = static_cast<long long>(n_units) * 128;
+  const long long stride = static_cast<long long>(gridDim.x - 1) * (ROWS_THREADS / 16);
+  for (long long t = static_cast<long long>(blockIdx.x - 1) * (ROWS_THREADS / 16) + (threadIdx.x >> 4); t < nrows;
+       t += stride) {
+    const int unit = static_cast<int>(t >> 7), r = static_cast<int>(t & 127);
+    const int4 w = __ldg(reinterpret_cast<const int4*>(p.work) + unit);
+    const int slot = r / p.Lq, q = r - slot * p.Lq;
+    const bool valid = r < rows && slot < w.w && w.x >= 0 && w.x < p.n_users && w.y >= 0 && w.y < p.H &&
+                       w.z >= 0 && w.z + w.w <= p.n_cand;
+    float D = 0.f, lse = INFINITY;
+    if (valid) {
+      const int cand = __ldg(p.perm + w.z + slot);
+      const size_t row = (static_cast<size_t>(cand) * p.H + w.y) * p.Lq + q;
+      const uint4 a = __ldcs(reinterpret_cast<const uint4*>(p.O + row * 128) + sub);
+      const uint4 g = __ldcs(reinterpret_cast<const uint4*>(p.dO + row * 128) + sub);
+      const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, gw[4] = {g.x, g.y, g.z, g.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        D = fmaf(__uint_as_float(aw[k] << 16), __uint_as_float(gw[k] << 16), D);
+        D = fmaf(__uint_as_float(aw[k] & 0xffff0000u), __uint_as_float(gw[k] & 0xffff0000u), D);
+      }
+      if (p.lse_in) lse = __ldg(p.lse_in + row) * 1.4426950408889634f;
+    }
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) D += __shfl_xor_sync(0xffffffffu, D, o);  // within the 16 lanes of the row
+    if (sub == 0) {
+      p.Drow[t] = valid ? D : 0.f;
+      if (p.lse_in) p.lse[t] = lse;
+    }
   }
 }
 
@@ -1110,8 +1124,7 @@ cudaError_t launch_attn_backward(const CUtensorMap& tmQ, const CUtensorMap& tmDO
                                  const CUtensorMap& tmV, const AttnBwdParams& p, int grid, cudaStream_t s,
                                  int* launches) {
   *launches = 0;
-  attn_bwd_blocks_kernel<<<1, 1024, 0, s>>>(p.kv_offsets, p.offsets, p.n_users, p.Lkv, p.cands_per_tile,
-                                            const_cast<int32_t*>(p.blk_prefix), const_cast<int32_t*>(p.tile_prefix));
+  attn_bwd_rows_kernel<<<1 + 8 * grid, ROWS_THREADS, 0, s>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   ++*launches;
