@@ -33,6 +33,12 @@ cudaError_t launch_bwd_act(const CUtensorMap& tmX, const CUtensorMap& tmW, const
                            cudaStream_t s);
 bool bwd_wgrad_configure(WgradParams* p, int num_sms, size_t max_smem);
 size_t bwd_wgrad_part_elems(const WgradParams& p);
+bool bwd_cand_configure(CandParams* p, size_t max_smem);
+int bwd_cand_grid(const CandParams& p, int num_sms);
+cudaError_t launch_bwd_cand(const CUtensorMap& tmDY, const CUtensorMap& tmC, const CandParams& p, int grid,
+                            cudaStream_t s);
+cudaError_t launch_bwd_sfinish(const SFinishParams& p, cudaStream_t s);
+cudaError_t launch_bwd_wreduce(const float* part, float* dW, int M, int N, int R, cudaStream_t s);
 cudaError_t launch_bwd_wgrad(const CUtensorMap& tmA, const CUtensorMap& tmG, const WgradParams& p, float* dW,
                              int num_sms, cudaStream_t s, int* launches);
 size_t attn_bwd_smem_bytes();
@@ -74,6 +80,10 @@ struct ikbo_plan_s {
   size_t bwd_seg_elems = 0;
   float* d_bwd_wpart = nullptr;
   size_t bwd_wpart_elems = 0;
+  float* d_bwd_spart = nullptr;  // candidate pass: S partials of each CTA's first and last run
+  size_t bwd_spart_elems = 0;
+  long long* d_bwd_bounds = nullptr;  // candidate pass: the CTAs' tile ranges
+  size_t bwd_bounds_elems = 0;
   // attention backward workspaces
   float* d_abwd_lse = nullptr;
   size_t abwd_lse_elems = 0;
@@ -161,6 +171,8 @@ void free_plan(ikbo_plan_t p) {
   cudaFree(p->d_bwd_Sb);
   cudaFree(p->d_bwd_seg);
   cudaFree(p->d_bwd_wpart);
+  cudaFree(p->d_bwd_spart);
+  cudaFree(p->d_bwd_bounds);
   cudaFree(p->d_abwd_lse);
   cudaFree(p->d_abwd_drow);
   cudaFree(p->d_abwd_blk);
@@ -586,7 +598,16 @@ ikbo_status_t ikbo_lce_backward(ikbo_plan_t p, const void* U, const void* C, con
   if (D % 8 != 0 || N % 8 != 0 || N > 256) return IKBO_ERR_UNSUPPORTED;
   const int n_cand = p->n_cand, n_users = p->n_users;
 
-  // configure every product that is asked for before launching anything
+  // configure every product that is asked for before launching anything.
+  // dW_c and the segment sum S run as one candidate pass, which reads dY and
+  // C once, where the shape allows it (K_c <= 256, N <= 192); else as a
+  // segment-sum kernel and a weight-gradient kernel.  dC is the
+  // activation-gradient kernel in either case.
+  const bool need_S = dU || dWu || db;
+  CandParams cp{};
+  cp.n_cand = n_cand, cp.n_users = n_users, cp.K_c = K_c, cp.D = D, cp.N = N;
+  const bool use_cand = (dWc || need_S) && bwd_cand_configure(&cp, p->max_smem);
+  const int cgrid = use_cand ? bwd_cand_grid(cp, p->num_sms) : 0;
   ActParams ac{}, au{};
   WgradParams wc{}, wu{};
   ac.B = n_cand, ac.M = K_c, ac.D = D, ac.N = N;
@@ -595,12 +616,12 @@ ikbo_status_t ikbo_lce_backward(ikbo_plan_t p, const void* U, const void* C, con
   wu.M = K_u, wu.D = D, wu.N = N;
   wu.B = 2 * n_users;  // G = the hi/lo pair of S per user; A = U[b >> 1]
   wu.a_shift = 1;
-  if ((dC && !bwd_act_configure(&ac, p->max_smem, false)) || (dU && !bwd_act_configure(&au, p->max_smem, true)) ||
-      (dWc && !bwd_wgrad_configure(&wc, p->num_sms, p->max_smem)) ||
+  if ((dC && !bwd_act_configure(&ac, p->max_smem, false)) ||
+      (dU && !bwd_act_configure(&au, p->max_smem, true)) ||
+      (!use_cand && dWc && !bwd_wgrad_configure(&wc, p->num_sms, p->max_smem)) ||
       (dWu && !bwd_wgrad_configure(&wu, p->num_sms, p->max_smem)))
     return IKBO_ERR_UNSUPPORTED;
 
-  const bool need_S = dU || dWu || db;
   const int ND = N * D;
   const int NP = (N + 63) / 64 * 64;  // rows per half of the hi/lo pair
   SegSumParams sp{};
@@ -612,10 +633,15 @@ ikbo_status_t ikbo_lce_backward(ikbo_plan_t p, const void* U, const void* C, con
     if (grow(&p->d_bwd_S, &p->bwd_S_elems, nS, stream) != cudaSuccess ||
         grow(&p->d_bwd_Sb, &p->bwd_Sb_elems, static_cast<size_t>(n_users) * 2 * NP * D, stream) != cudaSuccess)
       return IKBO_ERR_CUDA;
-    if (sp.nch > 1 && grow(&p->d_bwd_seg, &p->bwd_seg_elems, nS * sp.nch, stream) != cudaSuccess) return IKBO_ERR_CUDA;
+    if (!use_cand && sp.nch > 1 && grow(&p->d_bwd_seg, &p->bwd_seg_elems, nS * sp.nch, stream) != cudaSuccess)
+      return IKBO_ERR_CUDA;
+    if (use_cand &&
+        (grow(&p->d_bwd_spart, &p->bwd_spart_elems, static_cast<size_t>(cgrid) * 2 * N * 128, stream) != cudaSuccess ||
+         grow(&p->d_bwd_bounds, &p->bwd_bounds_elems, static_cast<size_t>(cgrid) + 1, stream) != cudaSuccess))
+      return IKBO_ERR_CUDA;
   }
   size_t wpart = 0;
-  if (dWc) wpart = bwd_wgrad_part_elems(wc);
+  if (dWc) wpart = use_cand ? static_cast<size_t>(cp.n_mblk) * cgrid * 128 * N : bwd_wgrad_part_elems(wc);
   if (dWu && bwd_wgrad_part_elems(wu) > wpart) wpart = bwd_wgrad_part_elems(wu);
   if (wpart && grow(&p->d_bwd_wpart, &p->bwd_wpart_elems, wpart, stream) != cudaSuccess) return IKBO_ERR_CUDA;
 
@@ -634,6 +660,8 @@ ikbo_status_t ikbo_lce_backward(ikbo_plan_t p, const void* U, const void* C, con
   const uint32_t wbox[2] = {64, 128};
   CUtensorMap tmDY, tmSX, tmSG, tmWc, tmWu, tmC, tmU;
   if (!encode_bf16(&tmDY, dY, 3, dyd, dys, box64)) return IKBO_ERR_CUDA;
+  tmWc = tmDY;  // placeholders, not read where the product is not asked for
+  tmC = tmDY;
   if (need_S && (!encode_bf16(&tmSX, p->d_bwd_Sb, 3, s2x, s2xs, box64) ||
                  !encode_bf16(&tmSG, p->d_bwd_Sb, 3, s2g, s2gs, box64)))
     return IKBO_ERR_CUDA;
@@ -660,20 +688,52 @@ ikbo_status_t ikbo_lce_backward(ikbo_plan_t p, const void* U, const void* C, con
 
   int launches = 0;
   cudaError_t e = cudaSuccess;
-  if (need_S) {
+  // rows N .. NP-1 of each half of the S pair must read as zeros
+  if (need_S && NP != N)
+    e = cudaMemsetAsync(p->d_bwd_Sb, 0, sizeof(uint16_t) * static_cast<size_t>(n_users) * 2 * NP * D, stream);
+  if (e == cudaSuccess && use_cand) {
+    cp.perm = p->d_perm;
+    cp.map = p->d_map;
+    cp.wpart = dWc ? p->d_bwd_wpart : nullptr;
+    cp.S = need_S ? p->d_bwd_S : nullptr;
+    cp.spart = p->d_bwd_spart;
+    cp.bounds = p->d_bwd_bounds;
+    cp.status = p->d_status;
+    cp.timeout_ns = p->timeout_ns;
+    e = launch_bwd_cand(tmDY, tmC, cp, cgrid, stream);
+    if (e == cudaSuccess) ++launches;
+    if (e == cudaSuccess && need_S) {
+      SFinishParams fp{};
+      fp.offsets = p->d_offsets;
+      fp.S = p->d_bwd_S;
+      fp.spart = p->d_bwd_spart;
+      fp.bounds = p->d_bwd_bounds;
+      fp.S2 = p->d_bwd_Sb;
+      fp.n_cand = n_cand;
+      fp.n_users = n_users;
+      fp.N = N;
+      fp.D = D;
+      fp.NPD = NP * D;
+      fp.n_dblk = cp.n_dblk;
+      fp.G = cgrid;
+      e = launch_bwd_sfinish(fp, stream);
+      if (e == cudaSuccess) ++launches;
+    }
+    if (e == cudaSuccess && dWc) {
+      e = launch_bwd_wreduce(p->d_bwd_wpart, dWc, K_c, N, cgrid, stream);
+      if (e == cudaSuccess) ++launches;
+    }
+  } else if (e == cudaSuccess && need_S) {
     sp.dY = static_cast<const uint16_t*>(dY);
     sp.offsets = p->d_offsets;
     sp.perm = p->d_perm;
     sp.S = p->d_bwd_S;
     sp.S2 = p->d_bwd_Sb;
-    // rows N .. NP-1 of each half must read as zeros
-    if (NP != N)
-      e = cudaMemsetAsync(p->d_bwd_Sb, 0, sizeof(uint16_t) * static_cast<size_t>(n_users) * 2 * NP * D, stream);
     sp.part = p->d_bwd_seg;
     sp.n_cand = n_cand;
     sp.n_users = n_users;
     sp.ND = ND;
-    if (e == cudaSuccess) e = launch_bwd_segsum(sp, stream, &launches);
+    e = launch_bwd_segsum(sp, stream, &launches);
   }
   if (e == cudaSuccess && db) {
     e = launch_bwd_db(p->d_bwd_S, db, n_users, N, D, stream);
@@ -686,7 +746,7 @@ ikbo_status_t ikbo_lce_backward(ikbo_plan_t p, const void* U, const void* C, con
     e = launch_bwd_act(tmDY, tmWc, ac, p->num_sms, stream);
     if (e == cudaSuccess) ++launches;
   }
-  if (e == cudaSuccess && dWc) {
+  if (e == cudaSuccess && dWc && !use_cand) {
     wc.part = p->d_bwd_wpart;
     wc.status = p->d_status;
     wc.timeout_ns = p->timeout_ns;

@@ -193,6 +193,52 @@ struct WgradParams {
   uint64_t timeout_ns;
 };
 
+// Candidate pass of the LCE backward, one persistent launch that reads each
+// candidate's dY and C once: per tile (candidate b = perm[pos], 128-row
+// block of D), in the plan's user-grouped order,
+//   dW_c  += C[b] dY[b]^T                 (TMEM, <= 2 blocks of 128 K_c rows, per CTA)
+//   S[u]  += dY[b]                        (epilogue warps, from the staged dY tile)
+// dY stays in shared memory for the tile (two tile slots); C streams through
+// a ring of 16 KB slots.  dW_c leaves as per-CTA partials (the wgrad reduce
+// adds them in CTA order); S as direct stores for runs of (user, D block)
+// inside one CTA's range and as two partial slots per CTA (the range's first
+// and last run) added in CTA order by bwd_sfinish_kernel.  Applies when
+// K_c <= 256 and N <= 192.  (dC = W_c dY stays with the activation-gradient
+// kernel, which keeps W_c in shared memory: streaming W_c beside C, one
+// 96 KB copy per tile, starved this kernel's ring.)
+constexpr int BWD_CAND_SLOTS = 8;                    // 16 KB C slots
+constexpr int BWD_CAND_DY_BYTES = 2 * 3 * 64 * 64 * 2;  // a dY tile: 2 d halves x <= 3 n chunks of 64 x 64
+constexpr int BWD_CAND_MAX_N = 192;
+constexpr int BWD_CAND_MAX_KC = 256;
+
+struct CandParams {
+  const int32_t* perm;       // [n_cand] the plan's user-grouped order (out-of-range candidates last)
+  const int32_t* map;        // [n_cand]
+  float* wpart;              // [n_mblk][G][128][N] fp32 dW_c partials (G = grid), or null (no dW_c)
+  float* S;                  // [n_users][N][D] fp32, or null (no S)
+  float* spart;              // [G][2][N][128] fp32 S partials of each CTA's first and last run
+  long long* bounds;         // [G + 1] each CTA's first tile (and the tile count), for the S finish
+  uint32_t* status;
+  int n_cand, n_users, K_c, D, N;
+  int n_dblk;                // ceil(D / 128)
+  int kcn;                   // ceil(N / 64): dY n chunks (<= 3)
+  int n_mblk;                // ceil(K_c / 128): dW_c blocks (1 or 2)
+  int n_mma;                 // roundup(N, 16): dW_c accumulator columns per block
+  uint64_t timeout_ns;
+};
+
+// S finish: for every (user, D block), S = the sum of its partial slots in
+// CTA order (or, for a run inside one CTA's range, the direct value), in
+// fp32 and as the bf16 hi/lo pair the user-side products read.
+struct SFinishParams {
+  const int32_t* offsets;    // [n_users + 1] the plan's segment offsets
+  float* S;                  // [n_users][N][D]
+  const float* spart;        // [G][2][N][128]
+  const long long* bounds;   // [G + 1] the candidate pass's CTA ranges
+  uint16_t* S2;              // [n_users][2][NP][D] hi, lo
+  int n_cand, n_users, N, D, NPD, n_dblk, G;
+};
+
 // ----------------------------------------------------------- attention
 constexpr int ATT_BM = 128;        // query rows per tile (TMEM lanes)
 constexpr int ATT_BN = 128;        // keys per K/V tile

@@ -573,6 +573,404 @@ __global__ void __launch_bounds__(WG_RED_OUT* WG_RED_SPLIT)
   }
 }
 
+// ============================================================ candidate pass
+// See CandParams.  Per CTA (one per SM, 12 warps): warp 0 TMA producer,
+// warp 1 MMA issuer, warp 2 TMEM owner, warps 4-11 epilogue (S sums).
+// Tiles q = dblk * n_cand + pos (D-block-major over the plan's grouped
+// order), one contiguous range per CTA, so a CTA's consecutive tiles share a
+// user and its S sums stay in registers.
+// TMEM columns: dW_c block 0 [0, n_mma), block 1 [n_mma, 2 n_mma) (lanes =
+// K_c rows, columns = n), accumulated over the CTA's tiles.
+// Shared memory: two dY tile slots, each [d half][n rows][64 d] (128-byte
+// rows, 128-byte swizzle), read K-major as dW_c's B; then the ring of 16 KB
+// C slots, per tile one per (128-row block of K_c, 64-d half).
+constexpr uint32_t CB_SLOT = 128 * 64 * 2;  // 16 KB: 128 rows x 64 bf16
+constexpr uint32_t CB_DYHALF = 3 * BOX;     // one d half of a dY tile (<= 192 n rows)
+constexpr uint32_t CAND_TILES = 2 * BWD_CAND_DY_BYTES + BWD_CAND_SLOTS * CB_SLOT;
+constexpr int CAND_BARS = 4 + 2 * BWD_CAND_SLOTS + 1;
+constexpr size_t CAND_SMEM = 1024 + CAND_TILES + 8 * CAND_BARS + 8;
+static_assert(CAND_SMEM <= 227 * 1024, "candidate pass does not fit in shared memory");
+
+struct CandSmem {
+  uint8_t* dy;
+  uint8_t* ring;
+  uint64_t* dy_full;   // [2]
+  uint64_t* dy_empty;  // [2] MMA reads done (commit) and the S sums taken
+  uint64_t* st_full;   // [SLOTS]
+  uint64_t* st_empty;  // [SLOTS]
+  uint64_t* w_full;    // the CTA's dW_c partial is complete in TMEM
+  uint32_t* tmem_slot;
+  uint32_t* abort;
+};
+
+__device__ __forceinline__ CandSmem cand_carve(uint8_t* base) {
+  CandSmem s;
+  s.dy = base;
+  s.ring = base + 2 * BWD_CAND_DY_BYTES;
+  uint64_t* b = reinterpret_cast<uint64_t*>(base + CAND_TILES);
+  s.dy_full = b;
+  s.dy_empty = b + 2;
+  s.st_full = b + 4;
+  s.st_empty = s.st_full + BWD_CAND_SLOTS;
+  s.w_full = s.st_empty + BWD_CAND_SLOTS;
+  s.tmem_slot = reinterpret_cast<uint32_t*>(s.w_full + 1);
+  s.abort = s.tmem_slot + 1;
+  return s;
+}
+
+__device__ __forceinline__ void cand_range(const CandParams& p, long long& q0, long long& q1) {
+  const long long nq = static_cast<long long>(p.n_dblk) * p.n_cand;
+  q0 = blockIdx.x * nq / gridDim.x;
+  q1 = (blockIdx.x + 1) * nq / gridDim.x;
+}
+
+// The candidate (and its user, -1 if out of range) of tile q, looked up by
+// the warp 32 tiles at a time: lane l holds tile wbase + l.
+struct CandWin {
+  long long base = -1;
+  int b = 0, u = -1;
+};
+__device__ __forceinline__ void cand_tile(const CandParams& p, long long q, long long q1, CandWin& w, int& b, int& u) {
+  if (w.base < 0 || q >= w.base + 32) {
+    w.base = q;
+    const long long ql = q + static_cast<long long>(lane_id());
+    w.b = 0;
+    w.u = -1;
+    if (ql < q1) {
+      const int pos = static_cast<int>(ql % p.n_cand);
+      const int bb = __ldg(p.perm + pos);
+      w.b = (bb >= 0 && bb < p.n_cand) ? bb : 0;
+      const int uu = (bb >= 0 && bb < p.n_cand) ? __ldg(p.map + bb) : -1;
+      w.u = (uu >= 0 && uu < p.n_users) ? uu : -1;
+    }
+  }
+  const int k = static_cast<int>(q - w.base);
+  b = __shfl_sync(0xffffffffu, w.b, k);
+  u = __shfl_sync(0xffffffffu, w.u, k);
+}
+
+struct SlotRing {
+  int slot = 0;
+  uint32_t phase = 0;
+  __device__ __forceinline__ void next() {
+    if (++slot == BWD_CAND_SLOTS) {
+      slot = 0;
+      phase ^= 1u;
+    }
+  }
+};
+
+// S sums of a run (user u, D block dblk) of this CTA: the run inside the
+// CTA's range goes straight to S; the range's first run to partial slot 0,
+// its last (when another) to slot 1.  Thread: d pair 2pd, 2pd+1 of the block,
+// rows n = 64 j + 16 ng + i.
+__device__ __forceinline__ void cand_flush(const CandParams& p, const float (&acc)[3][16][2], int u, int dblk,
+                                           int slot, int pd, int ng) {
+  const int d = 2 * pd;
+  const bool dok = dblk * 128 + d < p.D;  // D is a multiple of 8: both of the pair or neither
+#pragma unroll
+  for (int j = 0; j < 3; ++j)
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int n = 64 * j + 16 * ng + i;
+      if (n >= p.N || !dok) continue;
+      float2* dst = slot < 0 ? reinterpret_cast<float2*>(p.S + (static_cast<size_t>(u) * p.N + n) * p.D + dblk * 128 + d)
+                             : reinterpret_cast<float2*>(p.spart +
+                                                         ((static_cast<size_t>(blockIdx.x) * 2 + slot) * p.N + n) * 128 + d);
+      *dst = make_float2(acc[j][i][0], acc[j][i][1]);
+    }
+}
+
+__global__ void __launch_bounds__(BWD_THREADS, 1)
+    bwd_cand_kernel(const __grid_constant__ CUtensorMap tmDY, const __grid_constant__ CUtensorMap tmC,
+                    const CandParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const CandSmem s = cand_carve(base);
+  const int warp = threadIdx.x >> 5;
+  const bool do_s = p.S != nullptr;
+  const bool do_w = p.wpart != nullptr;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s.dy_full[i], 1);
+      mbar_init(&s.dy_empty[i], 1 + (do_s ? BWD_THREADS - 128 : 0));
+    }
+    for (int i = 0; i < BWD_CAND_SLOTS; ++i) {
+      mbar_init(&s.st_full[i], 1);
+      mbar_init(&s.st_empty[i], 1);
+    }
+    mbar_init(s.w_full, 1);
+    *s.abort = 0;
+    fence_barrier_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == 0 && lane_id() == 0) {
+    tma_prefetch_desc(&tmDY);
+    if (do_w) tma_prefetch_desc(&tmC);
+  }
+  if (warp == 2) {
+    tmem_alloc(s.tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *s.tmem_slot;
+  long long q0, q1;
+  cand_range(p, q0, q1);
+  if (threadIdx.x == 0 && do_s) {  // the range, for the S finish
+    p.bounds[blockIdx.x] = q0;
+    if (blockIdx.x + 1 == gridDim.x) p.bounds[gridDim.x] = q1;
+  }
+  const int nc = do_w ? 2 * p.n_mblk : 0;  // C slots per tile
+  const uint32_t dy_bytes = static_cast<uint32_t>(2 * p.kcn) * BOX;
+
+  if (warp == 0) {
+    // ---- TMA producer: the dY tile into its slot, then the tile's C slots
+    CandWin win;
+    SlotRing ring;
+    int t = 0;
+    for (long long q = q0; q < q1; ++q, ++t) {
+      int b, u;
+      cand_tile(p, q, q1, win, b, u);
+      const int dblk = static_cast<int>(q / p.n_cand);
+      const int y = t & 1;
+      if (!warp_wait(&s.dy_empty[y], ((t >> 1) & 1) ^ 1u, s.abort, p.timeout_ns)) goto done;
+      if (elect_one()) {
+        uint8_t* dst = s.dy + y * BWD_CAND_DY_BYTES;
+        mbar_arrive_expect_tx(&s.dy_full[y], dy_bytes);
+        for (int h = 0; h < 2; ++h)
+          for (int j = 0; j < p.kcn; ++j)
+            tma_load_3d(dst + h * CB_DYHALF + j * BOX, &tmDY, &s.dy_full[y], dblk * 128 + 64 * h, 64 * j, b);
+      }
+      __syncwarp();
+      for (int c = 0; c < nc; ++c, ring.next()) {  // C block c / 2, d half c % 2
+        if (!warp_wait(&s.st_empty[ring.slot], ring.phase ^ 1u, s.abort, p.timeout_ns)) goto done;
+        if (elect_one()) {
+          uint64_t* bar = &s.st_full[ring.slot];
+          mbar_arrive_expect_tx(bar, CB_SLOT);
+          tma_load_3d(s.ring + ring.slot * CB_SLOT, &tmC, bar, dblk * 128 + 64 * (c & 1), 128 * (c >> 1), b);
+        }
+        __syncwarp();
+      }
+    }
+  } else if (warp == 1) {
+    // ---- MMA issuer: dW_c[m][n] += C[b][m][d] dY[b][n][d]; A = the C slot
+    // (K-major), B = a dY d half (K-major, n rows), 4 steps of 16 d per slot
+    SlotRing ring;
+    const uint32_t idesc = idesc_bf16_f32(128, static_cast<uint32_t>(p.n_mma), false, false);
+    int t = 0;
+    for (long long q = q0; q < q1; ++q, ++t) {
+      const int y = t & 1;
+      if (!warp_wait(&s.dy_full[y], (t >> 1) & 1u, s.abort, p.timeout_ns)) goto done;
+      tc_fence_after();
+      const uint32_t dy_base = smem_u32(s.dy + y * BWD_CAND_DY_BYTES);
+      for (int c = 0; c < nc; ++c, ring.next()) {
+        if (!warp_wait(&s.st_full[ring.slot], ring.phase, s.abort, p.timeout_ns)) goto done;
+        tc_fence_after();
+        if (elect_one()) {
+          const uint64_t adesc = sdesc_sw128(smem_u32(s.ring + ring.slot * CB_SLOT), 16, 1024u);
+          const uint64_t bdesc = sdesc_sw128(dy_base + (c & 1) * CB_DYHALF, 16, 1024u);
+          const uint32_t d_tmem = tmem + static_cast<uint32_t>((c >> 1) * p.n_mma);
+#pragma unroll
+          for (int st = 0; st < 4; ++st)
+            mma_bf16_ss(d_tmem, adesc + st * (32u >> 4), bdesc + st * (32u >> 4), idesc,
+                        (t == 0 && (c & 1) == 0 && st == 0) ? 0u : 1u);
+          mma_commit(&s.st_empty[ring.slot]);
+        }
+        __syncwarp();
+      }
+      if (elect_one()) mma_commit(&s.dy_empty[y]);  // every product of this tile has read dY
+      __syncwarp();
+    }
+    if (elect_one()) mma_commit(s.w_full);
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ---- epilogue: the S sums, then the CTA's dW_c partial
+    const int et = static_cast<int>(threadIdx.x) - 128;
+    const int quarter = warp & 3, half = (warp - 4) >> 2;
+    const uint32_t lane_base = static_cast<uint32_t>(32 * quarter) << 16;
+    const int pd = et & 63, ng = et >> 6;  // S: d pair, group of 16 n rows in each 64-n chunk
+    if (do_s) {
+      float acc[3][16][2];
+#pragma unroll
+      for (int j = 0; j < 3; ++j)
+#pragma unroll
+        for (int i = 0; i < 16; ++i) acc[j][i][0] = acc[j][i][1] = 0.f;
+      // the open run of (user, D block); whether it holds the range's first
+      // tile (its sums go to slot 0) and whether the last tile seen was in it
+      int run_u = -2, run_dblk = -1;
+      bool run_first = false, last_in_run = false, bad_seen = false;
+      CandWin win;
+      int t = 0;
+      for (long long q = q0; q < q1; ++q, ++t) {
+        int b, u;
+        cand_tile(p, q, q1, win, b, u);
+        const int dblk = static_cast<int>(q / p.n_cand);
+        const int y = t & 1;
+        if (!warp_wait(&s.dy_full[y], (t >> 1) & 1u, s.abort, p.timeout_ns)) goto done;
+        if (u < 0) {  // out of range: in no user's sum (candidates after the valid ones in perm)
+          bad_seen = true;
+          last_in_run = false;
+        } else {
+          if (u != run_u || dblk != run_dblk) {
+            if (run_u >= 0) {  // a run ends inside the range: slot 0 if it held the first tile, else S
+              cand_flush(p, acc, run_u, run_dblk, run_first ? 0 : -1, pd, ng);
+#pragma unroll
+              for (int j = 0; j < 3; ++j)
+#pragma unroll
+                for (int i = 0; i < 16; ++i) acc[j][i][0] = acc[j][i][1] = 0.f;
+            }
+            run_first = q == q0;
+          }
+          run_u = u;
+          run_dblk = dblk;
+          last_in_run = true;
+          // this thread's 96 elements of the staged tile: d half pd / 32,
+          // byte (2 pd % 64) * 2 of row n, 16-byte chunk swizzled by n % 8
+          const uint8_t* tile = s.dy + y * BWD_CAND_DY_BYTES + (pd >> 5) * CB_DYHALF;
+          const int dd = (2 * pd) & 63;
+#pragma unroll
+          for (int j = 0; j < 3; ++j) {
+            if (j < p.kcn) {
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                const int n = 64 * j + 16 * ng + i;
+                const uint32_t w = *reinterpret_cast<const uint32_t*>(
+                    tile + n * 128 + ((((dd >> 3) ^ (n & 7)) << 4) | ((dd & 7) << 1)));
+                acc[j][i][0] += __uint_as_float(w << 16);
+                acc[j][i][1] += __uint_as_float(w & 0xffff0000u);
+              }
+            }
+          }
+        }
+        mbar_arrive(&s.dy_empty[y]);
+      }
+      // the open run: slot 0 if it held the first tile; else slot 1 if it runs
+      // past the range's end (its last tile was the range's), else S
+      if (run_u >= 0) cand_flush(p, acc, run_u, run_dblk, run_first ? 0 : (last_in_run ? 1 : -1), pd, ng);
+      if (bad_seen && et == 0) atomicOr(p.status, DEV_ERR_MAP_RANGE);
+    }
+    // the CTA's dW_c partial: TMEM lane = K_c row of a block, columns = n
+    if (do_w && q1 > q0) {
+      if (!warp_wait(s.w_full, 0, s.abort, p.timeout_ns)) goto done;
+      tc_fence_after();
+      const int row = quarter * 32 + static_cast<int>(lane_id());
+      const int nchunks = (p.N + 31) / 32;
+      for (int mb = 0; mb < p.n_mblk; ++mb) {
+        float* out = p.wpart + (static_cast<size_t>(mb * gridDim.x + blockIdx.x) * 128 + row) * p.N;
+        for (int c = half; c < nchunks; c += 2) {
+          uint32_t v[32];
+          tmem_ld32(tmem + lane_base + static_cast<uint32_t>(mb * p.n_mma + c * 32), v);
+          tmem_ld_wait(v);
+          if (c * 32 + 32 <= p.N) {
+            float4* o4 = reinterpret_cast<float4*>(out + c * 32);
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              o4[k] = make_float4(__uint_as_float(v[4 * k]), __uint_as_float(v[4 * k + 1]),
+                                  __uint_as_float(v[4 * k + 2]), __uint_as_float(v[4 * k + 3]));
+          } else {
+#pragma unroll
+            for (int k = 0; k < 32; ++k)
+              if (c * 32 + k < p.N) out[c * 32 + k] = __uint_as_float(v[k]);
+          }
+        }
+      }
+    }
+  }
+done:
+  tc_fence_before();
+  __syncthreads();
+  if (*s.abort && threadIdx.x == 0) atomicOr(p.status, DEV_ERR_PIPE_TIMEOUT);
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// S of (user u, D block dblk, slice of N x 128 elements): the run's tiles
+// [a, a + cnt) in q order; a run inside one CTA's range that is neither its
+// first nor its last run was stored straight to S; otherwise the partial
+// slots of the CTAs that share it are added in CTA order (slot 0 where the
+// run holds the CTA's first tile, else slot 1).  Then the hi/lo pair.
+constexpr int SF_THREADS = 256;
+constexpr int SF_ELEMS = 4 * SF_THREADS;  // elements per block
+constexpr int SF_MAX_CTAS = 1024;  // contributors a run may have (the grid never exceeds the SM count)
+__global__ void __launch_bounds__(SF_THREADS) bwd_sfinish_kernel(const SFinishParams p) {
+  __shared__ int c_lo, c_n, c_direct;
+  __shared__ uint32_t c_slot[SF_MAX_CTAS / 32];  // bit k: contributor c_lo + k reads slot 1
+  const int elems = p.N * 128;
+  const int slices = (elems + SF_ELEMS - 1) / SF_ELEMS;
+  const int sl = blockIdx.x % slices;
+  const int ud = blockIdx.x / slices;
+  const int u = ud / p.n_dblk, dblk = ud - u * p.n_dblk;
+  if (u >= p.n_users) return;  // uniform over the block
+  const long long a = static_cast<long long>(dblk) * p.n_cand + __ldg(p.offsets + u);
+  const long long e = static_cast<long long>(dblk) * p.n_cand + __ldg(p.offsets + u + 1);
+  // the run's contributing CTAs and the slot each holds it in, once per
+  // block: every thread tests the ranges [bounds[k], bounds[k + 1]) at once
+  if (threadIdx.x == 0) {
+    c_lo = 0;
+    c_n = 0;
+    c_direct = 0;
+  }
+  __syncthreads();
+  if (e > a) {
+    int c1 = -1;
+    for (int k = static_cast<int>(threadIdx.x); k < p.G; k += SF_THREADS) {
+      const long long b0 = __ldg(p.bounds + k), b1 = __ldg(p.bounds + k + 1);
+      if (b0 <= a && a < b1) {
+        c_lo = k;
+        if (a > b0 && e < b1) c_direct = 1;  // inside one range, neither its first nor its last run: S already
+      }
+      if (b0 <= e - 1 && e - 1 < b1) c1 = k;
+    }
+    __syncthreads();
+    if (c1 >= 0) c_n = c1 - c_lo + 1;
+  }
+  __syncthreads();
+  const int nc = c_n;
+  for (int w = static_cast<int>(threadIdx.x); w < (nc + 31) / 32; w += SF_THREADS) c_slot[w] = 0;
+  __syncthreads();
+  for (int k = static_cast<int>(threadIdx.x); k < nc; k += SF_THREADS)
+    if (a > __ldg(p.bounds + c_lo + k)) atomicOr(&c_slot[k >> 5], 1u << (k & 31));
+  __syncthreads();
+  for (int r = 0; r < SF_ELEMS / SF_THREADS; ++r) {
+    const int idx = sl * SF_ELEMS + r * SF_THREADS + static_cast<int>(threadIdx.x);
+    if (idx >= elems) break;
+    const int n = idx >> 7, dl = idx & 127;
+    const int d = dblk * 128 + dl;
+    if (d >= p.D) continue;
+    float* Sp = p.S + (static_cast<size_t>(u) * p.N + n) * p.D + d;
+    float v = 0.f;
+    if (c_direct) {
+      v = *Sp;
+    } else {
+      // the contributors' values, loaded 8 at a time, then added in CTA order
+      const float* base = p.spart + static_cast<size_t>(n) * 128 + dl;
+      const size_t slot_stride = static_cast<size_t>(p.N) * 128;
+      for (int k0 = 0; k0 < nc; k0 += 8) {
+        float w[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int k = k0 + j;
+          const int slot = k < nc ? static_cast<int>((c_slot[k >> 5] >> (k & 31)) & 1u) : 0;
+          w[j] = k < nc ? __ldg(base + (static_cast<size_t>(c_lo + k) * 2 + slot) * slot_stride) : 0.f;
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          if (k0 + j < nc) v += w[j];
+      }
+      *Sp = v;  // 0 for a user without candidates
+    }
+    const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+    const __nv_bfloat16 lo = __float2bfloat16_rn(v - __bfloat162float(hi));
+    uint16_t* s2 = p.S2 + static_cast<size_t>(u) * 2 * p.NPD + static_cast<size_t>(n) * p.D + d;
+    s2[0] = __bfloat16_as_ushort(hi);
+    s2[p.NPD] = __bfloat16_as_ushort(lo);
+  }
+}
+
 }  // namespace
 
 // ------------------------------------------------------------------- host
@@ -605,6 +1003,45 @@ cudaError_t launch_bwd_segsum(const SegSumParams& p, cudaStream_t s, int* launch
 
 cudaError_t launch_bwd_db(const float* S, float* db, int n_users, int N, int D, cudaStream_t s) {
   bwd_db_kernel<<<N, BWD_DB_THREADS, 0, s>>>(S, db, n_users, N, D);
+  return cudaGetLastError();
+}
+
+// The candidate pass (see CandParams): false where it does not apply.
+bool bwd_cand_configure(CandParams* p, size_t max_smem) {
+  if (p->K_c < 1 || p->K_c > BWD_CAND_MAX_KC || p->N < 1 || p->N > BWD_CAND_MAX_N || p->D < 1) return false;
+  if (CAND_SMEM > max_smem) return false;
+  p->n_dblk = (p->D + 127) / 128;
+  p->kcn = (p->N + 63) / 64;
+  p->n_mblk = (p->K_c + 127) / 128;
+  p->n_mma = (p->N + 15) / 16 * 16;
+  return true;
+}
+
+int bwd_cand_grid(const CandParams& p, int num_sms) {
+  const long long nq = static_cast<long long>(p.n_dblk) * p.n_cand;
+  return static_cast<int>(nq < num_sms ? nq : num_sms);
+}
+
+cudaError_t launch_bwd_cand(const CUtensorMap& tmDY, const CUtensorMap& tmC, const CandParams& p, int grid,
+                            cudaStream_t s) {
+  cudaError_t e = cudaFuncSetAttribute(bwd_cand_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(CAND_SMEM));
+  if (e != cudaSuccess) return e;
+  bwd_cand_kernel<<<grid, BWD_THREADS, CAND_SMEM, s>>>(tmDY, tmC, p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_sfinish(const SFinishParams& p, cudaStream_t s) {
+  const int slices = (p.N * 128 + SF_ELEMS - 1) / SF_ELEMS;
+  bwd_sfinish_kernel<<<p.n_users * p.n_dblk * slices, SF_THREADS, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+// The in-order reduce of split-K partials part[(mblk * R + r) * 128 + row][n] into dW.
+cudaError_t launch_bwd_wreduce(const float* part, float* dW, int M, int N, int R, cudaStream_t s) {
+  const int total = M * N;
+  bwd_wgrad_reduce_kernel<<<(total + WG_RED_OUT - 1) / WG_RED_OUT, dim3(WG_RED_OUT, WG_RED_SPLIT), 0, s>>>(part, dW,
+                                                                                                       M, N, R);
   return cudaGetLastError();
 }
 

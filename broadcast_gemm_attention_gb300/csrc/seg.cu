@@ -7,7 +7,8 @@
 // candidates are grouped per user first:
 //   counts[u]  = #{i : map[i] = u}
 //   offsets    = exclusive prefix sum of counts (offsets[n_users] = #valid)
-//   perm       = candidates grouped by user, ascending i inside a user (stable)
+//   perm       = candidates grouped by user, ascending i inside a user (stable);
+//                candidates with a map value out of range follow, ascending
 //   work       = for u, for h, for each run of <= cands_per_unit entries of
 //                u's segment: (u, h, first perm position, run length)
 // Everything is integer work, so the result is unique and bit-exact.
@@ -173,6 +174,24 @@ __global__ void __launch_bounds__(SEG_THREADS, 1) seg_build_kernel(SegParams p) 
         }
         __syncthreads();
       }
+    }
+  }
+
+  // candidates whose map value is out of range follow the valid ones in
+  // perm, in index order: they belong to no user's segment, but a kernel that
+  // walks every position of perm (the LCE backward's candidate pass) still
+  // reaches them
+  if (__syncthreads_or(bad)) {
+    int tail = total;
+    for (int base = 0; base < p.n_cand; base += SEG_THREADS) {
+      const int i = base + tid;
+      const int u = i < p.n_cand ? p.map[i] : 0;
+      const bool inv = i < p.n_cand && (u < 0 || u >= nu);
+      int block_inv;
+      const int pre = block_exclusive_scan(inv ? 1 : 0, warp_sums, &block_inv);
+      if (inv) p.perm[tail + pre] = i;
+      tail += block_inv;
+      __syncthreads();  // warp_sums is reused by the next scan
     }
   }
 

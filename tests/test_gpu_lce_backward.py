@@ -65,19 +65,22 @@ def test_lce_backward_full(shape):
     dY = gen.make_lce_grad(91, x.n_cand, x.N, x.D)
     out, st, launched = run_backward(x, dY)
     assert st == B.IKBO_OK
-    assert launched >= 7  # segment sum, db, dC, dWc (+ reduce), dU, dWu (+ reduce)
+    # candidate pass (or segment sum and dW_c), S finish / db, reduces, dC, dU, dW_u
+    assert launched >= 7
     check_all(x, dY, out, what=str(shape))
 
 
 def test_lce_backward_few_users_many_candidates():
-    """One or two users with many candidates: each user's segment sum is split
-    into chunks whose partial sums are added in a second pass."""
+    """One or two users with many candidates: each user's segment sum is
+    spread over many CTAs of the candidate pass, whose partial sums the finish
+    kernel adds in CTA order."""
     for n_users in (1, 2):
         x = gen.make_lce("bwd_chunks", 92, 2048, n_users, 64, 48, 128, 64, map_kind="permuted")
         dY = gen.make_lce_grad(92, x.n_cand, x.N, x.D)
         out, st, launched = run_backward(x, dY)
         assert st == B.IKBO_OK
-        assert launched == 9  # the segment sum took two passes
+        # candidate pass (dW_c, S), S finish, dW_c reduce, db, dC, dU, dW_u (+ reduce)
+        assert launched == 8
         check_all(x, dY, out, what=f"{n_users} users")
 
 
