@@ -83,7 +83,9 @@ ikbo_status_t ikbo_plan(ikbo_plan_t p, const int32_t* d_map, int n_cand, int n_u
 
 /* Borrow the segment arrays of the last ikbo_plan (device pointers, valid
  * until the next ikbo_plan or ikbo_plan_destroy): counts [n_users], offsets
- * [n_users+1], perm [n_cand].  Any output pointer may be NULL. */
+ * [n_users+1], perm [n_cand] (positions offsets[n_users] .. n_cand-1 hold
+ * the candidates whose map value is out of range, ascending).  Any output
+ * pointer may be NULL. */
 ikbo_status_t ikbo_plan_segments(ikbo_plan_t p, const int32_t** d_counts, const int32_t** d_offsets,
                                  const int32_t** d_perm);
 
@@ -293,9 +295,9 @@ ikbo_status_t ikbo_plan_set_timeout_ns(ikbo_plan_t p, uint64_t timeout_ns);
 /* Launch schedule of ikbo_lce_forward (plan-time kernel selection over the
  * shape range, the "compile for a range of shapes" idea of the pages done as
  * a runtime choice):
- *   0  chosen from the shape (default): 3 where it applies and the request
- *      has at least two users; 2 for a single user; otherwise 2 when the
- *      request has fewer than 8 candidate tiles of 128 D-rows per SM, else 1
+ *   0  chosen from the shape (default): 3 where it applies; otherwise 2 for
+ *      a single user or when the request has fewer than 8 candidate tiles
+ *      of 128 D-rows per SM, else 1
  *   1  two launches: user tiles (fp32 partials in the plan's workspace, with
  *      release flags), then candidate tiles
  *   2  one launch: user tiles first in every CTA's list.  Its candidate
