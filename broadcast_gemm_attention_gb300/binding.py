@@ -30,6 +30,7 @@ IKBO_ERR_TIMEOUT = 5
 IKBO_ERR_NOT_PLANNED = 6
 IKBO_ERR_INTERNAL = 7
 DEBUG_WITHHOLD_USER_PARTIAL = 1
+DEBUG_NO_COOPERATIVE = 2
 
 # every function the header declares: name -> (restype, argtypes)
 _vp, _i, _u64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_uint64

@@ -35,10 +35,8 @@ bool bwd_wgrad_configure(WgradParams* p, int num_sms, size_t max_smem);
 size_t bwd_wgrad_part_elems(const WgradParams& p);
 bool bwd_cand_configure(CandParams* p, size_t max_smem);
 int bwd_cand_grid(const CandParams& p, int num_sms);
-cudaError_t launch_bwd_cand(const CUtensorMap& tmDY, const CUtensorMap& tmC, const CandParams& p, int grid,
-                            cudaStream_t s);
-cudaError_t launch_bwd_sfinish(const SFinishParams& p, cudaStream_t s);
-cudaError_t launch_bwd_wreduce(const float* part, float* dW, int M, int N, int R, cudaStream_t s);
+cudaError_t launch_bwd_cand(const CUtensorMap& tmDY, const CUtensorMap& tmC, const CUtensorMap& tmW,
+                            const CandParams& p, int num_sms, bool cooperative, cudaStream_t s, int* launches);
 cudaError_t launch_bwd_wgrad(const CUtensorMap& tmA, const CUtensorMap& tmG, const WgradParams& p, float* dW,
                              int num_sms, cudaStream_t s, int* launches);
 size_t attn_bwd_smem_bytes();
@@ -82,8 +80,13 @@ struct ikbo_plan_s {
   size_t bwd_wpart_elems = 0;
   float* d_bwd_spart = nullptr;  // candidate pass: S partials of each CTA's first and last run
   size_t bwd_spart_elems = 0;
-  long long* d_bwd_bounds = nullptr;  // candidate pass: the CTAs' tile ranges
-  size_t bwd_bounds_elems = 0;
+  float* d_bwd_dbcta = nullptr;  // candidate pass: each CTA's share of db
+  size_t bwd_dbcta_elems = 0;
+  uint32_t* d_bwd_ctrl = nullptr;  // candidate pass: grid barrier counts
+  size_t bwd_ctrl_elems = 0;
+  // a second stream (created on first use) on which dW_u runs beside dU
+  cudaStream_t side = nullptr;
+  cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
   // attention backward workspaces
   float* d_abwd_lse = nullptr;
   size_t abwd_lse_elems = 0;
@@ -172,7 +175,11 @@ void free_plan(ikbo_plan_t p) {
   cudaFree(p->d_bwd_seg);
   cudaFree(p->d_bwd_wpart);
   cudaFree(p->d_bwd_spart);
-  cudaFree(p->d_bwd_bounds);
+  cudaFree(p->d_bwd_dbcta);
+  cudaFree(p->d_bwd_ctrl);
+  if (p->ev_fork) cudaEventDestroy(p->ev_fork);
+  if (p->ev_join) cudaEventDestroy(p->ev_join);
+  if (p->side) cudaStreamDestroy(p->side);
   cudaFree(p->d_abwd_lse);
   cudaFree(p->d_abwd_drow);
   cudaFree(p->d_abwd_blk);
@@ -599,14 +606,14 @@ ikbo_status_t ikbo_lce_backward(ikbo_plan_t p, const void* U, const void* C, con
   const int n_cand = p->n_cand, n_users = p->n_users;
 
   // configure every product that is asked for before launching anything.
-  // dW_c and the segment sum S run as one candidate pass, which reads dY and
-  // C once, where the shape allows it (K_c <= 256, N <= 192); else as a
-  // segment-sum kernel and a weight-gradient kernel.  dC is the
-  // activation-gradient kernel in either case.
+  // Where the shape allows it (K_c <= 256, N <= 192) one candidate pass
+  // reads dY and C once for dC, dW_c and the segment sum S (with db); else
+  // a segment-sum kernel, the activation-gradient kernel (dC) and a
+  // weight-gradient kernel (dW_c).  dU and dW_u read S at n_users.
   const bool need_S = dU || dWu || db;
   CandParams cp{};
   cp.n_cand = n_cand, cp.n_users = n_users, cp.K_c = K_c, cp.D = D, cp.N = N;
-  const bool use_cand = (dWc || need_S) && bwd_cand_configure(&cp, p->max_smem);
+  const bool use_cand = (dC || dWc || need_S) && bwd_cand_configure(&cp, p->max_smem);
   const int cgrid = use_cand ? bwd_cand_grid(cp, p->num_sms) : 0;
   ActParams ac{}, au{};
   WgradParams wc{}, wu{};
@@ -616,7 +623,7 @@ ikbo_status_t ikbo_lce_backward(ikbo_plan_t p, const void* U, const void* C, con
   wu.M = K_u, wu.D = D, wu.N = N;
   wu.B = 2 * n_users;  // G = the hi/lo pair of S per user; A = U[b >> 1]
   wu.a_shift = 1;
-  if ((dC && !bwd_act_configure(&ac, p->max_smem, false)) ||
+  if ((!use_cand && dC && !bwd_act_configure(&ac, p->max_smem, false)) ||
       (dU && !bwd_act_configure(&au, p->max_smem, true)) ||
       (!use_cand && dWc && !bwd_wgrad_configure(&wc, p->num_sms, p->max_smem)) ||
       (dWu && !bwd_wgrad_configure(&wu, p->num_sms, p->max_smem)))
@@ -625,21 +632,23 @@ ikbo_status_t ikbo_lce_backward(ikbo_plan_t p, const void* U, const void* C, con
   const int ND = N * D;
   const int NP = (N + 63) / 64 * 64;  // rows per half of the hi/lo pair
   SegSumParams sp{};
+  const size_t n_ctrl = 2;
   if (need_S) {
     sp.nch = bwd_segsum_chunks(n_cand, n_users, ND, p->num_sms);
     sp.slices = (ND + BWD_SEG_SLICE - 1) / BWD_SEG_SLICE;
     sp.NPD = NP * D;
     const size_t nS = static_cast<size_t>(n_users) * ND;
-    if (grow(&p->d_bwd_S, &p->bwd_S_elems, nS, stream) != cudaSuccess ||
-        grow(&p->d_bwd_Sb, &p->bwd_Sb_elems, static_cast<size_t>(n_users) * 2 * NP * D, stream) != cudaSuccess)
+    if (grow(&p->d_bwd_Sb, &p->bwd_Sb_elems, static_cast<size_t>(n_users) * 2 * NP * D, stream) != cudaSuccess)
       return IKBO_ERR_CUDA;
-    if (!use_cand && sp.nch > 1 && grow(&p->d_bwd_seg, &p->bwd_seg_elems, nS * sp.nch, stream) != cudaSuccess)
+    if (!use_cand && (grow(&p->d_bwd_S, &p->bwd_S_elems, nS, stream) != cudaSuccess ||
+                      (sp.nch > 1 && grow(&p->d_bwd_seg, &p->bwd_seg_elems, nS * sp.nch, stream) != cudaSuccess)))
       return IKBO_ERR_CUDA;
     if (use_cand &&
-        (grow(&p->d_bwd_spart, &p->bwd_spart_elems, static_cast<size_t>(cgrid) * 2 * N * 128, stream) != cudaSuccess ||
-         grow(&p->d_bwd_bounds, &p->bwd_bounds_elems, static_cast<size_t>(cgrid) + 1, stream) != cudaSuccess))
+        (grow(&p->d_bwd_spart, &p->bwd_spart_elems, static_cast<size_t>(cgrid) * 2 * N * 64, stream) != cudaSuccess ||
+         grow(&p->d_bwd_dbcta, &p->bwd_dbcta_elems, static_cast<size_t>(cgrid) * N, stream) != cudaSuccess))
       return IKBO_ERR_CUDA;
   }
+  if (use_cand && grow(&p->d_bwd_ctrl, &p->bwd_ctrl_elems, n_ctrl, stream) != cudaSuccess) return IKBO_ERR_CUDA;
   size_t wpart = 0;
   if (dWc) wpart = use_cand ? static_cast<size_t>(cp.n_mblk) * cgrid * 128 * N : bwd_wgrad_part_elems(wc);
   if (dWu && bwd_wgrad_part_elems(wu) > wpart) wpart = bwd_wgrad_part_elems(wu);
@@ -692,37 +701,28 @@ ikbo_status_t ikbo_lce_backward(ikbo_plan_t p, const void* U, const void* C, con
   if (need_S && NP != N)
     e = cudaMemsetAsync(p->d_bwd_Sb, 0, sizeof(uint16_t) * static_cast<size_t>(n_users) * 2 * NP * D, stream);
   if (e == cudaSuccess && use_cand) {
+    // the grid barrier's counts start at zero (the pass leaves them so; this
+    // also covers a call that ended on a timeout)
+    e = cudaMemsetAsync(p->d_bwd_ctrl, 0, sizeof(uint32_t) * n_ctrl, stream);
     cp.perm = p->d_perm;
     cp.map = p->d_map;
+    cp.offsets = p->d_offsets;
+    cp.dC = static_cast<uint16_t*>(dC);
     cp.wpart = dWc ? p->d_bwd_wpart : nullptr;
-    cp.S = need_S ? p->d_bwd_S : nullptr;
+    cp.dWc = dWc;
+    cp.S2 = need_S ? p->d_bwd_Sb : nullptr;
     cp.spart = p->d_bwd_spart;
-    cp.bounds = p->d_bwd_bounds;
+    cp.dbcta = p->d_bwd_dbcta;
+    cp.db = db;
+    cp.ctrl = p->d_bwd_ctrl;
     cp.status = p->d_status;
+    cp.NPD = NP * D;
+    cp.G = cgrid;
     cp.timeout_ns = p->timeout_ns;
-    e = launch_bwd_cand(tmDY, tmC, cp, cgrid, stream);
-    if (e == cudaSuccess) ++launches;
-    if (e == cudaSuccess && need_S) {
-      SFinishParams fp{};
-      fp.offsets = p->d_offsets;
-      fp.S = p->d_bwd_S;
-      fp.spart = p->d_bwd_spart;
-      fp.bounds = p->d_bwd_bounds;
-      fp.S2 = p->d_bwd_Sb;
-      fp.n_cand = n_cand;
-      fp.n_users = n_users;
-      fp.N = N;
-      fp.D = D;
-      fp.NPD = NP * D;
-      fp.n_dblk = cp.n_dblk;
-      fp.G = cgrid;
-      e = launch_bwd_sfinish(fp, stream);
-      if (e == cudaSuccess) ++launches;
-    }
-    if (e == cudaSuccess && dWc) {
-      e = launch_bwd_wreduce(p->d_bwd_wpart, dWc, K_c, N, cgrid, stream);
-      if (e == cudaSuccess) ++launches;
-    }
+    int n = 0;
+    const bool coop = (p->debug & DEBUG_NO_COOPERATIVE) == 0;
+    if (e == cudaSuccess) e = launch_bwd_cand(tmDY, tmC, tmWc, cp, p->num_sms, coop, stream, &n);
+    if (e == cudaSuccess) launches += n;
   } else if (e == cudaSuccess && need_S) {
     sp.dY = static_cast<const uint16_t*>(dY);
     sp.offsets = p->d_offsets;
@@ -734,12 +734,12 @@ ikbo_status_t ikbo_lce_backward(ikbo_plan_t p, const void* U, const void* C, con
     sp.n_users = n_users;
     sp.ND = ND;
     e = launch_bwd_segsum(sp, stream, &launches);
+    if (e == cudaSuccess && db) {
+      e = launch_bwd_db(p->d_bwd_S, db, n_users, N, D, stream);
+      if (e == cudaSuccess) ++launches;
+    }
   }
-  if (e == cudaSuccess && db) {
-    e = launch_bwd_db(p->d_bwd_S, db, n_users, N, D, stream);
-    if (e == cudaSuccess) ++launches;
-  }
-  if (e == cudaSuccess && dC) {
+  if (e == cudaSuccess && dC && !use_cand) {
     ac.out = static_cast<uint16_t*>(dC);
     ac.status = p->d_status;
     ac.timeout_ns = p->timeout_ns;
@@ -752,6 +752,25 @@ ikbo_status_t ikbo_lce_backward(ikbo_plan_t p, const void* U, const void* C, con
     wc.timeout_ns = p->timeout_ns;
     e = launch_bwd_wgrad(tmC, tmDY, wc, dWc, p->num_sms, stream, &launches);
   }
+  // dU and dW_u both read S and nothing else of each other: with both asked
+  // for, dW_u (and its reduce) runs on the plan's second stream beside dU
+  // (fork and join through events, so the call stays ordered on `stream`)
+  cudaStream_t wu_stream = stream;
+  if (e == cudaSuccess && dU && dWu) {
+    if ((!p->side && cudaStreamCreateWithFlags(&p->side, cudaStreamNonBlocking) != cudaSuccess) ||
+        (!p->ev_fork && cudaEventCreateWithFlags(&p->ev_fork, cudaEventDisableTiming) != cudaSuccess) ||
+        (!p->ev_join && cudaEventCreateWithFlags(&p->ev_join, cudaEventDisableTiming) != cudaSuccess))
+      e = cudaErrorMemoryAllocation;
+    if (e == cudaSuccess) e = cudaEventRecord(p->ev_fork, stream);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(p->side, p->ev_fork, 0);
+    if (e == cudaSuccess) wu_stream = p->side;
+  }
+  if (e == cudaSuccess && dWu) {
+    wu.part = p->d_bwd_wpart;
+    wu.status = p->d_status;
+    wu.timeout_ns = p->timeout_ns;
+    e = launch_bwd_wgrad(tmU, tmSG, wu, dWu, p->num_sms, wu_stream, &launches);
+  }
   if (e == cudaSuccess && dU) {
     au.out = static_cast<uint16_t*>(dU);
     au.status = p->d_status;
@@ -759,11 +778,10 @@ ikbo_status_t ikbo_lce_backward(ikbo_plan_t p, const void* U, const void* C, con
     e = launch_bwd_act(tmSX, tmWu, au, p->num_sms, stream);
     if (e == cudaSuccess) ++launches;
   }
-  if (e == cudaSuccess && dWu) {
-    wu.part = p->d_bwd_wpart;
-    wu.status = p->d_status;
-    wu.timeout_ns = p->timeout_ns;
-    e = launch_bwd_wgrad(tmU, tmSG, wu, dWu, p->num_sms, stream, &launches);
+  if (wu_stream != stream) {  // join, also after a failed launch on either stream
+    const cudaError_t e2 = cudaEventRecord(p->ev_join, wu_stream);
+    const cudaError_t e3 = e2 == cudaSuccess ? cudaStreamWaitEvent(stream, p->ev_join, 0) : e2;
+    if (e == cudaSuccess) e = e3;
   }
   p->launches += static_cast<uint64_t>(launches);
   return e == cudaSuccess ? IKBO_OK : IKBO_ERR_CUDA;

@@ -22,6 +22,7 @@ enum : uint32_t {
 // Debug switches (ikbo_plan_set_debug).
 enum : uint32_t {
   DEBUG_WITHHOLD_USER_PARTIAL = 1u << 0,  // LCE: never publish user partials
+  DEBUG_NO_COOPERATIVE = 1u << 1,         // LCE backward: the candidate pass and its finish as two launches
 };
 
 // ------------------------------------------------------------ segments
@@ -193,50 +194,51 @@ struct WgradParams {
   uint64_t timeout_ns;
 };
 
-// Candidate pass of the LCE backward, one persistent launch that reads each
-// candidate's dY and C once: per tile (candidate b = perm[pos], 128-row
-// block of D), in the plan's user-grouped order,
-//   dW_c  += C[b] dY[b]^T                 (TMEM, <= 2 blocks of 128 K_c rows, per CTA)
-//   S[u]  += dY[b]                        (epilogue warps, from the staged dY tile)
-// dY stays in shared memory for the tile (two tile slots); C streams through
-// a ring of 16 KB slots.  dW_c leaves as per-CTA partials (the wgrad reduce
-// adds them in CTA order); S as direct stores for runs of (user, D block)
-// inside one CTA's range and as two partial slots per CTA (the range's first
-// and last run) added in CTA order by bwd_sfinish_kernel.  Applies when
-// K_c <= 256 and N <= 192.  (dC = W_c dY stays with the activation-gradient
-// kernel, which keeps W_c in shared memory: streaming W_c beside C, one
-// 96 KB copy per tile, starved this kernel's ring.)
-constexpr int BWD_CAND_SLOTS = 8;                    // 16 KB C slots
-constexpr int BWD_CAND_DY_BYTES = 2 * 3 * 64 * 64 * 2;  // a dY tile: 2 d halves x <= 3 n chunks of 64 x 64
+// Candidate pass of the LCE backward: one persistent launch that reads each
+// candidate's dY (and C) once.  Unit = (candidate b = perm[pos], 64-wide
+// block dh of D), numbered dh * n_cand + pos (the plan's user-grouped order
+// within each D block); each CTA takes one contiguous range of units.  Per
+// unit, from the dY block staged in shared memory:
+//   dC[b]  = W_c dY[b]            (W_c resident in shared memory; TMEM)
+//   dW_c  += C[b] dY[b]^T         (TMEM, <= 2 blocks of 128 K_c rows, per CTA)
+//   S[u]  += dY[b]                (epilogue warps, fp32 registers)
+// S of a run (user u, D block dh) that lies inside one CTA's range is
+// written by that CTA; a run shared by several CTAs leaves partial slots
+// (each CTA's first and last run).  S leaves as the bf16 hi/lo pair the
+// user-side products read.  Each CTA also keeps its share of db (per n, its
+// runs' sums over d).  The finish -- dW_c as the sum of the per-CTA partials
+// in CTA order, S of the shared runs as the sum of their slots in CTA order,
+// db as the sum of the CTAs' shares in CTA order -- runs after a grid
+// barrier in the same launch (cooperative: all CTAs resident), or, where a
+// cooperative launch is refused, as a second kernel.  Applies when
+// K_c <= 256 and N <= 192.
+constexpr int BWD_CAND_DY_SLOTS = 2;    // dY blocks: <= 3 n chunks of 64 n x 64 d (24 KB)
+constexpr int BWD_CAND_C_SLOTS = 5;     // C slots: 128 K_c rows x 64 d (16 KB)
 constexpr int BWD_CAND_MAX_N = 192;
 constexpr int BWD_CAND_MAX_KC = 256;
 
 struct CandParams {
   const int32_t* perm;       // [n_cand] the plan's user-grouped order (out-of-range candidates last)
   const int32_t* map;        // [n_cand]
-  float* wpart;              // [n_mblk][G][128][N] fp32 dW_c partials (G = grid), or null (no dW_c)
-  float* S;                  // [n_users][N][D] fp32, or null (no S)
-  float* spart;              // [G][2][N][128] fp32 S partials of each CTA's first and last run
-  long long* bounds;         // [G + 1] each CTA's first tile (and the tile count), for the S finish
-  uint32_t* status;
-  int n_cand, n_users, K_c, D, N;
-  int n_dblk;                // ceil(D / 128)
-  int kcn;                   // ceil(N / 64): dY n chunks (<= 3)
-  int n_mblk;                // ceil(K_c / 128): dW_c blocks (1 or 2)
-  int n_mma;                 // roundup(N, 16): dW_c accumulator columns per block
-  uint64_t timeout_ns;
-};
-
-// S finish: for every (user, D block), S = the sum of its partial slots in
-// CTA order (or, for a run inside one CTA's range, the direct value), in
-// fp32 and as the bf16 hi/lo pair the user-side products read.
-struct SFinishParams {
   const int32_t* offsets;    // [n_users + 1] the plan's segment offsets
-  float* S;                  // [n_users][N][D]
-  const float* spart;        // [G][2][N][128]
-  const long long* bounds;   // [G + 1] the candidate pass's CTA ranges
-  uint16_t* S2;              // [n_users][2][NP][D] hi, lo
-  int n_cand, n_users, N, D, NPD, n_dblk, G;
+  uint16_t* dC;              // [n_cand][K_c][D] bf16, or null (no dC)
+  float* wpart;              // [n_mblk][G][N][128] fp32 dW_c partials (K_c row of the block
+                             // innermost), or null (no dW_c)
+  float* dWc;                // [K_c][N] fp32 (with wpart)
+  uint16_t* S2;              // [n_users][2][NP][D] bf16 hi, lo of S, or null (no S)
+  float* spart;              // [G][2][N][64] fp32 S partials of each CTA's first and last run
+  float* dbcta;              // [G][N] each CTA's share of db
+  float* db;                 // [N] or null
+  uint32_t* ctrl;            // [2] grid barrier: arrivals, departures (zero at launch)
+  uint32_t* status;
+  int n_cand, n_users, K_c, D, N, NPD;  // NPD = NP * D, NP = roundup(N, 64)
+  int n_dh;                  // ceil(D / 64)
+  int kcn;                   // ceil(N / 64): dY n chunks (<= 3)
+  int n_mblk;                // ceil(K_c / 128): K_c blocks (1 or 2)
+  int n_mma;                 // roundup(N, 16): dW_c accumulator columns per block
+  int G;                     // grid of the candidate pass (the number of dW_c partials)
+  int fused_finish;          // 1: the finish runs in the same (cooperative) launch
+  uint64_t timeout_ns;
 };
 
 // ----------------------------------------------------------- attention

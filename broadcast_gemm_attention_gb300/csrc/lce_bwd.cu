@@ -574,63 +574,90 @@ __global__ void __launch_bounds__(WG_RED_OUT* WG_RED_SPLIT)
 }
 
 // ============================================================ candidate pass
-// See CandParams.  Per CTA (one per SM, 12 warps): warp 0 TMA producer,
-// warp 1 MMA issuer, warp 2 TMEM owner, warps 4-11 epilogue (S sums).
-// Tiles q = dblk * n_cand + pos (D-block-major over the plan's grouped
-// order), one contiguous range per CTA, so a CTA's consecutive tiles share a
-// user and its S sums stay in registers.
+// See CandParams.  Per CTA (one per SM, 12 warps): warp 0 TMA producer of
+// W_c and dY, warp 1 MMA issuer, warp 2 TMEM owner, warp 3 TMA producer of
+// C, warps 4-11 epilogue (S sums, dC read-out, the dW_c partial).
+// Units q = dh * n_cand + pos (D-block-major over the plan's grouped order),
+// one contiguous range per CTA, so a CTA's consecutive units share a user
+// and its S sums stay in registers.
 // TMEM columns: dW_c block 0 [0, n_mma), block 1 [n_mma, 2 n_mma) (lanes =
-// K_c rows, columns = n), accumulated over the CTA's tiles.
-// Shared memory: two dY tile slots, each [d half][n rows][64 d] (128-byte
-// rows, 128-byte swizzle), read K-major as dW_c's B; then the ring of 16 KB
-// C slots, per tile one per (128-row block of K_c, 64-d half).
-constexpr uint32_t CB_SLOT = 128 * 64 * 2;  // 16 KB: 128 rows x 64 bf16
-constexpr uint32_t CB_DYHALF = 3 * BOX;     // one d half of a dY tile (<= 192 n rows)
-constexpr uint32_t CAND_TILES = 2 * BWD_CAND_DY_BYTES + BWD_CAND_SLOTS * CB_SLOT;
-constexpr int CAND_BARS = 4 + 2 * BWD_CAND_SLOTS + 1;
-constexpr size_t CAND_SMEM = 1024 + CAND_TILES + 8 * CAND_BARS + 8;
+// K_c rows, columns = n), accumulated over the CTA's units; two dC
+// accumulators of 64 columns at CAND_DC_COL (lanes = K_c rows of one block,
+// columns = the unit's 64 d), used in turn: accumulator c of the CTA (c =
+// unit * n_mblk + block) is read out by epilogue warps 4-7 if c is even,
+// 8-11 if odd.
+// Shared memory: W_c ([n chunk][K_c row][64 n], 128-byte swizzle: K-major A
+// of dC), the dY slots ([n chunk][64 n rows][64 d]: K-major B of dW_c and
+// MN-major B of dC), the ring of C slots (128 K_c rows x 64 d: K-major A of
+// dW_c), the barriers.
+constexpr uint32_t CB_SLOT = 128 * 64 * 2;      // 16 KB
+constexpr uint32_t CAND_DY_SLOT = 3 * BOX;      // 24 KB
+constexpr uint32_t CAND_W_BYTES = 3 * 256 * 128;  // W_c: <= 3 n chunks x 256 rows x 128 B
+constexpr uint32_t CAND_TILES =
+    CAND_W_BYTES + BWD_CAND_DY_SLOTS * CAND_DY_SLOT + BWD_CAND_C_SLOTS * CB_SLOT;
+constexpr int CAND_BARS = 2 * BWD_CAND_DY_SLOTS + 2 * BWD_CAND_C_SLOTS + 1 + 4 + 1;
+constexpr size_t CAND_SMEM = 1024 + CAND_TILES + 8 * CAND_BARS + 16 + 4 * BWD_CAND_MAX_N;
 static_assert(CAND_SMEM <= 227 * 1024, "candidate pass does not fit in shared memory");
+constexpr uint32_t CAND_DC_COL = 2 * BWD_CAND_MAX_N;  // after the two dW_c blocks
+static_assert(CAND_DC_COL + 128 <= 512, "candidate pass accumulators exceed TMEM");
+constexpr int CAND_EPI = BWD_THREADS - 128;  // epilogue threads
 
 struct CandSmem {
+  uint8_t* w;
   uint8_t* dy;
   uint8_t* ring;
-  uint64_t* dy_full;   // [2]
-  uint64_t* dy_empty;  // [2] MMA reads done (commit) and the S sums taken
-  uint64_t* st_full;   // [SLOTS]
-  uint64_t* st_empty;  // [SLOTS]
-  uint64_t* w_full;    // the CTA's dW_c partial is complete in TMEM
+  uint64_t* dy_full;   // [DY_SLOTS]
+  uint64_t* dy_empty;  // [DY_SLOTS] MMA reads done (commit) and the S sums taken
+  uint64_t* st_full;   // [C_SLOTS]
+  uint64_t* st_empty;  // [C_SLOTS]
+  uint64_t* w_full;    // W_c resident
+  uint64_t* dc_full;   // [2]
+  uint64_t* dc_empty;  // [2]
+  uint64_t* wacc_full;  // the CTA's dW_c partial is complete in TMEM
   uint32_t* tmem_slot;
   uint32_t* abort;
+  uint32_t* flag;      // the grid barrier was passed
+  float* dbsm;         // [BWD_CAND_MAX_N] this CTA's share of db
 };
 
 __device__ __forceinline__ CandSmem cand_carve(uint8_t* base) {
   CandSmem s;
-  s.dy = base;
-  s.ring = base + 2 * BWD_CAND_DY_BYTES;
+  s.w = base;
+  s.dy = base + CAND_W_BYTES;
+  s.ring = s.dy + BWD_CAND_DY_SLOTS * CAND_DY_SLOT;
   uint64_t* b = reinterpret_cast<uint64_t*>(base + CAND_TILES);
   s.dy_full = b;
-  s.dy_empty = b + 2;
-  s.st_full = b + 4;
-  s.st_empty = s.st_full + BWD_CAND_SLOTS;
-  s.w_full = s.st_empty + BWD_CAND_SLOTS;
-  s.tmem_slot = reinterpret_cast<uint32_t*>(s.w_full + 1);
+  s.dy_empty = s.dy_full + BWD_CAND_DY_SLOTS;
+  s.st_full = s.dy_empty + BWD_CAND_DY_SLOTS;
+  s.st_empty = s.st_full + BWD_CAND_C_SLOTS;
+  s.w_full = s.st_empty + BWD_CAND_C_SLOTS;
+  s.dc_full = s.w_full + 1;
+  s.dc_empty = s.dc_full + 2;
+  s.wacc_full = s.dc_empty + 2;
+  s.tmem_slot = reinterpret_cast<uint32_t*>(s.wacc_full + 1);
   s.abort = s.tmem_slot + 1;
+  s.flag = s.abort + 1;
+  s.dbsm = reinterpret_cast<float*>(s.flag + 2);  // 8-byte aligned
   return s;
 }
 
-__device__ __forceinline__ void cand_range(const CandParams& p, long long& q0, long long& q1) {
-  const long long nq = static_cast<long long>(p.n_dblk) * p.n_cand;
-  q0 = blockIdx.x * nq / gridDim.x;
-  q1 = (blockIdx.x + 1) * nq / gridDim.x;
+// Unit ranges: CTA g of G takes [g * nq / G, (g + 1) * nq / G); the CTA
+// whose range holds unit x is ((x + 1) G - 1) / nq.
+__device__ __forceinline__ long long cand_q0(long long nq, int g, int G) { return g * nq / G; }
+__device__ __forceinline__ int cand_cta_of(long long x, long long nq, int G) {
+  return static_cast<int>(((x + 1) * G - 1) / nq);
 }
 
-// The candidate (and its user, -1 if out of range) of tile q, looked up by
-// the warp 32 tiles at a time: lane l holds tile wbase + l.
+// The candidate (and its user, -1 if out of range) of unit q, looked up by
+// the warp 32 units at a time: lane l holds unit wbase + l.  With kBounds
+// also the user's segment [offsets[u], offsets[u + 1]).
 struct CandWin {
   long long base = -1;
-  int b = 0, u = -1;
+  int b = 0, u = -1, oa = 0, ob = 0;
 };
-__device__ __forceinline__ void cand_tile(const CandParams& p, long long q, long long q1, CandWin& w, int& b, int& u) {
+template <bool kBounds = false>
+__device__ __forceinline__ void cand_tile(const CandParams& p, long long q, long long q1, CandWin& w, int& b, int& u,
+                                          int* oa = nullptr, int* ob = nullptr) {
   if (w.base < 0 || q >= w.base + 32) {
     w.base = q;
     const long long ql = q + static_cast<long long>(lane_id());
@@ -642,64 +669,287 @@ __device__ __forceinline__ void cand_tile(const CandParams& p, long long q, long
       w.b = (bb >= 0 && bb < p.n_cand) ? bb : 0;
       const int uu = (bb >= 0 && bb < p.n_cand) ? __ldg(p.map + bb) : -1;
       w.u = (uu >= 0 && uu < p.n_users) ? uu : -1;
+      if (kBounds && w.u >= 0) {
+        w.oa = __ldg(p.offsets + w.u);
+        w.ob = __ldg(p.offsets + w.u + 1);
+      }
     }
   }
   const int k = static_cast<int>(q - w.base);
   b = __shfl_sync(0xffffffffu, w.b, k);
   u = __shfl_sync(0xffffffffu, w.u, k);
+  if (kBounds) {
+    *oa = __shfl_sync(0xffffffffu, w.oa, k);
+    *ob = __shfl_sync(0xffffffffu, w.ob, k);
+  }
 }
 
+template <int kSlots>
 struct SlotRing {
   int slot = 0;
   uint32_t phase = 0;
   __device__ __forceinline__ void next() {
-    if (++slot == BWD_CAND_SLOTS) {
+    if (++slot == kSlots) {
       slot = 0;
       phase ^= 1u;
     }
   }
 };
 
-// S sums of a run (user u, D block dblk) of this CTA: the run inside the
-// CTA's range goes straight to S; the range's first run to partial slot 0,
-// its last (when another) to slot 1.  Thread: d pair 2pd, 2pd+1 of the block,
-// rows n = 64 j + 16 ng + i.
-__device__ __forceinline__ void cand_flush(const CandParams& p, const float (&acc)[3][16][2], int u, int dblk,
-                                           int slot, int pd, int ng) {
-  const int d = 2 * pd;
-  const bool dok = dblk * 128 + d < p.D;  // D is a multiple of 8: both of the pair or neither
+// Epilogue thread layout for S: d pair pd (d = 2 pd, 2 pd + 1 of the unit's
+// 64) = lane, rows n = 64 j + 8 ng + i (j < 3, i < 8) with ng = epilogue
+// warp; acc[j][i] holds the pair.
+using CandAcc = float[3][8][2];
+
+// The final S of run (u, dh) from this thread's sums: the bf16 hi/lo pair
+// the user-side products read.
+__device__ __forceinline__ void cand_final(const CandParams& p, const CandAcc& acc, int u, int dh, int pd, int ng) {
+  const int d = dh * 64 + 2 * pd;
+  if (d >= p.D) return;  // D is a multiple of 8: both of the pair or neither
+  uint16_t* s2 = p.S2 + static_cast<size_t>(u) * 2 * p.NPD + d;
 #pragma unroll
   for (int j = 0; j < 3; ++j)
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const int n = 64 * j + 16 * ng + i;
-      if (n >= p.N || !dok) continue;
-      float2* dst = slot < 0 ? reinterpret_cast<float2*>(p.S + (static_cast<size_t>(u) * p.N + n) * p.D + dblk * 128 + d)
-                             : reinterpret_cast<float2*>(p.spart +
-                                                         ((static_cast<size_t>(blockIdx.x) * 2 + slot) * p.N + n) * 128 + d);
-      *dst = make_float2(acc[j][i][0], acc[j][i][1]);
+    for (int i = 0; i < 8; ++i) {
+      const int n = 64 * j + 8 * ng + i;
+      if (n < p.N) {
+        const uint32_t hi = pack_bf16x2(acc[j][i][0], acc[j][i][1]);
+        const uint32_t lo = pack_bf16x2(acc[j][i][0] - __uint_as_float(hi << 16),
+                                        acc[j][i][1] - __uint_as_float(hi & 0xffff0000u));
+        *reinterpret_cast<uint32_t*>(s2 + static_cast<size_t>(n) * p.D) = hi;
+        *reinterpret_cast<uint32_t*>(s2 + p.NPD + static_cast<size_t>(n) * p.D) = lo;
+      }
     }
+}
+
+// This CTA's share of db: per row n, the sum over the run's 64 d (a fixed
+// butterfly over the warp's lanes), added to dbsm[n] run after run.  Each
+// row belongs to one epilogue warp, whose lane 0 updates it.
+__device__ __forceinline__ void cand_db_add(const CandParams& p, const CandAcc& acc, int ng, float* dbsm) {
+  float r[3][8];
+#pragma unroll
+  for (int j = 0; j < 3; ++j)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      float x = acc[j][i][0] + acc[j][i][1];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+      r[j][i] = x;
+    }
+  if (lane_id() != 0) return;
+#pragma unroll
+  for (int j = 0; j < 3; ++j)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int n = 64 * j + 8 * ng + i;
+      if (n < p.N) dbsm[n] += r[j][i];
+    }
+}
+
+// A run (u, dh) ends in this CTA's range [q0, q1).  Inside the range: final
+// here.  Else its sums go to partial slot 1 if the run began inside the range
+// (it runs past the end), else slot 0 (it holds the range's first unit); the
+// finish adds the slots of the run's CTAs in CTA order.
+__device__ __forceinline__ void cand_flush(const CandParams& p, const CandAcc& acc, int u, int dh, int oa, int ob,
+                                           long long q0, long long nq, int pd, int ng, float* dbsm) {
+  const int G = static_cast<int>(gridDim.x);
+  const long long a = static_cast<long long>(dh) * p.n_cand + oa;
+  const long long e = static_cast<long long>(dh) * p.n_cand + ob;
+  if (cand_cta_of(a, nq, G) == cand_cta_of(e - 1, nq, G)) {
+    cand_final(p, acc, u, dh, pd, ng);
+  } else {
+    const int slot = a > q0 ? 1 : 0;
+    float* dst = p.spart + (static_cast<size_t>(blockIdx.x) * 2 + slot) * p.N * 64 + 2 * pd;
+#pragma unroll
+    for (int j = 0; j < 3; ++j)
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int n = 64 * j + 8 * ng + i;
+        if (n < p.N) *reinterpret_cast<float2*>(dst + n * 64) = make_float2(acc[j][i][0], acc[j][i][1]);
+      }
+  }
+  cand_db_add(p, acc, ng, dbsm);
+}
+
+// The finish, spread over G2 blocks (block g) of CF_THREADS threads whose
+// warps work on three parts at once, `red` = CF_RED floats of shared memory:
+//   warps 0..CF_CHUNKS-1: dW_c = the partials of the candidate pass's G
+//     CTAs, added in a fixed order (warp w sums the CTAs of chunk w in CTA
+//     order, 4 consecutive K_c rows of one n per lane, every load of the
+//     chunk in flight at once; lane by lane the chunk sums are then added in
+//     chunk order);
+//   the other warps: S of the runs shared by several CTAs (their slots added
+//     in CTA order), then db[n] for n = g, g + G2, ... (the CTAs' shares
+//     added in CTA order).
+constexpr int CF_CHUNKS = 8;
+constexpr int CF_MAX_PER_CHUNK = 24;  // CTAs per chunk: G <= CF_CHUNKS * 24 = 192
+constexpr int CF_THREADS = BWD_THREADS;
+constexpr int CF_SIDE = CF_THREADS - 32 * CF_CHUNKS;  // threads on the runs and db
+constexpr int CF_SLICES = 4;          // slices of a shared run's S
+constexpr int CF_UNROLL = 6;
+constexpr int CF_RED = CF_CHUNKS * 128 + CF_CHUNKS * CF_MAX_PER_CHUNK;  // chunk sums, then the CTAs' db shares of one n
+static_assert(CF_SIDE >= 64 && CF_SIDE % 32 == 0, "finish: too few threads for the runs");
+__device__ __forceinline__ void cand_finish(const CandParams& p, int g, int G2, float* red) {
+  const int t = static_cast<int>(threadIdx.x), w = t >> 5, lane = t & 31;
+  if (w < CF_CHUNKS) {
+    if (!p.wpart) return;
+    const int total4 = p.n_mblk * p.N * 32;  // (block, n, group of 4 rows)
+    const size_t cstride = static_cast<size_t>(p.N) * 128;
+    const int c0 = w * p.G / CF_CHUNKS, c1 = (w + 1) * p.G / CF_CHUNKS;
+    for (int base = g * 32; base < total4; base += G2 * 32) {
+      const int e4 = base + lane;
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (e4 < total4) {
+        const int mb = e4 / (p.N * 32), rem = e4 - mb * p.N * 32;
+        const float* src = p.wpart + static_cast<size_t>(mb) * p.G * cstride + static_cast<size_t>(rem) * 4;
+        float4 x[CF_MAX_PER_CHUNK];
+#pragma unroll
+        for (int j = 0; j < CF_MAX_PER_CHUNK; ++j)
+          if (c0 + j < c1) x[j] = __ldcg(reinterpret_cast<const float4*>(src + (c0 + j) * cstride));
+#pragma unroll
+        for (int j = 0; j < CF_MAX_PER_CHUNK; ++j)
+          if (c0 + j < c1) {
+            v.x += x[j].x;
+            v.y += x[j].y;
+            v.z += x[j].z;
+            v.w += x[j].w;
+          }
+      }
+      reinterpret_cast<float4*>(red)[w * 32 + lane] = v;
+      named_barrier_sync(1, 32 * CF_CHUNKS);
+      if (w == 0 && e4 < total4) {
+        float4 r = reinterpret_cast<const float4*>(red)[lane];
+#pragma unroll
+        for (int c = 1; c < CF_CHUNKS; ++c) {
+          const float4 y = reinterpret_cast<const float4*>(red)[c * 32 + lane];
+          r.x += y.x;
+          r.y += y.y;
+          r.z += y.z;
+          r.w += y.w;
+        }
+        const int mb = e4 / (p.N * 32), rem = e4 - mb * p.N * 32;
+        const int n = rem >> 5, k = mb * 128 + (rem & 31) * 4;
+        float* dst = p.dWc + static_cast<size_t>(k) * p.N + n;
+        if (k < p.K_c) dst[0] = r.x;
+        if (k + 1 < p.K_c) dst[p.N] = r.y;
+        if (k + 2 < p.K_c) dst[2 * p.N] = r.z;
+        if (k + 3 < p.K_c) dst[3 * p.N] = r.w;
+      }
+      named_barrier_sync(1, 32 * CF_CHUNKS);
+    }
+    return;
+  }
+  if (!p.S2) return;
+  // runs shared by several CTAs: task (run r = (u, dh), slice) goes to block
+  // (r * CF_SLICES + slice) mod G2, two d per thread, CF_UNROLL pairs per
+  // thread at a time
+  const int ts = t - 32 * CF_CHUNKS;
+  const long long nq = static_cast<long long>(p.n_dh) * p.n_cand;
+  const size_t slot_elems = static_cast<size_t>(p.N) * 64;
+  const int pairs = p.N * 32, per_slice = (pairs + CF_SLICES - 1) / CF_SLICES;
+  for (int task = g; task < p.n_users * p.n_dh * CF_SLICES; task += G2) {
+    const int r = task / CF_SLICES, sl = task - r * CF_SLICES;
+    const int u = r / p.n_dh, dh = r - u * p.n_dh;
+    const long long a = static_cast<long long>(dh) * p.n_cand + __ldg(p.offsets + u);
+    const long long e = static_cast<long long>(dh) * p.n_cand + __ldg(p.offsets + u + 1);
+    if (e == a) continue;  // no candidates: zero from the start
+    const int c_lo = cand_cta_of(a, nq, p.G), c_hi = cand_cta_of(e - 1, nq, p.G);
+    if (c_lo == c_hi) continue;  // final already
+    const int slot_lo = a > cand_q0(nq, c_lo, p.G) ? 1 : 0;
+    const int i0 = sl * per_slice, i1 = min(pairs, i0 + per_slice);
+    for (int ib = i0 + ts; ib < i1; ib += CF_UNROLL * CF_SIDE) {
+      float2 v[CF_UNROLL];
+#pragma unroll
+      for (int k = 0; k < CF_UNROLL; ++k) v[k] = make_float2(0.f, 0.f);
+      for (int c0 = c_lo; c0 <= c_hi; c0 += 8) {
+        float2 x[CF_UNROLL][8];
+#pragma unroll
+        for (int k = 0; k < CF_UNROLL; ++k) {
+          const int idx = ib + k * CF_SIDE;
+          const float* src = p.spart + static_cast<size_t>(idx >> 5) * 64 + 2 * (idx & 31);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int c = c0 + j;
+            const int slot = c == c_lo ? slot_lo : 0;
+            x[k][j] = (c <= c_hi && idx < i1)
+                          ? __ldcg(reinterpret_cast<const float2*>(src + (static_cast<size_t>(c) * 2 + slot) * slot_elems))
+                          : make_float2(0.f, 0.f);
+          }
+        }
+#pragma unroll
+        for (int k = 0; k < CF_UNROLL; ++k)
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            if (c0 + j <= c_hi) {
+              v[k].x += x[k][j].x;
+              v[k].y += x[k][j].y;
+            }
+      }
+#pragma unroll
+      for (int k = 0; k < CF_UNROLL; ++k) {
+        const int idx = ib + k * CF_SIDE;
+        const int n = idx >> 5, d = dh * 64 + 2 * (idx & 31);
+        if (idx >= i1 || d >= p.D) continue;
+        uint16_t* s2 = p.S2 + static_cast<size_t>(u) * 2 * p.NPD + static_cast<size_t>(n) * p.D + d;
+        const uint32_t hi = pack_bf16x2(v[k].x, v[k].y);
+        *reinterpret_cast<uint32_t*>(s2) = hi;
+        *reinterpret_cast<uint32_t*>(s2 + p.NPD) =
+            pack_bf16x2(v[k].x - __uint_as_float(hi << 16), v[k].y - __uint_as_float(hi & 0xffff0000u));
+      }
+    }
+  }
+  // db[n] = the CTAs' shares added in CTA order: the side threads load them
+  // (CTA c to thread c mod CF_SIDE), the first adds them from shared memory
+  if (!p.db) return;
+  float* shares = red + CF_CHUNKS * 128;
+  for (int n = g; n < p.N; n += G2) {
+    for (int c = ts; c < p.G; c += CF_SIDE) shares[c] = __ldcg(p.dbcta + static_cast<size_t>(c) * p.N + n);
+    named_barrier_sync(2, CF_SIDE);
+    if (ts == 0) {
+      float v = 0.f;
+      for (int c = 0; c < p.G; ++c) v += shares[c];
+      p.db[n] = v;
+    }
+    named_barrier_sync(2, CF_SIDE);
+  }
+}
+
+// Users without candidates: S = 0 (both halves of the pair); CTA g takes
+// users g, g + G, ...
+__device__ __forceinline__ void cand_empty_users(const CandParams& p) {
+  for (int u = blockIdx.x; u < p.n_users; u += gridDim.x) {
+    if (__ldg(p.offsets + u + 1) != __ldg(p.offsets + u)) continue;
+    uint4* dst = reinterpret_cast<uint4*>(p.S2 + static_cast<size_t>(u) * 2 * p.NPD);
+    const int n16 = 2 * p.NPD / 8;
+    for (int i = threadIdx.x; i < n16; i += blockDim.x) dst[i] = make_uint4(0, 0, 0, 0);
+  }
 }
 
 __global__ void __launch_bounds__(BWD_THREADS, 1)
     bwd_cand_kernel(const __grid_constant__ CUtensorMap tmDY, const __grid_constant__ CUtensorMap tmC,
-                    const CandParams p) {
+                    const __grid_constant__ CUtensorMap tmW, const CandParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const CandSmem s = cand_carve(base);
   const int warp = threadIdx.x >> 5;
-  const bool do_s = p.S != nullptr;
+  const bool do_s = p.S2 != nullptr;
   const bool do_w = p.wpart != nullptr;
+  const bool do_c = p.dC != nullptr;
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < BWD_CAND_DY_SLOTS; ++i) {
       mbar_init(&s.dy_full[i], 1);
-      mbar_init(&s.dy_empty[i], 1 + (do_s ? BWD_THREADS - 128 : 0));
+      mbar_init(&s.dy_empty[i], 1 + (do_s ? CAND_EPI : 0));
     }
-    for (int i = 0; i < BWD_CAND_SLOTS; ++i) {
+    for (int i = 0; i < BWD_CAND_C_SLOTS; ++i) {
       mbar_init(&s.st_full[i], 1);
       mbar_init(&s.st_empty[i], 1);
     }
     mbar_init(s.w_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s.dc_full[i], 1);
+      mbar_init(&s.dc_empty[i], 128);
+    }
+    mbar_init(s.wacc_full, 1);
     *s.abort = 0;
     fence_barrier_init();
     fence_proxy_async_smem();
@@ -707,6 +957,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
   if (warp == 0 && lane_id() == 0) {
     tma_prefetch_desc(&tmDY);
     if (do_w) tma_prefetch_desc(&tmC);
+    if (do_c) tma_prefetch_desc(&tmW);
   }
   if (warp == 2) {
     tmem_alloc(s.tmem_slot, 512);
@@ -716,164 +967,250 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *s.tmem_slot;
-  long long q0, q1;
-  cand_range(p, q0, q1);
-  if (threadIdx.x == 0 && do_s) {  // the range, for the S finish
-    p.bounds[blockIdx.x] = q0;
-    if (blockIdx.x + 1 == gridDim.x) p.bounds[gridDim.x] = q1;
-  }
-  const int nc = do_w ? 2 * p.n_mblk : 0;  // C slots per tile
-  const uint32_t dy_bytes = static_cast<uint32_t>(2 * p.kcn) * BOX;
+  const long long nq = static_cast<long long>(p.n_dh) * p.n_cand;
+  const long long q0 = cand_q0(nq, blockIdx.x, gridDim.x), q1 = cand_q0(nq, blockIdx.x + 1, gridDim.x);
+  if (do_s) cand_empty_users(p);
+  const int m_rows = p.n_mblk * 128;
+  const uint32_t dy_bytes = static_cast<uint32_t>(p.kcn) * BOX;
 
   if (warp == 0) {
-    // ---- TMA producer: the dY tile into its slot, then the tile's C slots
+    // ---- TMA producer of W_c (once) and the dY blocks
+    if (do_c && elect_one()) {
+      mbar_arrive_expect_tx(s.w_full, static_cast<uint32_t>(p.kcn * m_rows) * 128u);
+      for (int kc = 0; kc < p.kcn; ++kc)
+        for (int r = 0; r < m_rows; r += 128)
+          tma_load_2d(s.w + (static_cast<size_t>(kc) * m_rows + r) * 128, &tmW, s.w_full, kc * 64, r);
+    }
+    __syncwarp();
     CandWin win;
-    SlotRing ring;
-    int t = 0;
-    for (long long q = q0; q < q1; ++q, ++t) {
+    SlotRing<BWD_CAND_DY_SLOTS> dyr;
+    for (long long q = q0; q < q1; ++q, dyr.next()) {
       int b, u;
       cand_tile(p, q, q1, win, b, u);
-      const int dblk = static_cast<int>(q / p.n_cand);
-      const int y = t & 1;
-      if (!warp_wait(&s.dy_empty[y], ((t >> 1) & 1) ^ 1u, s.abort, p.timeout_ns)) goto done;
+      const int dh = static_cast<int>(q / p.n_cand);
+      if (!warp_wait(&s.dy_empty[dyr.slot], dyr.phase ^ 1u, s.abort, p.timeout_ns)) goto done;
       if (elect_one()) {
-        uint8_t* dst = s.dy + y * BWD_CAND_DY_BYTES;
-        mbar_arrive_expect_tx(&s.dy_full[y], dy_bytes);
-        for (int h = 0; h < 2; ++h)
-          for (int j = 0; j < p.kcn; ++j)
-            tma_load_3d(dst + h * CB_DYHALF + j * BOX, &tmDY, &s.dy_full[y], dblk * 128 + 64 * h, 64 * j, b);
+        uint8_t* dst = s.dy + dyr.slot * CAND_DY_SLOT;
+        mbar_arrive_expect_tx(&s.dy_full[dyr.slot], dy_bytes);
+        for (int j = 0; j < p.kcn; ++j) tma_load_3d(dst + j * BOX, &tmDY, &s.dy_full[dyr.slot], dh * 64, 64 * j, b);
       }
       __syncwarp();
-      for (int c = 0; c < nc; ++c, ring.next()) {  // C block c / 2, d half c % 2
-        if (!warp_wait(&s.st_empty[ring.slot], ring.phase ^ 1u, s.abort, p.timeout_ns)) goto done;
-        if (elect_one()) {
-          uint64_t* bar = &s.st_full[ring.slot];
-          mbar_arrive_expect_tx(bar, CB_SLOT);
-          tma_load_3d(s.ring + ring.slot * CB_SLOT, &tmC, bar, dblk * 128 + 64 * (c & 1), 128 * (c >> 1), b);
+    }
+  } else if (warp == 3) {
+    // ---- TMA producer of the C slots (its own warp, so that C runs ahead of
+    // dY by the depth of its ring)
+    if (do_w) {
+      CandWin win;
+      SlotRing<BWD_CAND_C_SLOTS> ring;
+      for (long long q = q0; q < q1; ++q) {
+        int b, u;
+        cand_tile(p, q, q1, win, b, u);
+        const int dh = static_cast<int>(q / p.n_cand);
+        for (int mb = 0; mb < p.n_mblk; ++mb, ring.next()) {
+          if (!warp_wait(&s.st_empty[ring.slot], ring.phase ^ 1u, s.abort, p.timeout_ns)) goto done;
+          if (elect_one()) {
+            uint64_t* bar = &s.st_full[ring.slot];
+            mbar_arrive_expect_tx(bar, CB_SLOT);
+            tma_load_3d(s.ring + ring.slot * CB_SLOT, &tmC, bar, dh * 64, 128 * mb, b);
+          }
+          __syncwarp();
         }
-        __syncwarp();
       }
     }
   } else if (warp == 1) {
-    // ---- MMA issuer: dW_c[m][n] += C[b][m][d] dY[b][n][d]; A = the C slot
-    // (K-major), B = a dY d half (K-major, n rows), 4 steps of 16 d per slot
-    SlotRing ring;
-    const uint32_t idesc = idesc_bf16_f32(128, static_cast<uint32_t>(p.n_mma), false, false);
+    // ---- MMA issuer, per unit:
+    //   dC^T block mb [K_c rows][64 d] = W_c block mb (A, K-major: n) x dY (B, MN-major: d), K = n
+    //   dW_c block mb [K_c rows][n] += C slot (A, K-major: d) x dY (B, K-major: d), K = the unit's 64 d
+    const uint32_t idesc_w = idesc_bf16_f32(128, static_cast<uint32_t>(p.n_mma), false, false);
+    constexpr uint32_t idesc_c = idesc_bf16_f32(128, 64, false, true);
+    const int csteps = 4 * p.kcn;
+    SlotRing<BWD_CAND_DY_SLOTS> dyr;
+    SlotRing<BWD_CAND_C_SLOTS> ring;
+    if (do_c && !warp_wait(s.w_full, 0, s.abort, p.timeout_ns)) goto done;
     int t = 0;
-    for (long long q = q0; q < q1; ++q, ++t) {
-      const int y = t & 1;
-      if (!warp_wait(&s.dy_full[y], (t >> 1) & 1u, s.abort, p.timeout_ns)) goto done;
+    for (long long q = q0; q < q1; ++q, ++t, dyr.next()) {
+      if (!warp_wait(&s.dy_full[dyr.slot], dyr.phase, s.abort, p.timeout_ns)) goto done;
       tc_fence_after();
-      const uint32_t dy_base = smem_u32(s.dy + y * BWD_CAND_DY_BYTES);
-      for (int c = 0; c < nc; ++c, ring.next()) {
-        if (!warp_wait(&s.st_full[ring.slot], ring.phase, s.abort, p.timeout_ns)) goto done;
-        tc_fence_after();
-        if (elect_one()) {
-          const uint64_t adesc = sdesc_sw128(smem_u32(s.ring + ring.slot * CB_SLOT), 16, 1024u);
-          const uint64_t bdesc = sdesc_sw128(dy_base + (c & 1) * CB_DYHALF, 16, 1024u);
-          const uint32_t d_tmem = tmem + static_cast<uint32_t>((c >> 1) * p.n_mma);
-#pragma unroll
-          for (int st = 0; st < 4; ++st)
-            mma_bf16_ss(d_tmem, adesc + st * (32u >> 4), bdesc + st * (32u >> 4), idesc,
-                        (t == 0 && (c & 1) == 0 && st == 0) ? 0u : 1u);
-          mma_commit(&s.st_empty[ring.slot]);
+      const uint32_t dy_base = smem_u32(s.dy + dyr.slot * CAND_DY_SLOT);
+      if (do_c) {
+        for (int mb = 0; mb < p.n_mblk; ++mb) {
+          const int c = t * p.n_mblk + mb;
+          const int acc = c & 1;
+          if (!warp_wait(&s.dc_empty[acc], ((c >> 1) & 1) ^ 1u, s.abort, p.timeout_ns)) goto done;
+          tc_fence_after();
+          if (elect_one()) {
+            const uint32_t a_base = smem_u32(s.w) + static_cast<uint32_t>(mb * 128 * 128);
+            for (int st = 0; st < csteps; ++st) {
+              const uint64_t adesc =
+                  sdesc_sw128(a_base + static_cast<uint32_t>((st >> 2) * m_rows * 128 + (st & 3) * 32), 16, 1024u);
+              const uint64_t bdesc =
+                  sdesc_sw128(dy_base + static_cast<uint32_t>((st >> 2) * BOX + (st & 3) * 2048), BOX, 1024u);
+              mma_bf16_ss(tmem + CAND_DC_COL + static_cast<uint32_t>(acc * 64), adesc, bdesc, idesc_c,
+                          st > 0 ? 1u : 0u);
+            }
+            mma_commit(&s.dc_full[acc]);
+          }
+          __syncwarp();
         }
-        __syncwarp();
       }
-      if (elect_one()) mma_commit(&s.dy_empty[y]);  // every product of this tile has read dY
+      if (do_w) {
+        for (int mb = 0; mb < p.n_mblk; ++mb, ring.next()) {
+          if (!warp_wait(&s.st_full[ring.slot], ring.phase, s.abort, p.timeout_ns)) goto done;
+          tc_fence_after();
+          if (elect_one()) {
+            const uint64_t adesc = sdesc_sw128(smem_u32(s.ring + ring.slot * CB_SLOT), 16, 1024u);
+            const uint64_t bdesc = sdesc_sw128(dy_base, 16, 1024u);
+            const uint32_t d_tmem = tmem + static_cast<uint32_t>(mb * p.n_mma);
+#pragma unroll
+            for (int st = 0; st < 4; ++st)
+              mma_bf16_ss(d_tmem, adesc + st * (32u >> 4), bdesc + st * (32u >> 4), idesc_w,
+                          (t == 0 && st == 0) ? 0u : 1u);
+            mma_commit(&s.st_empty[ring.slot]);
+          }
+          __syncwarp();
+        }
+      }
+      if (elect_one()) mma_commit(&s.dy_empty[dyr.slot]);  // every product of this unit has read dY
       __syncwarp();
     }
-    if (elect_one()) mma_commit(s.w_full);
+    if (do_w && elect_one()) mma_commit(s.wacc_full);
     __syncwarp();
   } else if (warp >= 4) {
-    // ---- epilogue: the S sums, then the CTA's dW_c partial
+    // ---- epilogue: per unit the S sums, then this group's dC accumulators;
+    // at the end the CTA's dW_c partial
     const int et = static_cast<int>(threadIdx.x) - 128;
-    const int quarter = warp & 3, half = (warp - 4) >> 2;
+    const int quarter = warp & 3, grp = (warp - 4) >> 2;
     const uint32_t lane_base = static_cast<uint32_t>(32 * quarter) << 16;
-    const int pd = et & 63, ng = et >> 6;  // S: d pair, group of 16 n rows in each 64-n chunk
-    if (do_s) {
-      float acc[3][16][2];
+    const int pd = et & 31, ng = et >> 5;
+    float acc[3][8][2];
+#pragma unroll
+    for (int j = 0; j < 3; ++j)
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[j][i][0] = acc[j][i][1] = 0.f;
+    if (do_s && lane_id() == 0) {  // this CTA's share of db starts at zero (rows of this warp)
 #pragma unroll
       for (int j = 0; j < 3; ++j)
 #pragma unroll
-        for (int i = 0; i < 16; ++i) acc[j][i][0] = acc[j][i][1] = 0.f;
-      // the open run of (user, D block); whether it holds the range's first
-      // tile (its sums go to slot 0) and whether the last tile seen was in it
-      int run_u = -2, run_dblk = -1;
-      bool run_first = false, last_in_run = false, bad_seen = false;
-      CandWin win;
-      int t = 0;
-      for (long long q = q0; q < q1; ++q, ++t) {
-        int b, u;
-        cand_tile(p, q, q1, win, b, u);
-        const int dblk = static_cast<int>(q / p.n_cand);
-        const int y = t & 1;
-        if (!warp_wait(&s.dy_full[y], (t >> 1) & 1u, s.abort, p.timeout_ns)) goto done;
+        for (int i = 0; i < 8; ++i) s.dbsm[64 * j + 8 * ng + i] = 0.f;
+    }
+    // the open run of (user, D block) and its user's segment
+    int run_u = -1, run_dh = -1, run_oa = 0, run_ob = 0;
+    bool bad_seen = false;
+    CandWin win;
+    SlotRing<BWD_CAND_DY_SLOTS> dyr;
+    int t = 0;
+    for (long long q = q0; q < q1; ++q, ++t, dyr.next()) {
+      int b, u, oa, ob;
+      cand_tile<true>(p, q, q1, win, b, u, &oa, &ob);
+      const int dh = static_cast<int>(q / p.n_cand);
+      if (do_s) {
+        if (!warp_wait(&s.dy_full[dyr.slot], dyr.phase, s.abort, p.timeout_ns)) goto done;
         if (u < 0) {  // out of range: in no user's sum (candidates after the valid ones in perm)
           bad_seen = true;
-          last_in_run = false;
         } else {
-          if (u != run_u || dblk != run_dblk) {
-            if (run_u >= 0) {  // a run ends inside the range: slot 0 if it held the first tile, else S
-              cand_flush(p, acc, run_u, run_dblk, run_first ? 0 : -1, pd, ng);
+          if (u != run_u || dh != run_dh) {
+            if (run_u >= 0) {
+              cand_flush(p, acc, run_u, run_dh, run_oa, run_ob, q0, nq, pd, ng, s.dbsm);
 #pragma unroll
               for (int j = 0; j < 3; ++j)
 #pragma unroll
-                for (int i = 0; i < 16; ++i) acc[j][i][0] = acc[j][i][1] = 0.f;
+                for (int i = 0; i < 8; ++i) acc[j][i][0] = acc[j][i][1] = 0.f;
             }
-            run_first = q == q0;
+            run_u = u;
+            run_dh = dh;
+            run_oa = oa;
+            run_ob = ob;
           }
-          run_u = u;
-          run_dblk = dblk;
-          last_in_run = true;
-          // this thread's 96 elements of the staged tile: d half pd / 32,
-          // byte (2 pd % 64) * 2 of row n, 16-byte chunk swizzled by n % 8
-          const uint8_t* tile = s.dy + y * BWD_CAND_DY_BYTES + (pd >> 5) * CB_DYHALF;
-          const int dd = (2 * pd) & 63;
+          // this thread's 48 elements of the staged block: row n = 64 j + r
+          // of chunk j, bytes 4 pd .. 4 pd + 3, 16-byte chunk swizzled by r % 8 = i
+          const uint8_t* blk = s.dy + dyr.slot * CAND_DY_SLOT;
 #pragma unroll
           for (int j = 0; j < 3; ++j) {
             if (j < p.kcn) {
 #pragma unroll
-              for (int i = 0; i < 16; ++i) {
-                const int n = 64 * j + 16 * ng + i;
+              for (int i = 0; i < 8; ++i) {
+                const int r = 8 * ng + i;
                 const uint32_t w = *reinterpret_cast<const uint32_t*>(
-                    tile + n * 128 + ((((dd >> 3) ^ (n & 7)) << 4) | ((dd & 7) << 1)));
+                    blk + j * BOX + r * 128 + ((((pd >> 2) ^ i) << 4) | ((pd & 3) << 2)));
                 acc[j][i][0] += __uint_as_float(w << 16);
                 acc[j][i][1] += __uint_as_float(w & 0xffff0000u);
               }
             }
           }
         }
-        mbar_arrive(&s.dy_empty[y]);
+        mbar_arrive(&s.dy_empty[dyr.slot]);
       }
-      // the open run: slot 0 if it held the first tile; else slot 1 if it runs
-      // past the range's end (its last tile was the range's), else S
-      if (run_u >= 0) cand_flush(p, acc, run_u, run_dblk, run_first ? 0 : (last_in_run ? 1 : -1), pd, ng);
-      if (bad_seen && et == 0) atomicOr(p.status, DEV_ERR_MAP_RANGE);
+      if (do_c) {
+        for (int mb = 0; mb < p.n_mblk; ++mb) {
+          const int c = t * p.n_mblk + mb;
+          if ((c & 1) != grp) continue;
+          if (!warp_wait(&s.dc_full[grp], (c >> 1) & 1, s.abort, p.timeout_ns)) goto done;
+          tc_fence_after();
+          uint32_t v0[32], v1[32];
+          const uint32_t ta = tmem + lane_base + CAND_DC_COL + static_cast<uint32_t>(grp * 64);
+          tmem_ld32(ta, v0);
+          tmem_ld32(ta + 32, v1);
+          tmem_ld_wait(v0);
+          tmem_ld_wait(v1);
+          tc_fence_before();
+          mbar_arrive(&s.dc_empty[grp]);
+          const int k = mb * 128 + quarter * 32 + static_cast<int>(lane_id());
+          if (k < p.K_c) {
+            // streaming stores: dC is written once and not read here, so it
+            // should not push the S slots and dW_c partials out of L2
+            uint16_t* dst = p.dC + (static_cast<size_t>(b) * p.K_c + k) * p.D + dh * 64;
+            const int dlim = p.D - dh * 64;
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+              if (8 * h < dlim)
+                __stcs(reinterpret_cast<uint4*>(dst + 8 * h),
+                       make_uint4(pack_bf16x2(__uint_as_float(v0[8 * h]), __uint_as_float(v0[8 * h + 1])),
+                                  pack_bf16x2(__uint_as_float(v0[8 * h + 2]), __uint_as_float(v0[8 * h + 3])),
+                                  pack_bf16x2(__uint_as_float(v0[8 * h + 4]), __uint_as_float(v0[8 * h + 5])),
+                                  pack_bf16x2(__uint_as_float(v0[8 * h + 6]), __uint_as_float(v0[8 * h + 7]))));
+            }
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+              if (32 + 8 * h < dlim)
+                __stcs(reinterpret_cast<uint4*>(dst + 32 + 8 * h),
+                       make_uint4(pack_bf16x2(__uint_as_float(v1[8 * h]), __uint_as_float(v1[8 * h + 1])),
+                                  pack_bf16x2(__uint_as_float(v1[8 * h + 2]), __uint_as_float(v1[8 * h + 3])),
+                                  pack_bf16x2(__uint_as_float(v1[8 * h + 4]), __uint_as_float(v1[8 * h + 5])),
+                                  pack_bf16x2(__uint_as_float(v1[8 * h + 6]), __uint_as_float(v1[8 * h + 7]))));
+            }
+          }
+        }
+      }
     }
-    // the CTA's dW_c partial: TMEM lane = K_c row of a block, columns = n
+    if (do_s) {
+      if (run_u >= 0) cand_flush(p, acc, run_u, run_dh, run_oa, run_ob, q0, nq, pd, ng, s.dbsm);
+      if (bad_seen && et == 0) atomicOr(p.status, DEV_ERR_MAP_RANGE);
+      if (lane_id() == 0) {  // this CTA's share of db, for the finish
+#pragma unroll
+        for (int j = 0; j < 3; ++j)
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int n = 64 * j + 8 * ng + i;
+            if (n < p.N) p.dbcta[static_cast<size_t>(blockIdx.x) * p.N + n] = s.dbsm[n];
+          }
+      }
+    }
+    // the CTA's dW_c partial, stored [n][K_c row of the block] so that each
+    // store of the warp covers 32 consecutive rows (TMEM lane = row, column = n)
     if (do_w && q1 > q0) {
-      if (!warp_wait(s.w_full, 0, s.abort, p.timeout_ns)) goto done;
+      if (!warp_wait(s.wacc_full, 0, s.abort, p.timeout_ns)) goto done;
       tc_fence_after();
       const int row = quarter * 32 + static_cast<int>(lane_id());
       const int nchunks = (p.N + 31) / 32;
       for (int mb = 0; mb < p.n_mblk; ++mb) {
-        float* out = p.wpart + (static_cast<size_t>(mb * gridDim.x + blockIdx.x) * 128 + row) * p.N;
-        for (int c = half; c < nchunks; c += 2) {
+        float* out = p.wpart + static_cast<size_t>(mb * gridDim.x + blockIdx.x) * p.N * 128 + row;
+        for (int c = grp; c < nchunks; c += 2) {
           uint32_t v[32];
           tmem_ld32(tmem + lane_base + static_cast<uint32_t>(mb * p.n_mma + c * 32), v);
           tmem_ld_wait(v);
-          if (c * 32 + 32 <= p.N) {
-            float4* o4 = reinterpret_cast<float4*>(out + c * 32);
 #pragma unroll
-            for (int k = 0; k < 8; ++k)
-              o4[k] = make_float4(__uint_as_float(v[4 * k]), __uint_as_float(v[4 * k + 1]),
-                                  __uint_as_float(v[4 * k + 2]), __uint_as_float(v[4 * k + 3]));
-          } else {
-#pragma unroll
-            for (int k = 0; k < 32; ++k)
-              if (c * 32 + k < p.N) out[c * 32 + k] = __uint_as_float(v[k]);
-          }
+          for (int k = 0; k < 32; ++k)
+            if (c * 32 + k < p.N) out[static_cast<size_t>(c * 32 + k) * 128] = __uint_as_float(v[k]);
         }
       }
     }
@@ -886,89 +1223,38 @@ done:
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
+  if (!p.fused_finish || !(do_w || do_s)) return;
+  // grid barrier (every CTA is resident: cooperative launch), then the finish
+  if (threadIdx.x == 0) {
+    __threadfence();
+    atomicAdd(p.ctrl, 1u);
+    const uint64_t t0 = globaltimer_ns();
+    bool ok = true;
+    while (ld_acquire_gpu(p.ctrl) < gridDim.x) {
+      if (globaltimer_ns() - t0 > p.timeout_ns) {
+        ok = false;
+        atomicOr(p.status, DEV_ERR_PIPE_TIMEOUT);
+        break;
+      }
+    }
+    __threadfence();
+    *s.flag = ok ? 1u : 0u;
+  }
+  __syncthreads();
+  if (*s.flag == 0) return;
+  // the pipeline's shared memory is free again: the finish's sums go there
+  cand_finish(p, blockIdx.x, gridDim.x, reinterpret_cast<float*>(s.dy));
+  __syncthreads();
+  // the last CTA out resets the barrier for the next call
+  if (threadIdx.x == 0 && atomicAdd(p.ctrl + 1, 1u) == gridDim.x - 1) {
+    p.ctrl[0] = 0;
+    p.ctrl[1] = 0;
+  }
 }
 
-// S of (user u, D block dblk, slice of N x 128 elements): the run's tiles
-// [a, a + cnt) in q order; a run inside one CTA's range that is neither its
-// first nor its last run was stored straight to S; otherwise the partial
-// slots of the CTAs that share it are added in CTA order (slot 0 where the
-// run holds the CTA's first tile, else slot 1).  Then the hi/lo pair.
-constexpr int SF_THREADS = 256;
-constexpr int SF_ELEMS = 4 * SF_THREADS;  // elements per block
-constexpr int SF_MAX_CTAS = 1024;  // contributors a run may have (the grid never exceeds the SM count)
-__global__ void __launch_bounds__(SF_THREADS) bwd_sfinish_kernel(const SFinishParams p) {
-  __shared__ int c_lo, c_n, c_direct;
-  __shared__ uint32_t c_slot[SF_MAX_CTAS / 32];  // bit k: contributor c_lo + k reads slot 1
-  const int elems = p.N * 128;
-  const int slices = (elems + SF_ELEMS - 1) / SF_ELEMS;
-  const int sl = blockIdx.x % slices;
-  const int ud = blockIdx.x / slices;
-  const int u = ud / p.n_dblk, dblk = ud - u * p.n_dblk;
-  if (u >= p.n_users) return;  // uniform over the block
-  const long long a = static_cast<long long>(dblk) * p.n_cand + __ldg(p.offsets + u);
-  const long long e = static_cast<long long>(dblk) * p.n_cand + __ldg(p.offsets + u + 1);
-  // the run's contributing CTAs and the slot each holds it in, once per
-  // block: every thread tests the ranges [bounds[k], bounds[k + 1]) at once
-  if (threadIdx.x == 0) {
-    c_lo = 0;
-    c_n = 0;
-    c_direct = 0;
-  }
-  __syncthreads();
-  if (e > a) {
-    int c1 = -1;
-    for (int k = static_cast<int>(threadIdx.x); k < p.G; k += SF_THREADS) {
-      const long long b0 = __ldg(p.bounds + k), b1 = __ldg(p.bounds + k + 1);
-      if (b0 <= a && a < b1) {
-        c_lo = k;
-        if (a > b0 && e < b1) c_direct = 1;  // inside one range, neither its first nor its last run: S already
-      }
-      if (b0 <= e - 1 && e - 1 < b1) c1 = k;
-    }
-    __syncthreads();
-    if (c1 >= 0) c_n = c1 - c_lo + 1;
-  }
-  __syncthreads();
-  const int nc = c_n;
-  for (int w = static_cast<int>(threadIdx.x); w < (nc + 31) / 32; w += SF_THREADS) c_slot[w] = 0;
-  __syncthreads();
-  for (int k = static_cast<int>(threadIdx.x); k < nc; k += SF_THREADS)
-    if (a > __ldg(p.bounds + c_lo + k)) atomicOr(&c_slot[k >> 5], 1u << (k & 31));
-  __syncthreads();
-  for (int r = 0; r < SF_ELEMS / SF_THREADS; ++r) {
-    const int idx = sl * SF_ELEMS + r * SF_THREADS + static_cast<int>(threadIdx.x);
-    if (idx >= elems) break;
-    const int n = idx >> 7, dl = idx & 127;
-    const int d = dblk * 128 + dl;
-    if (d >= p.D) continue;
-    float* Sp = p.S + (static_cast<size_t>(u) * p.N + n) * p.D + d;
-    float v = 0.f;
-    if (c_direct) {
-      v = *Sp;
-    } else {
-      // the contributors' values, loaded 8 at a time, then added in CTA order
-      const float* base = p.spart + static_cast<size_t>(n) * 128 + dl;
-      const size_t slot_stride = static_cast<size_t>(p.N) * 128;
-      for (int k0 = 0; k0 < nc; k0 += 8) {
-        float w[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int k = k0 + j;
-          const int slot = k < nc ? static_cast<int>((c_slot[k >> 5] >> (k & 31)) & 1u) : 0;
-          w[j] = k < nc ? __ldg(base + (static_cast<size_t>(c_lo + k) * 2 + slot) * slot_stride) : 0.f;
-        }
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-          if (k0 + j < nc) v += w[j];
-      }
-      *Sp = v;  // 0 for a user without candidates
-    }
-    const __nv_bfloat16 hi = __float2bfloat16_rn(v);
-    const __nv_bfloat16 lo = __float2bfloat16_rn(v - __bfloat162float(hi));
-    uint16_t* s2 = p.S2 + static_cast<size_t>(u) * 2 * p.NPD + static_cast<size_t>(n) * p.D + d;
-    s2[0] = __bfloat16_as_ushort(hi);
-    s2[p.NPD] = __bfloat16_as_ushort(lo);
-  }
+__global__ void __launch_bounds__(CF_THREADS) bwd_cand_finish_kernel(const CandParams p) {
+  __shared__ float4 red[(CF_RED + 3) / 4];
+  cand_finish(p, blockIdx.x, gridDim.x, reinterpret_cast<float*>(red));
 }
 
 }  // namespace
@@ -1010,7 +1296,7 @@ cudaError_t launch_bwd_db(const float* S, float* db, int n_users, int N, int D, 
 bool bwd_cand_configure(CandParams* p, size_t max_smem) {
   if (p->K_c < 1 || p->K_c > BWD_CAND_MAX_KC || p->N < 1 || p->N > BWD_CAND_MAX_N || p->D < 1) return false;
   if (CAND_SMEM > max_smem) return false;
-  p->n_dblk = (p->D + 127) / 128;
+  p->n_dh = (p->D + 63) / 64;
   p->kcn = (p->N + 63) / 64;
   p->n_mblk = (p->K_c + 127) / 128;
   p->n_mma = (p->N + 15) / 16 * 16;
@@ -1018,32 +1304,56 @@ bool bwd_cand_configure(CandParams* p, size_t max_smem) {
 }
 
 int bwd_cand_grid(const CandParams& p, int num_sms) {
-  const long long nq = static_cast<long long>(p.n_dblk) * p.n_cand;
-  return static_cast<int>(nq < num_sms ? nq : num_sms);
+  const long long nq = static_cast<long long>(p.n_dh) * p.n_cand;
+  long long g = nq < num_sms ? nq : num_sms;
+  if (g > CF_CHUNKS * CF_MAX_PER_CHUNK) g = CF_CHUNKS * CF_MAX_PER_CHUNK;  // the finish's chunks
+  return static_cast<int>(g);
 }
 
-cudaError_t launch_bwd_cand(const CUtensorMap& tmDY, const CUtensorMap& tmC, const CandParams& p, int grid,
-                            cudaStream_t s) {
+// p.G CTAs.  With a finish (dW_c, S), as one cooperative launch that ends
+// with it when `cooperative`; where that is refused (not all CTAs can be
+// resident) or not asked for, the pass and then the finish kernel.
+// *launches receives the number of kernels.
+cudaError_t launch_bwd_cand(const CUtensorMap& tmDY, const CUtensorMap& tmC, const CUtensorMap& tmW,
+                            const CandParams& p, int num_sms, bool cooperative, cudaStream_t s, int* launches) {
   cudaError_t e = cudaFuncSetAttribute(bwd_cand_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(CAND_SMEM));
   if (e != cudaSuccess) return e;
-  bwd_cand_kernel<<<grid, BWD_THREADS, CAND_SMEM, s>>>(tmDY, tmC, p);
-  return cudaGetLastError();
+  const bool finish = p.wpart != nullptr || p.S2 != nullptr;
+  CandParams q = p;
+  q.fused_finish = 0;
+  if (finish && cooperative) {
+    q.fused_finish = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(p.G));
+    cfg.blockDim = dim3(BWD_THREADS);
+    cfg.dynamicSmemBytes = CAND_SMEM;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, bwd_cand_kernel, tmDY, tmC, tmW, q);
+    if (e == cudaSuccess) {
+      *launches = 1;
+      return e;
+    }
+    if (e != cudaErrorCooperativeLaunchTooLarge) return e;
+    (void)cudaGetLastError();
+    q.fused_finish = 0;
+  }
+  bwd_cand_kernel<<<p.G, BWD_THREADS, CAND_SMEM, s>>>(tmDY, tmC, tmW, q);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  *launches = 1;
+  if (!finish) return e;
+  bwd_cand_finish_kernel<<<num_sms, CF_THREADS, 0, s>>>(q);
+  e = cudaGetLastError();
+  if (e == cudaSuccess) *launches = 2;
+  return e;
 }
 
-cudaError_t launch_bwd_sfinish(const SFinishParams& p, cudaStream_t s) {
-  const int slices = (p.N * 128 + SF_ELEMS - 1) / SF_ELEMS;
-  bwd_sfinish_kernel<<<p.n_users * p.n_dblk * slices, SF_THREADS, 0, s>>>(p);
-  return cudaGetLastError();
-}
-
-// The in-order reduce of split-K partials part[(mblk * R + r) * 128 + row][n] into dW.
-cudaError_t launch_bwd_wreduce(const float* part, float* dW, int M, int N, int R, cudaStream_t s) {
-  const int total = M * N;
-  bwd_wgrad_reduce_kernel<<<(total + WG_RED_OUT - 1) / WG_RED_OUT, dim3(WG_RED_OUT, WG_RED_SPLIT), 0, s>>>(part, dW,
-                                                                                                       M, N, R);
-  return cudaGetLastError();
-}
 
 size_t bwd_act_smem(const ActParams& p) {
   return SMEM_ALIGN_PAD + act_w_bytes(p.kc, p.m_rows) + static_cast<size_t>(p.stages) * 2 * BOX +
@@ -1091,9 +1401,12 @@ bool bwd_wgrad_configure(WgradParams* p, int num_sms, size_t max_smem) {
   // at the 70:1 shape (dW_c: the second read of dY mostly hits L2 anyway).
   p->mg = 1;
   p->n_mgrp = (p->n_mblk + p->mg - 1) / p->mg;
+  // b ranges: enough to fill the SMs, but at least two batches each (fewer
+  // partials for the reduce; measured 132.7 vs 134.8 us for the LCE backward
+  // at the 70:1 shape, where dW_u's 2 n_users batches would give one each)
   int R = num_sms / p->n_mgrp;
+  if (R > p->B / 2) R = p->B / 2;
   if (R < 1) R = 1;
-  if (R > p->B) R = p->B;
   p->R = R;
   p->dc = (p->D + 63) / 64;
   p->n_mma = (p->N + 15) / 16 * 16;

@@ -188,7 +188,13 @@ ikbo_status_t ikbo_lce_forward_staged(ikbo_plan_t p, const void* U, const void* 
  * bit.  Candidates whose map value is out of range are left out of S (so of
  * dU, dWu and db) and reported by the plan's status; they still enter dC and
  * dWc.  Workspaces (S, partial sums) are plan-owned and grown on first use
- * (that call allocates synchronously).  Limits: D, N multiples of 8,
+ * (that call allocates synchronously).  With both dU and dWu asked for, dWu
+ * runs on a second stream the plan creates on first use, forked from and
+ * joined back into `stream` through events: the call stays ordered on
+ * `stream` like a single-stream one.  With K_c <= 256 and N <= 192 the
+ * candidate side (dC, dWc, S, db) is one cooperative launch whose CTAs wait
+ * for one another once (bounded by the plan's timeout); where a cooperative
+ * launch is refused it is two launches.  Limits: D, N multiples of 8,
  * N <= 256; for dC / dU, K <= 512 and the weight, roundup(K, 128) *
  * ceil(N / 64) * 128 bytes, fits in shared memory beside two 16 KB stages
  * (about 190 KB); else IKBO_ERR_UNSUPPORTED. */
@@ -287,8 +293,11 @@ ikbo_status_t ikbo_plan_get_status(ikbo_plan_t p, cudaStream_t stream);
 /* Debug and robustness knobs.  flags: bit 0 = LCE user tiles compute but do
  * not publish their partials (candidate epilogues then wait, give up after
  * the timeout, form the partial themselves on the CUDA cores, still write a
- * correct Y, and the call reports IKBO_ERR_TIMEOUT).  The timeout bounds
- * every wait inside the kernels (default 2 s). */
+ * correct Y, and the call reports IKBO_ERR_TIMEOUT); bit 1 = the LCE
+ * backward's candidate pass does not end with its finish in the same
+ * (cooperative) launch but is followed by a finish kernel, the path taken
+ * where a cooperative launch is refused.  The timeout bounds every wait
+ * inside the kernels (default 2 s). */
 ikbo_status_t ikbo_plan_set_debug(ikbo_plan_t p, unsigned flags);
 ikbo_status_t ikbo_plan_set_timeout_ns(ikbo_plan_t p, uint64_t timeout_ns);
 

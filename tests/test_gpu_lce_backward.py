@@ -19,7 +19,7 @@ from gpu_util import assert_lce_close, to_dev
 pytestmark = pytest.mark.gpu
 
 
-def run_backward(x, dY, plan=None, want=("dU", "dC", "dWu", "dWc", "db")):
+def run_backward(x, dY, plan=None, want=("dU", "dC", "dWu", "dWc", "db"), debug=0):
     U, C, Wu, Wc, m, g = to_dev(x.U, x.C, x.Wu, x.Wc, x.map, dY)
     bf, f32 = torch.bfloat16, torch.float32
     shapes = {"dU": ((x.n_users, x.K_u, x.D), bf), "dC": ((x.n_cand, x.K_c, x.D), bf),
@@ -28,12 +28,16 @@ def run_backward(x, dY, plan=None, want=("dU", "dC", "dWu", "dWc", "db")):
     own = plan is None
     p = plan or B.Plan(x.n_cand, x.n_users, 1)
     try:
+        if debug:
+            B.ikbo_plan_set_debug(p.handle, debug)
         p.plan(m, x.n_users)
         l0 = p.launches()
         p.lce_backward(U, C, Wu, Wc, g, **out)
         launched = p.launches() - l0
         st = p.status()
     finally:
+        if debug:
+            B.ikbo_plan_set_debug(p.handle, 0)
         if own:
             p.close()
     return out, st, launched
@@ -65,8 +69,10 @@ def test_lce_backward_full(shape):
     dY = gen.make_lce_grad(91, x.n_cand, x.N, x.D)
     out, st, launched = run_backward(x, dY)
     assert st == B.IKBO_OK
-    # candidate pass (or segment sum and dW_c), S finish / db, reduces, dC, dU, dW_u
-    assert launched >= 7
+    if shape["K_c"] <= 256 and shape["N"] <= 192:
+        assert launched == 4  # candidate pass (dC, dW_c, S, db: one cooperative launch), dU, dW_u + reduce
+    else:
+        assert launched >= 7  # segment sum, db, dC, dW_c + reduce, dU, dW_u + reduce
     check_all(x, dY, out, what=str(shape))
 
 
@@ -79,9 +85,30 @@ def test_lce_backward_few_users_many_candidates():
         dY = gen.make_lce_grad(92, x.n_cand, x.N, x.D)
         out, st, launched = run_backward(x, dY)
         assert st == B.IKBO_OK
-        # candidate pass (dW_c, S), S finish, dW_c reduce, db, dC, dU, dW_u (+ reduce)
-        assert launched == 8
+        assert launched == 4  # candidate pass, dU, dW_u + reduce
         check_all(x, dY, out, what=f"{n_users} users")
+
+
+@pytest.mark.parametrize("shape", [
+    dict(n_cand=300, n_users=7, K_u=100, K_c=243, D=256, N=192, map_kind="permuted"),
+    # users 1 and 3 without candidates, ragged D block
+    dict(n_cand=37, n_users=5, K_u=37, K_c=29, D=136, N=40, explicit_map=[(0, 2, 4)[i % 3] for i in range(37)]),
+])
+def test_lce_backward_finish_kernel(shape):
+    """The path taken where a cooperative launch is refused: the candidate
+    pass, then the finish (dW_c reduce, db, zero S of users without
+    candidates) as a second kernel.  Same bits as the one-launch path."""
+    x = gen.make_lce("bwd_fin", 96, **shape)
+    dY = gen.make_lce_grad(96, x.n_cand, x.N, x.D)
+    with B.Plan(x.n_cand, x.n_users, 1) as p:
+        two, st, launched = run_backward(x, dY, plan=p, debug=B.DEBUG_NO_COOPERATIVE)
+        assert st == B.IKBO_OK
+        assert launched == 5
+        one, st, launched = run_backward(x, dY, plan=p)
+        assert st == B.IKBO_OK and launched == 4
+    for k in one:
+        assert torch.equal(one[k], two[k]), k
+    check_all(x, dY, two, what=str(shape))
 
 
 def test_lce_backward_70to1_full():
