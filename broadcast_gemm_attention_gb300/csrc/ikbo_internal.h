@@ -165,8 +165,9 @@ struct ActParams {
   int n_dblk;                // ceil(D / 128)
   int kc;                    // ceil(N / 64): resident W chunks
   int kcx;                   // X chunks per b (kc, or 2 * kc for a hi/lo pair)
-  int m_pad;                 // roundup(M, 16): accumulator columns
-  int m_rows;                // roundup(M, 128): resident W rows per K chunk
+  int m_pad;                 // accumulator columns: roundup(M, 16), or 128 when M is split
+  int m_rows;                // resident W rows per K chunk: roundup(M, 128), or 128 when M is split
+  int n_mgrp;                // blocks of m_rows rows M is split into (1: not split)
   int bufs;                  // accumulator buffers (2 when m_pad <= 256)
   int stages;                // X ring depth
   uint64_t timeout_ns;

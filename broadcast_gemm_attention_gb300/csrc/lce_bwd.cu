@@ -205,9 +205,11 @@ __device__ __forceinline__ ActSmem act_carve(uint8_t* base, const ActParams& p) 
   return s;
 }
 
-// Tiles q = dblk * B + b (D-block-major); each CTA takes one contiguous range.
+// Tiles q = (mg * n_dblk + dblk) * B + b (block of M rows, then
+// D-block-major); each CTA takes one contiguous range (one tile per CTA
+// when M is split, so that its resident W block is the tile's).
 __device__ __forceinline__ void act_range(const ActParams& p, int& q0, int& q1) {
-  const long long nq = static_cast<long long>(p.B) * p.n_dblk;
+  const long long nq = static_cast<long long>(p.B) * p.n_dblk * p.n_mgrp;
   q0 = static_cast<int>(blockIdx.x * nq / gridDim.x);
   q1 = static_cast<int>((blockIdx.x + 1) * nq / gridDim.x);
 }
@@ -249,18 +251,21 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
   act_range(p, q0, q1);
 
   if (warp == 0) {
-    // ---- TMA producer: W once, then the X chunks of every tile
+    // ---- TMA producer: W (the CTA's block of M rows) once, then the X
+    // chunks of every tile
     if (elect_one()) {
+      const int m0 = (q0 / (p.n_dblk * p.B)) * p.m_rows;
       mbar_arrive_expect_tx(s.w_full, act_w_bytes(p.kc, p.m_rows));
       for (int kc = 0; kc < p.kc; ++kc)
         for (int r = 0; r < p.m_rows; r += 128)
-          tma_load_2d(s.w + (static_cast<size_t>(kc) * p.m_rows + r) * 128, &tmW, s.w_full, kc * 64, r);
+          tma_load_2d(s.w + (static_cast<size_t>(kc) * p.m_rows + r) * 128, &tmW, s.w_full, kc * 64, m0 + r);
     }
     __syncwarp();
     int stage = 0;
     uint32_t phase = 0;
     for (int q = q0; q < q1; ++q) {
-      const int dblk = q / p.B, b = q - dblk * p.B;
+      const int rem = q % (p.n_dblk * p.B);
+      const int dblk = rem / p.B, b = rem - dblk * p.B;
       for (int kc = 0; kc < p.kcx; ++kc) {
         if (!warp_wait(&s.a_empty[stage], phase ^ 1u, s.abort, p.timeout_ns)) goto done;
         if (elect_one()) {
@@ -321,16 +326,19 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     // ---- epilogue: TMEM lane = row d of the D block, columns = m
     const int quarter = warp & 3, half = (warp - 4) >> 2;
     const uint32_t lane_base = static_cast<uint32_t>(32 * quarter) << 16;
-    const int nchunks = (p.M + 31) / 32;
     for (int q = q0, t = 0; q < q1; ++q, ++t) {
-      const int dblk = q / p.B, b = q - dblk * p.B;
+      const int mg = q / (p.n_dblk * p.B), rem = q - mg * (p.n_dblk * p.B);
+      const int dblk = rem / p.B, b = rem - dblk * p.B;
+      const int m0 = mg * p.m_rows, mlen = min(p.M - m0, p.m_rows);
+      const int nchunks = (mlen + 31) / 32;
       const int buf = p.bufs == 2 ? (t & 1) : 0;
       const uint32_t use = static_cast<uint32_t>(p.bufs == 2 ? (t >> 1) : t);
       if (!warp_wait(&s.acc_full[buf], use & 1u, s.abort, p.timeout_ns)) goto done;
       tc_fence_after();
       const int d = dblk * 128 + quarter * 32 + static_cast<int>(lane_id());
       const bool dok = d < p.D;
-      __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out) + static_cast<size_t>(b) * p.M * p.D + d;
+      __nv_bfloat16* out =
+          reinterpret_cast<__nv_bfloat16*>(p.out) + (static_cast<size_t>(b) * p.M + m0) * p.D + d;
       for (int c = half; c < nchunks; c += 2) {
         uint32_t v[32];
         tmem_ld32(tmem + lane_base + static_cast<uint32_t>(buf * 256 + c * 32), v);
@@ -338,7 +346,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         __nv_bfloat16* o = out + static_cast<size_t>(c * 32) * p.D;
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
-          if (c * 32 + j < p.M && dok) *o = __float2bfloat16_rn(__uint_as_float(v[j]));
+          if (c * 32 + j < mlen && dok) *o = __float2bfloat16_rn(__uint_as_float(v[j]));
           o += p.D;
         }
       }
@@ -596,7 +604,7 @@ constexpr uint32_t CAND_W_BYTES = 3 * 256 * 128;  // W_c: <= 3 n chunks x 256 ro
 constexpr uint32_t CAND_TILES =
     CAND_W_BYTES + BWD_CAND_DY_SLOTS * CAND_DY_SLOT + BWD_CAND_C_SLOTS * CB_SLOT;
 constexpr int CAND_BARS = 2 * BWD_CAND_DY_SLOTS + 2 * BWD_CAND_C_SLOTS + 1 + 4 + 1;
-constexpr size_t CAND_SMEM = 1024 + CAND_TILES + 8 * CAND_BARS + 16 + 4 * BWD_CAND_MAX_N;
+constexpr size_t CAND_SMEM = 1024 + CAND_TILES + 8 * CAND_BARS + 16 + 4 * BWD_CAND_MAX_N + 16 * 4;
 static_assert(CAND_SMEM <= 227 * 1024, "candidate pass does not fit in shared memory");
 constexpr uint32_t CAND_DC_COL = 2 * BWD_CAND_MAX_N;  // after the two dW_c blocks
 static_assert(CAND_DC_COL + 128 <= 512, "candidate pass accumulators exceed TMEM");
@@ -618,6 +626,7 @@ struct CandSmem {
   uint32_t* abort;
   uint32_t* flag;      // the grid barrier was passed
   float* dbsm;         // [BWD_CAND_MAX_N] this CTA's share of db
+  int4* pre;           // [4] bounds of this CTA's first finish tasks
 };
 
 __device__ __forceinline__ CandSmem cand_carve(uint8_t* base) {
@@ -638,6 +647,7 @@ __device__ __forceinline__ CandSmem cand_carve(uint8_t* base) {
   s.abort = s.tmem_slot + 1;
   s.flag = s.abort + 1;
   s.dbsm = reinterpret_cast<float*>(s.flag + 2);  // 8-byte aligned
+  s.pre = reinterpret_cast<int4*>(s.dbsm + BWD_CAND_MAX_N);  // 16-byte aligned
   return s;
 }
 
@@ -781,15 +791,35 @@ __device__ __forceinline__ void cand_flush(const CandParams& p, const CandAcc& a
 //   the other warps: S of the runs shared by several CTAs (their slots added
 //     in CTA order), then db[n] for n = g, g + G2, ... (the CTAs' shares
 //     added in CTA order).
-constexpr int CF_CHUNKS = 8;
-constexpr int CF_MAX_PER_CHUNK = 24;  // CTAs per chunk: G <= CF_CHUNKS * 24 = 192
+constexpr int CF_CHUNKS = 6;
+constexpr int CF_MAX_PER_CHUNK = 26;  // CTAs per chunk: G <= CF_CHUNKS * 26 = 156
 constexpr int CF_THREADS = BWD_THREADS;
 constexpr int CF_SIDE = CF_THREADS - 32 * CF_CHUNKS;  // threads on the runs and db
 constexpr int CF_SLICES = 4;          // slices of a shared run's S
-constexpr int CF_UNROLL = 6;
+constexpr int CF_UNROLL = 8;        // pairs per thread at a time: a slice of N = 192 in one round
+constexpr int CF_BATCH = 4;         // contributing CTAs per round of loads
+constexpr int CF_PRE = 4;           // tasks whose bounds the candidate pass looks up ahead
 constexpr int CF_RED = CF_CHUNKS * 128 + CF_CHUNKS * CF_MAX_PER_CHUNK;  // chunk sums, then the CTAs' db shares of one n
 static_assert(CF_SIDE >= 64 && CF_SIDE % 32 == 0, "finish: too few threads for the runs");
-__device__ __forceinline__ void cand_finish(const CandParams& p, int g, int G2, float* red) {
+// Bounds of finish task `task` (run r = (u, dh), slice): (u, dh * CF_SLICES
+// + slice, c_lo, c_hi with the low bit of c_lo's slot in bit 16 of .y), or
+// x = -1 when the run needs no finish (no candidates, or inside one CTA).
+__device__ __forceinline__ int4 cand_task_bounds(const CandParams& p, int task) {
+  const int r = task / CF_SLICES, sl = task - r * CF_SLICES;
+  const int u = r / p.n_dh, dh = r - u * p.n_dh;
+  const long long nq = static_cast<long long>(p.n_dh) * p.n_cand;
+  const long long a = static_cast<long long>(dh) * p.n_cand + __ldg(p.offsets + u);
+  const long long e = static_cast<long long>(dh) * p.n_cand + __ldg(p.offsets + u + 1);
+  if (e == a) return make_int4(-1, 0, 0, 0);  // no candidates: zero from the start
+  const int c_lo = cand_cta_of(a, nq, p.G), c_hi = cand_cta_of(e - 1, nq, p.G);
+  if (c_lo == c_hi) return make_int4(-1, 0, 0, 0);  // final already
+  const int slot_lo = a > cand_q0(nq, c_lo, p.G) ? 1 : 0;
+  return make_int4(u, (dh * CF_SLICES + sl) | (slot_lo << 16), c_lo, c_hi);
+}
+
+// `pre`: the bounds of this block's first CF_PRE tasks, looked up ahead (or
+// null).
+__device__ __forceinline__ void cand_finish(const CandParams& p, int g, int G2, float* red, const int4* pre) {
   const int t = static_cast<int>(threadIdx.x), w = t >> 5, lane = t & 31;
   if (w < CF_CHUNKS) {
     if (!p.wpart) return;
@@ -841,34 +871,29 @@ __device__ __forceinline__ void cand_finish(const CandParams& p, int g, int G2, 
   }
   if (!p.S2) return;
   // runs shared by several CTAs: task (run r = (u, dh), slice) goes to block
-  // (r * CF_SLICES + slice) mod G2, two d per thread, CF_UNROLL pairs per
-  // thread at a time
+  // task mod G2; two d per thread, all of a thread's pairs of the slice and
+  // CF_BATCH contributing CTAs per round of loads
   const int ts = t - 32 * CF_CHUNKS;
-  const long long nq = static_cast<long long>(p.n_dh) * p.n_cand;
   const size_t slot_elems = static_cast<size_t>(p.N) * 64;
   const int pairs = p.N * 32, per_slice = (pairs + CF_SLICES - 1) / CF_SLICES;
-  for (int task = g; task < p.n_users * p.n_dh * CF_SLICES; task += G2) {
-    const int r = task / CF_SLICES, sl = task - r * CF_SLICES;
-    const int u = r / p.n_dh, dh = r - u * p.n_dh;
-    const long long a = static_cast<long long>(dh) * p.n_cand + __ldg(p.offsets + u);
-    const long long e = static_cast<long long>(dh) * p.n_cand + __ldg(p.offsets + u + 1);
-    if (e == a) continue;  // no candidates: zero from the start
-    const int c_lo = cand_cta_of(a, nq, p.G), c_hi = cand_cta_of(e - 1, nq, p.G);
-    if (c_lo == c_hi) continue;  // final already
-    const int slot_lo = a > cand_q0(nq, c_lo, p.G) ? 1 : 0;
+  for (int task = g, k_task = 0; task < p.n_users * p.n_dh * CF_SLICES; task += G2, ++k_task) {
+    const int4 tb = (pre && k_task < CF_PRE) ? pre[k_task] : cand_task_bounds(p, task);
+    if (tb.x < 0) continue;
+    const int u = tb.x, dh = (tb.y & 0xffff) / CF_SLICES, sl = (tb.y & 0xffff) - dh * CF_SLICES;
+    const int slot_lo = tb.y >> 16, c_lo = tb.z, c_hi = tb.w;
     const int i0 = sl * per_slice, i1 = min(pairs, i0 + per_slice);
     for (int ib = i0 + ts; ib < i1; ib += CF_UNROLL * CF_SIDE) {
       float2 v[CF_UNROLL];
 #pragma unroll
       for (int k = 0; k < CF_UNROLL; ++k) v[k] = make_float2(0.f, 0.f);
-      for (int c0 = c_lo; c0 <= c_hi; c0 += 8) {
-        float2 x[CF_UNROLL][8];
+      for (int c0 = c_lo; c0 <= c_hi; c0 += CF_BATCH) {
+        float2 x[CF_UNROLL][CF_BATCH];
 #pragma unroll
         for (int k = 0; k < CF_UNROLL; ++k) {
           const int idx = ib + k * CF_SIDE;
           const float* src = p.spart + static_cast<size_t>(idx >> 5) * 64 + 2 * (idx & 31);
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
+          for (int j = 0; j < CF_BATCH; ++j) {
             const int c = c0 + j;
             const int slot = c == c_lo ? slot_lo : 0;
             x[k][j] = (c <= c_hi && idx < i1)
@@ -879,7 +904,7 @@ __device__ __forceinline__ void cand_finish(const CandParams& p, int g, int G2, 
 #pragma unroll
         for (int k = 0; k < CF_UNROLL; ++k)
 #pragma unroll
-          for (int j = 0; j < 8; ++j)
+          for (int j = 0; j < CF_BATCH; ++j)
             if (c0 + j <= c_hi) {
               v[k].x += x[k][j].x;
               v[k].y += x[k][j].y;
@@ -967,6 +992,12 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *s.tmem_slot;
+  if (warp == 2 && p.fused_finish && do_s && lane_id() < CF_PRE) {
+    // idle until the end: look up this CTA's first finish tasks now (the
+    // grid's CTAs are the finish's blocks)
+    const int task = blockIdx.x + static_cast<int>(lane_id()) * gridDim.x;
+    s.pre[lane_id()] = task < p.n_users * p.n_dh * CF_SLICES ? cand_task_bounds(p, task) : make_int4(-1, 0, 0, 0);
+  }
   const long long nq = static_cast<long long>(p.n_dh) * p.n_cand;
   const long long q0 = cand_q0(nq, blockIdx.x, gridDim.x), q1 = cand_q0(nq, blockIdx.x + 1, gridDim.x);
   if (do_s) cand_empty_users(p);
@@ -1243,7 +1274,7 @@ done:
   __syncthreads();
   if (*s.flag == 0) return;
   // the pipeline's shared memory is free again: the finish's sums go there
-  cand_finish(p, blockIdx.x, gridDim.x, reinterpret_cast<float*>(s.dy));
+  cand_finish(p, blockIdx.x, gridDim.x, reinterpret_cast<float*>(s.dy), s.pre);
   __syncthreads();
   // the last CTA out resets the barrier for the next call
   if (threadIdx.x == 0 && atomicAdd(p.ctrl + 1, 1u) == gridDim.x - 1) {
@@ -1254,7 +1285,7 @@ done:
 
 __global__ void __launch_bounds__(CF_THREADS) bwd_cand_finish_kernel(const CandParams p) {
   __shared__ float4 red[(CF_RED + 3) / 4];
-  cand_finish(p, blockIdx.x, gridDim.x, reinterpret_cast<float*>(red));
+  cand_finish(p, blockIdx.x, gridDim.x, reinterpret_cast<float*>(red), nullptr);
 }
 
 }  // namespace
@@ -1361,13 +1392,23 @@ size_t bwd_act_smem(const ActParams& p) {
 }
 
 // Fills the derived fields from B, M, D, N; `pair`: X holds a hi/lo pair
-// (2 * kc chunks per b).  False for shapes it cannot run.
-bool bwd_act_configure(ActParams* p, size_t max_smem, bool pair) {
+// (2 * kc chunks per b).  When the tiles are fewer than the SMs even with M
+// split into 128-row blocks, each CTA takes one (tile, M block) and keeps
+// only that block of W (a third of the weight at K_u = 381, and three times
+// the CTAs).  False for shapes it cannot run.
+bool bwd_act_configure(ActParams* p, size_t max_smem, bool pair, int num_sms) {
   if (p->B < 1 || p->M < 1 || p->D < 1 || p->N < 1) return false;
   p->n_dblk = (p->D + 127) / 128;
   p->kc = (p->N + 63) / 64;
   p->m_pad = (p->M + 15) / 16 * 16;
   p->m_rows = (p->M + 127) / 128 * 128;
+  p->n_mgrp = 1;
+  const int mblocks = p->m_rows / 128;
+  if (mblocks > 1 && static_cast<long long>(p->B) * p->n_dblk * mblocks <= num_sms) {
+    p->n_mgrp = mblocks;
+    p->m_rows = 128;
+    p->m_pad = 128;
+  }
   p->bufs = p->m_pad <= 256 ? 2 : 1;
   p->kcx = pair ? 2 * p->kc : p->kc;
   if (p->m_pad > 512) return false;
@@ -1382,7 +1423,7 @@ cudaError_t launch_bwd_act(const CUtensorMap& tmX, const CUtensorMap& tmW, const
   cudaError_t e =
       cudaFuncSetAttribute(bwd_act_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  const long long tiles = static_cast<long long>(p.B) * p.n_dblk;
+  const long long tiles = static_cast<long long>(p.B) * p.n_dblk * p.n_mgrp;
   const int grid = static_cast<int>(tiles < num_sms ? tiles : num_sms);
   bwd_act_kernel<<<grid, BWD_THREADS, smem, s>>>(tmX, tmW, p);
   return cudaGetLastError();
