@@ -28,7 +28,7 @@ cudaError_t launch_attn(const CUtensorMap& tmQ, const CUtensorMap& tmQu, const C
 int bwd_segsum_chunks(int n_cand, int n_users, int ND, int num_sms);
 cudaError_t launch_bwd_segsum(const SegSumParams& p, cudaStream_t s, int* launches);
 cudaError_t launch_bwd_db(const float* S, float* db, int n_users, int N, int D, cudaStream_t s);
-bool bwd_act_configure(ActParams* p, size_t max_smem, bool pair, int num_sms);
+bool bwd_act_configure(ActParams* p, size_t max_smem, bool pair, int num_sms, bool split);
 cudaError_t launch_bwd_act(const CUtensorMap& tmX, const CUtensorMap& tmW, const ActParams& p, int num_sms,
                            cudaStream_t s);
 bool bwd_wgrad_configure(WgradParams* p, int num_sms, size_t max_smem);
@@ -623,8 +623,12 @@ ikbo_status_t ikbo_lce_backward(ikbo_plan_t p, const void* U, const void* C, con
   wu.M = K_u, wu.D = D, wu.N = N;
   wu.B = 2 * n_users;  // G = the hi/lo pair of S per user; A = U[b >> 1]
   wu.a_shift = 1;
-  if ((!use_cand && dC && !bwd_act_configure(&ac, p->max_smem, false, p->num_sms)) ||
-      (dU && !bwd_act_configure(&au, p->max_smem, true, p->num_sms)) ||
+  // dU splits K_u over more CTAs only when it runs alone: beside dW_u, whose
+  // split-K CTAs form clusters, its 30 CTAs at 70:1 leave room for them
+  // (118.4 vs 123.5 us for the call at 70:1; alone, dU takes 57.0 us split
+  // and 61.1 unsplit, both timed with the candidate pass before it)
+  if ((!use_cand && dC && !bwd_act_configure(&ac, p->max_smem, false, p->num_sms, false)) ||
+      (dU && !bwd_act_configure(&au, p->max_smem, true, p->num_sms, dWu == nullptr)) ||
       (!use_cand && dWc && !bwd_wgrad_configure(&wc, p->num_sms, p->max_smem)) ||
       (dWu && !bwd_wgrad_configure(&wu, p->num_sms, p->max_smem)))
     return IKBO_ERR_UNSUPPORTED;

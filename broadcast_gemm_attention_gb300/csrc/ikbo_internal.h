@@ -180,7 +180,10 @@ struct ActParams {
 constexpr int BWD_WG_MAX_STAGES = 4;
 
 struct WgradParams {
-  float* part;               // [n_units][128][N] fp32
+  float* part;               // [n_units][128][N] fp32 (split-K partials; not used with clusters)
+  float* dW;                 // [M][N] fp32, written by the kernel itself with clusters
+  int cluster;               // 0: partials + reduce kernel; else the R CTAs of an m block form a
+                             // cluster and add their partials through distributed shared memory
   uint32_t* status;
   int B, M, D, N;            // B = batches of G; A's batch is b >> a_shift
   int a_shift;               // 1 when G holds a hi/lo pair per batch of A

@@ -364,6 +364,30 @@ done:
   }
 }
 
+// ------------------------------------------------ thread-block clusters
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Every thread of every CTA of the cluster (a hardware barrier like
+// __syncthreads; each path to it is bounded).
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// The address of this CTA's shared-memory location `saddr` in the CTA of
+// cluster rank `rank`.
+__device__ __forceinline__ uint32_t cluster_map(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+
 // ---------------------------------------------------- weight-gradient GEMM
 // A unit covers a group of up to two 128-row m blocks (accumulators at TMEM
 // columns 0 and 256) over one b range, so the G tiles it loads serve both
@@ -521,6 +545,18 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       wg_unit(p, u, mblk0, nblk, r, b0, b1);
       if (!warp_wait(s.acc_full, use & 1u, s.abort, p.timeout_ns)) goto done;
       tc_fence_after();
+      if (p.cluster) {  // one unit per CTA, one m block: the partial goes to this CTA's own shared memory
+        float* red = reinterpret_cast<float*>(s.ring) + row * (p.n_mma + 1);
+        for (int c = half; c < nchunks; c += 2) {
+          uint32_t v[32];
+          tmem_ld32(tmem + lane_base + static_cast<uint32_t>(c * 32), v);
+          tmem_ld_wait(v);
+#pragma unroll
+          for (int k = 0; k < 32; ++k)
+            if (c * 32 + k < p.N) red[c * 32 + k] = __uint_as_float(v[k]);
+        }
+        nblk = 0;
+      }
       for (int j = 0; j < nblk; ++j) {
         float* out = p.part + (static_cast<size_t>((mblk0 + j) * p.R + r) * 128 + row) * p.N;
         for (int c = half; c < nchunks; c += 2) {
@@ -552,6 +588,28 @@ done:
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
+  if (!p.cluster) return;
+  // the R partials of m block blockIdx.x / R, in the shared memory of the R
+  // CTAs of this cluster: CTA rank k writes rows [k*128/R, (k+1)*128/R) of
+  // dW, each the sum of the partials in rank order (a fixed order)
+  cluster_sync_all();
+  {
+    const uint32_t R = static_cast<uint32_t>(p.R), rank = cluster_rank();
+    const int mblk = static_cast<int>(blockIdx.x) / p.R;
+    const int r0 = static_cast<int>(rank * 128u / R), r1 = static_cast<int>((rank + 1u) * 128u / R);
+    const int RS = p.n_mma + 1;
+    const uint32_t red = smem_u32(s.ring);
+    for (int e = threadIdx.x; e < (r1 - r0) * p.N; e += BWD_THREADS) {
+      const int row = r0 + e / p.N, n = e - (e / p.N) * p.N;
+      const int m = mblk * 128 + row;
+      if (m >= p.M) continue;
+      const uint32_t off = static_cast<uint32_t>(row * RS + n) * 4u;
+      float v = 0.f;
+      for (uint32_t k = 0; k < R; ++k) v += ld_cluster_f32(cluster_map(red + off, k));
+      p.dW[static_cast<size_t>(m) * p.N + n] = v;
+    }
+  }
+  cluster_sync_all();  // no CTA leaves while another still reads its partial
 }
 
 // dW[m][n] = sum over the b ranges of m's block.  32 outputs per CTA, 8
@@ -1392,11 +1450,11 @@ size_t bwd_act_smem(const ActParams& p) {
 }
 
 // Fills the derived fields from B, M, D, N; `pair`: X holds a hi/lo pair
-// (2 * kc chunks per b).  When the tiles are fewer than the SMs even with M
-// split into 128-row blocks, each CTA takes one (tile, M block) and keeps
-// only that block of W (a third of the weight at K_u = 381, and three times
-// the CTAs).  False for shapes it cannot run.
-bool bwd_act_configure(ActParams* p, size_t max_smem, bool pair, int num_sms) {
+// (2 * kc chunks per b).  With `split`, when the tiles are fewer than the
+// SMs even with M split into 128-row blocks, each CTA takes one (tile, M
+// block) and keeps only that block of W (a third of the weight at K_u = 381,
+// and three times the CTAs).  False for shapes it cannot run.
+bool bwd_act_configure(ActParams* p, size_t max_smem, bool pair, int num_sms, bool split) {
   if (p->B < 1 || p->M < 1 || p->D < 1 || p->N < 1) return false;
   p->n_dblk = (p->D + 127) / 128;
   p->kc = (p->N + 63) / 64;
@@ -1404,7 +1462,7 @@ bool bwd_act_configure(ActParams* p, size_t max_smem, bool pair, int num_sms) {
   p->m_rows = (p->M + 127) / 128 * 128;
   p->n_mgrp = 1;
   const int mblocks = p->m_rows / 128;
-  if (mblocks > 1 && static_cast<long long>(p->B) * p->n_dblk * mblocks <= num_sms) {
+  if (split && mblocks > 1 && static_cast<long long>(p->B) * p->n_dblk * mblocks <= num_sms) {
     p->n_mgrp = mblocks;
     p->m_rows = 128;
     p->m_pad = 128;
@@ -1462,6 +1520,9 @@ size_t bwd_wgrad_part_elems(const WgradParams& p) {
 }
 
 // The split-K kernel (partials into p.part) and the in-order reduce into dW.
+// With mg == 1, R <= 16 and the R CTAs of an m block co-schedulable as a
+// cluster, one launch (the partials are added through distributed shared
+// memory); else the partials kernel and the reduce kernel.
 cudaError_t launch_bwd_wgrad(const CUtensorMap& tmA, const CUtensorMap& tmG, const WgradParams& p, float* dW,
                              int num_sms, cudaStream_t s, int* launches) {
   const size_t smem = bwd_wgrad_smem(p);
@@ -1469,7 +1530,36 @@ cudaError_t launch_bwd_wgrad(const CUtensorMap& tmA, const CUtensorMap& tmG, con
       cudaFuncSetAttribute(bwd_wgrad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   const int units = p.n_mgrp * p.R;
-  bwd_wgrad_kernel<<<units < num_sms ? units : num_sms, BWD_THREADS, smem, s>>>(tmA, tmG, p);
+  const size_t red_bytes = static_cast<size_t>(128) * (p.n_mma + 1) * sizeof(float);
+  if (p.mg == 1 && p.R >= 2 && p.R <= 16 && red_bytes <= static_cast<size_t>(p.stages) * wg_stage_bytes(p.mg, p.nb)) {
+    WgradParams q = p;
+    q.cluster = 1;
+    q.dW = dW;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(units));
+    cfg.blockDim = dim3(BWD_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(p.R);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int active = 0;
+    if ((p.R <= 8 || cudaFuncSetAttribute(bwd_wgrad_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+                         cudaSuccess) &&
+        cudaOccupancyMaxActiveClusters(&active, bwd_wgrad_kernel, &cfg) == cudaSuccess && active >= 1) {
+      e = cudaLaunchKernelEx(&cfg, bwd_wgrad_kernel, tmA, tmG, q);
+      if (e == cudaSuccess) *launches += 1;
+      return e;
+    }
+    (void)cudaGetLastError();  // no cluster of that size fits: partials and the reduce kernel
+  }
+  WgradParams q = p;
+  q.cluster = 0;
+  bwd_wgrad_kernel<<<units < num_sms ? units : num_sms, BWD_THREADS, smem, s>>>(tmA, tmG, q);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int total = p.M * p.N;

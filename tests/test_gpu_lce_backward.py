@@ -70,7 +70,9 @@ def test_lce_backward_full(shape):
     out, st, launched = run_backward(x, dY)
     assert st == B.IKBO_OK
     if shape["K_c"] <= 256 and shape["N"] <= 192:
-        assert launched == 4  # candidate pass (dC, dW_c, S, db: one cooperative launch), dU, dW_u + reduce
+        # candidate pass (dC, dW_c, S, db: one cooperative launch), dU, dW_u (one
+        # launch as a cluster per K_u block, or split-K partials + reduce)
+        assert launched in (3, 4)
     else:
         assert launched >= 7  # segment sum, db, dC, dW_c + reduce, dU, dW_u + reduce
     check_all(x, dY, out, what=str(shape))
@@ -85,7 +87,7 @@ def test_lce_backward_few_users_many_candidates():
         dY = gen.make_lce_grad(92, x.n_cand, x.N, x.D)
         out, st, launched = run_backward(x, dY)
         assert st == B.IKBO_OK
-        assert launched == 4  # candidate pass, dU, dW_u + reduce
+        assert launched in (3, 4)  # candidate pass, dU, dW_u (cluster, or partials + reduce)
         check_all(x, dY, out, what=f"{n_users} users")
 
 
@@ -103,9 +105,9 @@ def test_lce_backward_finish_kernel(shape):
     with B.Plan(x.n_cand, x.n_users, 1) as p:
         two, st, launched = run_backward(x, dY, plan=p, debug=B.DEBUG_NO_COOPERATIVE)
         assert st == B.IKBO_OK
-        assert launched == 5
+        assert launched in (4, 5)
         one, st, launched = run_backward(x, dY, plan=p)
-        assert st == B.IKBO_OK and launched == 4
+        assert st == B.IKBO_OK and launched in (3, 4)
     for k in one:
         assert torch.equal(one[k], two[k]), k
     check_all(x, dY, two, what=str(shape))
