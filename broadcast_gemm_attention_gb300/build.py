@@ -23,7 +23,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libikbo.so")
 SOURCES = ["seg.cu", "lce.cu", "lce_noalloc.cu", "lce_bwd.cu", "attn.cu", "attn_bwd.cu", "api.cu"]
-HEADERS = ["ptx.cuh", "ikbo_internal.h"]
+HEADERS = ["ptx.cuh", "ikbo_internal.h", "bwd_internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

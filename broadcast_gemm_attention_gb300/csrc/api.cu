@@ -12,7 +12,7 @@
 #include <new>
 
 #include "ikbo.h"
-#include "ikbo_internal.h"
+#include "bwd_internal.h"
 
 namespace ikbo {
 cudaError_t launch_seg_build(const SegParams& p, cudaStream_t s);

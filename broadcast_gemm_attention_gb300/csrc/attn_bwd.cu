@@ -40,7 +40,7 @@
 #include <cuda_bf16.h>
 #include <math.h>
 
-#include "ikbo_internal.h"
+#include "bwd_internal.h"
 #include "ptx.cuh"
 
 namespace ikbo {

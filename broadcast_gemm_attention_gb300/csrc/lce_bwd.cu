@@ -24,7 +24,7 @@
 // lane), warp 2 TMEM owner, warps 4-11 epilogue.  Every wait is bounded.
 #include <cuda_bf16.h>
 
-#include "ikbo_internal.h"
+#include "bwd_internal.h"
 #include "ptx.cuh"
 
 namespace ikbo {
