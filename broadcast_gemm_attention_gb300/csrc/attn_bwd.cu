@@ -150,6 +150,40 @@ __device__ __forceinline__ void store_bf16x32(uint16_t* dst, const uint32_t (&v)
                       pack_bf16x2(__uint_as_float(v[8 * k + 6]), __uint_as_float(v[8 * k + 7])));
 }
 
+// Paired fp32 arithmetic (one f32x2 instruction for two lanes of work).
+// (r0, r1) = (a0, a1) * (b0, b1) + (c0, c1)
+__device__ __forceinline__ void fma2v(float& r0, float& r1, float a0, float a1, float b0, float b1, float c0,
+                                      float c1) {
+  asm("{.reg .b64 x, y, z, w;\n\t"
+      "mov.b64 x, {%2, %3};\n\t"
+      "mov.b64 y, {%4, %5};\n\t"
+      "mov.b64 z, {%6, %7};\n\t"
+      "fma.rn.f32x2 w, x, y, z;\n\t"
+      "mov.b64 {%0, %1}, w;}"
+      : "=f"(r0), "=f"(r1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+// (r0, r1) = (a0, a1) * (b0, b1)
+__device__ __forceinline__ void mul2(float& r0, float& r1, float a0, float a1, float b0, float b1) {
+  asm("{.reg .b64 x, y, w;\n\t"
+      "mov.b64 x, {%2, %3};\n\t"
+      "mov.b64 y, {%4, %5};\n\t"
+      "mul.rn.f32x2 w, x, y;\n\t"
+      "mov.b64 {%0, %1}, w;}"
+      : "=f"(r0), "=f"(r1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+// (r0, r1) = (a0, a1) - (b0, b1)
+__device__ __forceinline__ void sub2(float& r0, float& r1, float a0, float a1, float b0, float b1) {
+  asm("{.reg .b64 x, y, w;\n\t"
+      "mov.b64 x, {%2, %3};\n\t"
+      "mov.b64 y, {%4, %5};\n\t"
+      "sub.rn.f32x2 w, x, y;\n\t"
+      "mov.b64 {%0, %1}, w;}"
+      : "=f"(r0), "=f"(r1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
 // ================================================================ dQ kernel
 // TMEM columns: S0 [0,128), S1 [128,256) (dS written over S in pass 2),
 // dP [256,384), dQ [384,512).
@@ -551,7 +585,12 @@ __global__ void __launch_bounds__(ABWD_THREADS, 1)
 #pragma unroll
             for (int c = 0; c < 2; ++c)
 #pragma unroll
-              for (int j = 0; j < 32; ++j) pf[c * 32 + j] = ex2(fmaf(__uint_as_float(v[c][j]), sl, -lse2));
+              for (int j = 0; j < 16; ++j) {
+                float t0, t1;
+                fma2v(t0, t1, __uint_as_float(v[c][2 * j]), __uint_as_float(v[c][2 * j + 1]), sl, sl, -lse2, -lse2);
+                pf[c * 32 + 2 * j] = ex2(t0);
+                pf[c * 32 + 2 * j + 1] = ex2(t1);
+              }
           } else {
 #pragma unroll
             for (int c = 0; c < 2; ++c)
@@ -572,13 +611,17 @@ __global__ void __launch_bounds__(ABWD_THREADS, 1)
           tmem_ld_wait(dv[1]);
           tc_fence_before();
           mbar_arrive(s.dp_read);  // the next dP may land
+          const float sc = p.scale, dsc = -D * p.scale;  // dS = P (dP scale - D scale)
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
             uint32_t pk[16];
 #pragma unroll
-            for (int j = 0; j < 16; ++j)
-              pk[j] = pack_bf16x2(pf[c * 32 + 2 * j] * (__uint_as_float(dv[c][2 * j]) - D) * p.scale,
-                                  pf[c * 32 + 2 * j + 1] * (__uint_as_float(dv[c][2 * j + 1]) - D) * p.scale);
+            for (int j = 0; j < 16; ++j) {
+              float a0, a1;
+              fma2v(a0, a1, __uint_as_float(dv[c][2 * j]), __uint_as_float(dv[c][2 * j + 1]), sc, sc, dsc, dsc);
+              mul2(a0, a1, a0, a1, pf[c * 32 + 2 * j], pf[c * 32 + 2 * j + 1]);
+              pk[j] = pack_bf16x2(a0, a1);
+            }
             tmem_st16(tmem + lane_base + TQ_S + 128u * b + col0 + 16 * c, pk);
           }
         }
@@ -949,9 +992,11 @@ __global__ void __launch_bounds__(ABWD_THREADS, 1)
 #pragma unroll
             for (int j4 = 0; j4 < 8; ++j4) {
               const float4 l4 = *reinterpret_cast<const float4*>(lse + 4 * j4);
-              const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+              float t[4];
+              fma2v(t[0], t[1], __uint_as_float(v[4 * j4]), __uint_as_float(v[4 * j4 + 1]), sl, sl, -l4.x, -l4.y);
+              fma2v(t[2], t[3], __uint_as_float(v[4 * j4 + 2]), __uint_as_float(v[4 * j4 + 3]), sl, sl, -l4.z, -l4.w);
 #pragma unroll
-              for (int e = 0; e < 4; ++e) pf[4 * j4 + e] = ex2(fmaf(__uint_as_float(v[4 * j4 + e]), sl, -lv[e]));
+              for (int e = 0; e < 4; ++e) pf[4 * j4 + e] = ex2(t[e]);
             }
             if (!all_keys && !kvalid) {
 #pragma unroll
@@ -977,10 +1022,13 @@ __global__ void __launch_bounds__(ABWD_THREADS, 1)
               const float4 e4 = *reinterpret_cast<const float4*>(drow + 8 * j4 + 4);
               const float dv8[8] = {d4.x, d4.y, d4.z, d4.w, e4.x, e4.y, e4.z, e4.w};
 #pragma unroll
-              for (int e = 0; e < 4; ++e) {
+              for (int e = 0; e < 4; ++e) {  // dS = (P scale) (dP - D)
                 const int j = 8 * j4 + 2 * e;
-                pk[4 * j4 + e] = pack_bf16x2(pf[j] * (__uint_as_float(v[j]) - dv8[2 * e]) * p.scale,
-                                             pf[j + 1] * (__uint_as_float(v[j + 1]) - dv8[2 * e + 1]) * p.scale);
+                float a0, a1, s0, s1;
+                sub2(a0, a1, __uint_as_float(v[j]), __uint_as_float(v[j + 1]), dv8[2 * e], dv8[2 * e + 1]);
+                mul2(s0, s1, pf[j], pf[j + 1], p.scale, p.scale);
+                mul2(a0, a1, a0, a1, s0, s1);
+                pk[4 * j4 + e] = pack_bf16x2(a0, a1);
               }
             }
             tmem_st16(tmem + lane_base + X + 64u + qc, pk);
