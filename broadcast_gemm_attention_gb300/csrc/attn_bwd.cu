@@ -1133,32 +1133,58 @@ __global__ void __launch_bounds__(ROWS_THREADS) attn_bwd_rows_kernel(const AttnB
   const int sub = static_cast<int>(threadIdx.x & 15u);                               // lane within the row
   const long long nrows = static_cast<long long>(n_units) * 128;
   const long long stride = static_cast<long long>(gridDim.x - 1) * (ROWS_THREADS / 16);
-  for (long long t = static_cast<long long>(blockIdx.x - 1) * (ROWS_THREADS / 16) + (threadIdx.x >> 4); t < nrows;
-       t += stride) {
-    const int unit = static_cast<int>(t >> 7), r = static_cast<int>(t & 127);
-    const int4 w = __ldg(reinterpret_cast<const int4*>(p.work) + unit);
-    const int slot = r / p.Lq, q = r - slot * p.Lq;
-    const bool valid = r < rows && slot < w.w && w.x >= 0 && w.x < p.n_users && w.y >= 0 && w.y < p.H &&
-                       w.z >= 0 && w.z + w.w <= p.n_cand;
-    float D = 0.f, lse = INFINITY;
-    if (valid) {
-      const int cand = __ldg(p.perm + w.z + slot);
-      const size_t row = (static_cast<size_t>(cand) * p.H + w.y) * p.Lq + q;
-      const uint4 a = __ldcs(reinterpret_cast<const uint4*>(p.O + row * 128) + sub);
-      const uint4 g = __ldcs(reinterpret_cast<const uint4*>(p.dO + row * 128) + sub);
-      const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, gw[4] = {g.x, g.y, g.z, g.w};
+  // ROWS_PER rows per half-warp at a time: their work entries, candidates
+  // and O / dO loads are independent, so all of them are in flight at once
+  constexpr int ROWS_PER = 4;
+  for (long long t0 = static_cast<long long>(blockIdx.x - 1) * (ROWS_THREADS / 16) + (threadIdx.x >> 4); t0 < nrows;
+       t0 += ROWS_PER * stride) {
+    bool valid[ROWS_PER];
+    size_t row[ROWS_PER];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        D = fmaf(__uint_as_float(aw[k] << 16), __uint_as_float(gw[k] << 16), D);
-        D = fmaf(__uint_as_float(aw[k] & 0xffff0000u), __uint_as_float(gw[k] & 0xffff0000u), D);
+    for (int k = 0; k < ROWS_PER; ++k) {
+      const long long t = t0 + k * stride;
+      valid[k] = false;
+      row[k] = 0;
+      if (t < nrows) {
+        const int unit = static_cast<int>(t >> 7), r = static_cast<int>(t & 127);
+        const int4 w = __ldg(reinterpret_cast<const int4*>(p.work) + unit);
+        const int slot = r / p.Lq, q = r - slot * p.Lq;
+        valid[k] = r < rows && slot < w.w && w.x >= 0 && w.x < p.n_users && w.y >= 0 && w.y < p.H && w.z >= 0 &&
+                   w.z + w.w <= p.n_cand;
+        if (valid[k]) {
+          const int cand = __ldg(p.perm + w.z + slot);
+          row[k] = (static_cast<size_t>(cand) * p.H + w.y) * p.Lq + q;
+        }
       }
-      if (p.lse_in) lse = __ldg(p.lse_in + row) * 1.4426950408889634f;
+    }
+    uint4 a[ROWS_PER], g[ROWS_PER];
+    float lse[ROWS_PER];
+#pragma unroll
+    for (int k = 0; k < ROWS_PER; ++k) {
+      a[k] = g[k] = make_uint4(0, 0, 0, 0);
+      lse[k] = INFINITY;
+      if (valid[k]) {
+        a[k] = __ldcs(reinterpret_cast<const uint4*>(p.O + row[k] * 128) + sub);
+        g[k] = __ldcs(reinterpret_cast<const uint4*>(p.dO + row[k] * 128) + sub);
+        if (p.lse_in) lse[k] = __ldg(p.lse_in + row[k]) * 1.4426950408889634f;
+      }
     }
 #pragma unroll
-    for (int o = 8; o > 0; o >>= 1) D += __shfl_xor_sync(0xffffffffu, D, o);  // within the 16 lanes of the row
-    if (sub == 0) {
-      p.Drow[t] = valid ? D : 0.f;
-      if (p.lse_in) p.lse[t] = lse;
+    for (int k = 0; k < ROWS_PER; ++k) {
+      const uint32_t aw[4] = {a[k].x, a[k].y, a[k].z, a[k].w}, gw[4] = {g[k].x, g[k].y, g[k].z, g[k].w};
+      float D = 0.f;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        D = fmaf(__uint_as_float(aw[e] << 16), __uint_as_float(gw[e] << 16), D);
+        D = fmaf(__uint_as_float(aw[e] & 0xffff0000u), __uint_as_float(gw[e] & 0xffff0000u), D);
+      }
+#pragma unroll
+      for (int o = 8; o > 0; o >>= 1) D += __shfl_xor_sync(0xffffffffu, D, o);  // within the 16 lanes of the row
+      const long long t = t0 + k * stride;
+      if (sub == 0 && t < nrows) {
+        p.Drow[t] = valid[k] ? D : 0.f;
+        if (p.lse_in) p.lse[t] = lse[k];
+      }
     }
   }
 }
