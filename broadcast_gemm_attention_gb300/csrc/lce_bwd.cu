@@ -1128,14 +1128,19 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
           if (!warp_wait(&s.dc_empty[acc], ((c >> 1) & 1) ^ 1u, s.abort, p.timeout_ns)) goto done;
           tc_fence_after();
           if (elect_one()) {
-            const uint32_t a_base = smem_u32(s.w) + static_cast<uint32_t>(mb * 128 * 128);
-            for (int st = 0; st < csteps; ++st) {
-              const uint64_t adesc =
-                  sdesc_sw128(a_base + static_cast<uint32_t>((st >> 2) * m_rows * 128 + (st & 3) * 32), 16, 1024u);
-              const uint64_t bdesc =
-                  sdesc_sw128(dy_base + static_cast<uint32_t>((st >> 2) * BOX + (st & 3) * 2048), BOX, 1024u);
-              mma_bf16_ss(tmem + CAND_DC_COL + static_cast<uint32_t>(acc * 64), adesc, bdesc, idesc_c,
-                          st > 0 ? 1u : 0u);
+            // descriptors built once, then advanced by adding (offset >> 4) to
+            // the start-address field (shared memory is below 256 KB: no carry)
+            const uint64_t ad0 = sdesc_sw128(smem_u32(s.w) + static_cast<uint32_t>(mb * 128 * 128), 16, 1024u);
+            const uint64_t bd0 = sdesc_sw128(dy_base, BOX, 1024u);
+            const uint32_t a_chunk = static_cast<uint32_t>(m_rows * 128) >> 4;  // one 64-n chunk of W_c
+            const uint32_t d_tmem = tmem + CAND_DC_COL + static_cast<uint32_t>(acc * 64);
+#pragma unroll
+            for (int st = 0; st < 12; ++st) {
+              if (st < csteps) {
+                const uint32_t aoff = static_cast<uint32_t>(st >> 2) * a_chunk + (((st & 3) * 32) >> 4);
+                const uint32_t boff = static_cast<uint32_t>((st >> 2) * BOX + (st & 3) * 2048) >> 4;
+                mma_bf16_ss(d_tmem, ad0 + aoff, bd0 + boff, idesc_c, st > 0 ? 1u : 0u);
+              }
             }
             mma_commit(&s.dc_full[acc]);
           }
