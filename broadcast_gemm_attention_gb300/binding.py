@@ -362,6 +362,7 @@ class Plan:
     """Owns one ikbo_plan_t; `with Plan(...) as p:` destroys it on exit."""
 
     def __init__(self, max_cand: int, max_users: int, max_heads: int = 1):
+        self._map = None
         self.handle = ikbo_plan_create(max_cand, max_users, max_heads)
 
     def __enter__(self):
@@ -374,6 +375,7 @@ class Plan:
         if self.handle:
             ikbo_plan_destroy(self.handle)
             self.handle = None
+        self._map = None
 
     def __del__(self):
         try:
@@ -383,6 +385,9 @@ class Plan:
 
     def plan(self, map_, n_users, H=1, Lq=8, stream=None):
         ikbo_plan(self.handle, map_, n_users, H, Lq, stream)
+        # the plan borrows the map for every later call of this request: hold
+        # the tensor so that a temporary passed here stays allocated
+        self._map = map_
 
     def lce_forward(self, U, C, Wu, Wc, b, Y, stream=None):
         ikbo_lce_forward(self.handle, U, C, Wu, Wc, b, Y, stream)

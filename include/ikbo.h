@@ -67,7 +67,8 @@ ikbo_status_t ikbo_plan_create(ikbo_plan_t* out, int max_cand, int max_users, in
  * paragraph; grouping the candidates of one user is what lets their K/V be
  * loaded once, aixai.ru "Deep Dive: Flash Attention"):
  *   d_map     int32 [n_cand], values in [0, n_users); BORROWED: must stay
- *             valid and unchanged until the last forward call of this request
+ *             valid and unchanged until the last call of this request (the
+ *             forward and backward calls read it)
  *   n_cand    1..max_cand;  n_users 1..max_users
  *   H, Lq     attention heads (1..max_heads) and queries per candidate
  *             (multiple of 8, at most 128); they shape the work list.

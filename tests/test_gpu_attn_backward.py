@@ -190,7 +190,8 @@ def test_attn_backward_errors():
         with pytest.raises(B.IkboError) as e:
             p.attn_backward(Q, K, V, O, dO, None, dQ, dK, dV)
         assert e.value.code == B.IKBO_ERR_NOT_PLANNED
-        p.plan(x.map.cuda(), 2, 1, 8)
+        m = x.map.cuda()  # borrowed by the plan for the calls below
+        p.plan(m, 2, 1, 8)
         lse = torch.zeros(4, 1, 8, dtype=torch.float32, device=Q.device)
         args = [Q.data_ptr(), K.data_ptr(), V.data_ptr(), O.data_ptr(), dO.data_ptr(), None, None, dQ.data_ptr(),
                 dK.data_ptr(), dV.data_ptr(), 16, 128, 0.1, None]

@@ -64,7 +64,8 @@ def test_lce_stage_argument_and_map_errors():
     bad = x.map.clone()
     bad[5] = 7
     with B.Plan(x.n_cand, x.n_users, 1) as p:
-        p.plan(bad.cuda(), x.n_users)
+        m = bad.cuda()  # borrowed by the plan for the calls below
+        p.plan(m, x.n_users)
         for st in (0, 2, 5):
             with pytest.raises(B.IkboError) as e:
                 p.lce_forward_staged(U, C, Wu, Wc, b, Y, st)
