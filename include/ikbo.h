@@ -134,8 +134,8 @@ ikbo_status_t ikbo_lce_forward(ikbo_plan_t p, const void* U, const void* C, cons
  * Notes:
  *   - every GPU that loads the library holds the 16 MiB until process exit;
  *   - the first call made with a given device current looks up the array's
- *     device address (cudaGetSymbolAddress) and the device's limits; make
- *     that first call before capturing any stream;
+ *     device address (cudaGetSymbolAddress) and the device's limits (host
+ *     queries that later calls on that device do not repeat);
  *   - all calls share the array and it keeps the last call's contents; each
  *     call first clears, on its stream, the words that must start at zero
  *     (status and readiness flags); calls that overlap on the GPU (two
