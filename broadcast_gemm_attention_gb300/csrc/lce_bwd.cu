@@ -14,14 +14,21 @@
 // S is rounded to bf16 for the two tensor-core products that read it.
 //
 // Kernels:
-//   bwd_segsum_kernel / bwd_segsum_finish_kernel  S (HBM-bound reduction)
-//   bwd_db_kernel                                 db from S
-//   bwd_act_kernel     out[b][m][d] = sum_n W[m][n] X[b][n][d]   (dC, dU)
-//   bwd_wgrad_kernel   split-K partials of sum_b sum_d A[b][m][d] G[b][n][d]
-//   bwd_wgrad_reduce_kernel                       (dW_c, dW_u)
-// The two GEMM kernels are persistent, one CTA per SM, warp-specialised like
-// the forward: warp 0 TMA (elected lane issues), warp 1 tcgen05.mma (elected
-// lane), warp 2 TMEM owner, warps 4-11 epilogue.  Every wait is bounded.
+//   bwd_cand_kernel    the candidate side in one pass over dY (and C): dC,
+//                      dW_c, S and db, ending (cooperative launch) with the
+//                      finish -- or bwd_cand_finish_kernel after it
+//   bwd_act_kernel     out[b][m][d] = sum_n W[m][n] X[b][n][d]   (dU; dC where
+//                      the candidate pass does not apply)
+//   bwd_wgrad_kernel   split-K sum_b sum_d A[b][m][d] G[b][n][d] (dW_u; dW_c
+//                      where the candidate pass does not apply): the split-K
+//                      CTAs of an m block add their partials as a cluster,
+//                      or write them for bwd_wgrad_reduce_kernel
+//   bwd_segsum_kernel / bwd_segsum_finish_kernel, bwd_db_kernel: S and db
+//                      where the candidate pass does not apply
+// The GEMM kernels are persistent, one CTA per SM, warp-specialised like the
+// forward: TMA producer warp(s) (elected lane issues), warp 1 tcgen05.mma
+// (elected lane), warp 2 TMEM owner, warps 4-11 epilogue.  Every wait on an
+// mbarrier, a flag or the grid barrier is bounded.
 #include <cuda_bf16.h>
 
 #include "bwd_internal.h"
