@@ -63,6 +63,8 @@ def check_all(x, dY, out, cands=None, users=None, what=""):
     dict(n_cand=300, n_users=7, K_u=381, K_c=243, D=384, N=200),   # K_u > 256: one accumulator; N -> 208 columns
     dict(n_cand=90, n_users=30, K_u=130, K_c=260, D=200, N=128),   # K_c > 256, ragged D block
     dict(n_cand=40, n_users=6, K_u=100, K_c=60, D=64, N=256),      # N = 256: the widest weight-gradient tile
+    dict(n_cand=500, n_users=40, K_u=50, K_c=100, D=200, N=192),   # one K_c block, many short runs, ragged D block
+    dict(n_cand=64, n_users=5, K_u=70, K_c=256, D=64, N=176),      # K_c = 256 exactly, N = 176 (3 n chunks)
 ])
 def test_lce_backward_full(shape):
     x = gen.make_lce("bwd", 91, map_kind="permuted", **shape)
