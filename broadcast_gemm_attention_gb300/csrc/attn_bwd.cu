@@ -575,12 +575,23 @@ __global__ void __launch_bounds__(ABWD_THREADS, 1)
         tc_fence_after();
         const int kcol = jt * 128 + static_cast<int>(col0);
         float pf[64];
+        uint32_t dv[2][32];
         {
           uint32_t v[2][32];
           tmem_ld32(tmem + lane_base + TQ_S + 128u * b + col0, v[0]);
           tmem_ld32(tmem + lane_base + TQ_S + 128u * b + col0 + 32, v[1]);
           tmem_ld_wait(v[0]);
           tmem_ld_wait(v[1]);
+          // dP first: the single dP buffer is released before P is formed
+          if (!wwait(s.dp_full, ndp & 1u, s.abort, p.timeout_ns)) goto done;
+          ++ndp;
+          tc_fence_after();
+          tmem_ld32(tmem + lane_base + TQ_DP + col0, dv[0]);
+          tmem_ld32(tmem + lane_base + TQ_DP + col0 + 32, dv[1]);
+          tmem_ld_wait(dv[0]);
+          tmem_ld_wait(dv[1]);
+          tc_fence_before();
+          mbar_arrive(s.dp_read);  // the next dP may land
           if (kcol + 64 <= x.k.L) {  // every column of this half is a key (the common case)
 #pragma unroll
             for (int c = 0; c < 2; ++c)
@@ -600,17 +611,7 @@ __global__ void __launch_bounds__(ABWD_THREADS, 1)
                     kcol + c * 32 + j < x.k.L ? ex2(fmaf(__uint_as_float(v[c][j]), sl, -lse2)) : 0.f;
           }
         }
-        if (!wwait(s.dp_full, ndp & 1u, s.abort, p.timeout_ns)) goto done;
-        ++ndp;
-        tc_fence_after();
         {
-          uint32_t dv[2][32];
-          tmem_ld32(tmem + lane_base + TQ_DP + col0, dv[0]);
-          tmem_ld32(tmem + lane_base + TQ_DP + col0 + 32, dv[1]);
-          tmem_ld_wait(dv[0]);
-          tmem_ld_wait(dv[1]);
-          tc_fence_before();
-          mbar_arrive(s.dp_read);  // the next dP may land
           const float sc = p.scale, dsc = -D * p.scale;  // dS = P (dP scale - D scale)
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
