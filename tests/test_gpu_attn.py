@@ -109,6 +109,15 @@ def test_attn_ratio_sweep_full(ratio):
     check_attn_all(O, x)
 
 
+def test_attn_runs_of_every_length_per_user():
+    """Users whose runs of candidates end in a partial unit, fill units
+    exactly, or have a single candidate (Lq 32: 4 candidates per unit;
+    counts 1, 5, 8, 13, 20), over three heads."""
+    m = [0] * 1 + [1] * 5 + [2] * 8 + [3] * 13 + [4] * 20
+    x = gen.make_attn("runs", 67, n_cand=len(m), n_users=5, H=3, Lq=32, d=128, Lkv=260, explicit_map=m)
+    full_check(x)
+
+
 def test_attn_materialised_ablation_matches():
     x = gen.make_attn("abl", 64, n_cand=24, n_users=3, H=2, Lq=32, d=128, Lkv=256, map_kind="permuted")
     idx = x.map.long()
