@@ -647,6 +647,65 @@ def run_sweep(args):
                       "status": B.ikbo_status_string(st)}), flush=True)
 
 
+CASES = ("attn_stress", "attn_ratio70", "lce_4096_70")
+
+
+def run_case(args):
+    """One forward workload alone, --warmup untimed and --steps timed calls
+    with L2 flushed before each (events; median), for a profiler to capture
+    one kernel at a shape other than the 70:1 request: the Zipf / jagged
+    attention stress request, the attention ratio sweep at 4096 candidates
+    and ratio 70, or the LCE sweep point of 4096 candidates and ratio 70.
+    One JSON line; not the headline metric."""
+    import statistics
+    import torch
+    import __graft_entry__ as ge
+    from broadcast_gemm_attention_gb300 import binding as B
+    from broadcast_gemm_attention_gb300 import inputs as gen
+    ge.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    flush = L2Flush(dev)
+    if args.case == "lce_4096_70":
+        n, r, seed = [t for t in gen.lce_sweep_points() if t[0] == 4096 and t[1] == 70][0]
+        x = gen.lce_sweep(n, r, seed)
+        U, C, Wu, Wc, b, m = [t.to(dev) for t in (x.U, x.C, x.Wu, x.Wc, x.b, x.map)]
+        out = torch.empty(x.n_cand, x.N, x.D, dtype=torch.bfloat16, device=dev)
+        p = B.Plan(x.n_cand, x.n_users, 1)
+        p.plan(m, x.n_users, 1, 8, stream)
+        call = lambda: p.lce_forward(U, C, Wu, Wc, b, out, stream)  # noqa: E731
+    else:
+        if args.case == "attn_stress":
+            x = gen.attn_stress()
+        else:
+            n, r, seed = [t for t in gen.attn_ratio_sweep_points() if t[1] == 70][0]
+            x = gen.attn_ratio_sweep(n, r, seed)
+        Q, K, V, m = [t.to(dev) for t in (x.Q, x.K, x.V, x.map)]
+        offs = None if x.kv_offsets is None else x.kv_offsets.to(dev)
+        out = torch.empty_like(Q)
+        p = B.Plan(x.n_cand, x.n_users, x.H)
+        p.plan(m, x.n_users, x.H, x.Lq, stream)
+        call = lambda: p.attn_forward(Q, K, V, offs, out, None, stream)  # noqa: E731
+    ts = []
+    for k in range(args.warmup + args.steps):
+        flush()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        call()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        if k >= args.warmup:
+            ts.append(e0.elapsed_time(e1) * 1e3)
+    st = p.status()
+    p.close()
+    print(json.dumps({"case": args.case, "n_cand": x.n_cand, "n_users": x.n_users, "steps": args.steps,
+                      "us_median": statistics.median(ts) if ts else None, "status": B.ikbo_status_string(st)}),
+          flush=True)
+    if st != B.IKBO_OK:
+        raise SystemExit(1)
+
+
 def e2e_run(plan, d, Y, O, x, a, step_flops, args, K, world, dist, dev):
     """End to end through the C ABI from pinned host memory, the way a server
     would run consecutive requests: request k's inputs go host -> device on a
@@ -935,8 +994,12 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target length of the CPU-oracle baseline (0 skips it, e.g. under a profiler)")
     ap.add_argument("--ref-budget", type=float, default=120.0, help="reference arm: total seconds of oracle work")
+    ap.add_argument("--case", choices=CASES, default=None,
+                    help="run one forward workload alone (for a profiler) instead of the benchmark")
     args = ap.parse_args()
-    if args.sweep:
+    if args.case:
+        run_case(args)
+    elif args.sweep:
         run_sweep(args)
     elif args.impl == "reference":
         run_reference(args)
