@@ -118,6 +118,15 @@ def test_attn_runs_of_every_length_per_user():
     full_check(x)
 
 
+def test_attn_at_the_user_limit():
+    """8 192 users (the segment builder's limit) with 1-3 candidates each over
+    short dense histories (Lkv 130: a full and a 2-key tile), Lq 16."""
+    rng = np.random.default_rng(68)
+    m = rng.integers(0, 8192, size=12000).tolist()
+    x = gen.make_attn("umax", 69, n_cand=len(m), n_users=8192, H=1, Lq=16, d=128, Lkv=130, explicit_map=m)
+    full_check(x)
+
+
 def test_attn_materialised_ablation_matches():
     x = gen.make_attn("abl", 64, n_cand=24, n_users=3, H=2, Lq=32, d=128, Lkv=256, map_kind="permuted")
     idx = x.map.long()

@@ -95,6 +95,17 @@ def test_lce_users_past_1024():
     assert_lce_close(Y, ref, "users past 1024")
 
 
+def test_lce_at_the_user_limit():
+    """8 192 users (the segment builder's limit), 12 000 candidates in a
+    permuted map: most users have one or two candidates, some none."""
+    m = np.random.default_rng(35).integers(0, 8192, size=12000)
+    x = gen.make_lce("umax", 36, 12000, 8192, 24, 40, 64, 16, explicit_map=m.tolist())
+    Y, st = run_lce(x)
+    assert st == B.IKBO_OK
+    ref = oracle.lce(x.map, x.U, x.C, x.Wu, x.Wc, x.b)
+    assert_lce_close(Y, ref, "8192 users")
+
+
 @pytest.mark.parametrize("n_cand,ratio", [(n, r) for n, r, _ in gen.lce_sweep_points()])
 def test_lce_sweep_point_full(n_cand, ratio):
     """Every point of the shape sweep (256 / 1024 / 4096 candidates x ratio

@@ -24,6 +24,9 @@ def _maps():
     # the few-user scatter's limit (32 users, several blocks of 1024) and one past it
     yield "users_32_blocks", gen.permuted_multinomial_map(rng, 3000, 32), 32
     yield "users_33_blocks", gen.permuted_multinomial_map(rng, 3000, 33), 33
+    # the builder's user limit (8192, its counts and cursors in shared memory):
+    # ~2.4 candidates per user, about 9 % of the users empty
+    yield "max_users_8192", rng.integers(0, 8192, size=20000).astype(np.int32), 8192
 
 
 @pytest.mark.parametrize("name,m,n_users", list(_maps()), ids=[x[0] for x in _maps()])
@@ -77,3 +80,13 @@ def test_plan_argument_errors():
         with pytest.raises(B.IkboError) as e:
             p.plan(dmap[:4], 2, 3, 8)  # H above max_heads
         assert e.value.code == B.IKBO_ERR_INVALID_ARG
+
+
+def test_plan_user_limit():
+    """A plan for more users than the segment builder holds is refused
+    before any allocation; one at the limit is accepted."""
+    with pytest.raises(B.IkboError) as e:
+        B.ikbo_plan_create(16, 8193, 1)
+    assert e.value.code == B.IKBO_ERR_UNSUPPORTED
+    h = B.ikbo_plan_create(16, 8192, 1)
+    B.ikbo_plan_destroy(h)
