@@ -703,8 +703,12 @@ __device__ void att_softmax(const AttnParams& p, const AttSmem& s, uint32_t tmem
       int epi = prev.pending ? 1 : 0;  // the previous unit's epilogue: 1 read O next, 2 store it next
       int mine = 0;                     // this group's tiles of the unit so far
       float mref = -INFINITY, l = 0.f;  // this group's reference and row sum
-      for (int jt = 0; jt < x.ntiles; ++jt, ++g) {
-        if (static_cast<int>(g & 1u) != grp) continue;  // the other group's tile
+      // this group's key tiles only: g, the tile's place in the CTA's sequence,
+      // runs over g % 2 == group (visiting every tile to skip half of them
+      // cost the group ~3 % of the kernel's time in loop control)
+      const uint32_t g0 = g;
+      for (int jt = static_cast<int>((static_cast<uint32_t>(grp) - g0) & 1u); jt < x.ntiles; jt += 2) {
+        g = g0 + static_cast<uint32_t>(jt);
         if (!mbar_wait(&s.s_full[grp], (g >> 1) & 1u, s.abort, p.timeout_ns, 1)) return;
         tc_fence_after();
         const int ncols = min(ATT_BN, x.L - jt * ATT_BN);  // valid key columns of this tile
@@ -813,6 +817,7 @@ __device__ void att_softmax(const AttnParams& p, const AttSmem& s, uint32_t tmem
           ncand = (nrv && !nx.self) ? __ldg(p.perm + nx.start + slot) : 0;
         }
       }
+      g = g0 + static_cast<uint32_t>(x.ntiles);
       if (epi == 1 && !att_epilogue_read<kLse>(p, s, Ot, prev, ln, ou)) return;
       if (epi >= 1) att_epilogue_store(s, prev, ln);
       prev.pending = true;
